@@ -1,0 +1,170 @@
+"""Storage formats used by the CSA2 oracle, written from their definitions.
+
+TEST INFRASTRUCTURE ONLY. This module belongs to the CPU oracle: only the
+tests, the smoke check and the benchmark's CPU-baseline leg may import it.
+The CUDA product path never calls into it and shares no code with it.
+
+Formats (all decoded exactly into float64):
+
+* bf16: 1 sign, 8 exponent (bias 127), 7 fraction bits; the upper half of an
+  IEEE binary32. Encoding is round-to-nearest-even from float64.
+* e4m3 ("fn" variant): 1 sign, 4 exponent (bias 7), 3 fraction bits, no
+  infinities, 0x7F/0xFF are NaN, largest finite value 448, subnormals
+  m * 2^-9. Encoding is round-to-nearest-even with saturation to +-448.
+* ue8m0: an unsigned power-of-two scale 2^(E-127), E in [0, 254].
+
+The block-32 fp8 KV format (one e4m3 code per channel plus one ue8m0 scale
+per 32 consecutive channels) follows the page "DeepSeek-V4.1-Flash on WASTE",
+section "The shape" (fp8 e4m3 with ue8m0 scales) and the PocketLLM page,
+section "The CSA2 attention layers" (window quantized to FP8 over 32
+elements). The pages do not state how the scale is chosen; the reading used
+here is the smallest power of two that brings the block's largest magnitude
+into the e4m3 range: scale = 2^k with k the least integer such that
+amax <= 448 * 2^k, and an all-zero block takes E = 0.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+FP8_BLOCK = 32
+
+
+# ----------------------------------------------------------------------------
+# bf16
+# ----------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16 array) as float64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to bf16 (round half to even); returns uint16 bits.
+
+    The value is rounded once, directly from float64: the quantum of the
+    binade that holds |x| is 2^(e-8) for |x| in [2^(e-1), 2^e) with 8
+    significant bits, and 2^-133 below the smallest normal 2^-126.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    flat_x = x.reshape(-1)
+    flat_o = out.reshape(-1)
+    ax = np.abs(flat_x)
+    sign = np.signbit(flat_x)
+    _, e = np.frexp(ax)  # ax = m * 2^e with m in [0.5, 1)
+    q_exp = np.maximum(e, -125) - 8
+    quantum = np.ldexp(1.0, q_exp)
+    rounded = np.rint(ax / quantum) * quantum  # rint: half to even
+    with np.errstate(over="ignore"):
+        as32 = rounded.astype(np.float32)  # exact: rounded has <= 8 significant bits
+    bits = (as32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    # overflow: anything that rounded past the largest finite bf16 is inf
+    bits = np.where(rounded >= 2.0 ** 128, np.uint16(0x7F80), bits)
+    bits = np.where(np.isnan(flat_x), np.uint16(0x7FC0), bits)
+    bits = np.where(sign & ~np.isnan(flat_x), bits | np.uint16(0x8000), bits)
+    flat_o[:] = bits
+    return out
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 -> nearest bf16 value (as float64)."""
+    return bf16_bits_to_f64(f64_to_bf16_bits(x))
+
+
+def bf16_ulp(x) -> np.ndarray:
+    """Spacing of bf16 values at |x| (the quantum of x's binade)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(ax)
+    return np.ldexp(1.0, np.maximum(e, -125) - 8)
+
+
+# ----------------------------------------------------------------------------
+# e4m3 and ue8m0
+# ----------------------------------------------------------------------------
+
+def _e4m3_table() -> np.ndarray:
+    vals = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        s = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            vals[code] = np.nan
+        elif e == 0:
+            vals[code] = s * m * 2.0 ** -9
+        else:
+            vals[code] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+E4M3_VALUES = _e4m3_table()
+# non-negative finite codes sorted by value: code c in [0, 126] has value
+# E4M3_VALUES[c], strictly increasing in c
+_POS_VALUES = E4M3_VALUES[:127]
+
+
+def e4m3_bits_to_f64(bits) -> np.ndarray:
+    return E4M3_VALUES[np.asarray(bits, dtype=np.uint8)]
+
+
+def f64_to_e4m3_bits(x) -> np.ndarray:
+    """Round to e4m3 (half to even), saturating to +-448. NaN is not accepted."""
+    x = np.asarray(x, dtype=np.float64)
+    if np.isnan(x).any():
+        raise ValueError("NaN has no e4m3 encoding in this format")
+    ax = np.abs(x)
+    _, e = np.frexp(ax)  # binade [2^(e-1), 2^e)
+    # 3 fraction bits: quantum 2^(e-1-3); subnormal quantum 2^-9 below 2^-6
+    quantum = np.ldexp(1.0, np.maximum(e - 1, -6) - 3)
+    r = np.rint(ax / quantum) * quantum
+    r = np.minimum(r, E4M3_MAX)
+    code = np.searchsorted(_POS_VALUES, r)
+    if not np.all(_POS_VALUES[np.minimum(code, 126)] == r):
+        raise AssertionError("rounded value is not an e4m3 grid point")
+    code = code.astype(np.uint8)
+    # the sign survives rounding to zero (a negative value that underflows is -0)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def ue8m0_to_f64(e) -> np.ndarray:
+    e = np.asarray(e, dtype=np.int64)
+    return np.ldexp(1.0, e - 127)
+
+
+def fp8_block_scale_exponent(amax: float) -> int:
+    """ue8m0 byte for one block: least k with amax <= 448 * 2^k, E = k + 127."""
+    if amax == 0.0:
+        return 0
+    k = int(np.ceil(np.log2(amax / E4M3_MAX)))
+    # settle the rounding of log2 exactly with power-of-two comparisons
+    while amax > E4M3_MAX * 2.0 ** k:
+        k += 1
+    while amax <= E4M3_MAX * 2.0 ** (k - 1):
+        k -= 1
+    return int(min(max(k + 127, 0), 254))
+
+
+def fp8_block_quantize(x, block: int = FP8_BLOCK):
+    """Quantize rows [n, D] to (codes uint8 [n, D], scale bytes uint8 [n, D/block])."""
+    x = np.asarray(x, dtype=np.float64)
+    n, d = x.shape
+    if d % block:
+        raise ValueError("row length must be a multiple of the block")
+    xb = x.reshape(n, d // block, block)
+    amax = np.abs(xb).max(axis=2)
+    exps = np.empty((n, d // block), dtype=np.uint8)
+    for i in range(n):
+        for b in range(d // block):
+            exps[i, b] = fp8_block_scale_exponent(float(amax[i, b]))
+    scale = ue8m0_to_f64(exps)[:, :, None]
+    codes = f64_to_e4m3_bits(xb / scale).reshape(n, d)
+    return codes, exps
+
+
+def fp8_block_dequantize(codes, exps, block: int = FP8_BLOCK) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, d = codes.shape
+    v = e4m3_bits_to_f64(codes).reshape(n, d // block, block)
+    return (v * ue8m0_to_f64(exps)[:, :, None]).reshape(n, d)
