@@ -1,0 +1,494 @@
+"""Benchmark of one CSA2 layer step on GB300.
+
+A step is one pass of the whole hot path over one batch: compress of the
+groups that close at this step, index scores over every visible compressed
+entry, top-512 selection, and the two-source attention with sink. The
+headline workload is decode at batch 32 with 65,536-token contexts
+(ratio 4 -> 16,384 compressed entries per sequence), bf16, seeded synthetic
+inputs. Units are query tokens: tokens/s = 32 * steps / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun each rank runs its own batch (data-parallel over sequences,
+no collective on the data path); the line reports the whole-job rate over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import PRESETS, make_inputs  # noqa: E402
+
+METRIC = "CSA2 decode tokens/s and HBM GB/s (% of ~8 TB/s) at 64K and 1M context"
+N_COPIES = 4  # rotating input copies: each step's working set is evicted from L2 by the other three
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        t0, t1 = (self.marks[0], self.marks[1]) if len(self.marks) >= 2 else (0, 1e30)
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        use = inside if inside else self.samples
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in use:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except Exception:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, device):
+    if pg is not None:
+        if device.type == "cuda":
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device) -> float:
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device if device.type == "cuda" else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workload bytes
+
+def algorithmic_bytes(wl, has_compress=True):
+    """Minimal HBM bytes of one step: every visible index key once, the gathered
+    window and selected rows once, q/q^I/w in, the output out, and the closing
+    groups' raw tokens and gates in plus their stored entries out."""
+    row = 528 if wl.kv_fp8 else 1024
+    key = 132 if wl.idx_fp8 else 256
+    total = 0
+    for b in range(wl.n_seq):
+        n = wl.ctx_len[b]
+        for i in range(wl.n_query_per_seq):
+            t = n - wl.n_query_per_seq + i
+            nv = (t + 1) // wl.m
+            win = min(wl.window, t + 1)
+            total += nv * key + (win + min(wl.topk, nv)) * row
+            total += wl.n_heads * wl.head_dim * 2 * 2 + wl.idx_heads * wl.idx_dim * 2 + wl.idx_heads * 4
+        if has_compress and n % wl.m == 0:
+            total += wl.m * wl.head_dim * (2 + 4) + row + key
+    return total
+
+
+def index_bytes(wl):
+    key = 132 if wl.idx_fp8 else 256
+    tot = 0
+    for b in range(wl.n_seq):
+        n = wl.ctx_len[b]
+        for i in range(wl.n_query_per_seq):
+            t = n - wl.n_query_per_seq + i
+            nv = (t + 1) // wl.m
+            tot += nv * (key + 4) + wl.idx_heads * wl.idx_dim * 2 + wl.idx_heads * 4
+    return tot
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Copy:
+    """One resident copy of a step's inputs and outputs."""
+
+    def __init__(self, ctx, wl, seed_offset, device):
+        from compressed_sparse_attention_gb300 import binding
+        wlc = wl.scaled(seed=wl.seed + 1000 * seed_offset)
+        inp = make_inputs(wlc, device)
+        if wl.kv_fp8:
+            for src, dst, w in (("win_kv_f32", "win_kv", 512), ("pool_kv_f32", "pool_kv", 512)):
+                x = inp.pop(src)
+                codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
+                sc = torch.empty((x.shape[0], w // 32), dtype=torch.uint8, device=device)
+                for i in range(0, x.shape[0], 1 << 20):
+                    ctx.store_rows(x[i:i + (1 << 20)], None, binding.KV_FP8, codes[i:i + (1 << 20)],
+                                   sc[i:i + (1 << 20)])
+                inp[dst], inp[dst.replace("_kv", "_scale")] = codes, sc
+                del x
+        if wl.idx_fp8:
+            x = inp.pop("idx_keys_f32")
+            codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
+            sc = torch.empty((x.shape[0], 4), dtype=torch.uint8, device=device)
+            for i in range(0, x.shape[0], 1 << 21):
+                ctx.store_rows(x[i:i + (1 << 21)], None, binding.KV_FP8, codes[i:i + (1 << 21)], sc[i:i + (1 << 21)])
+            inp["idx_keys"], inp["idx_key_scale"] = codes, sc
+            del x
+        torch.cuda.synchronize()
+        self.inp = inp
+        Q = wl.n_query
+        self.max_vis = int(inp["n_vis"].max())
+        self.out = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty((Q, wl.topk), dtype=torch.int32, device=device)
+        self.ws = binding.workspace(ctx.step_workspace_size(Q, self.max_vis), device)
+        self.scores = torch.empty((Q, self.max_vis), dtype=torch.float32, device=device)
+        self.wl = wl
+
+    def step(self, ctx, q=None, raw=None, gate=None, out=None):
+        i = self.inp
+        ctx.step(0, self.wl.n_seq, self.max_vis, q=i["q"] if q is None else q, q_pos=i["q_pos"],
+                 seq_of_q=i["seq_of_q"], n_vis=i["n_vis"], sink=i["sink"], win_kv=i["win_kv"],
+                 win_scale=i.get("win_scale"), win_off=i["win_off"], pool_kv=i["pool_kv"],
+                 pool_scale=i.get("pool_scale"), pool_off=i["pool_off"], topk_idx=self.idx,
+                 out=self.out if out is None else out, workspace=self.ws, q_idx=i["q_idx"], w_heads=i["w_heads"],
+                 idx_keys=i["idx_keys"], idx_key_scale=i.get("idx_key_scale"),
+                 raw=i["raw"] if raw is None else raw, gate=i["gate"] if gate is None else gate,
+                 tok_off=i["tok_off"], first_pos=i["first_pos"], norm_w=i["norm_w"], w_idx=i["w_idx"],
+                 k_norm_w=i["k_norm_w"])
+
+    def index_only(self, ctx):
+        i = self.inp
+        ctx.index_score(self.wl.n_seq, i["q_idx"], i["w_heads"], i["idx_keys"], i.get("idx_key_scale"),
+                        i["pool_off"], i["seq_of_q"], i["n_vis"], self.max_vis, self.scores)
+
+
+def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
+    from compressed_sparse_attention_gb300 import binding, build
+    build.build()
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=int(wl.kv_fp8),
+                          idx_key_format=int(wl.idx_fp8))
+    copies = [Copy(ctx, wl, rank * N_COPIES + c, device) for c in range(N_COPIES)]
+    stream = torch.cuda.Stream(device=device)
+    # launches per step
+    with torch.cuda.stream(stream):
+        copies[0].step(ctx)
+    launches_per_step = ctx.last_launch_count
+    torch.cuda.synchronize()
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the bench workload")
+    # one CUDA graph per copy
+    graphs = []
+    for c in copies:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            c.step(ctx)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    for i in range(max(args.warmup, 3)):
+        graphs[i % N_COPIES].replay()
+    torch.cuda.synchronize()
+    # ---- timed region: exactly K steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg, device)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % N_COPIES].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark()
+    barrier(pg, device)
+    ms = e0.elapsed_time(e1)
+    ms_max = max_over_ranks(pg, ms, device)
+    # ---- dominant kernel (index score) timed alone, on its launch stream
+    n_idx = max(args.steps, 20)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            copies[i % N_COPIES].index_only(ctx)
+        torch.cuda.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for i in range(n_idx):
+            copies[i % N_COPIES].index_only(ctx)
+        k1.record(stream)
+    torch.cuda.synchronize()
+    idx_ms = k0.elapsed_time(k1) / n_idx
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, ctx, copies, stream, device, wl)
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} after timing")
+    return dict(ms=ms, ms_max=ms_max, launches=launches_per_step, idx_ms=idx_ms, e2e=e2e)
+
+
+def run_e2e(args, ctx, copies, stream, device, wl):
+    """Per step: H2D of the step's inputs (q, and the closing groups' raw tokens
+    and gates) from pinned host memory, the step through csa2_step, D2H of the
+    output; the caches (window, pool, index keys) stay resident."""
+    steps = max(10, min(args.steps, 200))
+    hosts = []
+    for c in copies:
+        i = c.inp
+        hosts.append(dict(q=i["q"].cpu().pin_memory(), raw=i["raw"].cpu().pin_memory(),
+                          gate=i["gate"].cpu().pin_memory()))
+    dq = torch.empty_like(copies[0].inp["q"])
+    draw = torch.empty_like(copies[0].inp["raw"])
+    dgate = torch.empty_like(copies[0].inp["gate"])
+    dout = torch.empty_like(copies[0].out)
+    hout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h2d = (dq.numel() * dq.element_size() + draw.numel() * draw.element_size() + dgate.numel() * dgate.element_size())
+    d2h = dout.numel() * dout.element_size()
+
+    def one(i):
+        c = copies[i % N_COPIES]
+        h = hosts[i % N_COPIES]
+        dq.copy_(h["q"], non_blocking=True)
+        draw.copy_(h["raw"], non_blocking=True)
+        dgate.copy_(h["gate"], non_blocking=True)
+        c.step(ctx, q=dq, raw=draw, gate=dgate, out=dout)
+        hout.copy_(dout, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return dict(ms_per_step=ms / steps, steps=steps, h2d=h2d, d2h=d2h)
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+class OracleSample:
+    """The CPU oracle on whole decode queries of the workload's first sequence
+    (a bounded sample of the same workload); inputs are prepared once."""
+
+    def __init__(self, wl):
+        import numpy as np
+        from oracle import csa2_oracle as O
+        from oracle import formats as F
+        self.O = O
+        self.geom = O.Geometry(compress_ratio=wl.m, idx_heads=wl.idx_heads, topk=wl.topk, window=wl.window)
+        g = self.geom
+        self.f = O.yarn_inv_freq(64, g.rope_theta, g.yarn_factor, g.yarn_orig_len, g.yarn_beta_fast, g.yarn_beta_slow)
+        one = wl.scaled(n_seq=1, ctx_len=wl.ctx_len[:1])
+        inp = make_inputs(one, "cpu")
+
+        def bf(t):
+            return F.bf16_bits_to_f64(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+        def fp8(t):
+            return F.fp8_block_dequantize(*F.fp8_block_quantize(t.double().numpy()))
+
+        self.keys = fp8(inp["idx_keys_f32"]) if wl.idx_fp8 else bf(inp["idx_keys"])
+        self.pool = fp8(inp["pool_kv_f32"]) if wl.kv_fp8 else bf(inp["pool_kv"])
+        self.win = fp8(inp["win_kv_f32"]) if wl.kv_fp8 else bf(inp["win_kv"])
+        self.q = bf(inp["q"][0])
+        self.qi, self.w = bf(inp["q_idx"][0]), inp["w_heads"][0].double().numpy()
+        self.sink = inp["sink"].double().numpy()
+        self.t = int(inp["q_pos"][0])
+        self.wl = wl
+
+    def run_one(self):
+        cap = self.win.shape[0]
+        win = self.win
+        self.O.step_query(self.O.MODE_REINDEX, self.geom, self.f, q=self.q, t=self.t,
+                          win_rows_by_pos=lambda p: win[p % cap], comp_rows=self.pool, sink=self.sink,
+                          q_idx=self.qi, w_heads=self.w, idx_keys=self.keys)
+
+
+def cpu_baseline(wl, budget_s):
+    s = OracleSample(wl)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        s.run_one()
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} decode queries of {wl.name} (one sequence, {wl.ctx_len[0]} context) through the "
+                      f"float64 NumPy oracle (score, top-k, attend), {el:.1f} s, default BLAS threads"}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="decode_64k_b32", choices=sorted(PRESETS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true", help="skip the 1M-context line item")
+    args = ap.parse_args()
+
+    world, rank, local, pg = dist_setup(args)
+    wl = PRESETS[args.workload]
+    units_per_step = wl.n_query
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sample = OracleSample(wl)
+        for _ in range(args.warmup):
+            sample.run_one()
+        t0 = time.perf_counter()
+        n_done = 0
+        for _ in range(args.steps):
+            sample.run_one()
+            n_done += 1
+        el = time.perf_counter() - t0
+        val = n_done / el
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": wl.name, "batch": wl.n_seq, "context": wl.ctx_len[0],
+                           "compress_ratio": wl.m, "topk": wl.topk, "window": wl.window,
+                           "step_sample": "one decode query per step (a bounded sample of the batch)"},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"{args.steps} single-query steps of {wl.name} through the float64 "
+                                           "NumPy oracle"},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the gb300 arm")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
+    sampler = ClockSampler(local)
+    sampler.start()
+    r = run_gpu_workload(args, wl, rank, pg, device, (hbm, bf16_burst))
+    sampler.stop()
+    clocks = sampler.summary()
+    ms_step = r["ms_max"] / args.steps
+    value = world * units_per_step * args.steps / (r["ms_max"] / 1000.0)
+    step_bytes = algorithmic_bytes(wl)
+    gbs = step_bytes / (ms_step / 1000.0) / 1e9
+    idx_b = index_bytes(wl)
+    idx_gbs = idx_b / (r["idx_ms"] / 1000.0) / 1e9
+    e2e = r["e2e"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.n_seq, "context": wl.ctx_len[0], "compress_ratio": wl.m,
+                   "topk": wl.topk, "window": wl.window, "heads": "64x512", "indexer": f"{wl.idx_heads}x128",
+                   "kv": "fp8_e4m3_ue8m0_b32" if wl.kv_fp8 else "bf16",
+                   "l2": f"{N_COPIES} rotating input copies ({N_COPIES * step_bytes / 1e6:.0f} MB > 129 MB L2)",
+                   "graph": "one CUDA graph per step"},
+        "hbm_gbs": gbs, "hbm_frac": gbs / hbm, "step_algorithmic_bytes": step_bytes,
+        "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": idx_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": idx_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                     "bytes_per_launch": idx_b, "ms_per_launch": r["idx_ms"]},
+        "e2e": {"value": world * units_per_step / (e2e["ms_per_step"] / 1000.0), "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"]},
+        "gpu_launches": r["launches"] * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_extra and wl.name == "decode_64k_b32" and world == 1:
+        try:
+            wl4 = PRESETS["decode_1m_b8_fp8"]
+            a2 = argparse.Namespace(**vars(args))
+            a2.steps = min(args.steps, 500)
+            r4 = run_gpu_workload(a2, wl4, rank, None, device, (hbm, bf16_burst))
+            ms4 = r4["ms"] / a2.steps
+            b4 = algorithmic_bytes(wl4)
+            line["extra_1m"] = {"workload": wl4.name, "tokens_per_s": wl4.n_query / (ms4 / 1000.0),
+                                "ms_per_step": ms4, "hbm_gbs": b4 / (ms4 / 1000.0) / 1e9,
+                                "hbm_frac": b4 / (ms4 / 1000.0) / 1e9 / hbm,
+                                "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_1m"] = {"error": repr(ex)[:300]}
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,399 @@
+// Host side of the CSA2 C ABI: context, argument validation, workspace
+// carving, kernel launches and the Full / Reindex / Reuse step dispatch.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "launchers.cuh"
+
+
+
+struct csa2_ctx {
+  csa2_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  csa2::RopeParams rope;
+  uint32_t* d_flags = nullptr;
+  std::string err;
+  int last_launches = 0;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t al(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+csa2_status fail(csa2_ctx* c, csa2_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  return s;
+}
+
+csa2_status cuda_fail(csa2_ctx* c, cudaError_t e, const char* where) {
+  return fail(c, CSA2_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+// YaRN ("NTK-by-parts", DeepSeek-V3 ramp) frequencies of the rotated pairs.
+void rope_frequencies(const csa2_config& c, double* f) {
+  const int half = c.rope_dim / 2;
+  for (int i = 0; i < half; ++i) f[i] = std::pow(c.rope_theta, -(2.0 * i) / c.rope_dim);
+  if (!(c.yarn_factor > 1.0)) return;
+  auto boundary = [&](double turns) {
+    return c.rope_dim * std::log(c.yarn_orig_len / (turns * 2.0 * M_PI)) / (2.0 * std::log(c.rope_theta));
+  };
+  double lo = std::floor(boundary(c.yarn_beta_fast));
+  double hi = std::ceil(boundary(c.yarn_beta_slow));
+  if (lo < 0) lo = 0;
+  if (hi > c.rope_dim - 1) hi = c.rope_dim - 1;
+  if (hi == lo) hi += 0.001;
+  for (int i = 0; i < half; ++i) {
+    double ramp = (i - lo) / (hi - lo);
+    ramp = ramp < 0 ? 0 : (ramp > 1 ? 1 : ramp);
+    // ramp 0 keeps the frequency, 1 divides it by the factor
+    f[i] = f[i] * (1.0 - ramp) + f[i] / c.yarn_factor * ramp;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa2_status check_ws(csa2_ctx* c, const void* ws, size_t have, size_t need) {
+  if (need == 0) return CSA2_OK;
+  if (ws == nullptr || have < need)
+    return fail(c, CSA2_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes");
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return fail(c, CSA2_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void csa2_default_config(csa2_config* c) {
+  if (!c) return;
+  std::memset(c, 0, sizeof(*c));
+  c->n_heads = 64;
+  c->head_dim = 512;
+  c->rope_dim = 64;
+  c->window = 128;
+  c->compress_ratio = 4;
+  c->idx_heads = 8;
+  c->idx_dim = 128;
+  c->topk = 512;
+  c->kv_format = CSA2_KV_BF16;
+  c->idx_key_format = CSA2_KV_BF16;
+  c->softmax_scale = 1.0f / std::sqrt(512.0f);
+  c->norm_eps = 1e-20f;
+  c->rope_theta = 160000.0;
+  c->yarn_factor = 16.0;
+  c->yarn_orig_len = 65536.0;
+  c->yarn_beta_fast = 32.0;
+  c->yarn_beta_slow = 1.0;
+}
+
+const char* csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported geometry";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_DEVICE_FLAG: return "bad input recorded on the device";
+    case CSA2_ERR_TIMEOUT: return "device wait timed out";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
+  if (!cfg || !out) return CSA2_ERR_INVALID_ARG;
+  *out = nullptr;
+  const csa2_config& c = *cfg;
+  if (c.n_heads != 64 || c.head_dim != 512 || c.idx_dim != 128) return CSA2_ERR_UNSUPPORTED;
+  if (!(c.rope_dim == 0 || c.rope_dim == 64)) return CSA2_ERR_UNSUPPORTED;
+  if (c.window < 1 || c.window > 128) return CSA2_ERR_UNSUPPORTED;
+  if (c.compress_ratio < 1 || c.compress_ratio > 16) return CSA2_ERR_UNSUPPORTED;
+  if (!(c.idx_heads == 8 || c.idx_heads == 16 || c.idx_heads == 32)) return CSA2_ERR_UNSUPPORTED;
+  if (c.topk < 1 || c.topk > 2048) return CSA2_ERR_UNSUPPORTED;
+  if ((c.kv_format != CSA2_KV_BF16 && c.kv_format != CSA2_KV_FP8_E4M3_B32) ||
+      (c.idx_key_format != CSA2_KV_BF16 && c.idx_key_format != CSA2_KV_FP8_E4M3_B32))
+    return CSA2_ERR_UNSUPPORTED;
+  if (!(c.rope_theta > 0) || !(c.yarn_orig_len > 0) || !(c.yarn_beta_fast > 0) || !(c.yarn_beta_slow > 0) ||
+      !std::isfinite(c.softmax_scale) || !(c.norm_eps >= 0))
+    return CSA2_ERR_INVALID_ARG;
+  csa2_ctx* ctx = new csa2_ctx();
+  ctx->cfg = c;
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_flags, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_flags, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (ctx->d_flags) cudaFree(ctx->d_flags);
+    delete ctx;
+    return CSA2_ERR_CUDA;
+  }
+  std::memset(&ctx->rope, 0, sizeof(ctx->rope));
+  ctx->rope.pairs = c.rope_dim / 2;
+  rope_frequencies(c, ctx->rope.freq);
+  *out = ctx;
+  return CSA2_OK;
+}
+
+void csa2_destroy(csa2_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->d_flags) cudaFree(ctx->d_flags);
+  delete ctx;
+}
+
+const char* csa2_last_error(const csa2_ctx* ctx) { return ctx ? ctx->err.c_str() : "no context"; }
+
+int32_t csa2_last_launch_count(const csa2_ctx* ctx) { return ctx ? ctx->last_launches : 0; }
+
+csa2_status csa2_rope_frequencies(const csa2_ctx* ctx, double* out, int32_t n) {
+  if (!ctx || !out || n < ctx->rope.pairs) return CSA2_ERR_INVALID_ARG;
+  for (int i = 0; i < ctx->rope.pairs; ++i) out[i] = ctx->rope.freq[i];
+  return CSA2_OK;
+}
+
+csa2_status csa2_check(csa2_ctx* ctx, void* stream, uint32_t* flags_out) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpy(&h, ctx->d_flags, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_flags, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "csa2_check");
+  if (flags_out) *flags_out = h;
+  if (h & CSA2_FLAG_WAIT_TIMEOUT) return fail(ctx, CSA2_ERR_TIMEOUT, "a device wait timed out");
+  if (h) {
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "device error word 0x%x", h);
+    return fail(ctx, CSA2_ERR_DEVICE_FLAG, buf);
+  }
+  return CSA2_OK;
+}
+
+csa2_status csa2_store_rows(csa2_ctx* ctx, void* stream, const float* rows, int64_t n_rows, int32_t dim,
+                            const int64_t* pos, int32_t format, void* out, uint8_t* out_scale) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (n_rows < 0 || !(dim == 512 || dim == 128)) return fail(ctx, CSA2_ERR_INVALID_ARG, "dim must be 128 or 512");
+  if (format != CSA2_KV_BF16 && format != CSA2_KV_FP8_E4M3_B32) return fail(ctx, CSA2_ERR_INVALID_ARG, "format");
+  if (n_rows == 0) return CSA2_OK;
+  if (!rows || !out || (format == CSA2_KV_FP8_E4M3_B32 && !out_scale) || !aligned16(rows) || !aligned16(out))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "store_rows: null or misaligned buffer");
+  cudaError_t e = csa2::launch_store_rows(reinterpret_cast<cudaStream_t>(stream), rows, n_rows, dim, pos,
+                                          ctx->rope, format == CSA2_KV_FP8_E4M3_B32, out, out_scale);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "store_rows");
+  ctx->last_launches = 1;
+  return CSA2_OK;
+}
+
+static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* raw, const float* gate, int32_t n_seq,
+                               int64_t n_tokens, const int64_t* tok_off, const int64_t* first_pos,
+                               const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
+                               const float* k_norm_w, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
+                               uint8_t* idx_key_scale) {
+  const csa2_config& c = ctx->cfg;
+  const int m = c.compress_ratio;
+  if (n_tokens < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_seq / n_tokens");
+  if (n_tokens == 0) return CSA2_OK;
+  if (n_tokens % m) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_tokens must be whole groups");
+  if (!raw || !tok_off || !first_pos || !pool_off || !norm_w || !pool_kv || (m > 1 && !gate))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: null pointer");
+  if (c.kv_format == CSA2_KV_FP8_E4M3_B32 && !pool_kv_scale)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: fp8 pool needs its scale array");
+  if (w_idx && (!k_norm_w || !idx_keys || (c.idx_key_format == CSA2_KV_FP8_E4M3_B32 && !idx_key_scale)))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: index key outputs missing");
+  if (!aligned16(raw) || (gate && !aligned16(gate)) || !aligned16(norm_w) || (w_idx && !aligned16(w_idx)))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: inputs must be 16-byte aligned");
+  cudaError_t e = csa2::launch_compress(st, n_tokens / m, raw, gate, m, n_seq, tok_off, first_pos, pool_off, norm_w,
+                                        w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
+                                        c.kv_format == CSA2_KV_FP8_E4M3_B32, c.idx_key_format == CSA2_KV_FP8_E4M3_B32,
+                                        pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
+  ctx->last_launches += 1;
+  return CSA2_OK;
+}
+
+csa2_status csa2_compress(csa2_ctx* ctx, void* stream, const uint16_t* raw, const float* gate, int32_t n_seq,
+                          int64_t n_tokens, const int64_t* tok_off, const int64_t* first_pos, const int64_t* pool_off,
+                          const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, void* pool_kv,
+                          uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_compress(ctx, reinterpret_cast<cudaStream_t>(stream), raw, gate, n_seq, n_tokens, tok_off, first_pos,
+                     pool_off, norm_w, w_idx, k_norm_w, pool_kv, pool_kv_scale, idx_keys, idx_key_scale);
+}
+
+static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q_idx,
+                            const float* w_heads, const void* idx_keys, const uint8_t* idx_key_scale,
+                            const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
+                            float* scores, int64_t ld) {
+  const csa2_config& c = ctx->cfg;
+  if (n_query < 0 || n_seq < 1 || max_vis < 0 || ld < max_vis)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: sizes");
+  if (n_query == 0 || max_vis == 0) return CSA2_OK;
+  if (!q_idx || !w_heads || !idx_keys || !pool_off || !seq_of_q || !n_vis || !scores)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: null pointer");
+  if (c.idx_key_format == CSA2_KV_FP8_E4M3_B32 && !idx_key_scale)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: fp8 keys need their scales");
+  if (!aligned16(q_idx) || !aligned16(idx_keys) || (idx_key_scale && (reinterpret_cast<uintptr_t>(idx_key_scale) & 3)))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: misaligned buffer");
+  cudaError_t e = csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, c.idx_key_format == CSA2_KV_FP8_E4M3_B32,
+                                           n_query, n_seq, max_vis, q_idx, w_heads, idx_keys, idx_key_scale, pool_off,
+                                           seq_of_q, n_vis, scores, ld, ctx->d_flags);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "index_score");
+  ctx->last_launches += 1;
+  return CSA2_OK;
+}
+
+csa2_status csa2_index_score(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q_idx,
+                             const float* w_heads, const void* idx_keys, const uint8_t* idx_key_scale,
+                             const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
+                             float* scores, int64_t scores_ld) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_index(ctx, reinterpret_cast<cudaStream_t>(stream), n_seq, n_query, q_idx, w_heads, idx_keys,
+                  idx_key_scale, pool_off, seq_of_q, n_vis, max_vis, scores, scores_ld);
+}
+
+size_t csa2_topk_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis) {
+  if (!ctx || n_query < 0 || max_vis < 0) return 0;
+  return csa2::topk_workspace_bytes(n_query, max_vis);
+}
+
+static csa2_status do_topk(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, const float* scores, int64_t ld,
+                           const int32_t* n_vis, int64_t max_vis, int32_t k, int32_t* out_idx, void* ws,
+                           size_t ws_bytes) {
+  if (n_query < 0 || max_vis < 0 || ld < max_vis || k < 1 || k > 2048)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "topk: sizes (k must be 1..2048)");
+  if (max_vis > 0xFFFFFFFEll) return fail(ctx, CSA2_ERR_UNSUPPORTED, "topk: rows longer than 2^32-2");
+  if (n_query == 0) return CSA2_OK;
+  if (!n_vis || !out_idx || (max_vis > 0 && !scores)) return fail(ctx, CSA2_ERR_INVALID_ARG, "topk: null pointer");
+  csa2_status s = check_ws(ctx, ws, ws_bytes, csa2::topk_workspace_bytes(n_query, max_vis));
+  if (s != CSA2_OK) return s;
+  int nl = 0;
+  cudaError_t e = csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "topk");
+  ctx->last_launches += nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores, int64_t scores_ld,
+                      const int32_t* n_vis, int64_t max_vis, int32_t k, int32_t* out_idx, void* workspace,
+                      size_t workspace_bytes) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_topk(ctx, reinterpret_cast<cudaStream_t>(stream), n_query, scores, scores_ld, n_vis, max_vis, k, out_idx,
+                 workspace, workspace_bytes);
+}
+
+size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query) {
+  if (!ctx || n_query < 0) return 0;
+  const int nt = csa2::attend_num_tiles(ctx->cfg.topk, true);
+  int ns = csa2::attend_num_splits(n_query, nt, ctx->num_sms);
+  const int tps = (nt + ns - 1) / ns;
+  ns = (nt + tps - 1) / tps;
+  return csa2::attend_workspace_bytes(n_query, ns);
+}
+
+static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                             const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv,
+                             const uint8_t* win_scale, const int64_t* win_off, const int64_t* win_lo,
+                             const void* pool_kv, const uint8_t* pool_scale, const int64_t* pool_off,
+                             const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse, void* ws,
+                             size_t ws_bytes) {
+  const csa2_config& c = ctx->cfg;
+  const bool fp8 = c.kv_format == CSA2_KV_FP8_E4M3_B32;
+  if (n_query < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: sizes");
+  if (n_query == 0) return CSA2_OK;
+  if (!q || !q_pos || !seq_of_q || !win_kv || !win_off || !sink || !out ||
+      (topk_idx && (!pool_kv || !pool_off)) || (fp8 && (!win_scale || (topk_idx && !pool_scale))))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: null pointer");
+  if (!aligned16(q) || !aligned16(win_kv) || (pool_kv && !aligned16(pool_kv)) || (reinterpret_cast<uintptr_t>(out) & 3))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: misaligned buffer");
+  const size_t need = csa2_attend_workspace_size(ctx, n_query);
+  csa2_status s = check_ws(ctx, ws, ws_bytes, topk_idx ? need : 0);
+  if (s != CSA2_OK) return s;
+  csa2::AttendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.q_pos = q_pos; p.seq_of_q = seq_of_q;
+  p.win_kv = win_kv; p.win_scale = win_scale; p.win_off = win_off; p.win_lo = win_lo;
+  p.pool_kv = pool_kv; p.pool_scale = pool_scale; p.pool_off = pool_off;
+  p.topk_idx = topk_idx; p.sink = sink; p.out = out; p.lse = lse;
+  p.flags = ctx->d_flags;
+  p.n_seq = n_seq; p.n_query = n_query; p.topk = c.topk; p.window = c.window;
+  p.scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  p.rp = ctx->rope;
+  int nl = 0;
+  cudaError_t e = csa2::launch_attend(st, ctx->num_sms, fp8, p, ws, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "attend");
+  ctx->last_launches += nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                        const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv, const uint8_t* win_scale,
+                        const int64_t* win_off, const int64_t* win_lo, const void* pool_kv, const uint8_t* pool_scale,
+                        const int64_t* pool_off, const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse,
+                        void* workspace, size_t workspace_bytes) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_attend(ctx, reinterpret_cast<cudaStream_t>(stream), n_seq, n_query, q, q_pos, seq_of_q, win_kv, win_scale,
+                   win_off, win_lo, pool_kv, pool_scale, pool_off, topk_idx, sink, out, lse, workspace,
+                   workspace_bytes);
+}
+
+size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis) {
+  if (!ctx || n_query < 0 || max_vis < 0) return 0;
+  const size_t scores = al((size_t)n_query * (size_t)(max_vis > 0 ? max_vis : 1) * 4);
+  const size_t tk = al(csa2_topk_workspace_size(ctx, n_query, max_vis));
+  const size_t at = al(csa2_attend_workspace_size(ctx, n_query));
+  return scores + (tk > at ? tk : at);
+}
+
+csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (!a) return fail(ctx, CSA2_ERR_INVALID_ARG, "step: null args");
+  if (a->mode != CSA2_MODE_FULL && a->mode != CSA2_MODE_REINDEX && a->mode != CSA2_MODE_REUSE)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "step: unknown mode");
+  if (!a->topk_idx) return fail(ctx, CSA2_ERR_INVALID_ARG, "step: topk_idx is required");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t need = csa2_step_workspace_size(ctx, a->n_query, a->max_vis);
+  csa2_status s = check_ws(ctx, a->workspace, a->workspace_bytes, need);
+  if (s != CSA2_OK) return s;
+  char* ws = reinterpret_cast<char*>(a->workspace);
+  const int64_t ld = a->max_vis > 0 ? a->max_vis : 1;
+  float* scores = reinterpret_cast<float*>(ws);
+  char* rest = ws + al((size_t)a->n_query * (size_t)ld * 4);
+  const size_t rest_bytes = a->workspace_bytes - (size_t)(rest - ws);
+  int launches = 0;
+  if (a->mode == CSA2_MODE_FULL) {
+    s = do_compress(ctx, st, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off, a->norm_w,
+                    a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale);
+    if (s != CSA2_OK) return s;
+    launches += ctx->last_launches;
+  }
+  if (a->mode == CSA2_MODE_FULL || a->mode == CSA2_MODE_REINDEX) {
+    ctx->last_launches = 0;
+    s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
+                 a->seq_of_q, a->n_vis, a->max_vis, scores, ld);
+    if (s != CSA2_OK) return s;
+    launches += ctx->last_launches;
+    ctx->last_launches = 0;
+    s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, rest, rest_bytes);
+    if (s != CSA2_OK) return s;
+    launches += ctx->last_launches;
+  }
+  ctx->last_launches = 0;
+  s = do_attend(ctx, st, a->n_seq, a->n_query, a->q, a->q_pos, a->seq_of_q, a->win_kv, a->win_scale, a->win_off,
+                a->win_lo, a->pool_kv, a->pool_scale, a->pool_off, a->topk_idx, a->sink, a->out, a->lse, rest,
+                rest_bytes);
+  if (s != CSA2_OK) return s;
+  ctx->last_launches += launches;
+  return CSA2_OK;
+}
+
+}  // extern "C"

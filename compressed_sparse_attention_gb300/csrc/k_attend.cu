@@ -1,0 +1,523 @@
+// Two-source sparse attention with a per-head sink ("Reading Notes of
+// DeepSeek-V4.1-Flash", section 3a and section 3f, C2 step 3; "DeepSeek-V4.1-
+// Flash on WASTE", "What is new" item 1: the sink enters the denominator only,
+// the output's rope channels are rotated back by -t).
+//
+// One CTA (128 threads) owns one query and a contiguous range of 128-row
+// tiles: tile 0 is the query's window, tiles 1.. are the selected compressed
+// entries, 128 per tile. All 64 heads share each KV row, so per tile the two
+// products are dense contractions on the tensor cores, in transposed form so
+// that the 128 gathered rows are the M = 128 dimension:
+//   S^T [128 rows x 64 heads] = KV [128 x 512] . Q^T          (K = 512)
+//   O^T [512 dims x 64 heads] += KV^T [512 x 128] . P^T       (K = 128)
+// KV sits in shared memory once, in the 128-byte-swizzled layout that is at
+// the same time the K-major A operand of the first product and the MN-major
+// A operand of the second. S^T (64 columns) and O^T (4 x 64 columns) live in
+// tensor memory. Softmax runs with one thread per row (TMEM lane), heads
+// reduced across lanes by a butterfly reduce-scatter; the running max / sum
+// rescale O^T in tensor memory when a later tile raises a head's max.
+// With several CTAs per query (split-K) each writes its unnormalised O^T and
+// (max, sum) and a merge kernel combines them with the sink.
+#include "launchers.cuh"
+
+namespace csa2 {
+
+constexpr int kTileRows = 128;
+constexpr int kAttThreads = 128;
+constexpr uint32_t SM_Q = 0;                          // [8 dim blocks][64 heads][128 B]
+constexpr uint32_t SM_KV = 65536;                     // [8 dim blocks][128 rows][128 B]
+constexpr uint32_t SM_P = SM_KV + 131072;             // [128 rows][128 B]  (64 heads, bf16)
+constexpr uint32_t SM_RED = SM_P + 16384;             // float [4][64]
+constexpr uint32_t SM_MRUN = SM_RED + 1024;           // float [64]
+constexpr uint32_t SM_LRUN = SM_MRUN + 256;           // float [64]
+constexpr uint32_t SM_MUSE = SM_LRUN + 256;           // float [64]
+constexpr uint32_t SM_ALPHA = SM_MUSE + 256;          // float [64]
+constexpr uint32_t SM_ROWS = SM_ALPHA + 256;          // int64 [128]
+constexpr uint32_t SM_MISC = SM_ROWS + 1024;          // mbarrier, tmem slot, flags
+constexpr uint32_t SM_TOTAL = SM_MISC + 64;
+constexpr uint32_t kAttSmemBytes = SM_TOTAL + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 64, 1, 1);
+
+// Butterfly reduce-scatter of 64 per-lane values over the 32 lanes of a warp:
+// afterwards lane l holds the reduction of heads h0(l), h0(l)+1 with
+// h0 = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0 (b_k = bit k of l).
+template <bool MAX>
+__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane, float& o0, float& o1) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int half = 32 >> step;      // values kept after this step
+    const int off = 16 >> step;       // xor distance
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < half) {
+        const float lo = v[i], hi = v[half + i];
+        const float send = upper ? lo : hi;
+        const float keep = upper ? hi : lo;
+        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+        v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+      }
+    }
+  }
+  o0 = v[0];
+  o1 = v[1];
+}
+
+__device__ __forceinline__ int rs_head(int lane) {
+  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 +
+         (lane & 1) * 2;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_s - raw_s);
+  float* red = reinterpret_cast<float*>(sm + SM_RED);
+  float* m_run = reinterpret_cast<float*>(sm + SM_MRUN);
+  float* l_run = reinterpret_cast<float*>(sm + SM_LRUN);
+  float* m_use = reinterpret_cast<float*>(sm + SM_MUSE);
+  float* alpha = reinterpret_cast<float*>(sm + SM_ALPHA);
+  int64_t* rows = reinterpret_cast<int64_t*>(sm + SM_ROWS);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + SM_MISC);  // [0..1] mbar, [2] tmem slot, [3] rescale, [4] abort
+  const uint32_t mbar = base_s + SM_MISC;
+  const uint32_t tslot = base_s + SM_MISC + 8;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qi = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
+  const int64_t t = p.q_pos[qi];
+  const int b = p.seq_of_q[qi];
+  const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
+  const int tile_begin = split * p.tiles_per_split;
+  const int tile_end = q_ok ? min(tile_begin + p.tiles_per_split, p.n_tiles) : tile_begin;
+  if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
+
+  if (warp == 0) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+    misc[3] = 0;
+    misc[4] = 0;
+  }
+  if (tid < kHeads) {
+    m_run[tid] = -INFINITY;
+    l_run[tid] = 0.f;
+  }
+  // ---- Q: rotate the rope channels at t, round to bf16, store swizzled (K-major B operand)
+  if (tile_begin < tile_end) {
+    const int first_rope = kDim - 2 * p.rp.pairs;
+    for (int h = warp; h < kHeads; h += 4) {
+      const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
+        uint4 v = *reinterpret_cast<const uint4*>(qh + 8 * c);
+        if (8 * c + 8 > first_rope && p.rp.pairs > 0) {
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int ch = 8 * c + 2 * k;
+            if (ch >= first_rope) {
+              float cs, sn;
+              rope_cs(p.rp, (ch - first_rope) >> 1, t, cs, sn);
+              const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
+              w[k] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+            }
+          }
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        const uint32_t off = SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
+                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + off) = v;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = misc[2];
+  const uint32_t tmem_s = taddr;        // columns [0, 64)
+  const uint32_t tmem_o = taddr + 64;   // columns [64, 320)
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  uint32_t phase = 0;
+  bool aborted = false;
+
+  const int64_t win_cap = q_ok ? (p.win_off[b + 1] - p.win_off[b]) : 0;
+  const int64_t lo_b = (q_ok && p.win_lo) ? max((int64_t)0, p.win_lo[b]) : 0;
+  const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
+  const int64_t plen = q_ok ? (p.pool_off[b + 1] - p.pool_off[b]) : 0;
+
+  for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
+    // ---- row sources of this tile (one thread per row)
+    {
+      const int r = tid;
+      int64_t src = -1;
+      if (tile == 0) {
+        const int64_t pos = lo_eff + r;
+        if (pos <= t && r < p.window) {
+          if (t - lo_eff + 1 > win_cap) {
+            set_flag(p.flags, CSA2_FLAG_BAD_WINDOW);
+          } else {
+            src = p.win_off[b] + (pos % win_cap);
+          }
+        }
+      } else {
+        const int col = (tile - 1) * kTileRows + r;
+        if (col < p.topk && p.topk_idx != nullptr) {
+          const int32_t j = p.topk_idx[(int64_t)qi * p.topk + col];
+          if (j >= 0 && j < plen) src = p.pool_off[b] + j;
+          else if (j != -1) set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+        }
+      }
+      rows[r] = src;
+    }
+    __syncthreads();
+    // ---- gather the tile's rows into the swizzled KV operand
+    const void* kvsrc = (tile == 0) ? p.win_kv : p.pool_kv;
+    if constexpr (!FP8) {
+      const uint16_t* kv = reinterpret_cast<const uint16_t*>(kvsrc);
+      for (int r = warp; r < kTileRows; r += 4) {
+        const int64_t src = rows[r];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = lane + 32 * cc;
+          const uint32_t dst = base_s + SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
+                               ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+          const uint16_t* g = src >= 0 ? kv + src * kDim + 8 * c : kv;
+          cp_async16(dst, g, src >= 0 ? 16u : 0u);
+        }
+      }
+      cp_async_wait_all();
+    } else {
+      const uint8_t* kv = reinterpret_cast<const uint8_t*>(kvsrc);
+      const uint8_t* ksc = (tile == 0) ? p.win_scale : p.pool_scale;
+      for (int r = warp; r < kTileRows; r += 4) {
+        const int64_t src = rows[r];
+        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (src >= 0) {
+          const uint4 codes = *reinterpret_cast<const uint4*>(kv + src * kDim + 16 * lane);
+          const float sc = ue8m0_value(ksc[src * (kDim / 32) + (lane >> 1)]);
+          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 a = e4m3x2_to_float2((uint16_t)(cw[k] & 0xFFFFu));
+            const float2 c2 = e4m3x2_to_float2((uint16_t)(cw[k] >> 16));
+            o[2 * k] = pack_bf16(a.x * sc, a.y * sc);
+            o[2 * k + 1] = pack_bf16(c2.x * sc, c2.y * sc);
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * lane + cc;  // bf16 chunk: channels 8c .. 8c+7
+          const uint32_t off = SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
+                               ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(sm + off) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    // ---- S^T = KV . Q^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll 4
+      for (int ks = 0; ks < 32; ++ks) {
+        const uint32_t koff = (uint32_t)(ks & 3) * 32u;
+        const uint64_t ad = sdesc_sw128(base_s + SM_KV + (uint32_t)(ks >> 2) * 16384u + koff, 16u, 1024u);
+        const uint64_t bd = sdesc_sw128(base_s + SM_Q + (uint32_t)(ks >> 2) * 8192u + koff, 16u, 1024u);
+        mma_bf16_ss(tmem_s, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+      }
+      mma_commit(mbar);
+    }
+    bool ok = mbar_wait(mbar, phase, p.flags);
+    phase ^= 1u;
+    if (!__syncthreads_and(ok)) { aborted = true; break; }
+    tc_fence_after();
+    // ---- softmax over this tile's rows (thread = row = TMEM lane)
+    float s[64];
+    {
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem_s + lane_base, r0);
+      tmem_ld32(tmem_s + lane_base + 32, r1);
+      tmem_wait_ld();
+      const bool valid = rows[tid] >= 0;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        s[k] = valid ? __uint_as_float(r0[k]) * p.scale_log2 : -INFINITY;
+        s[32 + k] = valid ? __uint_as_float(r1[k]) * p.scale_log2 : -INFINITY;
+      }
+    }
+    {
+      float v[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) v[k] = s[k];
+      float a0, a1;
+      reduce_scatter64<true>(v, lane, a0, a1);
+      const int h0 = rs_head(lane);
+      red[warp * 64 + h0] = a0;
+      red[warp * 64 + h0 + 1] = a1;
+    }
+    __syncthreads();
+    if (tid < kHeads) {
+      const float tmax = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+      const float mo = m_run[tid];
+      const float mn = fmaxf(mo, tmax);
+      const float mu = (mn == -INFINITY) ? 0.f : mn;
+      const float al = (mo == -INFINITY) ? 1.f : exp2f(mo - mu);
+      m_use[tid] = mu;
+      alpha[tid] = al;
+      m_run[tid] = mn;
+      if (al != 1.f && tile > tile_begin) misc[3] = 1;
+    }
+    __syncthreads();
+    {
+      float v[64];
+      uint32_t packed[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = exp2f(s[2 * k] - m_use[2 * k]);
+        const float p1 = exp2f(s[2 * k + 1] - m_use[2 * k + 1]);
+        packed[k] = pack_bf16(p0, p1);
+        v[2 * k] = bf16lo(packed[k]);
+        v[2 * k + 1] = bf16hi(packed[k]);
+      }
+      // P^T row `tid`: 64 heads = 8 chunks of 16 B (MN-major B operand)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t off = SM_P + (uint32_t)tid * 128u + ((uint32_t)(c ^ (tid & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + off) =
+            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+      }
+      float a0, a1;
+      reduce_scatter64<false>(v, lane, a0, a1);
+      const int h0 = rs_head(lane);
+      __syncthreads();  // every warp has read red[] (max) before it is reused for sums
+      red[warp * 64 + h0] = a0;
+      red[warp * 64 + h0 + 1] = a1;
+    }
+    __syncthreads();
+    if (tid < kHeads) {
+      const float ts = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+      l_run[tid] = alpha[tid] * l_run[tid] + ts;
+    }
+    // ---- rescale O^T in tensor memory where a head's running max rose
+    if (misc[3]) {
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          const uint32_t a = tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base;
+          tmem_ld32(a, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[32 * hh + k]);
+          tmem_st32(a, r);
+        }
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) misc[3] = 0;
+    // ---- O^T += KV^T . P^T
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = sdesc_sw128(base_s + SM_KV + (uint32_t)(2 * mt) * 16384u + (uint32_t)ks * 2048u,
+                                          16384u, 1024u);
+          const uint64_t bd = sdesc_sw128(base_s + SM_P + (uint32_t)ks * 2048u, 8192u, 1024u);
+          mma_bf16_ss(tmem_o + 64u * (uint32_t)mt, ad, bd, kIdescPV, (tile > tile_begin || ks > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(mbar);
+    }
+    ok = mbar_wait(mbar, phase, p.flags);
+    phase ^= 1u;
+    if (!__syncthreads_and(ok)) { aborted = true; break; }
+    tc_fence_after();
+  }
+
+  // ---- epilogue
+  __syncthreads();
+  const bool have_o = (tile_begin < tile_end) && !aborted;
+  const int first_rope = kDim - 2 * p.rp.pairs;
+  if (p.n_split == 1) {
+    // final normalisation with the sink: fo = e^{m - M} / den, den = l e^{m - M} + e^{sink - M}
+    if (tid < kHeads) {
+      const float sk = p.sink[tid] * 1.4426950408889634f;
+      const float mr = have_o ? m_run[tid] : -INFINITY;
+      const float M = fmaxf(mr, sk);
+      float fo = 0.f, lse = -INFINITY;
+      if (M != -INFINITY) {
+        const float em = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+        const float den = l_run[tid] * em + exp2f(sk - M);
+        fo = em / den;
+        lse = (M + log2f(den)) * 0.6931471805599453f;
+      }
+      alpha[tid] = fo;
+      if (p.lse) p.lse[(int64_t)qi * kHeads + tid] = lse;
+    }
+    __syncthreads();
+    uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
+    for (int mt = 0; mt < 4; ++mt) {
+      const int d = 128 * mt + 32 * warp + lane;
+      float cs = 1.f, sn = 0.f;
+      const bool rope = p.rp.pairs > 0 && d >= first_rope;
+      if (rope) rope_cs(p.rp, (d - first_rope) >> 1, t, cs, sn);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[32];
+        if (have_o) {
+          tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int h = 32 * hh + k;
+          float v = __uint_as_float(r[k]) * alpha[h];
+          const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+          if (rope) v = (d & 1) ? (v * cs - partner * sn) : (v * cs + partner * sn);
+          out[(int64_t)h * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+      }
+    }
+  } else {
+    // unnormalised partial O^T and (m, l) for the merge
+    const int64_t slot = (int64_t)qi * p.n_split + split;
+    if (tid < kHeads)
+      p.ws_ml[slot * kHeads + tid] = make_float2(have_o ? m_run[tid] : -INFINITY, have_o ? l_run[tid] : 0.f);
+    if (have_o) {
+      float* wo = p.ws_o + slot * kHeads * kDim;
+      for (int mt = 0; mt < 4; ++mt) {
+        const int d = 128 * mt + 32 * warp + lane;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) wo[(int64_t)(32 * hh + k) * kDim + d] = __uint_as_float(r[k]);
+        }
+      }
+    }
+  }
+  if (aborted) {
+    // let any tensor-core work still in flight land before freeing its memory
+    mbar_wait(mbar, phase ^ 1u, p.flags, 1000000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(taddr, kTmemCols);
+}
+
+// merge of split-K partials: one CTA per query, thread i owns channel pair (2i, 2i+1)
+__global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p) {
+  __shared__ float wsplit[8][kHeads];
+  __shared__ float lse_s[kHeads];
+  const int qi = blockIdx.x, tid = threadIdx.x;
+  const int ns = p.n_split;
+  const float2* ml = p.ws_ml + (int64_t)qi * ns * kHeads;
+  if (tid < kHeads) {
+    const float sk = p.sink[tid] * 1.4426950408889634f;
+    float M = sk;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * kHeads + tid].x);
+    float den = 0.f;
+    if (M != -INFINITY) {
+      den = exp2f(sk - M);
+      for (int s = 0; s < ns; ++s) {
+        const float2 v = ml[s * kHeads + tid];
+        if (v.x != -INFINITY) den += v.y * exp2f(v.x - M);
+      }
+    }
+    for (int s = 0; s < ns; ++s) {
+      const float2 v = ml[s * kHeads + tid];
+      wsplit[s][tid] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - M) / den;
+    }
+    lse_s[tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * 0.6931471805599453f;
+    if (p.lse) p.lse[(int64_t)qi * kHeads + tid] = lse_s[tid];
+  }
+  __syncthreads();
+  const int d0 = 2 * tid;
+  const int64_t t = p.q_pos[qi];
+  const int first_rope = kDim - 2 * p.rp.pairs;
+  float cs = 1.f, sn = 0.f;
+  const bool rope = p.rp.pairs > 0 && d0 >= first_rope;
+  if (rope) rope_cs(p.rp, (d0 - first_rope) >> 1, t, cs, sn);
+  uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
+  for (int h = 0; h < kHeads; ++h) {
+    float x0 = 0.f, x1 = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float w = wsplit[s][h];
+      if (w != 0.f) {
+        const float2 o = *reinterpret_cast<const float2*>(p.ws_o + (((int64_t)qi * ns + s) * kHeads + h) * kDim + d0);
+        x0 = fmaf(w, o.x, x0);
+        x1 = fmaf(w, o.y, x1);
+      }
+    }
+    if (rope) {
+      const float y0 = x0 * cs + x1 * sn;
+      const float y1 = x1 * cs - x0 * sn;
+      x0 = y0;
+      x1 = y1;
+    }
+    *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + d0) = pack_bf16(x0, x1);
+  }
+}
+
+int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
+
+int attend_num_splits(int n_query, int n_tiles, int num_sms) {
+  if (n_query <= 0) return 1;
+  int ns = (num_sms + n_query - 1) / n_query;
+  if (ns > n_tiles) ns = n_tiles;
+  if (ns > 8) ns = 8;
+  if (ns < 1) ns = 1;
+  return ns;
+}
+
+size_t attend_workspace_bytes(int n_query, int n_split) {
+  if (n_split <= 1) return 0;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return al((size_t)n_query * n_split * kHeads * kDim * 4) + al((size_t)n_query * n_split * kHeads * 8);
+}
+
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch) {
+  if (p.n_query == 0) return cudaSuccess;
+  p.n_tiles = attend_num_tiles(p.topk, p.topk_idx != nullptr);
+  p.n_split = attend_num_splits(p.n_query, p.n_tiles, num_sms);
+  p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
+  p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  if (p.n_split > 1) {
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) +
+                                        al((size_t)p.n_query * p.n_split * kHeads * kDim * 4));
+  }
+  cudaError_t e;
+  if (kv_fp8) e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
+  else e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)(p.n_query * p.n_split));
+  if (kv_fp8) attend_kernel<true><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
+  else attend_kernel<false><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
+  *n_launch += 1;
+  if (p.n_split > 1) {
+    attend_merge_kernel<<<p.n_query, 256, 0, st>>>(p);
+    *n_launch += 1;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,259 @@
+// Row storage (RoPE + bf16 / fp8-block-32 store) and the CSA2 compressor.
+//
+// Compressor: "Reading Notes of DeepSeek-V4.1-Flash", section 3f, C2 step 1
+// (softmax-gated pooling of m consecutive tokens); "DeepSeek-V4.1-Flash on
+// WASTE", "What is new" item 1 (fp32 pooling, then RMS-normalised); PocketLLM
+// "DeepSeek-V4.1-Flash", "The CSA2 attention layers" (the index key is taken
+// from the unrotated latent; the latent is rotated at its group's first token
+// position j*m before it is stored).
+#include "launchers.cuh"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------------------
+// store_rows: one warp per row; lane owns DIM/32 contiguous channels.
+// ---------------------------------------------------------------------------
+template <int DIM, bool FP8>
+__global__ void __launch_bounds__(256) store_rows_kernel(const float* __restrict__ rows, int64_t n_rows,
+                                                         const int64_t* __restrict__ pos, RopeParams rp,
+                                                         void* __restrict__ out, uint8_t* __restrict__ out_scale) {
+  constexpr int E = DIM / 32;  // channels per lane (4 or 16)
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  float v[E];
+  const float4* src = reinterpret_cast<const float4*>(rows + row * DIM + lane * E);
+#pragma unroll
+  for (int k = 0; k < E / 4; ++k) {
+    float4 f = src[k];
+    v[4 * k] = f.x; v[4 * k + 1] = f.y; v[4 * k + 2] = f.z; v[4 * k + 3] = f.w;
+  }
+  if (pos != nullptr && rp.pairs > 0) {
+    const int64_t p = pos[row];
+    const int first = DIM - 2 * rp.pairs;
+#pragma unroll
+    for (int k = 0; k < E; k += 2) {
+      const int ch = lane * E + k;
+      if (ch >= first) {
+        float c, s;
+        rope_cs(rp, (ch - first) >> 1, p, c, s);
+        const float x0 = v[k], x1 = v[k + 1];
+        v[k] = x0 * c - x1 * s;
+        v[k + 1] = x0 * s + x1 * c;
+      }
+    }
+  }
+  if constexpr (!FP8) {
+    uint32_t w[E / 2];
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) w[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
+    uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + row * DIM + lane * E);
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k) dst[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+  } else {
+    constexpr int LPB = 32 / E;  // lanes per 32-channel block
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(v[k]));
+#pragma unroll
+    for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const uint32_t eb = fp8_scale_byte(amax);
+    const int sh = 127 - (int)eb;  // x / 2^(eb-127), exact
+    uint8_t* dst = reinterpret_cast<uint8_t*>(out) + row * DIM + lane * E;
+#pragma unroll
+    for (int k = 0; k < E; k += 4) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) word |= (uint32_t)f32_to_e4m3(ldexpf(v[k + u], sh)) << (8 * u);
+      *reinterpret_cast<uint32_t*>(dst + k) = word;
+    }
+    if ((lane % LPB) == 0) out_scale[row * (DIM / 32) + lane / LPB] = (uint8_t)eb;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compress: one CTA of 128 threads per closed group; thread t owns channels
+// 4t..4t+3 of the 512-wide latent.
+// ---------------------------------------------------------------------------
+template <bool KV_FP8, bool IDX_FP8>
+__global__ void __launch_bounds__(128) compress_kernel(
+    const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
+    const int64_t* __restrict__ tok_off, const int64_t* __restrict__ first_pos,
+    const int64_t* __restrict__ pool_off, const float* __restrict__ norm_w,
+    const uint16_t* __restrict__ w_idx, const float* __restrict__ k_norm_w, int idx_dim, float eps,
+    RopeParams rp, void* __restrict__ pool_kv, uint8_t* __restrict__ pool_kv_scale,
+    void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags) {
+  __shared__ float c_hat_s[kDim];
+  __shared__ float k_lin_s[kIdxDim];
+  __shared__ float red_s[4];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t tok0 = (int64_t)blockIdx.x * m;
+  const int b = find_segment(tok_off, n_seq + 1, tok0);
+  const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
+  if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || b >= n_seq || tok0 >= seg1) {
+    if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
+    return;
+  }
+  const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
+  const int64_t j = pos0 / m;
+  const int64_t prow = pool_off[b] + j;
+  if (prow >= pool_off[b + 1]) {
+    if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
+    return;
+  }
+  const int c0 = 4 * tid;
+  // ---- pooling (fp32): per channel softmax of the gate logits over the group
+  float pooled[4];
+  if (m == 1) {
+    const uint2 w = *reinterpret_cast<const uint2*>(raw + tok0 * kDim + c0);
+    pooled[0] = bf16lo(w.x); pooled[1] = bf16hi(w.x); pooled[2] = bf16lo(w.y); pooled[3] = bf16hi(w.y);
+  } else {
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int u = 0; u < m; ++u) {
+      const float4 gv = *reinterpret_cast<const float4*>(gate + (tok0 + u) * kDim + c0);
+      mx[0] = fmaxf(mx[0], gv.x); mx[1] = fmaxf(mx[1], gv.y);
+      mx[2] = fmaxf(mx[2], gv.z); mx[3] = fmaxf(mx[3], gv.w);
+    }
+    float den[4] = {0.f, 0.f, 0.f, 0.f}, num[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int u = 0; u < m; ++u) {
+      const float4 gv = *reinterpret_cast<const float4*>(gate + (tok0 + u) * kDim + c0);
+      const uint2 w = *reinterpret_cast<const uint2*>(raw + (tok0 + u) * kDim + c0);
+      const float e0 = expf(gv.x - mx[0]), e1 = expf(gv.y - mx[1]);
+      const float e2 = expf(gv.z - mx[2]), e3 = expf(gv.w - mx[3]);
+      den[0] += e0; den[1] += e1; den[2] += e2; den[3] += e3;
+      num[0] = fmaf(e0, bf16lo(w.x), num[0]); num[1] = fmaf(e1, bf16hi(w.x), num[1]);
+      num[2] = fmaf(e2, bf16lo(w.y), num[2]); num[3] = fmaf(e3, bf16hi(w.y), num[3]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pooled[k] = num[k] / den[k];
+  }
+  // ---- RMSNorm with norm_w
+  float ss = pooled[0] * pooled[0] + pooled[1] * pooled[1] + pooled[2] * pooled[2] + pooled[3] * pooled[3];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red_s[warp] = ss;
+  __syncthreads();
+  const float tot = red_s[0] + red_s[1] + red_s[2] + red_s[3];
+  const float inv = 1.0f / sqrtf(tot / (float)kDim + eps);
+  const float4 nw = *reinterpret_cast<const float4*>(norm_w + c0);
+  float ch[4] = {pooled[0] * inv * nw.x, pooled[1] * inv * nw.y, pooled[2] * inv * nw.z, pooled[3] * inv * nw.w};
+  // ---- index key from the unrotated latent
+  if (w_idx != nullptr) {
+    *reinterpret_cast<float4*>(&c_hat_s[c0]) = make_float4(ch[0], ch[1], ch[2], ch[3]);
+    __syncthreads();
+    float cv[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) cv[k] = c_hat_s[16 * lane + k];
+    const int per_warp = idx_dim / 4;
+    for (int oo = 0; oo < per_warp; ++oo) {
+      const int o = warp * per_warp + oo;
+      const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)o * kDim + 16 * lane);
+      const uint4 wa = wr[0], wb = wr[1];
+      float acc = 0.f;
+      acc = fmaf(cv[0], bf16lo(wa.x), acc); acc = fmaf(cv[1], bf16hi(wa.x), acc);
+      acc = fmaf(cv[2], bf16lo(wa.y), acc); acc = fmaf(cv[3], bf16hi(wa.y), acc);
+      acc = fmaf(cv[4], bf16lo(wa.z), acc); acc = fmaf(cv[5], bf16hi(wa.z), acc);
+      acc = fmaf(cv[6], bf16lo(wa.w), acc); acc = fmaf(cv[7], bf16hi(wa.w), acc);
+      acc = fmaf(cv[8], bf16lo(wb.x), acc); acc = fmaf(cv[9], bf16hi(wb.x), acc);
+      acc = fmaf(cv[10], bf16lo(wb.y), acc); acc = fmaf(cv[11], bf16hi(wb.y), acc);
+      acc = fmaf(cv[12], bf16lo(wb.z), acc); acc = fmaf(cv[13], bf16hi(wb.z), acc);
+      acc = fmaf(cv[14], bf16lo(wb.w), acc); acc = fmaf(cv[15], bf16hi(wb.w), acc);
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+      if (lane == 0) k_lin_s[o] = acc;
+    }
+    __syncthreads();
+    // RMSNorm of the key; warp w owns outputs [32w, 32w+32) (one fp8 block)
+    float kss = 0.f;
+    for (int o = lane; o < idx_dim; o += 32) kss += k_lin_s[o] * k_lin_s[o];
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) kss += __shfl_xor_sync(0xffffffffu, kss, s);
+    const float kinv = 1.0f / sqrtf(kss / (float)idx_dim + eps);
+    for (int base = warp * 32; base < idx_dim; base += 128) {
+      const int o = base + lane;
+      const float kv = k_lin_s[o] * kinv * k_norm_w[o];
+      if constexpr (!IDX_FP8) {
+        reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] =
+            (uint16_t)(pack_bf16(kv, 0.f) & 0xFFFFu);
+      } else {
+        float amax = fabsf(kv);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+        const uint32_t eb = fp8_scale_byte(amax);
+        reinterpret_cast<uint8_t*>(idx_keys)[prow * idx_dim + o] = f32_to_e4m3(ldexpf(kv, 127 - (int)eb));
+        if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + base / 32] = (uint8_t)eb;
+      }
+    }
+  }
+  // ---- RoPE at the group's first token position, then store
+  if (rp.pairs > 0) {
+    const int first = kDim - 2 * rp.pairs;
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+      const int c = c0 + k;
+      if (c >= first) {
+        float cs, sn;
+        rope_cs(rp, (c - first) >> 1, pos0, cs, sn);
+        const float x0 = ch[k], x1 = ch[k + 1];
+        ch[k] = x0 * cs - x1 * sn;
+        ch[k + 1] = x0 * sn + x1 * cs;
+      }
+    }
+  }
+  if constexpr (!KV_FP8) {
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(pool_kv) + prow * kDim + c0) =
+        make_uint2(pack_bf16(ch[0], ch[1]), pack_bf16(ch[2], ch[3]));
+  } else {
+    float amax = fmaxf(fmaxf(fabsf(ch[0]), fabsf(ch[1])), fmaxf(fabsf(ch[2]), fabsf(ch[3])));
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+    const uint32_t eb = fp8_scale_byte(amax);
+    const int sh = 127 - (int)eb;
+    uint32_t word = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) word |= (uint32_t)f32_to_e4m3(ldexpf(ch[u], sh)) << (8 * u);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(pool_kv) + prow * kDim + c0) = word;
+    if ((tid & 7) == 0) pool_kv_scale[prow * (kDim / 32) + tid / 8] = (uint8_t)eb;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
+                              const RopeParams& rp, int fp8, void* out, uint8_t* out_scale) {
+  if (n_rows == 0) return cudaSuccess;
+  const int rows_per_block = 8;
+  const dim3 grid((unsigned)((n_rows + rows_per_block - 1) / rows_per_block));
+  if (dim == 512) {
+    if (fp8) store_rows_kernel<512, true><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+    else store_rows_kernel<512, false><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+  } else {
+    if (fp8) store_rows_kernel<128, true><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+    else store_rows_kernel<128, false><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
+                            int n_seq, const int64_t* tok_off, const int64_t* first_pos,
+                            const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
+                            const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fp8,
+                            int idx_fp8, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
+                            uint8_t* idx_key_scale, uint32_t* flags) {
+  if (n_groups == 0) return cudaSuccess;
+  const dim3 grid((unsigned)n_groups);
+#define CSA2_COMPRESS(KF, IF)                                                                      \
+  compress_kernel<KF, IF><<<grid, 128, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
+                                                norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
+                                                pool_kv_scale, idx_keys, idx_key_scale, flags)
+  if (kv_fp8) {
+    if (idx_fp8) CSA2_COMPRESS(true, true); else CSA2_COMPRESS(true, false);
+  } else {
+    if (idx_fp8) CSA2_COMPRESS(false, true); else CSA2_COMPRESS(false, false);
+  }
+#undef CSA2_COMPRESS
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,56 @@
+// Internal launcher declarations shared by the kernel files and the C-ABI host
+// code (not part of the public interface).
+#pragma once
+#include "common.cuh"
+
+namespace csa2 {
+
+struct AttendParams {
+  const uint16_t* q;
+  const int64_t* q_pos;
+  const int32_t* seq_of_q;
+  const void* win_kv;
+  const uint8_t* win_scale;
+  const int64_t* win_off;
+  const int64_t* win_lo;
+  const void* pool_kv;
+  const uint8_t* pool_scale;
+  const int64_t* pool_off;
+  const int32_t* topk_idx;
+  const float* sink;
+  uint16_t* out;
+  float* lse;
+  float* ws_o;    // [n_query][n_split][64][512] unnormalised partial outputs
+  float2* ws_ml;  // [n_query][n_split][64] running (max, sum) per head
+  uint32_t* flags;
+  int n_seq;
+  int n_query;
+  int topk;
+  int window;
+  int n_tiles;
+  int n_split;
+  int tiles_per_split;
+  float scale_log2;  // softmax_scale * log2(e)
+  RopeParams rp;
+};
+
+cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
+                              const RopeParams& rp, int fp8, void* out, uint8_t* out_scale);
+cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
+                            int n_seq, const int64_t* tok_off, const int64_t* first_pos, const int64_t* pool_off,
+                            const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
+                            float eps, const RopeParams& rp, int kv_fp8, int idx_fp8, void* pool_kv,
+                            uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags);
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fp8, int n_query, int n_seq,
+                               int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
+                               const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
+                               const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags);
+size_t topk_workspace_bytes(int n_query, int64_t max_vis);
+cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
+                        int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch);
+int attend_num_tiles(int topk, bool has_idx);
+int attend_num_splits(int n_query, int n_tiles, int num_sms);
+size_t attend_workspace_bytes(int n_query, int n_split);
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch);
+
+}  // namespace csa2

@@ -1,0 +1,298 @@
+/*
+ * csa2.h - C ABI of the CSA2 compressed-sparse-attention step on one GB300
+ * (sm_103a) GPU.
+ *
+ * The step follows the method described in "Reading Notes of
+ * DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression",
+ * section 3f, component C2 (steps 1-4), together with "DeepSeek-V4.1-Flash
+ * on WASTE", section "What is new", item 1, and the PocketLLM page
+ * "DeepSeek-V4.1-Flash", section "The CSA2 attention layers". One layer step
+ * of a query at position t is:
+ *
+ *   compress     m raw KV vectors of a closed group -> one stored entry
+ *   index_score  sigma(j) = sum_h w_h * relu(q^I_h . k^I_j) over visible j
+ *   topk         the K largest sigma, ties to the lower index
+ *   attend       one softmax with a per-head sink over the window rows
+ *                [max(lo, t-w+1), t] and the selected entries
+ *
+ * Conventions for every entry point:
+ *   - Every array argument is a DEVICE pointer into memory the caller owns
+ *     (PyTorch allocates it), unless the comment says "host".
+ *   - Rows are row-major with the last axis contiguous. bf16 values travel as
+ *     uint16_t bit patterns. The fp8 format (CSA2_KV_FP8_E4M3_B32) stores one
+ *     e4m3 byte per channel plus one ue8m0 scale byte (value 2^(E-127)) per 32
+ *     consecutive channels, in a separate [rows, dim/32] byte array.
+ *   - `stream` is a cudaStream_t passed as void*; every call only enqueues
+ *     work on it (asynchronous, stream-ordered) and returns after host-side
+ *     argument validation.
+ *   - Nothing here aborts or traps. Host-side validation failures return
+ *     CSA2_ERR_INVALID_ARG / CSA2_ERR_UNSUPPORTED without enqueuing anything.
+ *     Bad values found on the device (an index outside its pool, a window
+ *     position outside its buffer, n_vis larger than the pool, a segment not
+ *     made of whole groups) are skipped by the kernels, which record a bit in
+ *     a device error word; csa2_check() synchronises and reports it.
+ *   - The library allocates device memory only inside csa2_create (one
+ *     status word). Scratch space is the caller's `workspace`, whose size the
+ *     *_workspace_size functions give; it must be 256-byte aligned.
+ *   - Strings returned by the library are owned by it.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned buffer    */
+  CSA2_ERR_UNSUPPORTED = 2,  /* a geometry the kernels were not built for     */
+  CSA2_ERR_CUDA = 3,         /* a CUDA runtime call failed (see last_error)   */
+  CSA2_ERR_DEVICE_FLAG = 4,  /* a kernel recorded bad input (csa2_check)      */
+  CSA2_ERR_TIMEOUT = 5,      /* a bounded device wait gave up (csa2_check)    */
+  CSA2_ERR_WORKSPACE = 6     /* workspace too small                           */
+} csa2_status;
+
+/* Layer modes: "Reading Notes ...", section 3f, C2 step 4 (mode table). */
+typedef enum csa2_mode {
+  CSA2_MODE_FULL = 0,    /* compress own entries, score, select, attend      */
+  CSA2_MODE_REINDEX = 1, /* borrowed pool and keys; own score + selection    */
+  CSA2_MODE_REUSE = 2    /* borrowed pool and selection; attend only         */
+} csa2_mode;
+
+typedef enum csa2_kv_format {
+  CSA2_KV_BF16 = 0,
+  CSA2_KV_FP8_E4M3_B32 = 1 /* e4m3 codes + one ue8m0 scale per 32 channels */
+} csa2_kv_format;
+
+/* Device error word bits (csa2_check / csa2_device_flags). */
+#define CSA2_FLAG_BAD_TOPK_INDEX   0x01u /* selected index outside [0, pool length) */
+#define CSA2_FLAG_BAD_WINDOW       0x02u /* window position outside its buffer      */
+#define CSA2_FLAG_BAD_SEGMENT      0x04u /* compress segment not whole groups, or
+                                            its entries fall outside the pool       */
+#define CSA2_FLAG_NVIS_TOO_LARGE   0x08u /* n_vis larger than the sequence's pool   */
+#define CSA2_FLAG_WAIT_TIMEOUT     0x10u /* a bounded mbarrier wait gave up         */
+#define CSA2_FLAG_BAD_QUERY        0x20u /* seq_of_q outside [0, n_seq)             */
+
+/* Geometry and numerics of one CSA2 layer ("DeepSeek-V4.1-Flash on WASTE",
+ * section "The shape"; PocketLLM page, geometry table). Supported values:
+ *   n_heads 64, head_dim 512, rope_dim 0 or 64 (the last rope_dim channels
+ *   are rotated, adjacent pairs), window 1..128, compress_ratio 1..16,
+ *   idx_heads 8/16/32, idx_dim 128, topk 1..2048 (multiple of 1),
+ *   kv_format / idx_key_format a csa2_kv_format.
+ * softmax_scale multiplies q.k (1/sqrt(512)); the sink is a logit on the
+ * same scale. RoPE frequencies follow YaRN (DeepSeek-V3 ramp): rope_theta,
+ * yarn_factor (<= 1 disables the ramp), yarn_orig_len, yarn_beta_fast/slow. */
+typedef struct csa2_config {
+  int32_t n_heads;
+  int32_t head_dim;
+  int32_t rope_dim;
+  int32_t window;
+  int32_t compress_ratio;
+  int32_t idx_heads;
+  int32_t idx_dim;
+  int32_t topk;
+  int32_t kv_format;
+  int32_t idx_key_format;
+  float softmax_scale;
+  float norm_eps;
+  double rope_theta;
+  double yarn_factor;
+  double yarn_orig_len;
+  double yarn_beta_fast;
+  double yarn_beta_slow;
+} csa2_config;
+
+typedef struct csa2_ctx csa2_ctx;
+
+/* Fills `cfg` (host) with the DeepSeek-V4.1-Flash compressed-layer defaults:
+ * 64 x 512, rope 64, window 128, ratio 4, 8 x 128 indexer, top-512, bf16,
+ * scale 1/sqrt(512), eps 1e-20, theta 160000, YaRN 16 over 65536, beta 32/1. */
+void csa2_default_config(csa2_config* cfg);
+
+/* Validates `cfg` (host), computes the RoPE frequencies in double precision
+ * and allocates the device status word on the current CUDA device. The
+ * context is bound to that device; use it from one host thread at a time. */
+csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out);
+void csa2_destroy(csa2_ctx* ctx);
+
+/* Message of the last failure on this context (never NULL). */
+const char* csa2_last_error(const csa2_ctx* ctx);
+const char* csa2_status_string(csa2_status s);
+/* Writes the ctx's RoPE frequencies (rope_dim/2 doubles) to `out` (host). */
+csa2_status csa2_rope_frequencies(const csa2_ctx* ctx, double* out, int32_t n);
+
+/* Synchronises `stream`, reads and clears the device error word; returns
+ * CSA2_ERR_DEVICE_FLAG / CSA2_ERR_TIMEOUT if a kernel recorded bad input. The
+ * word's bits are written to *flags_out (host, nullable). */
+csa2_status csa2_check(csa2_ctx* ctx, void* stream, uint32_t* flags_out);
+
+/* ------------------------------------------------------------------------
+ * csa2_store_rows: store fp32 rows in a KV storage format, optionally rotated.
+ * Used to append window rows ("DeepSeek-V4.1-Flash on WASTE", item 1: the
+ * window stores each position's KV already rotated) and to put index keys or
+ * pool rows into the fp8 format (PocketLLM page, "The CSA2 attention layers":
+ * the window is quantised to FP8 over 32 elements).
+ *   rows     [n_rows, dim] fp32
+ *   pos      [n_rows] int64, nullable: when given and rope_dim > 0 the last
+ *            rope_dim channels of row i are rotated by angle pos[i]*f_k first
+ *   format   csa2_kv_format; out [n_rows, dim] bf16 or e4m3 bytes,
+ *            out_scale [n_rows, dim/32] ue8m0 bytes (fp8 only, else NULL)
+ * dim must be a multiple of 32 and at most 1024. */
+csa2_status csa2_store_rows(csa2_ctx* ctx, void* stream, const float* rows, int64_t n_rows,
+                            int32_t dim, const int64_t* pos, int32_t format, void* out,
+                            uint8_t* out_scale);
+
+/* ------------------------------------------------------------------------
+ * csa2_compress: step 1 ("Reading Notes ...", 3f C2 step 1; WASTE item 1;
+ * PocketLLM "The CSA2 attention layers"). For every closed group of m =
+ * compress_ratio tokens: per-channel softmax of the gate logits over the
+ * group, weighted sum of the raw vectors (fp32), RMSNorm with norm_w; the
+ * index key RMSNorm_{k_norm_w}(c_hat . w_idx^T) from the unrotated c_hat;
+ * then RoPE of c_hat at the group's first token position j*m; store both.
+ *   raw        [n_tokens, 512] bf16 tokens, sequences packed by tok_off
+ *   gate       [n_tokens, 512] fp32 gate logits (ignored, may be NULL, at m=1)
+ *   tok_off    [n_seq+1] int64 token offsets; each segment a multiple of m
+ *   first_pos  [n_seq] int64 position of each segment's first token (a
+ *              multiple of m); group j of sequence b is written to pool row
+ *              pool_off[b] + j, j = position / m
+ *   pool_off   [n_seq+1] int64 pool row offsets
+ *   norm_w     [512] fp32; w_idx [idx_dim, 512] bf16 (NULL: no index keys);
+ *   k_norm_w   [idx_dim] fp32
+ *   pool_kv / pool_kv_scale   rows in kv_format (scale NULL for bf16)
+ *   idx_keys / idx_key_scale  rows in idx_key_format (both NULL if w_idx NULL)
+ * n_tokens (host) is the total token count; 0 enqueues nothing. */
+csa2_status csa2_compress(csa2_ctx* ctx, void* stream, const uint16_t* raw, const float* gate,
+                          int32_t n_seq, int64_t n_tokens, const int64_t* tok_off,
+                          const int64_t* first_pos, const int64_t* pool_off, const float* norm_w,
+                          const uint16_t* w_idx, const float* k_norm_w, void* pool_kv,
+                          uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale);
+
+/* ------------------------------------------------------------------------
+ * csa2_index_score: step 2 ("Reading Notes ...", 3f C2 step 2, the lightning
+ * indexer form). scores[q, j] = sum_h w_heads[q,h] * max(0, q_idx[q,h,:] .
+ * key_j) for j < n_vis[q], key_j = row pool_off[seq_of_q[q]] + j of idx_keys.
+ * Entries j >= n_vis[q] of the scores row are not written.
+ *   q_idx     [n_query, idx_heads, idx_dim] bf16
+ *   w_heads   [n_query, idx_heads] fp32
+ *   idx_keys  [pool rows, idx_dim] in idx_key_format; idx_key_scale its
+ *             [rows, idx_dim/32] scales (fp8 only)
+ *   pool_off  [n_seq+1] int64; seq_of_q [n_query] int32; n_vis [n_query] int32
+ *   max_vis   (host) an upper bound of every n_vis[q]
+ *   scores    [n_query, scores_ld] fp32, scores_ld >= max_vis
+ * Products are exact (bf16 x bf16, or e4m3 codes), sums in fp32. */
+csa2_status csa2_index_score(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
+                             const uint16_t* q_idx, const float* w_heads, const void* idx_keys,
+                             const uint8_t* idx_key_scale, const int64_t* pool_off,
+                             const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
+                             float* scores, int64_t scores_ld);
+
+/* ------------------------------------------------------------------------
+ * csa2_topk: step 2's selection S_t = TopK sigma_t ("Reading Notes ...", 3f
+ * C2 step 2; PocketLLM "The CSA2 attention layers", -1 padding). For each
+ * query: the min(k, n_vis[q]) largest of scores[q, 0:n_vis[q]], ties broken
+ * toward the lower index, -0.0 equal to +0.0; written in ascending index
+ * order to out_idx[q, 0:k], the rest -1. Scores must not be NaN.
+ *   scores  [n_query, scores_ld] fp32; n_vis [n_query] int32
+ *   k       1..2048; out_idx [n_query, k] int32
+ *   max_vis (host) upper bound of n_vis
+ *   workspace of csa2_topk_workspace_size(ctx, n_query, max_vis) bytes */
+size_t csa2_topk_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
+csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores,
+                      int64_t scores_ld, const int32_t* n_vis, int64_t max_vis, int32_t k,
+                      int32_t* out_idx, void* workspace, size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * csa2_attend: step 3 ("Reading Notes ...", section 3a attention formula and
+ * 3f C2 step 3; WASTE item 1: the sink in the denominator only and the
+ * de-rotation of the output's rope channels). For query q at t = q_pos[q] of
+ * sequence b = seq_of_q[q], per head h:
+ *   q~ = RoPE_t(q[q,h,:]);  rows R = window positions [max(lo_b, t-w+1), t]
+ *   (row win_off[b] + p % (win_off[b+1]-win_off[b]) of win_kv) followed by
+ *   the pool rows pool_off[b] + j for j in topk_idx[q, :], j != -1;
+ *   s_r = softmax_scale * q~ . row_r;  o = sum_r e^{s_r} row_r /
+ *   (sum_r e^{s_r} + e^{sink[h]});  out[q,h,:] = o with its rope channels
+ *   rotated by -t. The same row is key and value.
+ *   q        [n_query, 64, 512] bf16 (unrotated); q_pos [n_query] int64
+ *   win_kv   stored window rows in kv_format, win_scale their scales
+ *   win_off  [n_seq+1] int64 (capacity of sequence b's buffer = difference)
+ *   win_lo   [n_seq] int64 window cut positions (nullable: 0)
+ *   pool_kv  stored compressed rows in kv_format, pool_scale their scales
+ *   topk_idx [n_query, topk] int32 (-1 = none); NULL: window only
+ *   sink     [64] fp32; out [n_query, 64, 512] bf16; lse [n_query, 64] fp32
+ *            natural-log denominator (nullable)
+ * QK^T and PV run on tcgen05 tensor cores with bf16 operands (P rounded to
+ * bf16) and fp32 accumulation in tensor memory.
+ *   workspace of csa2_attend_workspace_size(ctx, n_query) bytes */
+size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query);
+csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
+                        const uint16_t* q, const int64_t* q_pos, const int32_t* seq_of_q,
+                        const void* win_kv, const uint8_t* win_scale, const int64_t* win_off,
+                        const int64_t* win_lo, const void* pool_kv, const uint8_t* pool_scale,
+                        const int64_t* pool_off, const int32_t* topk_idx, const float* sink,
+                        uint16_t* out, float* lse, void* workspace, size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * csa2_step: one layer step in one of the three modes ("Reading Notes ...",
+ * 3f C2 step 4): Full = compress (when n_tokens > 0) + index_score + topk +
+ * attend; Reindex = index_score + topk + attend on the borrowed pool and
+ * keys; Reuse = attend with the borrowed selection in topk_idx. Every mode
+ * uses its own q, window and sink. Field meanings are those of the
+ * single-step calls above. */
+typedef struct csa2_step_args {
+  int32_t mode;      /* csa2_mode */
+  int32_t n_seq;
+  int32_t n_query;
+  int64_t max_vis;   /* host bound of n_vis */
+  /* queries */
+  const uint16_t* q;
+  const int64_t* q_pos;
+  const int32_t* seq_of_q;
+  const int32_t* n_vis;
+  const uint16_t* q_idx;   /* Full / Reindex */
+  const float* w_heads;    /* Full / Reindex */
+  const float* sink;
+  /* window */
+  const void* win_kv;
+  const uint8_t* win_scale;
+  const int64_t* win_off;
+  const int64_t* win_lo;
+  /* compressed pool and index keys (written by Full's compress) */
+  void* pool_kv;
+  uint8_t* pool_scale;
+  void* idx_keys;
+  uint8_t* idx_key_scale;
+  const int64_t* pool_off;
+  /* compressor inputs (Full only) */
+  int64_t n_tokens;
+  const uint16_t* raw;
+  const float* gate;
+  const int64_t* tok_off;
+  const int64_t* first_pos;
+  const float* norm_w;
+  const uint16_t* w_idx;
+  const float* k_norm_w;
+  /* selection: written by Full / Reindex, read by Reuse */
+  int32_t* topk_idx;
+  /* outputs */
+  uint16_t* out;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+} csa2_step_args;
+
+size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
+csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* args);
+
+/* Number of kernel launches the last entry point call on this context
+ * enqueued (host). */
+int32_t csa2_last_launch_count(const csa2_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

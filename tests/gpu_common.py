@@ -1,0 +1,122 @@
+"""Helpers shared by the GPU parity tests: context setup, conversions of the
+device tensors to float64 for the oracle, and the tolerances.
+
+Tolerances (derivations are in the repository's design notes):
+  attention : max |gpu - oracle| <= 2e-2 and ||gpu - oracle|| / ||oracle|| <= 1e-2
+              per query (bf16 operands, P rounded to bf16, fp32 accumulation)
+  scores    : |gpu - oracle| <= 1e-3 |oracle| + 1e-5 * sum_h |w_h| ||q_h|| ||k||
+              (relative 1e-3, plus the fp32 accumulation bound of a 128-term dot)
+  top-k     : bit-exact on identical fp32 scores
+  stored rows (bf16): |gpu - oracle| <= 1 bf16 ulp of the oracle value + 1e-5 * row rms
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import csa2_oracle as O
+from oracle import formats as F
+
+ATT_MAX_ABS = 2e-2
+ATT_REL_L2 = 1e-2
+SCORE_REL = 1e-3
+SCORE_ABS_FRAC = 1e-5
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+_CTX_CACHE = {}
+
+
+def context(**overrides):
+    from compressed_sparse_attention_gb300 import binding, build
+    build.build()
+    key = tuple(sorted(overrides.items()))
+    if key not in _CTX_CACHE:
+        _CTX_CACHE[key] = binding.Context(**overrides)
+    return _CTX_CACHE[key]
+
+
+def geometry(cfg) -> O.Geometry:
+    return O.Geometry(n_heads=cfg.n_heads, head_dim=cfg.head_dim, rope_dim=cfg.rope_dim, window=cfg.window,
+                      compress_ratio=cfg.compress_ratio, idx_heads=cfg.idx_heads, idx_dim=cfg.idx_dim,
+                      topk=cfg.topk, softmax_scale=float(cfg.softmax_scale), norm_eps=float(cfg.norm_eps),
+                      rope_theta=cfg.rope_theta, yarn_factor=cfg.yarn_factor, yarn_orig_len=cfg.yarn_orig_len,
+                      yarn_beta_fast=cfg.yarn_beta_fast, yarn_beta_slow=cfg.yarn_beta_slow)
+
+
+def inv_freq(geom: O.Geometry) -> np.ndarray:
+    if geom.rope_dim == 0:
+        return np.zeros(0)
+    return O.yarn_inv_freq(geom.rope_dim, geom.rope_theta, geom.yarn_factor, geom.yarn_orig_len,
+                           geom.yarn_beta_fast, geom.yarn_beta_slow)
+
+
+def bf16_np(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 values of a bf16 tensor."""
+    u = t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    return F.bf16_bits_to_f64(u)
+
+
+def f32_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().double().numpy()
+
+
+def oracle_fp8_rows(x_f32: np.ndarray):
+    """The oracle's own fp8 block-32 quantisation of fp32 rows: (codes, exps, values)."""
+    codes, exps = F.fp8_block_quantize(x_f32)
+    return codes, exps, F.fp8_block_dequantize(codes, exps)
+
+
+def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    err = np.abs(got - ref)
+    mx = float(err.max()) if err.size else 0.0
+    den = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got - ref))
+    assert mx <= ATT_MAX_ABS and rel <= ATT_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
+
+
+def score_tolerance(ref: np.ndarray, q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray) -> np.ndarray:
+    bound = (np.abs(w) * np.linalg.norm(q_idx, axis=1)).sum() * np.linalg.norm(keys, axis=1)
+    return SCORE_REL * np.abs(ref) + SCORE_ABS_FRAC * bound
+
+
+def assert_rows_close_bf16(got: np.ndarray, ref: np.ndarray, what: str = ""):
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    tol = F.bf16_ulp(ref) + 1e-5 * rms
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, worst {float(np.abs(got - ref).max()):.3e}"
+
+
+def assert_rows_close_fp8(got: np.ndarray, ref: np.ndarray, scale: np.ndarray, what: str = ""):
+    """One e4m3 grid step: relative 2^-3 of the value plus the subnormal step 2^-9 * scale."""
+    tol = 2.0 ** -3 * np.abs(ref) + 2.0 ** -9 * np.repeat(scale, 32, axis=-1) + 1e-30
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off"
+
+
+def check_topk_valid(sel_gpu: np.ndarray, sel_ref: np.ndarray, scores_ref: np.ndarray, tol: np.ndarray):
+    """The GPU's selection differs from the oracle's only among scores within `tol` of the threshold."""
+    a = set(int(x) for x in sel_gpu if x >= 0)
+    b = set(int(x) for x in sel_ref if x >= 0)
+    assert len(a) == len(b)
+    if a == b:
+        return True
+    thr = min(scores_ref[list(b)]) if b else -np.inf
+    for j in a ^ b:
+        assert abs(scores_ref[j] - thr) <= 2 * tol[j] + 1e-30, f"entry {j} is not a near tie"
+    return False
+
+
+def rope_sanity(ctx):
+    """The library's RoPE frequencies against the oracle's own (both computed in double)."""
+    g = geometry(ctx.cfg)
+    ref = inv_freq(g)
+    got = np.array(ctx.rope_frequencies())
+    assert np.allclose(got, ref, rtol=1e-14, atol=0)

@@ -1,0 +1,328 @@
+"""GPU parity of each CSA2 kernel against the float64 oracle on identical seeded inputs.
+
+Sizes here are ones the oracle finishes in seconds while still spanning
+several tiles and ragged tails; full-size checks are in test_gpu_fullsize.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import (assert_attention_close, assert_rows_close_bf16, assert_rows_close_fp8, bf16_np,
+                        check_topk_valid, context, f32_np, geometry, inv_freq, oracle_fp8_rows, require_gpu,
+                        rope_sanity, score_tolerance)
+from oracle import csa2_oracle as O
+from oracle import formats as F
+from workloads import Workload, make_inputs, make_selection, make_topk_scores
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    require_gpu()
+
+
+# ----------------------------------------------------------------------------- storage / rope
+
+@pytest.mark.parametrize("dim", [512, 128])
+def test_store_rows_bf16_and_fp8_bit_exact_without_rope(dim):
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    g = torch.Generator(device=DEV).manual_seed(5)
+    x = torch.randn((333, dim), generator=g, device=DEV) * torch.exp(torch.randn((333, 1), generator=g, device=DEV) * 3)
+    x[7] = 0.0
+    x[9, :32] = 0.0
+    out = torch.empty((333, dim), dtype=torch.bfloat16, device=DEV)
+    ctx.store_rows(x, None, binding.KV_BF16, out)
+    ref = F.f64_to_bf16_bits(f32_np(x))
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+    codes = torch.empty((333, dim), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((333, dim // 32), dtype=torch.uint8, device=DEV)
+    ctx.store_rows(x, None, binding.KV_FP8, codes, sc)
+    rc, re_, _ = oracle_fp8_rows(f32_np(x))
+    assert np.array_equal(sc.cpu().numpy(), re_)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert ctx.check()[0] == 0
+
+
+def test_store_rows_rope_matches_oracle():
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    rope_sanity(ctx)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    x = torch.randn((200, 512), generator=g, device=DEV)
+    pos = torch.randint(0, 1 << 20, (200,), generator=g, device=DEV)
+    pos[0] = 0
+    pos[1] = (1 << 20) - 1
+    out = torch.empty((200, 512), dtype=torch.bfloat16, device=DEV)
+    ctx.store_rows(x, pos, binding.KV_BF16, out)
+    ref = O.rope_rotate(f32_np(x), pos.cpu().numpy(), f)
+    assert_rows_close_bf16(bf16_np(out), ref, "rope store bf16")
+    codes = torch.empty((200, 512), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((200, 16), dtype=torch.uint8, device=DEV)
+    ctx.store_rows(x, pos, binding.KV_FP8, codes, sc)
+    got = F.fp8_block_dequantize(codes.cpu().numpy(), sc.cpu().numpy())
+    assert_rows_close_fp8(got, ref, F.ue8m0_to_f64(sc.cpu().numpy()), "rope store fp8")
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _attend_case(wl, ctx, fp8=False, win_lo=None, sel_seed=11, layer=0):
+    """Run csa2_attend on workload wl with a random valid selection; return (gpu out, lse, oracle refs)."""
+    from compressed_sparse_attention_gb300 import binding
+    inp = make_inputs(wl, DEV, layer=layer, with_compress=False)
+    if layer > 0:
+        base = make_inputs(wl, DEV, layer=0, with_compress=False)
+        for k in ("pool_off", "pool_kv", "pool_kv_f32", "n_vis"):
+            if k in base:
+                inp[k] = base[k]
+    sel = make_selection(wl, inp["n_vis"], sel_seed, DEV)
+    B, Q = wl.n_seq, wl.n_query
+    if fp8:
+        win = torch.empty(inp["win_kv_f32"].shape, dtype=torch.uint8, device=DEV)
+        win_sc = torch.empty((win.shape[0], 16), dtype=torch.uint8, device=DEV)
+        ctx.store_rows(inp["win_kv_f32"], None, binding.KV_FP8, win, win_sc)
+        pool = torch.empty(inp["pool_kv_f32"].shape, dtype=torch.uint8, device=DEV)
+        pool_sc = torch.empty((pool.shape[0], 16), dtype=torch.uint8, device=DEV)
+        ctx.store_rows(inp["pool_kv_f32"], None, binding.KV_FP8, pool, pool_sc)
+    else:
+        win, win_sc, pool, pool_sc = inp["win_kv"], None, inp["pool_kv"], None
+    lo_t = None if win_lo is None else torch.tensor(win_lo, dtype=torch.int64, device=DEV)
+    out = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((Q, 64), dtype=torch.float32, device=DEV)
+    ws = binding.workspace(ctx.attend_workspace_size(Q), DEV)
+    ctx.attend(B, inp["q"], inp["q_pos"], inp["seq_of_q"], win, win_sc, inp["win_off"], lo_t, pool, pool_sc,
+               inp["pool_off"], sel, inp["sink"], out, lse, ws)
+    flags, _ = ctx.check()
+    assert flags == 0
+    # oracle on the same inputs
+    if fp8:
+        win_np = oracle_fp8_rows(f32_np(inp["win_kv_f32"]))[2]
+        pool_np = oracle_fp8_rows(f32_np(inp["pool_kv_f32"]))[2]
+    else:
+        win_np, pool_np = bf16_np(win), bf16_np(pool)
+    return dict(inp=inp, sel=sel.cpu().numpy(), out=bf16_np(out), lse=f32_np(lse), win_np=win_np, pool_np=pool_np,
+                win_lo=win_lo)
+
+
+def _oracle_attend(case, geom, f, qi):
+    inp = case["inp"]
+    b = int(inp["seq_of_q"][qi])
+    t = int(inp["q_pos"][qi])
+    woff = inp["win_off"].cpu().numpy()
+    poff = inp["pool_off"].cpu().numpy()
+    cap = woff[b + 1] - woff[b]
+    lo = 0 if case["win_lo"] is None else max(0, case["win_lo"][b])
+    rows = O.gather_rows(t, geom, lambda p: case["win_np"][woff[b] + (p % cap)], case["pool_np"][poff[b]:poff[b + 1]],
+                         case["sel"][qi], lo)
+    q = bf16_np(inp["q"][qi])
+    return O.attend(q, t, rows, f32_np(inp["sink"]), geom.softmax_scale, f)
+
+
+def test_attend_softmax_worked_example():
+    """q = 1, k = (0, ln 3), v = (10, 20) gives 17.5 (the reading notes' worked example)."""
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context(rope_dim=0, softmax_scale=1.0)
+    win = torch.zeros((128, 512), dtype=torch.float32, device=DEV)
+    t = 200
+    win[(t - 1) % 128, 1] = 10.0
+    win[t % 128, 0] = math.log(3.0)
+    win[t % 128, 1] = 20.0
+    # every other window position holds a row whose key is very negative
+    other = [p for p in range(t - 127, t - 1)]
+    for p in other:
+        win[p % 128, 0] = -1000.0
+    win_bf = torch.empty((128, 512), dtype=torch.bfloat16, device=DEV)
+    ctx.store_rows(win, None, binding.KV_BF16, win_bf)
+    q = torch.zeros((1, 64, 512), dtype=torch.bfloat16, device=DEV)
+    q[0, :, 0] = 1.0
+    out = torch.empty((1, 64, 512), dtype=torch.bfloat16, device=DEV)
+    sink = torch.full((64,), -math.inf, device=DEV)
+    ctx.attend(1, q, torch.tensor([t], device=DEV), torch.zeros(1, dtype=torch.int32, device=DEV), win_bf, None,
+               torch.tensor([0, 128], device=DEV), None, None, None, None, None, sink, out, None, None)
+    assert ctx.check()[0] == 0
+    o = bf16_np(out)
+    # ln 3 is stored as bf16 (1.1015625) and the output is rounded to bf16 (step 0.125 near 17.5)
+    assert np.all(np.abs(o[:, 1] - 17.5) <= 0.07)
+    assert np.all(np.abs(o[:, 2:]) == 0)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_attend_decode_ragged(fp8):
+    ctx = context(kv_format=1 if fp8 else 0)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    wl = Workload("attend_ragged", 4, (300, 4100, 40, 2051), 4, seed=21, kv_fp8=fp8, outlier_frac=0.02)
+    lo = [0, 4000, 0, 1990]
+    case = _attend_case(wl, ctx, fp8=fp8, win_lo=lo)
+    for qi in range(wl.n_query):
+        ref, lse = _oracle_attend(case, geom, f, qi)
+        assert_attention_close(case["out"][qi], ref, f"query {qi}")
+        assert np.allclose(case["lse"][qi], lse, atol=2e-2)
+
+
+def test_attend_many_queries_single_split_rescale():
+    """Prefill-shaped: 200 causal queries on one sequence with a linear window
+    buffer -> one CTA per query runs all five tiles with the running max."""
+    ctx = context(compress_ratio=2)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    wl = Workload("attend_prefill", 1, (2300,), 2, seed=22, n_query_per_seq=200, win_linear=True,
+                  outlier_frac=0.05, outlier_scale=16.0)
+    case = _attend_case(wl, ctx)
+    for qi in (0, 1, 57, 123, 199):
+        ref, _ = _oracle_attend(case, geom, f, qi)
+        assert_attention_close(case["out"][qi], ref, f"query {qi}")
+
+
+def test_attend_reports_bad_index_and_skips_row():
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    wl = Workload("attend_bad", 1, (4096,), 4, seed=23)
+    inp = make_inputs(wl, DEV, with_compress=False)
+    sel = make_selection(wl, inp["n_vis"], 1, DEV)
+    sel[0, 3] = 1024  # == pool length: out of range
+    out = torch.empty((1, 64, 512), dtype=torch.bfloat16, device=DEV)
+    ws = binding.workspace(ctx.attend_workspace_size(1), DEV)
+    ctx.attend(1, inp["q"], inp["q_pos"], inp["seq_of_q"], inp["win_kv"], None, inp["win_off"], None,
+               inp["pool_kv"], None, inp["pool_off"], sel, inp["sink"], out, None, ws)
+    flags, st = ctx.check()
+    assert flags & binding.FLAG_BAD_TOPK_INDEX and st == 4
+    assert torch.isfinite(out.float()).all()
+
+
+# ----------------------------------------------------------------------------- indexer
+
+@pytest.mark.parametrize("idx_heads", [8, 16, 32])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_index_score(idx_heads, fp8):
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context(idx_heads=idx_heads, idx_key_format=1 if fp8 else 0)
+    wl = Workload("idx", 3, (4000, 148, 10404), 4, seed=31 + idx_heads, idx_heads=idx_heads, idx_fp8=fp8,
+                  n_query_per_seq=2)
+    inp = make_inputs(wl, DEV, with_compress=False)
+    Q = wl.n_query
+    nv = inp["n_vis"].clone()
+    nv[1] = 7      # ragged, shorter than the pool
+    nv[2] = 0      # nothing visible
+    max_vis = int(nv.max())
+    if fp8:
+        keys = torch.empty(inp["idx_keys_f32"].shape, dtype=torch.uint8, device=DEV)
+        ksc = torch.empty((keys.shape[0], 4), dtype=torch.uint8, device=DEV)
+        ctx.store_rows(inp["idx_keys_f32"], None, binding.KV_FP8, keys, ksc)
+        keys_np = oracle_fp8_rows(f32_np(inp["idx_keys_f32"]))[2]
+    else:
+        keys, ksc = inp["idx_keys"], None
+        keys_np = bf16_np(keys)
+    ld = max_vis + 5
+    scores = torch.full((Q, ld), float("nan"), device=DEV)
+    ctx.index_score(wl.n_seq, inp["q_idx"], inp["w_heads"], keys, ksc, inp["pool_off"], inp["seq_of_q"], nv,
+                    max_vis, scores)
+    assert ctx.check()[0] == 0
+    s = f32_np(scores)
+    poff = inp["pool_off"].cpu().numpy()
+    for qi in range(Q):
+        b = int(inp["seq_of_q"][qi])
+        n = int(nv[qi])
+        qv = bf16_np(inp["q_idx"][qi])
+        w = f32_np(inp["w_heads"][qi])
+        kk = keys_np[poff[b]:poff[b] + n]
+        ref = O.index_scores(qv, w, kk)
+        tol = score_tolerance(ref, qv, w, kk)
+        assert np.all(np.abs(s[qi, :n] - ref) <= tol), f"query {qi}"
+        assert np.all(np.isnan(s[qi, n:])), "entries past n_vis must stay untouched"
+
+
+# ----------------------------------------------------------------------------- top-k
+
+@pytest.mark.parametrize("n,tie_levels,k", [(3000, 0, 512), (3000, 3, 512), (20000, 2, 512), (5000, 0, 2048),
+                                            (777, 0, 1), (262144, 0, 512), (262144, 40, 512), (100, 0, 512)])
+def test_topk_bit_exact(n, tie_levels, k):
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    Q = 4
+    sc = make_topk_scores(Q, n, seed=n + tie_levels + k, tie_levels=tie_levels)
+    nv = torch.tensor([n, max(0, n - 1), min(n, k - 1 if k > 1 else 1), 0], dtype=torch.int32)
+    scores = sc.to(DEV)
+    out = torch.empty((Q, k), dtype=torch.int32, device=DEV)
+    ws = binding.workspace(ctx.topk_workspace_size(Q, n), DEV)
+    ctx.topk(scores, nv.to(DEV), n, k, out, ws)
+    assert ctx.check()[0] == 0
+    got = out.cpu().numpy()
+    s = sc.numpy()
+    for qi in range(Q):
+        ref = O.topk_select(s[qi, :int(nv[qi])], k)
+        assert np.array_equal(got[qi], ref), f"query {qi}"
+
+
+# ----------------------------------------------------------------------------- compressor
+
+@pytest.mark.parametrize("m", [1, 2, 4])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_compress(m, fp8):
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context(compress_ratio=m, kv_format=1 if fp8 else 0, idx_key_format=1 if fp8 else 0)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    g = torch.Generator(device=DEV).manual_seed(40 + m)
+    seg_groups = [3, 1, 5]
+    first_group = [0, 17, 1000]
+    T = sum(seg_groups) * m
+    raw = torch.randn((T, 512), generator=g, device=DEV).to(torch.bfloat16)
+    gate = torch.randn((T, 512), generator=g, device=DEV) * 2
+    norm_w = 0.5 + torch.rand(512, generator=g, device=DEV)
+    w_idx = (torch.randn((128, 512), generator=g, device=DEV) / math.sqrt(512)).to(torch.bfloat16)
+    k_norm_w = 0.5 + torch.rand(128, generator=g, device=DEV)
+    tok_off = torch.tensor(np.concatenate([[0], np.cumsum(seg_groups) * m]), dtype=torch.int64, device=DEV)
+    first_pos = torch.tensor([x * m for x in first_group], dtype=torch.int64, device=DEV)
+    plen = [first_group[i] + seg_groups[i] + 2 for i in range(3)]
+    pool_off = torch.tensor(np.concatenate([[0], np.cumsum(plen)]), dtype=torch.int64, device=DEV)
+    P = int(pool_off[-1])
+    if fp8:
+        pool = torch.zeros((P, 512), dtype=torch.uint8, device=DEV)
+        psc = torch.zeros((P, 16), dtype=torch.uint8, device=DEV)
+        keys = torch.zeros((P, 128), dtype=torch.uint8, device=DEV)
+        ksc = torch.zeros((P, 4), dtype=torch.uint8, device=DEV)
+    else:
+        pool = torch.zeros((P, 512), dtype=torch.bfloat16, device=DEV)
+        keys = torch.zeros((P, 128), dtype=torch.bfloat16, device=DEV)
+        psc = ksc = None
+    ctx.compress(raw, gate if m > 1 else None, 3, tok_off, first_pos, pool_off, norm_w, w_idx, k_norm_w,
+                 pool, psc, keys, ksc)
+    assert ctx.check()[0] == 0
+    raw_np, gate_np = bf16_np(raw), f32_np(gate)
+    for b in range(3):
+        t0, t1 = int(tok_off[b]), int(tok_off[b + 1])
+        kv, c_hat, kidx = O.compress(raw_np[t0:t1], gate_np[t0:t1], m, int(first_pos[b]), f32_np(norm_w),
+                                     geom.norm_eps, f, bf16_np(w_idx), f32_np(k_norm_w))
+        r0 = int(pool_off[b]) + first_group[b]
+        rows = slice(r0, r0 + seg_groups[b])
+        if fp8:
+            got_kv = F.fp8_block_dequantize(pool[rows].cpu().numpy(), psc[rows].cpu().numpy())
+            assert_rows_close_fp8(got_kv, kv, F.ue8m0_to_f64(psc[rows].cpu().numpy()), f"kv seq {b}")
+            got_k = F.fp8_block_dequantize(keys[rows].cpu().numpy(), ksc[rows].cpu().numpy())
+            assert_rows_close_fp8(got_k, kidx, F.ue8m0_to_f64(ksc[rows].cpu().numpy()), f"key seq {b}")
+        else:
+            assert_rows_close_bf16(bf16_np(pool[rows]), kv, f"kv seq {b}")
+            assert_rows_close_bf16(bf16_np(keys[rows]), kidx, f"key seq {b}")
+        # rows outside the written groups stay untouched
+        assert float(pool[int(pool_off[b]) + first_group[b] + seg_groups[b]].float().abs().sum()) == 0.0
+
+
+def test_compress_rejects_misaligned_segment():
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context(compress_ratio=4)
+    raw = torch.zeros((8, 512), dtype=torch.bfloat16, device=DEV)
+    gate = torch.zeros((8, 512), device=DEV)
+    pool = torch.zeros((10, 512), dtype=torch.bfloat16, device=DEV)
+    ctx.compress(raw, gate, 1, torch.tensor([0, 8], device=DEV), torch.tensor([2], device=DEV),
+                 torch.tensor([0, 10], device=DEV), torch.ones(512, device=DEV), None, None, pool, None, None, None)
+    flags, st = ctx.check()
+    assert flags & binding.FLAG_BAD_SEGMENT and st == 4
+    assert float(pool.float().abs().sum()) == 0.0
