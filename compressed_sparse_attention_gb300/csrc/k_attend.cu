@@ -24,8 +24,8 @@ namespace csa2 {
 
 constexpr int kTileRows = 128;
 constexpr int kAttThreads = 128;
-constexpr uint32_t SM_Q = 0;                          // [8 dim blocks][64 heads][128 B]
-constexpr uint32_t SM_KV = 65536;                     // [8 dim blocks][128 rows][128 B]
+constexpr uint32_t SM_Q = 0;                          // [9 dim blocks][64 heads][128 B]; block 8 = rope residual
+constexpr uint32_t SM_KV = 73728;                     // [8 dim blocks][128 rows][128 B]
 constexpr uint32_t SM_P = SM_KV + 131072;             // [128 rows][128 B]  (64 heads, bf16)
 constexpr uint32_t SM_RED = SM_P + 16384;             // float [4][64]
 constexpr uint32_t SM_MRUN = SM_RED + 1024;           // float [64]
@@ -118,23 +118,25 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       for (int cc = 0; cc < 2; ++cc) {
         const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
         uint4 v = *reinterpret_cast<const uint4*>(qh + 8 * c);
-        if (8 * c + 8 > first_rope && p.rp.pairs > 0) {
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+        if (8 * c >= first_rope && p.rp.pairs > 0) {
+          // rotated q = hi + lo, both bf16: the tensor cores see the rotation
+          // to ~2^-16 relative instead of one bf16 rounding
+          uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int ch = 8 * c + 2 * k;
-            if (ch >= first_rope) {
-              float cs, sn;
-              rope_cs(p.rp, (ch - first_rope) >> 1, t, cs, sn);
-              const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
-              w[k] = pack_bf16(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-            }
+            float cs, sn;
+            rope_cs(p.rp, (ch - first_rope) >> 1, t, cs, sn);
+            const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
+            const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+            w[k] = pack_bf16(y0, y1);
+            lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
           }
           v = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        const uint32_t off = SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
-                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm + off) = v;
+        *reinterpret_cast<uint4*>(sm + SM_Q + (uint32_t)(c >> 3) * 8192u + inblk) = v;
       }
     }
   }
@@ -151,7 +153,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t win_cap = q_ok ? (p.win_off[b + 1] - p.win_off[b]) : 0;
   const int64_t lo_b = (q_ok && p.win_lo) ? max((int64_t)0, p.win_lo[b]) : 0;
   const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
-  const int64_t plen = q_ok ? (p.pool_off[b + 1] - p.pool_off[b]) : 0;
+  // no selection (window-only call): the pool arguments may be NULL
+  const int64_t plen = (q_ok && p.pool_off != nullptr) ? (p.pool_off[b + 1] - p.pool_off[b]) : 0;
 
   for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row)
@@ -226,10 +229,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     // ---- S^T = KV . Q^T
     if (tid == 0) {
       tc_fence_after();
+      // K steps 0..31 cover the 8 channel blocks; 32..35 add the rope residual
+      // block of q against the KV's last channel block (the rope channels)
+      const int n_ks = p.rp.pairs > 0 ? 36 : 32;
 #pragma unroll 4
-      for (int ks = 0; ks < 32; ++ks) {
+      for (int ks = 0; ks < n_ks; ++ks) {
         const uint32_t koff = (uint32_t)(ks & 3) * 32u;
-        const uint64_t ad = sdesc_sw128(base_s + SM_KV + (uint32_t)(ks >> 2) * 16384u + koff, 16u, 1024u);
+        const uint32_t kblk = ks < 32 ? (uint32_t)(ks >> 2) : 7u;
+        const uint64_t ad = sdesc_sw128(base_s + SM_KV + kblk * 16384u + koff, 16u, 1024u);
         const uint64_t bd = sdesc_sw128(base_s + SM_Q + (uint32_t)(ks >> 2) * 8192u + koff, 16u, 1024u);
         mma_bf16_ss(tmem_s, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
       }

@@ -270,6 +270,30 @@ def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
 # a4. Two-source attention with sink (R, 3a and C2 step 3; W item 1)
 # ----------------------------------------------------------------------------
 
+def attention_weights(q: np.ndarray, t: int, rows: np.ndarray, sink: np.ndarray, scale: float,
+                      inv_freq: np.ndarray):
+    """Softmax weights p[h, r] = e^{s_r} / (sum_r' e^{s_r'} + e^{sink_h}) and the log-denominator.
+
+    q [H, D] (unrotated), rows [R, D], sink [H]; s_r = scale * RoPE_t(q_h) . row_r.
+    A head whose logits and sink are all -inf gets zero weights and lse -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.float64).reshape(-1, q.shape[1])
+    sink = np.asarray(sink, dtype=np.float64)
+    qr = rope_rotate(q, t, inv_freq)
+    s = scale * (qr @ rows.T)  # [H, R]
+    mx = np.max(np.concatenate([s, sink[:, None]], axis=1), axis=1)  # [H]
+    p = np.zeros_like(s)
+    lse = np.full(q.shape[0], -np.inf)
+    finite = np.isfinite(mx)
+    if finite.any():
+        e = np.exp(s[finite] - mx[finite, None])
+        den = e.sum(axis=1) + np.exp(sink[finite] - mx[finite])
+        p[finite] = e / den[:, None]
+        lse[finite] = mx[finite] + np.log(den)
+    return p, lse
+
+
 def attend(q: np.ndarray, t: int, rows: np.ndarray, sink: np.ndarray, scale: float,
            inv_freq: np.ndarray):
     """One query over the concatenated rows (window rows then selected entries).
@@ -281,21 +305,9 @@ def attend(q: np.ndarray, t: int, rows: np.ndarray, sink: np.ndarray, scale: flo
       out_h = RoPE_{-t} applied to the rope dims of o_h.
     Returns (out [H, D] float64, lse [H] = log(sum_r e^{s_r} + e^{sink_h})).
     """
-    q = np.asarray(q, dtype=np.float64)
-    rows = np.asarray(rows, dtype=np.float64).reshape(-1, q.shape[1])
-    sink = np.asarray(sink, dtype=np.float64)
-    qr = rope_rotate(q, t, inv_freq)
-    s = scale * (qr @ rows.T)  # [H, R]
-    mx = np.max(np.concatenate([s, sink[:, None]], axis=1), axis=1)  # [H]
-    out = np.zeros_like(q)
-    lse = np.full(q.shape[0], -np.inf)
-    finite = np.isfinite(mx)
-    if finite.any():
-        e = np.exp(s[finite] - mx[finite, None])
-        den = e.sum(axis=1) + np.exp(sink[finite] - mx[finite])
-        out[finite] = (e @ rows) / den[:, None]
-        lse[finite] = mx[finite] + np.log(den)
-    out = rope_rotate(out, t, inv_freq, inverse=True)
+    rows = np.asarray(rows, dtype=np.float64).reshape(-1, np.asarray(q).shape[1])
+    p, lse = attention_weights(q, t, rows, sink, scale, inv_freq)
+    out = rope_rotate(p @ rows, t, inv_freq, inverse=True)
     return out, lse
 
 

@@ -2,8 +2,9 @@
 device tensors to float64 for the oracle, and the tolerances.
 
 Tolerances (derivations are in the repository's design notes):
-  attention : max |gpu - oracle| <= 2e-2 and ||gpu - oracle|| / ||oracle|| <= 1e-2
-              per query (bf16 operands, P rounded to bf16, fp32 accumulation)
+  attention : |gpu - oracle| <= 2e-2 + 1e-2 sum_r p_r |v_r| per element and
+              ||gpu - oracle|| / ||oracle|| <= 1e-2 per query (bf16 operands,
+              P rounded to bf16, fp32 accumulation)
   scores    : |gpu - oracle| <= 1e-3 |oracle| + 1e-5 * sum_h |w_h| ||q_h|| ||k||
               (relative 1e-3, plus the fp32 accumulation bound of a 128-term dot)
   top-k     : bit-exact on identical fp32 scores
@@ -22,6 +23,7 @@ from oracle import formats as F
 
 ATT_MAX_ABS = 2e-2
 ATT_REL_L2 = 1e-2
+ATT_REL_ELEM = 1e-2
 SCORE_REL = 1e-3
 SCORE_ABS_FRAC = 1e-5
 
@@ -74,12 +76,38 @@ def oracle_fp8_rows(x_f32: np.ndarray):
     return codes, exps, F.fp8_block_dequantize(codes, exps)
 
 
-def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
+def attention_bound(q, t, rows, sink, scale, f) -> np.ndarray:
+    """sum_r p_r |v_r| per head and channel (the scale of the terms each output
+    element sums, before cancellation); the two channels of a rope pair share
+    the sum of their bounds since the de-rotation mixes them."""
+    p, _ = O.attention_weights(q, t, rows, sink, scale, f)
+    bnd = p @ np.abs(np.asarray(rows, dtype=np.float64))
+    r = 2 * f.shape[0]
+    if r:
+        d = bnd.shape[-1]
+        pair = bnd[:, d - r::2] + bnd[:, d - r + 1::2]
+        bnd[:, d - r::2] = pair
+        bnd[:, d - r + 1::2] = pair
+    return bnd
+
+
+def assert_attention_close(got: np.ndarray, ref: np.ndarray, bound: np.ndarray, what: str = ""):
+    """Per element |gpu - oracle| <= 2e-2 + 1e-2 * sum_r p_r |v_r|, and rel-L2 <= 1e-2.
+
+    The flat 2e-2 is the stated bar for unit-scale outputs. The second term is
+    what bf16 arithmetic costs on a weighted sum whose terms are large and
+    cancel (outlier rows reach |v| ~ 50 while |o| is a few units): P is rounded
+    to bf16 (2^-9 of each weight), the output to bf16 (2^-9 of |o|), and the
+    fp32-accumulated scores move each weight by a few 1e-4.
+    """
     err = np.abs(got - ref)
-    mx = float(err.max()) if err.size else 0.0
+    lim = ATT_MAX_ABS + ATT_REL_ELEM * bound
+    worst = int(np.argmax(err - lim)) if err.size else 0
     den = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got - ref))
-    assert mx <= ATT_MAX_ABS and rel <= ATT_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rel:.3e}"
+    ok = bool(np.all(err <= lim)) and rel <= ATT_REL_L2
+    assert ok, (f"{what}: worst |err| {float(err.flat[worst]):.3e} at |ref| {float(np.abs(ref).flat[worst]):.3e} "
+                f"bound {float(bound.flat[worst]):.3e}, max-abs {float(err.max()):.3e}, rel-L2 {rel:.3e}")
 
 
 def score_tolerance(ref: np.ndarray, q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray) -> np.ndarray:

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import (assert_attention_close, assert_rows_close_bf16, assert_rows_close_fp8, bf16_np,
+from gpu_common import (assert_attention_close, attention_bound, assert_rows_close_bf16, assert_rows_close_fp8, bf16_np,
                         check_topk_valid, context, f32_np, geometry, inv_freq, oracle_fp8_rows, require_gpu,
                         rope_sanity, score_tolerance)
 from oracle import csa2_oracle as O
@@ -122,7 +122,8 @@ def _oracle_attend(case, geom, f, qi):
     rows = O.gather_rows(t, geom, lambda p: case["win_np"][woff[b] + (p % cap)], case["pool_np"][poff[b]:poff[b + 1]],
                          case["sel"][qi], lo)
     q = bf16_np(inp["q"][qi])
-    return O.attend(q, t, rows, f32_np(inp["sink"]), geom.softmax_scale, f)
+    out, lse = O.attend(q, t, rows, f32_np(inp["sink"]), geom.softmax_scale, f)
+    return out, lse, attention_bound(q, t, rows, f32_np(inp["sink"]), geom.softmax_scale, f)
 
 
 def test_attend_softmax_worked_example():
@@ -147,9 +148,10 @@ def test_attend_softmax_worked_example():
     ctx.attend(1, q, torch.tensor([t], device=DEV), torch.zeros(1, dtype=torch.int32, device=DEV), win_bf, None,
                torch.tensor([0, 128], device=DEV), None, None, None, None, None, sink, out, None, None)
     assert ctx.check()[0] == 0
-    o = bf16_np(out)
+    o = bf16_np(out)[0]  # [64 heads, 512 channels]
     # ln 3 is stored as bf16 (1.1015625) and the output is rounded to bf16 (step 0.125 near 17.5)
     assert np.all(np.abs(o[:, 1] - 17.5) <= 0.07)
+    assert np.all(np.abs(o[:, 0] - 0.75 * math.log(3.0)) <= 0.01)
     assert np.all(np.abs(o[:, 2:]) == 0)
 
 
@@ -162,8 +164,8 @@ def test_attend_decode_ragged(fp8):
     lo = [0, 4000, 0, 1990]
     case = _attend_case(wl, ctx, fp8=fp8, win_lo=lo)
     for qi in range(wl.n_query):
-        ref, lse = _oracle_attend(case, geom, f, qi)
-        assert_attention_close(case["out"][qi], ref, f"query {qi}")
+        ref, lse, bnd = _oracle_attend(case, geom, f, qi)
+        assert_attention_close(case["out"][qi], ref, bnd, f"query {qi}")
         assert np.allclose(case["lse"][qi], lse, atol=2e-2)
 
 
@@ -177,8 +179,8 @@ def test_attend_many_queries_single_split_rescale():
                   outlier_frac=0.05, outlier_scale=16.0)
     case = _attend_case(wl, ctx)
     for qi in (0, 1, 57, 123, 199):
-        ref, _ = _oracle_attend(case, geom, f, qi)
-        assert_attention_close(case["out"][qi], ref, f"query {qi}")
+        ref, _, bnd = _oracle_attend(case, geom, f, qi)
+        assert_attention_close(case["out"][qi], ref, bnd, f"query {qi}")
 
 
 def test_attend_reports_bad_index_and_skips_row():
