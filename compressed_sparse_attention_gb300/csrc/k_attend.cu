@@ -34,7 +34,8 @@ constexpr uint32_t SM_MUSE = SM_LRUN + 256;           // float [64]
 constexpr uint32_t SM_ALPHA = SM_MUSE + 256;          // float [64]
 constexpr uint32_t SM_ROWS = SM_ALPHA + 256;          // int64 [128]
 constexpr uint32_t SM_MISC = SM_ROWS + 1024;          // mbarrier, tmem slot, flags
-constexpr uint32_t SM_TOTAL = SM_MISC + 64;
+constexpr uint32_t SM_ROPE = SM_MISC + 64;            // float2 [32]: cos, sin of t * f_i
+constexpr uint32_t SM_TOTAL = SM_ROPE + 256;
 constexpr uint32_t kAttSmemBytes = SM_TOTAL + 1024;   // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0, 0);
@@ -109,37 +110,29 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     m_run[tid] = -INFINITY;
     l_run[tid] = 0.f;
   }
-  // ---- Q: rotate the rope channels at t, round to bf16, store swizzled (K-major B operand)
+  float2* rope_tab = reinterpret_cast<float2*>(sm + SM_ROPE);
+  if (tid < p.rp.pairs) {
+    float c = 1.f, sn = 0.f;
+    if (q_ok) rope_cs(p.rp, tid, t, c, sn);
+    rope_tab[tid] = make_float2(c, sn);
+  }
+  __syncthreads();
+  // ---- Q: copied asynchronously into its swizzled K-major slots (it lands
+  // together with the first tile's rows); the rope channels are rotated in
+  // place once both have arrived
   if (tile_begin < tile_end) {
-    const int first_rope = kDim - 2 * p.rp.pairs;
     for (int h = warp; h < kHeads; h += 4) {
       const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
-        uint4 v = *reinterpret_cast<const uint4*>(qh + 8 * c);
-        const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
-        if (8 * c >= first_rope && p.rp.pairs > 0) {
-          // rotated q = hi + lo, both bf16: the tensor cores see the rotation
-          // to ~2^-16 relative instead of one bf16 rounding
-          uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int ch = 8 * c + 2 * k;
-            float cs, sn;
-            rope_cs(p.rp, (ch - first_rope) >> 1, t, cs, sn);
-            const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
-            const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
-            w[k] = pack_bf16(y0, y1);
-            lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
-          }
-          v = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        *reinterpret_cast<uint4*>(sm + SM_Q + (uint32_t)(c >> 3) * 8192u + inblk) = v;
+        const uint32_t dst = base_s + SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
+                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+        cp_async16(dst, qh + 8 * c, 16u);
       }
     }
   }
+  bool q_pending = true;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -221,6 +214,36 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
           const uint32_t off = SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
                                ((uint32_t)((c & 7) ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(sm + off) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+        }
+      }
+    }
+    cp_async_wait_all();
+    if (q_pending) {
+      q_pending = false;
+      if (p.rp.pairs > 0) {
+        __syncthreads();
+        // rotated q = hi + lo, both bf16: the tensor cores see the rotation to
+        // ~2^-16 relative instead of one bf16 rounding. Thread: head tid/2,
+        // chunks 56 + 4*(tid&1) .. +3 (the last 64 channels).
+        const int h = tid >> 1;
+        const int first_rope = kDim - 2 * p.rp.pairs;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = 56 + 4 * (tid & 1) + u;
+          const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+          uint4* hi_p = reinterpret_cast<uint4*>(sm + SM_Q + 7u * 8192u + inblk);
+          const uint4 v = *hi_p;
+          uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 cs2 = rope_tab[(8 * c + 2 * k - first_rope) >> 1];
+            const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
+            const float y0 = x0 * cs2.x - x1 * cs2.y, y1 = x0 * cs2.y + x1 * cs2.x;
+            w[k] = pack_bf16(y0, y1);
+            lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
+          }
+          *hi_p = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
@@ -381,7 +404,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       const int d = 128 * mt + 32 * warp + lane;
       float cs = 1.f, sn = 0.f;
       const bool rope = p.rp.pairs > 0 && d >= first_rope;
-      if (rope) rope_cs(p.rp, (d - first_rope) >> 1, t, cs, sn);
+      if (rope) {
+        const float2 cs2 = rope_tab[(d - first_rope) >> 1];
+        cs = cs2.x;
+        sn = cs2.y;
+      }
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
         if (have_o) {
@@ -429,58 +456,75 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   if (warp == 0) tmem_dealloc(taddr, kTmemCols);
 }
 
-// merge of split-K partials: one CTA per query, thread i owns channel pair (2i, 2i+1)
+// merge of split-K partials: one CTA per (query, group of 4 heads); thread
+// (head hl = tid/64, chunk = tid%64) owns channels 8*chunk .. 8*chunk+7. All
+// splits' loads are issued before any is used.
+constexpr int kMergeHeadsPerCta = 4;
 __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p) {
-  __shared__ float wsplit[8][kHeads];
-  __shared__ float lse_s[kHeads];
-  const int qi = blockIdx.x, tid = threadIdx.x;
+  __shared__ float wsplit[8][kMergeHeadsPerCta];
+  __shared__ float2 rope_tab[kMaxPairs];
+  const int qi = blockIdx.x / (kHeads / kMergeHeadsPerCta);
+  const int hg = blockIdx.x % (kHeads / kMergeHeadsPerCta);
+  const int tid = threadIdx.x, hl = tid >> 6, chunk = tid & 63;
+  const int h = hg * kMergeHeadsPerCta + hl;
   const int ns = p.n_split;
   const float2* ml = p.ws_ml + (int64_t)qi * ns * kHeads;
-  if (tid < kHeads) {
-    const float sk = p.sink[tid] * 1.4426950408889634f;
+  const int64_t t = p.q_pos[qi];
+  if (tid < kMergeHeadsPerCta) {
+    const int hh = hg * kMergeHeadsPerCta + tid;
+    const float sk = p.sink[hh] * 1.4426950408889634f;
     float M = sk;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * kHeads + tid].x);
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * kHeads + hh].x);
     float den = 0.f;
     if (M != -INFINITY) {
       den = exp2f(sk - M);
       for (int s = 0; s < ns; ++s) {
-        const float2 v = ml[s * kHeads + tid];
+        const float2 v = ml[s * kHeads + hh];
         if (v.x != -INFINITY) den += v.y * exp2f(v.x - M);
       }
     }
     for (int s = 0; s < ns; ++s) {
-      const float2 v = ml[s * kHeads + tid];
+      const float2 v = ml[s * kHeads + hh];
       wsplit[s][tid] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - M) / den;
     }
-    lse_s[tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * 0.6931471805599453f;
-    if (p.lse) p.lse[(int64_t)qi * kHeads + tid] = lse_s[tid];
+    if (p.lse) p.lse[(int64_t)qi * kHeads + hh] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * 0.6931471805599453f;
+  }
+  if (tid >= 32 && tid - 32 < p.rp.pairs) {
+    float c, sn;
+    rope_cs(p.rp, tid - 32, t, c, sn);
+    rope_tab[tid - 32] = make_float2(c, sn);
   }
   __syncthreads();
-  const int d0 = 2 * tid;
-  const int64_t t = p.q_pos[qi];
-  const int first_rope = kDim - 2 * p.rp.pairs;
-  float cs = 1.f, sn = 0.f;
-  const bool rope = p.rp.pairs > 0 && d0 >= first_rope;
-  if (rope) rope_cs(p.rp, (d0 - first_rope) >> 1, t, cs, sn);
-  uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
-  for (int h = 0; h < kHeads; ++h) {
-    float x0 = 0.f, x1 = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = wsplit[s][h];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float* base = p.ws_o + ((int64_t)qi * ns * kHeads + h) * kDim + 8 * chunk;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (s < ns) {
+      const float w = wsplit[s][hl];
       if (w != 0.f) {
-        const float2 o = *reinterpret_cast<const float2*>(p.ws_o + (((int64_t)qi * ns + s) * kHeads + h) * kDim + d0);
-        x0 = fmaf(w, o.x, x0);
-        x1 = fmaf(w, o.y, x1);
+        const float4* src = reinterpret_cast<const float4*>(base + (int64_t)s * kHeads * kDim);
+        const float4 a = src[0], b = src[1];
+        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+        acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+        acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
       }
     }
-    if (rope) {
-      const float y0 = x0 * cs + x1 * sn;
-      const float y1 = x1 * cs - x0 * sn;
-      x0 = y0;
-      x1 = y1;
-    }
-    *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + d0) = pack_bf16(x0, x1);
   }
+  const int first_rope = kDim - 2 * p.rp.pairs;
+  if (p.rp.pairs > 0 && 8 * chunk >= first_rope) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 cs = rope_tab[(8 * chunk + 2 * k - first_rope) >> 1];
+      const float x0 = acc[2 * k], x1 = acc[2 * k + 1];
+      acc[2 * k] = x0 * cs.x + x1 * cs.y;       // rotation by -t
+      acc[2 * k + 1] = x1 * cs.x - x0 * cs.y;
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(p.out + ((int64_t)qi * kHeads + h) * kDim + 8 * chunk) = o;
 }
 
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
@@ -521,7 +565,7 @@ cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams
   else attend_kernel<false><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
   *n_launch += 1;
   if (p.n_split > 1) {
-    attend_merge_kernel<<<p.n_query, 256, 0, st>>>(p);
+    attend_merge_kernel<<<p.n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(p);
     *n_launch += 1;
   }
   return cudaGetLastError();

@@ -72,11 +72,32 @@ __global__ void __launch_bounds__(256) store_rows_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------
-// compress: one CTA of 128 threads per closed group; thread t owns channels
-// 4t..4t+3 of the 512-wide latent.
+// compress: one CTA of 256 threads per closed group; thread t owns channels
+// 2t, 2t+1 of the 512-wide latent. The kernel is latency-bound (a few KB per
+// group), so every independent load is issued as early as possible: the
+// index-key weights (warp w owns outputs 16w .. 16w+15, 32 x 16 B per lane)
+// at kernel start, the segment lookup as a warp-parallel search.
 // ---------------------------------------------------------------------------
+constexpr int kCmpThreads = 256;
+
+// largest b in [0, n) with off[b] <= x (off non-decreasing, off[0] = 0); warp-wide
+__device__ __forceinline__ int find_segment_warp(const int64_t* __restrict__ off, int n, int64_t x) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int stride = (hi - lo + 31) / 32;
+    const int i = lo + lane * stride;
+    const bool le = i < hi && off[i] <= x;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, le));  // >= 1: off[lo] <= x
+    const int nlo = lo + (cnt - 1) * stride;
+    hi = min(hi, nlo + stride);
+    lo = nlo;
+  }
+  return lo;
+}
+
 template <bool KV_FP8, bool IDX_FP8>
-__global__ void __launch_bounds__(128) compress_kernel(
+__global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
     const int64_t* __restrict__ tok_off, const int64_t* __restrict__ first_pos,
     const int64_t* __restrict__ pool_off, const float* __restrict__ norm_w,
@@ -85,135 +106,145 @@ __global__ void __launch_bounds__(128) compress_kernel(
     void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags) {
   __shared__ float c_hat_s[kDim];
   __shared__ float k_lin_s[kIdxDim];
-  __shared__ float red_s[4];
+  __shared__ float red_s[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t tok0 = (int64_t)blockIdx.x * m;
-  const int b = find_segment(tok_off, n_seq + 1, tok0);
-  const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
-  if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || b >= n_seq || tok0 >= seg1) {
-    if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
-    return;
+  // ---- index-key weights first: nothing they depend on
+  uint4 wa[16], wb[16];
+  if (w_idx != nullptr) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
+      wa[u] = wr[0];
+      wb[u] = wr[1];
+    }
   }
+  const int c0 = 2 * tid;
+  const float2 nw = *reinterpret_cast<const float2*>(norm_w + c0);
+  const float knw = (w_idx != nullptr && warp < idx_dim / 32) ? k_norm_w[warp * 32 + lane] : 0.f;
+  const int64_t tok0 = (int64_t)blockIdx.x * m;
+  // the group's tokens depend only on the group index: load them before the
+  // segment lookup (m <= 16)
+  uint32_t rw[16];
+  float2 gv[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    if (u < m) {
+      rw[u] = *reinterpret_cast<const uint32_t*>(raw + (tok0 + u) * kDim + c0);
+      gv[u] = m > 1 ? *reinterpret_cast<const float2*>(gate + (tok0 + u) * kDim + c0) : make_float2(0.f, 0.f);
+    }
+  }
+  const int b = find_segment_warp(tok_off, n_seq, tok0);
+  const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
+  const int64_t pbase = pool_off[b], pend = pool_off[b + 1];
   const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
   const int64_t j = pos0 / m;
-  const int64_t prow = pool_off[b] + j;
-  if (prow >= pool_off[b + 1]) {
+  const int64_t prow = pbase + j;
+  if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || tok0 >= seg1 || prow >= pend) {
     if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
     return;
   }
-  const int c0 = 4 * tid;
   // ---- pooling (fp32): per channel softmax of the gate logits over the group
-  float pooled[4];
+  float pooled[2];
   if (m == 1) {
-    const uint2 w = *reinterpret_cast<const uint2*>(raw + tok0 * kDim + c0);
-    pooled[0] = bf16lo(w.x); pooled[1] = bf16hi(w.x); pooled[2] = bf16lo(w.y); pooled[3] = bf16hi(w.y);
+    pooled[0] = bf16lo(rw[0]);
+    pooled[1] = bf16hi(rw[0]);
   } else {
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    for (int u = 0; u < m; ++u) {
-      const float4 gv = *reinterpret_cast<const float4*>(gate + (tok0 + u) * kDim + c0);
-      mx[0] = fmaxf(mx[0], gv.x); mx[1] = fmaxf(mx[1], gv.y);
-      mx[2] = fmaxf(mx[2], gv.z); mx[3] = fmaxf(mx[3], gv.w);
-    }
-    float den[4] = {0.f, 0.f, 0.f, 0.f}, num[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int u = 0; u < m; ++u) {
-      const float4 gv = *reinterpret_cast<const float4*>(gate + (tok0 + u) * kDim + c0);
-      const uint2 w = *reinterpret_cast<const uint2*>(raw + (tok0 + u) * kDim + c0);
-      const float e0 = expf(gv.x - mx[0]), e1 = expf(gv.y - mx[1]);
-      const float e2 = expf(gv.z - mx[2]), e3 = expf(gv.w - mx[3]);
-      den[0] += e0; den[1] += e1; den[2] += e2; den[3] += e3;
-      num[0] = fmaf(e0, bf16lo(w.x), num[0]); num[1] = fmaf(e1, bf16hi(w.x), num[1]);
-      num[2] = fmaf(e2, bf16lo(w.y), num[2]); num[3] = fmaf(e3, bf16hi(w.y), num[3]);
-    }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) pooled[k] = num[k] / den[k];
+    for (int u = 0; u < 16; ++u) {
+      if (u < m) {
+        mx0 = fmaxf(mx0, gv[u].x);
+        mx1 = fmaxf(mx1, gv[u].y);
+      }
+    }
+    float d0 = 0.f, d1 = 0.f, n0 = 0.f, n1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (u < m) {
+        const float e0 = expf(gv[u].x - mx0), e1 = expf(gv[u].y - mx1);
+        d0 += e0;
+        d1 += e1;
+        n0 = fmaf(e0, bf16lo(rw[u]), n0);
+        n1 = fmaf(e1, bf16hi(rw[u]), n1);
+      }
+    }
+    pooled[0] = n0 / d0;
+    pooled[1] = n1 / d1;
   }
   // ---- RMSNorm with norm_w
-  float ss = pooled[0] * pooled[0] + pooled[1] * pooled[1] + pooled[2] * pooled[2] + pooled[3] * pooled[3];
+  float ss = pooled[0] * pooled[0] + pooled[1] * pooled[1];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red_s[warp] = ss;
   __syncthreads();
-  const float tot = red_s[0] + red_s[1] + red_s[2] + red_s[3];
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red_s[w];
   const float inv = 1.0f / sqrtf(tot / (float)kDim + eps);
-  const float4 nw = *reinterpret_cast<const float4*>(norm_w + c0);
-  float ch[4] = {pooled[0] * inv * nw.x, pooled[1] * inv * nw.y, pooled[2] * inv * nw.z, pooled[3] * inv * nw.w};
+  float ch[2] = {pooled[0] * inv * nw.x, pooled[1] * inv * nw.y};
   // ---- index key from the unrotated latent
   if (w_idx != nullptr) {
-    *reinterpret_cast<float4*>(&c_hat_s[c0]) = make_float4(ch[0], ch[1], ch[2], ch[3]);
+    *reinterpret_cast<float2*>(&c_hat_s[c0]) = make_float2(ch[0], ch[1]);
     __syncthreads();
     float cv[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) cv[k] = c_hat_s[16 * lane + k];
-    const int per_warp = idx_dim / 4;
-    for (int oo = 0; oo < per_warp; ++oo) {
-      const int o = warp * per_warp + oo;
-      const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)o * kDim + 16 * lane);
-      const uint4 wa = wr[0], wb = wr[1];
-      float acc = 0.f;
-      acc = fmaf(cv[0], bf16lo(wa.x), acc); acc = fmaf(cv[1], bf16hi(wa.x), acc);
-      acc = fmaf(cv[2], bf16lo(wa.y), acc); acc = fmaf(cv[3], bf16hi(wa.y), acc);
-      acc = fmaf(cv[4], bf16lo(wa.z), acc); acc = fmaf(cv[5], bf16hi(wa.z), acc);
-      acc = fmaf(cv[6], bf16lo(wa.w), acc); acc = fmaf(cv[7], bf16hi(wa.w), acc);
-      acc = fmaf(cv[8], bf16lo(wb.x), acc); acc = fmaf(cv[9], bf16hi(wb.x), acc);
-      acc = fmaf(cv[10], bf16lo(wb.y), acc); acc = fmaf(cv[11], bf16hi(wb.y), acc);
-      acc = fmaf(cv[12], bf16lo(wb.z), acc); acc = fmaf(cv[13], bf16hi(wb.z), acc);
-      acc = fmaf(cv[14], bf16lo(wb.w), acc); acc = fmaf(cv[15], bf16hi(wb.w), acc);
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-      if (lane == 0) k_lin_s[o] = acc;
+    for (int u = 0; u < 16; ++u) {
+      float acc = 0.f;
+      acc = fmaf(cv[0], bf16lo(wa[u].x), acc); acc = fmaf(cv[1], bf16hi(wa[u].x), acc);
+      acc = fmaf(cv[2], bf16lo(wa[u].y), acc); acc = fmaf(cv[3], bf16hi(wa[u].y), acc);
+      acc = fmaf(cv[4], bf16lo(wa[u].z), acc); acc = fmaf(cv[5], bf16hi(wa[u].z), acc);
+      acc = fmaf(cv[6], bf16lo(wa[u].w), acc); acc = fmaf(cv[7], bf16hi(wa[u].w), acc);
+      acc = fmaf(cv[8], bf16lo(wb[u].x), acc); acc = fmaf(cv[9], bf16hi(wb[u].x), acc);
+      acc = fmaf(cv[10], bf16lo(wb[u].y), acc); acc = fmaf(cv[11], bf16hi(wb[u].y), acc);
+      acc = fmaf(cv[12], bf16lo(wb[u].z), acc); acc = fmaf(cv[13], bf16hi(wb[u].z), acc);
+      acc = fmaf(cv[14], bf16lo(wb[u].w), acc); acc = fmaf(cv[15], bf16hi(wb[u].w), acc);
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+      if (lane == 0) k_lin_s[warp * 16 + u] = acc;
     }
     __syncthreads();
-    // RMSNorm of the key; warp w owns outputs [32w, 32w+32) (one fp8 block)
-    float kss = 0.f;
-    for (int o = lane; o < idx_dim; o += 32) kss += k_lin_s[o] * k_lin_s[o];
+    // RMSNorm of the key; warps 0..3 own outputs [32w, 32w+32) (one fp8 block each)
+    if (warp < idx_dim / 32) {
+      float kss = 0.f;
+      for (int o = lane; o < idx_dim; o += 32) kss += k_lin_s[o] * k_lin_s[o];
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) kss += __shfl_xor_sync(0xffffffffu, kss, s);
-    const float kinv = 1.0f / sqrtf(kss / (float)idx_dim + eps);
-    for (int base = warp * 32; base < idx_dim; base += 128) {
-      const int o = base + lane;
-      const float kv = k_lin_s[o] * kinv * k_norm_w[o];
+      for (int sh = 16; sh > 0; sh >>= 1) kss += __shfl_xor_sync(0xffffffffu, kss, sh);
+      const float kinv = 1.0f / sqrtf(kss / (float)idx_dim + eps);
+      const int o = warp * 32 + lane;
+      const float kv = k_lin_s[o] * kinv * knw;
       if constexpr (!IDX_FP8) {
-        reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] =
-            (uint16_t)(pack_bf16(kv, 0.f) & 0xFFFFu);
+        reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] = (uint16_t)(pack_bf16(kv, 0.f) & 0xFFFFu);
       } else {
         float amax = fabsf(kv);
 #pragma unroll
-        for (int s = 16; s > 0; s >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
         const uint32_t eb = fp8_scale_byte(amax);
         reinterpret_cast<uint8_t*>(idx_keys)[prow * idx_dim + o] = f32_to_e4m3(ldexpf(kv, 127 - (int)eb));
-        if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + base / 32] = (uint8_t)eb;
+        if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + warp] = (uint8_t)eb;
       }
     }
   }
   // ---- RoPE at the group's first token position, then store
-  if (rp.pairs > 0) {
-    const int first = kDim - 2 * rp.pairs;
-#pragma unroll
-    for (int k = 0; k < 4; k += 2) {
-      const int c = c0 + k;
-      if (c >= first) {
-        float cs, sn;
-        rope_cs(rp, (c - first) >> 1, pos0, cs, sn);
-        const float x0 = ch[k], x1 = ch[k + 1];
-        ch[k] = x0 * cs - x1 * sn;
-        ch[k + 1] = x0 * sn + x1 * cs;
-      }
-    }
+  if (rp.pairs > 0 && c0 >= kDim - 2 * rp.pairs) {
+    float cs, sn;
+    rope_cs(rp, (c0 - (kDim - 2 * rp.pairs)) >> 1, pos0, cs, sn);
+    const float x0 = ch[0], x1 = ch[1];
+    ch[0] = x0 * cs - x1 * sn;
+    ch[1] = x0 * sn + x1 * cs;
   }
   if constexpr (!KV_FP8) {
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(pool_kv) + prow * kDim + c0) =
-        make_uint2(pack_bf16(ch[0], ch[1]), pack_bf16(ch[2], ch[3]));
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(pool_kv) + prow * kDim + c0) = pack_bf16(ch[0], ch[1]);
   } else {
-    float amax = fmaxf(fmaxf(fabsf(ch[0]), fabsf(ch[1])), fmaxf(fabsf(ch[2]), fabsf(ch[3])));
+    float amax = fmaxf(fabsf(ch[0]), fabsf(ch[1]));
 #pragma unroll
-    for (int s = 1; s < 8; s <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, s));
+    for (int sh = 1; sh < 16; sh <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
     const uint32_t eb = fp8_scale_byte(amax);
     const int sh = 127 - (int)eb;
-    uint32_t word = 0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) word |= (uint32_t)f32_to_e4m3(ldexpf(ch[u], sh)) << (8 * u);
-    *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(pool_kv) + prow * kDim + c0) = word;
-    if ((tid & 7) == 0) pool_kv_scale[prow * (kDim / 32) + tid / 8] = (uint8_t)eb;
+    const uint32_t word = (uint32_t)f32_to_e4m3(ldexpf(ch[0], sh)) | ((uint32_t)f32_to_e4m3(ldexpf(ch[1], sh)) << 8);
+    *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pool_kv) + prow * kDim + c0) = (uint16_t)word;
+    if ((tid & 15) == 0) pool_kv_scale[prow * (kDim / 32) + tid / 16] = (uint8_t)eb;
   }
 }
 
@@ -244,7 +275,7 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   if (n_groups == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_groups);
 #define CSA2_COMPRESS(KF, IF)                                                                      \
-  compress_kernel<KF, IF><<<grid, 128, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
+  compress_kernel<KF, IF><<<grid, kCmpThreads, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
                                                 norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
                                                 pool_kv_scale, idx_keys, idx_key_scale, flags)
   if (kv_fp8) {

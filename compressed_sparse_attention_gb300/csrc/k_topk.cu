@@ -13,6 +13,13 @@
 //              candidates' unique 64-bit composite key<<32 | ~index (larger
 //              composite = larger score, then lower index), keeps the
 //              composites at or above the threshold, and sorts their indices.
+// For rows up to 16 x 16,384 scores the three steps run in ONE launch: a
+// thread-block cluster per query, each CTA holding a 16,384-score slice in
+// shared memory, the histograms summed across the cluster through distributed
+// shared memory and the candidates gathered by the cluster's first CTA. Longer
+// rows take the three-kernel path through global memory.
+#include <cooperative_groups.h>
+
 #include "launchers.cuh"
 
 namespace csa2 {
@@ -130,9 +137,15 @@ __device__ unsigned long long radix_select64(Src src, uint32_t n, uint32_t need,
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist_s[i] = 0;
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-      const unsigned long long v = src(i);
-      if ((v & mask) == prefix) atomicAdd(&hist_s[(v >> shift) & 0xFF], 1u);
+    // warp-aggregated: near the threshold most candidates share the high
+    // digits, so one atomic per distinct digit per warp instead of one each
+    const uint32_t n_pad = (n + 31u) & ~31u;
+    for (uint32_t i = threadIdx.x; i < n_pad; i += blockDim.x) {
+      const unsigned long long v = i < n ? src(i) : 0ull;
+      const bool ok = i < n && (v & mask) == prefix;
+      const uint32_t dig = ok ? (uint32_t)((v >> shift) & 0xFF) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, dig);
+      if (ok && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist_s[dig], (uint32_t)__popc(peers));
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -231,6 +244,281 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const int32_t* __rest
   for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = (uint32_t)i < ns ? (int32_t)sel[i] : -1;
 }
 
+namespace cg = cooperative_groups;
+
+// ---------------------------------------------------------------------------
+// Single-launch top-k for rows of up to 16 x 16,384 scores: a thread-block
+// cluster per query, CTA r holding scores [r*S, (r+1)*S) of the row in shared
+// memory as order-preserving keys (element li of the slice sits in thread
+// li % 1024, round li / 1024, so a warp's ballot in round u is bit-word
+// u*32 + warp of the slice's bitmap, and word w holds elements 32w..32w+31).
+//   1. four 8-bit digit levels (MSD radix select): each level histograms the
+//      keys that match the digits chosen so far, one warp sums the 256 bins
+//      across the cluster through distributed shared memory and picks the
+//      digit holding the k-th largest key; after four levels the exact key T
+//      and the number of keys equal to T to take are known in every CTA;
+//   2. keys equal to T are taken lowest index first: a CTA takes as many as
+//      remain after the ties of the CTAs before it (CTAs are in index order);
+//   3. every CTA writes its chosen indices in ascending order at its offset
+//      (the chosen counts of the CTAs before it) from its bitmap.
+// No candidate list, no sort, and no CTA works for the others.
+// ---------------------------------------------------------------------------
+constexpr int kTkThreads = 1024;
+constexpr int kTkMaxCluster = 16;
+
+template <int PER>
+struct TkLayout {
+  static constexpr int kSlice = kTkThreads * PER;
+  static constexpr int kWords = kSlice / 32;
+  static constexpr uint32_t KEYS = 0;
+  static constexpr uint32_t HIST = KEYS + kSlice * 4;   // [4 levels][256]
+  static constexpr uint32_t TOT = HIST + 4 * 256 * 4;   // [256] cluster-summed bins, top digit first
+  static constexpr uint32_t BM = TOT + 256 * 4;         // chosen bitmap
+  static constexpr uint32_t TB = BM + kWords * 4;       // tie bitmap
+  static constexpr uint32_t TP = TB + kWords * 4;       // ties before each word
+  static constexpr uint32_t MISC = TP + kWords * 4;
+  static constexpr uint32_t SMEM = MISC + 1024;
+};
+
+// inclusive block-wide scan of one value per thread (1024 threads); warp_s[31] = total
+__device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  __syncthreads();
+  if (lane == 31) warp_s[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_s[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += x;
+    }
+    warp_s[lane] = w;
+  }
+  __syncthreads();
+  return v + (warp > 0 ? warp_s[warp - 1] : 0u);
+}
+
+// u32 at `local` in every CTA r < C of the cluster; all loads issued at once
+__device__ __forceinline__ void cluster_gather_u32(cg::cluster_group& cluster, const uint32_t* local, uint32_t C,
+                                                   uint32_t (&v)[kTkMaxCluster]) {
+#pragma unroll
+  for (int r = 0; r < kTkMaxCluster; ++r)
+    v[r] = (uint32_t)r < C ? *cluster.map_shared_rank(local, (unsigned)r) : 0u;
+}
+
+// Pick the digit holding the need-th largest key of a level: threads 0..255
+// sum their bin over the cluster (one round of remote loads), warp 0 scans
+// the 256 sums from the top digit down. Leaves (digit, count above) in res.
+__device__ __forceinline__ void cluster_pick_digit(cg::cluster_group& cluster, uint32_t C, const uint32_t* h,
+                                                   uint32_t* tot, uint32_t need, uint32_t* res) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 256) {
+    uint32_t v[kTkMaxCluster];
+    cluster_gather_u32(cluster, h + (255 - tid), C, v);
+    uint32_t c = 0;
+#pragma unroll
+    for (int r = 0; r < kTkMaxCluster; ++r) c += v[r];
+    tot[tid] = c;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    uint32_t loc[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      loc[j] = tot[8 * lane + j];
+      sum += loc[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < need && need <= incl) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + loc[j] >= need) {
+          res[0] = (uint32_t)(255 - (8 * lane + j));
+          res[1] = run;
+          break;
+        }
+        run += loc[j];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <int PER>
+__global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
+                                                                    const int32_t* __restrict__ n_vis,
+                                                                    int64_t max_vis, int k,
+                                                                    int32_t* __restrict__ out_idx) {
+  using L = TkLayout<PER>;
+  extern __shared__ __align__(16) unsigned char tk_smem[];
+  uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem + L::KEYS);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(tk_smem + L::HIST);
+  uint32_t* tot = reinterpret_cast<uint32_t*>(tk_smem + L::TOT);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(tk_smem + L::BM);
+  uint32_t* tb = reinterpret_cast<uint32_t*>(tk_smem + L::TB);
+  uint32_t* tp = reinterpret_cast<uint32_t*>(tk_smem + L::TP);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(tk_smem + L::MISC);
+  // misc: [0..31] warp scan, [32..33] picked digit / count above, [34] keys > T here, [35] ties here
+  uint32_t* warp_s = misc;
+  uint32_t* res = misc + 32;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const uint32_t rank = cluster.block_rank();
+  const uint32_t C = cluster.num_blocks();
+  const int q = blockIdx.x / C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nv = (int)min((int64_t)max(n_vis[q], 0), max_vis);
+  const int64_t base = (int64_t)rank * L::kSlice;
+  const int cnt = (int)max((int64_t)0, min((int64_t)L::kSlice, (int64_t)nv - base));
+  const uint32_t need = (uint32_t)min(k, nv);
+  const bool all = (uint32_t)nv <= need;  // every visible entry is chosen (uniform over the cluster)
+
+  if (tid < 4 * 256) hist[tid] = 0;
+  if (tid < 4) misc[32 + tid] = 0;
+  // ---- slice -> keys
+  {
+    const float* row = scores + (int64_t)q * ld + base;
+    float v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int li = u * kTkThreads + tid;
+      v[u] = li < cnt ? row[li] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int li = u * kTkThreads + tid;
+      keys[li] = li < cnt ? score_key(v[u]) : 0u;
+    }
+  }
+  __syncthreads();
+  uint32_t T = 0, take_t = 0;  // keys > T are chosen; of keys == T, the first take_t (by index)
+  if (!all) {
+    // ---- four 8-bit digit levels; warp-aggregated adds only on the first
+    // (almost every score shares its top byte), plain adds below it
+    uint32_t prefix = 0, rem = need;
+#pragma unroll 1
+    for (int lvl = 0; lvl < 4; ++lvl) {
+      const int shift = 24 - 8 * lvl;
+      uint32_t* h = hist + 256 * lvl;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int li = u * kTkThreads + tid;
+        const uint32_t key = keys[li];
+        const bool ok = li < cnt && (lvl == 0 || (key >> (shift + 8)) == prefix);
+        const uint32_t d = (key >> shift) & 0xFFu;
+        if (lvl == 0) {
+          const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+          const uint32_t same = __ballot_sync(0xffffffffu, ok && d == d0);
+          if (lane == 0 && same) atomicAdd(&h[d0], (uint32_t)__popc(same));
+          if (ok && d != d0) atomicAdd(&h[d], 1u);
+        } else if (ok) {
+          atomicAdd(&h[d], 1u);
+        }
+      }
+      cluster.sync();
+      cluster_pick_digit(cluster, C, h, tot, rem, res);
+      prefix = (prefix << 8) | res[0];
+      rem -= res[1];
+      __syncthreads();
+    }
+    T = prefix;
+    take_t = rem;
+  }
+  // ---- counts above T and ties here, exchanged once across the cluster
+  uint32_t quota = 0, off = 0;
+  if (!all) {
+    uint32_t ngt = 0, nt = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int li = u * kTkThreads + tid;
+      const uint32_t key = keys[li];
+      const uint32_t bt = __ballot_sync(0xffffffffu, li < cnt && key == T);
+      const uint32_t bg = __ballot_sync(0xffffffffu, li < cnt && key > T);
+      if (lane == 0) tb[u * 32 + warp] = bt;
+      nt += __popc(bt);
+      ngt += __popc(bg);
+    }
+    if (lane == 0) {
+      atomicAdd(&misc[34], ngt);
+      atomicAdd(&misc[35], nt);
+    }
+    cluster.sync();
+    uint32_t g[kTkMaxCluster], t[kTkMaxCluster];
+    cluster_gather_u32(cluster, misc + 34, C, g);
+    cluster_gather_u32(cluster, misc + 35, C, t);
+    uint32_t ties_before = 0;
+#pragma unroll
+    for (int r = 0; r < kTkMaxCluster; ++r) {
+      if ((uint32_t)r < rank) {
+        const uint32_t qr = take_t > ties_before ? min(t[r], take_t - ties_before) : 0u;
+        off += g[r] + qr;
+        ties_before += t[r];
+      }
+    }
+    quota = take_t > ties_before ? take_t - ties_before : 0u;  // ties this CTA may take, lowest index first
+    if (quota > 0) {
+      const uint32_t tw = tid < L::kWords ? tb[tid] : 0u;  // thread tid owns word tid
+      const uint32_t pre = block_scan_incl(__popc(tw), warp_s) - __popc(tw);
+      if (tid < L::kWords) tp[tid] = pre;
+      __syncthreads();
+    }
+  } else {
+    off = (uint32_t)base;  // every earlier CTA is full and fully chosen
+  }
+  // ---- chosen bitmap: keys > T, plus the first `quota` ties in index order
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int li = u * kTkThreads + tid;
+    const int w = u * 32 + warp;
+    const uint32_t key = keys[li];
+    bool chosen = li < cnt && (all || key > T);
+    if (!all && li < cnt && key == T && quota > 0)
+      chosen = tp[w] + __popc(tb[w] & ((1u << lane) - 1u)) < quota;
+    const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
+    if (lane == 0) bm[w] = bal;
+  }
+  __syncthreads();
+  // ---- write chosen indices ascending at this CTA's offset; word w covers
+  // slice elements 32w .. 32w+31 and thread tid owns word tid
+  {
+    const uint32_t wbits = tid < L::kWords ? bm[tid] : 0u;
+    const uint32_t pre = block_scan_incl(__popc(wbits), warp_s) - __popc(wbits);
+    int32_t* o = out_idx + (int64_t)q * k;
+    if (tid < L::kWords) {
+      const int64_t li0 = base + 32 * (int64_t)tid;
+      uint32_t bits = wbits, pos = off + pre;
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        if (pos < (uint32_t)k) o[pos] = (int32_t)(li0 + bit);
+        ++pos;
+      }
+    }
+    if (rank == 0)
+      for (int i = (int)need + tid; i < k; i += kTkThreads) o[i] = -1;
+  }
+  // keep every CTA's shared memory alive until all remote reads are done
+  if (!all) cluster.sync();
+}
+
+static int topk_cluster_size(int64_t max_vis, int slice) {
+  const int64_t c = (max_vis + slice - 1) / slice;
+  return (int)(c < 1 ? 1 : c);
+}
+
 size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return al((size_t)n_query * kHistBins * 4) + al((size_t)n_query * 4) +
@@ -240,6 +528,39 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch) {
   if (n_query == 0) return cudaSuccess;
+  // one CTA per 16,384 scores (a 64K-context decode row is one CTA; 1M rows take 16)
+  const bool small = false;
+  const int slice = TkLayout<16>::kSlice;
+  const int csize = topk_cluster_size(max_vis, slice);
+  if (csize <= kTkMaxCluster) {
+    const void* fn = small ? (const void*)topk_cluster_kernel<4> : (const void*)topk_cluster_kernel<16>;
+    const uint32_t smem = small ? TkLayout<4>::SMEM : TkLayout<16>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && csize > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(n_query * csize));
+    cfg.blockDim = dim3(kTkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int max_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
+    if (e == cudaSuccess && max_clusters > 0) {
+      if (small) e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<4>, scores, ld, n_vis, max_vis, k, out_idx);
+      else e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<16>, scores, ld, n_vis, max_vis, k, out_idx);
+      if (e != cudaSuccess) return e;
+      *n_launch += 1;
+      return cudaGetLastError();
+    }
+    cudaGetLastError();  // cluster shape not schedulable here: use the global-memory path
+  }
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* p = reinterpret_cast<char*>(ws);
   uint32_t* hist = reinterpret_cast<uint32_t*>(p);
