@@ -90,6 +90,9 @@ SIGNATURES = {
     "csa2_step_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int64]),
     "csa2_step": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(StepArgs)]),
     "csa2_last_launch_count": (C.c_int32, [C.c_void_p]),
+    "csa2_attend_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
 }
 
 

@@ -5,19 +5,8 @@
 #include <cstring>
 #include <string>
 
+#include "ctx.cuh"
 #include "launchers.cuh"
-
-
-
-struct csa2_ctx {
-  csa2_config cfg;
-  int device = 0;
-  int num_sms = 0;
-  csa2::RopeParams rope;
-  uint32_t* d_flags = nullptr;
-  std::string err;
-  int last_launches = 0;
-};
 
 namespace {
 

@@ -33,7 +33,9 @@
  *     a device error word; csa2_check() synchronises and reports it.
  *   - The library allocates device memory only inside csa2_create (one
  *     status word). Scratch space is the caller's `workspace`, whose size the
- *     *_workspace_size functions give; it must be 256-byte aligned.
+ *     *_workspace_size functions give; it must be 256-byte aligned. The one
+ *     exception is csa2_attend_noalloc, whose scratch is a fixed device array
+ *     owned by the library (see its comment).
  *   - Strings returned by the library are owned by it.
  */
 #ifndef CSA2_H_
@@ -286,6 +288,33 @@ typedef struct csa2_step_args {
 
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* args);
+
+/* ------------------------------------------------------------------------
+ * csa2_attend_noalloc: csa2_attend for callers that cannot allocate device
+ * memory themselves (a host that owns all device memory through its own pool
+ * and forbids outside allocations, or a loop that must never trigger the
+ * allocator's implicit synchronisation). This entry point is an engineering
+ * addition with no counterpart in the method's description; it computes
+ * exactly what csa2_attend computes, with the same arguments minus the
+ * workspace.
+ *   - It allocates nothing and calls no allocating routine. Its split-K scratch
+ *     is a library-owned device array of CSA2_NOALLOC_SCRATCH_BYTES, placed on
+ *     each device that loads the library's module and held until exit.
+ *   - Calls needing more scratch than that (csa2_attend_workspace_size(ctx,
+ *     n_query) > CSA2_NOALLOC_SCRATCH_BYTES) are rejected with
+ *     CSA2_ERR_WORKSPACE and a message; nothing is enqueued.
+ *   - The first call on a device looks up the array's device address (the
+ *     context's device must be current); make that first call before any
+ *     stream capture begins on the device.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; calls whose work overlaps on the GPU race on it, so
+ *     order them on one stream. */
+#define CSA2_NOALLOC_SCRATCH_BYTES (32u << 20)
+csa2_status csa2_attend_noalloc(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                                const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv,
+                                const uint8_t* win_scale, const int64_t* win_off, const int64_t* win_lo,
+                                const void* pool_kv, const uint8_t* pool_scale, const int64_t* pool_off,
+                                const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse);
 
 /* Number of kernel launches the last entry point call on this context
  * enqueued (host). */
