@@ -146,6 +146,19 @@ def fp8_block_scale_exponent(amax: float) -> int:
     return int(min(max(k + 127, 0), 254))
 
 
+def fp8_block_scale_exponents(amax) -> np.ndarray:
+    """The same rule as fp8_block_scale_exponent, for an array of block maxima.
+
+    With amax = f * 2^e (f in [0.5, 1), from frexp) and 448 = 0.875 * 2^9,
+    amax <= 448 * 2^k holds exactly when k >= e - 9 (f <= 0.875) or
+    k >= e - 8 (f > 0.875); the least such k is taken.
+    """
+    amax = np.asarray(amax, dtype=np.float64)
+    f, e = np.frexp(amax)
+    k = np.where(f <= 0.875, e - 9, e - 8)
+    return np.where(amax == 0.0, 0, np.clip(k + 127, 0, 254)).astype(np.uint8)
+
+
 def fp8_block_quantize(x, block: int = FP8_BLOCK):
     """Quantize rows [n, D] to (codes uint8 [n, D], scale bytes uint8 [n, D/block])."""
     x = np.asarray(x, dtype=np.float64)
@@ -154,10 +167,7 @@ def fp8_block_quantize(x, block: int = FP8_BLOCK):
         raise ValueError("row length must be a multiple of the block")
     xb = x.reshape(n, d // block, block)
     amax = np.abs(xb).max(axis=2)
-    exps = np.empty((n, d // block), dtype=np.uint8)
-    for i in range(n):
-        for b in range(d // block):
-            exps[i, b] = fp8_block_scale_exponent(float(amax[i, b]))
+    exps = fp8_block_scale_exponents(amax)
     scale = ue8m0_to_f64(exps)[:, :, None]
     codes = f64_to_e4m3_bits(xb / scale).reshape(n, d)
     return codes, exps

@@ -386,3 +386,12 @@ def test_fp8_block_scale_choice():
     blk = np.abs(x).reshape(6, 2, 32).max(axis=2)
     assert np.all(np.abs(back - x).reshape(6, 2, 32) <= blk[:, :, None] * 2.0 ** -4 + 1e-300)
     assert np.all(np.abs(back).reshape(6, 2, 32).max(axis=2) <= 448 * F.ue8m0_to_f64(exps))
+
+
+def test_fp8_block_scale_vectorised_equals_scalar_definition():
+    rng = np.random.default_rng(13)
+    amax = np.abs(rng.standard_normal(5000)) * np.exp(rng.standard_normal(5000) * 6)
+    amax[:6] = [0.0, 448.0, np.nextafter(448.0, 1e9), 224.0, 2.0 ** -140, 3.0e38]
+    got = F.fp8_block_scale_exponents(amax)
+    ref = np.array([F.fp8_block_scale_exponent(float(a)) for a in amax], dtype=np.uint8)
+    assert np.array_equal(got, ref)
