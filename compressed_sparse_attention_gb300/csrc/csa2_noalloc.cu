@@ -29,12 +29,12 @@
 #include "ctx.cuh"
 #include "launchers.cuh"
 
+// the scratch: split-K partial outputs and (max, sum) pairs of csa2_attend
+static __device__ __align__(256) unsigned char g_attend_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
-
-// the scratch: split-K partial outputs and (max, sum) pairs of csa2_attend
-__device__ __align__(256) unsigned char g_attend_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
