@@ -34,6 +34,9 @@ from workloads import PRESETS, make_inputs  # noqa: E402
 
 METRIC = "CSA2 decode tokens/s and HBM GB/s (% of ~8 TB/s) at 64K and 1M context"
 N_COPIES = 4  # rotating input copies: each step's working set is evicted from L2 by the other three
+# dram bytes read + written by one index_score launch on decode_64k_b32, from the
+# ncu capture summarised in profiles/index_score_decode_64k_b32.md (same kernel)
+INDEX_TRAFFIC_BYTES = 134_299_136 + 3_737_856
 
 
 def load_peaks():
@@ -461,7 +464,9 @@ def main():
                    "graph": "one CUDA graph per step"},
         "hbm_gbs": gbs, "hbm_frac": gbs / hbm, "step_algorithmic_bytes": step_bytes,
         "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": idx_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": idx_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                     "frac": idx_gbs / hbm,
+                     "traffic": INDEX_TRAFFIC_BYTES if wl.name == "decode_64k_b32" else None,
+                     "peak_source": peak_src,
                      "bytes_per_launch": idx_b, "ms_per_launch": r["idx_ms"]},
         "e2e": {"value": world * units_per_step / (e2e["ms_per_step"] / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
