@@ -115,9 +115,15 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_flags, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(ctx->d_flags, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
     if (ctx->d_flags) cudaFree(ctx->d_flags);
+    if (ctx->side) cudaStreamDestroy(ctx->side);
+    if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+    if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
     delete ctx;
     return CSA2_ERR_CUDA;
   }
@@ -131,6 +137,9 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
 void csa2_destroy(csa2_ctx* ctx) {
   if (!ctx) return;
   if (ctx->d_flags) cudaFree(ctx->d_flags);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
+  if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+  if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
   delete ctx;
 }
 
@@ -280,23 +289,19 @@ csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float*
 
 size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query) {
   if (!ctx || n_query < 0) return 0;
-  const int nt = csa2::attend_num_tiles(ctx->cfg.topk, true);
-  int ns = csa2::attend_num_splits(n_query, nt, ctx->num_sms);
-  const int tps = (nt + ns - 1) / ns;
-  ns = (nt + tps - 1) / tps;
-  return csa2::attend_workspace_bytes(n_query, ns);
+  return csa2::attend_workspace_bytes(n_query, csa2::attend_plan(n_query, ctx->cfg.topk, true, ctx->num_sms));
 }
 
-static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q,
-                             const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv,
-                             const uint8_t* win_scale, const int64_t* win_off, const int64_t* win_lo,
-                             const void* pool_kv, const uint8_t* pool_scale, const int64_t* pool_off,
-                             const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse, void* ws,
-                             size_t ws_bytes) {
+// validates the attend arguments and fills the kernel parameters
+static csa2_status attend_params(csa2_ctx* ctx, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                                 const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv,
+                                 const uint8_t* win_scale, const int64_t* win_off, const int64_t* win_lo,
+                                 const void* pool_kv, const uint8_t* pool_scale, const int64_t* pool_off,
+                                 const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse, void* ws,
+                                 size_t ws_bytes, csa2::AttendParams* pp) {
   const csa2_config& c = ctx->cfg;
   const bool fp8 = c.kv_format == CSA2_KV_FP8_E4M3_B32;
   if (n_query < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: sizes");
-  if (n_query == 0) return CSA2_OK;
   if (!q || !q_pos || !seq_of_q || !win_kv || !win_off || !sink || !out ||
       (topk_idx && (!pool_kv || !pool_off)) || (fp8 && (!win_scale || (topk_idx && !pool_scale))))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: null pointer");
@@ -305,7 +310,8 @@ static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int3
   const size_t need = csa2_attend_workspace_size(ctx, n_query);
   csa2_status s = check_ws(ctx, ws, ws_bytes, topk_idx ? need : 0);
   if (s != CSA2_OK) return s;
-  csa2::AttendParams p;
+  if (n_query == 0) return CSA2_OK;
+  csa2::AttendParams& p = *pp;
   std::memset(&p, 0, sizeof(p));
   p.q = q; p.q_pos = q_pos; p.seq_of_q = seq_of_q;
   p.win_kv = win_kv; p.win_scale = win_scale; p.win_off = win_off; p.win_lo = win_lo;
@@ -315,8 +321,21 @@ static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int3
   p.n_seq = n_seq; p.n_query = n_query; p.topk = c.topk; p.window = c.window;
   p.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   p.rp = ctx->rope;
+  return CSA2_OK;
+}
+
+static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                             const int64_t* q_pos, const int32_t* seq_of_q, const void* win_kv,
+                             const uint8_t* win_scale, const int64_t* win_off, const int64_t* win_lo,
+                             const void* pool_kv, const uint8_t* pool_scale, const int64_t* pool_off,
+                             const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse, void* ws,
+                             size_t ws_bytes) {
+  csa2::AttendParams p;
+  csa2_status s = attend_params(ctx, n_seq, n_query, q, q_pos, seq_of_q, win_kv, win_scale, win_off, win_lo, pool_kv,
+                                pool_scale, pool_off, topk_idx, sink, out, lse, ws, ws_bytes, &p);
+  if (s != CSA2_OK || n_query == 0) return s;
   int nl = 0;
-  cudaError_t e = csa2::launch_attend(st, ctx->num_sms, fp8, p, ws, &nl);
+  cudaError_t e = csa2::launch_attend(st, ctx->num_sms, ctx->cfg.kv_format == CSA2_KV_FP8_E4M3_B32, p, ws, &nl);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attend");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -339,7 +358,7 @@ size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
   const size_t scores = al((size_t)n_query * (size_t)(max_vis > 0 ? max_vis : 1) * 4);
   const size_t tk = al(csa2_topk_workspace_size(ctx, n_query, max_vis));
   const size_t at = al(csa2_attend_workspace_size(ctx, n_query));
-  return scores + (tk > at ? tk : at);
+  return scores + tk + at;
 }
 
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
@@ -356,32 +375,82 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   char* ws = reinterpret_cast<char*>(a->workspace);
   const int64_t ld = a->max_vis > 0 ? a->max_vis : 1;
   float* scores = reinterpret_cast<float*>(ws);
-  char* rest = ws + al((size_t)a->n_query * (size_t)ld * 4);
-  const size_t rest_bytes = a->workspace_bytes - (size_t)(rest - ws);
+  char* tk_ws = ws + al((size_t)a->n_query * (size_t)ld * 4);
+  const size_t tk_bytes = al(csa2_topk_workspace_size(ctx, a->n_query, a->max_vis));
+  char* at_ws = tk_ws + tk_bytes;
+  const size_t at_bytes = a->workspace_bytes - (size_t)(at_ws - ws);
+  // the attention arguments are checked before anything is enqueued
+  csa2::AttendParams ap;
+  s = attend_params(ctx, a->n_seq, a->n_query, a->q, a->q_pos, a->seq_of_q, a->win_kv, a->win_scale, a->win_off,
+                    a->win_lo, a->pool_kv, a->pool_scale, a->pool_off, a->topk_idx, a->sink, a->out, a->lse, at_ws,
+                    at_bytes, &ap);
+  if (s != CSA2_OK) return s;
+  const int fp8 = ctx->cfg.kv_format == CSA2_KV_FP8_E4M3_B32;
+  const csa2::AttendPlan pl = csa2::attend_plan(a->n_query, ctx->cfg.topk, true, ctx->num_sms);
   int launches = 0;
   if (a->mode == CSA2_MODE_FULL) {
+    ctx->last_launches = 0;
     s = do_compress(ctx, st, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off, a->norm_w,
                     a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale);
     if (s != CSA2_OK) return s;
     launches += ctx->last_launches;
   }
-  if (a->mode == CSA2_MODE_FULL || a->mode == CSA2_MODE_REINDEX) {
+  if (a->n_query == 0) {
+    ctx->last_launches = launches;
+    return CSA2_OK;
+  }
+  if (a->mode == CSA2_MODE_REUSE) {
+    // nothing to overlap with: window and selected tiles share one launch
     ctx->last_launches = 0;
-    s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
-                 a->seq_of_q, a->n_vis, a->max_vis, scores, ld);
-    if (s != CSA2_OK) return s;
-    launches += ctx->last_launches;
-    ctx->last_launches = 0;
-    s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, rest, rest_bytes);
-    if (s != CSA2_OK) return s;
-    launches += ctx->last_launches;
+    cudaError_t e = csa2::launch_attend(st, ctx->num_sms, fp8, ap, at_ws, &ctx->last_launches);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
+    ctx->last_launches += launches;
+    return CSA2_OK;
   }
   ctx->last_launches = 0;
-  s = do_attend(ctx, st, a->n_seq, a->n_query, a->q, a->q_pos, a->seq_of_q, a->win_kv, a->win_scale, a->win_off,
-                a->win_lo, a->pool_kv, a->pool_scale, a->pool_off, a->topk_idx, a->sink, a->out, a->lse, rest,
-                rest_bytes);
+  s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
+               a->seq_of_q, a->n_vis, a->max_vis, scores, ld);
   if (s != CSA2_OK) return s;
-  ctx->last_launches += launches;
+  launches += ctx->last_launches;
+  // The window tile reads only the window buffer, which nothing in the step
+  // writes. It runs on the side stream beside top-k, whose grid (a cluster per
+  // query) leaves most SMs free; the caller's stream joins it before the
+  // merge. It is forked after the index launch, whose CTAs fill every SM and
+  // share out the pool statically, so that none of them waits for it.
+  bool forked = false;
+  cudaError_t e = cudaSuccess;
+  if (pl.split_window) {
+    e = cudaEventRecord(ctx->ev_fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0);
+    if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, fp8, ap, pl, at_ws, &launches);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_join, ctx->side);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step: window tile");
+    forked = true;
+  }
+  // every exit after the fork joins the side stream back, so that a capture
+  // of the step stays well formed and the caller's stream orders after it
+  auto join = [&](csa2_status so) -> csa2_status {
+    if (!forked) return so;
+    forked = false;
+    const cudaError_t je = cudaStreamWaitEvent(st, ctx->ev_join, 0);
+    if (je != cudaSuccess && so == CSA2_OK) return cuda_fail(ctx, je, "step: join");
+    return so;
+  };
+  ctx->last_launches = 0;
+  s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes);
+  if (s != CSA2_OK) return join(s);
+  launches += ctx->last_launches;
+  if (pl.split_window) {
+    e = csa2::launch_attend_main(st, fp8, ap, pl, at_ws, &launches);
+    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
+    s = join(CSA2_OK);
+    if (s != CSA2_OK) return s;
+    e = csa2::launch_attend_merge(st, ap, pl, at_ws, &launches);
+  } else {
+    e = csa2::launch_attend(st, ctx->num_sms, fp8, ap, at_ws, &launches);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
+  ctx->last_launches = launches;
   return CSA2_OK;
 }
 

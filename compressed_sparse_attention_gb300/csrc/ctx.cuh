@@ -10,6 +10,9 @@ struct csa2_ctx {
   int num_sms = 0;
   csa2::RopeParams rope;
   uint32_t* d_flags = nullptr;
+  cudaStream_t side = nullptr;    // step side stream: the window tile
+  cudaEvent_t ev_fork = nullptr;  // recorded on the caller's stream at the start of a step
+  cudaEvent_t ev_join = nullptr;  // recorded on the side stream after the window tile
   std::string err;
   int last_launches = 0;
 };

@@ -92,8 +92,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t t = p.q_pos[qi];
   const int b = p.seq_of_q[qi];
   const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
-  const int tile_begin = split * p.tiles_per_split;
-  const int tile_end = q_ok ? min(tile_begin + p.tiles_per_split, p.n_tiles) : tile_begin;
+  // split 0 takes the launch's first tile alone when lead_single is set (the
+  // window tile); the other splits take tiles_per_split tiles each
+  const int lead = p.lead_single ? 1 : 0;
+  const int tile_begin = (lead && split == 0) ? p.tile_base : p.tile_base + lead + (split - lead) * p.tiles_per_split;
+  const int tile_cap = (lead && split == 0) ? tile_begin + 1 : tile_begin + p.tiles_per_split;
+  const int tile_end = q_ok ? min(tile_cap, p.tile_base + p.tile_count) : tile_begin;
   if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
 
   if (warp == 0) {
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   __syncthreads();
   const bool have_o = (tile_begin < tile_end) && !aborted;
   const int first_rope = kDim - 2 * p.rp.pairs;
-  if (p.n_split == 1) {
+  if (p.direct) {
     // final normalisation with the sink: fo = e^{m - M} / den, den = l e^{m - M} + e^{sink - M}
     if (tid < kHeads) {
       const float sk = p.sink[tid] * 1.4426950408889634f;
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     }
   } else {
     // unnormalised partial O^T and (m, l) for the merge
-    const int64_t slot = (int64_t)qi * p.n_split + split;
+    const int64_t slot = (int64_t)qi * p.n_slots + p.slot_base + split;
     if (tid < kHeads)
       p.ws_ml[slot * kHeads + tid] = make_float2(have_o ? m_run[tid] : -INFINITY, have_o ? l_run[tid] : 0.f);
     if (have_o) {
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   const int hg = blockIdx.x % (kHeads / kMergeHeadsPerCta);
   const int tid = threadIdx.x, hl = tid >> 6, chunk = tid & 63;
   const int h = hg * kMergeHeadsPerCta + hl;
-  const int ns = p.n_split;
+  const int ns = p.n_slots;
   const float2* ml = p.ws_ml + (int64_t)qi * ns * kHeads;
   const int64_t t = p.q_pos[qi];
   if (tid < kMergeHeadsPerCta) {
@@ -529,33 +533,54 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
 
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
 
-int attend_num_splits(int n_query, int n_tiles, int num_sms) {
-  if (n_query <= 0) return 1;
-  int ns = (num_sms + n_query - 1) / n_query;
-  if (ns > n_tiles) ns = n_tiles;
-  if (ns > 8) ns = 8;
-  if (ns < 1) ns = 1;
-  return ns;
+// How one attend call is cut into launches. With few queries (decode) the
+// window tile, which does not depend on the selection, is its own launch (the
+// step runs it on a side stream from the start), the selected tiles are cut
+// so that all their CTAs fit in one wave, and a merge combines the partials.
+// With many queries (prefill) one CTA per query runs every tile and writes the
+// output directly.
+AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
+  AttendPlan pl{};
+  pl.n_tiles = attend_num_tiles(topk, has_idx);
+  if (n_query < 1) n_query = 1;
+  if (pl.n_tiles >= 2 && 2 * n_query <= num_sms) {
+    pl.split_window = 1;
+    int ns = num_sms / n_query;
+    if (ns > pl.n_tiles - 1) ns = pl.n_tiles - 1;
+    if (ns > 7) ns = 7;
+    pl.tps = (pl.n_tiles - 1 + ns - 1) / ns;
+    pl.ns = (pl.n_tiles - 1 + pl.tps - 1) / pl.tps;
+    pl.n_slots = 1 + pl.ns;
+  } else {
+    pl.split_window = 0;
+    int ns = (num_sms + n_query - 1) / n_query;
+    if (ns > pl.n_tiles) ns = pl.n_tiles;
+    if (ns > 8) ns = 8;
+    if (ns < 1) ns = 1;
+    pl.tps = (pl.n_tiles + ns - 1) / ns;
+    pl.ns = (pl.n_tiles + pl.tps - 1) / pl.tps;
+    pl.n_slots = pl.ns > 1 ? pl.ns : 0;
+  }
+  return pl;
 }
 
-size_t attend_workspace_bytes(int n_query, int n_split) {
-  if (n_split <= 1) return 0;
+size_t attend_workspace_bytes(int n_query, const AttendPlan& pl) {
+  if (pl.n_slots == 0) return 0;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)n_query * n_split * kHeads * kDim * 4) + al((size_t)n_query * n_split * kHeads * 8);
+  return al((size_t)n_query * pl.n_slots * kHeads * kDim * 4) + al((size_t)n_query * pl.n_slots * kHeads * 8);
 }
 
-cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch) {
-  if (p.n_query == 0) return cudaSuccess;
-  p.n_tiles = attend_num_tiles(p.topk, p.topk_idx != nullptr);
-  p.n_split = attend_num_splits(p.n_query, p.n_tiles, num_sms);
-  p.tiles_per_split = (p.n_tiles + p.n_split - 1) / p.n_split;
-  p.n_split = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
-  if (p.n_split > 1) {
+static void attach_ws(AttendParams& p, const AttendPlan& pl, void* ws) {
+  p.n_slots = pl.n_slots;
+  if (pl.n_slots > 0) {
     auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
     p.ws_o = reinterpret_cast<float*>(ws);
     p.ws_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) +
-                                        al((size_t)p.n_query * p.n_split * kHeads * kDim * 4));
+                                        al((size_t)p.n_query * pl.n_slots * kHeads * kDim * 4));
   }
+}
+
+static cudaError_t launch_tiles(cudaStream_t st, int kv_fp8, const AttendParams& p, int* n_launch) {
   cudaError_t e;
   if (kv_fp8) e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
   else e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
@@ -564,11 +589,76 @@ cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams
   if (kv_fp8) attend_kernel<true><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
   else attend_kernel<false><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
   *n_launch += 1;
-  if (p.n_split > 1) {
-    attend_merge_kernel<<<p.n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(p);
-    *n_launch += 1;
-  }
   return cudaGetLastError();
+}
+
+cudaError_t launch_attend_window(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+                                 int* n_launch) {
+  if (p.n_query == 0 || !pl.split_window) return cudaSuccess;
+  attach_ws(p, pl, ws);
+  p.n_tiles = pl.n_tiles;
+  p.tile_base = 0;
+  p.tile_count = 1;
+  p.n_split = 1;
+  p.tiles_per_split = 1;
+  p.lead_single = 0;
+  p.slot_base = 0;
+  p.direct = 0;
+  return launch_tiles(st, kv_fp8, p, n_launch);
+}
+
+cudaError_t launch_attend_main(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+                               int* n_launch) {
+  if (p.n_query == 0) return cudaSuccess;
+  attach_ws(p, pl, ws);
+  p.n_tiles = pl.n_tiles;
+  p.n_split = pl.ns;
+  p.tiles_per_split = pl.tps;
+  p.lead_single = 0;
+  if (pl.split_window) {
+    p.tile_base = 1;
+    p.tile_count = pl.n_tiles - 1;
+    p.slot_base = 1;
+    p.direct = 0;
+  } else {
+    p.tile_base = 0;
+    p.tile_count = pl.n_tiles;
+    p.slot_base = 0;
+    p.direct = pl.ns == 1 ? 1 : 0;
+  }
+  return launch_tiles(st, kv_fp8, p, n_launch);
+}
+
+cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch) {
+  if (p.n_query == 0 || pl.n_slots == 0) return cudaSuccess;
+  attach_ws(p, pl, ws);
+  attend_merge_kernel<<<p.n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(p);
+  *n_launch += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch) {
+  const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
+  cudaError_t e;
+  if (pl.split_window) {
+    // on one stream the window tile and the selected tiles share one launch:
+    // split 0 of each query takes the window, splits 1.. the selected tiles
+    AttendParams a = p;
+    attach_ws(a, pl, ws);
+    a.n_tiles = pl.n_tiles;
+    a.tile_base = 0;
+    a.tile_count = pl.n_tiles;
+    a.n_split = 1 + pl.ns;
+    a.tiles_per_split = pl.tps;
+    a.lead_single = 1;
+    a.slot_base = 0;
+    a.direct = 0;
+    e = launch_tiles(st, kv_fp8, a, n_launch);
+  } else {
+    e = launch_attend_main(st, kv_fp8, p, pl, ws, n_launch);
+  }
+  if (e == cudaSuccess) e = launch_attend_merge(st, p, pl, ws, n_launch);
+  return e;
 }
 
 }  // namespace csa2

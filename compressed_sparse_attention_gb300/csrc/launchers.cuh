@@ -27,9 +27,15 @@ struct AttendParams {
   int n_query;
   int topk;
   int window;
-  int n_tiles;
-  int n_split;
+  int n_tiles;          // tiles of one query: window + ceil(topk / 128)
+  int tile_base;        // first tile this launch covers
+  int tile_count;       // tiles this launch covers
+  int n_split;          // CTAs per query in this launch
   int tiles_per_split;
+  int lead_single;      // 1: split 0 covers the first tile alone, the others tiles_per_split each
+  int n_slots;          // partial slots per query in the workspace
+  int slot_base;        // slot of this launch's first split
+  int direct;           // 1: write the normalised output, no partials
   float scale_log2;  // softmax_scale * log2(e)
   RopeParams rp;
 };
@@ -48,9 +54,21 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
 size_t topk_workspace_bytes(int n_query, int64_t max_vis);
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch);
+struct AttendPlan {
+  int n_tiles;
+  int split_window;  // window tile launched on its own
+  int ns;            // CTAs per query of the main launch
+  int tps;           // tiles per CTA of the main launch
+  int n_slots;       // partial slots per query (0: direct output)
+};
 int attend_num_tiles(int topk, bool has_idx);
-int attend_num_splits(int n_query, int n_tiles, int num_sms);
-size_t attend_workspace_bytes(int n_query, int n_split);
+AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
+size_t attend_workspace_bytes(int n_query, const AttendPlan& pl);
+cudaError_t launch_attend_window(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+                                 int* n_launch);
+cudaError_t launch_attend_main(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+                               int* n_launch);
+cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch);
 
 }  // namespace csa2

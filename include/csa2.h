@@ -143,7 +143,7 @@ csa2_status csa2_check(csa2_ctx* ctx, void* stream, uint32_t* flags_out);
  *            rope_dim channels of row i are rotated by angle pos[i]*f_k first
  *   format   csa2_kv_format; out [n_rows, dim] bf16 or e4m3 bytes,
  *            out_scale [n_rows, dim/32] ue8m0 bytes (fp8 only, else NULL)
- * dim must be a multiple of 32 and at most 1024. */
+ * dim must be 128 (index keys) or 512 (attention rows). */
 csa2_status csa2_store_rows(csa2_ctx* ctx, void* stream, const float* rows, int64_t n_rows,
                             int32_t dim, const int64_t* pos, int32_t format, void* out,
                             uint8_t* out_scale);
@@ -243,7 +243,14 @@ csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_qu
  * attend; Reindex = index_score + topk + attend on the borrowed pool and
  * keys; Reuse = attend with the borrowed selection in topk_idx. Every mode
  * uses its own q, window and sink. Field meanings are those of the
- * single-step calls above. */
+ * single-step calls above.
+ * For few queries (2 * n_query <= SMs) the window tile of the attention runs
+ * on a stream the context owns, forked from `stream` after the index launch
+ * and joined back into it before the final merge; all work still orders
+ * after what precedes the call on `stream`, and work enqueued on `stream`
+ * after it orders after all of it (also under stream capture). Two steps on
+ * one context must not run at the same time on different streams, as they
+ * share that side stream. */
 typedef struct csa2_step_args {
   int32_t mode;      /* csa2_mode */
   int32_t n_seq;
