@@ -3,9 +3,12 @@
 // the chosen indices written in ascending order, -1 padded (PocketLLM
 // "DeepSeek-V4.1-Flash", "The CSA2 attention layers").
 //
-// Integer work on the scores' bit patterns:
-//   1. hist:   a 4096-bin histogram of the top 12 bits of each score's
-//              order-preserving key (per query, over all CTAs of the row);
+// Integer work on the scores' order-preserving bit patterns. Rows of up to
+// 262,144 scores take one launch: a thread-block cluster per query running an
+// MSD radix select over shared memory (described above the kernel below).
+// Longer rows take three launches through global memory:
+//   1. hist:   a 4096-bin histogram of the top 12 bits of each score's key
+//              (per query, over all CTAs of the row);
 //   2. filter: every CTA finds the bin that holds the k-th largest key and
 //              appends (key, index) of every element at or above it to a
 //              per-query candidate list;
@@ -13,11 +16,6 @@
 //              candidates' unique 64-bit composite key<<32 | ~index (larger
 //              composite = larger score, then lower index), keeps the
 //              composites at or above the threshold, and sorts their indices.
-// For rows up to 16 x 16,384 scores the three steps run in ONE launch: a
-// thread-block cluster per query, each CTA holding a 16,384-score slice in
-// shared memory, the histograms summed across the cluster through distributed
-// shared memory and the candidates gathered by the cluster's first CTA. Longer
-// rows take the three-kernel path through global memory.
 #include <cooperative_groups.h>
 
 #include "launchers.cuh"
@@ -247,38 +245,55 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const int32_t* __rest
 namespace cg = cooperative_groups;
 
 // ---------------------------------------------------------------------------
-// Single-launch top-k for rows of up to 16 x 16,384 scores: a thread-block
-// cluster per query, CTA r holding scores [r*S, (r+1)*S) of the row in shared
-// memory as order-preserving keys (element li of the slice sits in thread
-// li % 1024, round li / 1024, so a warp's ballot in round u is bit-word
-// u*32 + warp of the slice's bitmap, and word w holds elements 32w..32w+31).
-//   1. four 8-bit digit levels (MSD radix select): each level histograms the
-//      keys that match the digits chosen so far, one warp sums the 256 bins
-//      across the cluster through distributed shared memory and picks the
-//      digit holding the k-th largest key; after four levels the exact key T
-//      and the number of keys equal to T to take are known in every CTA;
-//   2. keys equal to T are taken lowest index first: a CTA takes as many as
-//      remain after the ties of the CTAs before it (CTAs are in index order);
-//   3. every CTA writes its chosen indices in ascending order at its offset
-//      (the chosen counts of the CTAs before it) from its bitmap.
+// Single-launch top-k for rows of up to 8 x 32,768 scores: a thread-block
+// cluster of C <= 8 CTAs per query (the portable size: a 1,024-thread CTA
+// holds a whole SM, and not every GPC has room for a 16-CTA cluster), CTA r
+// holding scores [r*S, (r+1)*S) of the row as order-preserving keys in
+// shared memory. Element li of a slice sits in thread li % 1024, round li / 1024,
+// so a warp's ballot in round u is bit-word u*32 + warp of the slice's
+// bitmap and word w covers elements 32w .. 32w+31.
+//   1. the cluster's smallest and largest key give the prefix that all keys
+//      share; the digits start below it, so that the first histogram already
+//      spreads the keys (scores of one row share most exponent bits);
+//   2. at most three 12-bit MSD digit levels: each histograms the keys that
+//      match the digits chosen so far, sums the bins over the cluster through
+//      distributed shared memory and picks the digit holding the k-th largest
+//      key. When the picked bin holds exactly the keys still needed the
+//      search ends: the chosen set is every key whose prefix is at or above
+//      the picked one;
+//   3. otherwise the full key T is known, with the number of keys equal to T
+//      still to take; they are taken lowest index first, each CTA taking what
+//      remains after the ties of the CTAs before it (CTAs are in index order);
+//   4. every CTA writes its chosen indices in ascending order at its offset
+//      (the chosen counts of the CTAs before it) from a ballot bitmap.
 // No candidate list, no sort, and no CTA works for the others.
 // ---------------------------------------------------------------------------
 constexpr int kTkThreads = 1024;
-constexpr int kTkMaxCluster = 16;
+constexpr int kTkMaxCluster = 8;
+constexpr int kTkDigit = 12;
+constexpr int kTkBins = 1 << kTkDigit;
 
 template <int PER>
 struct TkLayout {
   static constexpr int kSlice = kTkThreads * PER;
-  static constexpr int kWords = kSlice / 32;
-  static constexpr uint32_t KEYS = 0;
-  static constexpr uint32_t HIST = KEYS + kSlice * 4;   // [4 levels][256]
-  static constexpr uint32_t TOT = HIST + 4 * 256 * 4;   // [256] cluster-summed bins, top digit first
-  static constexpr uint32_t BM = TOT + 256 * 4;         // chosen bitmap
-  static constexpr uint32_t TB = BM + kWords * 4;       // tie bitmap
-  static constexpr uint32_t TP = TB + kWords * 4;       // ties before each word
+  static constexpr int kWords = kSlice / 32;                 // at most one per thread
+  static constexpr uint32_t KEYS = 0;                        // [kSlice]
+  static constexpr uint32_t HIST = KEYS + kSlice * 4;        // [3 levels][4096]
+  static constexpr uint32_t BM = HIST + 3 * kTkBins * 4;     // chosen bitmap
+  static constexpr uint32_t TB = BM + kWords * 4;            // tie bitmap
+  static constexpr uint32_t TP = TB + kWords * 4;            // ties before each word
   static constexpr uint32_t MISC = TP + kWords * 4;
   static constexpr uint32_t SMEM = MISC + 1024;
+  static_assert(kWords <= kTkThreads, "one bitmap word per thread");
 };
+
+// misc words
+constexpr int kMiscRes = 32;     // [32..34] picked digit, count above it, count in it
+constexpr int kMiscMin = 36;     // smallest valid key here
+constexpr int kMiscMax = 37;     // largest valid key here
+constexpr int kMiscGt = 38;      // keys > T here
+constexpr int kMiscTie = 39;     // keys == T here
+constexpr int kMiscChosen = 40;  // chosen keys here
 
 // inclusive block-wide scan of one value per thread (1024 threads); warp_s[31] = total
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s) {
@@ -312,46 +327,55 @@ __device__ __forceinline__ void cluster_gather_u32(cg::cluster_group& cluster, c
     v[r] = (uint32_t)r < C ? *cluster.map_shared_rank(local, (unsigned)r) : 0u;
 }
 
-// Pick the digit holding the need-th largest key of a level: threads 0..255
-// sum their bin over the cluster (one round of remote loads), warp 0 scans
-// the 256 sums from the top digit down. Leaves (digit, count above) in res.
-__device__ __forceinline__ void cluster_pick_digit(cg::cluster_group& cluster, uint32_t C, const uint32_t* h,
-                                                   uint32_t* tot, uint32_t need, uint32_t* res) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid < 256) {
-    uint32_t v[kTkMaxCluster];
-    cluster_gather_u32(cluster, h + (255 - tid), C, v);
-    uint32_t c = 0;
+__device__ __forceinline__ void tk_sync(cg::cluster_group& cluster, uint32_t C) {
+  if (C > 1) cluster.sync();
+  else __syncthreads();
+}
+
+// Pick the digit holding the need-th largest key of a level with nbins bins
+// (a power of two, at least 2): thread t sums bins nbins-1-4t .. nbins-4-4t
+// over the cluster, a block scan runs from the top digit down, and the thread
+// whose range holds the need-th key leaves (digit, count above, count in it)
+// in res. Ends with the block synchronised.
+__device__ __forceinline__ void tk_pick_digit(cg::cluster_group& cluster, uint32_t C, const uint32_t* h,
+                                              uint32_t nbins, uint32_t need, uint32_t* warp_s, uint32_t* res) {
+  const int tid = threadIdx.x;
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  const int top = (int)nbins - 1 - 4 * tid;  // highest bin of this thread
+  if (top >= 3) {
+    uint4 v[kTkMaxCluster];
 #pragma unroll
-    for (int r = 0; r < kTkMaxCluster; ++r) c += v[r];
-    tot[tid] = c;
-  }
-  __syncthreads();
-  if (tid < 32) {
-    uint32_t loc[8], sum = 0;
+    for (int r = 0; r < kTkMaxCluster; ++r)
+      if ((uint32_t)r < C) v[r] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(h + top - 3, (unsigned)r));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      loc[j] = tot[8 * lane + j];
-      sum += loc[j];
-    }
-    uint32_t incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += x;
-    }
-    const uint32_t excl = incl - sum;
-    if (excl < need && need <= incl) {
-      uint32_t run = excl;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (run + loc[j] >= need) {
-          res[0] = (uint32_t)(255 - (8 * lane + j));
-          res[1] = run;
-          break;
-        }
-        run += loc[j];
+    for (int r = 0; r < kTkMaxCluster; ++r) {
+      if ((uint32_t)r < C) {
+        c[0] += v[r].w;
+        c[1] += v[r].z;
+        c[2] += v[r].y;
+        c[3] += v[r].x;
       }
+    }
+  } else if (top >= 0) {
+    for (uint32_t r = 0; r < C; ++r) {
+      const uint32_t* rh = cluster.map_shared_rank(h, r);
+      for (int j = 0; j <= top; ++j) c[j] += rh[top - j];
+    }
+  }
+  const uint32_t sum = c[0] + c[1] + c[2] + c[3];
+  const uint32_t incl = block_scan_incl(sum, warp_s);
+  const uint32_t excl = incl - sum;
+  if (excl < need && need <= incl) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (run + c[j] >= need) {
+        res[0] = (uint32_t)(top - j);
+        res[1] = run;
+        res[2] = c[j];
+        break;
+      }
+      run += c[j];
     }
   }
   __syncthreads();
@@ -366,14 +390,12 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   extern __shared__ __align__(16) unsigned char tk_smem[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem + L::KEYS);
   uint32_t* hist = reinterpret_cast<uint32_t*>(tk_smem + L::HIST);
-  uint32_t* tot = reinterpret_cast<uint32_t*>(tk_smem + L::TOT);
   uint32_t* bm = reinterpret_cast<uint32_t*>(tk_smem + L::BM);
   uint32_t* tb = reinterpret_cast<uint32_t*>(tk_smem + L::TB);
   uint32_t* tp = reinterpret_cast<uint32_t*>(tk_smem + L::TP);
   uint32_t* misc = reinterpret_cast<uint32_t*>(tk_smem + L::MISC);
-  // misc: [0..31] warp scan, [32..33] picked digit / count above, [34] keys > T here, [35] ties here
   uint32_t* warp_s = misc;
-  uint32_t* res = misc + 32;
+  uint32_t* res = misc + kMiscRes;
 
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t rank = cluster.block_rank();
@@ -383,12 +405,10 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   const int nv = (int)min((int64_t)max(n_vis[q], 0), max_vis);
   const int64_t base = (int64_t)rank * L::kSlice;
   const int cnt = (int)max((int64_t)0, min((int64_t)L::kSlice, (int64_t)nv - base));
-  const uint32_t need = (uint32_t)min(k, nv);
+  const uint32_t need = (uint32_t)max(0, min(k, nv));
   const bool all = (uint32_t)nv <= need;  // every visible entry is chosen (uniform over the cluster)
 
-  if (tid < 4 * 256) hist[tid] = 0;
-  if (tid < 4) misc[32 + tid] = 0;
-  // ---- slice -> keys
+  // ---- slice -> keys; histogram and counter init meanwhile
   {
     const float* row = scores + (int64_t)q * ld + base;
     float v[PER];
@@ -397,68 +417,120 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
       const int li = u * kTkThreads + tid;
       v[u] = li < cnt ? row[li] : 0.f;
     }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int li = u * kTkThreads + tid;
-      keys[li] = li < cnt ? score_key(v[u]) : 0u;
+    uint4* h4 = reinterpret_cast<uint4*>(hist);
+    for (int i = tid; i < 3 * kTkBins / 4; i += kTkThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid == 0) {
+      misc[kMiscMin] = 0xFFFFFFFFu;
+      misc[kMiscMax] = 0u;
+      misc[kMiscGt] = 0u;
+      misc[kMiscTie] = 0u;
     }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) keys[u * kTkThreads + tid] = score_key(v[u]);
   }
   __syncthreads();
-  uint32_t T = 0, take_t = 0;  // keys > T are chosen; of keys == T, the first take_t (by index)
+
+  // state after the search: chosen = keys whose top (32 - shift) bits are > P,
+  // plus, when `exact`, those equal to P; otherwise (shift == 0) the first
+  // take_t keys equal to T = P in index order
+  uint32_t P = 0, take_t = 0;
+  int shift = 32;
+  bool exact = true;
   if (!all) {
-    // ---- four 8-bit digit levels; warp-aggregated adds only on the first
-    // (almost every score shares its top byte), plain adds below it
-    uint32_t prefix = 0, rem = need;
-#pragma unroll 1
-    for (int lvl = 0; lvl < 4; ++lvl) {
-      const int shift = 24 - 8 * lvl;
-      uint32_t* h = hist + 256 * lvl;
+    // ---- common prefix of the cluster's keys
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-      for (int u = 0; u < PER; ++u) {
-        const int li = u * kTkThreads + tid;
-        const uint32_t key = keys[li];
-        const bool ok = li < cnt && (lvl == 0 || (key >> (shift + 8)) == prefix);
-        const uint32_t d = (key >> shift) & 0xFFu;
-        if (lvl == 0) {
-          const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
-          const uint32_t same = __ballot_sync(0xffffffffu, ok && d == d0);
-          if (lane == 0 && same) atomicAdd(&h[d0], (uint32_t)__popc(same));
-          if (ok && d != d0) atomicAdd(&h[d], 1u);
-        } else if (ok) {
-          atomicAdd(&h[d], 1u);
+    for (int u = 0; u < PER; ++u) {
+      if (u * kTkThreads + tid < cnt) {
+        const uint32_t x = keys[u * kTkThreads + tid];
+        mn = min(mn, x);
+        mx = max(mx, x);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      atomicMin(&misc[kMiscMin], mn);
+      atomicMax(&misc[kMiscMax], mx);
+    }
+    tk_sync(cluster, C);
+    {
+      uint32_t a[kTkMaxCluster], b[kTkMaxCluster];
+      cluster_gather_u32(cluster, misc + kMiscMin, C, a);
+      cluster_gather_u32(cluster, misc + kMiscMax, C, b);
+      mn = 0xFFFFFFFFu;
+      mx = 0u;
+#pragma unroll
+      for (int r = 0; r < kTkMaxCluster; ++r) {
+        if ((uint32_t)r < C) {
+          mn = min(mn, a[r]);
+          mx = max(mx, b[r]);
         }
       }
-      cluster.sync();
-      cluster_pick_digit(cluster, C, h, tot, rem, res);
-      prefix = (prefix << 8) | res[0];
-      rem -= res[1];
-      __syncthreads();
     }
-    T = prefix;
+    const uint32_t diff = mn ^ mx;
+    shift = diff ? 32 - __clz(diff) : 0;  // bits below the shared prefix
+    P = shift >= 32 ? 0u : (mx >> shift);
+    uint32_t rem = need;
+    exact = false;
+    // ---- digit levels below the prefix
+#pragma unroll 1
+    for (int lvl = 0; shift > 0; ++lvl) {
+      const int w = min(kTkDigit, shift);
+      const int sh = shift - w;
+      const uint32_t dmask = (1u << w) - 1u;
+      uint32_t* h = hist + kTkBins * lvl;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const uint32_t x = keys[u * kTkThreads + tid];
+        const bool ok = u * kTkThreads + tid < cnt && (shift >= 32 || (x >> shift) == P);
+        if (ok) atomicAdd(&h[(x >> sh) & dmask], 1u);
+      }
+      tk_sync(cluster, C);
+      tk_pick_digit(cluster, C, h, 1u << w, rem, warp_s, res);
+      P = (shift >= 32 ? 0u : (P << w)) | res[0];
+      rem -= res[1];
+      const uint32_t at = res[2];
+      shift = sh;
+      __syncthreads();  // res is rewritten by the next level
+      if (at == rem) {
+        exact = true;
+        break;
+      }
+    }
     take_t = rem;
   }
-  // ---- counts above T and ties here, exchanged once across the cluster
+  // ---- ties at T (shift == 0, not exact): counts above T and at T here,
+  // exchanged once across the cluster; this CTA may take the ties that the
+  // CTAs before it leave, lowest index first
   uint32_t quota = 0, off = 0;
-  if (!all) {
+  bool off_known = false;
+  if (all) {
+    off = (uint32_t)base;  // every earlier CTA is full and fully chosen
+    off_known = true;
+  } else if (!exact) {
     uint32_t ngt = 0, nt = 0;
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int li = u * kTkThreads + tid;
-      const uint32_t key = keys[li];
-      const uint32_t bt = __ballot_sync(0xffffffffu, li < cnt && key == T);
-      const uint32_t bg = __ballot_sync(0xffffffffu, li < cnt && key > T);
+      const uint32_t x = keys[li];
+      const uint32_t bt = __ballot_sync(0xffffffffu, li < cnt && x == P);
+      const uint32_t bg = __ballot_sync(0xffffffffu, li < cnt && x > P);
       if (lane == 0) tb[u * 32 + warp] = bt;
       nt += __popc(bt);
       ngt += __popc(bg);
     }
     if (lane == 0) {
-      atomicAdd(&misc[34], ngt);
-      atomicAdd(&misc[35], nt);
+      atomicAdd(&misc[kMiscGt], ngt);
+      atomicAdd(&misc[kMiscTie], nt);
     }
-    cluster.sync();
+    tk_sync(cluster, C);
     uint32_t g[kTkMaxCluster], t[kTkMaxCluster];
-    cluster_gather_u32(cluster, misc + 34, C, g);
-    cluster_gather_u32(cluster, misc + 35, C, t);
+    cluster_gather_u32(cluster, misc + kMiscGt, C, g);
+    cluster_gather_u32(cluster, misc + kMiscTie, C, t);
     uint32_t ties_before = 0;
 #pragma unroll
     for (int r = 0; r < kTkMaxCluster; ++r) {
@@ -468,34 +540,49 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
         ties_before += t[r];
       }
     }
-    quota = take_t > ties_before ? take_t - ties_before : 0u;  // ties this CTA may take, lowest index first
+    off_known = true;
+    quota = take_t > ties_before ? take_t - ties_before : 0u;
     if (quota > 0) {
       const uint32_t tw = tid < L::kWords ? tb[tid] : 0u;  // thread tid owns word tid
       const uint32_t pre = block_scan_incl(__popc(tw), warp_s) - __popc(tw);
       if (tid < L::kWords) tp[tid] = pre;
       __syncthreads();
     }
-  } else {
-    off = (uint32_t)base;  // every earlier CTA is full and fully chosen
   }
-  // ---- chosen bitmap: keys > T, plus the first `quota` ties in index order
+  // ---- chosen bitmap
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int li = u * kTkThreads + tid;
     const int w = u * 32 + warp;
-    const uint32_t key = keys[li];
-    bool chosen = li < cnt && (all || key > T);
-    if (!all && li < cnt && key == T && quota > 0)
-      chosen = tp[w] + __popc(tb[w] & ((1u << lane) - 1u)) < quota;
+    const uint32_t x = keys[li];
+    bool chosen;
+    if (all) {
+      chosen = li < cnt;
+    } else if (exact) {
+      chosen = li < cnt && (x >> shift) >= P;
+    } else {
+      chosen = li < cnt && x > P;
+      if (li < cnt && x == P && quota > 0)
+        chosen = tp[w] + __popc(tb[w] & ((1u << lane) - 1u)) < quota;
+    }
     const uint32_t bal = __ballot_sync(0xffffffffu, chosen);
     if (lane == 0) bm[w] = bal;
   }
   __syncthreads();
-  // ---- write chosen indices ascending at this CTA's offset; word w covers
-  // slice elements 32w .. 32w+31 and thread tid owns word tid
+  // ---- offsets of the words (thread tid owns word tid) and of this CTA
+  const uint32_t wbits = tid < L::kWords ? bm[tid] : 0u;
+  const uint32_t pre = block_scan_incl(__popc(wbits), warp_s) - __popc(wbits);
+  if (!off_known && C > 1) {
+    if (tid == 0) misc[kMiscChosen] = warp_s[31];
+    cluster.sync();
+    uint32_t c[kTkMaxCluster];
+    cluster_gather_u32(cluster, misc + kMiscChosen, C, c);
+#pragma unroll
+    for (int r = 0; r < kTkMaxCluster; ++r)
+      if ((uint32_t)r < rank) off += c[r];
+  }
+  // ---- chosen indices, ascending, at this CTA's offset
   {
-    const uint32_t wbits = tid < L::kWords ? bm[tid] : 0u;
-    const uint32_t pre = block_scan_incl(__popc(wbits), warp_s) - __popc(wbits);
     int32_t* o = out_idx + (int64_t)q * k;
     if (tid < L::kWords) {
       const int64_t li0 = base + 32 * (int64_t)tid;
@@ -511,7 +598,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
       for (int i = (int)need + tid; i < k; i += kTkThreads) o[i] = -1;
   }
   // keep every CTA's shared memory alive until all remote reads are done
-  if (!all) cluster.sync();
+  if (C > 1) cluster.sync();
 }
 
 static int topk_cluster_size(int64_t max_vis, int slice) {
@@ -525,41 +612,55 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
          al((size_t)n_query * (size_t)(max_vis > 0 ? max_vis : 1) * 8);
 }
 
+template <int PER>
+static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, const float* scores, int64_t ld,
+                                      const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx, bool* launched) {
+  *launched = false;
+  const void* fn = (const void*)topk_cluster_kernel<PER>;
+  const uint32_t smem = TkLayout<PER>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(n_query * csize));
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
+  if (e != cudaSuccess || max_clusters < 1) {
+    cudaGetLastError();  // cluster shape not schedulable here: the caller takes the global-memory path
+    return cudaSuccess;
+  }
+  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<PER>, scores, ld, n_vis, max_vis, k, out_idx);
+  if (e != cudaSuccess) return e;
+  *launched = true;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch) {
   if (n_query == 0) return cudaSuccess;
-  // one CTA per 16,384 scores (a 64K-context decode row is one CTA; 1M rows take 16)
-  const bool small = false;
-  const int slice = TkLayout<16>::kSlice;
-  const int csize = topk_cluster_size(max_vis, slice);
-  if (csize <= kTkMaxCluster) {
-    const void* fn = small ? (const void*)topk_cluster_kernel<4> : (const void*)topk_cluster_kernel<16>;
-    const uint32_t smem = small ? TkLayout<4>::SMEM : TkLayout<16>::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && csize > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  // a cluster of up to 8 CTAs per query, each holding 16,384 scores (a
+  // 64K-context decode row is one CTA), or 32,768 for rows up to 262,144
+  const int c16 = topk_cluster_size(max_vis, TkLayout<16>::kSlice);
+  const int c32 = topk_cluster_size(max_vis, TkLayout<32>::kSlice);
+  if (c32 <= kTkMaxCluster) {
+    bool launched = false;
+    cudaError_t e = c16 <= kTkMaxCluster
+                        ? launch_topk_cluster<16>(st, c16, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched)
+                        : launch_topk_cluster<32>(st, c32, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(n_query * csize));
-    cfg.blockDim = dim3(kTkThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
-    if (e == cudaSuccess && max_clusters > 0) {
-      if (small) e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<4>, scores, ld, n_vis, max_vis, k, out_idx);
-      else e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<16>, scores, ld, n_vis, max_vis, k, out_idx);
-      if (e != cudaSuccess) return e;
+    if (launched) {
       *n_launch += 1;
-      return cudaGetLastError();
+      return cudaSuccess;
     }
-    cudaGetLastError();  // cluster shape not schedulable here: use the global-memory path
   }
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* p = reinterpret_cast<char*>(ws);

@@ -244,7 +244,8 @@ def test_index_score(idx_heads, fp8):
 # ----------------------------------------------------------------------------- top-k
 
 @pytest.mark.parametrize("n,tie_levels,k", [(3000, 0, 512), (3000, 3, 512), (20000, 2, 512), (5000, 0, 2048),
-                                            (777, 0, 1), (262144, 0, 512), (262144, 40, 512), (100, 0, 512)])
+                                            (777, 0, 1), (262144, 0, 512), (262144, 40, 512), (100, 0, 512),
+                                            (20000, 1, 512), (40000, 0, 64), (300000, 0, 512), (300000, 7, 512)])
 def test_topk_bit_exact(n, tie_levels, k):
     from compressed_sparse_attention_gb300 import binding
     ctx = context()
