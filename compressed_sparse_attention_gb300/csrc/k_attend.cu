@@ -197,13 +197,29 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     } else {
       const uint8_t* kv = reinterpret_cast<const uint8_t*>(kvsrc);
       const uint8_t* ksc = (tile == 0) ? p.win_scale : p.pool_scale;
-      for (int r = warp; r < kTileRows; r += 4) {
-        const int64_t src = rows[r];
-        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (src >= 0) {
-          const uint4 codes = *reinterpret_cast<const uint4*>(kv + src * kDim + 16 * lane);
-          const float sc = ue8m0_value(ksc[src * (kDim / 32) + (lane >> 1)]);
-          const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+      // a warp takes rows warp, warp+4, ...; the loads of 8 rows are in
+      // flight together before any of them is converted
+      constexpr int kBatch = 8;
+#pragma unroll 1
+      for (int r0 = warp; r0 < kTileRows; r0 += 4 * kBatch) {
+        uint4 codes[kBatch];
+        uint8_t sb[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int64_t src = rows[r0 + 4 * j];
+          codes[j] = make_uint4(0u, 0u, 0u, 0u);
+          sb[j] = 0;
+          if (src >= 0) {
+            codes[j] = ldg_stream16(kv + src * kDim + 16 * lane);
+            sb[j] = ksc[src * (kDim / 32) + (lane >> 1)];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int r = r0 + 4 * j;
+          const float sc = ue8m0_value(sb[j]);
+          const uint32_t cw[4] = {codes[j].x, codes[j].y, codes[j].z, codes[j].w};
+          uint32_t o[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float2 a = e4m3x2_to_float2((uint16_t)(cw[k] & 0xFFFFu));
@@ -211,13 +227,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
             o[2 * k] = pack_bf16(a.x * sc, a.y * sc);
             o[2 * k + 1] = pack_bf16(c2.x * sc, c2.y * sc);
           }
-        }
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * lane + cc;  // bf16 chunk: channels 8c .. 8c+7
-          const uint32_t off = SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
-                               ((uint32_t)((c & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(sm + off) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * lane + cc;  // bf16 chunk: channels 8c .. 8c+7
+            const uint32_t off = SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
+                                 ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + off) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+          }
         }
       }
     }

@@ -1,0 +1,42 @@
+"""The decode forms of the CSA2 step at small sizes, against the oracle.
+
+With few queries the step runs the window tile beside top-k and spreads the
+selected tiles over several CTAs per query, whose partials a merge kernel
+combines; how many CTAs, and how many tiles each takes, depends on the number
+of queries and on k. With more queries the window and the selected tiles
+share one launch. These cases pick batch sizes and k so that each form is
+taken (one selected tile for k = 128, five for k = 640, one to four CTAs per
+query, the shared launch for 90 queries). Every query of a small batch, and a
+sample of a large one, is checked: scores, selection, and the step's
+attention output whenever the selection equals the oracle's.
+"""
+import pytest
+import torch
+
+from gpu_common import context, geometry, inv_freq, require_gpu
+from test_gpu_fullsize import Case, _check_query, _full_state, _step
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("n_seq,topk", [(1, 512), (3, 128), (5, 640), (40, 512), (70, 512), (90, 512)])
+def test_step_decode_forms(n_seq, topk):
+    require_gpu()
+    from compressed_sparse_attention_gb300 import binding
+    g = torch.Generator().manual_seed(900 + n_seq)
+    lens = tuple(int(x) for x in torch.randint(2600, 9000, (n_seq,), generator=g))
+    wl = Workload(f"forms_{n_seq}_{topk}", n_seq, lens, 4, seed=900 + n_seq + topk, topk=topk,
+                  value_std=1.0 / 22.6, outlier_frac=0.01)
+    ctx = context(topk=topk)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    case = Case(ctx, wl)
+    idx = torch.empty((wl.n_query, topk), dtype=torch.int32, device=DEV)
+    out, scores = _step(ctx, case, binding.MODE_FULL, idx)
+    sel = idx.cpu().numpy()
+    state = _full_state(ctx, case, geom, f)
+    sample = range(wl.n_query) if wl.n_query <= 8 else sorted({0, 1, wl.n_query // 2, wl.n_query - 1})
+    same = [_check_query(ctx, case, qi, geom, f, out, scores, sel, state, wl.name)[1] for qi in sample]
+    assert sum(same) >= len(same) - 1, "the step's selection differs from the oracle's on more than one query"
