@@ -226,6 +226,12 @@ class Copy:
                  tok_off=i["tok_off"], first_pos=i["first_pos"], norm_w=i["norm_w"], w_idx=i["w_idx"],
                  k_norm_w=i["k_norm_w"])
 
+    def attend_only(self, ctx, ws):
+        """Attention alone on this copy's last selection (decode or prefill)."""
+        i = self.inp
+        ctx.attend(self.wl.n_seq, i["q"], i["q_pos"], i["seq_of_q"], i["win_kv"], i.get("win_scale"), i["win_off"],
+                   None, i["pool_kv"], i.get("pool_scale"), i["pool_off"], self.idx, i["sink"], self.out, None, ws)
+
     def index_only(self, ctx):
         i = self.inp
         ctx.index_score(self.wl.n_seq, i["q_idx"], i["w_heads"], i["idx_keys"], i.get("idx_key_scale"),
@@ -294,6 +300,59 @@ def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
     if flags:
         raise RuntimeError(f"device error word 0x{flags:x} after timing")
     return dict(ms=ms, ms_max=ms_max, launches=launches_per_step, idx_ms=idx_ms, e2e=e2e)
+
+
+def attention_flops(wl) -> float:
+    """QK^T + PV flops of one step: per query, 2 x rows x 64 heads x 512 dims
+    for each product, rows = window rows + selected entries."""
+    tot = 0
+    for b in range(wl.n_seq):
+        for i in range(wl.n_query_per_seq):
+            t = wl.ctx_len[b] - wl.n_query_per_seq + i
+            rows = min(wl.window, t + 1) + min(wl.topk, (t + 1) // wl.m)
+            tot += 2 * 2 * rows * wl.n_heads * wl.head_dim
+    return float(tot)
+
+
+def run_prefill_extra(args, device, bf16_peak):
+    """The chunked-prefill workload: the whole step (graph), and the attention
+    alone (its QK^T and PV contractions against the bf16 tensor peak)."""
+    from compressed_sparse_attention_gb300 import binding
+    wl = PRESETS["prefill_4k_after_8k"]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads)
+    copies = [Copy(ctx, wl, c, device) for c in range(2)]  # q alone is 256 MB per copy, > L2
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for c in copies:
+            c.step(ctx)
+    torch.cuda.synchronize()
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the prefill workload")
+    ws = [binding.workspace(ctx.attend_workspace_size(wl.n_query), device) for _ in copies]
+    steps = max(3, min(args.steps, 20))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                fn(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_step = timed(lambda i: copies[i % 2].step(ctx))
+    ms_att = timed(lambda i: copies[i % 2].attend_only(ctx, ws[i % 2]))
+    flops = attention_flops(wl)
+    tf = flops / (ms_att / 1000.0) / 1e12
+    return {"workload": wl.name, "queries": wl.n_query, "tokens_per_s": wl.n_query / (ms_step / 1000.0),
+            "ms_per_step": ms_step, "attend_ms": ms_att, "attend_flops": flops,
+            "roofline_attend": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                                "frac": tf / bf16_peak, "peak_kind": "bf16 dense, burst (kernel timed alone)"}}
 
 
 def run_e2e(args, ctx, copies, stream, device, wl):
@@ -488,6 +547,10 @@ def main():
                                 "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
         except Exception as ex:  # reported, never silently dropped
             line["extra_1m"] = {"error": repr(ex)[:300]}
+        try:
+            line["extra_prefill"] = run_prefill_extra(args, device, bf16_burst)
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_prefill"] = {"error": repr(ex)[:300]}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
         print(json.dumps(line))

@@ -305,7 +305,7 @@ static csa2_status attend_params(csa2_ctx* ctx, int32_t n_seq, int32_t n_query, 
   if (!q || !q_pos || !seq_of_q || !win_kv || !win_off || !sink || !out ||
       (topk_idx && (!pool_kv || !pool_off)) || (fp8 && (!win_scale || (topk_idx && !pool_scale))))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: null pointer");
-  if (!aligned16(q) || !aligned16(win_kv) || (pool_kv && !aligned16(pool_kv)) || (reinterpret_cast<uintptr_t>(out) & 3))
+  if (!aligned16(q) || !aligned16(win_kv) || (pool_kv && !aligned16(pool_kv)) || !aligned16(out))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: misaligned buffer");
   const size_t need = csa2_attend_workspace_size(ctx, n_query);
   csa2_status s = check_ws(ctx, ws, ws_bytes, topk_idx ? need : 0);

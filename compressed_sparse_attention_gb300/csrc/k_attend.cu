@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     l_run[tid] = 0.f;
   }
   float2* rope_tab = reinterpret_cast<float2*>(sm + SM_ROPE);
+  const float sink_l2 = (p.direct && tid < kHeads) ? p.sink[tid] * 1.4426950408889634f : 0.f;  // used at the end
   if (tid < p.rp.pairs) {
     float c = 1.f, sn = 0.f;
     if (q_ok) rope_cs(p.rp, tid, t, c, sn);
@@ -152,12 +153,23 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
   // no selection (window-only call): the pool arguments may be NULL
   const int64_t plen = (q_ok && p.pool_off != nullptr) ? (p.pool_off[b + 1] - p.pool_off[b]) : 0;
+  // selection entry of this thread's row in selected tile `tile` (-1 past k):
+  // each tile's entry is loaded one tile ahead
+  auto sel_entry = [&](int tile) -> int32_t {
+    const int col = (tile - 1) * kTileRows + tid;
+    return (tile >= 1 && tile < tile_end && col < p.topk && p.topk_idx != nullptr)
+               ? p.topk_idx[(int64_t)qi * p.topk + col]
+               : -1;
+  };
+  int32_t j_next = sel_entry(tile_begin);
 
   for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row)
     {
       const int r = tid;
       int64_t src = -1;
+      const int32_t j_cur = j_next;
+      j_next = sel_entry(tile + 1);
       if (tile == 0) {
         const int64_t pos = lo_eff + r;
         if (pos <= t && r < p.window) {
@@ -168,12 +180,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
           }
         }
       } else {
-        const int col = (tile - 1) * kTileRows + r;
-        if (col < p.topk && p.topk_idx != nullptr) {
-          const int32_t j = p.topk_idx[(int64_t)qi * p.topk + col];
-          if (j >= 0 && j < plen) src = p.pool_off[b] + j;
-          else if (j != -1) set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
-        }
+        const int32_t j = j_cur;
+        if (j >= 0 && j < plen) src = p.pool_off[b] + j;
+        else if (j != -1) set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
       }
       rows[r] = src;
     }
@@ -303,7 +312,17 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         s[32 + k] = valid ? __uint_as_float(r1[k]) * p.scale_log2 : -INFINITY;
       }
     }
-    {
+    // After a CTA's first tile the per-head max is needed only if some score
+    // exceeds its head's reference by more than 2^8 (see below); otherwise
+    // the reference stays and the max reduction is skipped.
+    bool need_max = (tile == tile_begin);
+    if (!need_max) {
+      bool over = false;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) over |= s[k] > m_run[k] + 8.f;
+      need_max = __syncthreads_or(over) != 0;
+    }
+    if (need_max) {
       float v[64];
 #pragma unroll
       for (int k = 0; k < 64; ++k) v[k] = s[k];
@@ -314,10 +333,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       red[warp * 64 + h0 + 1] = a1;
     }
     __syncthreads();
-    if (tid < kHeads) {
+    if (!need_max) {
+      if (tid < kHeads) alpha[tid] = 1.f;  // m_use and m_run stand
+    } else if (tid < kHeads) {
       const float tmax = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+      // the reference max of a head moves only when a tile's max exceeds it
+      // by more than 2^8: P = 2^(s - m) stays below 256 and the softmax is
+      // the same for any reference, so most tiles skip the O rescale
       const float mo = m_run[tid];
-      const float mn = fmaxf(mo, tmax);
+      const float mn = (mo == -INFINITY || tmax > mo + 8.f) ? fmaxf(mo, tmax) : mo;
       const float mu = (mn == -INFINITY) ? 0.f : mn;
       const float al = (mo == -INFINITY) ? 1.f : exp2f(mo - mu);
       m_use[tid] = mu;
@@ -405,7 +429,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   if (p.direct) {
     // final normalisation with the sink: fo = e^{m - M} / den, den = l e^{m - M} + e^{sink - M}
     if (tid < kHeads) {
-      const float sk = p.sink[tid] * 1.4426950408889634f;
+      const float sk = sink_l2;
       const float mr = have_o ? m_run[tid] : -INFINITY;
       const float M = fmaxf(mr, sk);
       float fo = 0.f, lse = -INFINITY;
@@ -420,6 +444,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     }
     __syncthreads();
     uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
+    float al_all[64];  // before any store: no reloads
+#pragma unroll
+    for (int k = 0; k < 64; ++k) al_all[k] = alpha[k];
     for (int mt = 0; mt < 4; ++mt) {
       const int d = 128 * mt + 32 * warp + lane;
       float cs = 1.f, sn = 0.f;
@@ -429,24 +456,37 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         cs = cs2.x;
         sn = cs2.y;
       }
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        if (have_o) {
-          tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
-          tmem_wait_ld();
-        } else {
+      // both 32-head halves of this dim come out of tensor memory together
+      uint32_t ra[32], rb[32];
+      if (have_o) {
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt) + lane_base, ra);
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32) + lane_base, rb);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = 0u;
-        }
+        for (int k = 0; k < 32; ++k) ra[k] = rb[k] = 0u;
+      }
+      auto emit = [&](const uint32_t (&r)[32], int hh) {
+        float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int h = 32 * hh + k;
-          float v = __uint_as_float(r[k]) * alpha[h];
-          const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-          if (rope) v = (d & 1) ? (v * cs - partner * sn) : (v * cs + partner * sn);
-          out[(int64_t)h * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          v[k] = __uint_as_float(r[k]) * al_all[32 * hh + k];
+          const float partner = __shfl_xor_sync(0xffffffffu, v[k], 1);
+          if (rope) v[k] = (d & 1) ? (v[k] * cs - partner * sn) : (v[k] * cs + partner * sn);
         }
-      }
+        // lanes d, d+1 swap halves so that each stores two adjacent dims of
+        // one head: the even lane head k, the odd lane head k+1
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const bool odd = (d & 1) != 0;
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[k] : v[k + 1], 1);
+          const int h = 32 * hh + k + (odd ? 1 : 0);
+          const uint32_t w = odd ? pack_bf16(recv, v[k + 1]) : pack_bf16(v[k], recv);
+          *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + (d & ~1)) = w;
+        }
+      };
+      emit(ra, 0);
+      emit(rb, 1);
     }
   } else {
     // unnormalised partial O^T and (m, l) for the merge
@@ -457,13 +497,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       float* wo = p.ws_o + slot * kHeads * kDim;
       for (int mt = 0; mt < 4; ++mt) {
         const int d = 128 * mt + 32 * warp + lane;
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
-          tmem_wait_ld();
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt) + lane_base, ra);
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32) + lane_base, rb);
+        tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) wo[(int64_t)(32 * hh + k) * kDim + d] = __uint_as_float(r[k]);
-        }
+        for (int k = 0; k < 32; ++k) wo[k * kDim + d] = __uint_as_float(ra[k]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) wo[(32 + k) * kDim + d] = __uint_as_float(rb[k]);
       }
     }
   }

@@ -228,7 +228,8 @@ csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float*
  *            natural-log denominator (nullable)
  * QK^T and PV run on tcgen05 tensor cores with bf16 operands (P rounded to
  * bf16) and fp32 accumulation in tensor memory.
- *   workspace of csa2_attend_workspace_size(ctx, n_query) bytes */
+ *   workspace of csa2_attend_workspace_size(ctx, n_query) bytes
+ * q, win_kv, pool_kv and out must be 16-byte aligned (CSA2_ERR_INVALID_ARG). */
 size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query);
 csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
                         const uint16_t* q, const int64_t* q_pos, const int32_t* seq_of_q,
