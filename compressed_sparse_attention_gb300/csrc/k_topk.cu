@@ -255,23 +255,30 @@ namespace cg = cooperative_groups;
 //   1. the cluster's smallest and largest key give the prefix that all keys
 //      share; the digits start below it, so that the first histogram already
 //      spreads the keys (scores of one row share most exponent bits);
-//   2. at most three 12-bit MSD digit levels: each histograms the keys that
-//      match the digits chosen so far, sums the bins over the cluster through
-//      distributed shared memory and picks the digit holding the k-th largest
-//      key. When the picked bin holds exactly the keys still needed the
-//      search ends: the chosen set is every key whose prefix is at or above
-//      the picked one;
-//   3. otherwise the full key T is known, with the number of keys equal to T
-//      still to take; they are taken lowest index first, each CTA taking what
-//      remains after the ties of the CTAs before it (CTAs are in index order);
+//   2. MSD digit levels of up to 12 bits: each histograms the keys that match
+//      the digits chosen so far and picks the digit that holds the k-th
+//      largest key; in a cluster in two stages, first among 64 blocks of
+//      bins, then among the bins of the chosen block, each summed over the
+//      cluster through distributed shared memory (a one-CTA row scans its
+//      own bins at once);
+//   3. the search ends as soon as the picked bin
+//      - holds exactly the keys still needed: the chosen set is every key
+//        whose prefix is at or above the picked one; or
+//      - (in a cluster) holds at most 256 keys: they are gathered from the
+//        whole cluster and each is ranked against the others by (key
+//        descending, index ascending), which takes ties lowest index first; or
+//      - is a full 32-bit key T held by more keys: the keys equal to T still
+//        needed are taken lowest index first, each CTA taking what remains
+//        after the ties of the CTAs before it (CTAs are in index order);
 //   4. every CTA writes its chosen indices in ascending order at its offset
 //      (the chosen counts of the CTAs before it) from a ballot bitmap.
-// No candidate list, no sort, and no CTA works for the others.
 // ---------------------------------------------------------------------------
 constexpr int kTkThreads = 1024;
 constexpr int kTkMaxCluster = 8;
 constexpr int kTkDigit = 12;
 constexpr int kTkBins = 1 << kTkDigit;
+constexpr int kTkBlocks = 64;   // coarse blocks of a level's bins
+constexpr int kTkCand = 256;    // candidates ranked directly
 
 template <int PER>
 struct TkLayout {
@@ -279,21 +286,33 @@ struct TkLayout {
   static constexpr int kWords = kSlice / 32;                 // at most one per thread
   static constexpr uint32_t KEYS = 0;                        // [kSlice]
   static constexpr uint32_t HIST = KEYS + kSlice * 4;        // [3 levels][4096]
-  static constexpr uint32_t BM = HIST + 3 * kTkBins * 4;     // chosen bitmap
+  static constexpr uint32_t BLK = HIST + 3 * kTkBins * 4;    // [3 levels][64] block sums of this CTA
+  static constexpr uint32_t FINE = BLK + 3 * kTkBlocks * 4;  // [64] cluster-summed bins of the picked block
+  static constexpr uint32_t COARSE = FINE + 64 * 4;          // [64] cluster-summed block sums
+  static constexpr uint32_t BM = COARSE + kTkBlocks * 4;     // chosen bitmap
   static constexpr uint32_t TB = BM + kWords * 4;            // tie bitmap
   static constexpr uint32_t TP = TB + kWords * 4;            // ties before each word
-  static constexpr uint32_t MISC = TP + kWords * 4;
+  static constexpr uint32_t XB = TP + kWords * 4;            // candidates chosen by rank
+  static constexpr uint32_t CKEY = XB + kWords * 4;          // [256] this CTA's candidates: key
+  static constexpr uint32_t CIDX = CKEY + kTkCand * 4;       // [256] and row index
+  static constexpr uint32_t AKEY = CIDX + kTkCand * 4;       // [256] the cluster's candidates: key
+  static constexpr uint32_t AIDX = AKEY + kTkCand * 4;       // [256] and row index
+  static constexpr uint32_t MISC = AIDX + kTkCand * 4;
   static constexpr uint32_t SMEM = MISC + 1024;
   static_assert(kWords <= kTkThreads, "one bitmap word per thread");
 };
 
 // misc words
-constexpr int kMiscRes = 32;     // [32..34] picked digit, count above it, count in it
-constexpr int kMiscMin = 36;     // smallest valid key here
-constexpr int kMiscMax = 37;     // largest valid key here
-constexpr int kMiscGt = 38;      // keys > T here
-constexpr int kMiscTie = 39;     // keys == T here
-constexpr int kMiscChosen = 40;  // chosen keys here
+constexpr int kMiscRes = 32;      // [32..34] picked digit, count above it, count in it
+constexpr int kMiscMin = 36;      // smallest valid key here
+constexpr int kMiscMax = 37;      // largest valid key here
+constexpr int kMiscGt = 38;       // keys > T here
+constexpr int kMiscTie = 39;      // keys == T here
+constexpr int kMiscChosen = 40;   // chosen keys here
+constexpr int kMiscCand = 41;     // candidates here
+constexpr int kMiscBlk = 42;      // [42..43] picked block, count above it
+constexpr int kMiscWarpMin = 64;  // [64..95] per-warp smallest key
+constexpr int kMiscWarpMax = 96;  // [96..127] per-warp largest key
 
 // inclusive block-wide scan of one value per thread (1024 threads); warp_s[31] = total
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s) {
@@ -319,12 +338,27 @@ __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s
   return v + (warp > 0 ? warp_s[warp - 1] : 0u);
 }
 
+// `local` in CTA r of the cluster; a plain shared-memory address when the
+// cluster is one CTA (distributed shared memory is slower even for oneself)
+template <typename T>
+__device__ __forceinline__ T* tk_at(cg::cluster_group& cluster, T* local, uint32_t r, uint32_t C) {
+  return C == 1 ? local : cluster.map_shared_rank(local, r);
+}
+
 // u32 at `local` in every CTA r < C of the cluster; all loads issued at once
 __device__ __forceinline__ void cluster_gather_u32(cg::cluster_group& cluster, const uint32_t* local, uint32_t C,
                                                    uint32_t (&v)[kTkMaxCluster]) {
 #pragma unroll
-  for (int r = 0; r < kTkMaxCluster; ++r)
-    v[r] = (uint32_t)r < C ? *cluster.map_shared_rank(local, (unsigned)r) : 0u;
+  for (int r = 0; r < kTkMaxCluster; ++r) v[r] = (uint32_t)r < C ? *tk_at(cluster, local, (uint32_t)r, C) : 0u;
+}
+
+__device__ __forceinline__ uint32_t cluster_sum_u32(cg::cluster_group& cluster, const uint32_t* local, uint32_t C) {
+  uint32_t v[kTkMaxCluster];
+  cluster_gather_u32(cluster, local, C, v);
+  uint32_t s = 0;
+#pragma unroll
+  for (int r = 0; r < kTkMaxCluster; ++r) s += v[r];
+  return s;
 }
 
 __device__ __forceinline__ void tk_sync(cg::cluster_group& cluster, uint32_t C) {
@@ -332,47 +366,116 @@ __device__ __forceinline__ void tk_sync(cg::cluster_group& cluster, uint32_t C) 
   else __syncthreads();
 }
 
-// Pick the digit holding the need-th largest key of a level with nbins bins
-// (a power of two, at least 2): thread t sums bins nbins-1-4t .. nbins-4-4t
-// over the cluster, a block scan runs from the top digit down, and the thread
-// whose range holds the need-th key leaves (digit, count above, count in it)
-// in res. Ends with the block synchronised.
-__device__ __forceinline__ void tk_pick_digit(cg::cluster_group& cluster, uint32_t C, const uint32_t* h,
-                                              uint32_t nbins, uint32_t need, uint32_t* warp_s, uint32_t* res) {
-  const int tid = threadIdx.x;
-  uint32_t c[4] = {0u, 0u, 0u, 0u};
-  const int top = (int)nbins - 1 - 4 * tid;  // highest bin of this thread
-  if (top >= 3) {
-    uint4 v[kTkMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kTkMaxCluster; ++r)
-      if ((uint32_t)r < C) v[r] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(h + top - 3, (unsigned)r));
-#pragma unroll
-    for (int r = 0; r < kTkMaxCluster; ++r) {
-      if ((uint32_t)r < C) {
-        c[0] += v[r].w;
-        c[1] += v[r].z;
-        c[2] += v[r].y;
-        c[3] += v[r].x;
-      }
+// The digit holding the need-th largest key of a level whose local histogram
+// h has nb = 2^w bins (bin = digit). Stage 1 sums this CTA's 64 block sums
+// (blk) over the cluster and picks a block; stage 2 sums that block's bins
+// over the cluster and picks the bin. Leaves (digit, count above, count in
+// it) in misc[kMiscRes..]; called by every thread of every CTA of the
+// cluster, ends with the block synchronised.
+__device__ __noinline__ void tk_pick(cg::cluster_group& cluster, uint32_t C, const uint32_t* h, uint32_t* blk,
+                                     uint32_t* coarse, uint32_t* fine, int w, uint32_t need, uint32_t* misc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nb = 1 << w;
+  const int n_blk = nb < kTkBlocks ? nb : kTkBlocks;
+  const int bpb = nb / n_blk;  // bins per block, a power of two up to 64
+  __syncthreads();  // this CTA's histogram is complete
+  if (bpb >= 4) {
+    const int g = bpb / 4;  // threads per block: 1 .. 16
+    uint32_t v = 0;
+    if (4 * tid < nb) {
+      const uint4 x = *reinterpret_cast<const uint4*>(h + 4 * tid);
+      v = x.x + x.y + x.z + x.w;
     }
-  } else if (top >= 0) {
-    for (uint32_t r = 0; r < C; ++r) {
-      const uint32_t* rh = cluster.map_shared_rank(h, r);
-      for (int j = 0; j <= top; ++j) c[j] += rh[top - j];
+    for (int o = 1; o < g; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (4 * tid < nb && (tid & (g - 1)) == 0) blk[tid / g] = v;
+  } else if (tid < n_blk) {
+    uint32_t v = 0;
+    for (int j = 0; j < bpb; ++j) v += h[tid * bpb + j];
+    blk[tid] = v;
+  }
+  tk_sync(cluster, C);  // every CTA's histogram and block sums are complete
+  if (tid < n_blk) coarse[tid] = cluster_sum_u32(cluster, blk + tid, C);
+  __syncthreads();
+  // stage 1 (warp 0): lane l takes blocks n_blk-1-2l and n_blk-2-2l
+  if (warp == 0) {
+    const int b0 = n_blk - 1 - 2 * lane, b1 = b0 - 1;
+    const uint32_t c0 = b0 >= 0 ? coarse[b0] : 0u, c1 = b1 >= 0 ? coarse[b1] : 0u;
+    const uint32_t sum = c0 + c1;
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < need && need <= incl) {
+      const bool first = excl + c0 >= need;
+      misc[kMiscBlk] = (uint32_t)(first ? b0 : b1);
+      misc[kMiscBlk + 1] = first ? excl : excl + c0;
     }
   }
-  const uint32_t sum = c[0] + c[1] + c[2] + c[3];
+  __syncthreads();
+  const int bsel = (int)misc[kMiscBlk];
+  const uint32_t above_blk = misc[kMiscBlk + 1];
+  // stage 2: the picked block's bins, top first
+  if (tid < bpb) fine[tid] = cluster_sum_u32(cluster, h + bsel * bpb + (bpb - 1 - tid), C);
+  __syncthreads();
+  if (warp == 0) {
+    const int i0 = 2 * lane, i1 = i0 + 1;  // positions from the top of the block
+    const uint32_t c0 = i0 < bpb ? fine[i0] : 0u, c1 = i1 < bpb ? fine[i1] : 0u;
+    const uint32_t sum = c0 + c1;
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t excl = incl - sum;
+    const uint32_t need2 = need - above_blk;
+    if (excl < need2 && need2 <= incl) {
+      const bool first = excl + c0 >= need2;
+      const int pos = first ? i0 : i1;
+      misc[kMiscRes] = (uint32_t)(bsel * bpb + (bpb - 1 - pos));
+      misc[kMiscRes + 1] = above_blk + (first ? excl : excl + c0);
+      misc[kMiscRes + 2] = first ? c0 : c1;
+    }
+  }
+  __syncthreads();
+}
+
+// One-CTA form of the pick (no cluster): thread t owns bins nb-1-4t ..
+// nb-4-4t of the local histogram and a block scan runs from the top digit
+// down. Same result in misc[kMiscRes..]; ends with the block synchronised.
+__device__ __noinline__ void tk_pick_local(const uint32_t* h, int w, uint32_t need, uint32_t* warp_s,
+                                           uint32_t* misc) {
+  const int tid = threadIdx.x;
+  const int nb = 1 << w;
+  __syncthreads();  // the histogram is complete
+  uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+  const int top = nb - 1 - 4 * tid;  // highest bin of this thread
+  if (top >= 3) {
+    const uint4 v = *reinterpret_cast<const uint4*>(h + top - 3);
+    c0 = v.w;
+    c1 = v.z;
+    c2 = v.y;
+    c3 = v.x;
+  } else if (top >= 0) {
+    c0 = h[top];
+    if (top >= 1) c1 = h[top - 1];
+    if (top >= 2) c2 = h[top - 2];
+  }
+  const uint32_t sum = c0 + c1 + c2 + c3;
   const uint32_t incl = block_scan_incl(sum, warp_s);
   const uint32_t excl = incl - sum;
   if (excl < need && need <= incl) {
+    const uint32_t c[4] = {c0, c1, c2, c3};
     uint32_t run = excl;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (run + c[j] >= need) {
-        res[0] = (uint32_t)(top - j);
-        res[1] = run;
-        res[2] = c[j];
+        misc[kMiscRes] = (uint32_t)(top - j);
+        misc[kMiscRes + 1] = run;
+        misc[kMiscRes + 2] = c[j];
         break;
       }
       run += c[j];
@@ -380,6 +483,8 @@ __device__ __forceinline__ void tk_pick_digit(cg::cluster_group& cluster, uint32
   }
   __syncthreads();
 }
+
+enum TkMode { kTkAll = 0, kTkExact = 1, kTkCandRank = 2, kTkTies = 3 };
 
 template <int PER>
 __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float* __restrict__ scores, int64_t ld,
@@ -390,12 +495,19 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   extern __shared__ __align__(16) unsigned char tk_smem[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(tk_smem + L::KEYS);
   uint32_t* hist = reinterpret_cast<uint32_t*>(tk_smem + L::HIST);
+  uint32_t* blk = reinterpret_cast<uint32_t*>(tk_smem + L::BLK);
+  uint32_t* fine = reinterpret_cast<uint32_t*>(tk_smem + L::FINE);
+  uint32_t* coarse = reinterpret_cast<uint32_t*>(tk_smem + L::COARSE);
   uint32_t* bm = reinterpret_cast<uint32_t*>(tk_smem + L::BM);
   uint32_t* tb = reinterpret_cast<uint32_t*>(tk_smem + L::TB);
   uint32_t* tp = reinterpret_cast<uint32_t*>(tk_smem + L::TP);
+  uint32_t* xb = reinterpret_cast<uint32_t*>(tk_smem + L::XB);
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(tk_smem + L::CKEY);
+  uint32_t* cidx = reinterpret_cast<uint32_t*>(tk_smem + L::CIDX);
+  uint32_t* akey = reinterpret_cast<uint32_t*>(tk_smem + L::AKEY);
+  uint32_t* aidx = reinterpret_cast<uint32_t*>(tk_smem + L::AIDX);
   uint32_t* misc = reinterpret_cast<uint32_t*>(tk_smem + L::MISC);
   uint32_t* warp_s = misc;
-  uint32_t* res = misc + kMiscRes;
 
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t rank = cluster.block_rank();
@@ -405,10 +517,12 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   const int nv = (int)min((int64_t)max(n_vis[q], 0), max_vis);
   const int64_t base = (int64_t)rank * L::kSlice;
   const int cnt = (int)max((int64_t)0, min((int64_t)L::kSlice, (int64_t)nv - base));
-  const uint32_t need = (uint32_t)max(0, min(k, nv));
+  const uint32_t need = (uint32_t)min(k, nv);
   const bool all = (uint32_t)nv <= need;  // every visible entry is chosen (uniform over the cluster)
 
-  // ---- slice -> keys; histogram and counter init meanwhile
+  // ---- slice -> keys (with this thread's smallest and largest); histograms,
+  // rank bitmap and counters zeroed meanwhile
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   {
     const float* row = scores + (int64_t)q * ld + base;
     float v[PER];
@@ -419,42 +533,55 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
     }
     uint4* h4 = reinterpret_cast<uint4*>(hist);
     for (int i = tid; i < 3 * kTkBins / 4; i += kTkThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < L::kWords) xb[tid] = 0u;
     if (tid == 0) {
-      misc[kMiscMin] = 0xFFFFFFFFu;
-      misc[kMiscMax] = 0u;
       misc[kMiscGt] = 0u;
       misc[kMiscTie] = 0u;
+      misc[kMiscCand] = 0u;
     }
 #pragma unroll
-    for (int u = 0; u < PER; ++u) keys[u * kTkThreads + tid] = score_key(v[u]);
+    for (int u = 0; u < PER; ++u) {
+      const uint32_t x = score_key(v[u]);
+      keys[u * kTkThreads + tid] = x;
+      if (u * kTkThreads + tid < cnt) {
+        kmin = min(kmin, x);
+        kmax = max(kmax, x);
+      }
+    }
   }
   __syncthreads();
 
-  // state after the search: chosen = keys whose top (32 - shift) bits are > P,
-  // plus, when `exact`, those equal to P; otherwise (shift == 0) the first
-  // take_t keys equal to T = P in index order
+  // state after the search: keys whose top (32 - shift) bits are > P are
+  // chosen; of those equal to P: all (exact), the ones marked in xb (rank),
+  // or, with shift == 0, the first take_t in index order (ties)
   uint32_t P = 0, take_t = 0;
   int shift = 32;
-  bool exact = true;
+  int mode = all ? kTkAll : kTkTies;
   if (!all) {
     // ---- common prefix of the cluster's keys
-    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      if (u * kTkThreads + tid < cnt) {
-        const uint32_t x = keys[u * kTkThreads + tid];
-        mn = min(mn, x);
-        mx = max(mx, x);
-      }
-    }
+    uint32_t mn = kmin, mx = kmax;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     if (lane == 0) {
-      atomicMin(&misc[kMiscMin], mn);
-      atomicMax(&misc[kMiscMax], mx);
+      misc[kMiscWarpMin + warp] = mn;
+      misc[kMiscWarpMax + warp] = mx;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      mn = misc[kMiscWarpMin + lane];
+      mx = misc[kMiscWarpMax + lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        misc[kMiscMin] = mn;
+        misc[kMiscMax] = mx;
+      }
     }
     tk_sync(cluster, C);
     {
@@ -475,7 +602,6 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
     shift = diff ? 32 - __clz(diff) : 0;  // bits below the shared prefix
     P = shift >= 32 ? 0u : (mx >> shift);
     uint32_t rem = need;
-    exact = false;
     // ---- digit levels below the prefix
 #pragma unroll 1
     for (int lvl = 0; shift > 0; ++lvl) {
@@ -489,29 +615,108 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
         const bool ok = u * kTkThreads + tid < cnt && (shift >= 32 || (x >> shift) == P);
         if (ok) atomicAdd(&h[(x >> sh) & dmask], 1u);
       }
-      tk_sync(cluster, C);
-      tk_pick_digit(cluster, C, h, 1u << w, rem, warp_s, res);
-      P = (shift >= 32 ? 0u : (P << w)) | res[0];
-      rem -= res[1];
-      const uint32_t at = res[2];
+      if (C == 1) tk_pick_local(h, w, rem, warp_s, misc);
+      else tk_pick(cluster, C, h, blk + kTkBlocks * lvl, coarse, fine, w, rem, misc);
+      P = (shift >= 32 ? 0u : (P << w)) | misc[kMiscRes];
+      rem -= misc[kMiscRes + 1];
+      const uint32_t at = misc[kMiscRes + 2];
       shift = sh;
-      __syncthreads();  // res is rewritten by the next level
+      __syncthreads();  // misc[kMiscRes..] is rewritten by the next level
       if (at == rem) {
-        exact = true;
+        mode = kTkExact;
+        break;
+      }
+      // across a cluster a few candidates are ranked at once; one CTA goes
+      // on with another level, which is cheaper there
+      if (C > 1 && at <= (uint32_t)kTkCand) {
+        mode = kTkCandRank;
         break;
       }
     }
     take_t = rem;
   }
-  // ---- ties at T (shift == 0, not exact): counts above T and at T here,
-  // exchanged once across the cluster; this CTA may take the ties that the
-  // CTAs before it leave, lowest index first
+  // ---- rank path: the keys whose top bits equal P (at most 256 over the
+  // cluster) are gathered and each CTA ranks its own against all of them
+  if (mode == kTkCandRank) {
+    // candidate bitmap (word w = u*32 + warp), then slots in index order from
+    // a block scan of the words' counts; no shared counter
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int li = u * kTkThreads + tid;
+      const uint32_t x = keys[li];
+      const uint32_t bal = __ballot_sync(0xffffffffu, li < cnt && (x >> shift) == P);
+      if (lane == 0) tb[u * 32 + warp] = bal;
+    }
+    __syncthreads();
+    {
+      const uint32_t cw = tid < L::kWords ? tb[tid] : 0u;  // thread tid owns word tid
+      uint32_t slot = block_scan_incl(__popc(cw), warp_s) - __popc(cw);
+      if (tid == 0) misc[kMiscCand] = warp_s[31];
+      uint32_t bits = cw;
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        if (slot < (uint32_t)kTkCand) {
+          const uint32_t li = 32u * (uint32_t)tid + (uint32_t)bit;
+          ckey[slot] = keys[li];
+          cidx[slot] = (uint32_t)base + li;
+        }
+        ++slot;
+      }
+    }
+    tk_sync(cluster, C);  // every CTA's candidate list is complete
+    uint32_t cn[kTkMaxCluster];
+    cluster_gather_u32(cluster, misc + kMiscCand, C, cn);
+    uint32_t n_all = 0, start = 0, src = 0;
+#pragma unroll
+    for (int r = 0; r < kTkMaxCluster; ++r) {
+      const uint32_t c = min(cn[r], (uint32_t)kTkCand);
+      if ((uint32_t)tid >= n_all && (uint32_t)tid < n_all + c) {
+        src = (uint32_t)r;
+        start = n_all;
+      }
+      n_all += c;
+    }
+    n_all = min(n_all, (uint32_t)kTkCand);
+    if ((uint32_t)tid < n_all) {
+      const uint32_t j = (uint32_t)tid - start;
+      akey[tid] = *tk_at(cluster, ckey + j, src, C);
+      aidx[tid] = *tk_at(cluster, cidx + j, src, C);
+    }
+    __syncthreads();
+    const uint32_t n_mine = min(misc[kMiscCand], (uint32_t)kTkCand);
+    {
+      // four threads per candidate (1024 / 256), each over every fourth
+      // entry; the four partial ranks meet by shuffles within the warp
+      const uint32_t i = (uint32_t)tid >> 2, part = (uint32_t)tid & 3u;
+      const bool mine = i < n_mine;
+      const uint32_t kx = mine ? ckey[i] : 0u, ix = mine ? cidx[i] : 0u;
+      uint32_t rk = 0;
+      if (mine) {
+#pragma unroll 4
+        for (uint32_t j = part; j < n_all; j += 4) {
+          const uint32_t ky = akey[j], iy = aidx[j];
+          rk += (ky > kx || (ky == kx && iy < ix)) ? 1u : 0u;
+        }
+      }
+      rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+      rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+      if (mine && part == 0 && rk < take_t) {
+        const uint32_t li = ix - (uint32_t)base;
+        atomicOr(&xb[li >> 5], 1u << (li & 31u));
+      }
+    }
+    __syncthreads();
+  }
+  // ---- ties at T = P (shift == 0, more ties than 256): counts above T and
+  // at T here, exchanged once across the cluster; this CTA may take the ties
+  // that the CTAs before it leave, lowest index first
   uint32_t quota = 0, off = 0;
   bool off_known = false;
-  if (all) {
+  if (mode == kTkAll) {
     off = (uint32_t)base;  // every earlier CTA is full and fully chosen
     off_known = true;
-  } else if (!exact) {
+  } else if (mode == kTkTies) {
     uint32_t ngt = 0, nt = 0;
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
@@ -556,10 +761,12 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
     const int w = u * 32 + warp;
     const uint32_t x = keys[li];
     bool chosen;
-    if (all) {
+    if (mode == kTkAll) {
       chosen = li < cnt;
-    } else if (exact) {
+    } else if (mode == kTkExact) {
       chosen = li < cnt && (x >> shift) >= P;
+    } else if (mode == kTkCandRank) {
+      chosen = li < cnt && ((x >> shift) > P || ((xb[w] >> lane) & 1u) != 0u);
     } else {
       chosen = li < cnt && x > P;
       if (li < cnt && x == P && quota > 0)
