@@ -253,13 +253,19 @@ def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
     flags, _ = ctx.check()
     if flags:
         raise RuntimeError(f"device error word 0x{flags:x} on the bench workload")
-    # one CUDA graph per copy
+    # one CUDA graph per copy, and one that runs the N_COPIES steps in turn
+    # (as a serving loop captures consecutive layers): the timed region
+    # replays the latter, so the graph launch cost is shared by four steps
     graphs = []
     for c in copies:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             c.step(ctx)
         graphs.append(g)
+    g_all = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for c in copies:
+            c.step(ctx)
     torch.cuda.synchronize()
     for i in range(max(args.warmup, 3)):
         graphs[i % N_COPIES].replay()
@@ -272,8 +278,10 @@ def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
         sampler.mark()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(args.steps):
-            graphs[i % N_COPIES].replay()
+        for _ in range(args.steps // N_COPIES):
+            g_all.replay()
+        for i in range(args.steps % N_COPIES):
+            graphs[i].replay()
         e1.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -520,7 +528,7 @@ def main():
                    "topk": wl.topk, "window": wl.window, "heads": "64x512", "indexer": f"{wl.idx_heads}x128",
                    "kv": "fp8_e4m3_ue8m0_b32" if wl.kv_fp8 else "bf16",
                    "l2": f"{N_COPIES} rotating input copies ({N_COPIES * step_bytes / 1e6:.0f} MB > 129 MB L2)",
-                   "graph": "one CUDA graph per step"},
+                   "graph": f"one CUDA graph per {N_COPIES} consecutive steps (one per input copy)"},
         "hbm_gbs": gbs, "hbm_frac": gbs / hbm, "step_algorithmic_bytes": step_bytes,
         "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": idx_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": idx_gbs / hbm,
