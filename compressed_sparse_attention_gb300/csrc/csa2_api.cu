@@ -238,9 +238,14 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: fp8 keys need their scales");
   if (!aligned16(q_idx) || !aligned16(idx_keys) || (idx_key_scale && (reinterpret_cast<uintptr_t>(idx_key_scale) & 3)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: misaligned buffer");
-  cudaError_t e = csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, c.idx_key_format == CSA2_KV_FP8_E4M3_B32,
-                                           n_query, n_seq, max_vis, q_idx, w_heads, idx_keys, idx_key_scale, pool_off,
-                                           seq_of_q, n_vis, scores, ld, ctx->d_flags);
+  const int fp8 = c.idx_key_format == CSA2_KV_FP8_E4M3_B32;
+  cudaError_t e =
+      csa2::index_tc_suited(fp8, n_query, n_seq, c.idx_heads)
+          ? csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
+                                        reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis,
+                                        scores, ld, ctx->d_flags)
+          : csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, fp8, n_query, n_seq, max_vis, q_idx, w_heads,
+                                     idx_keys, idx_key_scale, pool_off, seq_of_q, n_vis, scores, ld, ctx->d_flags);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "index_score");
   ctx->last_launches += 1;
   return CSA2_OK;

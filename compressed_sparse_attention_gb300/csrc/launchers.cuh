@@ -51,6 +51,12 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
                                int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
                                const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
                                const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags);
+// tensor-core form of the indexer for many queries per sequence (bf16 keys)
+bool index_tc_suited(int idx_fp8, int n_query, int n_seq, int idx_heads);
+cudaError_t launch_index_score_tc(cudaStream_t st, int num_sms, int idx_heads, int n_query, int n_seq,
+                                  int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const uint16_t* keys,
+                                  const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis,
+                                  float* scores, int64_t ld, uint32_t* flags);
 size_t topk_workspace_bytes(int n_query, int64_t max_vis);
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch);

@@ -241,6 +241,45 @@ def test_index_score(idx_heads, fp8):
         assert np.all(np.isnan(s[qi, n:])), "entries past n_vis must stay untouched"
 
 
+@pytest.mark.parametrize("idx_heads", [8, 16, 32])
+@pytest.mark.parametrize("interleave", [False, True])
+def test_index_score_many_queries(idx_heads, interleave):
+    """Many queries per sequence take the tensor-core indexer: query blocks of
+    256 / H_I queries against 128-key tiles. Interleaving two sequences makes
+    every block mixed, which is scored on the CUDA cores instead."""
+    ctx = context(idx_heads=idx_heads)
+    n_seq = 2 if interleave else 1
+    wl = Workload("idx_many", n_seq, (3000,) * n_seq if not interleave else (3000, 2200), 2,
+                  seed=77 + idx_heads, idx_heads=idx_heads, n_query_per_seq=300 if not interleave else 160)
+    inp = make_inputs(wl, DEV, with_compress=False)
+    Q = wl.n_query
+    perm = torch.randperm(Q, generator=torch.Generator().manual_seed(5)) if interleave else torch.arange(Q)
+    perm = perm.to(DEV)
+    q_idx, w, seq, nv = inp["q_idx"][perm].contiguous(), inp["w_heads"][perm].contiguous(), \
+        inp["seq_of_q"][perm].contiguous(), inp["n_vis"][perm].clone()
+    nv[5] = 0      # nothing visible
+    nv[7] = 3      # ragged inside the first tile
+    nv[40] = 129   # one key into the second tile
+    max_vis = int(nv.max())
+    ld = max_vis + 3
+    scores = torch.full((Q, ld), float("nan"), device=DEV)
+    ctx.index_score(wl.n_seq, q_idx, w, inp["idx_keys"], None, inp["pool_off"], seq, nv, max_vis, scores)
+    assert ctx.check()[0] == 0
+    s = f32_np(scores)
+    keys_np = bf16_np(inp["idx_keys"])
+    poff = inp["pool_off"].cpu().numpy()
+    for qi in range(Q):
+        b = int(seq[qi])
+        n = int(nv[qi])
+        qv = bf16_np(q_idx[qi])
+        wv = f32_np(w[qi])
+        kk = keys_np[poff[b]:poff[b] + n]
+        ref = O.index_scores(qv, wv, kk)
+        tol = score_tolerance(ref, qv, wv, kk)
+        assert np.all(np.abs(s[qi, :n] - ref) <= tol), f"query {qi}"
+        assert np.all(np.isnan(s[qi, n:])), "entries past n_vis must stay untouched"
+
+
 # ----------------------------------------------------------------------------- top-k
 
 @pytest.mark.parametrize("n,tie_levels,k", [(3000, 0, 512), (3000, 3, 512), (20000, 2, 512), (5000, 0, 2048),
