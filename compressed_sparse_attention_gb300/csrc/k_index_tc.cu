@@ -22,7 +22,7 @@
 
 namespace csa2 {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;  // 8 warps: warp w reads TMEM lanes 32(w%4).., column half w/4
 constexpr int kTcKeys = 128;                       // keys per tile (M)
 constexpr int kTcCols = 256;                       // (query, head) columns per tile (N)
 constexpr int kTcMaxBlocks = 4096;                 // query blocks handled by the tensor-core form
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
   const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   const uint32_t taddr = misc[4];  // written by tcgen05.alloc (slot at TC_MISC + 16)
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   uint32_t mph[2] = {0u, 0u};
   bool aborted = false;
 
@@ -246,34 +246,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       cp_async16(dst, ok ? src : p.keys, ok ? 16u : 0u);
     }
   };
-  // S^T of tile (block, kb) in tensor-memory half d -> scores
-  auto epilogue = [&](int b, int kb, int d) -> bool {
+  // the MMA into tensor-memory half d has completed (its key buffer is free)
+  auto epi_wait = [&](int d) -> bool {
     const bool ok = mbar_wait(mbar0 + 8u * (uint32_t)d, mph[d], p.flags);
     mph[d] ^= 1u;
     if (!__syncthreads_and(ok)) return false;
     tc_fence_after();
-    const int64_t j = (int64_t)kb * kTcKeys + tid;
+    return true;
+  };
+  // S^T of tile (block, kb) in tensor-memory half d -> scores: the thread
+  // owns key row tid % 128 and column chunks 4 (tid / 128) .. +3
+  auto epi_store = [&](int b, int kb, int d) {
+    const int row = tid & (kTcKeys - 1), half = tid / kTcKeys;
+    const int64_t j = (int64_t)kb * kTcKeys + row;
     const int q0 = b * QB;
 #pragma unroll 1
-    for (int c = 0; c < kTcCols / 32; ++c) {
-      float wc[32];
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c0 = 4 * half + 2 * cc;  // two 32-column chunks per round
+      uint32_t r0[32], r1[32];
+      tmem_ld32(taddr + (uint32_t)(256 * d + 32 * c0) + lane_base, r0);
+      tmem_ld32(taddr + (uint32_t)(256 * d + 32 * c0 + 32) + lane_base, r1);
+      float wc[64];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) wc[k] = wsm[32 * c + k];
-      int nvc[32 / HI];
+      for (int k = 0; k < 16; ++k) {
+        const float4 v = reinterpret_cast<const float4*>(wsm + 32 * c0)[k];
+        wc[4 * k] = v.x;
+        wc[4 * k + 1] = v.y;
+        wc[4 * k + 2] = v.z;
+        wc[4 * k + 3] = v.w;
+      }
+      int nvc[64 / HI];
 #pragma unroll
-      for (int k = 0; k < 32 / HI; ++k) nvc[k] = nvsm[c * (32 / HI) + k];
-      uint32_t r[32];
-      tmem_ld32(taddr + (uint32_t)(256 * d + 32 * c) + lane_base, r);
+      for (int k = 0; k < 64 / HI; ++k) nvc[k] = nvsm[c0 * (32 / HI) + k];
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 32 / HI; ++k) {
+      for (int k = 0; k < 64 / HI; ++k) {
         float sc = 0.f;
 #pragma unroll
-        for (int h = 0; h < HI; ++h) sc = fmaf(wc[k * HI + h], fmaxf(__uint_as_float(r[k * HI + h]), 0.f), sc);
-        if (j < nvc[k]) p.scores[(int64_t)(q0 + c * (32 / HI) + k) * p.ld + j] = sc;
+        for (int h = 0; h < HI; ++h) {
+          const int col = k * HI + h;
+          const float v = __uint_as_float(col < 32 ? r0[col] : r1[col - 32]);
+          sc = fmaf(wc[col], fmaxf(v, 0.f), sc);
+        }
+        if (j < nvc[k]) p.scores[(int64_t)(q0 + c0 * (32 / HI) + k) * p.ld + j] = sc;
       }
     }
     tc_fence_before();
+  };
+  auto epilogue = [&](int b, int kb, int d) -> bool {
+    if (!epi_wait(d)) return false;
+    epi_store(b, kb, d);
     return true;
   };
 
@@ -324,15 +346,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) index_score_tc_kernel(const Ind
       }
       mma_commit(mbar0 + 8u * (uint32_t)cur_d);
     }
-    if (pend) {
-      aborted = !epilogue(pend_b, pend_kb, pend_d);
-      pend = false;
-    }
+    // tile i-1's MMA done -> its key buffer takes the keys of tile i+1 (same
+    // block), which load while tile i-1's scores are written
+    if (pend) aborted = !epi_wait(pend_d);
     keys_ready = false;
-    if (!aborted && t + 1 < t_end && t + 1 < start[b + 1]) {  // next tile, same block: its keys now
+    if (!aborted && t + 1 < t_end && t + 1 < start[b + 1]) {
       load_keys(kb + 1, cur_d ^ 1);
       keys_ready = true;
     }
+    if (pend && !aborted) epi_store(pend_b, pend_kb, pend_d);
+    pend = false;
     pend = true;
     pend_b = b;
     pend_kb = kb;
