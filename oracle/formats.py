@@ -178,3 +178,116 @@ def fp8_block_dequantize(codes, exps, block: int = FP8_BLOCK) -> np.ndarray:
     n, d = codes.shape
     v = e4m3_bits_to_f64(codes).reshape(n, d // block, block)
     return (v * ue8m0_to_f64(exps)[:, :, None]).reshape(n, d)
+
+
+# ----------------------------------------------------------------------------
+# e2m1 (fp4) blocks
+#
+# "Reading Notes of DeepSeek-V4.1-Flash", section 3f, C4 (FP4 main KV cache):
+# each cached number is a 4-bit E2M1 code times a scale shared by 16
+# channels; the grid is {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}, the scale
+# s = amax / 6 is an 8-bit E4M3 number, c_i = round_E2M1(x_i / s) and the
+# decoded value is s * c_i. The PocketLLM page "DeepSeek-V4.1-Flash", section
+# "The op layer", fixes the two details the formula leaves open: the stored
+# scale is e4m3(amax / 6), the ratio rounded to E4M3, and the amax is floored
+# at 6 * 2^-9 so that an all-zero block still has a nonzero scale. The index
+# keys use the MXFP4 variant of the same codes (C2 "Resulting memory"; the
+# op-layer page: E8M0 scales over 32 channels), whose scale is
+# 2^round(log2(amax / 6)), amax floored at 6 * 2^-126.
+#
+# Readings where the pages are silent: round_E2M1 is round-to-nearest with
+# ties to the even code (mantissa bit 0), saturating at +-6 (x / s can pass 6
+# once s is rounded down); the code's sign bit is kept when a negative value
+# rounds to 0; round(log2(.)) rounds to nearest (an exact half never occurs
+# for a nonzero finite amax / 6 that is not a power of two times sqrt 2).
+# Codes are stored two to a byte, the even channel in the low nibble.
+# ----------------------------------------------------------------------------
+
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])  # magnitude of code & 7
+E2M1_MAX = 6.0
+FP4_BLOCK = 16
+MXFP4_BLOCK = 32
+FP4_AMAX_FLOOR = 6.0 * 2.0 ** -9
+MXFP4_AMAX_FLOOR = 6.0 * 2.0 ** -126
+
+
+def f64_to_e2m1_codes(x) -> np.ndarray:
+    """Nearest E2M1 code (ties to the even code, saturating at +-6); uint8 in [0, 15]."""
+    x = np.asarray(x, dtype=np.float64)
+    if np.isnan(x).any():
+        raise ValueError("NaN has no e2m1 encoding")
+    ax = np.minimum(np.abs(x), E2M1_MAX)
+    hi = np.searchsorted(E2M1_VALUES, ax)          # first magnitude >= ax
+    hi = np.minimum(hi, 7)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = ax - E2M1_VALUES[lo]
+    d_hi = E2M1_VALUES[hi] - ax
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(8), code).astype(np.uint8)
+
+
+def e2m1_codes_to_f64(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8)
+    v = E2M1_VALUES[c & 7]
+    return np.where(c & 8, -v, v)
+
+
+def fp4_block_quantize(x, block: int = FP4_BLOCK):
+    """Rows [n, D] -> (codes uint8 [n, D], e4m3 scale bytes uint8 [n, D/block])."""
+    x = np.asarray(x, dtype=np.float64)
+    n, d = x.shape
+    if d % block:
+        raise ValueError("row length must be a multiple of the block")
+    xb = x.reshape(n, d // block, block)
+    amax = np.abs(xb).max(axis=2)
+    sbits = f64_to_e4m3_bits(np.maximum(amax, FP4_AMAX_FLOOR) / E2M1_MAX)
+    s = e4m3_bits_to_f64(sbits)[:, :, None]
+    codes = f64_to_e2m1_codes(xb / s).reshape(n, d)
+    return codes, sbits
+
+
+def fp4_block_dequantize(codes, sbits, block: int = FP4_BLOCK) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, d = codes.shape
+    v = e2m1_codes_to_f64(codes).reshape(n, d // block, block)
+    return (v * e4m3_bits_to_f64(sbits)[:, :, None]).reshape(n, d)
+
+
+def mxfp4_block_quantize(x, block: int = MXFP4_BLOCK):
+    """Rows [n, D] -> (codes uint8 [n, D], ue8m0 scale bytes uint8 [n, D/block])."""
+    x = np.asarray(x, dtype=np.float64)
+    n, d = x.shape
+    if d % block:
+        raise ValueError("row length must be a multiple of the block")
+    xb = x.reshape(n, d // block, block)
+    amax = np.maximum(np.abs(xb).max(axis=2), MXFP4_AMAX_FLOOR)
+    # round(log2(r)) for r = f * 2^k, f in [0.5, 1): k - 1 when log2 f < -1/2,
+    # i.e. f < 2^-1/2, else k (f = 2^-1/2 exactly cannot occur)
+    f, k = np.frexp(amax / E2M1_MAX)
+    e = np.where(f < 2.0 ** -0.5, k - 1, k).astype(np.int64)
+    ebytes = np.clip(e + 127, 0, 254).astype(np.uint8)
+    s = ue8m0_to_f64(ebytes)[:, :, None]
+    codes = f64_to_e2m1_codes(xb / s).reshape(n, d)
+    return codes, ebytes
+
+
+def mxfp4_block_dequantize(codes, ebytes, block: int = MXFP4_BLOCK) -> np.ndarray:
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, d = codes.shape
+    v = e2m1_codes_to_f64(codes).reshape(n, d // block, block)
+    return (v * ue8m0_to_f64(ebytes)[:, :, None]).reshape(n, d)
+
+
+def pack_e2m1(codes) -> np.ndarray:
+    """[n, D] codes -> [n, D/2] bytes, channel 2i in the low nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_e2m1(packed) -> np.ndarray:
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty((b.shape[0], 2 * b.shape[1]), dtype=np.uint8)
+    out[:, 0::2] = b & 0xF
+    out[:, 1::2] = b >> 4
+    return out

@@ -395,3 +395,99 @@ def test_fp8_block_scale_vectorised_equals_scalar_definition():
     got = F.fp8_block_scale_exponents(amax)
     ref = np.array([F.fp8_block_scale_exponent(float(a)) for a in amax], dtype=np.uint8)
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- fp4 formats
+
+def test_fp4_worked_example():
+    """The page's 4-of-16 example: amax 2.4 gives s = 0.4 before the scale
+    itself is rounded to E4M3 (0.40625); both give codes (6, 3, -1.5, 0)."""
+    g = golden("fp4_worked_example.json")
+    x = np.zeros((1, 16))
+    x[0, :4] = g["x"]
+    # the page's arithmetic with its unrounded scale
+    s0 = g["scale_from_amax"]
+    assert np.allclose(np.array(g["x"]) / s0, g["x_over_s"], rtol=0, atol=1e-12)
+    assert F.e2m1_codes_to_f64(F.f64_to_e2m1_codes(np.array(g["x_over_s"]))).tolist() == g["codes"]
+    assert np.allclose(s0 * np.array(g["codes"]), g["decoded"], atol=1e-12)
+    # the stored form: scale e4m3(amax / 6), codes from x / stored scale
+    codes, sbits = F.fp4_block_quantize(x)
+    s = float(F.e4m3_bits_to_f64(sbits)[0, 0])
+    assert s == 0.40625                                  # nearest E4M3 to 0.4 (1.625 * 2^-2)
+    assert F.e2m1_codes_to_f64(codes)[0, :4].tolist() == g["codes"]
+    dec = F.fp4_block_dequantize(codes, sbits)[0, :4]
+    assert np.array_equal(dec, s * np.array(g["codes"]))
+    assert np.allclose(dec, g["decoded"], rtol=2.0 ** -4, atol=0)  # one E4M3 scale step from the page's
+
+
+def test_fp4_zero_block_takes_the_floor_scale():
+    g = golden("fp4_worked_example.json")
+    codes, sbits = F.fp4_block_quantize(np.zeros((2, 32)))
+    assert g["amax_floor"] == F.FP4_AMAX_FLOOR == 6 * 2.0 ** -9
+    assert np.all(F.e4m3_bits_to_f64(sbits) == 2.0 ** -9)   # e4m3(floor / 6): the smallest subnormal
+    assert np.all(F.e2m1_codes_to_f64(codes) == 0.0)
+    assert np.all(F.fp4_block_dequantize(codes, sbits) == 0.0)
+
+
+def test_fp4_scale_is_amax_over_six_not_amax():
+    x = np.zeros((1, 16))
+    x[0, 0], x[0, 1] = 3.0, -1.0
+    codes, sbits = F.fp4_block_quantize(x)
+    assert float(F.e4m3_bits_to_f64(sbits)[0, 0]) == 0.5     # 3 / 6, exact in E4M3 (e4m3(3) would be 6x)
+    assert F.e2m1_codes_to_f64(codes)[0, :2].tolist() == [6.0, -2.0]
+
+
+def test_e2m1_rounding_ties_and_saturation():
+    x = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.26, 2.6, 5.1, 7.0, 1e9, -0.25, -0.76, -3.5])
+    got = F.e2m1_codes_to_f64(F.f64_to_e2m1_codes(x))
+    # ties go to the code with a zero mantissa bit: 0, 1, 1, 2, 2, 4, 4
+    assert got.tolist() == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 0.5, 3.0, 6.0, 6.0, 6.0, -0.0, -1.0, -4.0]
+    assert int(F.f64_to_e2m1_codes(np.array([-0.25]))[0]) == 8   # the sign survives rounding to zero
+    # every code decodes onto the page's grid and encodes back to itself
+    allc = np.arange(16, dtype=np.uint8)
+    assert set(np.abs(F.e2m1_codes_to_f64(allc)).tolist()) == {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}
+    assert np.array_equal(F.f64_to_e2m1_codes(F.e2m1_codes_to_f64(allc)), allc)
+
+
+def test_mxfp4_scale_is_rounded_power_of_two():
+    def ebyte(amax):
+        x = np.zeros((1, 32))
+        x[0, 0] = amax
+        return int(F.mxfp4_block_quantize(x)[1][0, 0])
+    assert ebyte(6.0) == 127            # 2^round(log2(1)) = 1
+    assert ebyte(8.4) == 127            # log2(1.4) = 0.485 -> 0
+    assert ebyte(8.5) == 128            # log2(1.417) = 0.502 -> 1
+    assert ebyte(3.0) == 126
+    assert ebyte(0.0) == 1              # floor 6 * 2^-126 -> 2^-126
+    x = np.zeros((1, 32))
+    x[0, :2] = [8.4, -0.3]
+    codes, e = F.mxfp4_block_quantize(x)
+    # scale 1: 8.4 saturates to the largest code, -0.3 rounds to -0.5
+    assert F.mxfp4_block_dequantize(codes, e)[0, :2].tolist() == [6.0, -0.5]
+
+
+def test_fp4_pack_nibble_order_and_roundtrip():
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 16, size=(5, 64)).astype(np.uint8)
+    packed = F.pack_e2m1(codes)
+    assert packed.shape == (5, 32)
+    assert int(packed[0, 0]) == int(codes[0, 0]) | (int(codes[0, 1]) << 4)
+    assert np.array_equal(F.unpack_e2m1(packed), codes)
+
+
+def test_fp4_roundtrip_error_bound():
+    """Decoded values sit on the scaled grid, within half a grid gap of x
+    (the largest gap, 4..6, bounds it by one scale unit) unless saturated."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((64, 512)) * np.exp(rng.uniform(-6, 6, size=(64, 1)))
+    codes, sbits = F.fp4_block_quantize(x)
+    dec = F.fp4_block_dequantize(codes, sbits)
+    s = np.repeat(F.e4m3_bits_to_f64(sbits), 16, axis=1)
+    on_grid = np.isin(np.abs(dec / s), F.E2M1_VALUES)
+    assert on_grid.all()
+    unsat = np.abs(x / s) <= 6.0
+    assert np.all(np.abs(x - dec)[unsat] <= s[unsat] * 1.0 + 1e-300)
+    # the scale is within one E4M3 rounding of amax / 6
+    amax = np.abs(x.reshape(64, 32, 16)).max(axis=2)
+    sv = F.e4m3_bits_to_f64(sbits)
+    assert np.all(np.abs(sv - amax / 6) <= np.maximum(amax / 6, 2.0 ** -6) * 2.0 ** -4 + 2.0 ** -10)
