@@ -145,12 +145,22 @@ def max_over_ranks(pg, x: float, device) -> float:
 
 # ----------------------------------------------------------------------------- workload bytes
 
+# bytes of one stored row (codes + scales) per storage format code
+_ROW_BYTES = {0: 1024, 1: 512 + 16, 2: 256 + 32}     # 512-channel rows: bf16, fp8 (ue8m0 / 32), fp4 (e4m3 / 16)
+_KEY_BYTES = {0: 256, 1: 128 + 4, 3: 64 + 4}         # 128-channel keys: bf16, fp8, mxfp4 (e8m0 / 32)
+
+
+def row_bytes(wl):
+    """(window row, pool row, index key) bytes; an fp4 pool keeps an fp8 window."""
+    win = _ROW_BYTES[1] if wl.kv_fp8 else _ROW_BYTES[0]
+    return win, _ROW_BYTES[wl.kv_format], _KEY_BYTES[wl.idx_key_format]
+
+
 def algorithmic_bytes(wl, has_compress=True):
     """Minimal HBM bytes of one step: every visible index key once, the gathered
     window and selected rows once, q/q^I/w in, the output out, and the closing
     groups' raw tokens and gates in plus their stored entries out."""
-    row = 528 if wl.kv_fp8 else 1024
-    key = 132 if wl.idx_fp8 else 256
+    wrow, prow, key = row_bytes(wl)
     total = 0
     for b in range(wl.n_seq):
         n = wl.ctx_len[b]
@@ -158,15 +168,23 @@ def algorithmic_bytes(wl, has_compress=True):
             t = n - wl.n_query_per_seq + i
             nv = (t + 1) // wl.m
             win = min(wl.window, t + 1)
-            total += nv * key + (win + min(wl.topk, nv)) * row
+            total += nv * key + win * wrow + min(wl.topk, nv) * prow
             total += wl.n_heads * wl.head_dim * 2 * 2 + wl.idx_heads * wl.idx_dim * 2 + wl.idx_heads * 4
         if has_compress and n % wl.m == 0:
-            total += wl.m * wl.head_dim * (2 + 4) + row + key
+            total += wl.m * wl.head_dim * (2 + 4) + prow + key
     return total
 
 
+def kv_format_name(wl):
+    if not wl.kv_fp8:
+        return "bf16"
+    pool = "fp4_e2m1_e4m3_b16 pool, fp8 window" if wl.pool_fp4 else "fp8_e4m3_ue8m0_b32"
+    keys = "mxfp4_e2m1_ue8m0_b32 keys" if wl.key_fp4 else ("fp8 keys" if wl.idx_fp8 else "bf16 keys")
+    return f"{pool}; {keys}"
+
+
 def index_bytes(wl):
-    key = 132 if wl.idx_fp8 else 256
+    key = row_bytes(wl)[2]
     tot = 0
     for b in range(wl.n_seq):
         n = wl.ctx_len[b]
@@ -186,24 +204,22 @@ class Copy:
         from compressed_sparse_attention_gb300 import binding
         wlc = wl.scaled(seed=wl.seed + 1000 * seed_offset)
         inp = make_inputs(wlc, device)
+
+        def store(x, fmt):
+            dim = x.shape[1]
+            blk = 16 if fmt == binding.KV_FP4 else 32
+            codes = torch.empty((x.shape[0], dim if fmt == binding.KV_FP8 else dim // 2), dtype=torch.uint8,
+                                device=device)
+            sc = torch.empty((x.shape[0], dim // blk), dtype=torch.uint8, device=device)
+            for i in range(0, x.shape[0], 1 << 20):
+                ctx.store_rows(x[i:i + (1 << 20)], None, fmt, codes[i:i + (1 << 20)], sc[i:i + (1 << 20)])
+            return codes, sc
+
         if wl.kv_fp8:
-            for src, dst, w in (("win_kv_f32", "win_kv", 512), ("pool_kv_f32", "pool_kv", 512)):
-                x = inp.pop(src)
-                codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
-                sc = torch.empty((x.shape[0], w // 32), dtype=torch.uint8, device=device)
-                for i in range(0, x.shape[0], 1 << 20):
-                    ctx.store_rows(x[i:i + (1 << 20)], None, binding.KV_FP8, codes[i:i + (1 << 20)],
-                                   sc[i:i + (1 << 20)])
-                inp[dst], inp[dst.replace("_kv", "_scale")] = codes, sc
-                del x
+            inp["win_kv"], inp["win_scale"] = store(inp.pop("win_kv_f32"), binding.KV_FP8)
+            inp["pool_kv"], inp["pool_scale"] = store(inp.pop("pool_kv_f32"), wl.kv_format)
         if wl.idx_fp8:
-            x = inp.pop("idx_keys_f32")
-            codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
-            sc = torch.empty((x.shape[0], 4), dtype=torch.uint8, device=device)
-            for i in range(0, x.shape[0], 1 << 21):
-                ctx.store_rows(x[i:i + (1 << 21)], None, binding.KV_FP8, codes[i:i + (1 << 21)], sc[i:i + (1 << 21)])
-            inp["idx_keys"], inp["idx_key_scale"] = codes, sc
-            del x
+            inp["idx_keys"], inp["idx_key_scale"] = store(inp.pop("idx_keys_f32"), wl.idx_key_format)
         torch.cuda.synchronize()
         self.inp = inp
         Q = wl.n_query
@@ -241,8 +257,8 @@ class Copy:
 def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
     from compressed_sparse_attention_gb300 import binding, build
     build.build()
-    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=int(wl.kv_fp8),
-                          idx_key_format=int(wl.idx_fp8))
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=wl.kv_format,
+                          idx_key_format=wl.idx_key_format)
     copies = [Copy(ctx, wl, rank * N_COPIES + c, device) for c in range(N_COPIES)]
     stream = torch.cuda.Stream(device=device)
     # launches per step
@@ -427,9 +443,21 @@ class OracleSample:
         def fp8(t):
             return F.fp8_block_dequantize(*F.fp8_block_quantize(t.double().numpy()))
 
-        self.keys = fp8(inp["idx_keys_f32"]) if wl.idx_fp8 else bf(inp["idx_keys"])
-        self.pool = fp8(inp["pool_kv_f32"]) if wl.kv_fp8 else bf(inp["pool_kv"])
-        self.win = fp8(inp["win_kv_f32"]) if wl.kv_fp8 else bf(inp["win_kv"])
+        def fp4(t):
+            return F.fp4_block_dequantize(*F.fp4_block_quantize(t.double().numpy()))
+
+        def mxfp4(t):
+            return F.mxfp4_block_dequantize(*F.mxfp4_block_quantize(t.double().numpy()))
+
+        if wl.idx_fp8:
+            self.keys = (mxfp4 if wl.key_fp4 else fp8)(inp["idx_keys_f32"])
+        else:
+            self.keys = bf(inp["idx_keys"])
+        if wl.kv_fp8:
+            self.pool = (fp4 if wl.pool_fp4 else fp8)(inp["pool_kv_f32"])
+            self.win = fp8(inp["win_kv_f32"])
+        else:
+            self.pool, self.win = bf(inp["pool_kv"]), bf(inp["win_kv"])
         self.q = bf(inp["q"][0])
         self.qi, self.w = bf(inp["q_idx"][0]), inp["w_heads"][0].double().numpy()
         self.sink = inp["sink"].double().numpy()
@@ -526,7 +554,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "batch": wl.n_seq, "context": wl.ctx_len[0], "compress_ratio": wl.m,
                    "topk": wl.topk, "window": wl.window, "heads": "64x512", "indexer": f"{wl.idx_heads}x128",
-                   "kv": "fp8_e4m3_ue8m0_b32" if wl.kv_fp8 else "bf16",
+                   "kv": kv_format_name(wl),
                    "l2": f"{N_COPIES} rotating input copies ({N_COPIES * step_bytes / 1e6:.0f} MB > 129 MB L2)",
                    "graph": f"one CUDA graph per {N_COPIES} consecutive steps (one per input copy)"},
         "hbm_gbs": gbs, "hbm_frac": gbs / hbm, "step_algorithmic_bytes": step_bytes,
@@ -542,19 +570,21 @@ def main():
         "clocks": clocks,
     }
     if rank == 0 and not args.no_extra and wl.name == "decode_64k_b32" and world == 1:
-        try:
-            wl4 = PRESETS["decode_1m_b8_fp8"]
-            a2 = argparse.Namespace(**vars(args))
-            a2.steps = min(args.steps, 500)
-            r4 = run_gpu_workload(a2, wl4, rank, None, device, (hbm, bf16_burst))
-            ms4 = r4["ms"] / a2.steps
-            b4 = algorithmic_bytes(wl4)
-            line["extra_1m"] = {"workload": wl4.name, "tokens_per_s": wl4.n_query / (ms4 / 1000.0),
-                                "ms_per_step": ms4, "hbm_gbs": b4 / (ms4 / 1000.0) / 1e9,
-                                "hbm_frac": b4 / (ms4 / 1000.0) / 1e9 / hbm,
-                                "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
-        except Exception as ex:  # reported, never silently dropped
-            line["extra_1m"] = {"error": repr(ex)[:300]}
+        for key, name in (("extra_1m", "decode_1m_b8_fp8"), ("extra_1m_fp4", "decode_1m_b8_fp4")):
+            try:
+                wl4 = PRESETS[name]
+                a2 = argparse.Namespace(**vars(args))
+                a2.steps = min(args.steps, 500)
+                r4 = run_gpu_workload(a2, wl4, rank, None, device, (hbm, bf16_burst))
+                ms4 = r4["ms"] / a2.steps
+                b4 = algorithmic_bytes(wl4)
+                line[key] = {"workload": wl4.name, "kv": kv_format_name(wl4),
+                             "tokens_per_s": wl4.n_query / (ms4 / 1000.0), "ms_per_step": ms4,
+                             "hbm_gbs": b4 / (ms4 / 1000.0) / 1e9, "hbm_frac": b4 / (ms4 / 1000.0) / 1e9 / hbm,
+                             "step_algorithmic_bytes": b4,
+                             "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
+            except Exception as ex:  # reported, never silently dropped
+                line[key] = {"error": repr(ex)[:300]}
         try:
             line["extra_prefill"] = run_prefill_extra(args, device, bf16_burst)
         except Exception as ex:  # reported, never silently dropped

@@ -21,7 +21,7 @@ _LIB = None
 CSA2_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported geometry", 3: "CUDA error",
           4: "bad input recorded on the device", 5: "device wait timed out", 6: "workspace too small"}
-KV_BF16, KV_FP8 = 0, 1
+KV_BF16, KV_FP8, KV_FP4, KV_MXFP4 = 0, 1, 2, 3  # csa2_kv_format
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 
 FLAG_BAD_TOPK_INDEX = 0x01
@@ -124,7 +124,7 @@ def default_config(**overrides) -> Config:
     lib.csa2_default_config(C.byref(cfg))
     for k, v in overrides.items():
         if k in ("kv_format", "idx_key_format") and isinstance(v, str):
-            v = {"bf16": KV_BF16, "fp8": KV_FP8}[v]
+            v = {"bf16": KV_BF16, "fp8": KV_FP8, "fp4": KV_FP4, "mxfp4": KV_MXFP4}[v]
         setattr(cfg, k, v)
     return cfg
 

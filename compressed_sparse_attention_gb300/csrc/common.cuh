@@ -83,6 +83,58 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
   return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
 }
 
+// ---------------------------------------------------------------- fp4 (E2M1)
+// E2M1 code of x for a block scale s: the nearest of s * {0, 0.5, 1, 1.5, 2,
+// 3, 4, 6}, ties to the even code (mantissa bit 0), saturating at 6 s; the
+// sign bit follows x (also for -0). Each midpoint m * s has at most 7
+// significant bits (m <= 3 bits, s an e4m3 value or a power of two), so the
+// comparisons are exact and no division rounds.
+__device__ __forceinline__ uint32_t e2m1_code(float x, float s) {
+  const float ax = fabsf(x);
+  uint32_t c = 0u;
+  c += (ax > 0.25f * s) ? 1u : 0u;   // tie -> 0
+  c += (ax >= 0.75f * s) ? 1u : 0u;  // tie -> 1.0
+  c += (ax > 1.25f * s) ? 1u : 0u;   // tie -> 1.0
+  c += (ax >= 1.75f * s) ? 1u : 0u;  // tie -> 2.0
+  c += (ax > 2.5f * s) ? 1u : 0u;    // tie -> 2.0
+  c += (ax >= 3.5f * s) ? 1u : 0u;   // tie -> 4.0
+  c += (ax > 5.0f * s) ? 1u : 0u;    // tie -> 4.0
+  return c | ((__float_as_uint(x) >> 28) & 8u);
+}
+// two E2M1 codes (low nibble first) -> two floats, each 2^-14 times its value:
+// the code's exponent and mantissa bits dropped into fp16's low exponent and
+// top mantissa bits give exactly that (subnormal codes included)
+__device__ __forceinline__ float2 e2m1x2_to_float2_scaled(uint32_t two) {
+  const uint32_t lo = two & 0xFu, hi = (two >> 4) & 0xFu;
+  const uint32_t h = ((lo & 7u) << 9) | ((lo & 8u) << 12) | (((hi & 7u) << 9) << 16) | (((hi & 8u) << 12) << 16);
+  __half2_raw r;
+  r.x = (unsigned short)(h & 0xFFFFu);
+  r.y = (unsigned short)(h >> 16);
+  return __half22float2(__half2(r));
+}
+constexpr float kE2M1Unscale = 16384.0f;  // 2^14
+// e4m3 byte of the fp4 block scale: e4m3(max(amax, 6 * 2^-9) / 6), the
+// quotient formed in double (exact enough that its rounding to e4m3 equals
+// that of the real quotient) and rounded by CUDA's own conversion
+__device__ __forceinline__ uint8_t fp4_scale_e4m3(float amax) {
+  const double r = (double)fmaxf(amax, 6.0f * 0x1p-9f) / 6.0;
+  return (uint8_t)__nv_cvt_double_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
+}
+// value of an e4m3 byte
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  return e4m3x2_to_float2((uint16_t)(b & 0xFFu)).x;
+}
+// ue8m0 byte of the MXFP4 block scale 2^round(log2(max(amax, 6 * 2^-126) / 6)):
+// with r = f * 2^k (f in [0.5, 1)), round(log2 r) = k - 1 if f < 2^-1/2, else k
+__device__ __forceinline__ uint32_t mxfp4_scale_byte(float amax) {
+  const double r = (double)fmaxf(amax, 6.0f * 0x1p-126f) / 6.0;
+  int k;
+  const double f = frexp(r, &k);
+  const int e = (f < 0.70710678118654752440) ? k - 1 : k;
+  const int b = e + 127;
+  return (uint32_t)(b < 0 ? 0 : (b > 254 ? 254 : b));
+}
+
 // order-preserving 32-bit key of a score; -0.0 maps with +0.0
 __device__ __forceinline__ uint32_t score_key(float x) {
   uint32_t u = __float_as_uint(x);

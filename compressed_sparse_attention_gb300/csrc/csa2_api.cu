@@ -103,8 +103,9 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (c.compress_ratio < 1 || c.compress_ratio > 16) return CSA2_ERR_UNSUPPORTED;
   if (!(c.idx_heads == 8 || c.idx_heads == 16 || c.idx_heads == 32)) return CSA2_ERR_UNSUPPORTED;
   if (c.topk < 1 || c.topk > 2048) return CSA2_ERR_UNSUPPORTED;
-  if ((c.kv_format != CSA2_KV_BF16 && c.kv_format != CSA2_KV_FP8_E4M3_B32) ||
-      (c.idx_key_format != CSA2_KV_BF16 && c.idx_key_format != CSA2_KV_FP8_E4M3_B32))
+  if ((c.kv_format != CSA2_KV_BF16 && c.kv_format != CSA2_KV_FP8_E4M3_B32 && c.kv_format != CSA2_KV_FP4_E4M3_B16) ||
+      (c.idx_key_format != CSA2_KV_BF16 && c.idx_key_format != CSA2_KV_FP8_E4M3_B32 &&
+       c.idx_key_format != CSA2_KV_MXFP4_B32))
     return CSA2_ERR_UNSUPPORTED;
   if (!(c.rope_theta > 0) || !(c.yarn_orig_len > 0) || !(c.yarn_beta_fast > 0) || !(c.yarn_beta_slow > 0) ||
       !std::isfinite(c.softmax_scale) || !(c.norm_eps >= 0))
@@ -176,12 +177,12 @@ csa2_status csa2_store_rows(csa2_ctx* ctx, void* stream, const float* rows, int6
   if (!ctx) return CSA2_ERR_INVALID_ARG;
   ctx->last_launches = 0;
   if (n_rows < 0 || !(dim == 512 || dim == 128)) return fail(ctx, CSA2_ERR_INVALID_ARG, "dim must be 128 or 512");
-  if (format != CSA2_KV_BF16 && format != CSA2_KV_FP8_E4M3_B32) return fail(ctx, CSA2_ERR_INVALID_ARG, "format");
+  if (format < CSA2_KV_BF16 || format > CSA2_KV_MXFP4_B32) return fail(ctx, CSA2_ERR_INVALID_ARG, "format");
   if (n_rows == 0) return CSA2_OK;
-  if (!rows || !out || (format == CSA2_KV_FP8_E4M3_B32 && !out_scale) || !aligned16(rows) || !aligned16(out))
+  if (!rows || !out || (format != CSA2_KV_BF16 && !out_scale) || !aligned16(rows) || !aligned16(out))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "store_rows: null or misaligned buffer");
   cudaError_t e = csa2::launch_store_rows(reinterpret_cast<cudaStream_t>(stream), rows, n_rows, dim, pos,
-                                          ctx->rope, format == CSA2_KV_FP8_E4M3_B32, out, out_scale);
+                                          ctx->rope, format, out, out_scale);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "store_rows");
   ctx->last_launches = 1;
   return CSA2_OK;
@@ -199,15 +200,15 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
   if (n_tokens % m) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_tokens must be whole groups");
   if (!raw || !tok_off || !first_pos || !pool_off || !norm_w || !pool_kv || (m > 1 && !gate))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: null pointer");
-  if (c.kv_format == CSA2_KV_FP8_E4M3_B32 && !pool_kv_scale)
-    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: fp8 pool needs its scale array");
-  if (w_idx && (!k_norm_w || !idx_keys || (c.idx_key_format == CSA2_KV_FP8_E4M3_B32 && !idx_key_scale)))
+  if (c.kv_format != CSA2_KV_BF16 && !pool_kv_scale)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: an fp8 / fp4 pool needs its scale array");
+  if (w_idx && (!k_norm_w || !idx_keys || (c.idx_key_format != CSA2_KV_BF16 && !idx_key_scale)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: index key outputs missing");
   if (!aligned16(raw) || (gate && !aligned16(gate)) || !aligned16(norm_w) || (w_idx && !aligned16(w_idx)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: inputs must be 16-byte aligned");
   cudaError_t e = csa2::launch_compress(st, n_tokens / m, raw, gate, m, n_seq, tok_off, first_pos, pool_off, norm_w,
                                         w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
-                                        c.kv_format == CSA2_KV_FP8_E4M3_B32, c.idx_key_format == CSA2_KV_FP8_E4M3_B32,
+                                        c.kv_format, c.idx_key_format,
                                         pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
   ctx->last_launches += 1;
@@ -234,17 +235,17 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
   if (n_query == 0 || max_vis == 0) return CSA2_OK;
   if (!q_idx || !w_heads || !idx_keys || !pool_off || !seq_of_q || !n_vis || !scores)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: null pointer");
-  if (c.idx_key_format == CSA2_KV_FP8_E4M3_B32 && !idx_key_scale)
-    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: fp8 keys need their scales");
+  if (c.idx_key_format != CSA2_KV_BF16 && !idx_key_scale)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: fp8 / mxfp4 keys need their scales");
   if (!aligned16(q_idx) || !aligned16(idx_keys) || (idx_key_scale && (reinterpret_cast<uintptr_t>(idx_key_scale) & 3)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: misaligned buffer");
-  const int fp8 = c.idx_key_format == CSA2_KV_FP8_E4M3_B32;
+  const int kf = c.idx_key_format;
   cudaError_t e =
-      csa2::index_tc_suited(fp8, n_query, n_seq, c.idx_heads)
+      csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)
           ? csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
                                         reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis,
                                         scores, ld, ctx->d_flags)
-          : csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, fp8, n_query, n_seq, max_vis, q_idx, w_heads,
+          : csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, kf, n_query, n_seq, max_vis, q_idx, w_heads,
                                      idx_keys, idx_key_scale, pool_off, seq_of_q, n_vis, scores, ld, ctx->d_flags);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "index_score");
   ctx->last_launches += 1;
@@ -305,10 +306,10 @@ static csa2_status attend_params(csa2_ctx* ctx, int32_t n_seq, int32_t n_query, 
                                  const int32_t* topk_idx, const float* sink, uint16_t* out, float* lse, void* ws,
                                  size_t ws_bytes, csa2::AttendParams* pp) {
   const csa2_config& c = ctx->cfg;
-  const bool fp8 = c.kv_format == CSA2_KV_FP8_E4M3_B32;
+  const bool scaled = c.kv_format != CSA2_KV_BF16;  // fp8 window (fp8 or fp4 pool): scale arrays
   if (n_query < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: sizes");
   if (!q || !q_pos || !seq_of_q || !win_kv || !win_off || !sink || !out ||
-      (topk_idx && (!pool_kv || !pool_off)) || (fp8 && (!win_scale || (topk_idx && !pool_scale))))
+      (topk_idx && (!pool_kv || !pool_off)) || (scaled && (!win_scale || (topk_idx && !pool_scale))))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: null pointer");
   if (!aligned16(q) || !aligned16(win_kv) || (pool_kv && !aligned16(pool_kv)) || !aligned16(out))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "attend: misaligned buffer");
@@ -340,7 +341,7 @@ static csa2_status do_attend(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int3
                                 pool_scale, pool_off, topk_idx, sink, out, lse, ws, ws_bytes, &p);
   if (s != CSA2_OK || n_query == 0) return s;
   int nl = 0;
-  cudaError_t e = csa2::launch_attend(st, ctx->num_sms, ctx->cfg.kv_format == CSA2_KV_FP8_E4M3_B32, p, ws, &nl);
+  cudaError_t e = csa2::launch_attend(st, ctx->num_sms, ctx->cfg.kv_format, p, ws, &nl);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "attend");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -390,7 +391,7 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
                     a->win_lo, a->pool_kv, a->pool_scale, a->pool_off, a->topk_idx, a->sink, a->out, a->lse, at_ws,
                     at_bytes, &ap);
   if (s != CSA2_OK) return s;
-  const int fp8 = ctx->cfg.kv_format == CSA2_KV_FP8_E4M3_B32;
+  const int kvf = ctx->cfg.kv_format;
   const csa2::AttendPlan pl = csa2::attend_plan(a->n_query, ctx->cfg.topk, true, ctx->num_sms);
   int launches = 0;
   if (a->mode == CSA2_MODE_FULL) {
@@ -407,7 +408,7 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   if (a->mode == CSA2_MODE_REUSE) {
     // nothing to overlap with: window and selected tiles share one launch
     ctx->last_launches = 0;
-    cudaError_t e = csa2::launch_attend(st, ctx->num_sms, fp8, ap, at_ws, &ctx->last_launches);
+    cudaError_t e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &ctx->last_launches);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
     ctx->last_launches += launches;
     return CSA2_OK;
@@ -427,7 +428,7 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   if (pl.split_window) {
     e = cudaEventRecord(ctx->ev_fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0);
-    if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, fp8, ap, pl, at_ws, &launches);
+    if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
     if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_join, ctx->side);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step: window tile");
     forked = true;
@@ -446,13 +447,13 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
   if (pl.split_window) {
-    e = csa2::launch_attend_main(st, fp8, ap, pl, at_ws, &launches);
+    e = csa2::launch_attend_main(st, kvf, ap, pl, at_ws, &launches);
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
     s = join(CSA2_OK);
     if (s != CSA2_OK) return s;
     e = csa2::launch_attend_merge(st, ap, pl, at_ws, &launches);
   } else {
-    e = csa2::launch_attend(st, ctx->num_sms, fp8, ap, at_ws, &launches);
+    e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
   ctx->last_launches = launches;

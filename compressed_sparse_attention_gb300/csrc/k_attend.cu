@@ -71,7 +71,8 @@ __device__ __forceinline__ int rs_head(int lane) {
          (lane & 1) * 2;
 }
 
-template <bool FP8>
+// KVF: 0 bf16 rows; 1 fp8 rows; 2 fp8 window rows and fp4 pool rows
+template <int KVF>
 __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     __syncthreads();
     // ---- gather the tile's rows into the swizzled KV operand
     const void* kvsrc = (tile == 0) ? p.win_kv : p.pool_kv;
-    if constexpr (!FP8) {
+    if constexpr (KVF == 0) {
       const uint16_t* kv = reinterpret_cast<const uint16_t*>(kvsrc);
       for (int r = warp; r < kTileRows; r += 4) {
         const int64_t src = rows[r];
@@ -203,6 +204,45 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         }
       }
       cp_async_wait_all();
+    } else if (KVF == 2 && tile != 0) {
+      // fp4 pool rows: 256 B of E2M1 codes + 32 e4m3 scales; lane l converts
+      // channels 16l .. 16l+15 (8 code bytes, scale l), 8 rows' loads in flight
+      const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.pool_kv);
+      constexpr int kBatch = 8;
+#pragma unroll 1
+      for (int r0 = warp; r0 < kTileRows; r0 += 4 * kBatch) {
+        uint2 codes[kBatch];
+        uint8_t sb[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int64_t src = rows[r0 + 4 * j];
+          codes[j] = make_uint2(0u, 0u);
+          sb[j] = 0;
+          if (src >= 0) {
+            codes[j] = ldg_stream8(kv + src * (kDim / 2) + 8 * lane);
+            sb[j] = p.pool_scale[src * (kDim / 16) + lane];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int r = r0 + 4 * j;
+          const float sc = e4m3_value(sb[j]) * kE2M1Unscale;  // code values arrive scaled by 2^-14
+          uint32_t o[8];
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const uint32_t w = ((b < 4 ? codes[j].x : codes[j].y) >> (8 * (b & 3))) & 0xFFu;
+            const float2 f = e2m1x2_to_float2_scaled(w);
+            o[b] = pack_bf16(f.x * sc, f.y * sc);  // exact: <= 6 significant bits
+          }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * lane + cc;  // bf16 chunk: channels 8c .. 8c+7
+            const uint32_t off = SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
+                                 ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + off) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+          }
+        }
+      }
     } else {
       const uint8_t* kv = reinterpret_cast<const uint8_t*>(kvsrc);
       const uint8_t* ksc = (tile == 0) ? p.win_scale : p.pool_scale;
@@ -637,19 +677,24 @@ static void attach_ws(AttendParams& p, const AttendPlan& pl, void* ws) {
   }
 }
 
-static cudaError_t launch_tiles(cudaStream_t st, int kv_fp8, const AttendParams& p, int* n_launch) {
-  cudaError_t e;
-  if (kv_fp8) e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
-  else e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes);
-  if (e != cudaSuccess) return e;
+static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams& p, int* n_launch) {
   const dim3 grid((unsigned)(p.n_query * p.n_split));
-  if (kv_fp8) attend_kernel<true><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
-  else attend_kernel<false><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);
+  cudaError_t e;
+#define CSA2_ATT(F)                                                                                          \
+  do {                                                                                                       \
+    e = cudaFuncSetAttribute(attend_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes); \
+    if (e == cudaSuccess) attend_kernel<F><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);                     \
+  } while (0)
+  if (kv_fmt == 1) CSA2_ATT(1);
+  else if (kv_fmt == 2) CSA2_ATT(2);
+  else CSA2_ATT(0);
+#undef CSA2_ATT
+  if (e != cudaSuccess) return e;
   *n_launch += 1;
   return cudaGetLastError();
 }
 
-cudaError_t launch_attend_window(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+cudaError_t launch_attend_window(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                  int* n_launch) {
   if (p.n_query == 0 || !pl.split_window) return cudaSuccess;
   attach_ws(p, pl, ws);
@@ -661,10 +706,10 @@ cudaError_t launch_attend_window(cudaStream_t st, int kv_fp8, AttendParams p, co
   p.lead_single = 0;
   p.slot_base = 0;
   p.direct = 0;
-  return launch_tiles(st, kv_fp8, p, n_launch);
+  return launch_tiles(st, kv_fmt, p, n_launch);
 }
 
-cudaError_t launch_attend_main(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                int* n_launch) {
   if (p.n_query == 0) return cudaSuccess;
   attach_ws(p, pl, ws);
@@ -683,7 +728,7 @@ cudaError_t launch_attend_main(cudaStream_t st, int kv_fp8, AttendParams p, cons
     p.slot_base = 0;
     p.direct = pl.ns == 1 ? 1 : 0;
   }
-  return launch_tiles(st, kv_fp8, p, n_launch);
+  return launch_tiles(st, kv_fmt, p, n_launch);
 }
 
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch) {
@@ -694,7 +739,7 @@ cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPla
   return cudaGetLastError();
 }
 
-cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch) {
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch) {
   const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
   cudaError_t e;
   if (pl.split_window) {
@@ -710,9 +755,9 @@ cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams
     a.lead_single = 1;
     a.slot_base = 0;
     a.direct = 0;
-    e = launch_tiles(st, kv_fp8, a, n_launch);
+    e = launch_tiles(st, kv_fmt, a, n_launch);
   } else {
-    e = launch_attend_main(st, kv_fp8, p, pl, ws, n_launch);
+    e = launch_attend_main(st, kv_fmt, p, pl, ws, n_launch);
   }
   if (e == cudaSuccess) e = launch_attend_merge(st, p, pl, ws, n_launch);
   return e;

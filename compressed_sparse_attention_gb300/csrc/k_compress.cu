@@ -13,7 +13,8 @@ namespace csa2 {
 // ---------------------------------------------------------------------------
 // store_rows: one warp per row; lane owns DIM/32 contiguous channels.
 // ---------------------------------------------------------------------------
-template <int DIM, bool FP8>
+// FMT: 0 bf16, 1 fp8 (e4m3 + ue8m0 / 32), 2 fp4 (e2m1 + e4m3 / 16), 3 mxfp4 (e2m1 + ue8m0 / 32)
+template <int DIM, int FMT>
 __global__ void __launch_bounds__(256) store_rows_kernel(const float* __restrict__ rows, int64_t n_rows,
                                                          const int64_t* __restrict__ pos, RopeParams rp,
                                                          void* __restrict__ out, uint8_t* __restrict__ out_scale) {
@@ -43,14 +44,14 @@ __global__ void __launch_bounds__(256) store_rows_kernel(const float* __restrict
       }
     }
   }
-  if constexpr (!FP8) {
+  if constexpr (FMT == 0) {
     uint32_t w[E / 2];
 #pragma unroll
     for (int k = 0; k < E / 2; ++k) w[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
     uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + row * DIM + lane * E);
 #pragma unroll
     for (int k = 0; k < E / 4; ++k) dst[k] = make_uint2(w[2 * k], w[2 * k + 1]);
-  } else {
+  } else if constexpr (FMT == 1) {
     constexpr int LPB = 32 / E;  // lanes per 32-channel block
     float amax = 0.f;
 #pragma unroll
@@ -68,6 +69,27 @@ __global__ void __launch_bounds__(256) store_rows_kernel(const float* __restrict
       *reinterpret_cast<uint32_t*>(dst + k) = word;
     }
     if ((lane % LPB) == 0) out_scale[row * (DIM / 32) + lane / LPB] = (uint8_t)eb;
+  } else {
+    constexpr int BLK = (FMT == 2) ? 16 : 32;  // channels per scale
+    constexpr int LPB = (BLK / E) > 0 ? BLK / E : 1;  // lanes per block
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(v[k]));
+#pragma unroll
+    for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    float sc;
+    uint32_t sbyte;
+    if constexpr (FMT == 2) {
+      sbyte = fp4_scale_e4m3(amax);
+      sc = e4m3_value(sbyte);
+    } else {
+      sbyte = mxfp4_scale_byte(amax);
+      sc = ue8m0_value(sbyte);
+    }
+    uint8_t* dst = reinterpret_cast<uint8_t*>(out) + row * (DIM / 2) + lane * (E / 2);
+#pragma unroll
+    for (int k = 0; k < E; k += 2) dst[k / 2] = (uint8_t)(e2m1_code(v[k], sc) | (e2m1_code(v[k + 1], sc) << 4));
+    if ((lane % LPB) == 0) out_scale[row * (DIM / BLK) + lane / LPB] = (uint8_t)sbyte;
   }
 }
 
@@ -96,7 +118,8 @@ __device__ __forceinline__ int find_segment_warp(const int64_t* __restrict__ off
   return lo;
 }
 
-template <bool KV_FP8, bool IDX_FP8>
+// KVF: pool rows 0 bf16, 1 fp8, 2 fp4 (e4m3 / 16); IKF: keys 0 bf16, 1 fp8, 3 mxfp4
+template <int KVF, int IKF>
 __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
     const int64_t* __restrict__ tok_off, const int64_t* __restrict__ first_pos,
@@ -214,14 +237,25 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
       const float kinv = 1.0f / sqrtf(kss / (float)idx_dim + eps);
       const int o = warp * 32 + lane;
       const float kv = k_lin_s[o] * kinv * knw;
-      if constexpr (!IDX_FP8) {
+      if constexpr (IKF == 0) {
         reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] = (uint16_t)(pack_bf16(kv, 0.f) & 0xFFFFu);
-      } else {
+      } else if constexpr (IKF == 1) {
         float amax = fabsf(kv);
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
         const uint32_t eb = fp8_scale_byte(amax);
         reinterpret_cast<uint8_t*>(idx_keys)[prow * idx_dim + o] = f32_to_e4m3(ldexpf(kv, 127 - (int)eb));
+        if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + warp] = (uint8_t)eb;
+      }
+      else {
+        // mxfp4: this warp's 32 outputs are one scale block; lanes 2i, 2i+1 share a byte
+        float amax = fabsf(kv);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+        const uint32_t eb = mxfp4_scale_byte(amax);
+        const uint32_t code = e2m1_code(kv, ue8m0_value(eb));
+        const uint32_t partner = __shfl_xor_sync(0xffffffffu, code, 1);
+        if ((lane & 1) == 0) reinterpret_cast<uint8_t*>(idx_keys)[prow * (idx_dim / 2) + o / 2] = (uint8_t)(code | (partner << 4));
         if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + warp] = (uint8_t)eb;
       }
     }
@@ -234,9 +268,9 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     ch[0] = x0 * cs - x1 * sn;
     ch[1] = x0 * sn + x1 * cs;
   }
-  if constexpr (!KV_FP8) {
+  if constexpr (KVF == 0) {
     *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(pool_kv) + prow * kDim + c0) = pack_bf16(ch[0], ch[1]);
-  } else {
+  } else if constexpr (KVF == 1) {
     float amax = fmaxf(fabsf(ch[0]), fabsf(ch[1]));
 #pragma unroll
     for (int sh = 1; sh < 16; sh <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
@@ -245,6 +279,16 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const uint32_t word = (uint32_t)f32_to_e4m3(ldexpf(ch[0], sh)) | ((uint32_t)f32_to_e4m3(ldexpf(ch[1], sh)) << 8);
     *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(pool_kv) + prow * kDim + c0) = (uint16_t)word;
     if ((tid & 15) == 0) pool_kv_scale[prow * (kDim / 32) + tid / 16] = (uint8_t)eb;
+  } else {
+    // fp4: 16 channels (8 threads) per e4m3 scale; the thread's two channels share a byte
+    float amax = fmaxf(fabsf(ch[0]), fabsf(ch[1]));
+#pragma unroll
+    for (int sh = 1; sh < 8; sh <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
+    const uint32_t sb = fp4_scale_e4m3(amax);
+    const float sc = e4m3_value(sb);
+    reinterpret_cast<uint8_t*>(pool_kv)[prow * (kDim / 2) + tid] =
+        (uint8_t)(e2m1_code(ch[0], sc) | (e2m1_code(ch[1], sc) << 4));
+    if ((tid & 7) == 0) pool_kv_scale[prow * (kDim / 16) + tid / 8] = (uint8_t)sb;
   }
 }
 
@@ -252,25 +296,37 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
-                              const RopeParams& rp, int fp8, void* out, uint8_t* out_scale) {
+                              const RopeParams& rp, int fmt, void* out, uint8_t* out_scale) {
   if (n_rows == 0) return cudaSuccess;
   const int rows_per_block = 8;
   const dim3 grid((unsigned)((n_rows + rows_per_block - 1) / rows_per_block));
+#define CSA2_STORE(D, F) store_rows_kernel<D, F><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale)
   if (dim == 512) {
-    if (fp8) store_rows_kernel<512, true><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
-    else store_rows_kernel<512, false><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+    switch (fmt) {
+      case 0: CSA2_STORE(512, 0); break;
+      case 1: CSA2_STORE(512, 1); break;
+      case 2: CSA2_STORE(512, 2); break;
+      case 3: CSA2_STORE(512, 3); break;
+      default: return cudaErrorInvalidValue;
+    }
   } else {
-    if (fp8) store_rows_kernel<128, true><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
-    else store_rows_kernel<128, false><<<grid, 256, 0, st>>>(rows, n_rows, pos, rp, out, out_scale);
+    switch (fmt) {
+      case 0: CSA2_STORE(128, 0); break;
+      case 1: CSA2_STORE(128, 1); break;
+      case 2: CSA2_STORE(128, 2); break;
+      case 3: CSA2_STORE(128, 3); break;
+      default: return cudaErrorInvalidValue;
+    }
   }
+#undef CSA2_STORE
   return cudaGetLastError();
 }
 
 cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
                             int n_seq, const int64_t* tok_off, const int64_t* first_pos,
                             const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
-                            const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fp8,
-                            int idx_fp8, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
+                            const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fmt,
+                            int idx_fmt, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
                             uint8_t* idx_key_scale, uint32_t* flags) {
   if (n_groups == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_groups);
@@ -278,11 +334,16 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   compress_kernel<KF, IF><<<grid, kCmpThreads, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
                                                 norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
                                                 pool_kv_scale, idx_keys, idx_key_scale, flags)
-  if (kv_fp8) {
-    if (idx_fp8) CSA2_COMPRESS(true, true); else CSA2_COMPRESS(true, false);
-  } else {
-    if (idx_fp8) CSA2_COMPRESS(false, true); else CSA2_COMPRESS(false, false);
-  }
+#define CSA2_COMPRESS_K(KF)                               \
+  do {                                                    \
+    if (idx_fmt == 1) CSA2_COMPRESS(KF, 1);               \
+    else if (idx_fmt == 3) CSA2_COMPRESS(KF, 3);          \
+    else CSA2_COMPRESS(KF, 0);                            \
+  } while (0)
+  if (kv_fmt == 1) CSA2_COMPRESS_K(1);
+  else if (kv_fmt == 2) CSA2_COMPRESS_K(2);
+  else CSA2_COMPRESS_K(0);
+#undef CSA2_COMPRESS_K
 #undef CSA2_COMPRESS
   return cudaGetLastError();
 }

@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(
 // for each block b; mma step (b, s) covers channels 32b + 8t + 4s + {0..3},
 // so one step never mixes two scale blocks. Codes convert exactly to bf16;
 // each block's partial dot product is scaled by its power of two in fp32.
-template <int NT>
+// KF 1: e4m3 codes (128 B a key); KF 3: E2M1 codes two to a byte (64 B a key);
+// both with a ue8m0 scale per 32 channels
+template <int NT, int KF>
 __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
     int n_query, int n_seq, int64_t n_chunks, int64_t max_vis, const uint16_t* __restrict__ q_idx,
     const float* __restrict__ w_heads, const uint8_t* __restrict__ keys, const uint8_t* __restrict__ key_scale,
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
           if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_NVIS_TOO_LARGE);
           nv = (int)min(plen, max_vis);
         }
-        kbase = keys + pool_off[b] * kIdxDim;
+        kbase = keys + pool_off[b] * (KF == 3 ? kIdxDim / 2 : kIdxDim);
         sbase = key_scale + pool_off[b] * (kIdxDim / 32);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -175,8 +177,13 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
       const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
-        ca[u][bb] = ldg_stream8(kbase + ra * kIdxDim + 32 * bb + 8 * t);
-        cb[u][bb] = ldg_stream8(kbase + rb * kIdxDim + 32 * bb + 8 * t);
+        if constexpr (KF == 3) {  // 8 codes in 4 bytes
+          ca[u][bb] = make_uint2(*reinterpret_cast<const uint32_t*>(kbase + ra * (kIdxDim / 2) + 16 * bb + 4 * t), 0u);
+          cb[u][bb] = make_uint2(*reinterpret_cast<const uint32_t*>(kbase + rb * (kIdxDim / 2) + 16 * bb + 4 * t), 0u);
+        } else {
+          ca[u][bb] = ldg_stream8(kbase + ra * kIdxDim + 32 * bb + 8 * t);
+          cb[u][bb] = ldg_stream8(kbase + rb * kIdxDim + 32 * bb + 8 * t);
+        }
       }
       sa[u] = *reinterpret_cast<const uint32_t*>(sbase + ra * 4);
       sb[u] = *reinterpret_cast<const uint32_t*>(sbase + rb * 4);
@@ -188,9 +195,18 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
       for (int nt = 0; nt < NT; ++nt) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
-        // exact e4m3 -> bf16 of this block's 8 codes per row
+        // exact e4m3 -> bf16 (or E2M1 -> 2^-14 times its value, in bf16) of
+        // this block's 8 codes per row
         uint32_t a[4], b[4];
-        {
+        if constexpr (KF == 3) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 fa = e2m1x2_to_float2_scaled((ca[u][bb].x >> (8 * k)) & 0xFFu);
+            const float2 fb = e2m1x2_to_float2_scaled((cb[u][bb].x >> (8 * k)) & 0xFFu);
+            a[k] = pack_bf16(fa.x, fa.y);
+            b[k] = pack_bf16(fb.x, fb.y);
+          }
+        } else {
           const float2 f0 = e4m3x2_to_float2((uint16_t)(ca[u][bb].x & 0xFFFF));
           const float2 f1 = e4m3x2_to_float2((uint16_t)(ca[u][bb].x >> 16));
           const float2 f2 = e4m3x2_to_float2((uint16_t)(ca[u][bb].y & 0xFFFF));
@@ -204,8 +220,9 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
           b[0] = pack_bf16(h0.x, h0.y); b[1] = pack_bf16(h1.x, h1.y);
           b[2] = pack_bf16(h2.x, h2.y); b[3] = pack_bf16(h3.x, h3.y);
         }
-        const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu);
-        const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu);
+        const float unscale = KF == 3 ? kE2M1Unscale : 1.0f;
+        const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu) * unscale;
+        const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu) * unscale;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -236,7 +253,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
   }
 }
 
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fp8, int n_query, int n_seq,
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, int n_query, int n_seq,
                                int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
                                const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
                                const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags) {
@@ -247,8 +264,12 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
   const dim3 grid((unsigned)(items < cap ? items : cap));
 #define CSA2_IDX(NT)                                                                                   \
   do {                                                                                                 \
-    if (idx_fp8)                                                                                       \
-      index_score_fp8_kernel<NT><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
+    if (idx_fmt == 1)                                                                                  \
+      index_score_fp8_kernel<NT, 1><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
+                                                       (const uint8_t*)keys, key_scale, pool_off,      \
+                                                       seq_of_q, n_vis, scores, ld, flags);            \
+    else if (idx_fmt == 3)                                                                             \
+      index_score_fp8_kernel<NT, 3><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
                                                        (const uint8_t*)keys, key_scale, pool_off,      \
                                                        seq_of_q, n_vis, scores, ld, flags);            \
     else                                                                                               \

@@ -41,13 +41,13 @@ struct AttendParams {
 };
 
 cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
-                              const RopeParams& rp, int fp8, void* out, uint8_t* out_scale);
+                              const RopeParams& rp, int fmt, void* out, uint8_t* out_scale);
 cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
                             int n_seq, const int64_t* tok_off, const int64_t* first_pos, const int64_t* pool_off,
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
-                            float eps, const RopeParams& rp, int kv_fp8, int idx_fp8, void* pool_kv,
+                            float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
                             uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags);
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fp8, int n_query, int n_seq,
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, int n_query, int n_seq,
                                int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
                                const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
                                const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags);
@@ -70,11 +70,11 @@ struct AttendPlan {
 int attend_num_tiles(int topk, bool has_idx);
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
 size_t attend_workspace_bytes(int n_query, const AttendPlan& pl);
-cudaError_t launch_attend_window(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+cudaError_t launch_attend_window(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                  int* n_launch);
-cudaError_t launch_attend_main(cudaStream_t st, int kv_fp8, AttendParams p, const AttendPlan& pl, void* ws,
+cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                int* n_launch);
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);
-cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fp8, AttendParams p, void* ws, int* n_launch);
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch);
 
 }  // namespace csa2

@@ -21,7 +21,15 @@
  *   - Rows are row-major with the last axis contiguous. bf16 values travel as
  *     uint16_t bit patterns. The fp8 format (CSA2_KV_FP8_E4M3_B32) stores one
  *     e4m3 byte per channel plus one ue8m0 scale byte (value 2^(E-127)) per 32
- *     consecutive channels, in a separate [rows, dim/32] byte array.
+ *     consecutive channels, in a separate [rows, dim/32] byte array. The fp4
+ *     formats store E2M1 codes (grid 0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6)
+ *     two per byte, the even channel in the low nibble ([rows, dim/2] bytes):
+ *     CSA2_KV_FP4_E4M3_B16 with one e4m3 scale byte per 16 channels
+ *     ([rows, dim/16]), the scale e4m3(max(amax, 6*2^-9) / 6); CSA2_KV_MXFP4_B32
+ *     with one ue8m0 scale byte per 32 channels ([rows, dim/32]), the scale
+ *     2^round(log2(max(amax, 6*2^-126) / 6)) ("Reading Notes ...", 3f C4;
+ *     PocketLLM page, "The op layer"). Codes round to the nearest grid value,
+ *     ties to the even code, saturating at +-6.
  *   - `stream` is a cudaStream_t passed as void*; every call only enqueues
  *     work on it (asynchronous, stream-ordered) and returns after host-side
  *     argument validation.
@@ -67,7 +75,13 @@ typedef enum csa2_mode {
 
 typedef enum csa2_kv_format {
   CSA2_KV_BF16 = 0,
-  CSA2_KV_FP8_E4M3_B32 = 1 /* e4m3 codes + one ue8m0 scale per 32 channels */
+  CSA2_KV_FP8_E4M3_B32 = 1, /* e4m3 codes + one ue8m0 scale per 32 channels */
+  /* attention KV (kv_format) only: compressed pool rows fp4 with an e4m3
+     scale per 16 channels; window rows stay fp8 (CSA2_KV_FP8_E4M3_B32), as
+     the pages keep the sliding-window cache in FP8 ("Reading Notes ...", 3f C4) */
+  CSA2_KV_FP4_E4M3_B16 = 2,
+  /* index keys (idx_key_format) only: fp4 with a ue8m0 scale per 32 channels */
+  CSA2_KV_MXFP4_B32 = 3
 } csa2_kv_format;
 
 /* Device error word bits (csa2_check / csa2_device_flags). */
@@ -84,7 +98,7 @@ typedef enum csa2_kv_format {
  *   n_heads 64, head_dim 512, rope_dim 0 or 64 (the last rope_dim channels
  *   are rotated, adjacent pairs), window 1..128, compress_ratio 1..16,
  *   idx_heads 8/16/32, idx_dim 128, topk 1..2048 (multiple of 1),
- *   kv_format / idx_key_format a csa2_kv_format.
+ *   kv_format bf16 / fp8 / fp4-e4m3-b16, idx_key_format bf16 / fp8 / mxfp4.
  * softmax_scale multiplies q.k (1/sqrt(512)); the sink is a logit on the
  * same scale. RoPE frequencies follow YaRN (DeepSeek-V3 ramp): rope_theta,
  * yarn_factor (<= 1 disables the ramp), yarn_orig_len, yarn_beta_fast/slow. */

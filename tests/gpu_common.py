@@ -9,6 +9,10 @@ Tolerances (derivations are in the repository's design notes):
               (relative 1e-3, plus the fp32 accumulation bound of a 128-term dot)
   top-k     : bit-exact on identical fp32 scores
   stored rows (bf16): |gpu - oracle| <= 1 bf16 ulp of the oracle value + 1e-5 * row rms
+  stored rows (fp4/mxfp4, from values the GPU computes in fp32): per block of
+              scale s, |stored - exact| <= s + max(0, amax - 6 s) (half the
+              widest e2m1 gap, or the saturation), the scale byte within one
+              code of the oracle's
 """
 from __future__ import annotations
 
@@ -74,6 +78,79 @@ def oracle_fp8_rows(x_f32: np.ndarray):
     """The oracle's own fp8 block-32 quantisation of fp32 rows: (codes, exps, values)."""
     codes, exps = F.fp8_block_quantize(x_f32)
     return codes, exps, F.fp8_block_dequantize(codes, exps)
+
+
+# storage format codes of the library (kv_format / idx_key_format)
+FMT_BF16, FMT_FP8, FMT_FP4, FMT_MXFP4 = 0, 1, 2, 3
+SCALE_BLOCK = {FMT_FP8: 32, FMT_FP4: 16, FMT_MXFP4: 32}
+
+
+def code_bytes(dim: int, fmt: int) -> int:
+    """Bytes of one stored row's codes (scales excluded)."""
+    return {FMT_BF16: 2 * dim, FMT_FP8: dim, FMT_FP4: dim // 2, FMT_MXFP4: dim // 2}[fmt]
+
+
+def stored_values(codes, scale, fmt: int) -> np.ndarray:
+    """Exact values of rows stored in format `fmt`, decoded by the oracle."""
+    if fmt == FMT_BF16:
+        return bf16_np(codes)
+    c = codes.cpu().numpy() if isinstance(codes, torch.Tensor) else codes
+    sc = scale.cpu().numpy() if isinstance(scale, torch.Tensor) else scale
+    if fmt == FMT_FP8:
+        return F.fp8_block_dequantize(c, sc)
+    if fmt == FMT_FP4:
+        return F.fp4_block_dequantize(F.unpack_e2m1(c), sc)
+    if fmt == FMT_MXFP4:
+        return F.mxfp4_block_dequantize(F.unpack_e2m1(c), sc)
+    raise ValueError(fmt)
+
+
+def oracle_stored(x: np.ndarray, fmt: int) -> np.ndarray:
+    """The oracle's own stored form of float64 rows: quantise, then decode."""
+    if fmt == FMT_BF16:
+        return F.round_bf16(x)
+    if fmt == FMT_FP8:
+        return F.fp8_block_dequantize(*F.fp8_block_quantize(x))
+    if fmt == FMT_FP4:
+        return F.fp4_block_dequantize(*F.fp4_block_quantize(x))
+    if fmt == FMT_MXFP4:
+        return F.mxfp4_block_dequantize(*F.mxfp4_block_quantize(x))
+    raise ValueError(fmt)
+
+
+def scale_values(scale, fmt: int) -> np.ndarray:
+    sc = scale.cpu().numpy() if isinstance(scale, torch.Tensor) else np.asarray(scale)
+    return F.e4m3_bits_to_f64(sc) if fmt == FMT_FP4 else F.ue8m0_to_f64(sc)
+
+
+def storage_bound(exact: np.ndarray, scale, fmt: int) -> np.ndarray:
+    """Per element bound on |stored - exact| for rows the GPU quantised from
+    values it computed in fp32 (so either neighbour of a grid midpoint may be
+    taken): one bf16 ulp; one e4m3 step (2^-3 relative, 2^-9 of the scale
+    below the normal range); for e2m1 half the widest gap (2 s) plus what
+    saturation at 6 s clips."""
+    if fmt == FMT_BF16:
+        rms = np.sqrt(np.mean(exact * exact, axis=-1, keepdims=True))
+        return F.bf16_ulp(exact) + 1e-5 * rms
+    blk = SCALE_BLOCK[fmt]
+    s = scale_values(scale, fmt)
+    if fmt == FMT_FP8:
+        return 2.0 ** -3 * np.abs(exact) + 2.0 ** -9 * np.repeat(s, blk, axis=-1) + 1e-30
+    amax = np.abs(exact).reshape(*exact.shape[:-1], -1, blk).max(axis=-1)
+    per_block = s + np.maximum(0.0, amax * (1 + 1e-6) - 6.0 * s)
+    return np.repeat(per_block, blk, axis=-1) + 1e-6 * np.abs(exact) + 1e-30
+
+
+def assert_rows_close_stored(codes, scale, exact: np.ndarray, fmt: int, what: str = ""):
+    """Rows the GPU stored against the float64 values they encode; for the
+    scaled formats also the scale bytes against the oracle's (within one code)."""
+    got = stored_values(codes, scale, fmt)
+    bad = np.abs(got - exact) > storage_bound(exact, scale, fmt)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, worst {float(np.abs(got - exact).max()):.3e}"
+    if fmt in (FMT_FP4, FMT_MXFP4):
+        ref_sc = (F.fp4_block_quantize(exact) if fmt == FMT_FP4 else F.mxfp4_block_quantize(exact))[1]
+        d = np.abs(scale.cpu().numpy().astype(np.int32) - ref_sc.astype(np.int32))
+        assert d.max(initial=0) <= 1, f"{what}: scale bytes differ by {int(d.max())} codes"
 
 
 def attention_bound(q, t, rows, sink, scale, f) -> np.ndarray:

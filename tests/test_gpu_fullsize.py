@@ -18,24 +18,23 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import (assert_attention_close, assert_rows_close_bf16, assert_rows_close_fp8, attention_bound,
-                        bf16_np, check_topk_valid, context, f32_np, geometry, inv_freq, require_gpu,
-                        score_tolerance)
+from gpu_common import (FMT_BF16, FMT_FP8, SCALE_BLOCK, assert_attention_close, assert_rows_close_stored,
+                        attention_bound, bf16_np, check_topk_valid, code_bytes, context, f32_np, geometry, inv_freq,
+                        oracle_stored, require_gpu, score_tolerance, storage_bound)
 from oracle import csa2_oracle as O
-from oracle import formats as F
 from workloads import PRESETS, make_inputs
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = "cuda"
 
 
-def _to_fp8(ctx, x, dim):
-    from compressed_sparse_attention_gb300 import binding
-    codes = torch.empty(x.shape, dtype=torch.uint8, device=DEV)
-    sc = torch.empty((x.shape[0], dim // 32), dtype=torch.uint8, device=DEV)
+def _to_stored(ctx, x, dim, fmt):
+    """fp32 generator rows stored by csa2_store_rows in format `fmt` (codes, scales)."""
+    codes = torch.empty((x.shape[0], code_bytes(dim, fmt)), dtype=torch.uint8, device=DEV)
+    sc = torch.empty((x.shape[0], dim // SCALE_BLOCK[fmt]), dtype=torch.uint8, device=DEV)
     step = 1 << 20
     for i in range(0, x.shape[0], step):
-        ctx.store_rows(x[i:i + step], None, binding.KV_FP8, codes[i:i + step], sc[i:i + step])
+        ctx.store_rows(x[i:i + step], None, fmt, codes[i:i + step], sc[i:i + step])
     return codes, sc
 
 
@@ -50,11 +49,11 @@ class Case:
                 if k in base.inp:
                     inp[k] = base.inp[k]
         if wl.kv_fp8:
-            inp["win_kv"], inp["win_scale"] = _to_fp8(ctx, inp["win_kv_f32"], 512)
+            inp["win_kv"], inp["win_scale"] = _to_stored(ctx, inp["win_kv_f32"], 512, FMT_FP8)
             if base is None:
-                inp["pool_kv"], inp["pool_scale"] = _to_fp8(ctx, inp["pool_kv_f32"], 512)
+                inp["pool_kv"], inp["pool_scale"] = _to_stored(ctx, inp["pool_kv_f32"], 512, wl.kv_format)
         if wl.idx_fp8 and base is None:
-            inp["idx_keys"], inp["idx_key_scale"] = _to_fp8(ctx, inp["idx_keys_f32"], 128)
+            inp["idx_keys"], inp["idx_key_scale"] = _to_stored(ctx, inp["idx_keys_f32"], 128, wl.idx_key_format)
         torch.cuda.synchronize()
         self.inp, self.wl = inp, wl
 
@@ -81,18 +80,12 @@ def _step(ctx, case, mode, topk_idx):
     return out, scores
 
 
-def _rows_np(t_rows, t_scale, wl):
-    """Exact values of stored rows as the oracle reads them."""
-    if t_scale is None:
-        return bf16_np(t_rows)
-    return F.fp8_block_dequantize(t_rows.cpu().numpy(), t_scale.cpu().numpy())
-
-
-def _oracle_rows(src_f32, src_bf16, wl, fp8):
-    """The oracle's own copy of stored rows from the generator values."""
-    if fp8:
-        return F.fp8_block_dequantize(*F.fp8_block_quantize(f32_np(src_f32)))
-    return bf16_np(src_bf16)
+def _oracle_rows(src_f32, src_bf16, fmt):
+    """The oracle's own copy of stored rows from the generator values (bf16
+    rows are drawn as bf16; the scaled formats from fp32 values)."""
+    if fmt == FMT_BF16:
+        return bf16_np(src_bf16)
+    return oracle_stored(f32_np(src_f32), fmt)
 
 
 def _check_query(ctx, case, qi, geom, f, out_step, scores_step, sel_step, oracle_state, tag, borrowed=None):
@@ -107,7 +100,7 @@ def _check_query(ctx, case, qi, geom, f, out_step, scores_step, sel_step, oracle
     woff = i["win_off"].cpu().numpy()
     cap = int(woff[b + 1] - woff[b])
     win_rows = _oracle_rows(i.get("win_kv_f32", None)[woff[b]:woff[b + 1]] if wl.kv_fp8 else None,
-                            i["win_kv"][woff[b]:woff[b + 1]] if not wl.kv_fp8 else None, wl, wl.kv_fp8)
+                            i["win_kv"][woff[b]:woff[b + 1]] if not wl.kv_fp8 else None, int(wl.kv_fp8))
     q = bf16_np(i["q"][qi])
     sink = f32_np(i["sink"])
     if scores_step is not None:
@@ -152,6 +145,7 @@ def _full_state(ctx, case, geom, f):
     i, wl = case.inp, case.wl
     poff = i["pool_off"].cpu().numpy()
     tok_off = i["tok_off"].cpu().numpy()
+    kfmt, pfmt = wl.idx_key_format, wl.kv_format
     cache = {}
 
     def state(b):
@@ -159,44 +153,30 @@ def _full_state(ctx, case, geom, f):
             return cache[b]
         r0, r1 = int(poff[b]), int(poff[b + 1])
         keys = _oracle_rows(i.get("idx_keys_f32", None)[r0:r1] if wl.idx_fp8 else None,
-                            i["idx_keys"][r0:r1] if not wl.idx_fp8 else None, wl, wl.idx_fp8)
+                            i["idx_keys"][r0:r1] if not wl.idx_fp8 else None, kfmt)
         pool_src = i.get("pool_kv_f32") if wl.kv_fp8 else i["pool_kv"]
         t0, t1 = int(tok_off[b]), int(tok_off[b + 1])
         j0 = int(i["first_pos"][b]) // wl.m
         g = (t1 - t0) // wl.m
+        new_rows, key_step = None, None
         if g:
             kv, _, kidx = O.compress(bf16_np(i["raw"][t0:t1]), f32_np(i["gate"][t0:t1]), wl.m,
                                      int(i["first_pos"][b]), f32_np(i["norm_w"]), geom.norm_eps, f,
                                      bf16_np(i["w_idx"]), f32_np(i["k_norm_w"]))
-            # the stored forms of the new entries, and the GPU's against them
-            if wl.idx_fp8:
-                keys[j0:j0 + g] = F.fp8_block_dequantize(*F.fp8_block_quantize(kidx))
-                got_k = _rows_np(i["idx_keys"][r0 + j0:r0 + j0 + g], i["idx_key_scale"][r0 + j0:r0 + j0 + g], wl)
-                assert_rows_close_fp8(got_k, kidx, F.ue8m0_to_f64(i["idx_key_scale"][r0 + j0:r0 + j0 + g].cpu().numpy()))
-            else:
-                keys[j0:j0 + g] = F.round_bf16(kidx)
-                assert_rows_close_bf16(bf16_np(i["idx_keys"][r0 + j0:r0 + j0 + g]), kidx, f"keys seq {b}")
-            new_rows = kv
-            if wl.kv_fp8:
-                got = _rows_np(i["pool_kv"][r0 + j0:r0 + j0 + g], i["pool_scale"][r0 + j0:r0 + j0 + g], wl)
-                assert_rows_close_fp8(got, kv, F.ue8m0_to_f64(i["pool_scale"][r0 + j0:r0 + j0 + g].cpu().numpy()))
-                new_rows = F.fp8_block_dequantize(*F.fp8_block_quantize(kv))
-            else:
-                assert_rows_close_bf16(bf16_np(i["pool_kv"][r0 + j0:r0 + j0 + g]), kv, f"kv seq {b}")
-                new_rows = F.round_bf16(kv)
-        else:
-            new_rows = None
-        pool = _LazyPool(pool_src, r0, r1, wl.kv_fp8, j0, new_rows)
-        if g:
-            if wl.idx_fp8:
-                sc = F.ue8m0_to_f64(i["idx_key_scale"][r0 + j0:r0 + j0 + g].cpu().numpy())
-                step_ = 2.0 ** -3 * np.abs(keys[j0:j0 + g]) + 2.0 ** -9 * np.repeat(sc, 32, axis=-1)
-            else:
-                step_ = F.bf16_ulp(keys[j0:j0 + g])
+            # the GPU's stored forms of the new entries against the exact values,
+            # and the oracle's own stored forms in the state it scores with
+            new = slice(r0 + j0, r0 + j0 + g)
+            k_sc = i.get("idx_key_scale")[new] if kfmt != FMT_BF16 else None
+            p_sc = i.get("pool_scale")[new] if pfmt != FMT_BF16 else None
+            assert_rows_close_stored(i["idx_keys"][new], k_sc, kidx, kfmt, f"keys seq {b}")
+            assert_rows_close_stored(i["pool_kv"][new], p_sc, kv, pfmt, f"kv seq {b}")
+            keys[j0:j0 + g] = oracle_stored(kidx, kfmt)
+            new_rows = oracle_stored(kv, pfmt)
+            # the GPU's stored key and the oracle's each lie within one bound of
+            # the exact key
             key_step = np.zeros_like(keys)
-            key_step[j0:j0 + g] = step_
-        else:
-            key_step = None
+            key_step[j0:j0 + g] = 2.0 * storage_bound(kidx, k_sc, kfmt)
+        pool = _LazyPool(pool_src, r0, r1, pfmt, j0, new_rows)
         cache[b] = (keys, pool, (j0, j0 + g), key_step)
         return cache[b]
 
@@ -208,13 +188,13 @@ class _LazyPool:
     values on demand (a 1M-context pool is 256K rows), with this step's new
     entries in the oracle's own stored form."""
 
-    def __init__(self, src, r0, r1, fp8, j0, new_rows):
-        self.src, self.r0, self.n, self.fp8, self.j0, self.new = src, r0, r1 - r0, fp8, j0, new_rows
+    def __init__(self, src, r0, r1, fmt, j0, new_rows):
+        self.src, self.r0, self.n, self.fmt, self.j0, self.new = src, r0, r1 - r0, fmt, j0, new_rows
 
     def __getitem__(self, idx):
         idx = np.asarray(idx)
         rows = self.src[torch.as_tensor(self.r0 + idx, device=self.src.device)]
-        vals = (F.fp8_block_dequantize(*F.fp8_block_quantize(f32_np(rows))) if self.fp8 else bf16_np(rows))
+        vals = _oracle_rows(rows, rows, self.fmt)
         if self.new is not None:
             hit = (idx >= self.j0) & (idx < self.j0 + self.new.shape[0])
             vals[hit] = self.new[idx[hit] - self.j0]
@@ -225,8 +205,8 @@ def _run_full(preset, sample):
     require_gpu()
     from compressed_sparse_attention_gb300 import binding
     wl = PRESETS[preset]
-    ctx = context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=int(wl.kv_fp8),
-                  idx_key_format=int(wl.idx_fp8))
+    ctx = context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=wl.kv_format,
+                  idx_key_format=wl.idx_key_format)
     geom = geometry(ctx.cfg)
     f = inv_freq(geom)
     case = Case(ctx, wl)
@@ -244,6 +224,12 @@ def test_fullsize_decode_64k_b32():
 
 def test_fullsize_decode_1m_b8_fp8():
     same = _run_full("decode_1m_b8_fp8", [0, 7])
+    assert sum(same) >= 1
+
+
+def test_fullsize_decode_1m_b8_fp4():
+    """fp4 pool rows, an fp8 window and mxfp4 keys at 1M context."""
+    same = _run_full("decode_1m_b8_fp4", [0, 7])
     assert sum(same) >= 1
 
 

@@ -9,9 +9,10 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import (assert_attention_close, attention_bound, assert_rows_close_bf16, assert_rows_close_fp8, bf16_np,
-                        check_topk_valid, context, f32_np, geometry, inv_freq, oracle_fp8_rows, require_gpu,
-                        rope_sanity, score_tolerance)
+from gpu_common import (FMT_BF16, SCALE_BLOCK, assert_attention_close, attention_bound, assert_rows_close_bf16,
+                        assert_rows_close_fp8, assert_rows_close_stored, bf16_np, check_topk_valid, code_bytes,
+                        context, f32_np, geometry, inv_freq, oracle_fp8_rows, require_gpu, rope_sanity,
+                        score_tolerance)
 from oracle import csa2_oracle as O
 from oracle import formats as F
 from workloads import Workload, make_inputs, make_selection, make_topk_scores
@@ -306,10 +307,12 @@ def test_topk_bit_exact(n, tie_levels, k):
 # ----------------------------------------------------------------------------- compressor
 
 @pytest.mark.parametrize("m", [1, 2, 4])
-@pytest.mark.parametrize("fp8", [False, True])
-def test_compress(m, fp8):
-    from compressed_sparse_attention_gb300 import binding
-    ctx = context(compress_ratio=m, kv_format=1 if fp8 else 0, idx_key_format=1 if fp8 else 0)
+@pytest.mark.parametrize("fmts", [(0, 0), (1, 1), (2, 3)], ids=["bf16", "fp8", "fp4_mxfp4"])
+def test_compress(m, fmts):
+    """Compressed entries and their index keys stored in each format pair
+    (pool kv_format, index idx_key_format) against the oracle's exact values."""
+    kv_fmt, key_fmt = fmts
+    ctx = context(compress_ratio=m, kv_format=kv_fmt, idx_key_format=key_fmt)
     geom = geometry(ctx.cfg)
     f = inv_freq(geom)
     g = torch.Generator(device=DEV).manual_seed(40 + m)
@@ -326,15 +329,15 @@ def test_compress(m, fp8):
     plen = [first_group[i] + seg_groups[i] + 2 for i in range(3)]
     pool_off = torch.tensor(np.concatenate([[0], np.cumsum(plen)]), dtype=torch.int64, device=DEV)
     P = int(pool_off[-1])
-    if fp8:
-        pool = torch.zeros((P, 512), dtype=torch.uint8, device=DEV)
-        psc = torch.zeros((P, 16), dtype=torch.uint8, device=DEV)
-        keys = torch.zeros((P, 128), dtype=torch.uint8, device=DEV)
-        ksc = torch.zeros((P, 4), dtype=torch.uint8, device=DEV)
-    else:
-        pool = torch.zeros((P, 512), dtype=torch.bfloat16, device=DEV)
-        keys = torch.zeros((P, 128), dtype=torch.bfloat16, device=DEV)
-        psc = ksc = None
+
+    def buffers(dim, fmt):
+        if fmt == FMT_BF16:
+            return torch.zeros((P, dim), dtype=torch.bfloat16, device=DEV), None
+        return (torch.zeros((P, code_bytes(dim, fmt)), dtype=torch.uint8, device=DEV),
+                torch.zeros((P, dim // SCALE_BLOCK[fmt]), dtype=torch.uint8, device=DEV))
+
+    pool, psc = buffers(512, kv_fmt)
+    keys, ksc = buffers(128, key_fmt)
     ctx.compress(raw, gate if m > 1 else None, 3, tok_off, first_pos, pool_off, norm_w, w_idx, k_norm_w,
                  pool, psc, keys, ksc)
     assert ctx.check()[0] == 0
@@ -345,14 +348,8 @@ def test_compress(m, fp8):
                                      geom.norm_eps, f, bf16_np(w_idx), f32_np(k_norm_w))
         r0 = int(pool_off[b]) + first_group[b]
         rows = slice(r0, r0 + seg_groups[b])
-        if fp8:
-            got_kv = F.fp8_block_dequantize(pool[rows].cpu().numpy(), psc[rows].cpu().numpy())
-            assert_rows_close_fp8(got_kv, kv, F.ue8m0_to_f64(psc[rows].cpu().numpy()), f"kv seq {b}")
-            got_k = F.fp8_block_dequantize(keys[rows].cpu().numpy(), ksc[rows].cpu().numpy())
-            assert_rows_close_fp8(got_k, kidx, F.ue8m0_to_f64(ksc[rows].cpu().numpy()), f"key seq {b}")
-        else:
-            assert_rows_close_bf16(bf16_np(pool[rows]), kv, f"kv seq {b}")
-            assert_rows_close_bf16(bf16_np(keys[rows]), kidx, f"key seq {b}")
+        assert_rows_close_stored(pool[rows], None if psc is None else psc[rows], kv, kv_fmt, f"kv seq {b}")
+        assert_rows_close_stored(keys[rows], None if ksc is None else ksc[rows], kidx, key_fmt, f"key seq {b}")
         # rows outside the written groups stay untouched
         assert float(pool[int(pool_off[b]) + first_group[b] + seg_groups[b]].float().abs().sum()) == 0.0
 

@@ -45,13 +45,25 @@ class Workload:
     head_dim: int = 512
     idx_heads: int = 8
     idx_dim: int = 128
-    kv_fp8: bool = False
-    idx_fp8: bool = False
+    kv_fp8: bool = False      # window and pool drawn in fp32 and stored quantised (fp8 unless pool_fp4)
+    idx_fp8: bool = False     # index keys drawn in fp32 and stored quantised (fp8 unless key_fp4)
+    pool_fp4: bool = False    # pool rows stored fp4 e2m1 with an e4m3 scale per 16 (needs kv_fp8)
+    key_fp4: bool = False     # index keys stored mxfp4 with an e8m0 scale per 32 (needs idx_fp8)
     value_std: float = 1.0    # q and KV element std
     outlier_frac: float = 0.0  # fraction of KV rows scaled by outlier_scale
     outlier_scale: float = 8.0
     n_layers: int = 1         # >1: one Reindex layer then Reuse layers sharing pool and idx
     win_linear: bool = False  # window buffer holds every position (prefill) instead of a ring
+
+    @property
+    def kv_format(self) -> int:
+        """The library's kv_format code: 0 bf16, 1 fp8, 2 fp4 pool + fp8 window."""
+        return 2 if self.pool_fp4 else int(self.kv_fp8)
+
+    @property
+    def idx_key_format(self) -> int:
+        """The library's idx_key_format code: 0 bf16, 1 fp8, 3 mxfp4."""
+        return 3 if self.key_fp4 else int(self.idx_fp8)
 
     @property
     def n_query(self) -> int:
@@ -85,6 +97,10 @@ PRESETS = {
     # long-context decode batch 8 at 1,048,576, ratio 4 -> 262,144 entries, fp8 KV and keys
     "decode_1m_b8_fp8": Workload("decode_1m_b8_fp8", 8, (1 << 20,) * 8, 4, seed=3,
                                  kv_fp8=True, idx_fp8=True),
+    # the same decode with fp4 pool rows (e4m3 scale per 16), an fp8 window and
+    # mxfp4 index keys: 256 + 32 B per pool entry and 64 + 4 B per key
+    "decode_1m_b8_fp4": Workload("decode_1m_b8_fp4", 8, (1 << 20,) * 8, 4, seed=5,
+                                 kv_fp8=True, idx_fp8=True, pool_fp4=True, key_fp4=True),
     # mixed serving batch: 64 sequences, lengths log-uniform 1K-256K, ratio 1,
     # one Reindex layer then three Reuse layers
     "mixed_reuse_b64": Workload("mixed_reuse_b64", 64, _log_uniform_lengths(64, 1024, 262144, 4),
