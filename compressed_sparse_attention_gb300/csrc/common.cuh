@@ -54,6 +54,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// f16x2 bits of two floats (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t h2_bits(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// two e4m3 codes (low byte first) -> f16x2 (low half first), exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)(two & 0xFFFFu)));
+  return r;
+}
 // two e4m3 codes (low byte first) -> two floats, exact
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
   __half2_raw h;
@@ -113,6 +124,20 @@ __device__ __forceinline__ float2 e2m1x2_to_float2_scaled(uint32_t two) {
   return __half22float2(__half2(r));
 }
 constexpr float kE2M1Unscale = 16384.0f;  // 2^14
+// eight E2M1 codes (the nibbles n0 .. n7 of w, n0 lowest) -> four f16x2
+// words, each half 2^-14 times its code's value, in the pairs
+// o[0] = (n0, n4), o[1] = (n1, n5), o[2] = (n2, n6), o[3] = (n3, n7) (low
+// half first): a nibble's three magnitude bits go to f16 bits 9..11 (low two
+// exponent bits and the top mantissa bit) and its sign to bit 15, as in the
+// pair decoder above. The pairing puts nibbles i and i + 4 at the same shift,
+// so each word takes two shifts and one three-input logic op.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  constexpr uint32_t kMag = 0x0E000E00u, kSign = 0x80008000u;
+  o[0] = ((w << 9) & kMag) | ((w << 12) & kSign);
+  o[1] = ((w << 5) & kMag) | ((w << 8) & kSign);
+  o[2] = ((w << 1) & kMag) | ((w << 4) & kSign);
+  o[3] = ((w >> 3) & kMag) | (w & kSign);
+}
 // e4m3 byte of the fp4 block scale: e4m3(max(amax, 6 * 2^-9) / 6), the
 // quotient formed in double (exact enough that its rounding to e4m3 equals
 // that of the real quotient) and rounded by CUDA's own conversion
@@ -164,6 +189,11 @@ __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
   return r;
 }
 __device__ __forceinline__ uint2 ldg_stream8(const void* p) {
@@ -306,6 +336,14 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // ---------------------------------------------------------------- warp-level mma.sync (indexer)
 
 // D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(

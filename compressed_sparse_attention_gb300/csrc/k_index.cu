@@ -111,21 +111,92 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(
   }
 }
 
-// fp8 keys ---------------------------------------------------------------
-// A key row is 128 e4m3 codes plus 4 ue8m0 scales (one per 32 channels).
-// Thread (g, t) reads 8 codes at channels 32b + 8t .. +7 of rows g and g+8
-// for each block b; mma step (b, s) covers channels 32b + 8t + 4s + {0..3},
-// so one step never mixes two scale blocks. Codes convert exactly to bf16;
-// each block's partial dot product is scaled by its power of two in fp32.
-// KF 1: e4m3 codes (128 B a key); KF 3: E2M1 codes two to a byte (64 B a key);
-// both with a ue8m0 scale per 32 channels
+// fp8 / mxfp4 keys ---------------------------------------------------------
+// A key row is 128 codes (e4m3: 128 B; E2M1: two to a byte, 64 B) plus 4
+// ue8m0 scales, one per 32 channels. Thread (g, t) reads the codes of
+// channels 32b + 8t .. +7 of rows g and g+8 for each block b, so an mma step
+// never mixes two scale blocks; each block's partial dot product is scaled by
+// its power of two in fp32.
+//
+// Both code types decode exactly into f16 with few instructions (one convert
+// per e4m3 pair; two shifts and a logic op per E2M1 pair, which arrives as
+// 2^-14 times its value), so these products run as f16 x f16 -> f32 mma. The
+// indexer query is converted to f16 once per query, head h multiplied by a
+// power of two 2^s_h that puts its largest element in [2^14, 2^15): every
+// bf16 element at least 2^-24 of that largest one is then exact in f16, and
+// a smaller one moves by at most 2^-25 of it. The weight w_h takes the
+// inverse power (and the 2^14 of the E2M1 decode), which the ReLU commutes
+// with. k-slot order: for e4m3, mma step (b, 0) holds channel pairs
+// (8t, 8t+1) and (8t+2, 8t+3) of block b, step (b, 1) the pairs (8t+4, 8t+5)
+// and (8t+6, 8t+7); for E2M1 the pairs are (8t, 8t+4), (8t+1, 8t+5) and
+// (8t+2, 8t+6), (8t+3, 8t+7), the order the nibble decoder produces.
 template <int NT, int KF>
+__device__ __forceinline__ void idxq_load_query(const uint16_t* __restrict__ q_idx, const float* __restrict__ w_heads,
+                                                int q, int g, int t, uint32_t (&qb)[NT][8][2], float (&w0)[NT],
+                                                float (&w1)[NT]) {
+  constexpr int HI = NT * 8;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint16_t* qh = q_idx + ((int64_t)q * HI + nt * 8 + g) * kIdxDim;
+    // pass 1: the head's largest magnitude (bf16 -> float is exact)
+    float amax = 0.f;
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qh + 32 * bb + 8 * t);
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v.x << 16)), fabsf(__uint_as_float(v.x & 0xFFFF0000u))));
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v.y << 16)), fabsf(__uint_as_float(v.y & 0xFFFF0000u))));
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v.z << 16)), fabsf(__uint_as_float(v.z & 0xFFFF0000u))));
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(v.w << 16)), fabsf(__uint_as_float(v.w & 0xFFFF0000u))));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int ex = 0;
+    if (amax > 0.f) frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+    const int sh = max(-100, min(100, 15 - ex));
+    const float up = __uint_as_float((uint32_t)(sh + 127) << 23);
+    // pass 2: scaled f16 pairs in k-slot order (the row is in L1 from pass 1)
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qh + 32 * bb + 8 * t);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      float y[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        y[2 * k] = __uint_as_float(wv[k] << 16) * up;
+        y[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u) * up;
+      }
+      if constexpr (KF == 3) {
+        qb[nt][2 * bb][0] = h2_bits(y[0], y[4]);
+        qb[nt][2 * bb][1] = h2_bits(y[1], y[5]);
+        qb[nt][2 * bb + 1][0] = h2_bits(y[2], y[6]);
+        qb[nt][2 * bb + 1][1] = h2_bits(y[3], y[7]);
+      } else {
+        qb[nt][2 * bb][0] = h2_bits(y[0], y[1]);
+        qb[nt][2 * bb][1] = h2_bits(y[2], y[3]);
+        qb[nt][2 * bb + 1][0] = h2_bits(y[4], y[5]);
+        qb[nt][2 * bb + 1][1] = h2_bits(y[6], y[7]);
+      }
+    }
+    // the C fragment's columns are heads 2t and 2t+1, whose powers lanes 8t and 8t+4 hold
+    const int e = (KF == 3 ? 14 : 0) - sh;
+    const int e0 = __shfl_sync(0xffffffffu, e, 8 * t), e1 = __shfl_sync(0xffffffffu, e, 8 * t + 4);
+    w0[nt] = ldexpf(w_heads[(int64_t)q * HI + nt * 8 + 2 * t], e0);
+    w1[nt] = ldexpf(w_heads[(int64_t)q * HI + nt * 8 + 2 * t + 1], e1);
+  }
+}
+
+// U = tiles of 16 keys per warp per work item (chunk = 128 U keys): all of a
+// warp's loads for an item are issued before any is used, so U sets the bytes
+// in flight (16 warps an SM x U x 16 rows x row bytes); mxfp4 rows are half
+// the size of fp8 rows and take twice the tiles.
+template <int NT, int KF, int U>
 __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
     int n_query, int n_seq, int64_t n_chunks, int64_t max_vis, const uint16_t* __restrict__ q_idx,
     const float* __restrict__ w_heads, const uint8_t* __restrict__ keys, const uint8_t* __restrict__ key_scale,
     const int64_t* __restrict__ pool_off, const int32_t* __restrict__ seq_of_q,
     const int32_t* __restrict__ n_vis, float* __restrict__ scores, int64_t ld, uint32_t* flags) {
-  constexpr int HI = NT * 8;
+  constexpr int KB = KF == 3 ? kIdxDim / 2 : kIdxDim;  // code bytes a key
+  constexpr int CH = 128 * U;                         // keys a work item
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = n_chunks * (int64_t)n_query;
   int cur_q = -1;
@@ -137,7 +208,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
   bool q_ok = false;
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     const int q = (int)(item / n_chunks);
-    const int64_t j0 = (item % n_chunks) * kIdxChunk;
+    const int64_t j0 = (item % n_chunks) * CH;
     if (q != cur_q) {
       cur_q = q;
       const int b = seq_of_q[q];
@@ -151,83 +222,58 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
           if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_NVIS_TOO_LARGE);
           nv = (int)min(plen, max_vis);
         }
-        kbase = keys + pool_off[b] * (KF == 3 ? kIdxDim / 2 : kIdxDim);
+        kbase = keys + pool_off[b] * KB;
         sbase = key_scale + pool_off[b] * (kIdxDim / 32);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const uint16_t* qh = q_idx + ((int64_t)q * HI + nt * 8 + g) * kIdxDim;
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qh + 32 * bb + 8 * t);
-            qb[nt][2 * bb][0] = v.x; qb[nt][2 * bb][1] = v.y;
-            qb[nt][2 * bb + 1][0] = v.z; qb[nt][2 * bb + 1][1] = v.w;
-          }
-          w0[nt] = w_heads[(int64_t)q * HI + nt * 8 + 2 * t];
-          w1[nt] = w_heads[(int64_t)q * HI + nt * 8 + 2 * t + 1];
-        }
+        idxq_load_query<NT, KF>(q_idx, w_heads, q, g, t, qb, w0, w1);
       }
     }
     if (!q_ok || j0 >= nv) continue;
-    uint2 ca[2][4], cb[2][4];
-    uint32_t sa[2], sb[2];
-    int64_t rg[2];
+    // KF 3 keeps 4 code bytes per (tile, block, row) in .x; the .y words are unused
+    uint2 ca[U][4], cb[U][4];
+    uint32_t sa[U], sb[U];
+    int64_t rg[U];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       rg[u] = j0 + 128 * u + 16 * warp + g;
       const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
         if constexpr (KF == 3) {  // 8 codes in 4 bytes
-          ca[u][bb] = make_uint2(*reinterpret_cast<const uint32_t*>(kbase + ra * (kIdxDim / 2) + 16 * bb + 4 * t), 0u);
-          cb[u][bb] = make_uint2(*reinterpret_cast<const uint32_t*>(kbase + rb * (kIdxDim / 2) + 16 * bb + 4 * t), 0u);
+          ca[u][bb] = make_uint2(ldg_stream4(kbase + ra * KB + 16 * bb + 4 * t), 0u);
+          cb[u][bb] = make_uint2(ldg_stream4(kbase + rb * KB + 16 * bb + 4 * t), 0u);
         } else {
-          ca[u][bb] = ldg_stream8(kbase + ra * kIdxDim + 32 * bb + 8 * t);
-          cb[u][bb] = ldg_stream8(kbase + rb * kIdxDim + 32 * bb + 8 * t);
+          ca[u][bb] = ldg_stream8(kbase + ra * KB + 32 * bb + 8 * t);
+          cb[u][bb] = ldg_stream8(kbase + rb * KB + 32 * bb + 8 * t);
         }
       }
       sa[u] = *reinterpret_cast<const uint32_t*>(sbase + ra * 4);
       sb[u] = *reinterpret_cast<const uint32_t*>(sbase + rb * 4);
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < U; ++u) {
       float tot[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
-        // exact e4m3 -> bf16 (or E2M1 -> 2^-14 times its value, in bf16) of
-        // this block's 8 codes per row
+        // this block's 8 codes of rows g (a) and g+8 (b) as f16 pairs in k-slot order
         uint32_t a[4], b[4];
         if constexpr (KF == 3) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 fa = e2m1x2_to_float2_scaled((ca[u][bb].x >> (8 * k)) & 0xFFu);
-            const float2 fb = e2m1x2_to_float2_scaled((cb[u][bb].x >> (8 * k)) & 0xFFu);
-            a[k] = pack_bf16(fa.x, fa.y);
-            b[k] = pack_bf16(fb.x, fb.y);
-          }
+          e2m1x8_to_f16x2x4(ca[u][bb].x, a);
+          e2m1x8_to_f16x2x4(cb[u][bb].x, b);
         } else {
-          const float2 f0 = e4m3x2_to_float2((uint16_t)(ca[u][bb].x & 0xFFFF));
-          const float2 f1 = e4m3x2_to_float2((uint16_t)(ca[u][bb].x >> 16));
-          const float2 f2 = e4m3x2_to_float2((uint16_t)(ca[u][bb].y & 0xFFFF));
-          const float2 f3 = e4m3x2_to_float2((uint16_t)(ca[u][bb].y >> 16));
-          a[0] = pack_bf16(f0.x, f0.y); a[1] = pack_bf16(f1.x, f1.y);
-          a[2] = pack_bf16(f2.x, f2.y); a[3] = pack_bf16(f3.x, f3.y);
-          const float2 h0 = e4m3x2_to_float2((uint16_t)(cb[u][bb].x & 0xFFFF));
-          const float2 h1 = e4m3x2_to_float2((uint16_t)(cb[u][bb].x >> 16));
-          const float2 h2 = e4m3x2_to_float2((uint16_t)(cb[u][bb].y & 0xFFFF));
-          const float2 h3 = e4m3x2_to_float2((uint16_t)(cb[u][bb].y >> 16));
-          b[0] = pack_bf16(h0.x, h0.y); b[1] = pack_bf16(h1.x, h1.y);
-          b[2] = pack_bf16(h2.x, h2.y); b[3] = pack_bf16(h3.x, h3.y);
+          a[0] = e4m3x2_to_f16x2(ca[u][bb].x); a[1] = e4m3x2_to_f16x2(ca[u][bb].x >> 16);
+          a[2] = e4m3x2_to_f16x2(ca[u][bb].y); a[3] = e4m3x2_to_f16x2(ca[u][bb].y >> 16);
+          b[0] = e4m3x2_to_f16x2(cb[u][bb].x); b[1] = e4m3x2_to_f16x2(cb[u][bb].x >> 16);
+          b[2] = e4m3x2_to_f16x2(cb[u][bb].y); b[3] = e4m3x2_to_f16x2(cb[u][bb].y >> 16);
         }
-        const float unscale = KF == 3 ? kE2M1Unscale : 1.0f;
-        const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu) * unscale;
-        const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu) * unscale;
+        const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu);
+        const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_16816_bf16(acc, a[0], b[0], a[1], b[1], qb[nt][2 * bb][0], qb[nt][2 * bb][1]);
-          mma_16816_bf16(acc, a[2], b[2], a[3], b[3], qb[nt][2 * bb + 1][0], qb[nt][2 * bb + 1][1]);
+          mma_16816_f16(acc, a[0], b[0], a[1], b[1], qb[nt][2 * bb][0], qb[nt][2 * bb][1]);
+          mma_16816_f16(acc, a[2], b[2], a[3], b[3], qb[nt][2 * bb + 1][0], qb[nt][2 * bb + 1][1]);
           tot[nt][0] = fmaf(scg, acc[0], tot[nt][0]);
           tot[nt][1] = fmaf(scg, acc[1], tot[nt][1]);
           tot[nt][2] = fmaf(scg8, acc[2], tot[nt][2]);
@@ -258,32 +304,35 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
                                const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
                                const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags) {
   if (n_query == 0 || max_vis == 0) return cudaSuccess;
-  const int64_t n_chunks = (max_vis + kIdxChunk - 1) / kIdxChunk;
-  const int64_t items = n_chunks * n_query;
   const int64_t cap = (int64_t)num_sms * 2;
+  // chunk of one work item: 256 keys (bf16; fp8 and mxfp4 with 32 heads), 512
+  // (fp8 with 8 heads, mxfp4 with 8 or 16 heads)
+  const int u_q = ((idx_fmt == 3 && idx_heads <= 16) || (idx_fmt == 1 && idx_heads == 8)) ? 4 : 2;
+  const int64_t chunk = idx_fmt == 0 ? kIdxChunk : 128 * u_q;
+  const int64_t n_chunks = (max_vis + chunk - 1) / chunk;
+  const int64_t items = n_chunks * n_query;
   const dim3 grid((unsigned)(items < cap ? items : cap));
-#define CSA2_IDX(NT)                                                                                   \
-  do {                                                                                                 \
-    if (idx_fmt == 1)                                                                                  \
-      index_score_fp8_kernel<NT, 1><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
-                                                       (const uint8_t*)keys, key_scale, pool_off,      \
-                                                       seq_of_q, n_vis, scores, ld, flags);            \
-    else if (idx_fmt == 3)                                                                             \
-      index_score_fp8_kernel<NT, 3><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
-                                                       (const uint8_t*)keys, key_scale, pool_off,      \
-                                                       seq_of_q, n_vis, scores, ld, flags);            \
-    else                                                                                               \
+#define CSA2_IDXQ(NT, KF, U)                                                                                  \
+  index_score_fp8_kernel<NT, KF, U><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads,  \
+                                                          (const uint8_t*)keys, key_scale, pool_off, seq_of_q, \
+                                                          n_vis, scores, ld, flags)
+#define CSA2_IDX(NT, UQ, U8)                                                                               \
+  do {                                                                                                     \
+    if (idx_fmt == 1) CSA2_IDXQ(NT, 1, U8);                                                                \
+    else if (idx_fmt == 3) CSA2_IDXQ(NT, 3, UQ);                                                           \
+    else                                                                                                   \
       index_score_bf16_kernel<NT><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
-                                                        (const uint16_t*)keys, pool_off, seq_of_q,     \
-                                                        n_vis, scores, ld, flags);                     \
+                                                        (const uint16_t*)keys, pool_off, seq_of_q,         \
+                                                        n_vis, scores, ld, flags);                         \
   } while (0)
   switch (idx_heads) {
-    case 8: CSA2_IDX(1); break;
-    case 16: CSA2_IDX(2); break;
-    case 32: CSA2_IDX(4); break;
+    case 8: CSA2_IDX(1, 4, 4); break;
+    case 16: CSA2_IDX(2, 4, 2); break;
+    case 32: CSA2_IDX(4, 2, 2); break;
     default: return cudaErrorInvalidValue;
   }
 #undef CSA2_IDX
+#undef CSA2_IDXQ
   return cudaGetLastError();
 }
 
