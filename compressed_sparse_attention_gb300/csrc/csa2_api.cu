@@ -93,6 +93,15 @@ const char* csa2_status_string(csa2_status s) {
   return "unknown status";
 }
 
+static void release(csa2_ctx* ctx) {
+  if (ctx->d_flags) cudaFree(ctx->d_flags);
+  if (ctx->d_work) cudaFree(ctx->d_work);
+  if (ctx->side) cudaStreamDestroy(ctx->side);
+  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join})
+    if (ev) cudaEventDestroy(ev);
+  delete ctx;
+}
+
 csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (!cfg || !out) return CSA2_ERR_INVALID_ARG;
   *out = nullptr;
@@ -116,16 +125,16 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_flags, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(ctx->d_flags, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&ctx->d_work, 2 * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(ctx->d_work, 0, 2 * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_idx, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_tail, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    if (ctx->d_flags) cudaFree(ctx->d_flags);
-    if (ctx->side) cudaStreamDestroy(ctx->side);
-    if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
-    if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
-    delete ctx;
+    release(ctx);
     return CSA2_ERR_CUDA;
   }
   std::memset(&ctx->rope, 0, sizeof(ctx->rope));
@@ -137,11 +146,7 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
 
 void csa2_destroy(csa2_ctx* ctx) {
   if (!ctx) return;
-  if (ctx->d_flags) cudaFree(ctx->d_flags);
-  if (ctx->side) cudaStreamDestroy(ctx->side);
-  if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
-  if (ctx->ev_join) cudaEventDestroy(ctx->ev_join);
-  delete ctx;
+  release(ctx);
 }
 
 const char* csa2_last_error(const csa2_ctx* ctx) { return ctx ? ctx->err.c_str() : "no context"; }
@@ -225,10 +230,13 @@ csa2_status csa2_compress(csa2_ctx* ctx, void* stream, const uint16_t* raw, cons
                      pool_off, norm_w, w_idx, k_norm_w, pool_kv, pool_kv_scale, idx_keys, idx_key_scale);
 }
 
+// new_first / new_tok set: the scan leaves out the entries that this step's
+// compress writes (see IdxArgs); the caller scores them with do_index_tail
 static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q_idx,
                             const float* w_heads, const void* idx_keys, const uint8_t* idx_key_scale,
                             const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
-                            float* scores, int64_t ld) {
+                            float* scores, int64_t ld, const int64_t* new_first = nullptr,
+                            const int64_t* new_tok = nullptr, bool tail_only = false) {
   const csa2_config& c = ctx->cfg;
   if (n_query < 0 || n_seq < 1 || max_vis < 0 || ld < max_vis)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: sizes");
@@ -240,13 +248,34 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
   if (!aligned16(q_idx) || !aligned16(idx_keys) || (idx_key_scale && (reinterpret_cast<uintptr_t>(idx_key_scale) & 3)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: misaligned buffer");
   const int kf = c.idx_key_format;
-  cudaError_t e =
-      csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)
-          ? csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
-                                        reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis,
-                                        scores, ld, ctx->d_flags)
-          : csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, kf, n_query, n_seq, max_vis, q_idx, w_heads,
-                                     idx_keys, idx_key_scale, pool_off, seq_of_q, n_vis, scores, ld, ctx->d_flags);
+  csa2::IdxArgs ia;
+  ia.n_query = n_query;
+  ia.n_seq = n_seq;
+  ia.max_vis = max_vis;
+  ia.q_idx = q_idx;
+  ia.w_heads = w_heads;
+  ia.keys = idx_keys;
+  ia.key_scale = idx_key_scale;
+  ia.pool_off = pool_off;
+  ia.seq_of_q = seq_of_q;
+  ia.n_vis = n_vis;
+  ia.scores = scores;
+  ia.ld = ld;
+  ia.flags = ctx->d_flags;
+  ia.new_first = new_first;
+  ia.new_tok = new_tok;
+  ia.m = c.compress_ratio;
+  ia.work = ctx->d_work;
+  cudaError_t e;
+  if (tail_only) {
+    e = csa2::launch_index_tail(st, c.idx_heads, kf, ia);
+  } else if (new_first == nullptr && csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)) {
+    e = csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
+                                    reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis, scores,
+                                    ld, ctx->d_flags);
+  } else {
+    e = csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, kf, ia);
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "index_score");
   ctx->last_launches += 1;
   return CSA2_OK;
@@ -393,17 +422,56 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   if (s != CSA2_OK) return s;
   const int kvf = ctx->cfg.kv_format;
   const csa2::AttendPlan pl = csa2::attend_plan(a->n_query, ctx->cfg.topk, true, ctx->num_sms);
+  const int m = ctx->cfg.compress_ratio;
   int launches = 0;
-  if (a->mode == CSA2_MODE_FULL) {
+  // Every exit after a fork makes the caller's stream wait for the side
+  // stream's last launch, so that a capture of the step stays well formed and
+  // the caller's stream orders after all of it.
+  bool side_open = false;
+  auto join = [&](csa2_status so) -> csa2_status {
+    if (!side_open) return so;
+    side_open = false;
+    cudaError_t je = cudaEventRecord(ctx->ev_join, ctx->side);
+    if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ctx->ev_join, 0);
+    if (je != cudaSuccess && so == CSA2_OK) return cuda_fail(ctx, je, "step: join");
+    return so;
+  };
+  // A decode-shaped Full step (at most two closing groups per sequence, the
+  // scan in its CUDA-core form) runs compress on the side stream beside the
+  // scan of the entries that existed before the step. The scan hands out its
+  // work by tickets, so the SMs compress holds at the start cost it nothing.
+  // The tail kernel then scores the entries compress wrote, and the caller's
+  // stream waits for both before top-k.
+  const bool full = a->mode == CSA2_MODE_FULL;
+  const bool overlap = full && a->n_query > 0 && a->max_vis > 0 && a->n_tokens <= 2LL * m * a->n_seq &&
+                       !csa2::index_tc_suited(ctx->cfg.idx_key_format != CSA2_KV_BF16, a->n_query, a->n_seq,
+                                              ctx->cfg.idx_heads);
+  const bool tail = overlap && a->w_idx != nullptr;  // compress writes index keys: score the new ones apart
+  if (full) {
+    cudaStream_t cs = st;
+    if (overlap) {
+      cudaError_t e = cudaEventRecord(ctx->ev_fork, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "step: fork");
+      side_open = true;
+      cs = ctx->side;
+    }
     ctx->last_launches = 0;
-    s = do_compress(ctx, st, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off, a->norm_w,
-                    a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale);
-    if (s != CSA2_OK) return s;
+    s = do_compress(ctx, cs, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
+                    a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale);
+    if (s != CSA2_OK) return join(s);
     launches += ctx->last_launches;
+    if (tail) {
+      ctx->last_launches = 0;
+      s = do_index(ctx, ctx->side, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale,
+                   a->pool_off, a->seq_of_q, a->n_vis, a->max_vis, scores, ld, a->first_pos, a->tok_off, true);
+      if (s != CSA2_OK) return join(s);
+      launches += ctx->last_launches;
+    }
   }
   if (a->n_query == 0) {
     ctx->last_launches = launches;
-    return CSA2_OK;
+    return join(CSA2_OK);
   }
   if (a->mode == CSA2_MODE_REUSE) {
     // nothing to overlap with: window and selected tiles share one launch
@@ -415,33 +483,29 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   }
   ctx->last_launches = 0;
   s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
-               a->seq_of_q, a->n_vis, a->max_vis, scores, ld);
-  if (s != CSA2_OK) return s;
+               a->seq_of_q, a->n_vis, a->max_vis, scores, ld, tail ? a->first_pos : nullptr,
+               tail ? a->tok_off : nullptr);
+  if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
+  cudaError_t e = cudaSuccess;
+  if (overlap) {
+    e = cudaEventRecord(ctx->ev_tail, ctx->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ev_tail, 0);
+    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: wait for compress"));
+  }
   // The window tile reads only the window buffer, which nothing in the step
   // writes. It runs on the side stream beside top-k, whose grid (a cluster per
   // query) leaves most SMs free; the caller's stream joins it before the
-  // merge. It is forked after the index launch, whose CTAs fill every SM and
-  // share out the pool statically, so that none of them waits for it.
-  bool forked = false;
-  cudaError_t e = cudaSuccess;
+  // merge. It starts after the index scan, whose CTAs fill every SM.
   if (pl.split_window) {
-    e = cudaEventRecord(ctx->ev_fork, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0);
-    if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
-    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_join, ctx->side);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "step: window tile");
-    forked = true;
+    e = cudaEventRecord(ctx->ev_idx, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_idx, 0);
+    if (e == cudaSuccess) {
+      side_open = true;
+      e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
+    }
+    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: window tile"));
   }
-  // every exit after the fork joins the side stream back, so that a capture
-  // of the step stays well formed and the caller's stream orders after it
-  auto join = [&](csa2_status so) -> csa2_status {
-    if (!forked) return so;
-    forked = false;
-    const cudaError_t je = cudaStreamWaitEvent(st, ctx->ev_join, 0);
-    if (je != cudaSuccess && so == CSA2_OK) return cuda_fail(ctx, je, "step: join");
-    return so;
-  };
   ctx->last_launches = 0;
   s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes);
   if (s != CSA2_OK) return join(s);
@@ -453,6 +517,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     if (s != CSA2_OK) return s;
     e = csa2::launch_attend_merge(st, ap, pl, at_ws, &launches);
   } else {
+    s = join(CSA2_OK);
+    if (s != CSA2_OK) return s;
     e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");

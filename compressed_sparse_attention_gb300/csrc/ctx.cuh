@@ -10,9 +10,12 @@ struct csa2_ctx {
   int num_sms = 0;
   csa2::RopeParams rope;
   uint32_t* d_flags = nullptr;
-  cudaStream_t side = nullptr;    // step side stream: the window tile
+  unsigned long long* d_work = nullptr;  // [2] ticket counters of the index scan (zero between launches)
+  cudaStream_t side = nullptr;    // step side stream: compress and the tail scores, then the window tile
   cudaEvent_t ev_fork = nullptr;  // recorded on the caller's stream at the start of a step
-  cudaEvent_t ev_join = nullptr;  // recorded on the side stream after the window tile
+  cudaEvent_t ev_idx = nullptr;   // recorded on the caller's stream after the index scan
+  cudaEvent_t ev_tail = nullptr;  // recorded on the side stream after compress and the tail scores
+  cudaEvent_t ev_join = nullptr;  // recorded on the side stream after its last launch
   std::string err;
   int last_launches = 0;
 };

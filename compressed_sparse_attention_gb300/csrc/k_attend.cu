@@ -90,16 +90,49 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qi = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
-  const int64_t t = p.q_pos[qi];
-  const int b = p.seq_of_q[qi];
-  const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
   // split 0 takes the launch's first tile alone when lead_single is set (the
   // window tile); the other splits take tiles_per_split tiles each
   const int lead = p.lead_single ? 1 : 0;
   const int tile_begin = (lead && split == 0) ? p.tile_base : p.tile_base + lead + (split - lead) * p.tiles_per_split;
-  const int tile_cap = (lead && split == 0) ? tile_begin + 1 : tile_begin + p.tiles_per_split;
-  const int tile_end = q_ok ? min(tile_cap, p.tile_base + p.tile_count) : tile_begin;
+  const int tile_cap0 = (lead && split == 0) ? tile_begin + 1 : tile_begin + p.tiles_per_split;
+  const int tile_cap = min(tile_cap0, p.tile_base + p.tile_count);
+  // every load that depends only on the query index is issued before the
+  // setup below, so that their latencies overlap: the query's position and
+  // sequence, this thread's first selection entry, and Q itself
+  const int64_t t = p.q_pos[qi];
+  const int b = p.seq_of_q[qi];
+  // selection entry of this thread's row in selected tile `tile` (-1 past k)
+  auto sel_entry = [&](int tile, int tile_lim) -> int32_t {
+    const int col = (tile - 1) * kTileRows + tid;
+    return (tile >= 1 && tile < tile_lim && col < p.topk && p.topk_idx != nullptr)
+               ? p.topk_idx[(int64_t)qi * p.topk + col]
+               : -1;
+  };
+  int32_t j_next = sel_entry(tile_begin, tile_cap);
+  // Q is copied asynchronously into its swizzled K-major slots (it lands
+  // together with the first tile's rows); the rope channels are rotated in
+  // place once both have arrived
+  if (tile_begin < tile_cap) {
+    for (int h = warp; h < kHeads; h += 4) {
+      const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
+        const uint32_t dst = base_s + SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
+                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+        cp_async16(dst, qh + 8 * c, 16u);
+      }
+    }
+  }
+  const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
+  const int tile_end = q_ok ? tile_cap : tile_begin;
   if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
+  const int bs = q_ok ? b : 0;  // offsets of a valid sequence (unused when !q_ok)
+  const int64_t win_b0 = p.win_off[bs], win_b1 = p.win_off[bs + 1];
+  // no selection (window-only call): the pool arguments may be NULL
+  const int64_t pool_b0 = p.pool_off != nullptr ? p.pool_off[bs] : 0;
+  const int64_t pool_b1 = p.pool_off != nullptr ? p.pool_off[bs + 1] : 0;
+  const int64_t lo_raw = (q_ok && p.win_lo) ? p.win_lo[bs] : 0;
 
   if (warp == 0) {
     tmem_alloc(tslot, kTmemCols);
@@ -122,22 +155,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     if (q_ok) rope_cs(p.rp, tid, t, c, sn);
     rope_tab[tid] = make_float2(c, sn);
   }
-  __syncthreads();
-  // ---- Q: copied asynchronously into its swizzled K-major slots (it lands
-  // together with the first tile's rows); the rope channels are rotated in
-  // place once both have arrived
-  if (tile_begin < tile_end) {
-    for (int h = warp; h < kHeads; h += 4) {
-      const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
-        const uint32_t dst = base_s + SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
-                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
-        cp_async16(dst, qh + 8 * c, 16u);
-      }
-    }
-  }
   bool q_pending = true;
   tc_fence_before();
   __syncthreads();
@@ -149,20 +166,10 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   uint32_t phase = 0;
   bool aborted = false;
 
-  const int64_t win_cap = q_ok ? (p.win_off[b + 1] - p.win_off[b]) : 0;
-  const int64_t lo_b = (q_ok && p.win_lo) ? max((int64_t)0, p.win_lo[b]) : 0;
+  const int64_t win_cap = q_ok ? (win_b1 - win_b0) : 0;
+  const int64_t lo_b = max((int64_t)0, lo_raw);
   const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
-  // no selection (window-only call): the pool arguments may be NULL
-  const int64_t plen = (q_ok && p.pool_off != nullptr) ? (p.pool_off[b + 1] - p.pool_off[b]) : 0;
-  // selection entry of this thread's row in selected tile `tile` (-1 past k):
-  // each tile's entry is loaded one tile ahead
-  auto sel_entry = [&](int tile) -> int32_t {
-    const int col = (tile - 1) * kTileRows + tid;
-    return (tile >= 1 && tile < tile_end && col < p.topk && p.topk_idx != nullptr)
-               ? p.topk_idx[(int64_t)qi * p.topk + col]
-               : -1;
-  };
-  int32_t j_next = sel_entry(tile_begin);
+  const int64_t plen = q_ok ? (pool_b1 - pool_b0) : 0;
 
   for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row)
@@ -170,19 +177,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       const int r = tid;
       int64_t src = -1;
       const int32_t j_cur = j_next;
-      j_next = sel_entry(tile + 1);
+      j_next = sel_entry(tile + 1, tile_end);  // one tile ahead
       if (tile == 0) {
         const int64_t pos = lo_eff + r;
         if (pos <= t && r < p.window) {
           if (t - lo_eff + 1 > win_cap) {
             set_flag(p.flags, CSA2_FLAG_BAD_WINDOW);
           } else {
-            src = p.win_off[b] + (pos % win_cap);
+            src = win_b0 + (pos % win_cap);
           }
         }
       } else {
         const int32_t j = j_cur;
-        if (j >= 0 && j < plen) src = p.pool_off[b] + j;
+        if (j >= 0 && j < plen) src = pool_b0 + j;
         else if (j != -1) set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
       }
       rows[r] = src;
@@ -462,7 +469,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     tc_fence_after();
   }
 
-  // ---- epilogue
+  // ---- epilogue (no copy of Q may still be landing when the CTA exits,
+  // e.g. for a query without tiles)
+  cp_async_wait_all();
   __syncthreads();
   const bool have_o = (tile_begin < tile_end) && !aborted;
   const int first_rope = kDim - 2 * p.rp.pairs;
@@ -534,17 +543,30 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     if (tid < kHeads)
       p.ws_ml[slot * kHeads + tid] = make_float2(have_o ? m_run[tid] : -INFINITY, have_o ? l_run[tid] : 0.f);
     if (have_o) {
-      float* wo = p.ws_o + slot * kHeads * kDim;
+      // bf16 partials: the merge's weighted sum then carries 2^-9 of each
+      // partial's magnitude, below the bf16 rounding of the output itself
+      // relative to sum_r p_r |v_r|. Lanes d, d+1 swap halves so that each
+      // stores two adjacent dims of one head as one 32-bit word.
+      uint16_t* wo = p.ws_o + slot * kHeads * kDim;
       for (int mt = 0; mt < 4; ++mt) {
         const int d = 128 * mt + 32 * warp + lane;
+        const bool odd = (d & 1) != 0;
         uint32_t ra[32], rb[32];
         tmem_ld32(tmem_o + (uint32_t)(64 * mt) + lane_base, ra);
         tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32) + lane_base, rb);
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) wo[k * kDim + d] = __uint_as_float(ra[k]);
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t* r = hh ? rb : ra;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) wo[(32 + k) * kDim + d] = __uint_as_float(rb[k]);
+          for (int k = 0; k < 32; k += 2) {
+            const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const int h = 32 * hh + k + (odd ? 1 : 0);
+            const uint32_t w = odd ? pack_bf16(recv, v1) : pack_bf16(v0, recv);
+            *reinterpret_cast<uint32_t*>(wo + (int64_t)h * kDim + (d & ~1)) = w;
+          }
+        }
       }
     }
   }
@@ -597,18 +619,21 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   }
   __syncthreads();
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const float* base = p.ws_o + ((int64_t)qi * ns * kHeads + h) * kDim + 8 * chunk;
+  const uint16_t* base = p.ws_o + ((int64_t)qi * ns * kHeads + h) * kDim + 8 * chunk;
+  uint4 part[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    part[s] = (s < ns && wsplit[s][hl] != 0.f) ? *reinterpret_cast<const uint4*>(base + (int64_t)s * kHeads * kDim)
+                                               : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     if (s < ns) {
       const float w = wsplit[s][hl];
-      if (w != 0.f) {
-        const float4* src = reinterpret_cast<const float4*>(base + (int64_t)s * kHeads * kDim);
-        const float4 a = src[0], b = src[1];
-        acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
-        acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
-        acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
-        acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+      const uint32_t pw[4] = {part[s].x, part[s].y, part[s].z, part[s].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[2 * k] = fmaf(w, bf16lo(pw[k]), acc[2 * k]);
+        acc[2 * k + 1] = fmaf(w, bf16hi(pw[k]), acc[2 * k + 1]);
       }
     }
   }
@@ -664,16 +689,16 @@ AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
 size_t attend_workspace_bytes(int n_query, const AttendPlan& pl) {
   if (pl.n_slots == 0) return 0;
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al((size_t)n_query * pl.n_slots * kHeads * kDim * 4) + al((size_t)n_query * pl.n_slots * kHeads * 8);
+  return al((size_t)n_query * pl.n_slots * kHeads * kDim * 2) + al((size_t)n_query * pl.n_slots * kHeads * 8);
 }
 
 static void attach_ws(AttendParams& p, const AttendPlan& pl, void* ws) {
   p.n_slots = pl.n_slots;
   if (pl.n_slots > 0) {
     auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_o = reinterpret_cast<uint16_t*>(ws);
     p.ws_ml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) +
-                                        al((size_t)p.n_query * pl.n_slots * kHeads * kDim * 4));
+                                        al((size_t)p.n_query * pl.n_slots * kHeads * kDim * 2));
   }
 }
 

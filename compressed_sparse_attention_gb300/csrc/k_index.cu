@@ -14,7 +14,62 @@
 
 namespace csa2 {
 
-constexpr int kIdxChunk = 256;  // keys per work item: 16 tiles, 2 per warp
+constexpr int kIdxChunk = 256;  // keys per work item of the bf16 scan: 16 tiles, 2 per warp
+
+// Entries [0, n) of query q that the scan covers: n_vis clamped to the pool
+// and to max_vis (a larger n_vis is flagged), and, when the step scores the
+// entries it compresses separately (new_first set), only the entries that
+// existed before this step: those below first_pos[b] / m of a sequence that
+// closes a group now.
+__device__ __forceinline__ int idx_query_range(const IdxArgs& a, int q, int b, bool flag_thread, int* n_all) {
+  int nv = a.n_vis[q];
+  const int64_t plen = a.pool_off[b + 1] - a.pool_off[b];
+  if (nv > plen || nv > a.max_vis) {
+    if (flag_thread) set_flag(a.flags, CSA2_FLAG_NVIS_TOO_LARGE);
+    nv = (int)min(plen, a.max_vis);
+  }
+  if (nv < 0) nv = 0;
+  *n_all = nv;
+  if (a.new_first != nullptr && a.new_tok[b + 1] > a.new_tok[b]) nv = (int)min((int64_t)nv, a.new_first[b] / a.m);
+  return nv;
+}
+
+// Work items: each CTA first takes three quarters of its even share by
+// striding (items c, c + G, ...; no synchronisation), then the rest is handed
+// out by a 64-bit ticket counter, so that a CTA that started late (its SM
+// still held by a kernel running beside the scan) just takes fewer of them.
+// In the ticket phase thread 0 fetches the next ticket while the current item
+// is processed; the last CTA to finish puts the counters back to zero.
+__device__ __forceinline__ int64_t idx_static_items(int64_t n_items) {
+  return (n_items / gridDim.x) * 3 / 4 * gridDim.x;  // the strided phase covers items [0, this)
+}
+struct IdxTickets {
+  unsigned long long* s;  // shared [2]
+  unsigned long long* work;
+  unsigned long long base;  // first ticketed item
+  int par = 0;
+  __device__ void start() {
+    if (threadIdx.x == 0) s[0] = base + atomicAdd(work, 1ull);
+    __syncthreads();
+  }
+  __device__ unsigned long long cur() const { return s[par]; }
+  __device__ void prefetch() {
+    if (threadIdx.x == 0) s[par ^ 1] = base + atomicAdd(work, 1ull);
+  }
+  __device__ void advance() {
+    __syncthreads();
+    par ^= 1;
+  }
+  __device__ void finish() {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(work + 1, 1ull) == (unsigned long long)gridDim.x - 1ull) {
+        work[0] = 0ull;
+        work[1] = 0ull;
+      }
+    }
+  }
+};
 
 // bf16 keys --------------------------------------------------------------
 // Thread (g = lane/4, t = lane%4) loads, for key rows g and g+8 of a tile,
@@ -22,93 +77,100 @@ constexpr int kIdxChunk = 256;  // keys per work item: 16 tiles, 2 per warp
 // c = 2i + h (i = chunk slot, h = half) the logical k pair (2t, 2t+1) is
 // channels 8(t+4i)+4h+{0,1} and (2t+8, 2t+9) is 8(t+4i)+4h+{2,3}.
 template <int NT>
-__global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(
-    int n_query, int n_seq, int64_t n_chunks, int64_t max_vis, const uint16_t* __restrict__ q_idx,
-    const float* __restrict__ w_heads, const uint16_t* __restrict__ keys,
-    const int64_t* __restrict__ pool_off, const int32_t* __restrict__ seq_of_q,
-    const int32_t* __restrict__ n_vis, float* __restrict__ scores, int64_t ld, uint32_t* flags) {
+__global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs a) {
   constexpr int HI = NT * 8;
+  __shared__ unsigned long long s_tk[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int64_t n_items = n_chunks * (int64_t)n_query;
+  const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
+  const uint16_t* keys = reinterpret_cast<const uint16_t*>(a.keys);
   int cur_q = -1;
   uint32_t qb[NT][8][2];
   float w0[NT], w1[NT];
   int nv = 0;
   const uint16_t* kbase = nullptr;
   bool q_ok = false;
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int q = (int)(item / n_chunks);
-    const int64_t j0 = (item % n_chunks) * kIdxChunk;
+  auto run = [&](int64_t item) {
+    const int q = (int)(item / a.n_chunks);
+    const int64_t j0 = (item % a.n_chunks) * kIdxChunk;
     if (q != cur_q) {
       cur_q = q;
-      const int b = seq_of_q[q];
-      nv = n_vis[q];
-      q_ok = (b >= 0 && b < n_seq);
+      const int b = a.seq_of_q[q];
+      q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_BAD_QUERY);
+        if (threadIdx.x == 0 && j0 == 0) set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
       } else {
-        const int64_t plen = pool_off[b + 1] - pool_off[b];
-        if (nv > plen || nv > max_vis) {
-          if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_NVIS_TOO_LARGE);
-          nv = (int)min(plen, max_vis);
-        }
-        kbase = keys + pool_off[b] * kIdxDim;
+        int n_all;
+        nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
+        kbase = keys + a.pool_off[b] * kIdxDim;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint16_t* qh = q_idx + ((int64_t)q * HI + nt * 8 + g) * kIdxDim;
+          const uint16_t* qh = a.q_idx + ((int64_t)q * HI + nt * 8 + g) * kIdxDim;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const uint4 v = *reinterpret_cast<const uint4*>(qh + 8 * (t + 4 * i));
             qb[nt][2 * i][0] = v.x; qb[nt][2 * i][1] = v.y;
             qb[nt][2 * i + 1][0] = v.z; qb[nt][2 * i + 1][1] = v.w;
           }
-          w0[nt] = w_heads[(int64_t)q * HI + nt * 8 + 2 * t];
-          w1[nt] = w_heads[(int64_t)q * HI + nt * 8 + 2 * t + 1];
+          w0[nt] = a.w_heads[(int64_t)q * HI + nt * 8 + 2 * t];
+          w1[nt] = a.w_heads[(int64_t)q * HI + nt * 8 + 2 * t + 1];
         }
       }
     }
-    if (!q_ok || j0 >= nv) continue;
-    // two tiles per warp: rows j0 + 16*warp + {0..15} and j0 + 128 + 16*warp + {0..15}
-    uint4 ka[2][4], kb[2][4];
-    int64_t rg[2];
+    if (q_ok && j0 < nv) {
+      // two tiles per warp: rows j0 + 16*warp + {0..15} and j0 + 128 + 16*warp + {0..15}
+      uint4 ka[2][4], kb[2][4];
+      int64_t rg[2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      rg[u] = j0 + 128 * u + 16 * warp + g;
-      const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
-      const uint16_t* pa = kbase + ra * kIdxDim;
-      const uint16_t* pb = kbase + rb * kIdxDim;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ka[u][i] = ldg_stream16(pa + 8 * (t + 4 * i));
-        kb[u][i] = ldg_stream16(pb + 8 * (t + 4 * i));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float sg = 0.f, sg8 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int u = 0; u < 2; ++u) {
+        rg[u] = j0 + 128 * u + 16 * warp + g;
+        const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
+        const uint16_t* pa = kbase + ra * kIdxDim;
+        const uint16_t* pb = kbase + rb * kIdxDim;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          mma_16816_bf16(acc, ka[u][i].x, kb[u][i].x, ka[u][i].y, kb[u][i].y, qb[nt][2 * i][0], qb[nt][2 * i][1]);
-          mma_16816_bf16(acc, ka[u][i].z, kb[u][i].z, ka[u][i].w, kb[u][i].w, qb[nt][2 * i + 1][0],
-                         qb[nt][2 * i + 1][1]);
+          ka[u][i] = ldg_stream16(pa + 8 * (t + 4 * i));
+          kb[u][i] = ldg_stream16(pb + 8 * (t + 4 * i));
         }
-        sg = fmaf(w0[nt], fmaxf(acc[0], 0.f), sg);
-        sg = fmaf(w1[nt], fmaxf(acc[1], 0.f), sg);
-        sg8 = fmaf(w0[nt], fmaxf(acc[2], 0.f), sg8);
-        sg8 = fmaf(w1[nt], fmaxf(acc[3], 0.f), sg8);
       }
-      sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-      sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-      sg8 += __shfl_xor_sync(0xffffffffu, sg8, 1);
-      sg8 += __shfl_xor_sync(0xffffffffu, sg8, 2);
-      float* srow = scores + (int64_t)q * ld;
-      if (t == 0 && rg[u] < nv) srow[rg[u]] = sg;
-      if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float sg = 0.f, sg8 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mma_16816_bf16(acc, ka[u][i].x, kb[u][i].x, ka[u][i].y, kb[u][i].y, qb[nt][2 * i][0], qb[nt][2 * i][1]);
+            mma_16816_bf16(acc, ka[u][i].z, kb[u][i].z, ka[u][i].w, kb[u][i].w, qb[nt][2 * i + 1][0],
+                           qb[nt][2 * i + 1][1]);
+          }
+          sg = fmaf(w0[nt], fmaxf(acc[0], 0.f), sg);
+          sg = fmaf(w1[nt], fmaxf(acc[1], 0.f), sg);
+          sg8 = fmaf(w0[nt], fmaxf(acc[2], 0.f), sg8);
+          sg8 = fmaf(w1[nt], fmaxf(acc[3], 0.f), sg8);
+        }
+        sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+        sg8 += __shfl_xor_sync(0xffffffffu, sg8, 1);
+        sg8 += __shfl_xor_sync(0xffffffffu, sg8, 2);
+        float* srow = a.scores + (int64_t)q * a.ld;
+        if (t == 0 && rg[u] < nv) srow[rg[u]] = sg;
+        if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
+      }
     }
+  };
+  const int64_t n_static = idx_static_items(n_items);
+  for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static};
+  tk.start();
+  for (;;) {
+    const unsigned long long item = tk.cur();
+    if (item >= (unsigned long long)n_items) break;
+    tk.prefetch();
+    run((int64_t)item);
+    tk.advance();
   }
+  tk.finish();
 }
 
 // fp8 / mxfp4 keys ---------------------------------------------------------
@@ -190,15 +252,13 @@ __device__ __forceinline__ void idxq_load_query(const uint16_t* __restrict__ q_i
 // in flight (16 warps an SM x U x 16 rows x row bytes); mxfp4 rows are half
 // the size of fp8 rows and take twice the tiles.
 template <int NT, int KF, int U>
-__global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
-    int n_query, int n_seq, int64_t n_chunks, int64_t max_vis, const uint16_t* __restrict__ q_idx,
-    const float* __restrict__ w_heads, const uint8_t* __restrict__ keys, const uint8_t* __restrict__ key_scale,
-    const int64_t* __restrict__ pool_off, const int32_t* __restrict__ seq_of_q,
-    const int32_t* __restrict__ n_vis, float* __restrict__ scores, int64_t ld, uint32_t* flags) {
+__global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a) {
   constexpr int KB = KF == 3 ? kIdxDim / 2 : kIdxDim;  // code bytes a key
   constexpr int CH = 128 * U;                         // keys a work item
+  __shared__ unsigned long long s_tk[2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int64_t n_items = n_chunks * (int64_t)n_query;
+  const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
+  const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.keys);
   int cur_q = -1;
   uint32_t qb[NT][8][2];
   float w0[NT], w1[NT];
@@ -206,124 +266,186 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(
   const uint8_t* kbase = nullptr;
   const uint8_t* sbase = nullptr;
   bool q_ok = false;
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int q = (int)(item / n_chunks);
-    const int64_t j0 = (item % n_chunks) * CH;
+  auto run = [&](int64_t item) {
+    const int q = (int)(item / a.n_chunks);
+    const int64_t j0 = (item % a.n_chunks) * CH;
     if (q != cur_q) {
       cur_q = q;
-      const int b = seq_of_q[q];
-      nv = n_vis[q];
-      q_ok = (b >= 0 && b < n_seq);
+      const int b = a.seq_of_q[q];
+      q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_BAD_QUERY);
+        if (threadIdx.x == 0 && j0 == 0) set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
       } else {
-        const int64_t plen = pool_off[b + 1] - pool_off[b];
-        if (nv > plen || nv > max_vis) {
-          if (threadIdx.x == 0 && j0 == 0) set_flag(flags, CSA2_FLAG_NVIS_TOO_LARGE);
-          nv = (int)min(plen, max_vis);
-        }
-        kbase = keys + pool_off[b] * KB;
-        sbase = key_scale + pool_off[b] * (kIdxDim / 32);
-        idxq_load_query<NT, KF>(q_idx, w_heads, q, g, t, qb, w0, w1);
+        int n_all;
+        nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
+        kbase = keys + a.pool_off[b] * KB;
+        sbase = a.key_scale + a.pool_off[b] * (kIdxDim / 32);
+        idxq_load_query<NT, KF>(a.q_idx, a.w_heads, q, g, t, qb, w0, w1);
       }
     }
-    if (!q_ok || j0 >= nv) continue;
-    // KF 3 keeps 4 code bytes per (tile, block, row) in .x; the .y words are unused
-    uint2 ca[U][4], cb[U][4];
-    uint32_t sa[U], sb[U];
-    int64_t rg[U];
+    if (q_ok && j0 < nv) {
+      // KF 3 keeps 4 code bytes per (tile, block, row) in .x; the .y words are unused
+      uint2 ca[U][4], cb[U][4];
+      uint32_t sa[U], sb[U];
+      int64_t rg[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      rg[u] = j0 + 128 * u + 16 * warp + g;
-      const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
+      for (int u = 0; u < U; ++u) {
+        rg[u] = j0 + 128 * u + 16 * warp + g;
+        const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        if constexpr (KF == 3) {  // 8 codes in 4 bytes
-          ca[u][bb] = make_uint2(ldg_stream4(kbase + ra * KB + 16 * bb + 4 * t), 0u);
-          cb[u][bb] = make_uint2(ldg_stream4(kbase + rb * KB + 16 * bb + 4 * t), 0u);
-        } else {
-          ca[u][bb] = ldg_stream8(kbase + ra * KB + 32 * bb + 8 * t);
-          cb[u][bb] = ldg_stream8(kbase + rb * KB + 32 * bb + 8 * t);
+        for (int bb = 0; bb < 4; ++bb) {
+          if constexpr (KF == 3) {  // 8 codes in 4 bytes
+            ca[u][bb] = make_uint2(ldg_stream4(kbase + ra * KB + 16 * bb + 4 * t), 0u);
+            cb[u][bb] = make_uint2(ldg_stream4(kbase + rb * KB + 16 * bb + 4 * t), 0u);
+          } else {
+            ca[u][bb] = ldg_stream8(kbase + ra * KB + 32 * bb + 8 * t);
+            cb[u][bb] = ldg_stream8(kbase + rb * KB + 32 * bb + 8 * t);
+          }
         }
+        sa[u] = *reinterpret_cast<const uint32_t*>(sbase + ra * 4);
+        sb[u] = *reinterpret_cast<const uint32_t*>(sbase + rb * 4);
       }
-      sa[u] = *reinterpret_cast<const uint32_t*>(sbase + ra * 4);
-      sb[u] = *reinterpret_cast<const uint32_t*>(sbase + rb * 4);
-    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float tot[NT][4];
+      for (int u = 0; u < U; ++u) {
+        float tot[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) tot[nt][0] = tot[nt][1] = tot[nt][2] = tot[nt][3] = 0.f;
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        // this block's 8 codes of rows g (a) and g+8 (b) as f16 pairs in k-slot order
-        uint32_t a[4], b[4];
-        if constexpr (KF == 3) {
-          e2m1x8_to_f16x2x4(ca[u][bb].x, a);
-          e2m1x8_to_f16x2x4(cb[u][bb].x, b);
-        } else {
-          a[0] = e4m3x2_to_f16x2(ca[u][bb].x); a[1] = e4m3x2_to_f16x2(ca[u][bb].x >> 16);
-          a[2] = e4m3x2_to_f16x2(ca[u][bb].y); a[3] = e4m3x2_to_f16x2(ca[u][bb].y >> 16);
-          b[0] = e4m3x2_to_f16x2(cb[u][bb].x); b[1] = e4m3x2_to_f16x2(cb[u][bb].x >> 16);
-          b[2] = e4m3x2_to_f16x2(cb[u][bb].y); b[3] = e4m3x2_to_f16x2(cb[u][bb].y >> 16);
+        for (int bb = 0; bb < 4; ++bb) {
+          // this block's 8 codes of rows g (a) and g+8 (b) as f16 pairs in k-slot order
+          uint32_t a[4], b[4];
+          if constexpr (KF == 3) {
+            e2m1x8_to_f16x2x4(ca[u][bb].x, a);
+            e2m1x8_to_f16x2x4(cb[u][bb].x, b);
+          } else {
+            a[0] = e4m3x2_to_f16x2(ca[u][bb].x); a[1] = e4m3x2_to_f16x2(ca[u][bb].x >> 16);
+            a[2] = e4m3x2_to_f16x2(ca[u][bb].y); a[3] = e4m3x2_to_f16x2(ca[u][bb].y >> 16);
+            b[0] = e4m3x2_to_f16x2(cb[u][bb].x); b[1] = e4m3x2_to_f16x2(cb[u][bb].x >> 16);
+            b[2] = e4m3x2_to_f16x2(cb[u][bb].y); b[3] = e4m3x2_to_f16x2(cb[u][bb].y >> 16);
+          }
+          const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu);
+          const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_16816_f16(acc, a[0], b[0], a[1], b[1], qb[nt][2 * bb][0], qb[nt][2 * bb][1]);
+            mma_16816_f16(acc, a[2], b[2], a[3], b[3], qb[nt][2 * bb + 1][0], qb[nt][2 * bb + 1][1]);
+            tot[nt][0] = fmaf(scg, acc[0], tot[nt][0]);
+            tot[nt][1] = fmaf(scg, acc[1], tot[nt][1]);
+            tot[nt][2] = fmaf(scg8, acc[2], tot[nt][2]);
+            tot[nt][3] = fmaf(scg8, acc[3], tot[nt][3]);
+          }
         }
-        const float scg = ue8m0_value((sa[u] >> (8 * bb)) & 0xFFu);
-        const float scg8 = ue8m0_value((sb[u] >> (8 * bb)) & 0xFFu);
+        float sg = 0.f, sg8 = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_16816_f16(acc, a[0], b[0], a[1], b[1], qb[nt][2 * bb][0], qb[nt][2 * bb][1]);
-          mma_16816_f16(acc, a[2], b[2], a[3], b[3], qb[nt][2 * bb + 1][0], qb[nt][2 * bb + 1][1]);
-          tot[nt][0] = fmaf(scg, acc[0], tot[nt][0]);
-          tot[nt][1] = fmaf(scg, acc[1], tot[nt][1]);
-          tot[nt][2] = fmaf(scg8, acc[2], tot[nt][2]);
-          tot[nt][3] = fmaf(scg8, acc[3], tot[nt][3]);
+          sg = fmaf(w0[nt], fmaxf(tot[nt][0], 0.f), sg);
+          sg = fmaf(w1[nt], fmaxf(tot[nt][1], 0.f), sg);
+          sg8 = fmaf(w0[nt], fmaxf(tot[nt][2], 0.f), sg8);
+          sg8 = fmaf(w1[nt], fmaxf(tot[nt][3], 0.f), sg8);
         }
+        sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+        sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+        sg8 += __shfl_xor_sync(0xffffffffu, sg8, 1);
+        sg8 += __shfl_xor_sync(0xffffffffu, sg8, 2);
+        float* srow = a.scores + (int64_t)q * a.ld;
+        if (t == 0 && rg[u] < nv) srow[rg[u]] = sg;
+        if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
       }
-      float sg = 0.f, sg8 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        sg = fmaf(w0[nt], fmaxf(tot[nt][0], 0.f), sg);
-        sg = fmaf(w1[nt], fmaxf(tot[nt][1], 0.f), sg);
-        sg8 = fmaf(w0[nt], fmaxf(tot[nt][2], 0.f), sg8);
-        sg8 = fmaf(w1[nt], fmaxf(tot[nt][3], 0.f), sg8);
-      }
-      sg += __shfl_xor_sync(0xffffffffu, sg, 1);
-      sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-      sg8 += __shfl_xor_sync(0xffffffffu, sg8, 1);
-      sg8 += __shfl_xor_sync(0xffffffffu, sg8, 2);
-      float* srow = scores + (int64_t)q * ld;
-      if (t == 0 && rg[u] < nv) srow[rg[u]] = sg;
-      if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
     }
+  };
+  const int64_t n_static = idx_static_items(n_items);
+  for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static};
+  tk.start();
+  for (;;) {
+    const unsigned long long item = tk.cur();
+    if (item >= (unsigned long long)n_items) break;
+    tk.prefetch();
+    run((int64_t)item);
+    tk.advance();
+  }
+  tk.finish();
+}
+
+// Scores of the entries compressed in this step (a decode step closes at
+// most a group or two per sequence): one warp per query, lane l holding
+// channels 4l .. 4l+3 of every head; keys of any of the three formats decode
+// exactly to fp32, products and sums in fp32. The scan above leaves these
+// entries out when new_first is set, so that it can run while the step's
+// compress is still writing them.
+template <int HI, int KF>
+__global__ void __launch_bounds__(256) index_tail_kernel(const IdxArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = blockIdx.x * 8 + warp;
+  if (q >= a.n_query) return;
+  const int b = a.seq_of_q[q];
+  if (b < 0 || b >= a.n_seq) return;  // flagged by the scan
+  if (a.new_tok[b + 1] <= a.new_tok[b]) return;
+  int n_all;
+  const int j_begin = idx_query_range(a, q, b, false, &n_all);
+  if (j_begin >= n_all) return;
+  float qv[HI][4], w[HI];
+#pragma unroll
+  for (int h = 0; h < HI; ++h) {
+    const uint2 v = *reinterpret_cast<const uint2*>(a.q_idx + ((int64_t)q * HI + h) * kIdxDim + 4 * lane);
+    qv[h][0] = bf16lo(v.x); qv[h][1] = bf16hi(v.x);
+    qv[h][2] = bf16lo(v.y); qv[h][3] = bf16hi(v.y);
+    w[h] = a.w_heads[(int64_t)q * HI + h];
+  }
+  const int64_t row0 = a.pool_off[b];
+  for (int j = j_begin; j < n_all; ++j) {
+    const int64_t row = row0 + j;
+    float k[4];
+    if constexpr (KF == 0) {
+      const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(a.keys) + row * kIdxDim +
+                                                      4 * lane);
+      k[0] = bf16lo(v.x); k[1] = bf16hi(v.x); k[2] = bf16lo(v.y); k[3] = bf16hi(v.y);
+    } else {
+      const float sc = ue8m0_value(a.key_scale[row * (kIdxDim / 32) + lane / 8]);
+      if constexpr (KF == 1) {
+        const uint32_t c = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(a.keys) +
+                                                              row * kIdxDim + 4 * lane);
+        const float2 f0 = e4m3x2_to_float2((uint16_t)(c & 0xFFFFu)), f1 = e4m3x2_to_float2((uint16_t)(c >> 16));
+        k[0] = f0.x * sc; k[1] = f0.y * sc; k[2] = f1.x * sc; k[3] = f1.y * sc;
+      } else {
+        const uint32_t c = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(a.keys) +
+                                                              row * (kIdxDim / 2) + 2 * lane);
+        const float2 f0 = e2m1x2_to_float2_scaled(c & 0xFFu), f1 = e2m1x2_to_float2_scaled(c >> 8);
+        const float s2 = sc * kE2M1Unscale;
+        k[0] = f0.x * s2; k[1] = f0.y * s2; k[2] = f1.x * s2; k[3] = f1.y * s2;
+      }
+    }
+    float sigma = 0.f;
+#pragma unroll
+    for (int h = 0; h < HI; ++h) {
+      float d = qv[h][0] * k[0];
+      d = fmaf(qv[h][1], k[1], d);
+      d = fmaf(qv[h][2], k[2], d);
+      d = fmaf(qv[h][3], k[3], d);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      sigma = fmaf(w[h], fmaxf(d, 0.f), sigma);
+    }
+    if (lane == 0) a.scores[(int64_t)q * a.ld + j] = sigma;
   }
 }
 
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, int n_query, int n_seq,
-                               int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
-                               const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
-                               const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags) {
-  if (n_query == 0 || max_vis == 0) return cudaSuccess;
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a) {
+  if (a.n_query == 0 || a.max_vis == 0) return cudaSuccess;
   const int64_t cap = (int64_t)num_sms * 2;
   // chunk of one work item: 256 keys (bf16; fp8 and mxfp4 with 32 heads), 512
   // (fp8 with 8 heads, mxfp4 with 8 or 16 heads)
   const int u_q = ((idx_fmt == 3 && idx_heads <= 16) || (idx_fmt == 1 && idx_heads == 8)) ? 4 : 2;
   const int64_t chunk = idx_fmt == 0 ? kIdxChunk : 128 * u_q;
-  const int64_t n_chunks = (max_vis + chunk - 1) / chunk;
-  const int64_t items = n_chunks * n_query;
+  a.n_chunks = (a.max_vis + chunk - 1) / chunk;
+  const int64_t items = a.n_chunks * a.n_query;
   const dim3 grid((unsigned)(items < cap ? items : cap));
-#define CSA2_IDXQ(NT, KF, U)                                                                                  \
-  index_score_fp8_kernel<NT, KF, U><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads,  \
-                                                          (const uint8_t*)keys, key_scale, pool_off, seq_of_q, \
-                                                          n_vis, scores, ld, flags)
-#define CSA2_IDX(NT, UQ, U8)                                                                               \
-  do {                                                                                                     \
-    if (idx_fmt == 1) CSA2_IDXQ(NT, 1, U8);                                                                \
-    else if (idx_fmt == 3) CSA2_IDXQ(NT, 3, UQ);                                                           \
-    else                                                                                                   \
-      index_score_bf16_kernel<NT><<<grid, 256, 0, st>>>(n_query, n_seq, n_chunks, max_vis, q_idx, w_heads, \
-                                                        (const uint16_t*)keys, pool_off, seq_of_q,         \
-                                                        n_vis, scores, ld, flags);                         \
+#define CSA2_IDX(NT, UQ, U8)                                                         \
+  do {                                                                               \
+    if (idx_fmt == 1) index_score_fp8_kernel<NT, 1, U8><<<grid, 256, 0, st>>>(a);    \
+    else if (idx_fmt == 3) index_score_fp8_kernel<NT, 3, UQ><<<grid, 256, 0, st>>>(a); \
+    else index_score_bf16_kernel<NT><<<grid, 256, 0, st>>>(a);                       \
   } while (0)
   switch (idx_heads) {
     case 8: CSA2_IDX(1, 4, 4); break;
@@ -332,7 +454,25 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
     default: return cudaErrorInvalidValue;
   }
 #undef CSA2_IDX
-#undef CSA2_IDXQ
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_tail(cudaStream_t st, int idx_heads, int idx_fmt, const IdxArgs& a) {
+  if (a.n_query == 0 || a.max_vis == 0 || a.new_first == nullptr) return cudaSuccess;
+  const dim3 grid((unsigned)((a.n_query + 7) / 8));
+#define CSA2_TAIL(HI)                                                     \
+  do {                                                                    \
+    if (idx_fmt == 1) index_tail_kernel<HI, 1><<<grid, 256, 0, st>>>(a);  \
+    else if (idx_fmt == 3) index_tail_kernel<HI, 3><<<grid, 256, 0, st>>>(a); \
+    else index_tail_kernel<HI, 0><<<grid, 256, 0, st>>>(a);               \
+  } while (0)
+  switch (idx_heads) {
+    case 8: CSA2_TAIL(8); break;
+    case 16: CSA2_TAIL(16); break;
+    case 32: CSA2_TAIL(32); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef CSA2_TAIL
   return cudaGetLastError();
 }
 

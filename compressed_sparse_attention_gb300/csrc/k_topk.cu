@@ -819,6 +819,207 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
          al((size_t)n_query * (size_t)(max_vis > 0 ? max_vis : 1) * 8);
 }
 
+// ---------------------------------------------------------------------------
+// Rows of at most TPB * PER scores: one CTA per query, no cluster. Thread t
+// keeps the order-preserving keys of entries PER t .. PER t + PER - 1 in
+// registers. The search narrows the threshold eight bits at a time below the
+// row's common prefix (the leading bits that its smallest and largest keys
+// share): per-warp 256-bin histograms of the keys still in play, one warp
+// finds the bin that holds the k-th largest, and the search stops once that
+// bin holds exactly the keys still needed, or when no bits are left (ties at
+// one key value, taken in index order). One 64-bit block scan of
+// (above-threshold, at-threshold) counts then gives every thread the output
+// positions of its entries, which come out in ascending index order.
+template <int TPB, int PER>
+__global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
+                                                      const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
+                                                      int32_t* __restrict__ out_idx) {
+  constexpr int NW = TPB / 32;
+  __shared__ uint32_t hist[NW][256];
+  __shared__ uint32_t cnt[256];
+  __shared__ uint32_t red[2][NW];
+  __shared__ uint32_t res[3];
+  __shared__ unsigned long long wsum[NW];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = blockIdx.x;
+  const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
+  int32_t* out = out_idx + (int64_t)q * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += TPB) out[i] = i < n ? i : -1;
+    return;
+  }
+  // ---- keys of this thread's entries, and the row's smallest and largest key
+  const float* row = scores + (int64_t)q * ld;
+  const int e0 = PER * tid;
+  uint32_t key[PER];
+  if (((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15) == 0) && e0 + PER <= n) {
+#pragma unroll
+    for (int c = 0; c < PER / 4; ++c) {
+      const float4 v = reinterpret_cast<const float4*>(row + e0)[c];
+      key[4 * c] = score_key(v.x);
+      key[4 * c + 1] = score_key(v.y);
+      key[4 * c + 2] = score_key(v.z);
+      key[4 * c + 3] = score_key(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) key[i] = (e0 + i < n) ? score_key(row[e0 + i]) : 0u;
+  }
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (e0 + i < n) {
+      mn = min(mn, key[i]);
+      mx = max(mx, key[i]);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    red[0][warp] = mn;
+    red[1][warp] = mx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    mn = lane < NW ? red[0][lane] : 0xFFFFFFFFu;
+    mx = lane < NW ? red[1][lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      res[0] = mn;
+      res[1] = mx;
+    }
+  }
+  __syncthreads();
+  mn = res[0];
+  mx = res[1];
+  // ---- threshold search: keys in play share their bits at and above `hi`
+  // with P; the digit below them has at most 8 bits
+  int hi = (mn == mx) ? 0 : 32 - __clz(mn ^ mx);
+  uint32_t P = (hi == 0) ? mn : (hi >= 32 ? 0u : (mn >> hi));
+  uint32_t need = (uint32_t)k;
+  bool exact = false;
+  while (hi > 0) {
+    __syncthreads();  // res[] and cnt[] of the previous level have been read
+    const int lo = hi > 8 ? hi - 8 : 0;
+    const uint32_t dmask = (1u << (hi - lo)) - 1u;
+#pragma unroll
+    for (int i = lane; i < 256; i += 32) hist[warp][i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (e0 + i < n && (hi >= 32 || (key[i] >> hi) == P)) atomicAdd(&hist[warp][(key[i] >> lo) & dmask], 1u);
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) v += hist[w][tid];
+      cnt[tid] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l takes bins 255 - 8l .. 248 - 8l (descending); the bin where
+      // the running count from the top first reaches `need` holds the k-th key
+      uint32_t c[8], sl = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = cnt[255 - 8 * lane - i];
+        sl += c[i];
+      }
+      uint32_t incl = sl;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - sl;
+      const unsigned bal = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+      if (lane == __ffs(bal) - 1) {
+        uint32_t cum = excl;
+        int i = 0;
+#pragma unroll 1
+        for (; i < 7; ++i) {
+          if (cum + c[i] >= need) break;
+          cum += c[i];
+        }
+        res[0] = (uint32_t)(255 - 8 * lane - i);
+        res[1] = c[i];
+        res[2] = cum;
+      }
+    }
+    __syncthreads();
+    const uint32_t bstar = res[0], nbin = res[1], above = res[2];
+    need -= above;
+    P = (hi >= 32 ? 0u : (P << (hi - lo))) | bstar;
+    hi = lo;
+    if (nbin == need) {
+      exact = true;
+      break;
+    }
+  }
+  // ---- output positions: entries above the threshold, then ties in index order
+  uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (e0 + i < n) {
+      const uint32_t top = key[i] >> hi;
+      n_gt += top > P ? 1u : 0u;
+      n_eq += top == P ? 1u : 0u;
+    }
+  unsigned long long v = ((unsigned long long)n_eq << 32) | n_gt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) wsum[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long w = lane < NW ? wsum[lane] : 0ull;
+    const unsigned long long own = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += u;
+    }
+    if (lane < NW) wsum[lane] = w - own;  // exclusive over warps
+  }
+  __syncthreads();
+  v += wsum[warp] - (((unsigned long long)n_eq << 32) | n_gt);  // exclusive over threads
+  const uint32_t gt_before = (uint32_t)(v & 0xFFFFFFFFull), eq_before = (uint32_t)(v >> 32);
+  uint32_t pos, eq_left;
+  if (exact) {
+    pos = gt_before + eq_before;
+    eq_left = n_eq;
+  } else {
+    pos = gt_before + min(eq_before, need);
+    eq_left = need > eq_before ? min(n_eq, need - eq_before) : 0u;
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (e0 + i < n) {
+      const uint32_t top = key[i] >> hi;
+      bool take = top > P;
+      if (top == P && eq_left > 0) {
+        take = true;
+        --eq_left;
+      }
+      if (take) out[pos++] = e0 + i;
+    }
+}
+
+template <int TPB, int PER>
+static cudaError_t launch_topk_row(cudaStream_t st, int n_query, const float* scores, int64_t ld,
+                                   const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx) {
+  topk_row_kernel<TPB, PER><<<n_query, TPB, 0, st>>>(scores, ld, n_vis, max_vis, k, out_idx);
+  return cudaGetLastError();
+}
+
 template <int PER>
 static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, const float* scores, int64_t ld,
                                       const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx, bool* launched) {
@@ -854,6 +1055,15 @@ static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, 
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch) {
   if (n_query == 0) return cudaSuccess;
+  // rows of up to 16,384 scores: one CTA per query holding its row in registers
+  if (max_vis <= 16384) {
+    cudaError_t e;
+    if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
+    else if (max_vis <= 8192) e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
+    else e = launch_topk_row<1024, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
+    if (e == cudaSuccess) *n_launch += 1;
+    return e;
+  }
   // a cluster of up to 8 CTAs per query, each holding 16,384 scores (a
   // 64K-context decode row is one CTA), or 32,768 for rows up to 262,144
   const int c16 = topk_cluster_size(max_vis, TkLayout<16>::kSlice);

@@ -20,7 +20,7 @@ struct AttendParams {
   const float* sink;
   uint16_t* out;
   float* lse;
-  float* ws_o;    // [n_query][n_split][64][512] unnormalised partial outputs
+  uint16_t* ws_o; // [n_query][n_slots][64][512] unnormalised partial outputs, bf16
   float2* ws_ml;  // [n_query][n_split][64] running (max, sum) per head
   uint32_t* flags;
   int n_seq;
@@ -47,10 +47,30 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
                             float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
                             uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags);
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, int n_query, int n_seq,
-                               int64_t max_vis, const uint16_t* q_idx, const float* w_heads, const void* keys,
-                               const uint8_t* key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
-                               const int32_t* n_vis, float* scores, int64_t ld, uint32_t* flags);
+// arguments of the index scan (csa2_index_score) and of its tail kernel
+struct IdxArgs {
+  int n_query = 0, n_seq = 0;
+  int64_t n_chunks = 0, max_vis = 0;
+  const uint16_t* q_idx = nullptr;
+  const float* w_heads = nullptr;
+  const void* keys = nullptr;
+  const uint8_t* key_scale = nullptr;
+  const int64_t* pool_off = nullptr;
+  const int32_t* seq_of_q = nullptr;
+  const int32_t* n_vis = nullptr;
+  float* scores = nullptr;
+  int64_t ld = 0;
+  uint32_t* flags = nullptr;
+  // set: the scan leaves out the entries this step compresses (entries at or
+  // above first_pos[b] / m of a sequence with tok_off[b+1] > tok_off[b]) and
+  // the tail kernel scores them
+  const int64_t* new_first = nullptr;
+  const int64_t* new_tok = nullptr;
+  int m = 1;
+  unsigned long long* work = nullptr;  // [2] ticket counters, zero between launches
+};
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a);
+cudaError_t launch_index_tail(cudaStream_t st, int idx_heads, int idx_fmt, const IdxArgs& a);
 // tensor-core form of the indexer for many queries per sequence (bf16 keys)
 bool index_tc_suited(int idx_fp8, int n_query, int n_seq, int idx_heads);
 cudaError_t launch_index_score_tc(cudaStream_t st, int num_sms, int idx_heads, int n_query, int n_seq,

@@ -285,7 +285,9 @@ def test_index_score_many_queries(idx_heads, interleave):
 
 @pytest.mark.parametrize("n,tie_levels,k", [(3000, 0, 512), (3000, 3, 512), (20000, 2, 512), (5000, 0, 2048),
                                             (777, 0, 1), (262144, 0, 512), (262144, 40, 512), (100, 0, 512),
-                                            (20000, 1, 512), (40000, 0, 64), (300000, 0, 512), (300000, 7, 512)])
+                                            (20000, 1, 512), (40000, 0, 64), (300000, 0, 512), (300000, 7, 512),
+                                            (16384, 0, 512), (16384, 1, 512), (16384, 6, 512), (8192, 2, 2048),
+                                            (2047, 0, 512), (6001, 0, 100)])
 def test_topk_bit_exact(n, tie_levels, k):
     from compressed_sparse_attention_gb300 import binding
     ctx = context()

@@ -40,3 +40,28 @@ def test_step_decode_forms(n_seq, topk):
     sample = range(wl.n_query) if wl.n_query <= 8 else sorted({0, 1, wl.n_query // 2, wl.n_query - 1})
     same = [_check_query(ctx, case, qi, geom, f, out, scores, sel, state, wl.name)[1] for qi in sample]
     assert sum(same) >= len(same) - 1, "the step's selection differs from the oracle's on more than one query"
+
+
+@pytest.mark.parametrize("m", [1, 2])
+def test_step_two_queries_per_sequence(m):
+    """Two decode queries per sequence at t = N-2 and N-1 with compress ratio
+    m: the step closes up to two groups per sequence, and the query at N-2
+    sees only the entries that close by its own position. These entries are
+    scored apart from the scan over the older ones while compress runs."""
+    require_gpu()
+    from compressed_sparse_attention_gb300 import binding
+    n_seq = 6
+    g = torch.Generator().manual_seed(950 + m)
+    lens = tuple(int(x) * m for x in torch.randint(1500, 4000, (n_seq,), generator=g))
+    wl = Workload(f"two_q_m{m}", n_seq, lens, m, seed=950 + m, n_query_per_seq=2, value_std=1.0 / 22.6,
+                  outlier_frac=0.01)
+    ctx = context(compress_ratio=m)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    case = Case(ctx, wl)
+    idx = torch.empty((wl.n_query, wl.topk), dtype=torch.int32, device=DEV)
+    out, scores = _step(ctx, case, binding.MODE_FULL, idx)
+    sel = idx.cpu().numpy()
+    state = _full_state(ctx, case, geom, f)
+    same = [_check_query(ctx, case, qi, geom, f, out, scores, sel, state, wl.name)[1] for qi in range(wl.n_query)]
+    assert sum(same) >= len(same) - 1
