@@ -59,7 +59,8 @@ class StepArgs(C.Structure):
                 ("first_pos", C.c_void_p), ("norm_w", C.c_void_p), ("w_idx", C.c_void_p),
                 ("k_norm_w", C.c_void_p),
                 ("topk_idx", C.c_void_p), ("out", C.c_void_p), ("lse", C.c_void_p),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+                ("append", C.c_int32), ("state_raw", C.c_void_p), ("state_gate", C.c_void_p)]
 
 
 # name -> (restype, argtypes); every symbol include/csa2.h declares
@@ -76,6 +77,9 @@ SIGNATURES = {
     "csa2_compress": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int64,
                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                 C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_compress_append": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int64,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "csa2_index_score": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                    C.c_void_p, C.c_int64]),
@@ -213,6 +217,19 @@ class Context:
             self._p(idx_keys, None, "idx_keys"), self._p(idx_key_scale, torch.uint8, "idx_key_scale")),
             "csa2_compress")
 
+    def compress_append(self, raw, gate, n_seq, tok_off, first_pos, pool_off, norm_w, w_idx, k_norm_w,
+                        pool_kv, pool_kv_scale, idx_keys, idx_key_scale, state_raw, state_gate):
+        n_tokens = 0 if raw is None else raw.shape[0]
+        self._ok(self.lib.csa2_compress_append(
+            self.h, C.c_void_p(_stream()), self._p(raw, torch.bfloat16, "raw"), self._p(gate, torch.float32, "gate"),
+            n_seq, n_tokens, self._p(tok_off, torch.int64, "tok_off"), self._p(first_pos, torch.int64, "first_pos"),
+            self._p(pool_off, torch.int64, "pool_off"), self._p(norm_w, torch.float32, "norm_w"),
+            self._p(w_idx, torch.bfloat16, "w_idx"), self._p(k_norm_w, torch.float32, "k_norm_w"),
+            self._p(pool_kv, None, "pool_kv"), self._p(pool_kv_scale, torch.uint8, "pool_kv_scale"),
+            self._p(idx_keys, None, "idx_keys"), self._p(idx_key_scale, torch.uint8, "idx_key_scale"),
+            self._p(state_raw, torch.bfloat16, "state_raw"), self._p(state_gate, torch.float32, "state_gate")),
+            "csa2_compress_append")
+
     def index_score(self, n_seq, q_idx, w_heads, idx_keys, idx_key_scale, pool_off, seq_of_q, n_vis, max_vis,
                     scores):
         self._ok(self.lib.csa2_index_score(
@@ -254,7 +271,7 @@ class Context:
     def step(self, mode, n_seq, max_vis, *, q, q_pos, seq_of_q, n_vis, sink, win_kv, win_off, pool_kv, pool_off,
              topk_idx, out, workspace, q_idx=None, w_heads=None, win_scale=None, win_lo=None, pool_scale=None,
              idx_keys=None, idx_key_scale=None, raw=None, gate=None, tok_off=None, first_pos=None, norm_w=None,
-             w_idx=None, k_norm_w=None, lse=None):
+             w_idx=None, k_norm_w=None, lse=None, append=False, state_raw=None, state_gate=None):
         a = StepArgs()
         a.mode, a.n_seq, a.n_query, a.max_vis = mode, n_seq, q.shape[0], max_vis
         a.q = self._p(q, torch.bfloat16, "q")
@@ -286,6 +303,9 @@ class Context:
         a.lse = self._p(lse, torch.float32, "lse")
         a.workspace = self._p(workspace, None, "workspace")
         a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        a.append = 1 if append else 0
+        a.state_raw = self._p(state_raw, torch.bfloat16, "state_raw")
+        a.state_gate = self._p(state_gate, torch.float32, "state_gate")
         self._ok(self.lib.csa2_step(self.h, C.c_void_p(_stream()), C.byref(a)), "csa2_step")
 
 

@@ -197,12 +197,15 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                int64_t n_tokens, const int64_t* tok_off, const int64_t* first_pos,
                                const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
                                const float* k_norm_w, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
-                               uint8_t* idx_key_scale) {
+                               uint8_t* idx_key_scale, bool append = false, uint16_t* state_raw = nullptr,
+                               float* state_gate = nullptr) {
   const csa2_config& c = ctx->cfg;
   const int m = c.compress_ratio;
   if (n_tokens < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_seq / n_tokens");
   if (n_tokens == 0) return CSA2_OK;
-  if (n_tokens % m) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_tokens must be whole groups");
+  if (!append && n_tokens % m) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_tokens must be whole groups");
+  if (append && m > 1 && (!state_raw || !state_gate || !aligned16(state_raw) || !aligned16(state_gate)))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "compress_append: the state must be given and 16-byte aligned");
   if (!raw || !tok_off || !first_pos || !pool_off || !norm_w || !pool_kv || (m > 1 && !gate))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: null pointer");
   if (c.kv_format != CSA2_KV_BF16 && !pool_kv_scale)
@@ -211,12 +214,20 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: index key outputs missing");
   if (!aligned16(raw) || (gate && !aligned16(gate)) || !aligned16(norm_w) || (w_idx && !aligned16(w_idx)))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: inputs must be 16-byte aligned");
-  cudaError_t e = csa2::launch_compress(st, n_tokens / m, raw, gate, m, n_seq, tok_off, first_pos, pool_off, norm_w,
+  csa2::AppendArgs app;
+  app.n_tokens = n_tokens;
+  app.state_raw = state_raw;
+  app.state_gate = state_gate;
+  // append form: each sequence closes at most floor(n_b / m) + 1 groups
+  const int64_t n_groups = append ? n_tokens / m + n_seq : n_tokens / m;
+  int nl = 0;
+  cudaError_t e = csa2::launch_compress(st, n_groups, raw, gate, m, n_seq, tok_off, first_pos, pool_off, norm_w,
                                         w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
                                         c.kv_format, c.idx_key_format,
-                                        pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags);
+                                        pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags,
+                                        append ? &app : nullptr, &nl);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
-  ctx->last_launches += 1;
+  ctx->last_launches += nl;
   return CSA2_OK;
 }
 
@@ -228,6 +239,18 @@ csa2_status csa2_compress(csa2_ctx* ctx, void* stream, const uint16_t* raw, cons
   ctx->last_launches = 0;
   return do_compress(ctx, reinterpret_cast<cudaStream_t>(stream), raw, gate, n_seq, n_tokens, tok_off, first_pos,
                      pool_off, norm_w, w_idx, k_norm_w, pool_kv, pool_kv_scale, idx_keys, idx_key_scale);
+}
+
+csa2_status csa2_compress_append(csa2_ctx* ctx, void* stream, const uint16_t* raw, const float* gate, int32_t n_seq,
+                                 int64_t n_tokens, const int64_t* tok_off, const int64_t* first_pos,
+                                 const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
+                                 const float* k_norm_w, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
+                                 uint8_t* idx_key_scale, uint16_t* state_raw, float* state_gate) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_compress(ctx, reinterpret_cast<cudaStream_t>(stream), raw, gate, n_seq, n_tokens, tok_off, first_pos,
+                     pool_off, norm_w, w_idx, k_norm_w, pool_kv, pool_kv_scale, idx_keys, idx_key_scale, true,
+                     state_raw, state_gate);
 }
 
 // new_first / new_tok set: the scan leaves out the entries that this step's
@@ -458,7 +481,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     }
     ctx->last_launches = 0;
     s = do_compress(ctx, cs, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
-                    a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale);
+                    a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale,
+                    a->append != 0, a->state_raw, a->state_gate);
     if (s != CSA2_OK) return join(s);
     launches += ctx->last_launches;
     if (tail) {

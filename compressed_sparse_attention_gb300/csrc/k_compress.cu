@@ -118,7 +118,45 @@ __device__ __forceinline__ int find_segment_warp(const int64_t* __restrict__ off
   return lo;
 }
 
-// KVF: pool rows 0 bf16, 1 fp8, 2 fp4 (e4m3 / 16); IKF: keys 0 bf16, 1 fp8, 3 mxfp4
+// Append form: sequence b closes g_b = floor((p_b + n_b) / m) - floor(p_b / m)
+// groups (p_b its first new position, n_b its new tokens); CTA i takes the
+// i-th closing group in sequence order. Warp-wide; false past the last one.
+__device__ __forceinline__ bool find_append_group(const int64_t* __restrict__ tok_off,
+                                                  const int64_t* __restrict__ first_pos, int n_seq, int m,
+                                                  int64_t i, int* b_out, int64_t* j_out) {
+  const int lane = threadIdx.x & 31;
+  int64_t base = 0;
+  for (int s0 = 0; s0 < n_seq; s0 += 32) {
+    const int b = s0 + lane;
+    int64_t g = 0;
+    if (b < n_seq) {
+      const int64_t p = first_pos[b], n = tok_off[b + 1] - tok_off[b];
+      g = (p >= 0 && n >= 0) ? (p + n) / m - p / m : 0;
+    }
+    int64_t incl = g;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+    if (i < base + total) {
+      const int64_t excl = base + incl - g;
+      const unsigned bal = __ballot_sync(0xffffffffu, g > 0 && excl <= i && i < excl + g);
+      const int src = __ffs(bal) - 1;
+      const int64_t e = __shfl_sync(0xffffffffu, excl, src);
+      *b_out = s0 + src;
+      *j_out = first_pos[s0 + src] / m + (i - e);
+      return true;
+    }
+    base += total;
+  }
+  return false;
+}
+
+// KVF: pool rows 0 bf16, 1 fp8, 2 fp4 (e4m3 / 16); IKF: keys 0 bf16, 1 fp8, 3 mxfp4.
+// st_raw set: the append form (csa2_compress_append), tokens of a group's
+// positions below first_pos[b] come from the state (slot b m + pos mod m).
 template <int KVF, int IKF>
 __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
@@ -126,7 +164,8 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const int64_t* __restrict__ pool_off, const float* __restrict__ norm_w,
     const uint16_t* __restrict__ w_idx, const float* __restrict__ k_norm_w, int idx_dim, float eps,
     RopeParams rp, void* __restrict__ pool_kv, uint8_t* __restrict__ pool_kv_scale,
-    void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags) {
+    void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags, int append,
+    const uint16_t* __restrict__ st_raw, const float* __restrict__ st_gate) {
   __shared__ float c_hat_s[kDim];
   __shared__ float k_lin_s[kIdxDim];
   __shared__ float red_s[8];
@@ -144,27 +183,54 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   const int c0 = 2 * tid;
   const float2 nw = *reinterpret_cast<const float2*>(norm_w + c0);
   const float knw = (w_idx != nullptr && warp < idx_dim / 32) ? k_norm_w[warp * 32 + lane] : 0.f;
-  const int64_t tok0 = (int64_t)blockIdx.x * m;
-  // the group's tokens depend only on the group index: load them before the
-  // segment lookup (m <= 16)
   uint32_t rw[16];
   float2 gv[16];
+  int64_t j, prow;
+  if (!append) {
+    const int64_t tok0 = (int64_t)blockIdx.x * m;
+    // the group's tokens depend only on the group index: load them before the
+    // segment lookup (m <= 16)
 #pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    if (u < m) {
-      rw[u] = *reinterpret_cast<const uint32_t*>(raw + (tok0 + u) * kDim + c0);
-      gv[u] = m > 1 ? *reinterpret_cast<const float2*>(gate + (tok0 + u) * kDim + c0) : make_float2(0.f, 0.f);
+    for (int u = 0; u < 16; ++u) {
+      if (u < m) {
+        rw[u] = *reinterpret_cast<const uint32_t*>(raw + (tok0 + u) * kDim + c0);
+        gv[u] = m > 1 ? *reinterpret_cast<const float2*>(gate + (tok0 + u) * kDim + c0) : make_float2(0.f, 0.f);
+      }
     }
-  }
-  const int b = find_segment_warp(tok_off, n_seq, tok0);
-  const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
-  const int64_t pbase = pool_off[b], pend = pool_off[b + 1];
-  const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
-  const int64_t j = pos0 / m;
-  const int64_t prow = pbase + j;
-  if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || tok0 >= seg1 || prow >= pend) {
-    if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
-    return;
+    const int b = find_segment_warp(tok_off, n_seq, tok0);
+    const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
+    const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
+    j = pos0 / m;
+    prow = pool_off[b] + j;
+    if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || tok0 >= seg1 ||
+        prow >= pool_off[b + 1]) {
+      if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
+      return;
+    }
+  } else {
+    int b;
+    if (!find_append_group(tok_off, first_pos, n_seq, m, blockIdx.x, &b, &j)) return;  // past the last group
+    const int64_t seg0 = tok_off[b], fp = first_pos[b];
+    prow = pool_off[b] + j;
+    if (prow >= pool_off[b + 1]) {
+      if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (u < m) {
+        const int64_t pos = j * m + u;
+        if (pos < fp) {  // an earlier call's token, waiting in the state
+          const int64_t slot = (int64_t)b * m + pos % m;
+          rw[u] = *reinterpret_cast<const uint32_t*>(st_raw + slot * kDim + c0);
+          gv[u] = m > 1 ? *reinterpret_cast<const float2*>(st_gate + slot * kDim + c0) : make_float2(0.f, 0.f);
+        } else {
+          const int64_t tok = seg0 + (pos - fp);
+          rw[u] = *reinterpret_cast<const uint32_t*>(raw + tok * kDim + c0);
+          gv[u] = m > 1 ? *reinterpret_cast<const float2*>(gate + tok * kDim + c0) : make_float2(0.f, 0.f);
+        }
+      }
+    }
   }
   // ---- pooling (fp32): per channel softmax of the gate logits over the group
   float pooled[2];
@@ -263,7 +329,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   // ---- RoPE at the group's first token position, then store
   if (rp.pairs > 0 && c0 >= kDim - 2 * rp.pairs) {
     float cs, sn;
-    rope_cs(rp, (c0 - (kDim - 2 * rp.pairs)) >> 1, pos0, cs, sn);
+    rope_cs(rp, (c0 - (kDim - 2 * rp.pairs)) >> 1, j * m, cs, sn);  // the group's first position
     const float x0 = ch[0], x1 = ch[1];
     ch[0] = x0 * cs - x1 * sn;
     ch[1] = x0 * sn + x1 * cs;
@@ -290,6 +356,33 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
         (uint8_t)(e2m1_code(ch[0], sc) | (e2m1_code(ch[1], sc) << 4));
     if ((tid & 7) == 0) pool_kv_scale[prow * (kDim / 16) + tid / 8] = (uint8_t)sb;
   }
+}
+
+// The append form's second launch: the new tokens of each sequence's group
+// still open after the call (positions from floor((p + n) / m) m on) go to
+// their state slots b m + pos mod m. One warp per new token: 1 KiB of raw
+// (bf16) and 2 KiB of gate logits.
+__global__ void __launch_bounds__(256) compress_state_store_kernel(
+    const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
+    const int64_t* __restrict__ tok_off, const int64_t* __restrict__ first_pos, int64_t n_tokens,
+    uint16_t* __restrict__ st_raw, float* __restrict__ st_gate) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tok = (int64_t)blockIdx.x * 8 + warp;
+  if (tok >= n_tokens) return;
+  const int b = find_segment_warp(tok_off, n_seq, tok);
+  const int64_t p = first_pos[b], n = tok_off[b + 1] - tok_off[b];
+  if (p < 0 || n < 0) return;
+  const int64_t pos = p + (tok - tok_off[b]);
+  if (pos < ((p + n) / m) * m) return;  // consumed by a group this call closed
+  const int64_t slot = (int64_t)b * m + pos % m;
+  const uint4* sr = reinterpret_cast<const uint4*>(raw + tok * kDim);
+  uint4* dr = reinterpret_cast<uint4*>(st_raw + slot * kDim);
+  dr[lane] = sr[lane];
+  dr[lane + 32] = sr[lane + 32];
+  const uint4* sg = reinterpret_cast<const uint4*>(gate + tok * kDim);
+  uint4* dg = reinterpret_cast<uint4*>(st_gate + slot * kDim);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) dg[lane + 32 * k] = sg[lane + 32 * k];
 }
 
 // ---------------------------------------------------------------------------
@@ -327,13 +420,17 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
                             const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fmt,
                             int idx_fmt, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
-                            uint8_t* idx_key_scale, uint32_t* flags) {
+                            uint8_t* idx_key_scale, uint32_t* flags, const AppendArgs* app, int* n_launch) {
   if (n_groups == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_groups);
+  const int append = app != nullptr ? 1 : 0;
+  const uint16_t* st_raw = app != nullptr ? app->state_raw : nullptr;
+  const float* st_gate = app != nullptr ? app->state_gate : nullptr;
 #define CSA2_COMPRESS(KF, IF)                                                                      \
   compress_kernel<KF, IF><<<grid, kCmpThreads, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
                                                 norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
-                                                pool_kv_scale, idx_keys, idx_key_scale, flags)
+                                                pool_kv_scale, idx_keys, idx_key_scale, flags, append, \
+                                                st_raw, st_gate)
 #define CSA2_COMPRESS_K(KF)                               \
   do {                                                    \
     if (idx_fmt == 1) CSA2_COMPRESS(KF, 1);               \
@@ -345,7 +442,17 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   else CSA2_COMPRESS_K(0);
 #undef CSA2_COMPRESS_K
 #undef CSA2_COMPRESS
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *n_launch += 1;
+  if (append && m > 1 && app->n_tokens > 0) {
+    const dim3 g2((unsigned)((app->n_tokens + 7) / 8));
+    compress_state_store_kernel<<<g2, 256, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, app->n_tokens,
+                                                    app->state_raw, app->state_gate);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *n_launch += 1;
+  }
+  return e;
 }
 
 }  // namespace csa2

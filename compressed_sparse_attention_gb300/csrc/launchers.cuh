@@ -42,11 +42,20 @@ struct AttendParams {
 
 cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
                               const RopeParams& rp, int fmt, void* out, uint8_t* out_scale);
+// the append form of the compressor (csa2_compress_append); NULL: whole groups
+struct AppendArgs {
+  int64_t n_tokens = 0;
+  uint16_t* state_raw = nullptr;
+  float* state_gate = nullptr;
+};
+// n_groups: the closing groups (whole-group form) or a bound of them (append
+// form: n_tokens / m + n_seq); n_launch counts the launches made
 cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
                             int n_seq, const int64_t* tok_off, const int64_t* first_pos, const int64_t* pool_off,
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
                             float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
-                            uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags);
+                            uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags,
+                            const AppendArgs* app, int* n_launch);
 // arguments of the index scan (csa2_index_score) and of its tail kernel
 struct IdxArgs {
   int n_query = 0, n_seq = 0;

@@ -188,6 +188,36 @@ csa2_status csa2_compress(csa2_ctx* ctx, void* stream, const uint16_t* raw, cons
                           uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale);
 
 /* ------------------------------------------------------------------------
+ * csa2_compress_append: the compressor with its partial group carried in
+ * state ("Reading Notes of DeepSeek-V4.1-Flash", 3f "the compressor": during
+ * decode an entry is emitted only every compress_ratio steps and the partial
+ * group waits in state; "DeepSeek-V4.1-Flash" (PocketLLM), "The container":
+ * the trailing group waits between calls and a step that closes no group
+ * writes nothing). Tokens arrive in any number per call and sequence:
+ *   raw, gate  [n_tokens, 512] new tokens (bf16) and gate logits (fp32; NULL
+ *              at m = 1), sequences packed by tok_off [n_seq+1] (any counts)
+ *   first_pos  [n_seq] int64 position of sequence b's first new token (any
+ *              position >= 0); its tokens have positions first_pos[b] ..
+ *              first_pos[b] + n_b - 1
+ *   state_raw  [n_seq, m, 512] bf16 and state_gate [n_seq, m, 512] fp32,
+ *              caller-owned: the token at position p of a group still open
+ *              lives in slot p mod m of its sequence. The tokens of b's open
+ *              group (positions floor(first_pos[b]/m) m .. first_pos[b] - 1)
+ *              must be there from earlier calls; NULL is allowed at m = 1.
+ * Every group that this call completes, j with first_pos[b] < (j+1) m <=
+ * first_pos[b] + n_b, is compressed exactly as csa2_compress does (same
+ * arithmetic, so the same bits whatever the chunking) into pool row
+ * pool_off[b] + j and its index key; then the new tokens of b's group still
+ * open are written to the state. Two launches (the compress, then the state
+ * store) on `stream`. Other arguments as for csa2_compress. */
+csa2_status csa2_compress_append(csa2_ctx* ctx, void* stream, const uint16_t* raw, const float* gate,
+                                 int32_t n_seq, int64_t n_tokens, const int64_t* tok_off,
+                                 const int64_t* first_pos, const int64_t* pool_off, const float* norm_w,
+                                 const uint16_t* w_idx, const float* k_norm_w, void* pool_kv,
+                                 uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale,
+                                 uint16_t* state_raw, float* state_gate);
+
+/* ------------------------------------------------------------------------
  * csa2_index_score: step 2 ("Reading Notes ...", 3f C2 step 2, the lightning
  * indexer form). scores[q, j] = sum_h w_heads[q,h] * max(0, q_idx[q,h,:] .
  * key_j) for j < n_vis[q], key_j = row pool_off[seq_of_q[q]] + j of idx_keys.
@@ -306,6 +336,13 @@ typedef struct csa2_step_args {
   float* lse;
   void* workspace;
   size_t workspace_bytes;
+  /* compressor state (Full only): append != 0 makes the step's compress
+   * follow csa2_compress_append, raw/gate/tok_off/first_pos being this
+   * step's new tokens and the open groups waiting in state_raw/state_gate;
+   * append == 0 keeps csa2_compress (whole groups only) */
+  int32_t append;
+  uint16_t* state_raw;
+  float* state_gate;
 } csa2_step_args;
 
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);

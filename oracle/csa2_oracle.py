@@ -189,6 +189,48 @@ def compress(raw: np.ndarray, gate, m: int, first_pos: int, norm_w: np.ndarray,
     return kv, c_hat, k_idx
 
 
+class CompressorState:
+    """The compressor with its open group carried between calls.
+
+    During decode an entry is emitted only once every m = compress_ratio
+    tokens, and the partial group waits in state (R, section 3f, C2 "the
+    compressor"; P, "The container": a step at a non-flush position writes
+    nothing). Tokens of one sequence are fed in order, in chunks of any size;
+    every group a chunk completes is compressed by `compress` above on its m
+    tokens, so the result cannot depend on the chunking.
+    """
+
+    def __init__(self, m: int, norm_w, eps: float, inv_freq, w_idx=None, k_norm_w=None):
+        self.m, self.norm_w, self.eps, self.inv_freq = m, norm_w, eps, inv_freq
+        self.w_idx, self.k_norm_w = w_idx, k_norm_w
+        self.next_pos = 0
+        self.raw, self.gate = [], []
+
+    def pending(self) -> int:
+        return len(self.raw)
+
+    def feed(self, raw, gate, first_pos: int):
+        """raw / gate [n, D]: the tokens at positions first_pos .. first_pos+n-1.
+        Returns [(j, kv_rotated, c_hat, k_idx)] for each group completed."""
+        if first_pos != self.next_pos:
+            raise ValueError("tokens must be fed in order")
+        raw = np.asarray(raw, dtype=np.float64)
+        gate = None if gate is None else np.asarray(gate, dtype=np.float64)
+        out = []
+        for i in range(raw.shape[0]):
+            self.raw.append(raw[i])
+            self.gate.append(None if gate is None else gate[i])
+            if len(self.raw) == self.m:
+                p0 = first_pos + i + 1 - self.m
+                g = None if self.m == 1 else np.stack(self.gate)
+                kv, c_hat, k_idx = compress(np.stack(self.raw), g, self.m, p0, self.norm_w, self.eps,
+                                            self.inv_freq, self.w_idx, self.k_norm_w)
+                out.append((p0 // self.m, kv[0], c_hat[0], None if k_idx is None else k_idx[0]))
+                self.raw, self.gate = [], []
+        self.next_pos = first_pos + raw.shape[0]
+        return out
+
+
 # ----------------------------------------------------------------------------
 # Global KV bytes per token (R, section 3c, the B_glob formula; C2 "Resulting
 # memory")

@@ -235,6 +235,51 @@ def test_compress_rope_at_first_token_and_unrotated_index_key():
     assert np.allclose(np.sqrt(np.mean((k0 / kn) ** 2, axis=1)), 1.0)
 
 
+@pytest.mark.parametrize("m", [1, 2, 4])
+def test_compressor_state_chunking_independent(m):
+    """Fed token by token, in random chunks, or at once, the stateful
+    compressor emits the same entries (exactly) as one compress of every
+    complete group, and keeps the open tail pending."""
+    rng = np.random.default_rng(60 + m)
+    T, D = 61, 32
+    raw, gate = rng.standard_normal((T, D)), rng.standard_normal((T, D))
+    w = 0.5 + rng.random(D)
+    f = O.yarn_inv_freq(8, 160000.0, 16.0, 65536.0, 32.0, 1.0)
+    wi, kn = rng.standard_normal((16, D)), 0.5 + rng.random(16)
+    n_full = (T // m) * m
+    kv_ref, ch_ref, k_ref = O.compress(raw[:n_full], gate[:n_full], m, 0, w, 1e-20, f, wi, kn)
+
+    def run(chunks):
+        st = O.CompressorState(m, w, 1e-20, f, wi, kn)
+        got, p = [], 0
+        for c in chunks:
+            got += st.feed(raw[p:p + c], gate[p:p + c], p)
+            p += c
+        return st, got
+
+    cuts = rng.integers(0, 7, size=40)
+    cuts = cuts[np.cumsum(cuts) <= T]
+    for chunks in ([T], [1] * T, list(cuts) + [T - int(cuts.sum())]):
+        st, got = run(chunks)
+        assert [g[0] for g in got] == list(range(T // m))
+        assert np.array_equal(np.stack([g[1] for g in got]), kv_ref)
+        assert np.array_equal(np.stack([g[2] for g in got]), ch_ref)
+        # the key's matrix product goes through BLAS, whose summation order
+        # depends on how many rows it multiplies at once: float64 rounding only
+        assert np.allclose(np.stack([g[3] for g in got]), k_ref, rtol=1e-13, atol=1e-13)
+        assert st.pending() == T - n_full
+
+
+def test_compressor_state_emits_only_when_a_group_closes():
+    rng = np.random.default_rng(66)
+    raw, gate = rng.standard_normal((9, 16)), rng.standard_normal((9, 16))
+    st = O.CompressorState(4, np.ones(16), 1e-20, NO_ROPE)
+    emitted = [len(st.feed(raw[i:i + 1], gate[i:i + 1], i)) for i in range(9)]
+    assert emitted == [0, 0, 0, 1, 0, 0, 0, 1, 0]  # a step at a non-flush position writes nothing
+    with pytest.raises(ValueError):
+        st.feed(raw[:1], gate[:1], 3)  # out of order
+
+
 # ---------------------------------------------------------------- indexer and top-k
 
 def test_index_scores_closed_forms():
