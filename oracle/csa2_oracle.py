@@ -189,6 +189,49 @@ def compress(raw: np.ndarray, gate, m: int, first_pos: int, norm_w: np.ndarray,
     return kv, c_hat, k_idx
 
 
+# ----------------------------------------------------------------------------
+# Hierarchical sparse indexer (R, section 3f, C3; P, "The container",
+# select_candidate_blocks)
+# ----------------------------------------------------------------------------
+
+def candidate_blocks(scores: np.ndarray, block: int = 8, n_keep: int = 2048) -> np.ndarray:
+    """First level: the candidate source's pool of blocks.
+
+    The n = len(scores) visible entries fall into blocks of `block`
+    consecutive entries; a block scores the largest index score among its
+    entries (R, C3: score(beta) = max over j in beta of sigma(j)). The block
+    holding the newest entry n-1 is still filling and is kept whatever its
+    score (P, "The container": pinned rather than ranked). The n_keep best
+    blocks, by score and then by the lower block index, form the pool.
+    Returns their block indices in ascending order."""
+    s = np.asarray(scores, dtype=np.float64)
+    n = s.shape[0]
+    if n == 0:
+        return np.zeros(0, dtype=np.int64)
+    nb = -(-n // block)
+    bs = np.array([s[b * block:min((b + 1) * block, n)].max() for b in range(nb)])
+    bs[nb - 1] = np.inf
+    order = np.lexsort((np.arange(nb), -bs))
+    return np.sort(order[:n_keep]).astype(np.int64)
+
+
+def pool_entries(cand: np.ndarray, n_vis: int, block: int = 8) -> np.ndarray:
+    """The entries of the pool (R, C3: P_t, the union of the kept blocks),
+    those below n_vis, ascending."""
+    j = (np.asarray(cand, dtype=np.int64)[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+    return j[j < n_vis]
+
+
+def pool_topk(scores: np.ndarray, cand: np.ndarray, k: int, block: int = 8) -> np.ndarray:
+    """Second level: a Reindex layer's own top-k inside the pool (R, C3:
+    S = TopK over j in P of sigma^(l)(j)); same order and tie rule as
+    topk_select, entry indices ascending, -1 padded."""
+    s = np.asarray(scores, dtype=np.float64)
+    P = pool_entries(cand, s.shape[0], block)
+    sel = topk_select(s[P], k)
+    return np.where(sel >= 0, P[np.maximum(sel, 0)], -1).astype(np.int64)
+
+
 class CompressorState:
     """The compressor with its open group carried between calls.
 

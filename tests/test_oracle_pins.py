@@ -282,6 +282,61 @@ def test_compressor_state_emits_only_when_a_group_closes():
 
 # ---------------------------------------------------------------- indexer and top-k
 
+def test_candidate_pool_is_everything_when_few_blocks():
+    """With no more blocks than n_keep the pool is every visible entry and the
+    pool top-k is the plain top-k (R, C3 reduces to C2 step 3)."""
+    rng = np.random.default_rng(80)
+    s = rng.standard_normal(1000)
+    cand = O.candidate_blocks(s, 8, 2048)
+    assert np.array_equal(cand, np.arange(125))
+    assert np.array_equal(O.pool_entries(cand, 1000), np.arange(1000))
+    assert np.array_equal(O.pool_topk(s, cand, 100), O.topk_select(s, 100))
+
+
+def test_candidate_blocks_brute_force_and_ties():
+    rng = np.random.default_rng(81)
+    for n in (37, 64, 203):
+        s = np.round(rng.standard_normal(n), 1)  # many equal block maxima
+        for keep in (1, 3, 6):
+            nb = -(-n // 8)
+            best = [max(s[8 * b:8 * b + 8]) for b in range(nb)]
+            rank = sorted(range(nb), key=lambda b: (b != nb - 1, -best[b], b))  # newest block first, then by score
+            assert list(O.candidate_blocks(s, 8, keep)) == sorted(rank[:keep])
+
+
+def test_candidate_pool_pins_the_block_still_filling():
+    """An older full block that outscores the newest, half-filled block does
+    not push it out of the pool (P, "The container")."""
+    s = np.concatenate([np.full(8, 5.0), np.full(8, 4.0), np.full(3, -1.0)])
+    assert list(O.candidate_blocks(s, 8, 1)) == [2]
+    assert list(O.candidate_blocks(s, 8, 2)) == [0, 2]
+    assert list(O.pool_entries(O.candidate_blocks(s, 8, 2), 19)) == list(range(8)) + [16, 17, 18]
+
+
+def test_pool_topk_selects_inside_the_pool():
+    rng = np.random.default_rng(82)
+    s = rng.standard_normal(4096)
+    cand = O.candidate_blocks(s, 8, 64)
+    P = O.pool_entries(cand, 4096)
+    assert P.shape[0] <= 64 * 8 and np.all(np.diff(P) > 0)
+    sel = O.pool_topk(s, cand, 40)
+    assert set(sel) <= set(P)
+    # the k largest pool scores, ties to the lower entry
+    order = sorted(P, key=lambda j: (-s[j], j))[:40]
+    assert list(sel) == sorted(order)
+
+
+def test_hierarchical_pool_size_arithmetic():
+    """R, C3: 2,048 blocks of 8 bound the pool at 16,384 entries; at N = 10^6
+    decoder scoring per query falls from 5 x 10^6 to 10^6 + 4 x 16,384, about
+    1.07 x 10^6 (4.7x), and each Reindex layer scores 61x fewer entries."""
+    s = np.random.default_rng(83).standard_normal(200000)
+    assert O.pool_entries(O.candidate_blocks(s, 8, 2048), s.shape[0]).shape[0] == 2048 * 8 == 16384
+    per_query = 10 ** 6 + 4 * 16384
+    assert round(per_query / 1e6, 2) == 1.07 and round(5e6 / per_query, 1) == 4.7
+    assert int(10 ** 6 / 16384) == 61
+
+
 def test_index_scores_closed_forms():
     rng = np.random.default_rng(9)
     qi, keys = rng.standard_normal((8, 16)), rng.standard_normal((50, 16))
