@@ -242,6 +242,21 @@ class Copy:
                  tok_off=i["tok_off"], first_pos=i["first_pos"], norm_w=i["norm_w"], w_idx=i["w_idx"],
                  k_norm_w=i["k_norm_w"])
 
+    def step_as(self, ctx, mode, cand_role=0, cand=None):
+        """A Full or Reindex step of this copy, optionally as the hierarchical
+        indexer's candidate source (cand_role 1) or pool reader (2)."""
+        i = self.inp
+        full = mode == 0
+        ctx.step(mode, self.wl.n_seq, self.max_vis, q=i["q"], q_pos=i["q_pos"], seq_of_q=i["seq_of_q"],
+                 n_vis=i["n_vis"], sink=i["sink"], win_kv=i["win_kv"], win_scale=i.get("win_scale"),
+                 win_off=i["win_off"], pool_kv=i["pool_kv"], pool_scale=i.get("pool_scale"), pool_off=i["pool_off"],
+                 topk_idx=self.idx, out=self.out, workspace=self.ws, q_idx=i["q_idx"], w_heads=i["w_heads"],
+                 idx_keys=i["idx_keys"], idx_key_scale=i.get("idx_key_scale"), raw=i["raw"] if full else None,
+                 gate=i["gate"] if full else None, tok_off=i["tok_off"] if full else None,
+                 first_pos=i["first_pos"] if full else None, norm_w=i["norm_w"] if full else None,
+                 w_idx=i["w_idx"] if full else None, k_norm_w=i["k_norm_w"] if full else None, cand_role=cand_role,
+                 cand=cand)
+
     def attend_only(self, ctx, ws):
         """Attention alone on this copy's last selection (decode or prefill)."""
         i = self.inp
@@ -377,6 +392,46 @@ def run_prefill_extra(args, device, bf16_peak):
             "ms_per_step": ms_step, "attend_ms": ms_att, "attend_flops": flops,
             "roofline_attend": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                                 "frac": tf / bf16_peak, "peak_kind": "bf16 dense, burst (kernel timed alone)"}}
+
+
+def run_hier_extra(args, device):
+    """The hierarchical sparse indexer at 1M (fp8): a Reindex step scoring the
+    whole pool against one scoring only the candidate pool of 2,048 blocks of
+    8 that a Full candidate-source step left (and that source step itself)."""
+    from compressed_sparse_attention_gb300 import binding
+    wl = PRESETS["decode_1m_b8_fp8"]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=wl.kv_format,
+                          idx_key_format=wl.idx_key_format)
+    copies = [Copy(ctx, wl, c, device) for c in range(2)]  # 280 MB of keys and rows each, > L2
+    cands = [torch.full((wl.n_query, int(ctx.cfg.cand_keep)), -1, dtype=torch.int32, device=device) for _ in copies]
+    stream = torch.cuda.Stream(device=device)
+    steps = max(5, min(args.steps, 100))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                fn(i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_source = timed(lambda i: copies[i % 2].step_as(ctx, 0, 1, cands[i % 2]))
+    ms_full = timed(lambda i: copies[i % 2].step_as(ctx, 0))
+    ms_reindex = timed(lambda i: copies[i % 2].step_as(ctx, 1))
+    ms_pool = timed(lambda i: copies[i % 2].step_as(ctx, 1, 2, cands[i % 2]))
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the hierarchical workload")
+    pool = int(ctx.cfg.cand_keep) * int(ctx.cfg.cand_block)
+    return {"workload": wl.name, "pool_entries": pool, "entries_per_query": int(copies[0].max_vis),
+            "ms_full_step": ms_full, "ms_full_step_as_candidate_source": ms_source,
+            "ms_reindex_step": ms_reindex, "ms_reindex_step_in_pool": ms_pool,
+            "reindex_speedup": ms_reindex / ms_pool}
 
 
 def run_e2e(args, ctx, copies, stream, device, wl):
@@ -585,6 +640,10 @@ def main():
                              "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
             except Exception as ex:  # reported, never silently dropped
                 line[key] = {"error": repr(ex)[:300]}
+        try:
+            line["extra_hier"] = run_hier_extra(args, device)
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_hier"] = {"error": repr(ex)[:300]}
         try:
             line["extra_prefill"] = run_prefill_extra(args, device, bf16_burst)
         except Exception as ex:  # reported, never silently dropped

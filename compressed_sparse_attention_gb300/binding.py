@@ -21,7 +21,8 @@ _LIB = None
 CSA2_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported geometry", 3: "CUDA error",
           4: "bad input recorded on the device", 5: "device wait timed out", 6: "workspace too small"}
-KV_BF16, KV_FP8, KV_FP4, KV_MXFP4 = 0, 1, 2, 3  # csa2_kv_format
+KV_BF16, KV_FP8, KV_FP4, KV_MXFP4 = 0, 1, 2, 3
+CAND_NONE, CAND_SOURCE, CAND_READ = 0, 1, 2  # csa2_kv_format
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 
 FLAG_BAD_TOPK_INDEX = 0x01
@@ -44,7 +45,8 @@ class Config(C.Structure):
                 ("idx_dim", C.c_int32), ("topk", C.c_int32), ("kv_format", C.c_int32),
                 ("idx_key_format", C.c_int32), ("softmax_scale", C.c_float), ("norm_eps", C.c_float),
                 ("rope_theta", C.c_double), ("yarn_factor", C.c_double), ("yarn_orig_len", C.c_double),
-                ("yarn_beta_fast", C.c_double), ("yarn_beta_slow", C.c_double)]
+                ("yarn_beta_fast", C.c_double), ("yarn_beta_slow", C.c_double),
+                ("cand_block", C.c_int32), ("cand_keep", C.c_int32)]
 
 
 class StepArgs(C.Structure):
@@ -60,7 +62,8 @@ class StepArgs(C.Structure):
                 ("k_norm_w", C.c_void_p),
                 ("topk_idx", C.c_void_p), ("out", C.c_void_p), ("lse", C.c_void_p),
                 ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
-                ("append", C.c_int32), ("state_raw", C.c_void_p), ("state_gate", C.c_void_p)]
+                ("append", C.c_int32), ("state_raw", C.c_void_p), ("state_gate", C.c_void_p),
+                ("cand_role", C.c_int32), ("cand", C.c_void_p)]
 
 
 # name -> (restype, argtypes); every symbol include/csa2.h declares
@@ -84,6 +87,14 @@ SIGNATURES = {
                                    C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                    C.c_void_p, C.c_int64]),
     "csa2_topk_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int64]),
+    "csa2_candidate_pool_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int64]),
+    "csa2_candidate_pool": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p,
+                                      C.c_int64, C.c_void_p, C.c_void_p, C.c_size_t]),
+    "csa2_index_score_pool": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
+                                        C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_topk_pool": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
+                                 C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t]),
     "csa2_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_int64,
                             C.c_int32, C.c_void_p, C.c_void_p, C.c_size_t]),
     "csa2_attend_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32]),
@@ -239,6 +250,34 @@ class Context:
             self._p(seq_of_q, torch.int32, "seq_of_q"), self._p(n_vis, torch.int32, "n_vis"), max_vis,
             self._p(scores, torch.float32, "scores"), scores.shape[1]), "csa2_index_score")
 
+    # -- the hierarchical indexer's pool
+    def candidate_pool_workspace_size(self, n_query, max_vis) -> int:
+        return int(self.lib.csa2_candidate_pool_workspace_size(self.h, n_query, max_vis))
+
+    def candidate_pool(self, scores, n_vis, max_vis, cand, workspace):
+        self._ok(self.lib.csa2_candidate_pool(
+            self.h, C.c_void_p(_stream()), n_vis.shape[0], self._p(scores, torch.float32, "scores"), scores.shape[1],
+            self._p(n_vis, torch.int32, "n_vis"), max_vis, self._p(cand, torch.int32, "cand"),
+            self._p(workspace, None, "workspace"),
+            0 if workspace is None else workspace.numel() * workspace.element_size()), "csa2_candidate_pool")
+
+    def index_score_pool(self, n_seq, q_idx, w_heads, idx_keys, idx_key_scale, pool_off, seq_of_q, n_vis, max_vis,
+                         cand, scores_pool, n_pool):
+        self._ok(self.lib.csa2_index_score_pool(
+            self.h, C.c_void_p(_stream()), n_seq, q_idx.shape[0], self._p(q_idx, torch.bfloat16, "q_idx"),
+            self._p(w_heads, torch.float32, "w_heads"), self._p(idx_keys, None, "idx_keys"),
+            self._p(idx_key_scale, torch.uint8, "idx_key_scale"), self._p(pool_off, torch.int64, "pool_off"),
+            self._p(seq_of_q, torch.int32, "seq_of_q"), self._p(n_vis, torch.int32, "n_vis"), max_vis,
+            self._p(cand, torch.int32, "cand"), self._p(scores_pool, torch.float32, "scores_pool"),
+            self._p(n_pool, torch.int32, "n_pool")), "csa2_index_score_pool")
+
+    def topk_pool(self, scores_pool, n_pool, cand, k, out_idx, workspace):
+        self._ok(self.lib.csa2_topk_pool(
+            self.h, C.c_void_p(_stream()), n_pool.shape[0], self._p(scores_pool, torch.float32, "scores_pool"),
+            self._p(n_pool, torch.int32, "n_pool"), self._p(cand, torch.int32, "cand"), k,
+            self._p(out_idx, torch.int32, "out_idx"), self._p(workspace, None, "workspace"),
+            0 if workspace is None else workspace.numel() * workspace.element_size()), "csa2_topk_pool")
+
     def topk_workspace_size(self, n_query, max_vis) -> int:
         return int(self.lib.csa2_topk_workspace_size(self.h, n_query, max_vis))
 
@@ -271,7 +310,8 @@ class Context:
     def step(self, mode, n_seq, max_vis, *, q, q_pos, seq_of_q, n_vis, sink, win_kv, win_off, pool_kv, pool_off,
              topk_idx, out, workspace, q_idx=None, w_heads=None, win_scale=None, win_lo=None, pool_scale=None,
              idx_keys=None, idx_key_scale=None, raw=None, gate=None, tok_off=None, first_pos=None, norm_w=None,
-             w_idx=None, k_norm_w=None, lse=None, append=False, state_raw=None, state_gate=None):
+             w_idx=None, k_norm_w=None, lse=None, append=False, state_raw=None, state_gate=None, cand_role=0,
+             cand=None):
         a = StepArgs()
         a.mode, a.n_seq, a.n_query, a.max_vis = mode, n_seq, q.shape[0], max_vis
         a.q = self._p(q, torch.bfloat16, "q")
@@ -306,6 +346,8 @@ class Context:
         a.append = 1 if append else 0
         a.state_raw = self._p(state_raw, torch.bfloat16, "state_raw")
         a.state_gate = self._p(state_gate, torch.float32, "state_gate")
+        a.cand_role = cand_role
+        a.cand = self._p(cand, torch.int32, "cand")
         self._ok(self.lib.csa2_step(self.h, C.c_void_p(_stream()), C.byref(a)), "csa2_step")
 
 

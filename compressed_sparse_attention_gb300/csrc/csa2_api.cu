@@ -1,5 +1,6 @@
 // Host side of the CSA2 C ABI: context, argument validation, workspace
 // carving, kernel launches and the Full / Reindex / Reuse step dispatch.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -78,6 +79,15 @@ void csa2_default_config(csa2_config* c) {
   c->yarn_orig_len = 65536.0;
   c->yarn_beta_fast = 32.0;
   c->yarn_beta_slow = 1.0;
+  c->cand_block = 8;
+  c->cand_keep = 2048;
+}
+
+// log2 of the candidate block size (a power of two)
+static int cand_shift(const csa2_config& c) {
+  int sh = 0;
+  while ((1 << sh) < c.cand_block) ++sh;
+  return sh;
 }
 
 const char* csa2_status_string(csa2_status s) {
@@ -97,7 +107,7 @@ static void release(csa2_ctx* ctx) {
   if (ctx->d_flags) cudaFree(ctx->d_flags);
   if (ctx->d_work) cudaFree(ctx->d_work);
   if (ctx->side) cudaStreamDestroy(ctx->side);
-  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join})
+  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join, ctx->ev_topk})
     if (ev) cudaEventDestroy(ev);
   delete ctx;
 }
@@ -112,6 +122,10 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (c.compress_ratio < 1 || c.compress_ratio > 16) return CSA2_ERR_UNSUPPORTED;
   if (!(c.idx_heads == 8 || c.idx_heads == 16 || c.idx_heads == 32)) return CSA2_ERR_UNSUPPORTED;
   if (c.topk < 1 || c.topk > 2048) return CSA2_ERR_UNSUPPORTED;
+  // pools must fit one top-k row of 16,384 entries
+  if (c.cand_block < 1 || c.cand_block > 64 || (c.cand_block & (c.cand_block - 1)) != 0 || c.cand_keep < 1 ||
+      c.cand_keep > 2048 || (int64_t)c.cand_keep * c.cand_block > 16384)
+    return CSA2_ERR_UNSUPPORTED;
   if ((c.kv_format != CSA2_KV_BF16 && c.kv_format != CSA2_KV_FP8_E4M3_B32 && c.kv_format != CSA2_KV_FP4_E4M3_B16) ||
       (c.idx_key_format != CSA2_KV_BF16 && c.idx_key_format != CSA2_KV_FP8_E4M3_B32 &&
        c.idx_key_format != CSA2_KV_MXFP4_B32))
@@ -132,6 +146,7 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_idx, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_tail, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_topk, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
     release(ctx);
@@ -259,9 +274,12 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
                             const float* w_heads, const void* idx_keys, const uint8_t* idx_key_scale,
                             const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
                             float* scores, int64_t ld, const int64_t* new_first = nullptr,
-                            const int64_t* new_tok = nullptr, bool tail_only = false) {
+                            const int64_t* new_tok = nullptr, bool tail_only = false,
+                            const int32_t* cand = nullptr, int32_t* n_pool = nullptr) {
   const csa2_config& c = ctx->cfg;
-  if (n_query < 0 || n_seq < 1 || max_vis < 0 || ld < max_vis)
+  // a pool row holds at most cand_keep blocks of entries
+  const int64_t row_need = cand != nullptr ? std::min(max_vis, (int64_t)c.cand_keep * c.cand_block) : max_vis;
+  if (n_query < 0 || n_seq < 1 || max_vis < 0 || ld < row_need)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score: sizes");
   if (n_query == 0 || max_vis == 0) return CSA2_OK;
   if (!q_idx || !w_heads || !idx_keys || !pool_off || !seq_of_q || !n_vis || !scores)
@@ -289,10 +307,15 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
   ia.new_tok = new_tok;
   ia.m = c.compress_ratio;
   ia.work = ctx->d_work;
+  ia.cand = cand;
+  ia.cand_ld = c.cand_keep;
+  ia.cand_shift = cand_shift(c);
+  ia.n_pool = n_pool;
   cudaError_t e;
   if (tail_only) {
     e = csa2::launch_index_tail(st, c.idx_heads, kf, ia);
-  } else if (new_first == nullptr && csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)) {
+  } else if (new_first == nullptr && cand == nullptr &&
+             csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)) {
     e = csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
                                     reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis, scores,
                                     ld, ctx->d_flags);
@@ -321,7 +344,7 @@ size_t csa2_topk_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
 
 static csa2_status do_topk(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, const float* scores, int64_t ld,
                            const int32_t* n_vis, int64_t max_vis, int32_t k, int32_t* out_idx, void* ws,
-                           size_t ws_bytes) {
+                           size_t ws_bytes, const int32_t* map = nullptr) {
   if (n_query < 0 || max_vis < 0 || ld < max_vis || k < 1 || k > 2048)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "topk: sizes (k must be 1..2048)");
   if (max_vis > 0xFFFFFFFEll) return fail(ctx, CSA2_ERR_UNSUPPORTED, "topk: rows longer than 2^32-2");
@@ -330,7 +353,10 @@ static csa2_status do_topk(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, cons
   csa2_status s = check_ws(ctx, ws, ws_bytes, csa2::topk_workspace_bytes(n_query, max_vis));
   if (s != CSA2_OK) return s;
   int nl = 0;
-  cudaError_t e = csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl);
+  cudaError_t e = map == nullptr
+                      ? csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl)
+                      : csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl, map,
+                                          ctx->cfg.cand_keep, cand_shift(ctx->cfg));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "topk");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -343,6 +369,62 @@ csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float*
   ctx->last_launches = 0;
   return do_topk(ctx, reinterpret_cast<cudaStream_t>(stream), n_query, scores, scores_ld, n_vis, max_vis, k, out_idx,
                  workspace, workspace_bytes);
+}
+
+size_t csa2_candidate_pool_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis) {
+  if (!ctx || n_query < 0 || max_vis < 0) return 0;
+  return csa2::candidate_pool_workspace_bytes(n_query, max_vis, cand_shift(ctx->cfg));
+}
+
+static csa2_status do_candidate_pool(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, const float* scores,
+                                     int64_t ld, const int32_t* n_vis, int64_t max_vis, int32_t* cand, void* ws,
+                                     size_t ws_bytes) {
+  if (n_query < 0 || max_vis < 0 || ld < max_vis) return fail(ctx, CSA2_ERR_INVALID_ARG, "candidate_pool: sizes");
+  if (max_vis > 0xFFFFFFFEll) return fail(ctx, CSA2_ERR_UNSUPPORTED, "candidate_pool: rows longer than 2^32-2");
+  if (n_query == 0) return CSA2_OK;
+  if (!n_vis || !cand || (max_vis > 0 && !scores)) return fail(ctx, CSA2_ERR_INVALID_ARG, "candidate_pool: null");
+  csa2_status s = check_ws(ctx, ws, ws_bytes, csa2_candidate_pool_workspace_size(ctx, n_query, max_vis));
+  if (s != CSA2_OK) return s;
+  int nl = 0;
+  cudaError_t e = csa2::launch_candidate_pool(st, n_query, scores, ld, n_vis, max_vis, cand_shift(ctx->cfg),
+                                              ctx->cfg.cand_keep, cand, ws, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "candidate_pool");
+  ctx->last_launches += nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_candidate_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores,
+                                int64_t scores_ld, const int32_t* n_vis, int64_t max_vis, int32_t* cand,
+                                void* workspace, size_t workspace_bytes) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  return do_candidate_pool(ctx, reinterpret_cast<cudaStream_t>(stream), n_query, scores, scores_ld, n_vis, max_vis,
+                           cand, workspace, workspace_bytes);
+}
+
+csa2_status csa2_index_score_pool(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
+                                  const uint16_t* q_idx, const float* w_heads, const void* idx_keys,
+                                  const uint8_t* idx_key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
+                                  const int32_t* n_vis, int64_t max_vis, const int32_t* cand, float* scores_pool,
+                                  int32_t* n_pool) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (!cand || !n_pool) return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score_pool: null pool");
+  const int64_t ld = (int64_t)ctx->cfg.cand_keep * ctx->cfg.cand_block;
+  return do_index(ctx, reinterpret_cast<cudaStream_t>(stream), n_seq, n_query, q_idx, w_heads, idx_keys,
+                  idx_key_scale, pool_off, seq_of_q, n_vis, max_vis, scores_pool, ld, nullptr, nullptr, false, cand,
+                  n_pool);
+}
+
+csa2_status csa2_topk_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores_pool,
+                           const int32_t* n_pool, const int32_t* cand, int32_t k, int32_t* out_idx, void* workspace,
+                           size_t workspace_bytes) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (!cand) return fail(ctx, CSA2_ERR_INVALID_ARG, "topk_pool: null pool");
+  const int64_t ld = (int64_t)ctx->cfg.cand_keep * ctx->cfg.cand_block;
+  return do_topk(ctx, reinterpret_cast<cudaStream_t>(stream), n_query, scores_pool, ld, n_pool, ld, k, out_idx,
+                 workspace, workspace_bytes, cand);
 }
 
 size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query) {
@@ -411,12 +493,29 @@ csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_qu
                    workspace_bytes);
 }
 
+// The step's workspace: index scores (full rows of max_vis, or pool rows of
+// cand_keep * cand_block for a pool reader), the pool sizes, the top-k
+// scratch, the candidate-pool scratch (a candidate source builds its pool
+// beside the attention) and the attention partials, side by side.
+struct StepWs {
+  size_t scores, n_pool, tk, cand, at;
+};
+static StepWs step_ws(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis) {
+  const int64_t ld = max_vis > 0 ? max_vis : 1;
+  const int64_t ldc = (int64_t)ctx->cfg.cand_keep * ctx->cfg.cand_block;
+  StepWs w;
+  w.scores = al((size_t)n_query * (size_t)std::max(ld, ldc) * 4);
+  w.n_pool = al((size_t)n_query * 4);
+  w.tk = al(csa2_topk_workspace_size(ctx, n_query, max_vis));
+  w.cand = al(csa2_candidate_pool_workspace_size(ctx, n_query, max_vis));
+  w.at = al(csa2_attend_workspace_size(ctx, n_query));
+  return w;
+}
+
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis) {
   if (!ctx || n_query < 0 || max_vis < 0) return 0;
-  const size_t scores = al((size_t)n_query * (size_t)(max_vis > 0 ? max_vis : 1) * 4);
-  const size_t tk = al(csa2_topk_workspace_size(ctx, n_query, max_vis));
-  const size_t at = al(csa2_attend_workspace_size(ctx, n_query));
-  return scores + tk + at;
+  const StepWs w = step_ws(ctx, n_query, max_vis);
+  return w.scores + w.n_pool + w.tk + w.cand + w.at;
 }
 
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
@@ -430,12 +529,20 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   const size_t need = csa2_step_workspace_size(ctx, a->n_query, a->max_vis);
   csa2_status s = check_ws(ctx, a->workspace, a->workspace_bytes, need);
   if (s != CSA2_OK) return s;
+  if (a->cand_role < 0 || a->cand_role > 2 || (a->cand_role != 0 && !a->cand) ||
+      (a->cand_role != 0 && a->mode == CSA2_MODE_REUSE))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "step: cand_role needs cand and a Full or Reindex step");
+  const bool pool_src = a->cand_role == 1, pool_read = a->cand_role == 2;
   char* ws = reinterpret_cast<char*>(a->workspace);
   const int64_t ld = a->max_vis > 0 ? a->max_vis : 1;
+  const int64_t ldc = (int64_t)ctx->cfg.cand_keep * ctx->cfg.cand_block;
+  const StepWs wl = step_ws(ctx, a->n_query, a->max_vis);
   float* scores = reinterpret_cast<float*>(ws);
-  char* tk_ws = ws + al((size_t)a->n_query * (size_t)ld * 4);
-  const size_t tk_bytes = al(csa2_topk_workspace_size(ctx, a->n_query, a->max_vis));
-  char* at_ws = tk_ws + tk_bytes;
+  int32_t* n_pool = reinterpret_cast<int32_t*>(ws + wl.scores);
+  char* tk_ws = ws + wl.scores + wl.n_pool;
+  const size_t tk_bytes = wl.tk;
+  char* cand_ws = tk_ws + wl.tk;
+  char* at_ws = cand_ws + wl.cand;
   const size_t at_bytes = a->workspace_bytes - (size_t)(at_ws - ws);
   // the attention arguments are checked before anything is enqueued
   csa2::AttendParams ap;
@@ -466,7 +573,7 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   // The tail kernel then scores the entries compress wrote, and the caller's
   // stream waits for both before top-k.
   const bool full = a->mode == CSA2_MODE_FULL;
-  const bool overlap = full && a->n_query > 0 && a->max_vis > 0 && a->n_tokens <= 2LL * m * a->n_seq &&
+  const bool overlap = full && !pool_read && a->n_query > 0 && a->max_vis > 0 && a->n_tokens <= 2LL * m * a->n_seq &&
                        !csa2::index_tc_suited(ctx->cfg.idx_key_format != CSA2_KV_BF16, a->n_query, a->n_seq,
                                               ctx->cfg.idx_heads);
   const bool tail = overlap && a->w_idx != nullptr;  // compress writes index keys: score the new ones apart
@@ -506,9 +613,13 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     return CSA2_OK;
   }
   ctx->last_launches = 0;
-  s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
-               a->seq_of_q, a->n_vis, a->max_vis, scores, ld, tail ? a->first_pos : nullptr,
-               tail ? a->tok_off : nullptr);
+  if (pool_read)  // the hierarchical indexer's second level: score inside the pool only
+    s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
+                 a->seq_of_q, a->n_vis, a->max_vis, scores, ldc, nullptr, nullptr, false, a->cand, n_pool);
+  else
+    s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
+                 a->seq_of_q, a->n_vis, a->max_vis, scores, ld, tail ? a->first_pos : nullptr,
+                 tail ? a->tok_off : nullptr);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
   cudaError_t e = cudaSuccess;
@@ -531,9 +642,16 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: window tile"));
   }
   ctx->last_launches = 0;
-  s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes);
+  if (pool_read)
+    s = do_topk(ctx, st, a->n_query, scores, ldc, n_pool, ldc, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes, a->cand);
+  else
+    s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
+  if (pool_src) {
+    e = cudaEventRecord(ctx->ev_topk, st);
+    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: record top-k"));
+  }
   if (pl.split_window) {
     e = csa2::launch_attend_main(st, kvf, ap, pl, at_ws, &launches);
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
@@ -546,6 +664,18 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
+  if (pool_src) {
+    // the candidate source's pool, for the layers after it, on the side
+    // stream beside the attention; the caller's stream waits for it last
+    e = cudaStreamWaitEvent(ctx->side, ctx->ev_topk, 0);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step: candidate pool");
+    side_open = true;
+    ctx->last_launches = 0;
+    s = do_candidate_pool(ctx, ctx->side, a->n_query, scores, ld, a->n_vis, a->max_vis, a->cand, cand_ws, wl.cand);
+    launches += ctx->last_launches;
+    s = join(s);
+    if (s != CSA2_OK) return s;
+  }
   ctx->last_launches = launches;
   return CSA2_OK;
 }

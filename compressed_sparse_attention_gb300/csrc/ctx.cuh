@@ -16,6 +16,7 @@ struct csa2_ctx {
   cudaEvent_t ev_idx = nullptr;   // recorded on the caller's stream after the index scan
   cudaEvent_t ev_tail = nullptr;  // recorded on the side stream after compress and the tail scores
   cudaEvent_t ev_join = nullptr;  // recorded on the side stream after its last launch
+  cudaEvent_t ev_topk = nullptr;  // recorded on the caller's stream after a candidate source's top-k
   std::string err;
   int last_launches = 0;
 };

@@ -31,7 +31,22 @@ __device__ __forceinline__ int idx_query_range(const IdxArgs& a, int q, int b, b
   if (nv < 0) nv = 0;
   *n_all = nv;
   if (a.new_first != nullptr && a.new_tok[b + 1] > a.new_tok[b]) nv = (int)min((int64_t)nv, a.new_first[b] / a.m);
+  if (a.cand != nullptr) {
+    // pool form: the kept blocks hold B (kept - 1) full blocks ahead of the
+    // pinned newest block, which holds the entries from B (nb - 1) on
+    const int sh = a.cand_shift;
+    const int nb = (nv + (1 << sh) - 1) >> sh;
+    nv = nb == 0 ? 0 : ((min(nb, a.cand_ld) - 1) << sh) + (nv - ((nb - 1) << sh));
+    if (flag_thread) a.n_pool[q] = nv;
+  }
   return nv;
+}
+
+// key row (relative to the sequence's pool) of row position p of query q
+__device__ __forceinline__ int64_t idx_row(const IdxArgs& a, int q, int64_t p) {
+  if (a.cand == nullptr) return p;
+  const int sh = a.cand_shift;
+  return ((int64_t)a.cand[(int64_t)q * a.cand_ld + (p >> sh)] << sh) | (p & ((1 << sh) - 1));
 }
 
 // Work items: each CTA first takes three quarters of its even share by
@@ -97,7 +112,10 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
       const int b = a.seq_of_q[q];
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+        if (threadIdx.x == 0 && j0 == 0) {
+          set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+          if (a.n_pool != nullptr) a.n_pool[q] = 0;
+        }
       } else {
         int n_all;
         nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
@@ -123,7 +141,8 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         rg[u] = j0 + 128 * u + 16 * warp + g;
-        const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
+        const int64_t ra = idx_row(a, q, min(rg[u], (int64_t)nv - 1));
+        const int64_t rb = idx_row(a, q, min(rg[u] + 8, (int64_t)nv - 1));
         const uint16_t* pa = kbase + ra * kIdxDim;
         const uint16_t* pb = kbase + rb * kIdxDim;
 #pragma unroll
@@ -274,7 +293,10 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
       const int b = a.seq_of_q[q];
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+        if (threadIdx.x == 0 && j0 == 0) {
+          set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+          if (a.n_pool != nullptr) a.n_pool[q] = 0;
+        }
       } else {
         int n_all;
         nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
@@ -291,7 +313,8 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         rg[u] = j0 + 128 * u + 16 * warp + g;
-        const int64_t ra = min(rg[u], (int64_t)nv - 1), rb = min(rg[u] + 8, (int64_t)nv - 1);
+        const int64_t ra = idx_row(a, q, min(rg[u], (int64_t)nv - 1));
+        const int64_t rb = idx_row(a, q, min(rg[u] + 8, (int64_t)nv - 1));
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
           if constexpr (KF == 3) {  // 8 codes in 4 bytes
@@ -438,7 +461,8 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
   // (fp8 with 8 heads, mxfp4 with 8 or 16 heads)
   const int u_q = ((idx_fmt == 3 && idx_heads <= 16) || (idx_fmt == 1 && idx_heads == 8)) ? 4 : 2;
   const int64_t chunk = idx_fmt == 0 ? kIdxChunk : 128 * u_q;
-  a.n_chunks = (a.max_vis + chunk - 1) / chunk;
+  const int64_t rows_max = a.cand != nullptr ? min(a.max_vis, (int64_t)a.cand_ld << a.cand_shift) : a.max_vis;
+  a.n_chunks = (rows_max + chunk - 1) / chunk;
   const int64_t items = a.n_chunks * a.n_query;
   const dim3 grid((unsigned)(items < cap ? items : cap));
 #define CSA2_IDX(NT, UQ, U8)                                                         \

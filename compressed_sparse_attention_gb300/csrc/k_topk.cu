@@ -830,10 +830,22 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
 // one key value, taken in index order). One 64-bit block scan of
 // (above-threshold, at-threshold) counts then gives every thread the output
 // positions of its entries, which come out in ascending index order.
+// map set: entry e of the row is pool position e, written out as the entry
+// index (map[q, e >> map_shift] << map_shift) | (e & (2^map_shift - 1))
+struct TkMap {
+  const int32_t* blocks = nullptr;
+  int ld = 0;
+  int shift = 0;
+  __device__ __forceinline__ int32_t operator()(int q, int e) const {
+    if (blocks == nullptr) return e;
+    return (blocks[(int64_t)q * ld + (e >> shift)] << shift) | (e & ((1 << shift) - 1));
+  }
+};
+
 template <int TPB, int PER>
 __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
                                                       const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
-                                                      int32_t* __restrict__ out_idx) {
+                                                      int32_t* __restrict__ out_idx, const TkMap map) {
   constexpr int NW = TPB / 32;
   __shared__ uint32_t hist[NW][256];
   __shared__ uint32_t cnt[256];
@@ -845,7 +857,7 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
   const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
   int32_t* out = out_idx + (int64_t)q * k;
   if (n <= k) {
-    for (int i = tid; i < k; i += TPB) out[i] = i < n ? i : -1;
+    for (int i = tid; i < k; i += TPB) out[i] = i < n ? map(q, i) : -1;
     return;
   }
   // ---- keys of this thread's entries, and the row's smallest and largest key
@@ -1009,15 +1021,61 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
         take = true;
         --eq_left;
       }
-      if (take) out[pos++] = e0 + i;
+      if (take) out[pos++] = map(q, e0 + i);
     }
 }
 
 template <int TPB, int PER>
 static cudaError_t launch_topk_row(cudaStream_t st, int n_query, const float* scores, int64_t ld,
-                                   const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx) {
-  topk_row_kernel<TPB, PER><<<n_query, TPB, 0, st>>>(scores, ld, n_vis, max_vis, k, out_idx);
+                                   const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx,
+                                   const TkMap& map) {
+  topk_row_kernel<TPB, PER><<<n_query, TPB, 0, st>>>(scores, ld, n_vis, max_vis, k, out_idx, map);
   return cudaGetLastError();
+}
+
+// The hierarchical indexer's block scores: the largest score among each
+// block's visible entries; the block holding entry n_vis - 1 (still filling)
+// scores +inf so that the block top-k keeps it. nb[q] = the number of blocks.
+__global__ void __launch_bounds__(256) block_max_kernel(const float* __restrict__ scores, int64_t ld,
+                                                        const int32_t* __restrict__ n_vis, int64_t max_vis,
+                                                        int shift, float* __restrict__ bscore, int64_t ld_b,
+                                                        int32_t* __restrict__ nb_out) {
+  const int q = blockIdx.y;
+  const int64_t b = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  const int64_t n = min((int64_t)max(n_vis[q], 0), max_vis);
+  const int64_t nb = (n + (1 << shift) - 1) >> shift;
+  if (blockIdx.x == 0 && threadIdx.x == 0) nb_out[q] = (int32_t)nb;
+  if (b >= nb) return;
+  const float* row = scores + (int64_t)q * ld + (b << shift);
+  const int lim = (int)min((int64_t)1 << shift, n - (b << shift));
+  float mx = row[0];
+  for (int i = 1; i < lim; ++i) mx = fmaxf(mx, row[i]);
+  bscore[(int64_t)q * ld_b + b] = (b == nb - 1) ? INFINITY : mx;
+}
+
+size_t candidate_pool_workspace_bytes(int n_query, int64_t max_vis, int shift) {
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const int64_t ld_b = max((int64_t)1, (max_vis + (1 << shift) - 1) >> shift);
+  return al((size_t)n_query * ld_b * 4) + al((size_t)n_query * 4) + al(topk_workspace_bytes(n_query, ld_b));
+}
+
+cudaError_t launch_candidate_pool(cudaStream_t st, int n_query, const float* scores, int64_t ld,
+                                  const int32_t* n_vis, int64_t max_vis, int shift, int keep, int32_t* cand,
+                                  void* ws, int* n_launch) {
+  if (n_query == 0) return cudaSuccess;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const int64_t ld_b = max((int64_t)1, (max_vis + (1 << shift) - 1) >> shift);
+  char* p = reinterpret_cast<char*>(ws);
+  float* bscore = reinterpret_cast<float*>(p);
+  p += al((size_t)n_query * ld_b * 4);
+  int32_t* nb = reinterpret_cast<int32_t*>(p);
+  p += al((size_t)n_query * 4);
+  const dim3 g((unsigned)((ld_b + 255) / 256), (unsigned)n_query);
+  block_max_kernel<<<g, 256, 0, st>>>(scores, ld, n_vis, max_vis, shift, bscore, ld_b, nb);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *n_launch += 1;
+  return launch_topk(st, n_query, bscore, ld_b, nb, ld_b, keep, cand, p, n_launch);
 }
 
 template <int PER>
@@ -1053,17 +1111,23 @@ static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, 
 }
 
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
-                        int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch) {
+                        int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch, const int32_t* map_blocks,
+                        int map_ld, int map_shift) {
   if (n_query == 0) return cudaSuccess;
+  TkMap map;
+  map.blocks = map_blocks;
+  map.ld = map_ld;
+  map.shift = map_shift;
   // rows of up to 16,384 scores: one CTA per query holding its row in registers
   if (max_vis <= 16384) {
     cudaError_t e;
-    if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
-    else if (max_vis <= 8192) e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
-    else e = launch_topk_row<1024, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx);
+    if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
+    else if (max_vis <= 8192) e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
+    else e = launch_topk_row<1024, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
     if (e == cudaSuccess) *n_launch += 1;
     return e;
   }
+  if (map_blocks != nullptr) return cudaErrorInvalidValue;  // pools hold at most 16,384 entries
   // a cluster of up to 8 CTAs per query, each holding 16,384 scores (a
   // 64K-context decode row is one CTA), or 32,768 for rows up to 262,144
   const int c16 = topk_cluster_size(max_vis, TkLayout<16>::kSlice);

@@ -77,6 +77,13 @@ struct IdxArgs {
   const int64_t* new_tok = nullptr;
   int m = 1;
   unsigned long long* work = nullptr;  // [2] ticket counters, zero between launches
+  // set: the hierarchical indexer's pool form. Row position p of query q is
+  // entry (cand[q * cand_ld + (p >> cand_shift)] << cand_shift) | low bits;
+  // n_pool[q] receives the number of pool entries below n_vis
+  const int32_t* cand = nullptr;
+  int cand_ld = 0;
+  int cand_shift = 0;
+  int32_t* n_pool = nullptr;
 };
 cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a);
 cudaError_t launch_index_tail(cudaStream_t st, int idx_heads, int idx_fmt, const IdxArgs& a);
@@ -87,8 +94,15 @@ cudaError_t launch_index_score_tc(cudaStream_t st, int num_sms, int idx_heads, i
                                   const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis,
                                   float* scores, int64_t ld, uint32_t* flags);
 size_t topk_workspace_bytes(int n_query, int64_t max_vis);
+// map_blocks set (rows of at most 16,384): row entry e is written as the
+// entry index (map_blocks[q * map_ld + (e >> map_shift)] << map_shift) | low bits
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
-                        int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch);
+                        int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch,
+                        const int32_t* map_blocks = nullptr, int map_ld = 0, int map_shift = 0);
+size_t candidate_pool_workspace_bytes(int n_query, int64_t max_vis, int shift);
+cudaError_t launch_candidate_pool(cudaStream_t st, int n_query, const float* scores, int64_t ld,
+                                  const int32_t* n_vis, int64_t max_vis, int shift, int keep, int32_t* cand,
+                                  void* ws, int* n_launch);
 struct AttendPlan {
   int n_tiles;
   int split_window;  // window tile launched on its own

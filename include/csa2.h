@@ -120,13 +120,19 @@ typedef struct csa2_config {
   double yarn_orig_len;
   double yarn_beta_fast;
   double yarn_beta_slow;
+  /* hierarchical indexer ("Reading Notes ...", 3f C3): blocks of cand_block
+   * consecutive entries (a power of two, 1..64; 8), of which the candidate
+   * source keeps cand_keep (1..2048; 2048) as the pool */
+  int32_t cand_block;
+  int32_t cand_keep;
 } csa2_config;
 
 typedef struct csa2_ctx csa2_ctx;
 
 /* Fills `cfg` (host) with the DeepSeek-V4.1-Flash compressed-layer defaults:
  * 64 x 512, rope 64, window 128, ratio 4, 8 x 128 indexer, top-512, bf16,
- * scale 1/sqrt(512), eps 1e-20, theta 160000, YaRN 16 over 65536, beta 32/1. */
+ * scale 1/sqrt(512), eps 1e-20, theta 160000, YaRN 16 over 65536, beta 32/1,
+ * candidate blocks of 8, 2048 kept. */
 void csa2_default_config(csa2_config* cfg);
 
 /* Validates `cfg` (host), computes the RoPE frequencies in double precision
@@ -252,6 +258,44 @@ csa2_status csa2_topk(csa2_ctx* ctx, void* stream, int32_t n_query, const float*
                       int32_t* out_idx, void* workspace, size_t workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * The hierarchical sparse indexer ("Reading Notes ...", 3f C3; PocketLLM
+ * "DeepSeek-V4.1-Flash", "The container", select_candidate_blocks).
+ *
+ * csa2_candidate_pool: the first level, on the candidate source's scores
+ * (csa2_index_score output). The n_vis[q] entries of query q fall into
+ * blocks of B = cand_block consecutive entries; a block scores the largest
+ * score among its entries; the block holding entry n_vis[q]-1 (still
+ * filling) is pinned; the cand_keep best blocks by (score, lower block index)
+ * form the pool, written to cand [n_query, cand_keep] as ascending block
+ * indices, -1 padded. Bit-exact on given fp32 scores.
+ *   scores [n_query, ld] fp32, n_vis [n_query] int32, max_vis (host bound)
+ *   workspace: csa2_candidate_pool_workspace_size bytes */
+size_t csa2_candidate_pool_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
+csa2_status csa2_candidate_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores,
+                                int64_t scores_ld, const int32_t* n_vis, int64_t max_vis, int32_t* cand,
+                                void* workspace, size_t workspace_bytes);
+
+/* csa2_index_score_pool: csa2_index_score over the pool only. Pool entry p
+ * of query q is entry j = B * cand[q, p / B] + p % B; its score goes to
+ * scores_pool[q, p] (row length cand_keep * B). The pool's entries below
+ * n_vis[q] are p < n_pool[q] = B (kept blocks - 1) + (n_vis - B (n_blocks - 1)),
+ * written to n_pool [n_query] int32 (out); other entries are not written.
+ * Keys, formats and the other arguments as for csa2_index_score. */
+csa2_status csa2_index_score_pool(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
+                                  const uint16_t* q_idx, const float* w_heads, const void* idx_keys,
+                                  const uint8_t* idx_key_scale, const int64_t* pool_off, const int32_t* seq_of_q,
+                                  const int32_t* n_vis, int64_t max_vis, const int32_t* cand, float* scores_pool,
+                                  int32_t* n_pool);
+
+/* csa2_topk_pool: the second level: a layer's own top-k inside the pool, from
+ * csa2_index_score_pool's scores, written as entry indices (ascending, ties
+ * to the lower entry, -1 padded), bit-exact on given scores.
+ *   workspace: csa2_topk_workspace_size(ctx, n_query, cand_keep * B) bytes */
+csa2_status csa2_topk_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores_pool,
+                           const int32_t* n_pool, const int32_t* cand, int32_t k, int32_t* out_idx,
+                           void* workspace, size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------
  * csa2_attend: step 3 ("Reading Notes ...", section 3a attention formula and
  * 3f C2 step 3; WASTE item 1: the sink in the denominator only and the
  * de-rotation of the output's rope channels). For query q at t = q_pos[q] of
@@ -343,6 +387,13 @@ typedef struct csa2_step_args {
   int32_t append;
   uint16_t* state_raw;
   float* state_gate;
+  /* hierarchical indexer: cand_role 1 = this Full / Reindex step is the
+   * candidate source and writes the pool of its queries to cand [n_query,
+   * cand_keep] after its own selection (on the side stream, beside the
+   * attention); 2 = this Reindex step scores and selects only inside the
+   * pool in cand; 0 = neither */
+  int32_t cand_role;
+  int32_t* cand;
 } csa2_step_args;
 
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
