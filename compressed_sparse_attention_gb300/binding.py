@@ -39,6 +39,10 @@ class Csa2Error(RuntimeError):
         self.status = status
 
 
+class HostIO(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("raw", C.c_void_p), ("gate", C.c_void_p), ("out", C.c_void_p)]
+
+
 class Config(C.Structure):
     _fields_ = [("n_heads", C.c_int32), ("head_dim", C.c_int32), ("rope_dim", C.c_int32),
                 ("window", C.c_int32), ("compress_ratio", C.c_int32), ("idx_heads", C.c_int32),
@@ -102,6 +106,10 @@ SIGNATURES = {
                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                               C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                               C.c_void_p, C.c_size_t]),
+    "csa2_step_host": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_step_graph_create": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_step_graph_launch": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "csa2_step_graph_destroy": (None, [C.c_void_p]),
     "csa2_step_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int64]),
     "csa2_step": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(StepArgs)]),
     "csa2_last_launch_count": (C.c_int32, [C.c_void_p]),
@@ -307,11 +315,20 @@ class Context:
     def step_workspace_size(self, n_query, max_vis) -> int:
         return int(self.lib.csa2_step_workspace_size(self.h, n_query, max_vis))
 
-    def step(self, mode, n_seq, max_vis, *, q, q_pos, seq_of_q, n_vis, sink, win_kv, win_off, pool_kv, pool_off,
-             topk_idx, out, workspace, q_idx=None, w_heads=None, win_scale=None, win_lo=None, pool_scale=None,
-             idx_keys=None, idx_key_scale=None, raw=None, gate=None, tok_off=None, first_pos=None, norm_w=None,
-             w_idx=None, k_norm_w=None, lse=None, append=False, state_raw=None, state_gate=None, cand_role=0,
-             cand=None):
+    def step(self, mode, n_seq, max_vis, **kw):
+        self._ok(self.lib.csa2_step(self.h, C.c_void_p(_stream()), C.byref(self.step_args(mode, n_seq, max_vis, **kw))),
+                 "csa2_step")
+
+    def prepare_step(self, mode, n_seq, max_vis, **kw) -> "PreparedStep":
+        """The step's argument block built once, for a serving loop that reuses
+        its buffers from step to step: each run is then a single C call."""
+        return PreparedStep(self, self.step_args(mode, n_seq, max_vis, **kw), kw)
+
+    def step_args(self, mode, n_seq, max_vis, *, q, q_pos, seq_of_q, n_vis, sink, win_kv, win_off, pool_kv,
+                  pool_off, topk_idx, out, workspace, q_idx=None, w_heads=None, win_scale=None, win_lo=None,
+                  pool_scale=None, idx_keys=None, idx_key_scale=None, raw=None, gate=None, tok_off=None,
+                  first_pos=None, norm_w=None, w_idx=None, k_norm_w=None, lse=None, append=False, state_raw=None,
+                  state_gate=None, cand_role=0, cand=None) -> StepArgs:
         a = StepArgs()
         a.mode, a.n_seq, a.n_query, a.max_vis = mode, n_seq, q.shape[0], max_vis
         a.q = self._p(q, torch.bfloat16, "q")
@@ -348,7 +365,58 @@ class Context:
         a.state_gate = self._p(state_gate, torch.float32, "state_gate")
         a.cand_role = cand_role
         a.cand = self._p(cand, torch.int32, "cand")
-        self._ok(self.lib.csa2_step(self.h, C.c_void_p(_stream()), C.byref(a)), "csa2_step")
+        return a
+
+
+class PreparedStep:
+    """A csa2_step argument block kept alive with the tensors it points at."""
+
+    def __init__(self, ctx: Context, args: StepArgs, tensors: dict):
+        self.ctx, self.args, self._keep = ctx, args, tensors
+        self.io = HostIO()
+
+    def run(self):
+        self.ctx._ok(self.ctx.lib.csa2_step(self.ctx.h, C.c_void_p(_stream()), C.byref(self.args)), "csa2_step")
+
+    def run_host(self, q=None, raw=None, gate=None, out=None):
+        """csa2_step_host: copy the step's inputs from host tensors (pinned)
+        into the prepared device buffers, run the step, copy the output back."""
+        io = self.io
+        io.q = None if q is None else q.data_ptr()
+        io.raw = None if raw is None else raw.data_ptr()
+        io.gate = None if gate is None else gate.data_ptr()
+        io.out = None if out is None else out.data_ptr()
+        self.ctx._ok(self.ctx.lib.csa2_step_host(self.ctx.h, C.c_void_p(_stream()), C.byref(self.args),
+                                                 C.byref(io)), "csa2_step_host")
+
+    def host_graph(self, q=None, raw=None, gate=None, out=None) -> "StepGraph":
+        """csa2_step_graph_create: this step with these host buffers captured
+        once; each StepGraph.launch() repeats the copies and the step."""
+        io = HostIO()
+        io.q = None if q is None else q.data_ptr()
+        io.raw = None if raw is None else raw.data_ptr()
+        io.gate = None if gate is None else gate.data_ptr()
+        io.out = None if out is None else out.data_ptr()
+        h = C.c_void_p()
+        self.ctx._ok(self.ctx.lib.csa2_step_graph_create(self.ctx.h, C.byref(self.args), C.byref(io), C.byref(h)),
+                     "csa2_step_graph_create")
+        return StepGraph(self, h, (q, raw, gate, out))
+
+
+class StepGraph:
+    """A captured host step; holds the prepared step and host tensors it uses."""
+
+    def __init__(self, prep: PreparedStep, handle, host_tensors):
+        self.prep, self.h, self._keep = prep, handle, host_tensors
+
+    def launch(self):
+        self.prep.ctx._ok(self.prep.ctx.lib.csa2_step_graph_launch(self.h, C.c_void_p(_stream())),
+                          "csa2_step_graph_launch")
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            self.prep.ctx.lib.csa2_step_graph_destroy(self.h)
+            self.h = None
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:

@@ -680,4 +680,84 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   return CSA2_OK;
 }
 
+csa2_status csa2_step_host(csa2_ctx* ctx, void* stream, const csa2_step_args* a, const csa2_host_io* io) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (!a || !io) return fail(ctx, CSA2_ERR_INVALID_ARG, "step_host: null args");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t q_bytes = (size_t)a->n_query * csa2::kHeads * csa2::kDim * 2;
+  const size_t raw_bytes = (size_t)a->n_tokens * csa2::kDim * 2, gate_bytes = (size_t)a->n_tokens * csa2::kDim * 4;
+  if ((io->q && !a->q) || (io->raw && !a->raw) || (io->gate && !a->gate) || (io->out && !a->out))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "step_host: a host buffer without its device buffer");
+  cudaError_t e = cudaSuccess;
+  if (io->q && q_bytes) e = cudaMemcpyAsync(const_cast<uint16_t*>(a->q), io->q, q_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && io->raw && raw_bytes)
+    e = cudaMemcpyAsync(const_cast<uint16_t*>(a->raw), io->raw, raw_bytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && io->gate && gate_bytes)
+    e = cudaMemcpyAsync(const_cast<float*>(a->gate), io->gate, gate_bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "step_host: copy in");
+  csa2_status s = csa2_step(ctx, stream, a);
+  if (s != CSA2_OK) return s;
+  if (io->out && q_bytes) {
+    e = cudaMemcpyAsync(io->out, a->out, q_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step_host: copy out");
+  }
+  return CSA2_OK;
+}
+
+struct csa2_step_graph {
+  csa2_ctx* ctx = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+csa2_status csa2_step_graph_create(csa2_ctx* ctx, const csa2_step_args* a, const csa2_host_io* io,
+                                   csa2_step_graph** out) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  if (!a || !io || !out) return fail(ctx, CSA2_ERR_INVALID_ARG, "step_graph_create: null argument");
+  *out = nullptr;
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "step_graph_create: stream");
+  csa2_step_graph* g = new csa2_step_graph();
+  g->ctx = ctx;
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  csa2_status s = CSA2_OK;
+  if (e == cudaSuccess) {
+    s = csa2_step_host(ctx, cs, a, io);
+    // end the capture whatever happened, so that the stream is usable again
+    const cudaError_t ee = cudaStreamEndCapture(cs, &g->graph);
+    if (s == CSA2_OK && ee != cudaSuccess) s = cuda_fail(ctx, ee, "step_graph_create: capture");
+  } else {
+    s = cuda_fail(ctx, e, "step_graph_create: begin capture");
+  }
+  if (s == CSA2_OK) {
+    e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+    if (e != cudaSuccess) s = cuda_fail(ctx, e, "step_graph_create: instantiate");
+  }
+  cudaStreamDestroy(cs);
+  if (s != CSA2_OK) {
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return s;
+  }
+  *out = g;
+  return CSA2_OK;
+}
+
+csa2_status csa2_step_graph_launch(csa2_step_graph* g, void* stream) {
+  if (!g) return CSA2_ERR_INVALID_ARG;
+  const cudaError_t e = cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(g->ctx, e, "step_graph_launch");
+  return CSA2_OK;
+}
+
+void csa2_step_graph_destroy(csa2_step_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
 }  // extern "C"

@@ -399,6 +399,35 @@ typedef struct csa2_step_args {
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* args);
 
+/* csa2_step_host: csa2_step with the step's inputs and output in host memory
+ * (pinned, so that the copies are asynchronous). On `stream`, in order: one
+ * copy each of io->q into args->q (n_query x 64 x 512 bf16), io->raw into
+ * args->raw (n_tokens x 512 bf16) and io->gate into args->gate (n_tokens x
+ * 512 fp32; skipped when NULL), then the step, then args->out into io->out
+ * (n_query x 64 x 512 bf16). A NULL host pointer skips that copy. The
+ * device buffers in args are the staging buffers; the caches stay resident.
+ * Returns after enqueueing; io->out is valid once `stream` has completed. */
+typedef struct csa2_host_io {
+  const void* q;
+  const void* raw;
+  const void* gate;
+  void* out;
+} csa2_host_io;
+csa2_status csa2_step_host(csa2_ctx* ctx, void* stream, const csa2_step_args* args, const csa2_host_io* io);
+
+/* A csa2_step_host call captured once into a CUDA graph (its copies, its
+ * launches on `stream` and on the context's side stream) and replayed by
+ * csa2_step_graph_launch: each launch copies the same host buffers in, runs
+ * the same step and copies the output back, in one driver call. Every buffer
+ * that args and io name must stay valid while the graph exists; launches of
+ * one context's graphs must not overlap in time (they share the context's
+ * work counters), which holds when they go to one stream. */
+typedef struct csa2_step_graph csa2_step_graph;
+csa2_status csa2_step_graph_create(csa2_ctx* ctx, const csa2_step_args* args, const csa2_host_io* io,
+                                   csa2_step_graph** out);
+csa2_status csa2_step_graph_launch(csa2_step_graph* graph, void* stream);
+void csa2_step_graph_destroy(csa2_step_graph* graph);
+
 /* ------------------------------------------------------------------------
  * csa2_attend_noalloc: csa2_attend for callers that cannot allocate device
  * memory themselves (a host that owns all device memory through its own pool

@@ -65,3 +65,41 @@ def test_step_two_queries_per_sequence(m):
     state = _full_state(ctx, case, geom, f)
     same = [_check_query(ctx, case, qi, geom, f, out, scores, sel, state, wl.name)[1] for qi in range(wl.n_query)]
     assert sum(same) >= len(same) - 1
+
+
+def test_step_host_equals_step():
+    """csa2_step_host (inputs copied from pinned host memory into staging
+    buffers, output copied back) gives the bits csa2_step gives."""
+    require_gpu()
+    from compressed_sparse_attention_gb300 import binding
+    wl = Workload("host_io", 5, (4100, 9000, 3003, 2600, 7777), 4, seed=960, value_std=1.0 / 22.6)
+    ctx = context()
+    case = Case(ctx, wl)
+    i = case.inp
+    Q = wl.n_query
+    max_vis = int(i["n_vis"].max())
+    idx = torch.empty((Q, 512), dtype=torch.int32, device=DEV)
+    out_dev = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=DEV)
+    ws = binding.workspace(ctx.step_workspace_size(Q, max_vis), DEV)
+    common = dict(q_pos=i["q_pos"], seq_of_q=i["seq_of_q"], n_vis=i["n_vis"], sink=i["sink"], win_kv=i["win_kv"],
+                  win_off=i["win_off"], pool_kv=i["pool_kv"], pool_off=i["pool_off"], topk_idx=idx, workspace=ws,
+                  q_idx=i["q_idx"], w_heads=i["w_heads"], idx_keys=i["idx_keys"], tok_off=i["tok_off"],
+                  first_pos=i["first_pos"], norm_w=i["norm_w"], w_idx=i["w_idx"], k_norm_w=i["k_norm_w"])
+    ctx.step(binding.MODE_FULL, wl.n_seq, max_vis, q=i["q"], raw=i["raw"], gate=i["gate"], out=out_dev, **common)
+    sq, sraw, sgate = torch.empty_like(i["q"]), torch.empty_like(i["raw"]), torch.empty_like(i["gate"])
+    sout = torch.empty_like(out_dev)
+    prep = ctx.prepare_step(binding.MODE_FULL, wl.n_seq, max_vis, q=sq, raw=sraw, gate=sgate, out=sout, **common)
+    hq, hraw, hgate = (t.cpu().pin_memory() for t in (i["q"], i["raw"], i["gate"]))
+    hout = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    prep.run_host(q=hq, raw=hraw, gate=hgate, out=hout)
+    torch.cuda.synchronize()
+    assert ctx.check() == (0, 0)
+    assert torch.equal(hout, out_dev.cpu())
+    # the same step captured with its copies and replayed
+    hout2 = torch.zeros_like(hout).pin_memory()
+    graph = prep.host_graph(q=hq, raw=hraw, gate=hgate, out=hout2)
+    for _ in range(2):
+        graph.launch()
+    torch.cuda.synchronize()
+    assert ctx.check() == (0, 0)
+    assert torch.equal(hout2, out_dev.cpu())
