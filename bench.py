@@ -135,6 +135,12 @@ def barrier(pg, device):
             pg.barrier()
 
 
+def aggregate_value(world: int, units_per_step: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processed its own
+    units_per_step each step; the job took the slowest rank's time."""
+    return world * units_per_step * steps / (ms_max / 1000.0)
+
+
 def max_over_ranks(pg, x: float, device) -> float:
     if pg is None:
         return x
@@ -615,7 +621,7 @@ def main():
     sampler.stop()
     clocks = sampler.summary()
     ms_step = r["ms_max"] / args.steps
-    value = world * units_per_step * args.steps / (r["ms_max"] / 1000.0)
+    value = aggregate_value(world, units_per_step, args.steps, r["ms_max"])
     step_bytes = algorithmic_bytes(wl)
     gbs = step_bytes / (ms_step / 1000.0) / 1e9
     idx_b = index_bytes(wl)
