@@ -23,7 +23,10 @@
 namespace csa2 {
 
 constexpr int kTileRows = 128;
-constexpr int kAttThreads = 128;
+// 8 warps: warp w reads tensor-memory lane quadrant w % 4 (tile rows, or
+// output dims, 32 (w % 4) .. +31) and takes heads 32 (w / 4) .. +31 of them
+constexpr int kAttWarps = 8;
+constexpr int kAttThreads = 32 * kAttWarps;
 constexpr uint32_t SM_Q = 0;                          // [9 dim blocks][64 heads][128 B]; block 8 = rope residual
 constexpr uint32_t SM_KV = 73728;                     // [8 dim blocks][128 rows][128 B]
 constexpr uint32_t SM_P = SM_KV + 131072;             // [128 rows][128 B]  (64 heads, bf16)
@@ -41,18 +44,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, 1, 1);
 
-// Butterfly reduce-scatter of 64 per-lane values over the 32 lanes of a warp:
-// afterwards lane l holds the reduction of heads h0(l), h0(l)+1 with
-// h0 = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0 (b_k = bit k of l).
+// Butterfly reduce-scatter of 32 per-lane values over the 32 lanes of a warp:
+// afterwards lane l holds the reduction of value l (step k exchanges the
+// half that lane bit 4-k selects).
 template <bool MAX>
-__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane, float& o0, float& o1) {
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
   for (int step = 0; step < 5; ++step) {
-    const int half = 32 >> step;      // values kept after this step
-    const int off = 16 >> step;       // xor distance
+    const int half = 16 >> step;
+    const int off = 16 >> step;
     const bool upper = (lane & off) != 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < 16; ++i) {
       if (i < half) {
         const float lo = v[i], hi = v[half + i];
         const float send = upper ? lo : hi;
@@ -62,14 +65,9 @@ __device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane, float
       }
     }
   }
-  o0 = v[0];
-  o1 = v[1];
+  return v[0];
 }
 
-__device__ __forceinline__ int rs_head(int lane) {
-  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 +
-         (lane & 1) * 2;
-}
 
 // KVF: 0 bf16 rows; 1 fp8 rows; 2 fp8 window rows and fp4 pool rows
 template <int KVF>
@@ -89,6 +87,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const uint32_t tslot = base_s + SM_MISC + 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hh = warp >> 2;  // lane quadrant and head half
+  const int row = quad * 32 + lane;           // this thread's tile row / output dim in a 128 block
   const int qi = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
   // split 0 takes the launch's first tile alone when lead_single is set (the
   // window tile); the other splits take tiles_per_split tiles each
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   // selection entry of this thread's row in selected tile `tile` (-1 past k)
   auto sel_entry = [&](int tile, int tile_lim) -> int32_t {
     const int col = (tile - 1) * kTileRows + tid;
-    return (tile >= 1 && tile < tile_lim && col < p.topk && p.topk_idx != nullptr)
+    return (tid < kTileRows && tile >= 1 && tile < tile_lim && col < p.topk && p.topk_idx != nullptr)
                ? p.topk_idx[(int64_t)qi * p.topk + col]
                : -1;
   };
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   // together with the first tile's rows); the rope channels are rotated in
   // place once both have arrived
   if (tile_begin < tile_cap) {
-    for (int h = warp; h < kHeads; h += 4) {
+    for (int h = warp; h < kHeads; h += kAttWarps) {
       const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const uint32_t taddr = misc[2];
   const uint32_t tmem_s = taddr;        // columns [0, 64)
   const uint32_t tmem_o = taddr + 64;   // columns [64, 320)
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   uint32_t phase = 0;
   bool aborted = false;
 
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
 
   for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row)
-    {
+    if (tid < kTileRows) {
       const int r = tid;
       int64_t src = -1;
       const int32_t j_cur = j_next;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     const void* kvsrc = (tile == 0) ? p.win_kv : p.pool_kv;
     if constexpr (KVF == 0) {
       const uint16_t* kv = reinterpret_cast<const uint16_t*>(kvsrc);
-      for (int r = warp; r < kTileRows; r += 4) {
+      for (int r = warp; r < kTileRows; r += kAttWarps) {
         const int64_t src = rows[r];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -217,12 +217,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.pool_kv);
       constexpr int kBatch = 8;
 #pragma unroll 1
-      for (int r0 = warp; r0 < kTileRows; r0 += 4 * kBatch) {
+      for (int r0 = warp; r0 < kTileRows; r0 += kAttWarps * kBatch) {
         uint2 codes[kBatch];
         uint8_t sb[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int64_t src = rows[r0 + 4 * j];
+          const int64_t src = rows[r0 + kAttWarps * j];
           codes[j] = make_uint2(0u, 0u);
           sb[j] = 0;
           if (src >= 0) {
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int r = r0 + 4 * j;
+          const int r = r0 + kAttWarps * j;
           const float sc = e4m3_value(sb[j]) * kE2M1Unscale;  // code values arrive scaled by 2^-14
           uint32_t o[8];
 #pragma unroll
@@ -253,16 +253,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     } else {
       const uint8_t* kv = reinterpret_cast<const uint8_t*>(kvsrc);
       const uint8_t* ksc = (tile == 0) ? p.win_scale : p.pool_scale;
-      // a warp takes rows warp, warp+4, ...; the loads of 8 rows are in
+      // a warp takes rows warp, warp+8, ...; the loads of 8 rows are in
       // flight together before any of them is converted
       constexpr int kBatch = 8;
 #pragma unroll 1
-      for (int r0 = warp; r0 < kTileRows; r0 += 4 * kBatch) {
+      for (int r0 = warp; r0 < kTileRows; r0 += kAttWarps * kBatch) {
         uint4 codes[kBatch];
         uint8_t sb[kBatch];
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int64_t src = rows[r0 + 4 * j];
+          const int64_t src = rows[r0 + kAttWarps * j];
           codes[j] = make_uint4(0u, 0u, 0u, 0u);
           sb[j] = 0;
           if (src >= 0) {
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         }
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-          const int r = r0 + 4 * j;
+          const int r = r0 + kAttWarps * j;
           const float sc = ue8m0_value(sb[j]);
           const uint32_t cw[4] = {codes[j].x, codes[j].y, codes[j].z, codes[j].w};
           uint32_t o[8];
@@ -299,13 +299,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       if (p.rp.pairs > 0) {
         __syncthreads();
         // rotated q = hi + lo, both bf16: the tensor cores see the rotation to
-        // ~2^-16 relative instead of one bf16 rounding. Thread: head tid/2,
-        // chunks 56 + 4*(tid&1) .. +3 (the last 64 channels).
-        const int h = tid >> 1;
+        // ~2^-16 relative instead of one bf16 rounding. Thread: head tid/4,
+        // chunks 56 + 2*(tid&3) .. +1 (the last 64 channels).
+        const int h = tid >> 2;
         const int first_rope = kDim - 2 * p.rp.pairs;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = 56 + 4 * (tid & 1) + u;
+        for (int u = 0; u < 2; ++u) {
+          const int c = 56 + 2 * (tid & 3) + u;
           const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
           uint4* hi_p = reinterpret_cast<uint4*>(sm + SM_Q + 7u * 8192u + inblk);
           const uint4 v = *hi_p;
@@ -345,19 +345,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     phase ^= 1u;
     if (!__syncthreads_and(ok)) { aborted = true; break; }
     tc_fence_after();
-    // ---- softmax over this tile's rows (thread = row = TMEM lane)
-    float s[64];
+    // ---- softmax over this tile's rows (thread = row = TMEM lane; this
+    // warp's 32 heads 32 hh .. +31)
+    float s[32];
     {
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem_s + lane_base, r0);
-      tmem_ld32(tmem_s + lane_base + 32, r1);
+      uint32_t r0[32];
+      tmem_ld32(tmem_s + lane_base + 32 * hh, r0);
       tmem_wait_ld();
-      const bool valid = rows[tid] >= 0;
+      const bool valid = rows[row] >= 0;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        s[k] = valid ? __uint_as_float(r0[k]) * p.scale_log2 : -INFINITY;
-        s[32 + k] = valid ? __uint_as_float(r1[k]) * p.scale_log2 : -INFINITY;
-      }
+      for (int k = 0; k < 32; ++k) s[k] = valid ? __uint_as_float(r0[k]) * p.scale_log2 : -INFINITY;
     }
     // After a CTA's first tile the per-head max is needed only if some score
     // exceeds its head's reference by more than 2^8 (see below); otherwise
@@ -366,18 +363,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     if (!need_max) {
       bool over = false;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) over |= s[k] > m_run[k] + 8.f;
+      for (int k = 0; k < 32; ++k) over |= s[k] > m_run[32 * hh + k] + 8.f;
       need_max = __syncthreads_or(over) != 0;
     }
     if (need_max) {
-      float v[64];
+      float v[32];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) v[k] = s[k];
-      float a0, a1;
-      reduce_scatter64<true>(v, lane, a0, a1);
-      const int h0 = rs_head(lane);
-      red[warp * 64 + h0] = a0;
-      red[warp * 64 + h0 + 1] = a1;
+      for (int k = 0; k < 32; ++k) v[k] = s[k];
+      red[quad * 64 + 32 * hh + lane] = reduce_scatter32<true>(v, lane);
     }
     __syncthreads();
     if (!need_max) {
@@ -398,29 +391,28 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     }
     __syncthreads();
     {
-      float v[64];
-      uint32_t packed[32];
+      float v[32];
+      uint32_t packed[16];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = exp2f(s[2 * k] - m_use[2 * k]);
-        const float p1 = exp2f(s[2 * k + 1] - m_use[2 * k + 1]);
+      for (int k = 0; k < 16; ++k) {
+        const float p0 = exp2f(s[2 * k] - m_use[32 * hh + 2 * k]);
+        const float p1 = exp2f(s[2 * k + 1] - m_use[32 * hh + 2 * k + 1]);
         packed[k] = pack_bf16(p0, p1);
         v[2 * k] = bf16lo(packed[k]);
         v[2 * k + 1] = bf16hi(packed[k]);
       }
-      // P^T row `tid`: 64 heads = 8 chunks of 16 B (MN-major B operand)
+      // P^T row `row`: 64 heads = 8 chunks of 16 B (MN-major B operand); this
+      // thread writes chunks 4 hh .. 4 hh + 3
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t off = SM_P + (uint32_t)tid * 128u + ((uint32_t)(c ^ (tid & 7)) << 4);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int c = 4 * hh + c4;
+        const uint32_t off = SM_P + (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
         *reinterpret_cast<uint4*>(sm + off) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            make_uint4(packed[4 * c4], packed[4 * c4 + 1], packed[4 * c4 + 2], packed[4 * c4 + 3]);
       }
-      float a0, a1;
-      reduce_scatter64<false>(v, lane, a0, a1);
-      const int h0 = rs_head(lane);
+      const float a = reduce_scatter32<false>(v, lane);
       __syncthreads();  // every warp has read red[] (max) before it is reused for sums
-      red[warp * 64 + h0] = a0;
-      red[warp * 64 + h0 + 1] = a1;
+      red[quad * 64 + 32 * hh + lane] = a;
     }
     __syncthreads();
     if (tid < kHeads) {
@@ -431,16 +423,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     if (misc[3]) {
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          const uint32_t a = tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base;
-          tmem_ld32(a, r);
-          tmem_wait_ld();
+        uint32_t r[32];
+        const uint32_t a = tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base;
+        tmem_ld32(a, r);
+        tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[32 * hh + k]);
-          tmem_st32(a, r);
-        }
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[32 * hh + k]);
+        tmem_st32(a, r);
       }
       tmem_wait_st();
     }
@@ -493,11 +482,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     }
     __syncthreads();
     uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
-    float al_all[64];  // before any store: no reloads
+    float al_all[32];  // this warp's head half, before any store: no reloads
 #pragma unroll
-    for (int k = 0; k < 64; ++k) al_all[k] = alpha[k];
+    for (int k = 0; k < 32; ++k) al_all[k] = alpha[32 * hh + k];
     for (int mt = 0; mt < 4; ++mt) {
-      const int d = 128 * mt + 32 * warp + lane;
+      const int d = 128 * mt + row;
       float cs = 1.f, sn = 0.f;
       const bool rope = p.rp.pairs > 0 && d >= first_rope;
       if (rope) {
@@ -505,21 +494,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         cs = cs2.x;
         sn = cs2.y;
       }
-      // both 32-head halves of this dim come out of tensor memory together
-      uint32_t ra[32], rb[32];
+      uint32_t ra[32];
       if (have_o) {
-        tmem_ld32(tmem_o + (uint32_t)(64 * mt) + lane_base, ra);
-        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32) + lane_base, rb);
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, ra);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) ra[k] = rb[k] = 0u;
+        for (int k = 0; k < 32; ++k) ra[k] = 0u;
       }
-      auto emit = [&](const uint32_t (&r)[32], int hh) {
+      {
+        const uint32_t (&r)[32] = ra;
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          v[k] = __uint_as_float(r[k]) * al_all[32 * hh + k];
+          v[k] = __uint_as_float(r[k]) * al_all[k];
           const float partner = __shfl_xor_sync(0xffffffffu, v[k], 1);
           if (rope) v[k] = (d & 1) ? (v[k] * cs - partner * sn) : (v[k] * cs + partner * sn);
         }
@@ -533,9 +521,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
           const uint32_t w = odd ? pack_bf16(recv, v[k + 1]) : pack_bf16(v[k], recv);
           *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + (d & ~1)) = w;
         }
-      };
-      emit(ra, 0);
-      emit(rb, 1);
+      }
     }
   } else {
     // unnormalised partial O^T and (m, l) for the merge
@@ -549,23 +535,18 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       // stores two adjacent dims of one head as one 32-bit word.
       uint16_t* wo = p.ws_o + slot * kHeads * kDim;
       for (int mt = 0; mt < 4; ++mt) {
-        const int d = 128 * mt + 32 * warp + lane;
+        const int d = 128 * mt + row;
         const bool odd = (d & 1) != 0;
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tmem_o + (uint32_t)(64 * mt) + lane_base, ra);
-        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32) + lane_base, rb);
+        uint32_t r[32];
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t* r = hh ? rb : ra;
-#pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
-            const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-            const int h = 32 * hh + k + (odd ? 1 : 0);
-            const uint32_t w = odd ? pack_bf16(recv, v1) : pack_bf16(v0, recv);
-            *reinterpret_cast<uint32_t*>(wo + (int64_t)h * kDim + (d & ~1)) = w;
-          }
+        for (int k = 0; k < 32; k += 2) {
+          const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+          const int h = 32 * hh + k + (odd ? 1 : 0);
+          const uint32_t w = odd ? pack_bf16(recv, v1) : pack_bf16(v0, recv);
+          *reinterpret_cast<uint32_t*>(wo + (int64_t)h * kDim + (d & ~1)) = w;
         }
       }
     }
