@@ -3,7 +3,7 @@
 // Flash on WASTE", "What is new" item 1: the sink enters the denominator only,
 // the output's rope channels are rotated back by -t).
 //
-// One CTA (128 threads) owns one query and a contiguous range of 128-row
+// One CTA (256 threads) owns one query and a contiguous range of 128-row
 // tiles: tile 0 is the query's window, tiles 1.. are the selected compressed
 // entries, 128 per tile. All 64 heads share each KV row, so per tile the two
 // products are dense contractions on the tensor cores, in transposed form so
@@ -13,8 +13,9 @@
 // KV sits in shared memory once, in the 128-byte-swizzled layout that is at
 // the same time the K-major A operand of the first product and the MN-major
 // A operand of the second. S^T (64 columns) and O^T (4 x 64 columns) live in
-// tensor memory. Softmax runs with one thread per row (TMEM lane), heads
-// reduced across lanes by a butterfly reduce-scatter; the running max / sum
+// tensor memory. Softmax runs with one thread per (row = TMEM lane, half of
+// the heads): warp w reads lane quadrant w % 4 and heads 32 (w / 4) .. +31,
+// heads reduced across lanes by a butterfly reduce-scatter; the running max / sum
 // rescale O^T in tensor memory when a later tile raises a head's max.
 // With several CTAs per query (split-K) each writes its unnormalised O^T and
 // (max, sum) and a merge kernel combines them with the sink.
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t plen = q_ok ? (pool_b1 - pool_b0) : 0;
 
   for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
-    // ---- row sources of this tile (one thread per row)
+    // ---- row sources of this tile (one thread per row, the first 128)
     if (tid < kTileRows) {
       const int r = tid;
       int64_t src = -1;
