@@ -379,8 +379,10 @@ class PreparedStep:
         self.ctx._ok(self.ctx.lib.csa2_step(self.ctx.h, C.c_void_p(_stream()), C.byref(self.args)), "csa2_step")
 
     def run_host(self, q=None, raw=None, gate=None, out=None):
-        """csa2_step_host: copy the step's inputs from host tensors (pinned)
-        into the prepared device buffers, run the step, copy the output back."""
+        """csa2_step_host: the step with its inputs in host tensors (pinned):
+        q is copied in beside the scan, the raw tokens and gates before
+        compress. A pinned `out` is written by the step directly; any other
+        host `out` gets one copy of the prepared device output."""
         io = self.io
         io.q = None if q is None else q.data_ptr()
         io.raw = None if raw is None else raw.data_ptr()

@@ -107,7 +107,8 @@ static void release(csa2_ctx* ctx) {
   if (ctx->d_flags) cudaFree(ctx->d_flags);
   if (ctx->d_work) cudaFree(ctx->d_work);
   if (ctx->side) cudaStreamDestroy(ctx->side);
-  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join, ctx->ev_topk})
+  if (ctx->copy) cudaStreamDestroy(ctx->copy);
+  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join, ctx->ev_topk, ctx->ev_copy, ctx->ev_q})
     if (ev) cudaEventDestroy(ev);
   delete ctx;
 }
@@ -147,6 +148,9 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_tail, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_topk, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->copy, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_copy, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_q, cudaEventDisableTiming);
   if (e != cudaSuccess) {
     cudaGetLastError();
     release(ctx);
@@ -518,14 +522,26 @@ size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
   return w.scores + w.n_pool + w.tk + w.cand + w.at;
 }
 
+// Host buffers of a step's inputs, copied in by the step itself (csa2_step_host)
+struct StepHostIn {
+  const void* q = nullptr;
+  const void* raw = nullptr;
+  const void* gate = nullptr;
+};
+
+static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_args* a, const StepHostIn* hin);
+
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
+  return step_impl(ctx, reinterpret_cast<cudaStream_t>(stream), a, nullptr);
+}
+
+static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_args* a, const StepHostIn* hin) {
   if (!ctx) return CSA2_ERR_INVALID_ARG;
   ctx->last_launches = 0;
   if (!a) return fail(ctx, CSA2_ERR_INVALID_ARG, "step: null args");
   if (a->mode != CSA2_MODE_FULL && a->mode != CSA2_MODE_REINDEX && a->mode != CSA2_MODE_REUSE)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "step: unknown mode");
   if (!a->topk_idx) return fail(ctx, CSA2_ERR_INVALID_ARG, "step: topk_idx is required");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t need = csa2_step_workspace_size(ctx, a->n_query, a->max_vis);
   csa2_status s = check_ws(ctx, a->workspace, a->workspace_bytes, need);
   if (s != CSA2_OK) return s;
@@ -557,15 +573,53 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   // Every exit after a fork makes the caller's stream wait for the side
   // stream's last launch, so that a capture of the step stays well formed and
   // the caller's stream orders after all of it.
-  bool side_open = false;
+  // The same holds for the copy stream that brings q in from host memory.
+  bool side_open = false, q_pending = false;
   auto join = [&](csa2_status so) -> csa2_status {
-    if (!side_open) return so;
-    side_open = false;
-    cudaError_t je = cudaEventRecord(ctx->ev_join, ctx->side);
-    if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ctx->ev_join, 0);
+    cudaError_t je = cudaSuccess;
+    if (side_open) {
+      side_open = false;
+      je = cudaEventRecord(ctx->ev_join, ctx->side);
+      if (je == cudaSuccess) je = cudaStreamWaitEvent(st, ctx->ev_join, 0);
+    }
+    if (q_pending) {
+      q_pending = false;
+      const cudaError_t qe = cudaStreamWaitEvent(st, ctx->ev_q, 0);
+      if (je == cudaSuccess) je = qe;
+    }
     if (je != cudaSuccess && so == CSA2_OK) return cuda_fail(ctx, je, "step: join");
     return so;
   };
+  // Host inputs. Nothing before the attention reads q, so its copy runs on
+  // the copy stream beside compress and the index scan, and every attention
+  // launch waits for it. The raw tokens and gates go on the stream that runs
+  // compress, just before it.
+  const size_t q_bytes = hin && hin->q ? (size_t)a->n_query * csa2::kHeads * csa2::kDim * 2 : 0;
+  const size_t raw_bytes = hin && hin->raw ? (size_t)a->n_tokens * csa2::kDim * 2 : 0;
+  const size_t gate_bytes = hin && hin->gate ? (size_t)a->n_tokens * csa2::kDim * 4 : 0;
+  auto wait_q = [&](cudaStream_t sw) -> cudaError_t {
+    if (!q_pending) return cudaSuccess;
+    const cudaError_t we = cudaStreamWaitEvent(sw, ctx->ev_q, 0);
+    if (we == cudaSuccess && sw == st) q_pending = false;
+    return we;
+  };
+  auto copy_tokens = [&](cudaStream_t sc) -> cudaError_t {
+    cudaError_t ce = cudaSuccess;
+    if (raw_bytes)
+      ce = cudaMemcpyAsync(const_cast<uint16_t*>(a->raw), hin->raw, raw_bytes, cudaMemcpyHostToDevice, sc);
+    if (ce == cudaSuccess && gate_bytes)
+      ce = cudaMemcpyAsync(const_cast<float*>(a->gate), hin->gate, gate_bytes, cudaMemcpyHostToDevice, sc);
+    return ce;
+  };
+  if (q_bytes) {
+    cudaError_t e = cudaEventRecord(ctx->ev_copy, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->copy, ctx->ev_copy, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<uint16_t*>(a->q), hin->q, q_bytes, cudaMemcpyHostToDevice, ctx->copy);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_q, ctx->copy);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "step: copy of q");
+    q_pending = true;
+  }
   // A decode-shaped Full step (at most two closing groups per sequence, the
   // scan in its CUDA-core form) runs compress on the side stream beside the
   // scan of the entries that existed before the step. The scan hands out its
@@ -586,6 +640,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
       side_open = true;
       cs = ctx->side;
     }
+    cudaError_t ce = copy_tokens(cs);
+    if (ce != cudaSuccess) return join(cuda_fail(ctx, ce, "step: copy of the raw tokens"));
     ctx->last_launches = 0;
     s = do_compress(ctx, cs, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
                     a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale,
@@ -600,6 +656,10 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
       launches += ctx->last_launches;
     }
   }
+  if (!full) {
+    const cudaError_t ce = copy_tokens(st);
+    if (ce != cudaSuccess) return join(cuda_fail(ctx, ce, "step: copy of the raw tokens"));
+  }
   if (a->n_query == 0) {
     ctx->last_launches = launches;
     return join(CSA2_OK);
@@ -607,7 +667,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
   if (a->mode == CSA2_MODE_REUSE) {
     // nothing to overlap with: window and selected tiles share one launch
     ctx->last_launches = 0;
-    cudaError_t e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &ctx->last_launches);
+    cudaError_t e = wait_q(st);
+    if (e == cudaSuccess) e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &ctx->last_launches);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
     ctx->last_launches += launches;
     return CSA2_OK;
@@ -637,7 +698,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_idx, 0);
     if (e == cudaSuccess) {
       side_open = true;
-      e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
+      e = wait_q(ctx->side);
+      if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
     }
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: window tile"));
   }
@@ -652,6 +714,8 @@ csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* a) {
     e = cudaEventRecord(ctx->ev_topk, st);
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: record top-k"));
   }
+  e = wait_q(st);
+  if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: wait for q"));
   if (pl.split_window) {
     e = csa2::launch_attend_main(st, kvf, ap, pl, at_ws, &launches);
     if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
@@ -686,20 +750,32 @@ csa2_status csa2_step_host(csa2_ctx* ctx, void* stream, const csa2_step_args* a,
   if (!a || !io) return fail(ctx, CSA2_ERR_INVALID_ARG, "step_host: null args");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t q_bytes = (size_t)a->n_query * csa2::kHeads * csa2::kDim * 2;
-  const size_t raw_bytes = (size_t)a->n_tokens * csa2::kDim * 2, gate_bytes = (size_t)a->n_tokens * csa2::kDim * 4;
   if ((io->q && !a->q) || (io->raw && !a->raw) || (io->gate && !a->gate) || (io->out && !a->out))
     return fail(ctx, CSA2_ERR_INVALID_ARG, "step_host: a host buffer without its device buffer");
-  cudaError_t e = cudaSuccess;
-  if (io->q && q_bytes) e = cudaMemcpyAsync(const_cast<uint16_t*>(a->q), io->q, q_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && io->raw && raw_bytes)
-    e = cudaMemcpyAsync(const_cast<uint16_t*>(a->raw), io->raw, raw_bytes, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && io->gate && gate_bytes)
-    e = cudaMemcpyAsync(const_cast<float*>(a->gate), io->gate, gate_bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "step_host: copy in");
-  csa2_status s = csa2_step(ctx, stream, a);
-  if (s != CSA2_OK) return s;
+  // An output buffer in page-locked host memory that the device addresses
+  // (16-byte aligned) is written by the step's last launch directly, over the
+  // host link; any other is filled by one copy from args->out after the step.
+  csa2_step_args da = *a;
+  bool direct_out = false;
   if (io->out && q_bytes) {
-    e = cudaMemcpyAsync(io->out, a->out, q_bytes, cudaMemcpyDeviceToHost, st);
+    cudaPointerAttributes pa;
+    const cudaError_t pe = cudaPointerGetAttributes(&pa, io->out);
+    if (pe == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer != nullptr &&
+        (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15) == 0) {
+      da.out = static_cast<uint16_t*>(pa.devicePointer);
+      direct_out = true;
+    } else if (pe != cudaSuccess) {
+      cudaGetLastError();  // an address CUDA does not know: take the copy
+    }
+  }
+  StepHostIn hin;
+  hin.q = io->q;
+  hin.raw = io->raw;
+  hin.gate = io->gate;
+  csa2_status s = step_impl(ctx, st, &da, &hin);
+  if (s != CSA2_OK) return s;
+  if (io->out && q_bytes && !direct_out) {
+    const cudaError_t e = cudaMemcpyAsync(io->out, a->out, q_bytes, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step_host: copy out");
   }
   return CSA2_OK;

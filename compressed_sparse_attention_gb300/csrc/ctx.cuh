@@ -17,6 +17,9 @@ struct csa2_ctx {
   cudaEvent_t ev_tail = nullptr;  // recorded on the side stream after compress and the tail scores
   cudaEvent_t ev_join = nullptr;  // recorded on the side stream after its last launch
   cudaEvent_t ev_topk = nullptr;  // recorded on the caller's stream after a candidate source's top-k
+  cudaStream_t copy = nullptr;    // host-buffer steps: the copy of q beside the first half of the step
+  cudaEvent_t ev_copy = nullptr;  // recorded on the caller's stream before that copy
+  cudaEvent_t ev_q = nullptr;     // recorded on the copy stream once q is on the device
   std::string err;
   int last_launches = 0;
 };

@@ -67,11 +67,16 @@ def test_step_two_queries_per_sequence(m):
     assert sum(same) >= len(same) - 1
 
 
-def test_step_host_equals_step():
-    """csa2_step_host (inputs copied from pinned host memory into staging
-    buffers, output copied back) gives the bits csa2_step gives."""
+@pytest.mark.parametrize("mode", ["full", "reindex", "reuse"])
+def test_step_host_equals_step(mode):
+    """csa2_step_host gives the bits csa2_step gives: q copied in on the copy
+    stream beside the scan, the raw tokens and gates before compress, and the
+    output either written straight into pinned host memory by the step's last
+    launch or, for pageable host memory, copied back from the staging buffer.
+    Also captured with its copies into a graph and replayed."""
     require_gpu()
     from compressed_sparse_attention_gb300 import binding
+    code = {"full": binding.MODE_FULL, "reindex": binding.MODE_REINDEX, "reuse": binding.MODE_REUSE}[mode]
     wl = Workload("host_io", 5, (4100, 9000, 3003, 2600, 7777), 4, seed=960, value_std=1.0 / 22.6)
     ctx = context()
     case = Case(ctx, wl)
@@ -85,16 +90,31 @@ def test_step_host_equals_step():
                   win_off=i["win_off"], pool_kv=i["pool_kv"], pool_off=i["pool_off"], topk_idx=idx, workspace=ws,
                   q_idx=i["q_idx"], w_heads=i["w_heads"], idx_keys=i["idx_keys"], tok_off=i["tok_off"],
                   first_pos=i["first_pos"], norm_w=i["norm_w"], w_idx=i["w_idx"], k_norm_w=i["k_norm_w"])
+    # a Full step first: it fills the pool and the selection Reuse reads
     ctx.step(binding.MODE_FULL, wl.n_seq, max_vis, q=i["q"], raw=i["raw"], gate=i["gate"], out=out_dev, **common)
+    if code != binding.MODE_FULL:
+        ctx.step(code, wl.n_seq, max_vis, q=i["q"], raw=i["raw"], gate=i["gate"], out=out_dev, **common)
+    torch.cuda.synchronize()
+    ref = out_dev.cpu()
+    sel = idx.clone()
     sq, sraw, sgate = torch.empty_like(i["q"]), torch.empty_like(i["raw"]), torch.empty_like(i["gate"])
-    sout = torch.empty_like(out_dev)
-    prep = ctx.prepare_step(binding.MODE_FULL, wl.n_seq, max_vis, q=sq, raw=sraw, gate=sgate, out=sout, **common)
+    sout = torch.zeros_like(out_dev)
+    prep = ctx.prepare_step(code, wl.n_seq, max_vis, q=sq, raw=sraw, gate=sgate, out=sout, **common)
     hq, hraw, hgate = (t.cpu().pin_memory() for t in (i["q"], i["raw"], i["gate"]))
     hout = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
     prep.run_host(q=hq, raw=hraw, gate=hgate, out=hout)
     torch.cuda.synchronize()
     assert ctx.check() == (0, 0)
-    assert torch.equal(hout, out_dev.cpu())
+    assert torch.equal(hout, ref)
+    assert torch.equal(idx, sel)
+    assert torch.equal(sq, i["q"]) and torch.equal(sraw, i["raw"]) and torch.equal(sgate, i["gate"])
+    assert float(sout.float().abs().sum()) == 0.0, "a pinned output is written directly, not staged"
+    # pageable host output: the step writes the staging buffer, one copy brings it back
+    hpage = torch.zeros(out_dev.shape, dtype=out_dev.dtype)
+    prep.run_host(q=hq, raw=hraw, gate=hgate, out=hpage)
+    torch.cuda.synchronize()
+    assert ctx.check() == (0, 0)
+    assert torch.equal(hpage, ref) and torch.equal(sout.cpu(), ref)
     # the same step captured with its copies and replayed
     hout2 = torch.zeros_like(hout).pin_memory()
     graph = prep.host_graph(q=hq, raw=hraw, gate=hgate, out=hout2)
@@ -102,4 +122,4 @@ def test_step_host_equals_step():
         graph.launch()
     torch.cuda.synchronize()
     assert ctx.check() == (0, 0)
-    assert torch.equal(hout2, out_dev.cpu())
+    assert torch.equal(hout2, ref)
