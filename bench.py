@@ -443,11 +443,15 @@ def run_hier_extra(args, device):
 
 
 def run_e2e(args, ctx, copies, stream, device, wl):
-    """Per step, one csa2_step_host call: H2D of the step's inputs (q, and the
-    closing groups' raw tokens and gates) from pinned host memory into the
-    staging buffers, the step, D2H of the output; the caches (window, pool,
-    index keys) stay resident. The argument block of each input copy is
-    prepared once, as a serving loop that reuses its buffers would."""
+    """The step through its host-buffer entry points, with the step's inputs
+    (q, and the closing groups' raw tokens and gates) and its output in pinned
+    host memory; the caches (window, pool, index keys) stay resident. Timed two
+    ways: one csa2_step_graph_launch per step (the host step captured once per
+    input copy) and one csa2_step_host call per step. Inside, q is staged by a
+    kernel beside the index scan, compress reads the raw tokens and gates in
+    place, and the merge writes the output into host memory. The argument
+    block of each input copy is prepared once, as a serving loop that reuses
+    its buffers would."""
     steps = max(10, min(args.steps, 200))
     hosts = []
     for c in copies:
@@ -627,6 +631,12 @@ def main():
     idx_b = index_bytes(wl)
     idx_gbs = idx_b / (r["idx_ms"] / 1000.0) / 1e9
     e2e = r["e2e"]
+    # the two public host-buffer paths, each the slowest rank's time; the
+    # faster of the two is the end-to-end figure
+    e2e_graph = max_over_ranks(pg, e2e["ms_per_step"], device)
+    e2e_direct = max_over_ranks(pg, e2e["direct_ms"], device)
+    e2e_ms = min(e2e_graph, e2e_direct)
+    e2e_api = ("csa2_step_graph_launch per step" if e2e_graph <= e2e_direct else "csa2_step_host per step")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -642,11 +652,13 @@ def main():
                      "traffic": INDEX_TRAFFIC_BYTES if wl.name == "decode_64k_b32" else None,
                      "peak_source": peak_src,
                      "bytes_per_launch": idx_b, "ms_per_launch": r["idx_ms"]},
-        "e2e": {"value": world * units_per_step / (e2e["ms_per_step"] / 1000.0), "unit": "tokens/s",
+        "e2e": {"value": world * units_per_step / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": e2e["ms_per_step"], "steps": e2e["steps"],
-                "api": "csa2_step_graph_launch per step (H2D of q, raw tokens, gates; the step; D2H of out)",
-                "ms_per_step_csa2_step_host": e2e["direct_ms"]},
+                "ms_per_step": e2e_ms, "steps": e2e["steps"],
+                "api": e2e_api + " (pinned host q, raw tokens, gates and out: q staged by a kernel beside the "
+                                 "index scan, raw tokens and gates read in place by compress, out written by "
+                                 "the merge over the host link)",
+                "ms_per_step_csa2_step_graph_launch": e2e_graph, "ms_per_step_csa2_step_host": e2e_direct},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": clocks,
     }

@@ -522,11 +522,17 @@ size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
   return w.scores + w.n_pool + w.tk + w.cand + w.at;
 }
 
-// Host buffers of a step's inputs, copied in by the step itself (csa2_step_host)
+// Host buffers of a step's inputs (csa2_step_host). A *_dev pointer is the
+// same buffer's device address, set when it is page-locked, mapped and 16-byte
+// aligned: then q is staged by a kernel and compress reads the raw tokens and
+// gates in place; otherwise the copy engines move them.
 struct StepHostIn {
   const void* q = nullptr;
   const void* raw = nullptr;
   const void* gate = nullptr;
+  const void* q_dev = nullptr;
+  const void* raw_dev = nullptr;
+  const void* gate_dev = nullptr;
 };
 
 static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_args* a, const StepHostIn* hin);
@@ -590,13 +596,17 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
     if (je != cudaSuccess && so == CSA2_OK) return cuda_fail(ctx, je, "step: join");
     return so;
   };
-  // Host inputs. Nothing before the attention reads q, so its copy runs on
-  // the copy stream beside compress and the index scan, and every attention
-  // launch waits for it. The raw tokens and gates go on the stream that runs
-  // compress, just before it.
+  // Host inputs. Nothing before the attention reads q, so it moves on the
+  // copy stream beside compress and the index scan (a staging kernel, placed
+  // first so that its CTAs start before the scan's fill the SMs), and every
+  // attention launch waits for it. Compress reads mapped raw tokens and gates
+  // where they lie; others are copied just before it on its stream.
   const size_t q_bytes = hin && hin->q ? (size_t)a->n_query * csa2::kHeads * csa2::kDim * 2 : 0;
-  const size_t raw_bytes = hin && hin->raw ? (size_t)a->n_tokens * csa2::kDim * 2 : 0;
-  const size_t gate_bytes = hin && hin->gate ? (size_t)a->n_tokens * csa2::kDim * 4 : 0;
+  const bool tok_direct = hin && hin->raw_dev && (hin->gate_dev || !hin->gate);
+  const size_t raw_bytes = hin && hin->raw && !tok_direct ? (size_t)a->n_tokens * csa2::kDim * 2 : 0;
+  const size_t gate_bytes = hin && hin->gate && !tok_direct ? (size_t)a->n_tokens * csa2::kDim * 4 : 0;
+  const uint16_t* raw_in = tok_direct ? static_cast<const uint16_t*>(hin->raw_dev) : a->raw;
+  const float* gate_in = tok_direct && hin->gate_dev ? static_cast<const float*>(hin->gate_dev) : a->gate;
   auto wait_q = [&](cudaStream_t sw) -> cudaError_t {
     if (!q_pending) return cudaSuccess;
     const cudaError_t we = cudaStreamWaitEvent(sw, ctx->ev_q, 0);
@@ -612,14 +622,27 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
     return ce;
   };
   if (q_bytes) {
-    cudaError_t e = cudaEventRecord(ctx->ev_copy, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->copy, ctx->ev_copy, 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(const_cast<uint16_t*>(a->q), hin->q, q_bytes, cudaMemcpyHostToDevice, ctx->copy);
-    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_q, ctx->copy);
+    const cudaError_t e = cudaEventRecord(ctx->ev_copy, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step: copy of q");
-    q_pending = true;
   }
+  // enqueued after the launches it must not delay (the scan's, whose CTAs then
+  // hold every SM: the staging runs as they retire, before top-k ends)
+  bool q_staged = false;
+  auto stage_q = [&]() -> cudaError_t {
+    if (!q_bytes || q_staged) return cudaSuccess;
+    q_staged = true;
+    cudaError_t e = cudaStreamWaitEvent(ctx->copy, ctx->ev_copy, 0);
+    if (e == cudaSuccess) {
+      q_pending = true;
+      if (hin->q_dev)
+        e = csa2::launch_stage_copy(ctx->copy, ctx->num_sms, hin->q_dev, const_cast<uint16_t*>(a->q),
+                                    (int64_t)q_bytes, &launches);
+      else
+        e = cudaMemcpyAsync(const_cast<uint16_t*>(a->q), hin->q, q_bytes, cudaMemcpyHostToDevice, ctx->copy);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_q, ctx->copy);
+    return e;
+  };
   // A decode-shaped Full step (at most two closing groups per sequence, the
   // scan in its CUDA-core form) runs compress on the side stream beside the
   // scan of the entries that existed before the step. The scan hands out its
@@ -643,7 +666,7 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
     cudaError_t ce = copy_tokens(cs);
     if (ce != cudaSuccess) return join(cuda_fail(ctx, ce, "step: copy of the raw tokens"));
     ctx->last_launches = 0;
-    s = do_compress(ctx, cs, a->raw, a->gate, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
+    s = do_compress(ctx, cs, raw_in, gate_in, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
                     a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale,
                     a->append != 0, a->state_raw, a->state_gate);
     if (s != CSA2_OK) return join(s);
@@ -667,7 +690,8 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
   if (a->mode == CSA2_MODE_REUSE) {
     // nothing to overlap with: window and selected tiles share one launch
     ctx->last_launches = 0;
-    cudaError_t e = wait_q(st);
+    cudaError_t e = stage_q();
+    if (e == cudaSuccess) e = wait_q(st);
     if (e == cudaSuccess) e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &ctx->last_launches);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
     ctx->last_launches += launches;
@@ -683,7 +707,8 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
                  tail ? a->tok_off : nullptr);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = stage_q();
+  if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: copy of q"));
   if (overlap) {
     e = cudaEventRecord(ctx->ev_tail, ctx->side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ev_tail, 0);
@@ -755,23 +780,32 @@ csa2_status csa2_step_host(csa2_ctx* ctx, void* stream, const csa2_step_args* a,
   // An output buffer in page-locked host memory that the device addresses
   // (16-byte aligned) is written by the step's last launch directly, over the
   // host link; any other is filled by one copy from args->out after the step.
+  auto dev_addr = [](const void* h) -> void* {
+    if (!h) return nullptr;
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, h) != cudaSuccess) {
+      cudaGetLastError();  // an address CUDA does not know: the copy engines move it
+      return nullptr;
+    }
+    if (pa.type != cudaMemoryTypeHost || !pa.devicePointer || (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15))
+      return nullptr;
+    return pa.devicePointer;
+  };
   csa2_step_args da = *a;
   bool direct_out = false;
   if (io->out && q_bytes) {
-    cudaPointerAttributes pa;
-    const cudaError_t pe = cudaPointerGetAttributes(&pa, io->out);
-    if (pe == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer != nullptr &&
-        (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15) == 0) {
-      da.out = static_cast<uint16_t*>(pa.devicePointer);
+    if (void* d = dev_addr(io->out)) {
+      da.out = static_cast<uint16_t*>(d);
       direct_out = true;
-    } else if (pe != cudaSuccess) {
-      cudaGetLastError();  // an address CUDA does not know: take the copy
     }
   }
   StepHostIn hin;
   hin.q = io->q;
   hin.raw = io->raw;
   hin.gate = io->gate;
+  hin.q_dev = dev_addr(io->q);
+  hin.raw_dev = dev_addr(io->raw);
+  hin.gate_dev = dev_addr(io->gate);
   csa2_status s = step_impl(ctx, st, &da, &hin);
   if (s != CSA2_OK) return s;
   if (io->out && q_bytes && !direct_out) {

@@ -455,4 +455,41 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   return e;
 }
 
+// ---------------------------------------------------------------------------
+// Staging copy of a step input that sits in page-locked host memory the device
+// can address: SMs read it over the host link and write it to device memory.
+// The copy engines are starved while the index scan holds the memory system,
+// loads issued by SMs are not. Eight 16-byte loads in flight per thread.
+constexpr int kStageThreads = 256;
+constexpr int kStageUnroll = 8;
+
+__global__ void __launch_bounds__(kStageThreads) stage_copy_kernel(const uint4* __restrict__ src,
+                                                                   uint4* __restrict__ dst, int64_t n16) {
+  const int64_t stride = (int64_t)gridDim.x * kStageThreads;
+  int64_t i = (int64_t)blockIdx.x * kStageThreads + threadIdx.x;
+  for (; i + (kStageUnroll - 1) * stride < n16; i += kStageUnroll * stride) {
+    uint4 v[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) dst[i + u * stride] = v[u];
+  }
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+
+cudaError_t launch_stage_copy(cudaStream_t st, int num_sms, const void* src, void* dst, int64_t bytes,
+                              int* n_launch) {
+  const int64_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  // about 4 KiB per thread-round: enough loads in flight to cover the link's
+  // latency, few enough CTAs to leave the index scan its SMs
+  const int64_t want = (n16 + (int64_t)kStageThreads * kStageUnroll - 1) / ((int64_t)kStageThreads * kStageUnroll);
+  const int64_t cap = num_sms / 4 > 0 ? num_sms / 4 : 1;
+  const dim3 grid((unsigned)(want < 1 ? 1 : (want < cap ? want : cap)));
+  stage_copy_kernel<<<grid, kStageThreads, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) *n_launch += 1;
+  return e;
+}
+
 }  // namespace csa2

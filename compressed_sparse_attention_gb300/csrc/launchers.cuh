@@ -50,6 +50,10 @@ struct AppendArgs {
 };
 // n_groups: the closing groups (whole-group form) or a bound of them (append
 // form: n_tokens / m + n_seq); n_launch counts the launches made
+// bytes (a multiple of 16, both pointers 16-byte aligned) from device-addressable
+// host memory to device memory, by a few CTAs
+cudaError_t launch_stage_copy(cudaStream_t st, int num_sms, const void* src, void* dst, int64_t bytes,
+                              int* n_launch);
 cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* raw, const float* gate, int m,
                             int n_seq, const int64_t* tok_off, const int64_t* first_pos, const int64_t* pool_off,
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,

@@ -400,21 +400,24 @@ size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* args);
 
 /* csa2_step_host: csa2_step with the step's inputs and output in host memory
- * (pinned, so that the copies are asynchronous). The device buffers in args
- * are the staging buffers; the caches stay resident.
- *   - io->q (n_query x 64 x 512 bf16) is copied into args->q on the
- *     context's copy stream, which starts after the work already on `stream`
- *     and runs beside compress and the index scan; every attention launch of
- *     the step waits for it (nothing before the attention reads q).
- *   - io->raw (n_tokens x 512 bf16) and io->gate (n_tokens x 512 fp32) are
- *     copied into args->raw and args->gate on the stream that runs compress,
- *     just before it.
- *   - io->out (n_query x 64 x 512 bf16): when it is page-locked host memory
- *     that the device can address (cudaHostAlloc, cudaMallocHost, or
- *     cudaHostRegister with mapping) and 16-byte aligned, the step's last
- *     launch writes the output into it directly over the host link and
- *     args->out is left untouched. Otherwise the step writes args->out and one
- *     copy on `stream` brings it into io->out.
+ * (pinned, so that the transfers are asynchronous). The device buffers in
+ * args are the staging buffers; the caches stay resident. A host buffer is
+ * "mapped" below when it is page-locked memory that the device can address
+ * (cudaHostAlloc, cudaMallocHost, or cudaHostRegister with mapping) and
+ * 16-byte aligned.
+ *   - io->q (n_query x 64 x 512 bf16) lands in args->q on the context's copy
+ *     stream, which starts after the work already on `stream` and runs beside
+ *     compress and the index scan: a mapped q by a small staging kernel (SM
+ *     loads over the host link), any other by a copy-engine copy. Every
+ *     attention launch of the step waits for it; nothing before reads q.
+ *   - io->raw (n_tokens x 512 bf16) and io->gate (n_tokens x 512 fp32): when
+ *     both are mapped, compress reads them where they lie and args->raw and
+ *     args->gate are left untouched; otherwise they are copied there on the
+ *     stream that runs compress, just before it.
+ *   - io->out (n_query x 64 x 512 bf16): when mapped, the step's last launch
+ *     writes the output into it directly over the host link and args->out is
+ *     left untouched. Otherwise the step writes args->out and one copy on
+ *     `stream` brings it into io->out.
  * A NULL host pointer skips that transfer. Returns after enqueueing; io->out
  * is valid once `stream` has completed, which orders after all of the step's
  * streams. Errors are those of csa2_step, plus CSA2_ERR_INVALID_ARG for a

@@ -69,11 +69,11 @@ def test_step_two_queries_per_sequence(m):
 
 @pytest.mark.parametrize("mode", ["full", "reindex", "reuse"])
 def test_step_host_equals_step(mode):
-    """csa2_step_host gives the bits csa2_step gives: q copied in on the copy
-    stream beside the scan, the raw tokens and gates before compress, and the
-    output either written straight into pinned host memory by the step's last
-    launch or, for pageable host memory, copied back from the staging buffer.
-    Also captured with its copies into a graph and replayed."""
+    """csa2_step_host gives the bits csa2_step gives. Pinned host buffers:
+    q staged by a kernel on the copy stream beside the scan, the raw tokens and
+    gates read in place by compress, the output written straight into host
+    memory by the step's last launch. Pageable host buffers: copy-engine copies
+    through the staging buffers. Also captured into a graph and replayed."""
     require_gpu()
     from compressed_sparse_attention_gb300 import binding
     code = {"full": binding.MODE_FULL, "reindex": binding.MODE_REINDEX, "reuse": binding.MODE_REUSE}[mode]
@@ -97,7 +97,7 @@ def test_step_host_equals_step(mode):
     torch.cuda.synchronize()
     ref = out_dev.cpu()
     sel = idx.clone()
-    sq, sraw, sgate = torch.empty_like(i["q"]), torch.empty_like(i["raw"]), torch.empty_like(i["gate"])
+    sq, sraw, sgate = torch.zeros_like(i["q"]), torch.zeros_like(i["raw"]), torch.zeros_like(i["gate"])
     sout = torch.zeros_like(out_dev)
     prep = ctx.prepare_step(code, wl.n_seq, max_vis, q=sq, raw=sraw, gate=sgate, out=sout, **common)
     hq, hraw, hgate = (t.cpu().pin_memory() for t in (i["q"], i["raw"], i["gate"]))
@@ -107,14 +107,19 @@ def test_step_host_equals_step(mode):
     assert ctx.check() == (0, 0)
     assert torch.equal(hout, ref)
     assert torch.equal(idx, sel)
-    assert torch.equal(sq, i["q"]) and torch.equal(sraw, i["raw"]) and torch.equal(sgate, i["gate"])
+    assert torch.equal(sq, i["q"]), "q is staged into the device buffer"
+    assert float(sraw.float().abs().sum()) == 0.0 and float(sgate.abs().sum()) == 0.0, \
+        "pinned raw tokens and gates are read in place, not staged"
     assert float(sout.float().abs().sum()) == 0.0, "a pinned output is written directly, not staged"
-    # pageable host output: the step writes the staging buffer, one copy brings it back
+    # pageable host buffers: copy-engine copies through the staging buffers
+    pq, praw, pgate = (t.cpu().clone() for t in (i["q"], i["raw"], i["gate"]))
+    sq.zero_()
     hpage = torch.zeros(out_dev.shape, dtype=out_dev.dtype)
-    prep.run_host(q=hq, raw=hraw, gate=hgate, out=hpage)
+    prep.run_host(q=pq, raw=praw, gate=pgate, out=hpage)
     torch.cuda.synchronize()
     assert ctx.check() == (0, 0)
-    assert torch.equal(hpage, ref) and torch.equal(sout.cpu(), ref)
+    assert torch.equal(hpage, ref) and torch.equal(sout.cpu(), ref) and torch.equal(idx, sel)
+    assert torch.equal(sq, i["q"]) and torch.equal(sraw, i["raw"]) and torch.equal(sgate, i["gate"])
     # the same step captured with its copies and replayed
     hout2 = torch.zeros_like(hout).pin_memory()
     graph = prep.host_graph(q=hq, raw=hraw, gate=hgate, out=hout2)
