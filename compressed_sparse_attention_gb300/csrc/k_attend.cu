@@ -28,6 +28,7 @@ constexpr int kTileRows = 128;
 // output dims, 32 (w % 4) .. +31) and takes heads 32 (w / 4) .. +31 of them
 constexpr int kAttWarps = 8;
 constexpr int kAttThreads = 32 * kAttWarps;
+constexpr int kKvGroups = 4;  // bf16 tiles land in 4 groups of two 64-channel blocks
 constexpr uint32_t SM_Q = 0;                          // [9 dim blocks][64 heads][128 B]; block 8 = rope residual
 constexpr uint32_t SM_KV = 73728;                     // [8 dim blocks][128 rows][128 B]
 constexpr uint32_t SM_P = SM_KV + 131072;             // [128 rows][128 B]  (64 heads, bf16)
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       }
     }
   }
+  cp_async_commit();  // Q's group lands before any KV group of the first tile
   const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
   const int tile_end = q_ok ? tile_cap : tile_begin;
   if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
@@ -199,19 +201,25 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     // ---- gather the tile's rows into the swizzled KV operand
     const void* kvsrc = (tile == 0) ? p.win_kv : p.pool_kv;
     if constexpr (KVF == 0) {
+      // four commit groups, one per pair of 64-channel blocks (16 chunks of
+      // 16 B per row): the QK^T steps of a pair start once its rows land. A
+      // half warp copies one row's 256 B of a pair.
       const uint16_t* kv = reinterpret_cast<const uint16_t*>(kvsrc);
-      for (int r = warp; r < kTileRows; r += kAttWarps) {
-        const int64_t src = rows[r];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = lane + 32 * cc;
+      for (int g = 0; g < kKvGroups; ++g) {
+#pragma unroll
+        for (int u = 0; u < kTileRows * 16 / kAttThreads; ++u) {
+          const int i = tid + kAttThreads * u;
+          const int r = i >> 4;
+          const int c = 16 * g + (i & 15);
+          const int64_t src = rows[r];
           const uint32_t dst = base_s + SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
                                ((uint32_t)((c & 7) ^ (r & 7)) << 4);
-          const uint16_t* g = src >= 0 ? kv + src * kDim + 8 * c : kv;
-          cp_async16(dst, g, src >= 0 ? 16u : 0u);
+          const uint16_t* gp = src >= 0 ? kv + src * kDim + 8 * c : kv;
+          cp_async16(dst, gp, src >= 0 ? 16u : 0u);
         }
+        cp_async_commit();
       }
-      cp_async_wait_all();
     } else if (KVF == 2 && tile != 0) {
       // fp4 pool rows: 256 B of E2M1 codes + 32 e4m3 scales; lane l converts
       // channels 16l .. 16l+15 (8 code bytes, scale l), 8 rows' loads in flight
@@ -294,53 +302,62 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         }
       }
     }
-    cp_async_wait_all();
-    if (q_pending) {
-      q_pending = false;
-      if (p.rp.pairs > 0) {
-        __syncthreads();
-        // rotated q = hi + lo, both bf16: the tensor cores see the rotation to
-        // ~2^-16 relative instead of one bf16 rounding. Thread: head tid/4,
-        // chunks 56 + 2*(tid&3) .. +1 (the last 64 channels).
-        const int h = tid >> 2;
-        const int first_rope = kDim - 2 * p.rp.pairs;
+    // bf16 tiles arrive in kKvGroups commit groups and their QK^T steps are
+    // issued group by group; the converting gathers above are complete
+    constexpr int n_groups = (KVF == 0) ? kKvGroups : 1;
+    const int n_ks = p.rp.pairs > 0 ? 36 : 32;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = 56 + 2 * (tid & 3) + u;
-          const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
-          uint4* hi_p = reinterpret_cast<uint4*>(sm + SM_Q + 7u * 8192u + inblk);
-          const uint4 v = *hi_p;
-          uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
+    for (int g = 0; g < n_groups; ++g) {
+      if constexpr (KVF == 0) cp_async_wait_pending(n_groups - 1 - g);
+      else cp_async_wait_all();
+      if (g == 0 && q_pending) {
+        q_pending = false;
+        if (p.rp.pairs > 0) {
+          __syncthreads();
+          // rotated q = hi + lo, both bf16: the tensor cores see the rotation to
+          // ~2^-16 relative instead of one bf16 rounding. Thread: head tid/4,
+          // chunks 56 + 2*(tid&3) .. +1 (the last 64 channels).
+          const int h = tid >> 2;
+          const int first_rope = kDim - 2 * p.rp.pairs;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 cs2 = rope_tab[(8 * c + 2 * k - first_rope) >> 1];
-            const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
-            const float y0 = x0 * cs2.x - x1 * cs2.y, y1 = x0 * cs2.y + x1 * cs2.x;
-            w[k] = pack_bf16(y0, y1);
-            lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
+          for (int u = 0; u < 2; ++u) {
+            const int c = 56 + 2 * (tid & 3) + u;
+            const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+            uint4* hi_p = reinterpret_cast<uint4*>(sm + SM_Q + 7u * 8192u + inblk);
+            const uint4 v = *hi_p;
+            uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 cs2 = rope_tab[(8 * c + 2 * k - first_rope) >> 1];
+              const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
+              const float y0 = x0 * cs2.x - x1 * cs2.y, y1 = x0 * cs2.y + x1 * cs2.x;
+              w[k] = pack_bf16(y0, y1);
+              lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
+            }
+            *hi_p = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
-          *hi_p = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    // ---- S^T = KV . Q^T
-    if (tid == 0) {
-      tc_fence_after();
-      // K steps 0..31 cover the 8 channel blocks; 32..35 add the rope residual
-      // block of q against the KV's last channel block (the rope channels)
-      const int n_ks = p.rp.pairs > 0 ? 36 : 32;
+      fence_proxy_async_smem();
+      __syncthreads();
+      // ---- S^T = KV . Q^T: K steps 0..31 cover the 8 channel blocks (this
+      // group's share of them); 32..35 add the rope residual block of q
+      // against the KV's last channel block (the rope channels)
+      if (tid == 0) {
+        tc_fence_after();
+        const int ks0 = g * 32 / n_groups;
+        const int ks1 = (g == n_groups - 1) ? n_ks : (g + 1) * 32 / n_groups;
 #pragma unroll 4
-      for (int ks = 0; ks < n_ks; ++ks) {
-        const uint32_t koff = (uint32_t)(ks & 3) * 32u;
-        const uint32_t kblk = ks < 32 ? (uint32_t)(ks >> 2) : 7u;
-        const uint64_t ad = sdesc_sw128(base_s + SM_KV + kblk * 16384u + koff, 16u, 1024u);
-        const uint64_t bd = sdesc_sw128(base_s + SM_Q + (uint32_t)(ks >> 2) * 8192u + koff, 16u, 1024u);
-        mma_bf16_ss(tmem_s, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+        for (int ks = ks0; ks < ks1; ++ks) {
+          const uint32_t koff = (uint32_t)(ks & 3) * 32u;
+          const uint32_t kblk = ks < 32 ? (uint32_t)(ks >> 2) : 7u;
+          const uint64_t ad = sdesc_sw128(base_s + SM_KV + kblk * 16384u + koff, 16u, 1024u);
+          const uint64_t bd = sdesc_sw128(base_s + SM_Q + (uint32_t)(ks >> 2) * 8192u + koff, 16u, 1024u);
+          mma_bf16_ss(tmem_s, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+        }
+        if (g == n_groups - 1) mma_commit(mbar);
       }
-      mma_commit(mbar);
     }
     bool ok = mbar_wait(mbar, phase, p.flags);
     phase ^= 1u;
