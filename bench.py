@@ -442,6 +442,87 @@ def run_hier_extra(args, device):
             "reindex_speedup": ms_reindex / ms_pool}
 
 
+def reuse_bytes(wl):
+    """Minimal HBM bytes of one Reuse layer: the borrowed selection, the
+    gathered window and selected rows once, q in and the output out."""
+    wrow, prow, _ = row_bytes(wl)
+    total = 0
+    for b in range(wl.n_seq):
+        n = wl.ctx_len[b]
+        for i in range(wl.n_query_per_seq):
+            t = n - wl.n_query_per_seq + i
+            nv = (t + 1) // wl.m
+            total += min(wl.window, t + 1) * wrow + min(wl.topk, nv) * prow
+            total += wl.topk * 4 + wl.n_heads * wl.head_dim * 2 * 2
+    return total
+
+
+def run_mixed_extra(args, device, hbm):
+    """The mixed serving batch: 64 decode sequences of log-uniform length
+    1K..256K, compress ratio 1. One Reindex layer scores every visible entry
+    and selects; three Reuse layers, each with its own q, window and sink,
+    attend over the borrowed pool and selection. The four layers are one CUDA
+    graph, timed back to back (the scan's 0.8 GB evicts L2 between groups)."""
+    from compressed_sparse_attention_gb300 import binding
+    wl = PRESETS["mixed_reuse_b64"]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads)
+    base = Copy(ctx, wl, 0, device)
+    shared = {k: base.inp[k] for k in ("n_vis", "pool_kv", "pool_off", "q_idx", "w_heads", "idx_keys")}
+    layers = []
+    for layer in (1, 2, 3):
+        li = make_inputs(wl.scaled(seed=wl.seed), device, layer=layer, with_compress=False)
+        layers.append((li, torch.empty_like(base.out)))
+    stream = torch.cuda.Stream(device=device)
+
+    def reindex():
+        base.step_as(ctx, binding.MODE_REINDEX)
+
+    def reuse(li, out):
+        ctx.step(binding.MODE_REUSE, wl.n_seq, base.max_vis, q=li["q"], q_pos=li["q_pos"], seq_of_q=li["seq_of_q"],
+                 sink=li["sink"], win_kv=li["win_kv"], win_off=li["win_off"], topk_idx=base.idx, out=out,
+                 workspace=base.ws, **shared)
+
+    def group():
+        reindex()
+        for li, out in layers:
+            reuse(li, out)
+
+    reps = max(5, min(args.steps, 100))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ms_group = timed(group)
+    ms_reindex = timed(reindex)
+    ms_reuse = timed(lambda: reuse(*layers[0]))
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the mixed workload")
+    b_reindex = algorithmic_bytes(wl, has_compress=False)
+    b_reuse = reuse_bytes(wl)
+    b_group = b_reindex + 3 * b_reuse
+    return {"workload": wl.name, "layers": "1 Reindex + 3 Reuse", "entries": int(base.inp["n_vis"].sum()),
+            "ms_per_group": ms_group, "layer_tokens_per_s": 4 * wl.n_query / (ms_group / 1000.0),
+            "ms_reindex_layer": ms_reindex, "ms_reuse_layer": ms_reuse,
+            "group_algorithmic_bytes": b_group, "hbm_gbs": b_group / (ms_group / 1000.0) / 1e9,
+            "hbm_frac": b_group / (ms_group / 1000.0) / 1e9 / hbm}
+
+
 def run_e2e(args, ctx, copies, stream, device, wl):
     """The step through its host-buffer entry points, with the step's inputs
     (q, and the closing groups' raw tokens and gates) and its output in pinned
@@ -686,6 +767,10 @@ def main():
             line["extra_prefill"] = run_prefill_extra(args, device, bf16_burst)
         except Exception as ex:  # reported, never silently dropped
             line["extra_prefill"] = {"error": repr(ex)[:300]}
+        try:
+            line["extra_mixed_reuse"] = run_mixed_extra(args, device, hbm)
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_mixed_reuse"] = {"error": repr(ex)[:300]}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
         print(json.dumps(line))
