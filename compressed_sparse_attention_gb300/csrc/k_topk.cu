@@ -4,9 +4,11 @@
 // "DeepSeek-V4.1-Flash", "The CSA2 attention layers").
 //
 // Integer work on the scores' order-preserving bit patterns. Rows of up to
-// 262,144 scores take one launch: a thread-block cluster per query running an
-// MSD radix select over shared memory (described above the kernel below).
-// Longer rows take three launches through global memory:
+// 16,384 scores take one launch of one CTA per query. Rows of up to 262,144
+// scores take one launch of a thread-block cluster per query running an MSD
+// radix select over shared memory (described above the kernel below), when
+// all the queries' clusters fit on the GPU at once. Longer rows, and more
+// queries than that, take three launches through global memory:
 //   1. hist:   a 4096-bin histogram of the top 12 bits of each score's key
 //              (per query, over all CTAs of the row);
 //   2. filter: every CTA finds the bin that holds the k-th largest key and
@@ -24,6 +26,7 @@ namespace csa2 {
 
 constexpr int kHistBins = 4096;
 constexpr int kTopkChunk = 4096;   // scores per CTA in hist / filter
+constexpr int kTopkBatch = 8;      // loads in flight per thread there
 constexpr int kSelCap = 8192;      // candidates held in shared memory by select
 constexpr int kMaxTopk = 2048;
 
@@ -40,12 +43,20 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float* __restrict_
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const float* row = scores + (int64_t)q * ld;
-  for (int i = threadIdx.x; i < kTopkChunk; i += blockDim.x) {
-    const int64_t j = c0 + i;
-    const bool ok = j < nv;
-    const uint32_t bin = ok ? hist_bin(score_key(row[j])) : 0xFFFFFFFFu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (ok && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  const int len = (int)min((int64_t)kTopkChunk, nv - c0);
+  for (int b0 = 0; b0 < len; b0 += 256 * kTopkBatch) {
+    float v[kTopkBatch];
+#pragma unroll
+    for (int u = 0; u < kTopkBatch; ++u) {
+      const int i = b0 + u * 256 + (int)threadIdx.x;
+      v[u] = i < len ? row[c0 + i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kTopkBatch; ++u) {
+      // plain shared-memory atomics: aggregating equal bins across the warp
+      // first (match) measured slower, even though the bins are few and hot
+      if (b0 + u * 256 + (int)threadIdx.x < len) atomicAdd(&h[hist_bin(score_key(v[u]))], 1u);
+    }
   }
   __syncthreads();
   uint32_t* gh = hist + (int64_t)q * kHistBins;
@@ -105,22 +116,29 @@ __global__ void __launch_bounds__(256) topk_filter_kernel(const float* __restric
   const float* row = scores + (int64_t)q * ld;
   unsigned long long* out = cand + (int64_t)q * cand_ld;
   const int lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kTopkChunk; i += blockDim.x) {
-    const int64_t j = c0 + i;
-    uint32_t key = 0;
-    bool take = false;
-    if (j < nv) {
-      key = score_key(row[j]);
-      take = hist_bin(key) >= bstar;
+  const int len = (int)min((int64_t)kTopkChunk, nv - c0);
+  for (int b0 = 0; b0 < len; b0 += 256 * kTopkBatch) {
+    float v[kTopkBatch];
+#pragma unroll
+    for (int u = 0; u < kTopkBatch; ++u) {
+      const int i = b0 + u * 256 + (int)threadIdx.x;
+      v[u] = i < len ? row[c0 + i] : 0.f;
     }
-    const uint32_t m = __ballot_sync(0xffffffffu, take);
-    if (m) {
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&cnt[q], (uint32_t)__popc(m));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (take) {
-        const uint32_t slot = base + __popc(m & ((1u << lane) - 1u));
-        out[slot] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+#pragma unroll
+    for (int u = 0; u < kTopkBatch; ++u) {
+      const int i = b0 + u * 256 + (int)threadIdx.x;
+      const uint32_t key = score_key(v[u]);
+      const bool take = i < len && hist_bin(key) >= bstar;
+      const uint32_t m = __ballot_sync(0xffffffffu, take);
+      if (m) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&cnt[q], (uint32_t)__popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (take) {
+          const uint32_t slot = base + __popc(m & ((1u << lane) - 1u));
+          const uint32_t j = (uint32_t)(c0 + i);
+          out[slot] = ((unsigned long long)key << 32) | (unsigned long long)(0xFFFFFFFFu - j);
+        }
       }
     }
   }
@@ -135,15 +153,9 @@ __device__ unsigned long long radix_select64(Src src, uint32_t n, uint32_t need,
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist_s[i] = 0;
     __syncthreads();
-    // warp-aggregated: near the threshold most candidates share the high
-    // digits, so one atomic per distinct digit per warp instead of one each
-    const uint32_t n_pad = (n + 31u) & ~31u;
-    for (uint32_t i = threadIdx.x; i < n_pad; i += blockDim.x) {
-      const unsigned long long v = i < n ? src(i) : 0ull;
-      const bool ok = i < n && (v & mask) == prefix;
-      const uint32_t dig = ok ? (uint32_t)((v >> shift) & 0xFF) : 0xFFFFFFFFu;
-      const uint32_t peers = __match_any_sync(0xffffffffu, dig);
-      if (ok && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist_s[dig], (uint32_t)__popc(peers));
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long v = src(i);
+      if ((v & mask) == prefix) atomicAdd(&hist_s[(uint32_t)((v >> shift) & 0xFF)], 1u);
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -167,6 +179,7 @@ __device__ unsigned long long radix_select64(Src src, uint32_t n, uint32_t need,
           if (run + loc[u] >= remaining) {
             bcast[0] = (unsigned long long)(255 - 8 * threadIdx.x - u);
             bcast[1] = (unsigned long long)(remaining - run);
+            bcast[2] = (unsigned long long)loc[u];
             break;
           }
           run += loc[u];
@@ -176,9 +189,13 @@ __device__ unsigned long long radix_select64(Src src, uint32_t n, uint32_t need,
     __syncthreads();
     const unsigned long long d = bcast[0];
     remaining = (uint32_t)bcast[1];
+    const bool whole_bin = bcast[2] == (unsigned long long)remaining;
     prefix |= d << shift;
     mask |= 0xFFull << shift;
     __syncthreads();
+    // every value in the chosen bin is needed: the threshold is the bin's
+    // smallest possible value, whatever the lower digits
+    if (whole_bin) break;
   }
   return prefix;
 }
@@ -191,7 +208,7 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const int32_t* __rest
   unsigned long long* cs = reinterpret_cast<unsigned long long*>(sm_raw);  // [kSelCap]
   uint32_t* sel = reinterpret_cast<uint32_t*>(cs + kSelCap);               // [kMaxTopk]
   __shared__ uint32_t hist_s[256];
-  __shared__ unsigned long long bcast[2];
+  __shared__ unsigned long long bcast[3];
   __shared__ uint32_t n_sel;
   const int q = blockIdx.x;
   const int nv = (int)min((int64_t)n_vis[q], max_vis);
@@ -220,26 +237,17 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const int32_t* __rest
   }
   __syncthreads();
   const uint32_t ns = min(n_sel, (uint32_t)kMaxTopk);
-  uint32_t pw = 1;
-  while (pw < ns) pw <<= 1;
-  for (uint32_t i = ns + threadIdx.x; i < pw; i += blockDim.x) sel[i] = 0xFFFFFFFFu;
-  __syncthreads();
-  // bitonic sort ascending
-  for (uint32_t size = 2; size <= pw; size <<= 1) {
-    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (uint32_t i = threadIdx.x; i < pw; i += blockDim.x) {
-        const uint32_t jx = i ^ stride;
-        if (jx > i) {
-          const bool up = (i & size) == 0;
-          const uint32_t a = sel[i], b = sel[jx];
-          if ((a > b) == up) { sel[i] = b; sel[jx] = a; }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  // ascending order: the chosen indices are distinct, so each one's output
+  // slot is the number of chosen indices below it (the reads of sel[j] are
+  // shared-memory broadcasts across the warp)
   int32_t* o = out_idx + (int64_t)q * k;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) o[i] = (uint32_t)i < ns ? (int32_t)sel[i] : -1;
+  for (uint32_t i = threadIdx.x; i < ns; i += blockDim.x) {
+    const uint32_t v = sel[i];
+    uint32_t r = 0;
+    for (uint32_t jx = 0; jx < ns; ++jx) r += sel[jx] < v ? 1u : 0u;
+    if (r < (uint32_t)k) o[r] = (int32_t)v;
+  }
+  for (int i = (int)ns + threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
 }
 
 namespace cg = cooperative_groups;
@@ -1104,6 +1112,10 @@ static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, 
     cudaGetLastError();  // cluster shape not schedulable here: the caller takes the global-memory path
     return cudaSuccess;
   }
+  // More queries than clusters resident at once: every query, however short,
+  // would hold csize SMs for a whole selection, wave after wave. The
+  // global-memory path spreads the work by each row's own length instead.
+  if (n_query > max_clusters) return cudaSuccess;
   e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<PER>, scores, ld, n_vis, max_vis, k, out_idx);
   if (e != cudaSuccess) return e;
   *launched = true;

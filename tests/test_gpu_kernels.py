@@ -306,6 +306,31 @@ def test_topk_bit_exact(n, tie_levels, k):
         assert np.array_equal(got[qi], ref), f"query {qi}"
 
 
+@pytest.mark.parametrize("tie_levels", [0, 2])
+def test_topk_many_queries_mixed_lengths(tie_levels):
+    """More queries than the GPU holds top-k clusters for at once, with row
+    lengths spread log-uniformly from 100 to 262,144 (and the edges: empty,
+    k - 1, exactly the one-CTA limit and one past it): the selections are
+    bit-exact against the oracle's, whichever path takes them."""
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    Q, n, k = 48, 262144, 512
+    sc = make_topk_scores(Q, n, seed=4242 + tie_levels, tie_levels=tie_levels)
+    rng = np.random.default_rng(7)
+    lens = np.exp(rng.uniform(np.log(100), np.log(n), Q)).astype(np.int32)
+    lens[:6] = [n, 0, k - 1, 16384, 16385, 100]
+    scores = sc.to(DEV)
+    out = torch.empty((Q, k), dtype=torch.int32, device=DEV)
+    ws = binding.workspace(ctx.topk_workspace_size(Q, n), DEV)
+    ctx.topk(scores, torch.from_numpy(lens).to(DEV), n, k, out, ws)
+    assert ctx.check()[0] == 0
+    got = out.cpu().numpy()
+    s = sc.numpy()
+    for qi in range(Q):
+        ref = O.topk_select(s[qi, :int(lens[qi])], k)
+        assert np.array_equal(got[qi], ref), f"query {qi} (n_vis {lens[qi]})"
+
+
 # ----------------------------------------------------------------------------- compressor
 
 @pytest.mark.parametrize("m", [1, 2, 4])
