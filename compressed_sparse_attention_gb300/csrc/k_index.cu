@@ -58,18 +58,40 @@ __device__ __forceinline__ int64_t idx_row(const IdxArgs& a, int q, int64_t p) {
 __device__ __forceinline__ int64_t idx_static_items(int64_t n_items) {
   return (n_items / gridDim.x) * 3 / 4 * gridDim.x;  // the strided phase covers items [0, this)
 }
+// An item whose chunk starts at or past its query's n_vis holds nothing to
+// score (entry 0's item still runs: it sets the query's flags and n_pool).
+// n_vis bounds every narrower range the scan uses, so the test is safe.
+__device__ __forceinline__ bool idx_item_empty(const IdxArgs& a, int q, int64_t j0) {
+  return j0 > 0 && j0 >= (int64_t)__ldg(a.n_vis + q);
+}
+
 struct IdxTickets {
   unsigned long long* s;  // shared [2]
   unsigned long long* work;
   unsigned long long base;  // first ticketed item
+  const IdxArgs* a;
+  int64_t chunk;            // keys an item
   int par = 0;
+  // the next ticket. One that lands in a query's empty tail means the rest of
+  // that tail is empty too: the counter jumps to the next query's first item
+  // (the counter only moves forward, so no item with entries is skipped)
+  __device__ unsigned long long draw() {
+    const unsigned long long n_items = (unsigned long long)a->n_chunks * (unsigned long long)a->n_query;
+    for (;;) {
+      const unsigned long long it = base + atomicAdd(work, 1ull);
+      if (it >= n_items) return it;
+      const int q = (int)(it / (unsigned long long)a->n_chunks);
+      if (!idx_item_empty(*a, q, (int64_t)(it % (unsigned long long)a->n_chunks) * chunk)) return it;
+      atomicMax(work, (unsigned long long)(q + 1) * (unsigned long long)a->n_chunks - base);
+    }
+  }
   __device__ void start() {
-    if (threadIdx.x == 0) s[0] = base + atomicAdd(work, 1ull);
+    if (threadIdx.x == 0) s[0] = draw();
     __syncthreads();
   }
   __device__ unsigned long long cur() const { return s[par]; }
   __device__ void prefetch() {
-    if (threadIdx.x == 0) s[par ^ 1] = base + atomicAdd(work, 1ull);
+    if (threadIdx.x == 0) s[par ^ 1] = draw();
   }
   __device__ void advance() {
     __syncthreads();
@@ -108,8 +130,11 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
     const int q = (int)(item / a.n_chunks);
     const int64_t j0 = (item % a.n_chunks) * kIdxChunk;
     if (q != cur_q) {
-      cur_q = q;
+      // an empty item of another query leaves the current one in place (the
+      // two loads go out together)
       const int b = a.seq_of_q[q];
+      if (idx_item_empty(a, q, j0)) return;
+      cur_q = q;
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
         if (threadIdx.x == 0 && j0 == 0) {
@@ -180,7 +205,7 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, &a, (int64_t)kIdxChunk};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
@@ -289,8 +314,11 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
     const int q = (int)(item / a.n_chunks);
     const int64_t j0 = (item % a.n_chunks) * CH;
     if (q != cur_q) {
-      cur_q = q;
+      // an empty item of another query leaves the current one in place (the
+      // two loads go out together)
       const int b = a.seq_of_q[q];
+      if (idx_item_empty(a, q, j0)) return;
+      cur_q = q;
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
         if (threadIdx.x == 0 && j0 == 0) {
@@ -379,7 +407,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, &a, (int64_t)CH};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
