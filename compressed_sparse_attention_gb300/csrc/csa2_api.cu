@@ -433,7 +433,10 @@ csa2_status csa2_topk_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const f
 
 size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query) {
   if (!ctx || n_query < 0) return 0;
-  return csa2::attend_workspace_bytes(n_query, csa2::attend_plan(n_query, ctx->cfg.topk, true, ctx->num_sms));
+  // the step's split plan or the single-launch plan, whichever needs more
+  return std::max(
+      csa2::attend_workspace_bytes(n_query, csa2::attend_plan(n_query, ctx->cfg.topk, true, ctx->num_sms)),
+      csa2::attend_workspace_bytes(n_query, csa2::attend_plan_single(n_query, ctx->cfg.topk, true, ctx->num_sms)));
 }
 
 // validates the attend arguments and fills the kernel parameters

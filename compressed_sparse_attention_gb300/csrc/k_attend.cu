@@ -660,6 +660,24 @@ int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTi
 // so that all their CTAs fit in one wave, and a merge combines the partials.
 // With many queries (prefill) one CTA per query runs every tile and writes the
 // output directly.
+// One launch for the window and the selected tiles (Reuse steps, and
+// csa2_attend): at most one wave of CTAs (one a SM), each query's tiles split
+// evenly over floor(num_sms / n_query) CTAs.
+AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms) {
+  AttendPlan pl{};
+  pl.n_tiles = attend_num_tiles(topk, has_idx);
+  if (n_query < 1) n_query = 1;
+  pl.split_window = 0;
+  int ns = num_sms / n_query;
+  if (ns > pl.n_tiles) ns = pl.n_tiles;
+  if (ns > 8) ns = 8;
+  if (ns < 1) ns = 1;
+  pl.tps = (pl.n_tiles + ns - 1) / ns;
+  pl.ns = (pl.n_tiles + pl.tps - 1) / pl.tps;
+  pl.n_slots = pl.ns > 1 ? pl.ns : 0;
+  return pl;
+}
+
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
   AttendPlan pl{};
   pl.n_tiles = attend_num_tiles(topk, has_idx);
@@ -673,14 +691,7 @@ AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
     pl.ns = (pl.n_tiles - 1 + pl.tps - 1) / pl.tps;
     pl.n_slots = 1 + pl.ns;
   } else {
-    pl.split_window = 0;
-    int ns = (num_sms + n_query - 1) / n_query;
-    if (ns > pl.n_tiles) ns = pl.n_tiles;
-    if (ns > 8) ns = 8;
-    if (ns < 1) ns = 1;
-    pl.tps = (pl.n_tiles + ns - 1) / ns;
-    pl.ns = (pl.n_tiles + pl.tps - 1) / pl.tps;
-    pl.n_slots = pl.ns > 1 ? pl.ns : 0;
+    pl = attend_plan_single(n_query, topk, has_idx, num_sms);
   }
   return pl;
 }
@@ -764,25 +775,9 @@ cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPla
 }
 
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch) {
-  const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
-  cudaError_t e;
-  if (pl.split_window) {
-    // on one stream the window tile and the selected tiles share one launch:
-    // split 0 of each query takes the window, splits 1.. the selected tiles
-    AttendParams a = p;
-    attach_ws(a, pl, ws);
-    a.n_tiles = pl.n_tiles;
-    a.tile_base = 0;
-    a.tile_count = pl.n_tiles;
-    a.n_split = 1 + pl.ns;
-    a.tiles_per_split = pl.tps;
-    a.lead_single = 1;
-    a.slot_base = 0;
-    a.direct = 0;
-    e = launch_tiles(st, kv_fmt, a, n_launch);
-  } else {
-    e = launch_attend_main(st, kv_fmt, p, pl, ws, n_launch);
-  }
+  // on one stream the window tile and the selected tiles share one launch
+  const AttendPlan pl = attend_plan_single(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
+  cudaError_t e = launch_attend_main(st, kv_fmt, p, pl, ws, n_launch);
   if (e == cudaSuccess) e = launch_attend_merge(st, p, pl, ws, n_launch);
   return e;
 }

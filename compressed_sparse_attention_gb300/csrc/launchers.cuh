@@ -116,6 +116,7 @@ struct AttendPlan {
 };
 int attend_num_tiles(int topk, bool has_idx);
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
+AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms);
 size_t attend_workspace_bytes(int n_query, const AttendPlan& pl);
 cudaError_t launch_attend_window(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                  int* n_launch);
