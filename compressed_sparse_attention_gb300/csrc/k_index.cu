@@ -61,28 +61,36 @@ __device__ __forceinline__ int64_t idx_static_items(int64_t n_items) {
 // An item whose chunk starts at or past its query's n_vis holds nothing to
 // score (entry 0's item still runs: it sets the query's flags and n_pool).
 // n_vis bounds every narrower range the scan uses, so the test is safe.
-__device__ __forceinline__ bool idx_item_empty(const IdxArgs& a, int q, int64_t j0) {
-  return j0 > 0 && j0 >= (int64_t)__ldg(a.n_vis + q);
+__device__ __forceinline__ bool idx_item_empty(const int32_t* n_vis, int q, int64_t j0) {
+  return j0 > 0 && j0 >= (int64_t)__ldg(n_vis + q);
+}
+
+// work item -> query: items stay below 2^32 (the launcher checks), so a
+// 32-bit division does (a 64-bit one costs a few hundred cycles per item)
+__device__ __forceinline__ int idx_item_query(unsigned long long item, unsigned long long n_chunks) {
+  return (int)((uint32_t)item / (uint32_t)n_chunks);
 }
 
 struct IdxTickets {
   unsigned long long* s;  // shared [2]
   unsigned long long* work;
-  unsigned long long base;  // first ticketed item
-  const IdxArgs* a;
-  int64_t chunk;            // keys an item
+  unsigned long long base;     // first ticketed item
+  const int32_t* n_vis;        // the fields of the launch's arguments it reads, by value
+  unsigned long long n_chunks;
+  unsigned long long n_items;
+  int64_t chunk;               // keys an item
   int par = 0;
   // the next ticket. One that lands in a query's empty tail means the rest of
   // that tail is empty too: the counter jumps to the next query's first item
-  // (the counter only moves forward, so no item with entries is skipped)
+  // and thread 0 draws again (the counter only moves forward, so no item with
+  // entries is skipped)
   __device__ unsigned long long draw() {
-    const unsigned long long n_items = (unsigned long long)a->n_chunks * (unsigned long long)a->n_query;
     for (;;) {
       const unsigned long long it = base + atomicAdd(work, 1ull);
       if (it >= n_items) return it;
-      const int q = (int)(it / (unsigned long long)a->n_chunks);
-      if (!idx_item_empty(*a, q, (int64_t)(it % (unsigned long long)a->n_chunks) * chunk)) return it;
-      atomicMax(work, (unsigned long long)(q + 1) * (unsigned long long)a->n_chunks - base);
+      const int q = idx_item_query(it, n_chunks);
+      if (!idx_item_empty(n_vis, q, (int64_t)(it - (unsigned long long)q * n_chunks) * chunk)) return it;
+      atomicMax(work, (unsigned long long)(q + 1) * n_chunks - base);
     }
   }
   __device__ void start() {
@@ -127,14 +135,11 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
   const uint16_t* kbase = nullptr;
   bool q_ok = false;
   auto run = [&](int64_t item) {
-    const int q = (int)(item / a.n_chunks);
-    const int64_t j0 = (item % a.n_chunks) * kIdxChunk;
+    const int q = idx_item_query((unsigned long long)item, (unsigned long long)a.n_chunks);
+    const int64_t j0 = (item - (int64_t)q * a.n_chunks) * kIdxChunk;
     if (q != cur_q) {
-      // an empty item of another query leaves the current one in place (the
-      // two loads go out together)
-      const int b = a.seq_of_q[q];
-      if (idx_item_empty(a, q, j0)) return;
       cur_q = q;
+      const int b = a.seq_of_q[q];
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
         if (threadIdx.x == 0 && j0 == 0) {
@@ -205,7 +210,8 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, &a, (int64_t)kIdxChunk};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, a.n_vis, (unsigned long long)a.n_chunks,
+                (unsigned long long)n_items, (int64_t)kIdxChunk};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
@@ -311,14 +317,11 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   const uint8_t* sbase = nullptr;
   bool q_ok = false;
   auto run = [&](int64_t item) {
-    const int q = (int)(item / a.n_chunks);
-    const int64_t j0 = (item % a.n_chunks) * CH;
+    const int q = idx_item_query((unsigned long long)item, (unsigned long long)a.n_chunks);
+    const int64_t j0 = (item - (int64_t)q * a.n_chunks) * CH;
     if (q != cur_q) {
-      // an empty item of another query leaves the current one in place (the
-      // two loads go out together)
-      const int b = a.seq_of_q[q];
-      if (idx_item_empty(a, q, j0)) return;
       cur_q = q;
+      const int b = a.seq_of_q[q];
       q_ok = (b >= 0 && b < a.n_seq);
       if (!q_ok) {
         if (threadIdx.x == 0 && j0 == 0) {
@@ -407,7 +410,8 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, &a, (int64_t)CH};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, a.n_vis, (unsigned long long)a.n_chunks,
+                (unsigned long long)n_items, (int64_t)CH};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
@@ -492,6 +496,7 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
   const int64_t rows_max = a.cand != nullptr ? min(a.max_vis, (int64_t)a.cand_ld << a.cand_shift) : a.max_vis;
   a.n_chunks = (rows_max + chunk - 1) / chunk;
   const int64_t items = a.n_chunks * a.n_query;
+  if (items >= (int64_t)1 << 32) return cudaErrorInvalidValue;  // item indices are split in 32 bits
   const dim3 grid((unsigned)(items < cap ? items : cap));
 #define CSA2_IDX(NT, UQ, U8)                                                         \
   do {                                                                               \
