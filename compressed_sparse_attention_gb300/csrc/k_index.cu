@@ -58,13 +58,6 @@ __device__ __forceinline__ int64_t idx_row(const IdxArgs& a, int q, int64_t p) {
 __device__ __forceinline__ int64_t idx_static_items(int64_t n_items) {
   return (n_items / gridDim.x) * 3 / 4 * gridDim.x;  // the strided phase covers items [0, this)
 }
-// An item whose chunk starts at or past its query's n_vis holds nothing to
-// score (entry 0's item still runs: it sets the query's flags and n_pool).
-// n_vis bounds every narrower range the scan uses, so the test is safe.
-__device__ __forceinline__ bool idx_item_empty(const int32_t* n_vis, int q, int64_t j0) {
-  return j0 > 0 && j0 >= (int64_t)__ldg(n_vis + q);
-}
-
 // work item -> query: items stay below 2^32 (the launcher checks), so a
 // 32-bit division does (a 64-bit one costs a few hundred cycles per item)
 __device__ __forceinline__ int idx_item_query(unsigned long long item, unsigned long long n_chunks) {
@@ -74,22 +67,17 @@ __device__ __forceinline__ int idx_item_query(unsigned long long item, unsigned 
 struct IdxTickets {
   unsigned long long* s;  // shared [2]
   unsigned long long* work;
-  unsigned long long base;     // first ticketed item
-  const int32_t* n_vis;        // the fields of the launch's arguments it reads, by value
-  unsigned long long n_chunks;
-  unsigned long long n_items;
-  int64_t chunk;               // keys an item
+  unsigned long long base;      // first ticketed item
+  unsigned long long n_chunks;  // items a query (by value: the launch arguments are not addressed)
   int par = 0;
-  // the next ticket. One that lands in a query's empty tail means the rest of
-  // that tail is empty too: the counter jumps to the next query's first item
-  // and thread 0 draws again (the counter only moves forward, so no item with
-  // entries is skipped)
-  __device__ unsigned long long draw() {
-    for (;;) {
-      const unsigned long long it = base + atomicAdd(work, 1ull);
-      if (it >= n_items) return it;
-      const int q = idx_item_query(it, n_chunks);
-      if (!idx_item_empty(n_vis, q, (int64_t)(it - (unsigned long long)q * n_chunks) * chunk)) return it;
+  __device__ unsigned long long draw() { return base + atomicAdd(work, 1ull); }
+  // The item just run had no entries, so neither have its query's later chunks
+  // (a ragged batch): the counter jumps to the next query's first item. It
+  // only moves forward, so no item with entries is skipped. A test at every
+  // draw was measured slower on full-length rows.
+  __device__ void skip_query(unsigned long long item) {
+    if (threadIdx.x == 0) {
+      const int q = idx_item_query(item, n_chunks);
       atomicMax(work, (unsigned long long)(q + 1) * n_chunks - base);
     }
   }
@@ -134,7 +122,7 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
   int nv = 0;
   const uint16_t* kbase = nullptr;
   bool q_ok = false;
-  auto run = [&](int64_t item) {
+  auto run = [&](int64_t item) -> bool {  // true: the item held entries
     const int q = idx_item_query((unsigned long long)item, (unsigned long long)a.n_chunks);
     const int64_t j0 = (item - (int64_t)q * a.n_chunks) * kIdxChunk;
     if (q != cur_q) {
@@ -207,17 +195,17 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
         if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
       }
     }
+    return q_ok && j0 < nv;
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, a.n_vis, (unsigned long long)a.n_chunks,
-                (unsigned long long)n_items, (int64_t)kIdxChunk};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, (unsigned long long)a.n_chunks};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
     if (item >= (unsigned long long)n_items) break;
     tk.prefetch();
-    run((int64_t)item);
+    if (!run((int64_t)item)) tk.skip_query(item);
     tk.advance();
   }
   tk.finish();
@@ -316,7 +304,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   const uint8_t* kbase = nullptr;
   const uint8_t* sbase = nullptr;
   bool q_ok = false;
-  auto run = [&](int64_t item) {
+  auto run = [&](int64_t item) -> bool {  // true: the item held entries
     const int q = idx_item_query((unsigned long long)item, (unsigned long long)a.n_chunks);
     const int64_t j0 = (item - (int64_t)q * a.n_chunks) * CH;
     if (q != cur_q) {
@@ -407,17 +395,17 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
         if (t == 1 && rg[u] + 8 < nv) srow[rg[u] + 8] = sg8;
       }
     }
+    return q_ok && j0 < nv;
   };
   const int64_t n_static = idx_static_items(n_items);
   for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
-  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, a.n_vis, (unsigned long long)a.n_chunks,
-                (unsigned long long)n_items, (int64_t)CH};
+  IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, (unsigned long long)a.n_chunks};
   tk.start();
   for (;;) {
     const unsigned long long item = tk.cur();
     if (item >= (unsigned long long)n_items) break;
     tk.prefetch();
-    run((int64_t)item);
+    if (!run((int64_t)item)) tk.skip_query(item);
     tk.advance();
   }
   tk.finish();
