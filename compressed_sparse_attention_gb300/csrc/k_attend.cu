@@ -592,23 +592,33 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   const int ns = p.n_slots;
   const float2* ml = p.ws_ml + (int64_t)qi * ns * kHeads;
   const int64_t t = p.q_pos[qi];
+  // every load goes out before any is used: this thread's slices of the
+  // partials (a split without rows may hold stale bytes; its weight is 0 and
+  // its slice is never used) and, for the weight threads, the splits' (max, sum)
+  const uint16_t* base = p.ws_o + ((int64_t)qi * ns * kHeads + h) * kDim + 8 * chunk;
+  uint4 part[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+    part[s] = s < ns ? *reinterpret_cast<const uint4*>(base + (int64_t)s * kHeads * kDim) : make_uint4(0u, 0u, 0u, 0u);
   if (tid < kMergeHeadsPerCta) {
     const int hh = hg * kMergeHeadsPerCta + tid;
+    float2 v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) v[s] = s < ns ? ml[s * kHeads + hh] : make_float2(-INFINITY, 0.f);
     const float sk = p.sink[hh] * 1.4426950408889634f;
     float M = sk;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s * kHeads + hh].x);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) M = fmaxf(M, v[s].x);
     float den = 0.f;
     if (M != -INFINITY) {
       den = exp2f(sk - M);
-      for (int s = 0; s < ns; ++s) {
-        const float2 v = ml[s * kHeads + hh];
-        if (v.x != -INFINITY) den += v.y * exp2f(v.x - M);
-      }
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (v[s].x != -INFINITY) den += v[s].y * exp2f(v[s].x - M);
     }
-    for (int s = 0; s < ns; ++s) {
-      const float2 v = ml[s * kHeads + hh];
-      wsplit[s][tid] = (M == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - M) / den;
-    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < ns) wsplit[s][tid] = (M == -INFINITY || v[s].x == -INFINITY) ? 0.f : exp2f(v[s].x - M) / den;
     if (p.lse) p.lse[(int64_t)qi * kHeads + hh] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * 0.6931471805599453f;
   }
   if (tid >= 32 && tid - 32 < p.rp.pairs) {
@@ -618,15 +628,9 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   }
   __syncthreads();
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint16_t* base = p.ws_o + ((int64_t)qi * ns * kHeads + h) * kDim + 8 * chunk;
-  uint4 part[8];
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-    part[s] = (s < ns && wsplit[s][hl] != 0.f) ? *reinterpret_cast<const uint4*>(base + (int64_t)s * kHeads * kDim)
-                                               : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
-    if (s < ns) {
+    if (s < ns && wsplit[s][hl] != 0.f) {
       const float w = wsplit[s][hl];
       const uint32_t pw[4] = {part[s].x, part[s].y, part[s].z, part[s].w};
 #pragma unroll
