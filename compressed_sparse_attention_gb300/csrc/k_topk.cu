@@ -855,6 +855,7 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
                                                       const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
                                                       int32_t* __restrict__ out_idx, const TkMap map) {
   constexpr int NW = TPB / 32;
+  static_assert(TPB >= 256 && TPB % 32 == 0 && PER % 4 == 0, "one thread a bin in the cross-warp sum; float4 loads");
   __shared__ uint32_t hist[NW][256];
   __shared__ uint32_t cnt[256];
   __shared__ uint32_t red[2][NW];
@@ -1133,7 +1134,11 @@ cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64
   // rows of up to 16,384 scores: one CTA per query holding its row in registers
   if (max_vis <= 16384) {
     cudaError_t e;
+    // the fewest keys a thread that fit: registers set how many rows an SM
+    // holds at once (chunked prefill has thousands of rows of up to 6,144)
     if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
+    else if (max_vis <= 4096) e = launch_topk_row<256, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
+    else if (max_vis <= 6144) e = launch_topk_row<256, 24>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
     else if (max_vis <= 8192) e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
     else e = launch_topk_row<1024, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
     if (e == cudaSuccess) *n_launch += 1;
