@@ -658,15 +658,10 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
 
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
 
-// How one attend call is cut into launches. With few queries (decode) the
-// window tile, which does not depend on the selection, is its own launch (the
-// step runs it on a side stream from the start), the selected tiles are cut
-// so that all their CTAs fit in one wave, and a merge combines the partials.
-// With many queries (prefill) one CTA per query runs every tile and writes the
-// output directly.
 // One launch for the window and the selected tiles (Reuse steps, and
 // csa2_attend): at most one wave of CTAs (one a SM), each query's tiles split
-// evenly over floor(num_sms / n_query) CTAs.
+// evenly over floor(num_sms / n_query) CTAs; with many queries (prefill) one
+// CTA per query runs every tile and writes the output directly.
 AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms) {
   AttendPlan pl{};
   pl.n_tiles = attend_num_tiles(topk, has_idx);
@@ -682,6 +677,11 @@ AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms) 
   return pl;
 }
 
+// How a step's attention is cut into launches. With few queries (decode) the
+// window tile, which does not depend on the selection, is its own launch (the
+// step runs it on a side stream beside top-k), the selected tiles are cut so
+// that all their CTAs fit in one wave, and a merge combines the partials.
+// Otherwise the single-launch plan above.
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
   AttendPlan pl{};
   pl.n_tiles = attend_num_tiles(topk, has_idx);
