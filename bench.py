@@ -529,8 +529,8 @@ def run_e2e(args, ctx, copies, stream, device, wl):
     host memory; the caches (window, pool, index keys) stay resident. Timed two
     ways: one csa2_step_graph_launch per step (the host step captured once per
     input copy) and one csa2_step_host call per step. Inside, q is staged by a
-    kernel beside the index scan, compress reads the raw tokens and gates in
-    place, and the merge writes the output into host memory. The argument
+    kernel on a copy stream as the index scan retires, compress reads the raw
+    tokens and gates in place, and the merge writes the output into host memory. The argument
     block of each input copy is prepared once, as a serving loop that reuses
     its buffers would."""
     steps = max(10, min(args.steps, 200))
