@@ -736,9 +736,9 @@ def main():
         "e2e": {"value": world * units_per_step / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e_ms, "steps": e2e["steps"],
-                "api": e2e_api + " (pinned host q, raw tokens, gates and out: q staged by a kernel beside the "
-                                 "index scan, raw tokens and gates read in place by compress, out written by "
-                                 "the merge over the host link)",
+                "api": e2e_api + " (pinned host q, raw tokens, gates and out: q staged by a kernel on a copy "
+                                 "stream as the index scan retires, raw tokens and gates read in place by "
+                                 "compress, out written by the merge over the host link)",
                 "ms_per_step_csa2_step_graph_launch": e2e_graph, "ms_per_step_csa2_step_host": e2e_direct},
         "gpu_launches": r["launches"] * args.steps,
         "clocks": clocks,
