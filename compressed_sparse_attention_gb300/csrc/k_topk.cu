@@ -830,12 +830,13 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
 // ---------------------------------------------------------------------------
 // Rows of at most TPB * PER scores: one CTA per query, no cluster. Thread t
 // keeps the order-preserving keys of entries PER t .. PER t + PER - 1 in
-// registers. The search narrows the threshold eight bits at a time below the
-// row's common prefix (the leading bits that its smallest and largest keys
-// share): per-warp 256-bin histograms of the keys still in play, one warp
-// finds the bin that holds the k-th largest, and the search stops once that
-// bin holds exactly the keys still needed, or when no bits are left (ties at
-// one key value, taken in index order). One 64-bit block scan of
+// registers. The search narrows the threshold eleven bits at a time from
+// the top: one CTA-wide histogram of the keys still in play (plain shared
+// atomics), a block scan over its bins finds the one that holds the k-th
+// largest, and the search stops once that bin holds exactly the keys still
+// needed, or when no bits are left (ties at one key value, taken in index
+// order). (Finding the row's common prefix first, or 8-bit digits in per-warp
+// histograms, measured slower.) One 64-bit block scan of
 // (above-threshold, at-threshold) counts then gives every thread the output
 // positions of its entries, which come out in ascending index order.
 // map set: entry e of the row is pool position e, written out as the entry
@@ -855,11 +856,13 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
                                                       const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
                                                       int32_t* __restrict__ out_idx, const TkMap map) {
   constexpr int NW = TPB / 32;
-  static_assert(TPB >= 256 && TPB % 32 == 0 && PER % 4 == 0, "one thread a bin in the cross-warp sum; float4 loads");
-  __shared__ uint32_t hist[NW][256];
-  __shared__ uint32_t cnt[256];
-  __shared__ uint32_t red[2][NW];
+  constexpr int DB = 11;        // digit bits a level
+  constexpr int NB = 1 << DB;
+  constexpr int BPT = NB / TPB;  // bins a thread owns in the scan
+  static_assert(NB % TPB == 0 && TPB % 32 == 0 && PER % 4 == 0, "bins split evenly; float4 loads");
+  __shared__ uint32_t hist[NB];
   __shared__ uint32_t res[3];
+  __shared__ uint32_t wtot[NW];
   __shared__ unsigned long long wsum[NW];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = blockIdx.x;
@@ -886,97 +889,79 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
 #pragma unroll
     for (int i = 0; i < PER; ++i) key[i] = (e0 + i < n) ? score_key(row[e0 + i]) : 0u;
   }
-  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-#pragma unroll
-  for (int i = 0; i < PER; ++i)
-    if (e0 + i < n) {
-      mn = min(mn, key[i]);
-      mx = max(mx, key[i]);
-    }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  }
-  if (lane == 0) {
-    red[0][warp] = mn;
-    red[1][warp] = mx;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    mn = lane < NW ? red[0][lane] : 0xFFFFFFFFu;
-    mx = lane < NW ? red[1][lane] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      res[0] = mn;
-      res[1] = mx;
-    }
-  }
-  __syncthreads();
-  mn = res[0];
-  mx = res[1];
   // ---- threshold search: keys in play share their bits at and above `hi`
-  // with P; the digit below them has at most 8 bits
-  int hi = (mn == mx) ? 0 : 32 - __clz(mn ^ mx);
-  uint32_t P = (hi == 0) ? mn : (hi >= 32 ? 0u : (mn >> hi));
+  // with P (nothing yet at the start). Each level counts the next DB bits of
+  // the keys in play in one CTA-wide histogram (plain shared atomics); a block
+  // scan over the bins, from the top, finds the one that holds the k-th
+  // largest key.
+  int hi = 32;
+  uint32_t P = 0u;
   uint32_t need = (uint32_t)k;
   bool exact = false;
   while (hi > 0) {
-    __syncthreads();  // res[] and cnt[] of the previous level have been read
-    const int lo = hi > 8 ? hi - 8 : 0;
-    const uint32_t dmask = (1u << (hi - lo)) - 1u;
-#pragma unroll
-    for (int i = lane; i < 256; i += 32) hist[warp][i] = 0u;
-    __syncwarp();
+    const int lo = hi > DB ? hi - DB : 0;
+    const int w = hi - lo;
+    const uint32_t dmask = (1u << w) - 1u;
+    const int nb = 1 << w;
+    // the previous level read hist before its scan barriers and res after
+    // its last one; both are rewritten only after the barriers below
+    for (int i = tid; i < nb; i += TPB) hist[i] = 0u;
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < PER; ++i)
-      if (e0 + i < n && (hi >= 32 || (key[i] >> hi) == P)) atomicAdd(&hist[warp][(key[i] >> lo) & dmask], 1u);
+      if (e0 + i < n && (hi >= 32 || (key[i] >> hi) == P)) atomicAdd(&hist[(key[i] >> lo) & dmask], 1u);
     __syncthreads();
-    if (tid < 256) {
-      uint32_t v = 0;
+    // thread t owns bins nb-1-BPT t .. nb-BPT (t+1), in descending order
+    uint32_t c[BPT], sl = 0;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) v += hist[w][tid];
-      cnt[tid] = v;
+    for (int b = 0; b < BPT; ++b) {
+      const int bin = nb - 1 - (BPT * tid + b);
+      c[b] = bin >= 0 ? hist[bin] : 0u;
+      sl += c[b];
     }
+    uint32_t incl = sl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wtot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      // lane l takes bins 255 - 8l .. 248 - 8l (descending); the bin where
-      // the running count from the top first reaches `need` holds the k-th key
-      uint32_t c[8], sl = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = cnt[255 - 8 * lane - i];
-        sl += c[i];
-      }
-      uint32_t incl = sl;
+      const uint32_t own = lane < NW ? wtot[lane] : 0u;
+      uint32_t t = own;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const uint32_t v = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += v;
       }
-      const uint32_t excl = incl - sl;
-      const unsigned bal = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-      if (lane == __ffs(bal) - 1) {
-        uint32_t cum = excl;
-        int i = 0;
-#pragma unroll 1
-        for (; i < 7; ++i) {
-          if (cum + c[i] >= need) break;
-          cum += c[i];
-        }
-        res[0] = (uint32_t)(255 - 8 * lane - i);
-        res[1] = c[i];
-        res[2] = cum;
+      if (lane < NW) wtot[lane] = t - own;
+    }
+    __syncthreads();
+    incl += wtot[warp];
+    const uint32_t excl = incl - sl;
+    if (excl < need && need <= incl) {
+      // the first of this thread's bins where the running count reaches need
+      // (predicated selects keep c[] in registers)
+      uint32_t cum = excl, pick = BPT - 1, at = c[BPT - 1], before = excl;
+      bool found = false;
+#pragma unroll
+      for (int b = 0; b < BPT; ++b) {
+        const bool here = !found && cum + c[b] >= need;
+        pick = here ? (uint32_t)b : pick;
+        at = here ? c[b] : at;
+        before = here ? cum : before;
+        found = found || here;
+        cum += c[b];
       }
+      res[0] = (uint32_t)(nb - 1 - BPT * tid) - pick;
+      res[1] = at;
+      res[2] = before;
     }
     __syncthreads();
     const uint32_t bstar = res[0], nbin = res[1], above = res[2];
     need -= above;
-    P = (hi >= 32 ? 0u : (P << (hi - lo))) | bstar;
+    P = (hi >= 32 ? 0u : (P << w)) | bstar;
     hi = lo;
     if (nbin == need) {
       exact = true;
