@@ -260,9 +260,7 @@ namespace cg = cooperative_groups;
 // shared memory. Element li of a slice sits in thread li % 1024, round li / 1024,
 // so a warp's ballot in round u is bit-word u*32 + warp of the slice's
 // bitmap and word w covers elements 32w .. 32w+31.
-//   1. the cluster's smallest and largest key give the prefix that all keys
-//      share; the digits start below it, so that the first histogram already
-//      spreads the keys (scores of one row share most exponent bits);
+//   1. (the digits start at the key's top bit);
 //   2. MSD digit levels of up to 12 bits: each histograms the keys that match
 //      the digits chosen so far and picks the digit that holds the k-th
 //      largest key; in a cluster in two stages, first among 64 blocks of
@@ -312,15 +310,11 @@ struct TkLayout {
 
 // misc words
 constexpr int kMiscRes = 32;      // [32..34] picked digit, count above it, count in it
-constexpr int kMiscMin = 36;      // smallest valid key here
-constexpr int kMiscMax = 37;      // largest valid key here
 constexpr int kMiscGt = 38;       // keys > T here
 constexpr int kMiscTie = 39;      // keys == T here
 constexpr int kMiscChosen = 40;   // chosen keys here
 constexpr int kMiscCand = 41;     // candidates here
 constexpr int kMiscBlk = 42;      // [42..43] picked block, count above it
-constexpr int kMiscWarpMin = 64;  // [64..95] per-warp smallest key
-constexpr int kMiscWarpMax = 96;  // [96..127] per-warp largest key
 
 // inclusive block-wide scan of one value per thread (1024 threads); warp_s[31] = total
 __device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s) {
@@ -528,9 +522,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   const uint32_t need = (uint32_t)min(k, nv);
   const bool all = (uint32_t)nv <= need;  // every visible entry is chosen (uniform over the cluster)
 
-  // ---- slice -> keys (with this thread's smallest and largest); histograms,
-  // rank bitmap and counters zeroed meanwhile
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  // ---- slice -> keys; histograms, rank bitmap and counters zeroed meanwhile
   {
     const float* row = scores + (int64_t)q * ld + base;
     float v[PER];
@@ -548,14 +540,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
       misc[kMiscCand] = 0u;
     }
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const uint32_t x = score_key(v[u]);
-      keys[u * kTkThreads + tid] = x;
-      if (u * kTkThreads + tid < cnt) {
-        kmin = min(kmin, x);
-        kmax = max(kmax, x);
-      }
-    }
+    for (int u = 0; u < PER; ++u) keys[u * kTkThreads + tid] = score_key(v[u]);
   }
   __syncthreads();
 
@@ -566,51 +551,12 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   int shift = 32;
   int mode = all ? kTkAll : kTkTies;
   if (!all) {
-    // ---- common prefix of the cluster's keys
-    uint32_t mn = kmin, mx = kmax;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      misc[kMiscWarpMin + warp] = mn;
-      misc[kMiscWarpMax + warp] = mx;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      mn = misc[kMiscWarpMin + lane];
-      mx = misc[kMiscWarpMax + lane];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      if (lane == 0) {
-        misc[kMiscMin] = mn;
-        misc[kMiscMax] = mx;
-      }
-    }
-    tk_sync(cluster, C);
-    {
-      uint32_t a[kTkMaxCluster], b[kTkMaxCluster];
-      cluster_gather_u32(cluster, misc + kMiscMin, C, a);
-      cluster_gather_u32(cluster, misc + kMiscMax, C, b);
-      mn = 0xFFFFFFFFu;
-      mx = 0u;
-#pragma unroll
-      for (int r = 0; r < kTkMaxCluster; ++r) {
-        if ((uint32_t)r < C) {
-          mn = min(mn, a[r]);
-          mx = max(mx, b[r]);
-        }
-      }
-    }
-    const uint32_t diff = mn ^ mx;
-    shift = diff ? 32 - __clz(diff) : 0;  // bits below the shared prefix
-    P = shift >= 32 ? 0u : (mx >> shift);
+    // the digits start at the top bit (finding the cluster's common prefix
+    // first, one more cluster-wide exchange, measured slower)
+    shift = 32;
+    P = 0u;
     uint32_t rem = need;
-    // ---- digit levels below the prefix
+    // ---- digit levels
 #pragma unroll 1
     for (int lvl = 0; shift > 0; ++lvl) {
       const int w = min(kTkDigit, shift);
