@@ -58,6 +58,18 @@ __device__ __forceinline__ int64_t idx_row(const IdxArgs& a, int q, int64_t p) {
 __device__ __forceinline__ int64_t idx_static_items(int64_t n_items) {
   return (n_items / gridDim.x) * 3 / 4 * gridDim.x;  // the strided phase covers items [0, this)
 }
+// The strided phase in blocks of B consecutive items when a CTA's share
+// K = n_static / gridDim.x is at least 8 (B the largest divisor of K that is
+// at most 4): a CTA then switches query about once a block instead of once an
+// item, and every CTA still takes exactly K items. With fewer items a CTA
+// strided single items measured faster (64K decode: 25.8 against 26.2 us; at
+// 1M, blocks of 3: 59.4 against 61.7 us).
+__device__ __forceinline__ int idx_static_block(int64_t n_static) {
+  const int64_t K = n_static / gridDim.x;
+  if (K < 8) return 1;
+  return K % 4 == 0 ? 4 : (K % 3 == 0 ? 3 : (K % 2 == 0 ? 2 : 1));
+}
+
 // work item -> query: items stay below 2^32 (the launcher checks), so a
 // 32-bit division does (a 64-bit one costs a few hundred cycles per item)
 __device__ __forceinline__ int idx_item_query(unsigned long long item, unsigned long long n_chunks) {
@@ -198,7 +210,11 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
     return q_ok && j0 < nv;
   };
   const int64_t n_static = idx_static_items(n_items);
-  for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
+  {
+    const int B = idx_static_block(n_static);
+    for (int64_t blk = blockIdx.x; blk * B < n_static; blk += gridDim.x)
+      for (int k = 0; k < B; ++k) run(blk * B + k);
+  }
   IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, (unsigned long long)a.n_chunks};
   tk.start();
   for (;;) {
@@ -398,7 +414,11 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
     return q_ok && j0 < nv;
   };
   const int64_t n_static = idx_static_items(n_items);
-  for (int64_t item = blockIdx.x; item < n_static; item += gridDim.x) run(item);
+  {
+    const int B = idx_static_block(n_static);
+    for (int64_t blk = blockIdx.x; blk * B < n_static; blk += gridDim.x)
+      for (int k = 0; k < B; ++k) run(blk * B + k);
+  }
   IdxTickets tk{s_tk, a.work, (unsigned long long)n_static, (unsigned long long)a.n_chunks};
   tk.start();
   for (;;) {
