@@ -328,6 +328,17 @@ def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
     barrier(pg, device)
     ms = e0.elapsed_time(e1)
     ms_max = max_over_ranks(pg, ms, device)
+    # ---- the same region's replays timed one by one: median per step
+    n_rep = 64
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            a.record(stream)
+            g_all.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    rep_ms = sorted(a.elapsed_time(b) / N_COPIES for a, b in ev)
+    ms_median = statistics.median(rep_ms)
     # ---- dominant kernel (index score) timed alone, on its launch stream
     n_idx = max(args.steps, 20)
     with torch.cuda.stream(stream):
@@ -346,7 +357,8 @@ def run_gpu_workload(args, wl, rank, pg, device, peaks, sampler=None):
     flags, _ = ctx.check()
     if flags:
         raise RuntimeError(f"device error word 0x{flags:x} after timing")
-    return dict(ms=ms, ms_max=ms_max, launches=launches_per_step, idx_ms=idx_ms, e2e=e2e)
+    return dict(ms=ms, ms_max=ms_max, launches=launches_per_step, idx_ms=idx_ms, e2e=e2e, ms_median=ms_median,
+                n_rep=n_rep)
 
 
 def attention_flops(wl) -> float:
@@ -400,6 +412,43 @@ def run_prefill_extra(args, device, bf16_peak):
             "ms_per_step": ms_step, "attend_ms": ms_att, "attend_flops": flops,
             "roofline_attend": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                                 "frac": tf / bf16_peak, "peak_kind": "bf16 dense, burst (kernel timed alone)"}}
+
+
+def run_tiny_extra(args, device):
+    """Latency of one CSA2 layer step on the tiny decode workload (batch 1,
+    4,096 context, ratio 4 -> 1,024 entries): one CUDA graph per step, each
+    replay timed alone, median and spread. Its ~1 MB working set stays in L2,
+    as it would from step to step of a real decode."""
+    from compressed_sparse_attention_gb300 import binding
+    wl = PRESETS["tiny_decode"]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads)
+    c = Copy(ctx, wl, 0, device)
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        c.step(ctx)
+    torch.cuda.synchronize()
+    launches = ctx.last_launch_count
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the tiny workload")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        c.step(ctx)
+    n = 200
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            g.replay()
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(1000.0 * a.elapsed_time(b) for a, b in ev)
+    return {"workload": wl.name, "us_per_step_median": statistics.median(us), "us_p10": us[n // 10],
+            "us_p90": us[(9 * n) // 10], "replays": n, "launches_per_step": launches,
+            "tokens_per_s": 1e6 / statistics.median(us),
+            "timing": "one graph replay per step, each timed alone with CUDA events (L2-resident inputs)"}
 
 
 def run_hier_extra(args, device):
@@ -636,7 +685,35 @@ class OracleSample:
                           q_idx=self.qi, w_heads=self.w, idx_keys=self.keys)
 
 
-def cpu_baseline(wl, budget_s):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    return v
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _cpu_baseline_child(name, budget_s, threads):
+    """Runs in a child process whose BLAS thread count was fixed by its
+    environment (and whose affinity is cut to `threads` cores): times whole
+    decode queries of the workload through the oracle for about budget_s."""
+    if hasattr(os, "sched_setaffinity"):
+        cpus = sorted(os.sched_getaffinity(0))
+        os.sched_setaffinity(0, set(cpus[:threads]))
+    wl = PRESETS[name]
     s = OracleSample(wl)
     done = 0
     t0 = time.perf_counter()
@@ -646,9 +723,37 @@ def cpu_baseline(wl, budget_s):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": done / el, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{done} decode queries of {wl.name} (one sequence, {wl.ctx_len[0]} context) through the "
-                      f"float64 NumPy oracle (score, top-k, attend), {el:.1f} s, default BLAS threads"}
+    print(json.dumps({"done": done, "seconds": el}))
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle, as it stands, on the host's cores: whole decode queries of
+    the workload's first sequence, timed twice in child processes, once with
+    the BLAS thread count and the affinity at every core of this process and
+    once at one core. The line's value is the all-core run."""
+    n_all = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    runs = {}
+    for threads in (n_all, 1):
+        env = dict(os.environ)
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                  "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+            env[k] = str(threads)
+        code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+                f"bench._cpu_baseline_child({wl.name!r}, {float(budget_s)!r}, {threads})")
+        try:
+            r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                               timeout=budget_s * 4 + 180)
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            runs[threads] = d["done"] / d["seconds"], d["done"], d["seconds"]
+        except Exception as ex:  # reported, never silently dropped
+            runs[threads] = None, 0, repr(ex)[:200]
+    v_all, n_done, el = runs[n_all]
+    v_one = runs[1][0]
+    return {"value": v_all, "unit": "tokens/s", "cores": n_all, "kind": "oracle",
+            "value_1_core": v_one, "cpu_model": cpu_model(),
+            "sample": f"{n_done} decode queries of {wl.name} (one sequence, {wl.ctx_len[0]} context) through the "
+                      f"float64 NumPy oracle (score, top-k, attend) in {el if isinstance(el, str) else f'{el:.1f} s'}, "
+                      f"BLAS threads and affinity at {n_all} cores; again at 1 core for value_1_core"}
 
 
 # ----------------------------------------------------------------------------- main
@@ -740,6 +845,9 @@ def main():
                                  "stream as the index scan retires, raw tokens and gates read in place by "
                                  "compress, out written by the merge over the host link)",
                 "ms_per_step_csa2_step_graph_launch": e2e_graph, "ms_per_step_csa2_step_host": e2e_direct},
+        "ms_per_step_median": max_over_ranks(pg, r["ms_median"], device),
+        "ms_per_step_median_how": f"median over {r['n_rep']} replays of the {N_COPIES}-step graph, each timed "
+                                  f"alone with CUDA events, divided by {N_COPIES}",
         "gpu_launches": r["launches"] * args.steps,
         "clocks": clocks,
     }
@@ -759,6 +867,10 @@ def main():
                              "index_gbs": index_bytes(wl4) / (r4["idx_ms"] / 1000.0) / 1e9}
             except Exception as ex:  # reported, never silently dropped
                 line[key] = {"error": repr(ex)[:300]}
+        try:
+            line["extra_tiny"] = run_tiny_extra(args, device)
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_tiny"] = {"error": repr(ex)[:300]}
         try:
             line["extra_hier"] = run_hier_extra(args, device)
         except Exception as ex:  # reported, never silently dropped

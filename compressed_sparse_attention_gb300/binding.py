@@ -79,6 +79,7 @@ SIGNATURES = {
     "csa2_status_string": (C.c_char_p, [C.c_int]),
     "csa2_rope_frequencies": (C.c_int, [C.c_void_p, C.POINTER(C.c_double), C.c_int32]),
     "csa2_check": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
+    "csa2_debug_wait_timeout": (C.c_int, [C.c_void_p, C.c_void_p, C.c_uint64]),
     "csa2_store_rows": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_void_p,
                                   C.c_int32, C.c_void_p, C.c_void_p]),
     "csa2_compress": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int32, C.c_int64,
@@ -215,6 +216,11 @@ class Context:
         if st not in (CSA2_OK, 4, 5):
             self._ok(st, "csa2_check")
         return int(fl.value), st
+
+    def debug_wait_timeout(self, limit_ns: int):
+        """Enqueue the wait probe (csa2_debug_wait_timeout) on the current stream."""
+        self._ok(self.lib.csa2_debug_wait_timeout(self.h, C.c_void_p(_stream()), int(limit_ns)),
+                 "csa2_debug_wait_timeout")
 
     # -- entry points
     def store_rows(self, rows, pos, fmt, out, out_scale=None):

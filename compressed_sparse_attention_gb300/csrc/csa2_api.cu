@@ -196,6 +196,17 @@ csa2_status csa2_check(csa2_ctx* ctx, void* stream, uint32_t* flags_out) {
   return CSA2_OK;
 }
 
+csa2_status csa2_debug_wait_timeout(csa2_ctx* ctx, void* stream, uint64_t limit_ns) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (limit_ns < 1 || limit_ns > 1000000000ull)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "debug_wait_timeout: limit_ns must be 1 .. 1e9");
+  const cudaError_t e = csa2::launch_wait_probe(reinterpret_cast<cudaStream_t>(stream), ctx->d_flags, limit_ns);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "debug_wait_timeout");
+  ctx->last_launches = 1;
+  return CSA2_OK;
+}
+
 csa2_status csa2_store_rows(csa2_ctx* ctx, void* stream, const float* rows, int64_t n_rows, int32_t dim,
                             const int64_t* pos, int32_t format, void* out, uint8_t* out_scale) {
   if (!ctx) return CSA2_ERR_INVALID_ARG;

@@ -13,10 +13,13 @@
 // that device, and it stays there until the process exits.
 //
 // Host code cannot use the array's name as a device address (on the host it
-// is only a stand-in symbol): the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call of this
-// entry point on the device. That first call should therefore come before
-// any stream capture begins on that device.
+// is only a stand-in symbol): the address is looked up with
+// cudaGetSymbolAddress, with the context's device current, by the first call
+// of this entry point made with a given context, and kept in that context.
+// A context is bound to one device and to the lifetime of the CUDA context it
+// was created in, so a context created after a device reset looks the address
+// up afresh. That first call should come before any stream capture begins on
+// the device.
 //
 // Every call on a device shares the same array and it keeps the last call's
 // contents. Nothing in it has to start at zero (each call writes every
@@ -24,35 +27,12 @@
 // different streams, without ordering between them) race on the array and
 // give wrong results: order such calls on one stream.
 #include <cstdio>
-#include <mutex>
 
 #include "ctx.cuh"
 #include "launchers.cuh"
 
 // the scratch: split-K partial outputs and (max, sum) pairs of csa2_attend
 static __device__ __align__(256) unsigned char g_attend_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-
-constexpr int kMaxDevices = 64;
-
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// device address of g_attend_scratch on `dev` (which must be current)
-cudaError_t scratch_address(int dev, void** out) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_attend_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
-}
-
-}  // namespace
 
 extern "C" csa2_status csa2_attend_noalloc(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
                                            const uint16_t* q, const int64_t* q_pos, const int32_t* seq_of_q,
@@ -78,16 +58,20 @@ extern "C" csa2_status csa2_attend_noalloc(csa2_ctx* ctx, void* stream, int32_t 
     ctx->err = std::string("attend_noalloc: cudaGetDevice: ") + cudaGetErrorString(e);
     return CSA2_ERR_CUDA;
   }
-  if (dev != ctx->device || dev < 0 || dev >= kMaxDevices) {
+  if (dev != ctx->device) {
     ctx->err = "attend_noalloc: the context's device must be the current device";
     return CSA2_ERR_INVALID_ARG;
   }
-  void* scratch = nullptr;
-  e = scratch_address(dev, &scratch);
-  if (e != cudaSuccess) {
-    ctx->err = std::string("attend_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e);
-    return CSA2_ERR_CUDA;
+  if (ctx->noalloc_scratch == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attend_scratch);
+    if (e != cudaSuccess) {
+      ctx->err = std::string("attend_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e);
+      return CSA2_ERR_CUDA;
+    }
+    ctx->noalloc_scratch = p;
   }
+  void* scratch = ctx->noalloc_scratch;
   return csa2_attend(ctx, stream, n_seq, n_query, q, q_pos, seq_of_q, win_kv, win_scale, win_off, win_lo, pool_kv,
                      pool_scale, pool_off, topk_idx, sink, out, lse, scratch, (size_t)CSA2_NOALLOC_SCRATCH_BYTES);
 }

@@ -20,6 +20,9 @@ struct csa2_ctx {
   cudaStream_t copy = nullptr;    // host-buffer steps: the copy of q beside the first half of the step
   cudaEvent_t ev_copy = nullptr;  // recorded on the caller's stream before that copy
   cudaEvent_t ev_q = nullptr;     // recorded on the copy stream once q is on the device
+  // csa2_attend_noalloc: device address of the library's fixed scratch array on
+  // this context's device, looked up by the first such call on this context
+  void* noalloc_scratch = nullptr;
   std::string err;
   int last_launches = 0;
 };

@@ -656,6 +656,25 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   *reinterpret_cast<uint4*>(p.out + ((int64_t)qi * kHeads + h) * kDim + 8 * chunk) = o;
 }
 
+// Test aid for the bounded waits: one thread initialises an mbarrier that
+// nothing ever arrives at and waits on its first phase with the attention
+// kernels' own bounded wait; after limit_ns the wait gives up, records
+// CSA2_FLAG_WAIT_TIMEOUT, and the kernel returns.
+__global__ void wait_probe_kernel(uint32_t* flags, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait(b, 0u, flags, limit_ns);
+  }
+}
+
+cudaError_t launch_wait_probe(cudaStream_t st, uint32_t* flags, uint64_t limit_ns) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(flags, limit_ns);
+  return cudaGetLastError();
+}
+
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
 
 // One launch for the window and the selected tiles (Reuse steps, and

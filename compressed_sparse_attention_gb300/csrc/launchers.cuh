@@ -124,5 +124,7 @@ cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, cons
                                int* n_launch);
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch);
+// one CTA waiting on an mbarrier nothing arrives at, for limit_ns (csa2_debug_wait_timeout)
+cudaError_t launch_wait_probe(cudaStream_t st, uint32_t* flags, uint64_t limit_ns);
 
 }  // namespace csa2

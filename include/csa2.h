@@ -39,8 +39,9 @@
  *     position outside its buffer, n_vis larger than the pool, a segment not
  *     made of whole groups) are skipped by the kernels, which record a bit in
  *     a device error word; csa2_check() synchronises and reports it.
- *   - The library allocates device memory only inside csa2_create (one
- *     status word). Scratch space is the caller's `workspace`, whose size the
+ *   - The library allocates device memory only inside csa2_create (two
+ *     small buffers: the device error word and the index scan's two 64-bit
+ *     work counters). Scratch space is the caller's `workspace`, whose size the
  *     *_workspace_size functions give; it must be 256-byte aligned. The one
  *     exception is csa2_attend_noalloc, whose scratch is a fixed device array
  *     owned by the library (see its comment).
@@ -136,8 +137,16 @@ typedef struct csa2_ctx csa2_ctx;
 void csa2_default_config(csa2_config* cfg);
 
 /* Validates `cfg` (host), computes the RoPE frequencies in double precision
- * and allocates the device status word on the current CUDA device. The
- * context is bound to that device; use it from one host thread at a time. */
+ * and allocates, on the current CUDA device, the device error word and the
+ * index scan's two 64-bit work counters; it also creates the context's side
+ * and copy streams and its events. The context is bound to that device; use
+ * it from one host thread at a time.
+ * One context's calls must not overlap on the GPU: every index scan of a
+ * context (csa2_index_score, csa2_index_score_pool, csa2_step) draws work
+ * from the context's one pair of counters, and csa2_step also uses the
+ * context's side stream and events. Calls enqueued on one stream are
+ * ordered and safe; to run work on several streams at once, give each
+ * stream its own context. */
 csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out);
 void csa2_destroy(csa2_ctx* ctx);
 
@@ -151,6 +160,14 @@ csa2_status csa2_rope_frequencies(const csa2_ctx* ctx, double* out, int32_t n);
  * CSA2_ERR_DEVICE_FLAG / CSA2_ERR_TIMEOUT if a kernel recorded bad input. The
  * word's bits are written to *flags_out (host, nullable). */
 csa2_status csa2_check(csa2_ctx* ctx, void* stream, uint32_t* flags_out);
+
+/* Test aid for the bounded device waits (no counterpart in the method):
+ * enqueues one kernel whose single thread waits, with the same bounded
+ * mbarrier wait the attention kernels use, on a barrier that nothing ever
+ * arrives at. After limit_ns nanoseconds (host, 1 .. 1e9) the wait gives up,
+ * records CSA2_FLAG_WAIT_TIMEOUT and the kernel returns: the next csa2_check
+ * on the stream reports CSA2_ERR_TIMEOUT, and the context stays usable. */
+csa2_status csa2_debug_wait_timeout(csa2_ctx* ctx, void* stream, uint64_t limit_ns);
 
 /* ------------------------------------------------------------------------
  * csa2_store_rows: store fp32 rows in a KV storage format, optionally rotated.
@@ -235,7 +252,9 @@ csa2_status csa2_compress_append(csa2_ctx* ctx, void* stream, const uint16_t* ra
  *   pool_off  [n_seq+1] int64; seq_of_q [n_query] int32; n_vis [n_query] int32
  *   max_vis   (host) an upper bound of every n_vis[q]
  *   scores    [n_query, scores_ld] fp32, scores_ld >= max_vis
- * Products are exact (bf16 x bf16, or e4m3 codes), sums in fp32. */
+ * Products are exact (bf16 x bf16, or e4m3 codes), sums in fp32.
+ * The scan hands out work through the context's counters: two index scans
+ * of one context must not run at the same time on different streams. */
 csa2_status csa2_index_score(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query,
                              const uint16_t* q_idx, const float* w_heads, const void* idx_keys,
                              const uint8_t* idx_key_scale, const int64_t* pool_off,
@@ -396,6 +415,8 @@ typedef struct csa2_step_args {
   int32_t* cand;
 } csa2_step_args;
 
+/* Two steps of one context must not overlap on the GPU: they share the
+ * context's scan counters, side stream and events (see csa2_create). */
 size_t csa2_step_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t max_vis);
 csa2_status csa2_step(csa2_ctx* ctx, void* stream, const csa2_step_args* args);
 
@@ -457,9 +478,9 @@ void csa2_step_graph_destroy(csa2_step_graph* graph);
  *   - Calls needing more scratch than that (csa2_attend_workspace_size(ctx,
  *     n_query) > CSA2_NOALLOC_SCRATCH_BYTES) are rejected with
  *     CSA2_ERR_WORKSPACE and a message; nothing is enqueued.
- *   - The first call on a device looks up the array's device address (the
- *     context's device must be current); make that first call before any
- *     stream capture begins on the device.
+ *   - The first call made with a context looks up the array's device
+ *     address on that context's device (which must be current) and keeps it
+ *     in the context; make that first call before any stream capture begins.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; calls whose work overlaps on the GPU race on it, so
  *     order them on one stream. */

@@ -96,6 +96,10 @@ def _check_query(ctx, case, qi, geom, f, out_step, scores_step, sel_step, oracle
     b = int(i["seq_of_q"][qi])
     t = int(i["q_pos"][qi])
     nv = int(i["n_vis"][qi])
+    # the generator's visibility against the oracle's own rule (entry j is
+    # visible at t iff its group has closed), so that a wrong rule in the
+    # generator cannot pass on both sides
+    assert nv == O.n_visible(t, wl.m), f"{tag} q{qi}: n_vis {nv} but the oracle's rule gives {O.n_visible(t, wl.m)}"
     keys, pool, new_rng, key_step = oracle_state(b)
     woff = i["win_off"].cpu().numpy()
     cap = int(woff[b + 1] - woff[b])
@@ -215,6 +219,14 @@ def _run_full(preset, sample):
     sel = idx.cpu().numpy()
     state = _full_state(ctx, case, geom, f)
     return [_check_query(ctx, case, qi, geom, f, out, scores, sel, state, preset)[1] for qi in sample]
+
+
+def test_fullsize_tiny_decode():
+    """Batch 1 at 4,096 context, ratio 4 (1,024 entries), q and KV ~ N(0,1)/sqrt(512),
+    seed 0: the one query of the batch, through csa2_step as the benchmark
+    runs it."""
+    same = _run_full("tiny_decode", [0])
+    assert all(same), "the tiny decode's selection differs from the oracle's"
 
 
 def test_fullsize_decode_64k_b32():
