@@ -114,6 +114,18 @@ SIGNATURES = {
     "csa2_step_workspace_size": (C.c_size_t, [C.c_void_p, C.c_int32, C.c_int64]),
     "csa2_step": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(StepArgs)]),
     "csa2_last_launch_count": (C.c_int32, [C.c_void_p]),
+    "csa2_shard_visible": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_int64,
+                                     C.c_void_p]),
+    "csa2_topk_pairs": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_void_p, C.c_int64, C.c_void_p, C.c_int32,
+                                  C.c_int64, C.c_void_p, C.c_void_p]),
+    "csa2_topk_merge": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                  C.c_int32, C.c_void_p]),
+    "csa2_attend_partial": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
+                                      C.c_void_p, C.c_void_p, C.c_void_p]),
+    "csa2_attend_combine": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "csa2_attend_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                       C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
@@ -317,6 +329,49 @@ class Context:
             self._p(sink, torch.float32, "sink"), self._p(out, torch.bfloat16, "out"),
             self._p(lse, torch.float32, "lse"), self._p(workspace, None, "workspace"),
             0 if workspace is None else workspace.numel() * workspace.element_size()), "csa2_attend")
+
+    # -- pool sharding (csa2_shard_visible .. csa2_attend_combine)
+    def shard_visible(self, n_vis, lo, hi, out):
+        self._ok(self.lib.csa2_shard_visible(self.h, C.c_void_p(_stream()), n_vis.shape[0],
+                                             self._p(n_vis, torch.int32, "n_vis"), int(lo), int(hi),
+                                             self._p(out, torch.int32, "n_vis_shard")), "csa2_shard_visible")
+
+    def topk_pairs(self, scores, sel, index_base, pair_score, pair_idx):
+        self._ok(self.lib.csa2_topk_pairs(self.h, C.c_void_p(_stream()), sel.shape[0],
+                                          self._p(scores, torch.float32, "scores"), scores.shape[1],
+                                          self._p(sel, torch.int32, "sel"), sel.shape[1], int(index_base),
+                                          self._p(pair_score, torch.float32, "pair_score"),
+                                          self._p(pair_idx, torch.int32, "pair_idx")), "csa2_topk_pairs")
+
+    def topk_merge(self, pair_score, pair_idx, k, out_idx):
+        """pair_score / pair_idx [n_lists, n_query, list_len] -> out_idx [n_query, k]."""
+        n_lists, n_query, list_len = pair_idx.shape
+        self._ok(self.lib.csa2_topk_merge(self.h, C.c_void_p(_stream()), n_query, n_lists, list_len,
+                                          self._p(pair_score, torch.float32, "pair_score"),
+                                          self._p(pair_idx, torch.int32, "pair_idx"), k,
+                                          self._p(out_idx, torch.int32, "out_idx")), "csa2_topk_merge")
+
+    def attend_partial(self, n_seq, q, q_pos, seq_of_q, with_window, win_kv, win_scale, win_off, win_lo, pool_kv,
+                       pool_scale, pool_off, topk_idx, shard_lo, shard_hi, part_o, part_m, part_l):
+        self._ok(self.lib.csa2_attend_partial(
+            self.h, C.c_void_p(_stream()), n_seq, q.shape[0], self._p(q, torch.bfloat16, "q"),
+            self._p(q_pos, torch.int64, "q_pos"), self._p(seq_of_q, torch.int32, "seq_of_q"), 1 if with_window else 0,
+            self._p(win_kv, None, "win_kv"), self._p(win_scale, torch.uint8, "win_scale"),
+            self._p(win_off, torch.int64, "win_off"), self._p(win_lo, torch.int64, "win_lo"),
+            self._p(pool_kv, None, "pool_kv"), self._p(pool_scale, torch.uint8, "pool_scale"),
+            self._p(pool_off, torch.int64, "pool_off"), self._p(topk_idx, torch.int32, "topk_idx"),
+            int(shard_lo), int(shard_hi), self._p(part_o, torch.float32, "part_o"),
+            self._p(part_m, torch.float32, "part_m"), self._p(part_l, torch.float32, "part_l")),
+            "csa2_attend_partial")
+
+    def attend_combine(self, part_o, part_m, part_l, q_pos, sink, out, lse=None):
+        """part_o [n_parts, n_query, 64, 512], part_m / part_l [n_parts, n_query, 64]."""
+        n_parts, n_query = part_m.shape[0], part_m.shape[1]
+        self._ok(self.lib.csa2_attend_combine(
+            self.h, C.c_void_p(_stream()), n_query, n_parts, self._p(part_o, torch.float32, "part_o"),
+            self._p(part_m, torch.float32, "part_m"), self._p(part_l, torch.float32, "part_l"),
+            self._p(q_pos, torch.int64, "q_pos"), self._p(sink, torch.float32, "sink"),
+            self._p(out, torch.bfloat16, "out"), self._p(lse, torch.float32, "lse")), "csa2_attend_combine")
 
     def step_workspace_size(self, n_query, max_vis) -> int:
         return int(self.lib.csa2_step_workspace_size(self.h, n_query, max_vis))

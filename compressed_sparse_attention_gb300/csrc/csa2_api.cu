@@ -479,6 +479,8 @@ static csa2_status attend_params(csa2_ctx* ctx, int32_t n_seq, int32_t n_query, 
   p.n_seq = n_seq; p.n_query = n_query; p.topk = c.topk; p.window = c.window;
   p.scale_log2 = c.softmax_scale * 1.4426950408889634f;
   p.rp = ctx->rope;
+  p.shard_lo = 0;
+  p.shard_hi = INT64_MAX;
   return CSA2_OK;
 }
 
@@ -509,6 +511,127 @@ csa2_status csa2_attend(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_qu
   return do_attend(ctx, reinterpret_cast<cudaStream_t>(stream), n_seq, n_query, q, q_pos, seq_of_q, win_kv, win_scale,
                    win_off, win_lo, pool_kv, pool_scale, pool_off, topk_idx, sink, out, lse, workspace,
                    workspace_bytes);
+}
+
+// ---------------------------------------------------------------------------
+// Pool sharding of one sequence's compressed pool over several devices or
+// launches: per shard the visible count, the local selection's (score,
+// entry) pairs, the merge of all shards' pairs, the shard's partial
+// attention and the log-sum-exp combine of the partials.
+// ---------------------------------------------------------------------------
+csa2_status csa2_shard_visible(csa2_ctx* ctx, void* stream, int32_t n_query, const int32_t* n_vis, int64_t shard_lo,
+                               int64_t shard_hi, int32_t* n_vis_shard) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (n_query < 0 || shard_lo < 0 || shard_hi < shard_lo || shard_hi - shard_lo > 0x7FFFFFFFll)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "shard_visible: sizes");
+  if (n_query == 0) return CSA2_OK;
+  if (!n_vis || !n_vis_shard) return fail(ctx, CSA2_ERR_INVALID_ARG, "shard_visible: null pointer");
+  int nl = 0;
+  const cudaError_t e = csa2::launch_shard_visible(reinterpret_cast<cudaStream_t>(stream), n_query, n_vis, shard_lo,
+                                                   shard_hi, n_vis_shard, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "shard_visible");
+  ctx->last_launches = nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_topk_pairs(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores, int64_t scores_ld,
+                            const int32_t* sel, int32_t k, int64_t index_base, float* pair_score, int32_t* pair_idx) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (n_query < 0 || k < 1 || k > 2048 || scores_ld < 1 || index_base < 0)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "topk_pairs: sizes");
+  if (n_query == 0) return CSA2_OK;
+  if (!scores || !sel || !pair_score || !pair_idx) return fail(ctx, CSA2_ERR_INVALID_ARG, "topk_pairs: null pointer");
+  int nl = 0;
+  const cudaError_t e = csa2::launch_topk_pairs(reinterpret_cast<cudaStream_t>(stream), n_query, scores, scores_ld, sel,
+                                                k, index_base, pair_score, pair_idx, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "topk_pairs");
+  ctx->last_launches = nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_topk_merge(csa2_ctx* ctx, void* stream, int32_t n_query, int32_t n_lists, int32_t list_len,
+                            const float* pair_score, const int32_t* pair_idx, int32_t k, int32_t* out_idx) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (n_query < 0 || n_lists < 1 || list_len < 1 || k < 1 || k > 2048)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "topk_merge: sizes");
+  if ((int64_t)n_lists * list_len > 8192)
+    return fail(ctx, CSA2_ERR_UNSUPPORTED, "topk_merge: n_lists * list_len must be at most 8192");
+  if (n_query == 0) return CSA2_OK;
+  if (!pair_score || !pair_idx || !out_idx) return fail(ctx, CSA2_ERR_INVALID_ARG, "topk_merge: null pointer");
+  int nl = 0;
+  const cudaError_t e = csa2::launch_topk_merge(reinterpret_cast<cudaStream_t>(stream), n_query, n_lists, list_len,
+                                                pair_score, pair_idx, k, out_idx, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "topk_merge");
+  ctx->last_launches = nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_attend_partial(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                                const int64_t* q_pos, const int32_t* seq_of_q, int32_t with_window,
+                                const void* win_kv, const uint8_t* win_scale, const int64_t* win_off,
+                                const int64_t* win_lo, const void* pool_kv, const uint8_t* pool_scale,
+                                const int64_t* pool_off, const int32_t* topk_idx, int64_t shard_lo, int64_t shard_hi,
+                                float* part_o, float* part_m, float* part_l) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  const csa2_config& c = ctx->cfg;
+  const bool scaled = c.kv_format != CSA2_KV_BF16;
+  if (n_query < 0 || n_seq < 1 || shard_lo < 0 || shard_hi < shard_lo)
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_partial: sizes or shard range");
+  if (!with_window && !topk_idx) return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_partial: neither window nor selection");
+  if (n_query == 0) return CSA2_OK;
+  if (!q || !q_pos || !seq_of_q || !part_o || !part_m || !part_l ||
+      (with_window && (!win_kv || !win_off || (scaled && !win_scale))) ||
+      (topk_idx && (!pool_kv || !pool_off || (scaled && !pool_scale))))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_partial: null pointer");
+  if (!aligned16(q) || !aligned16(part_o) || (with_window && !aligned16(win_kv)) || (pool_kv && !aligned16(pool_kv)))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_partial: misaligned buffer");
+  csa2::AttendParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.q_pos = q_pos; p.seq_of_q = seq_of_q;
+  // a shard without the window never reads it; win_off must still index
+  // sequences, so the pool offsets stand in for it
+  p.win_kv = with_window ? win_kv : pool_kv;
+  p.win_scale = with_window ? win_scale : pool_scale;
+  p.win_off = with_window ? win_off : pool_off;
+  p.win_lo = with_window ? win_lo : nullptr;
+  p.pool_kv = pool_kv; p.pool_scale = pool_scale; p.pool_off = pool_off;
+  p.topk_idx = topk_idx;
+  p.flags = ctx->d_flags;
+  p.n_seq = n_seq; p.n_query = n_query; p.topk = c.topk; p.window = c.window;
+  p.scale_log2 = c.softmax_scale * 1.4426950408889634f;
+  p.rp = ctx->rope;
+  p.shard_lo = shard_lo;
+  p.shard_hi = shard_hi;
+  p.part_o = part_o;
+  p.part_m = part_m;
+  p.part_l = part_l;
+  int nl = 0;
+  const cudaError_t e = csa2::launch_attend_partial(reinterpret_cast<cudaStream_t>(stream), c.kv_format, p,
+                                                    with_window ? 1 : 0, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "attend_partial");
+  ctx->last_launches = nl;
+  return CSA2_OK;
+}
+
+csa2_status csa2_attend_combine(csa2_ctx* ctx, void* stream, int32_t n_query, int32_t n_parts, const float* part_o,
+                                const float* part_m, const float* part_l, const int64_t* q_pos, const float* sink,
+                                uint16_t* out, float* lse) {
+  if (!ctx) return CSA2_ERR_INVALID_ARG;
+  ctx->last_launches = 0;
+  if (n_query < 0 || n_parts < 1 || n_parts > 16) return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_combine: n_parts 1..16");
+  if (n_query == 0) return CSA2_OK;
+  if (!part_o || !part_m || !part_l || !q_pos || !sink || !out || !aligned16(part_o) || !aligned16(out))
+    return fail(ctx, CSA2_ERR_INVALID_ARG, "attend_combine: null or misaligned buffer");
+  int nl = 0;
+  const cudaError_t e = csa2::launch_attend_combine(reinterpret_cast<cudaStream_t>(stream), n_query, n_parts, part_o,
+                                                    part_m, part_l, q_pos, sink, ctx->rope, out, lse, &nl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "attend_combine");
+  ctx->last_launches = nl;
+  return CSA2_OK;
 }
 
 // The step's workspace: index scores (full rows of max_vis, or pool rows of

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     l_run[tid] = 0.f;
   }
   float2* rope_tab = reinterpret_cast<float2*>(sm + SM_ROPE);
-  const float sink_l2 = (p.direct && tid < kHeads) ? p.sink[tid] * 1.4426950408889634f : 0.f;  // used at the end
+  const float sink_l2 = (p.direct == 1 && tid < kHeads) ? p.sink[tid] * 1.4426950408889634f : 0.f;  // used at the end
   if (tid < p.rp.pairs) {
     float c = 1.f, sn = 0.f;
     if (q_ok) rope_cs(p.rp, tid, t, c, sn);
@@ -191,9 +191,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
           }
         }
       } else {
+        // entries outside this launch's shard of the pool are not its rows
         const int32_t j = j_cur;
-        if (j >= 0 && j < plen) src = pool_b0 + j;
-        else if (j != -1) set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+        if (j >= 0 && j >= p.shard_lo && j < p.shard_hi) {
+          const int64_t jr = (int64_t)j - p.shard_lo;
+          if (jr < plen) src = pool_b0 + jr;
+          else set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+        } else if (j < -1) {
+          set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+        }
       }
       rows[r] = src;
     }
@@ -482,7 +488,30 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   __syncthreads();
   const bool have_o = (tile_begin < tile_end) && !aborted;
   const int first_rope = kDim - 2 * p.rp.pairs;
-  if (p.direct) {
+  if (p.direct == 2) {
+    // unnormalised partial for a log-sum-exp combine elsewhere: O (rope
+    // channels as they are), the reference max in natural-log units and the
+    // sum of weights; no sink, no rotation back
+    if (tid < kHeads) {
+      const int64_t o = (int64_t)qi * kHeads + tid;
+      p.part_m[o] = have_o ? m_run[tid] * 0.6931471805599453f : -INFINITY;
+      p.part_l[o] = have_o ? l_run[tid] : 0.f;
+    }
+    float* po = p.part_o + (int64_t)qi * kHeads * kDim;
+    for (int mt = 0; mt < 4; ++mt) {
+      const int d = 128 * mt + row;
+      uint32_t r[32];
+      if (have_o) {
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) po[(int64_t)(32 * hh + k) * kDim + d] = __uint_as_float(r[k]);
+    }
+  } else if (p.direct) {
     // final normalisation with the sink: fo = e^{m - M} / den, den = l e^{m - M} + e^{sink - M}
     if (tid < kHeads) {
       const float sk = sink_l2;
@@ -675,6 +704,89 @@ cudaError_t launch_wait_probe(cudaStream_t st, uint32_t* flags, uint64_t limit_n
   return cudaGetLastError();
 }
 
+// log-sum-exp combine of partials from several pool shards: one CTA per
+// (query, 4 heads), thread (head hl = tid/64, chunk = tid%64) owning channels
+// 8 chunk .. 8 chunk + 7. With M = max(max_g m_g, sink), the output is
+// sum_g e^(m_g - M) O_g / (sum_g e^(m_g - M) l_g + e^(sink - M)), its rope
+// channels rotated back by -t; lse = M + log(den).
+constexpr int kCombineMaxParts = 16;
+__global__ void __launch_bounds__(256) attend_combine_kernel(int n_query, int n_parts, const float* __restrict__ part_o,
+                                                             const float* __restrict__ part_m,
+                                                             const float* __restrict__ part_l,
+                                                             const int64_t* __restrict__ q_pos,
+                                                             const float* __restrict__ sink, const RopeParams rp,
+                                                             uint16_t* __restrict__ out, float* __restrict__ lse) {
+  __shared__ float wpart[kCombineMaxParts][kMergeHeadsPerCta];
+  __shared__ float2 rope_tab[kMaxPairs];
+  const int qi = blockIdx.x / (kHeads / kMergeHeadsPerCta);
+  const int hg = blockIdx.x % (kHeads / kMergeHeadsPerCta);
+  const int tid = threadIdx.x, hl = tid >> 6, chunk = tid & 63;
+  const int h = hg * kMergeHeadsPerCta + hl;
+  const int64_t t = q_pos[qi];
+  if (tid < kMergeHeadsPerCta) {
+    const int hh = hg * kMergeHeadsPerCta + tid;
+    const float sk = sink[hh];
+    float M = sk;
+    for (int g = 0; g < n_parts; ++g) M = fmaxf(M, part_m[((int64_t)g * n_query + qi) * kHeads + hh]);
+    float den = 0.f;
+    if (M != -INFINITY) {
+      den = expf(sk - M);
+      for (int g = 0; g < n_parts; ++g) {
+        const float mg = part_m[((int64_t)g * n_query + qi) * kHeads + hh];
+        if (mg != -INFINITY) den += part_l[((int64_t)g * n_query + qi) * kHeads + hh] * expf(mg - M);
+      }
+    }
+    for (int g = 0; g < n_parts; ++g) {
+      const float mg = part_m[((int64_t)g * n_query + qi) * kHeads + hh];
+      wpart[g][tid] = (M == -INFINITY || mg == -INFINITY) ? 0.f : expf(mg - M) / den;
+    }
+    if (lse) lse[(int64_t)qi * kHeads + hh] = (M == -INFINITY) ? -INFINITY : M + logf(den);
+  }
+  if (tid >= 32 && tid - 32 < rp.pairs) {
+    float c, sn;
+    rope_cs(rp, tid - 32, t, c, sn);
+    rope_tab[tid - 32] = make_float2(c, sn);
+  }
+  __syncthreads();
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int g = 0; g < n_parts; ++g) {
+    const float w = wpart[g][hl];
+    if (w == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(part_o + (((int64_t)g * n_query + qi) * kHeads + h) * kDim +
+                                                        8 * chunk);
+    const float4 a = src[0], b = src[1];
+    acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+    acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+    acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+    acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+  }
+  const int first_rope = kDim - 2 * rp.pairs;
+  if (rp.pairs > 0 && 8 * chunk >= first_rope) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 cs = rope_tab[(8 * chunk + 2 * k - first_rope) >> 1];
+      const float x0 = acc[2 * k], x1 = acc[2 * k + 1];
+      acc[2 * k] = x0 * cs.x + x1 * cs.y;  // rotation by -t
+      acc[2 * k + 1] = x1 * cs.x - x0 * cs.y;
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(out + ((int64_t)qi * kHeads + h) * kDim + 8 * chunk) = o;
+}
+
+cudaError_t launch_attend_combine(cudaStream_t st, int n_query, int n_parts, const float* part_o, const float* part_m,
+                                  const float* part_l, const int64_t* q_pos, const float* sink, const RopeParams& rp,
+                                  uint16_t* out, float* lse, int* n_launch) {
+  if (n_query == 0) return cudaSuccess;
+  if (n_parts < 1 || n_parts > kCombineMaxParts) return cudaErrorInvalidValue;
+  attend_combine_kernel<<<n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(n_query, n_parts, part_o, part_m,
+                                                                                part_l, q_pos, sink, rp, out, lse);
+  *n_launch += 1;
+  return cudaGetLastError();
+}
+
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
 
 // One launch for the window and the selected tiles (Reuse steps, and
@@ -795,6 +907,20 @@ cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPla
   attend_merge_kernel<<<p.n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(p);
   *n_launch += 1;
   return cudaGetLastError();
+}
+
+cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, int with_window, int* n_launch) {
+  if (p.n_query == 0) return cudaSuccess;
+  p.n_tiles = attend_num_tiles(p.topk, p.topk_idx != nullptr);
+  p.tile_base = with_window ? 0 : 1;
+  p.tile_count = p.n_tiles - p.tile_base;
+  p.n_split = 1;
+  p.tiles_per_split = p.tile_count;
+  p.lead_single = 0;
+  p.slot_base = 0;
+  p.n_slots = 0;
+  p.direct = 2;
+  return launch_tiles(st, kv_fmt, p, n_launch);
 }
 
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch) {

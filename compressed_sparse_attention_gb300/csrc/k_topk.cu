@@ -250,6 +250,122 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const int32_t* __rest
   for (int i = (int)ns + threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Pool sharding (one sequence's pool split over shards [lo, hi)): the
+// visible count of a shard, the (score, entry) pairs of a shard's local
+// selection, and the merge of the shards' pairs into the global top-k. The
+// merge keys each pair by the 64-bit composite key << 32 | ~entry, unique per
+// entry, so the k largest composites are the k largest scores with ties to
+// the lower entry, exactly the unsharded selection on the same scores.
+// ---------------------------------------------------------------------------
+__global__ void shard_visible_kernel(int n_query, const int32_t* __restrict__ n_vis, int64_t lo, int64_t hi,
+                                     int32_t* __restrict__ out) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= n_query) return;
+  const int64_t v = (int64_t)n_vis[q] - lo;
+  out[q] = (int32_t)max((int64_t)0, min(v, hi - lo));
+}
+
+cudaError_t launch_shard_visible(cudaStream_t st, int n_query, const int32_t* n_vis, int64_t lo, int64_t hi,
+                                 int32_t* n_vis_shard, int* n_launch) {
+  if (n_query == 0) return cudaSuccess;
+  shard_visible_kernel<<<(n_query + 255) / 256, 256, 0, st>>>(n_query, n_vis, lo, hi, n_vis_shard);
+  *n_launch += 1;
+  return cudaGetLastError();
+}
+
+__global__ void topk_pairs_kernel(int n_query, const float* __restrict__ scores, int64_t ld,
+                                  const int32_t* __restrict__ sel, int k, int64_t base, float* __restrict__ ps,
+                                  int32_t* __restrict__ pi) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)n_query * k) return;
+  const int64_t q = i / k;
+  const int32_t j = sel[i];
+  if (j >= 0) {
+    ps[i] = scores[q * ld + j];
+    pi[i] = (int32_t)(base + j);
+  } else {
+    ps[i] = -INFINITY;
+    pi[i] = -1;
+  }
+}
+
+cudaError_t launch_topk_pairs(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* sel, int k,
+                              int64_t index_base, float* pair_score, int32_t* pair_idx, int* n_launch) {
+  const int64_t n = (int64_t)n_query * k;
+  if (n == 0) return cudaSuccess;
+  topk_pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(n_query, scores, ld, sel, k, index_base, pair_score,
+                                                                pair_idx);
+  *n_launch += 1;
+  return cudaGetLastError();
+}
+
+// One 1024-thread CTA per query: the valid pairs of all lists become
+// composites in shared memory (at most kSelCap), a radix select finds the
+// k-th largest, and the chosen entries are written ascending, -1 padded.
+__global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lists, int k_in,
+                                                          const float* __restrict__ ps,
+                                                          const int32_t* __restrict__ pi, int k,
+                                                          int32_t* __restrict__ out_idx) {
+  extern __shared__ __align__(16) unsigned char sm_raw[];
+  unsigned long long* cs = reinterpret_cast<unsigned long long*>(sm_raw);  // [kSelCap]
+  uint32_t* sel = reinterpret_cast<uint32_t*>(cs + kSelCap);               // [kMaxTopk]
+  __shared__ uint32_t hist_s[256];
+  __shared__ unsigned long long bcast[3];
+  __shared__ uint32_t n_c, n_sel;
+  const int q = blockIdx.x;
+  if (threadIdx.x == 0) {
+    n_c = 0;
+    n_sel = 0;
+  }
+  __syncthreads();
+  const int total = n_lists * k_in;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int l = i / k_in, e = i - l * k_in;
+    const int64_t g = ((int64_t)l * n_query + q) * k_in + e;
+    const int32_t j = pi[g];
+    if (j >= 0) {
+      const uint32_t slot = atomicAdd(&n_c, 1u);
+      if (slot < (uint32_t)kSelCap)
+        cs[slot] = ((unsigned long long)score_key(ps[g]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+    }
+  }
+  __syncthreads();
+  const uint32_t n = min(n_c, (uint32_t)kSelCap);
+  const uint32_t take = min((uint32_t)k, n);
+  unsigned long long thr = 0;
+  if (take > 0 && take < n) thr = radix_select64([&](uint32_t i) { return cs[i]; }, n, take, hist_s, bcast);
+  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long v = cs[i];
+    if (take > 0 && v >= thr) {
+      const uint32_t slot = atomicAdd(&n_sel, 1u);
+      if (slot < (uint32_t)kMaxTopk) sel[slot] = 0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull);
+    }
+  }
+  __syncthreads();
+  const uint32_t ns = min(n_sel, (uint32_t)kMaxTopk);
+  int32_t* o = out_idx + (int64_t)q * k;
+  for (uint32_t i = threadIdx.x; i < ns; i += blockDim.x) {
+    const uint32_t v = sel[i];
+    uint32_t r = 0;
+    for (uint32_t jx = 0; jx < ns; ++jx) r += sel[jx] < v ? 1u : 0u;
+    if (r < (uint32_t)k) o[r] = (int32_t)v;
+  }
+  for (int i = (int)ns + threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
+}
+
+cudaError_t launch_topk_merge(cudaStream_t st, int n_query, int n_lists, int k_in, const float* pair_score,
+                              const int32_t* pair_idx, int k, int32_t* out_idx, int* n_launch) {
+  if (n_query == 0) return cudaSuccess;
+  if ((int64_t)n_lists * k_in > kSelCap || k > kMaxTopk) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)kSelCap * 8 + (size_t)kMaxTopk * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<n_query, 1024, smem, st>>>(n_query, n_lists, k_in, pair_score, pair_idx, k, out_idx);
+  *n_launch += 1;
+  return cudaGetLastError();
+}
+
 namespace cg = cooperative_groups;
 
 // ---------------------------------------------------------------------------

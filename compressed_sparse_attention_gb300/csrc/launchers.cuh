@@ -35,9 +35,18 @@ struct AttendParams {
   int lead_single;      // 1: split 0 covers the first tile alone, the others tiles_per_split each
   int n_slots;          // partial slots per query in the workspace
   int slot_base;        // slot of this launch's first split
-  int direct;           // 1: write the normalised output, no partials
+  int direct;           // 1: write the normalised output, no partials; 2: write the
+                        // unnormalised partial (part_o, part_m, part_l) of csa2_attend_partial
   float scale_log2;  // softmax_scale * log2(e)
   RopeParams rp;
+  // pool sharding (csa2_attend_partial): selected entries j outside
+  // [shard_lo, shard_hi) are skipped, the others read pool row j - shard_lo;
+  // the defaults 0 and INT64_MAX read every entry
+  int64_t shard_lo;
+  int64_t shard_hi;
+  float* part_o;  // [n_query][64][512] fp32, rope channels not rotated back
+  float* part_m;  // [n_query][64] reference max, natural-log units (-inf: no rows)
+  float* part_l;  // [n_query][64] sum of exp(s_r - m)
 };
 
 cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
@@ -124,6 +133,22 @@ cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, cons
                                int* n_launch);
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch);
+// one CTA per query over the window tile (when with_window) and the selected
+// tiles, writing the unnormalised partial (direct = 2)
+cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, int with_window, int* n_launch);
+// log-sum-exp combine of n_parts partials [n_parts][n_query] with the sink
+cudaError_t launch_attend_combine(cudaStream_t st, int n_query, int n_parts, const float* part_o, const float* part_m,
+                                  const float* part_l, const int64_t* q_pos, const float* sink, const RopeParams& rp,
+                                  uint16_t* out, float* lse, int* n_launch);
+// n_vis_shard[q] = clamp(n_vis[q] - lo, 0, hi - lo)
+cudaError_t launch_shard_visible(cudaStream_t st, int n_query, const int32_t* n_vis, int64_t lo, int64_t hi,
+                                 int32_t* n_vis_shard, int* n_launch);
+// (score, lo + j) pairs of a shard's local selection; -1 entries give (-inf, -1)
+cudaError_t launch_topk_pairs(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* sel, int k,
+                              int64_t index_base, float* pair_score, int32_t* pair_idx, int* n_launch);
+// the k best of n_lists lists of (score, index) pairs [n_lists][n_query][k_in]
+cudaError_t launch_topk_merge(cudaStream_t st, int n_query, int n_lists, int k_in, const float* pair_score,
+                              const int32_t* pair_idx, int k, int32_t* out_idx, int* n_launch);
 // one CTA waiting on an mbarrier nothing arrives at, for limit_ns (csa2_debug_wait_timeout)
 cudaError_t launch_wait_probe(cudaStream_t st, uint32_t* flags, uint64_t limit_ns);
 

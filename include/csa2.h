@@ -465,6 +465,83 @@ csa2_status csa2_step_graph_launch(csa2_step_graph* graph, void* stream);
 void csa2_step_graph_destroy(csa2_step_graph* graph);
 
 /* ------------------------------------------------------------------------
+ * Pool sharding: one sequence's compressed pool split over G shards (devices
+ * or launches), shard g holding entries [lo_g, hi_g) of every sequence. The
+ * selection semantics are those of the unsharded step ("Reading Notes ...",
+ * 3f C2 step 2, S_t = TopK sigma_t); the pages' own multi-rank form splits
+ * heads and all-reduces the indexer's scores (PocketLLM "The CSA2 attention
+ * layers"), this one splits the pool and exchanges 512 (score, entry) pairs
+ * and one (m, l, O) partial per shard instead. Per shard:
+ *   1. csa2_shard_visible: the shard's visible count;
+ *   2. csa2_index_score + csa2_topk over the shard's own keys (entry j of the
+ *      shard is global entry lo + j): its local top-k;
+ *   3. csa2_topk_pairs: that selection as (score, global entry) pairs;
+ *   4. exchange (all-gather) of the G pair lists; csa2_topk_merge: the global
+ *      top-k, equal to the unsharded selection on the same scores;
+ *   5. csa2_attend_partial over the global selection's entries that lie in
+ *      the shard (the window on one shard only): an unnormalised partial;
+ *   6. exchange of the G partials; csa2_attend_combine: the output, with the
+ *      sink counted once.
+ *
+ * csa2_shard_visible: n_vis_shard[q] = clamp(n_vis[q] - shard_lo, 0,
+ * shard_hi - shard_lo) for q < n_query; n_vis and n_vis_shard are [n_query]
+ * int32 device arrays; 0 <= shard_lo <= shard_hi (host). */
+csa2_status csa2_shard_visible(csa2_ctx* ctx, void* stream, int32_t n_query, const int32_t* n_vis, int64_t shard_lo,
+                               int64_t shard_hi, int32_t* n_vis_shard);
+
+/* csa2_topk_pairs: a local selection sel [n_query, k] int32 (ascending, -1
+ * padded, entries relative to the shard) as pairs: pair_score[q, i] =
+ * scores[q, sel[q, i]] and pair_idx[q, i] = index_base + sel[q, i]; a -1
+ * entry gives (-inf, -1). scores [n_query, scores_ld] fp32 (the local scan's
+ * rows); pair_score [n_query, k] fp32 and pair_idx [n_query, k] int32. */
+csa2_status csa2_topk_pairs(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores, int64_t scores_ld,
+                            const int32_t* sel, int32_t k, int64_t index_base, float* pair_score, int32_t* pair_idx);
+
+/* csa2_topk_merge: the k best of n_lists pair lists, list-major as an
+ * all-gather leaves them: pair_score / pair_idx [n_lists, n_query, list_len]
+ * (fp32 / int32; entries with idx -1 are padding; each entry index appears
+ * in at most one list). out_idx [n_query, k] int32 receives the k pairs of
+ * largest score, ties to the lower entry index, -0.0 equal to +0.0, as
+ * entry indices in ascending order, -1 padded: exactly csa2_topk's selection
+ * over the same scores. n_lists * list_len must be at most 8,192 (else
+ * CSA2_ERR_UNSUPPORTED); scores must not be NaN. One launch. */
+csa2_status csa2_topk_merge(csa2_ctx* ctx, void* stream, int32_t n_query, int32_t n_lists, int32_t list_len,
+                            const float* pair_score, const int32_t* pair_idx, int32_t k, int32_t* out_idx);
+
+/* csa2_attend_partial: csa2_attend's softmax restricted to one shard's rows,
+ * left unnormalised and without the sink, for csa2_attend_combine. The rows
+ * are the window [max(lo, t-w+1), t] when with_window != 0 (one shard only),
+ * and the entries j of topk_idx [n_query, topk] (global indices; NULL for
+ * none) with shard_lo <= j < shard_hi, read from row pool_off[b] + j -
+ * shard_lo of this shard's pool. For each query and head, with s_r = scale *
+ * RoPE_t(q) . row_r and m a reference at least max_r s_r - 8 ln 2:
+ *   part_o [n_query, 64, 512] fp32 = sum_r exp(s_r - m) row_r (rope
+ *          channels not rotated back), 16-byte aligned
+ *   part_m [n_query, 64] fp32 = m (natural-log units; -inf when the shard
+ *          holds no row of that query)
+ *   part_l [n_query, 64] fp32 = sum_r exp(s_r - m)
+ * Window arguments are read only when with_window != 0. No workspace: one
+ * CTA per query. Entries outside the shard are skipped; an entry inside it
+ * but past the shard's pool is recorded as CSA2_FLAG_BAD_TOPK_INDEX. */
+csa2_status csa2_attend_partial(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q,
+                                const int64_t* q_pos, const int32_t* seq_of_q, int32_t with_window,
+                                const void* win_kv, const uint8_t* win_scale, const int64_t* win_off,
+                                const int64_t* win_lo, const void* pool_kv, const uint8_t* pool_scale,
+                                const int64_t* pool_off, const int32_t* topk_idx, int64_t shard_lo, int64_t shard_hi,
+                                float* part_o, float* part_m, float* part_l);
+
+/* csa2_attend_combine: the log-sum-exp combine of n_parts (1..16) partials
+ * laid out part-major as an all-gather leaves them: part_o [n_parts, n_query,
+ * 64, 512], part_m and part_l [n_parts, n_query, 64] (fp32). With M =
+ * max(max_g m_g, sink_h): out = sum_g e^(m_g - M) O_g / (sum_g e^(m_g - M) l_g
+ * + e^(sink_h - M)), its rope channels rotated back by -t (q_pos [n_query]
+ * int64), written as bf16 to out [n_query, 64, 512]; lse [n_query, 64] fp32
+ * (nullable) = M + log(den). sink [64] fp32. */
+csa2_status csa2_attend_combine(csa2_ctx* ctx, void* stream, int32_t n_query, int32_t n_parts, const float* part_o,
+                                const float* part_m, const float* part_l, const int64_t* q_pos, const float* sink,
+                                uint16_t* out, float* lse);
+
+/* ------------------------------------------------------------------------
  * csa2_attend_noalloc: csa2_attend for callers that cannot allocate device
  * memory themselves (a host that owns all device memory through its own pool
  * and forbids outside allocations, or a loop that must never trigger the

@@ -23,8 +23,8 @@ Sources (pages are cited by title and section):
        section "The op layer" (the finite score floor so an all-invalid row
        yields zeros).
 
-Readings where the pages leave a step open (each one is also listed in the
-design notes of the repository):
+Readings where the pages leave a step open, each taken as the plainest one
+that the rest of the pages support:
 
 * Gate logits are per channel: g has the same shape as the raw KV c and the
   softmax runs over the m tokens of a group, channel by channel (R, C2 step 1

@@ -2,11 +2,13 @@
 device tensors to float64 for the oracle, and the tolerances.
 
 Tolerances:
-  attention : per element |gpu - oracle| <= 2e-2 + 3 * 2^-9 * B + 2^-8 |oracle| + S,
+  attention : per element |gpu - oracle| <= 2e-2 + u (D + B + |oracle|) + S,
               and ||gpu - oracle|| / ||oracle|| <= 1e-2 per query, where
-              B = sum_r p_r |v_r| (the magnitude of the weighted sum before
-              cancellation) and S the fp32 score term; each term is derived in
-              attention_bound below
+              u = 2^-8 is bf16's unit roundoff, B = sum_r p_r |v_r| (the size
+              of the weighted sum before cancellation), D = sum_r p_r |v_r - o|
+              (its spread about the output) and S the fp32 score term; each
+              term is derived in attention_bound below
+  lse       : |gpu - oracle| <= u + max_r delta_r per head (lse_bound)
   scores    : |gpu - oracle| <= 1e-3 |oracle| + 1e-5 * sum_h |w_h| ||q_h|| ||k||
               (relative 1e-3, plus the fp32 accumulation bound of a 128-term dot)
   top-k     : bit-exact on identical fp32 scores
@@ -34,8 +36,7 @@ from oracle import formats as F
 
 ATT_MAX_ABS = 2e-2          # the stated flat bar for unit-scale outputs
 ATT_REL_L2 = 1e-2           # the stated relative-L2 bar, per query
-ATT_SUM = 3 * 2.0 ** -9     # times B = sum_r p_r |v_r|: bf16 P (2 * 2^-9) and bf16 split-K partials (2^-9)
-ATT_OUT = 2.0 ** -8         # times |oracle|: the bf16 rounding of the output (half an ulp)
+BF16_U = 2.0 ** -8          # bf16 unit roundoff: 8 significant bits, round to nearest
 ATT_MMA_STEPS = 40          # fp32 roundings of one score: 36 MMA K-steps of 16 (32 + 4 rope hi/lo) + margin
 ATT_WEIGHT_FIX = 2.0 ** -21  # per weight: the log2(e) scaling, the max subtraction and exp2f (2 ulp)
 
@@ -168,10 +169,11 @@ def assert_rows_close_stored(codes, scale, exact: np.ndarray, fmt: int, what: st
 
 class AttBound:
     """The magnitudes the attention error bound is built from, per head and
-    channel of one query: B = sum_r p_r |v_r| and the fp32 score term S."""
+    channel of one query: B = sum_r p_r |v_r|, D = sum_r p_r |v_r - o| and
+    the fp32 score term S."""
 
-    def __init__(self, sum_pv: np.ndarray, score: np.ndarray):
-        self.sum_pv, self.score = sum_pv, score
+    def __init__(self, sum_pv: np.ndarray, spread: np.ndarray, score: np.ndarray):
+        self.sum_pv, self.spread, self.score = sum_pv, spread, score
 
 
 def attention_bound(q, t, rows, sink, scale, f) -> AttBound:
@@ -179,18 +181,21 @@ def attention_bound(q, t, rows, sink, scale, f) -> AttBound:
 
     The GPU computes o = sum_r P_r v_r / (sum_r P_r + e^sink) with bf16 rows,
     fp32 scores, P rounded to bf16 and an fp32 sum. Against the float64
-    oracle (w_r = p_r / den its exact weights, o its output):
-      * P in bf16: each weight moves by at most 2^-9 of itself, and the
-        denominator sums the same rounded weights, so o moves by at most
-        2^-9 sum_r w_r |v_r - o| <= 2^-9 (B + |o|) <= 2 * 2^-9 B;
-      * split-K partials stored in bf16: each partial moves by 2^-9 of its
-        own weighted sum, which the merge weights bring to 2^-9 B in all;
-      * the output rounded to bf16: half an ulp, at most 2^-8 |o|;
+    oracle (w_r = p_r / den its exact weights, o its output, u = 2^-8 the
+    bf16 unit roundoff):
+      * P in bf16: each weight moves by at most u of itself, and the
+        denominator sums the same rounded weights, so to first order o moves
+        by sum_r w_r eps_r (v_r - o), at most u D with D = sum_r w_r |v_r - o|;
+      * split-K partials stored in bf16: each partial moves by at most u of
+        its own weighted sum, which the merge weights bring to u B in all,
+        B = sum_r w_r |v_r|;
+      * the output rounded to bf16: half an ulp, at most u |o|;
       * fp32 scores: s_r = tau q~ . v_r accumulated by the tensor core in
-        fp32 over 36 K-steps, each rounding at most 2^-24 of the running
-        sum (<= tau sum_i |q~_i| |v_ri|); with the exp2 and scaling steps each
-        weight's relative error is delta_r <= 40 * 2^-24 * tau * sum_i |q~_i||v_ri|
-        + 2^-21, and o moves by at most S = sum_r w_r delta_r (|v_r| + |o|).
+        fp32 over 36 K-steps, each rounding at most 2^-24 of a running sum no
+        larger than tau sum_i |q~_i| |v_ri|; with the exp2 and scaling steps
+        each weight's relative error is delta_r <= 40 * 2^-24 * tau *
+        sum_i |q~_i||v_ri| + 2^-21, and o moves by at most
+        S = sum_r w_r delta_r |v_r - o|.
     The two channels of a rope pair share the sum of their bounds, since the
     output's de-rotation mixes them.
     """
@@ -198,18 +203,34 @@ def attention_bound(q, t, rows, sink, scale, f) -> AttBound:
     rows = np.asarray(rows, dtype=np.float64).reshape(-1, np.asarray(q).shape[1])
     ar = np.abs(rows)
     bnd = p @ ar
+    o = p @ rows  # [H, D], the output before the de-rotation (p already includes the sink's share)
+    dev = np.abs(rows[None, :, :] - o[:, None, :])  # [H, R, D]: |v_r - o|
+    spread = np.einsum("hr,hrd->hd", p, dev)
     qr = O.rope_rotate(np.asarray(q, dtype=np.float64), t, f)
     delta = ATT_MMA_STEPS * 2.0 ** -24 * abs(scale) * (np.abs(qr) @ ar.T) + ATT_WEIGHT_FIX  # [H, R]
-    pd = p * delta
-    sc = pd @ ar + pd.sum(axis=1, keepdims=True) * np.abs(p @ rows)
+    sc = np.einsum("hr,hrd->hd", p * delta, dev)
+    del dev
     r = 2 * f.shape[0]
     if r:
         d = bnd.shape[-1]
-        for x in (bnd, sc):
+        for x in (bnd, spread, sc):
             pair = x[:, d - r::2] + x[:, d - r + 1::2]
             x[:, d - r::2] = pair
             x[:, d - r + 1::2] = pair
-    return AttBound(bnd, sc)
+    return AttBound(bnd, spread, sc)
+
+
+def lse_bound(q, t, rows, scale, f) -> np.ndarray:
+    """Per head bound on |lse_gpu - lse_oracle|: the denominator sums the
+    bf16-rounded weights (relative u = 2^-8, so log(den) moves by at most u)
+    and each weight carries the fp32 score error delta_r of attention_bound,
+    so log(den) moves by at most max_r delta_r more."""
+    rows = np.asarray(rows, dtype=np.float64).reshape(-1, np.asarray(q).shape[1])
+    if rows.shape[0] == 0:
+        return np.full(np.asarray(q).shape[0], 1e-6)
+    qr = O.rope_rotate(np.asarray(q, dtype=np.float64), t, f)
+    delta = ATT_MMA_STEPS * 2.0 ** -24 * abs(scale) * (np.abs(qr) @ np.abs(rows).T) + ATT_WEIGHT_FIX
+    return BF16_U + delta.max(axis=1) + 1e-6
 
 
 def _current_test() -> str:
@@ -217,12 +238,12 @@ def _current_test() -> str:
 
 
 def assert_attention_close(got: np.ndarray, ref: np.ndarray, bound: AttBound, what: str = ""):
-    """Per element |gpu - oracle| <= 2e-2 + 3 * 2^-9 B + 2^-8 |oracle| + S, and
+    """Per element |gpu - oracle| <= 2e-2 + u (D + B + |oracle|) + S, and
     rel-L2 <= 1e-2 (terms as in attention_bound). The raw max-abs error and
     rel-L2 against the flat 2e-2 / 1e-2 bars go to PARITY_LOG and into the
     assertion message."""
     err = np.abs(got - ref)
-    lim = ATT_MAX_ABS + ATT_SUM * bound.sum_pv + ATT_OUT * np.abs(ref) + bound.score
+    lim = ATT_MAX_ABS + BF16_U * (bound.spread + bound.sum_pv + np.abs(ref)) + bound.score
     worst = int(np.argmax(err / lim)) if err.size else 0
     den = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got - ref))
@@ -232,7 +253,8 @@ def assert_attention_close(got: np.ndarray, ref: np.ndarray, bound: AttBound, wh
     PARITY_LOG.append((_current_test(), what, max_abs, rel, used, n_over, int(err.size)))
     ok = bool(np.all(err <= lim)) and rel <= ATT_REL_L2
     assert ok, (f"{what}: worst |err| {float(err.flat[worst]):.3e} at |ref| {float(np.abs(ref).flat[worst]):.3e} "
-                f"(B {float(bound.sum_pv.flat[worst]):.3e}, S {float(bound.score.flat[worst]):.3e}, limit "
+                f"(B {float(bound.sum_pv.flat[worst]):.3e}, D {float(bound.spread.flat[worst]):.3e}, "
+                f"S {float(bound.score.flat[worst]):.3e}, limit "
                 f"{float(lim.flat[worst]):.3e}); max-abs {max_abs:.3e} vs 2e-2 ({n_over} elements above), "
                 f"rel-L2 {rel:.3e} vs 1e-2")
 
