@@ -363,6 +363,14 @@ __device__ __forceinline__ void mma_16816_bf16(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel of its stream still runs: it must wait here before it
+// reads anything that kernel writes. Without such a launch this returns at
+// once. The trigger lets this kernel's dependents start before it ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- small utils
 
 __device__ __forceinline__ int find_segment(const int64_t* off, int n, int64_t x) {

@@ -108,7 +108,7 @@ static void release(csa2_ctx* ctx) {
   if (ctx->d_work) cudaFree(ctx->d_work);
   if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->copy) cudaStreamDestroy(ctx->copy);
-  for (cudaEvent_t ev : {ctx->ev_fork, ctx->ev_idx, ctx->ev_tail, ctx->ev_join, ctx->ev_topk, ctx->ev_copy, ctx->ev_q})
+  for (cudaEvent_t ev : {ctx->ev_join, ctx->ev_topk, ctx->ev_copy, ctx->ev_q})
     if (ev) cudaEventDestroy(ev);
   delete ctx;
 }
@@ -142,10 +142,11 @@ csa2_status csa2_create(const csa2_config* cfg, csa2_ctx** out) {
   if (e == cudaSuccess) e = cudaMemset(ctx->d_flags, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMalloc(&ctx->d_work, 2 * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(ctx->d_work, 0, 2 * sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_idx, cudaEventDisableTiming);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_tail, cudaEventDisableTiming);
+  int prio_low = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&prio_low, &ctx->prio_high);
+  // the side stream carries the work that runs beside the caller's stream (a
+  // candidate source's pool beside its attention): it goes first when both wait for SMs
+  if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&ctx->side, cudaStreamNonBlocking, ctx->prio_high);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->ev_topk, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ctx->copy, cudaStreamNonBlocking);
@@ -228,7 +229,7 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
                                const float* k_norm_w, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
                                uint8_t* idx_key_scale, bool append = false, uint16_t* state_raw = nullptr,
-                               float* state_gate = nullptr) {
+                               float* state_gate = nullptr, const csa2::CompressTail* tail = nullptr) {
   const csa2_config& c = ctx->cfg;
   const int m = c.compress_ratio;
   if (n_tokens < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_seq / n_tokens");
@@ -255,7 +256,7 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                         w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
                                         c.kv_format, c.idx_key_format,
                                         pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags,
-                                        append ? &app : nullptr, &nl);
+                                        append ? &app : nullptr, &nl, tail);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -284,13 +285,13 @@ csa2_status csa2_compress_append(csa2_ctx* ctx, void* stream, const uint16_t* ra
 }
 
 // new_first / new_tok set: the scan leaves out the entries that this step's
-// compress writes (see IdxArgs); the caller scores them with do_index_tail
+// compress writes (see IdxArgs); the compress kernel scores them
 static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32_t n_query, const uint16_t* q_idx,
                             const float* w_heads, const void* idx_keys, const uint8_t* idx_key_scale,
                             const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
                             float* scores, int64_t ld, const int64_t* new_first = nullptr,
-                            const int64_t* new_tok = nullptr, bool tail_only = false,
-                            const int32_t* cand = nullptr, int32_t* n_pool = nullptr) {
+                            const int64_t* new_tok = nullptr, const int32_t* cand = nullptr,
+                            int32_t* n_pool = nullptr, bool pdl = false) {
   const csa2_config& c = ctx->cfg;
   // a pool row holds at most cand_keep blocks of entries
   const int64_t row_need = cand != nullptr ? std::min(max_vis, (int64_t)c.cand_keep * c.cand_block) : max_vis;
@@ -327,15 +328,13 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
   ia.cand_shift = cand_shift(c);
   ia.n_pool = n_pool;
   cudaError_t e;
-  if (tail_only) {
-    e = csa2::launch_index_tail(st, c.idx_heads, kf, ia);
-  } else if (new_first == nullptr && cand == nullptr &&
+  if (new_first == nullptr && cand == nullptr &&
              csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)) {
     e = csa2::launch_index_score_tc(st, ctx->num_sms, c.idx_heads, n_query, n_seq, max_vis, q_idx, w_heads,
                                     reinterpret_cast<const uint16_t*>(idx_keys), pool_off, seq_of_q, n_vis, scores,
                                     ld, ctx->d_flags);
   } else {
-    e = csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, kf, ia);
+    e = csa2::launch_index_score(st, ctx->num_sms, c.idx_heads, kf, ia, pdl);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "index_score");
   ctx->last_launches += 1;
@@ -357,9 +356,11 @@ size_t csa2_topk_workspace_size(const csa2_ctx* ctx, int32_t n_query, int64_t ma
   return csa2::topk_workspace_bytes(n_query, max_vis);
 }
 
+// pdl: launched inside csa2_step right after the library's own index scan,
+// the top-k may start programmatically before the scan ends (it waits for it)
 static csa2_status do_topk(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, const float* scores, int64_t ld,
                            const int32_t* n_vis, int64_t max_vis, int32_t k, int32_t* out_idx, void* ws,
-                           size_t ws_bytes, const int32_t* map = nullptr) {
+                           size_t ws_bytes, const int32_t* map = nullptr, bool pdl = false) {
   if (n_query < 0 || max_vis < 0 || ld < max_vis || k < 1 || k > 2048)
     return fail(ctx, CSA2_ERR_INVALID_ARG, "topk: sizes (k must be 1..2048)");
   if (max_vis > 0xFFFFFFFEll) return fail(ctx, CSA2_ERR_UNSUPPORTED, "topk: rows longer than 2^32-2");
@@ -369,9 +370,10 @@ static csa2_status do_topk(csa2_ctx* ctx, cudaStream_t st, int32_t n_query, cons
   if (s != CSA2_OK) return s;
   int nl = 0;
   cudaError_t e = map == nullptr
-                      ? csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl)
+                      ? csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl, nullptr, 0, 0,
+                                          pdl)
                       : csa2::launch_topk(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, ws, &nl, map,
-                                          ctx->cfg.cand_keep, cand_shift(ctx->cfg));
+                                          ctx->cfg.cand_keep, cand_shift(ctx->cfg), pdl);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "topk");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -427,8 +429,7 @@ csa2_status csa2_index_score_pool(csa2_ctx* ctx, void* stream, int32_t n_seq, in
   if (!cand || !n_pool) return fail(ctx, CSA2_ERR_INVALID_ARG, "index_score_pool: null pool");
   const int64_t ld = (int64_t)ctx->cfg.cand_keep * ctx->cfg.cand_block;
   return do_index(ctx, reinterpret_cast<cudaStream_t>(stream), n_seq, n_query, q_idx, w_heads, idx_keys,
-                  idx_key_scale, pool_off, seq_of_q, n_vis, max_vis, scores_pool, ld, nullptr, nullptr, false, cand,
-                  n_pool);
+                  idx_key_scale, pool_off, seq_of_q, n_vis, max_vis, scores_pool, ld, nullptr, nullptr, cand, n_pool);
 }
 
 csa2_status csa2_topk_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const float* scores_pool,
@@ -444,10 +445,7 @@ csa2_status csa2_topk_pool(csa2_ctx* ctx, void* stream, int32_t n_query, const f
 
 size_t csa2_attend_workspace_size(const csa2_ctx* ctx, int32_t n_query) {
   if (!ctx || n_query < 0) return 0;
-  // the step's split plan or the single-launch plan, whichever needs more
-  return std::max(
-      csa2::attend_workspace_bytes(n_query, csa2::attend_plan(n_query, ctx->cfg.topk, true, ctx->num_sms)),
-      csa2::attend_workspace_bytes(n_query, csa2::attend_plan_single(n_query, ctx->cfg.topk, true, ctx->num_sms)));
+  return csa2::attend_workspace_bytes(n_query, csa2::attend_plan(n_query, ctx->cfg.topk, true, ctx->num_sms));
 }
 
 // validates the attend arguments and fills the kernel parameters
@@ -781,40 +779,40 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
     return e;
   };
   // A decode-shaped Full step (at most two closing groups per sequence, the
-  // scan in its CUDA-core form) runs compress on the side stream beside the
-  // scan of the entries that existed before the step. The scan hands out its
-  // work by tickets, so the SMs compress holds at the start cost it nothing.
-  // The tail kernel then scores the entries compress wrote, and the caller's
-  // stream waits for both before top-k.
+  // scan in its CUDA-core form): compress runs first on the caller's stream
+  // and scores the entries it writes itself, from the keys it stores. The
+  // scan over the entries that existed before the step starts
+  // programmatically beside it (its CTAs take the SMs compress leaves, and
+  // wait for compress only before they exit), so that every kernel of the
+  // step after compress has a single predecessor and can start early.
   const bool full = a->mode == CSA2_MODE_FULL;
   const bool overlap = full && !pool_read && a->n_query > 0 && a->max_vis > 0 && a->n_tokens <= 2LL * m * a->n_seq &&
                        !csa2::index_tc_suited(ctx->cfg.idx_key_format != CSA2_KV_BF16, a->n_query, a->n_seq,
                                               ctx->cfg.idx_heads);
-  const bool tail = overlap && a->w_idx != nullptr;  // compress writes index keys: score the new ones apart
+  const bool tail = overlap && a->w_idx != nullptr;  // compress writes index keys: it scores the new ones
   if (full) {
-    cudaStream_t cs = st;
-    if (overlap) {
-      cudaError_t e = cudaEventRecord(ctx->ev_fork, st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0);
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "step: fork");
-      side_open = true;
-      cs = ctx->side;
-    }
-    cudaError_t ce = copy_tokens(cs);
+    cudaError_t ce = copy_tokens(st);
     if (ce != cudaSuccess) return join(cuda_fail(ctx, ce, "step: copy of the raw tokens"));
     ctx->last_launches = 0;
-    s = do_compress(ctx, cs, raw_in, gate_in, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
+    csa2::CompressTail ct;
+    if (tail) {
+      if (!a->q_idx || !a->w_heads || !a->seq_of_q || !a->n_vis || !aligned16(a->q_idx))
+        return join(fail(ctx, CSA2_ERR_INVALID_ARG, "step: index arguments missing or misaligned"));
+      ct.n_query = a->n_query;
+      ct.idx_heads = ctx->cfg.idx_heads;
+      ct.max_vis = a->max_vis;
+      ct.ld = ld;
+      ct.seq_of_q = a->seq_of_q;
+      ct.n_vis = a->n_vis;
+      ct.q_idx = a->q_idx;
+      ct.w_heads = a->w_heads;
+      ct.scores = scores;
+    }
+    s = do_compress(ctx, st, raw_in, gate_in, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
                     a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale,
-                    a->append != 0, a->state_raw, a->state_gate);
+                    a->append != 0, a->state_raw, a->state_gate, tail ? &ct : nullptr);
     if (s != CSA2_OK) return join(s);
     launches += ctx->last_launches;
-    if (tail) {
-      ctx->last_launches = 0;
-      s = do_index(ctx, ctx->side, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale,
-                   a->pool_off, a->seq_of_q, a->n_vis, a->max_vis, scores, ld, a->first_pos, a->tok_off, true);
-      if (s != CSA2_OK) return join(s);
-      launches += ctx->last_launches;
-    }
   }
   if (!full) {
     const cudaError_t ce = copy_tokens(st);
@@ -837,39 +835,24 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
   ctx->last_launches = 0;
   if (pool_read)  // the hierarchical indexer's second level: score inside the pool only
     s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
-                 a->seq_of_q, a->n_vis, a->max_vis, scores, ldc, nullptr, nullptr, false, a->cand, n_pool);
+                 a->seq_of_q, a->n_vis, a->max_vis, scores, ldc, nullptr, nullptr, a->cand, n_pool);
   else
     s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
                  a->seq_of_q, a->n_vis, a->max_vis, scores, ld, tail ? a->first_pos : nullptr,
-                 tail ? a->tok_off : nullptr);
+                 tail ? a->tok_off : nullptr, nullptr, nullptr, overlap && a->n_tokens > 0);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
   cudaError_t e = stage_q();
   if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: copy of q"));
-  if (overlap) {
-    e = cudaEventRecord(ctx->ev_tail, ctx->side);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ev_tail, 0);
-    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: wait for compress"));
-  }
-  // The window tile reads only the window buffer, which nothing in the step
-  // writes. It runs on the side stream beside top-k, whose grid (a cluster per
-  // query) leaves most SMs free; the caller's stream joins it before the
-  // merge. It starts after the index scan, whose CTAs fill every SM.
-  if (pl.split_window) {
-    e = cudaEventRecord(ctx->ev_idx, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->side, ctx->ev_idx, 0);
-    if (e == cudaSuccess) {
-      side_open = true;
-      e = wait_q(ctx->side);
-      if (e == cudaSuccess) e = csa2::launch_attend_window(ctx->side, kvf, ap, pl, at_ws, &launches);
-    }
-    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: window tile"));
-  }
+  // top-k follows the library's own scan on this stream: it starts
+  // programmatically and waits for the scan before reading the scores
   ctx->last_launches = 0;
   if (pool_read)
-    s = do_topk(ctx, st, a->n_query, scores, ldc, n_pool, ldc, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes, a->cand);
+    s = do_topk(ctx, st, a->n_query, scores, ldc, n_pool, ldc, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes, a->cand,
+                true);
   else
-    s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes);
+    s = do_topk(ctx, st, a->n_query, scores, ld, a->n_vis, a->max_vis, ctx->cfg.topk, a->topk_idx, tk_ws, tk_bytes,
+                nullptr, true);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
   if (pool_src) {
@@ -878,18 +861,14 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
   }
   e = wait_q(st);
   if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: wait for q"));
-  if (pl.split_window) {
-    e = csa2::launch_attend_main(st, kvf, ap, pl, at_ws, &launches);
-    if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
-    s = join(CSA2_OK);
-    if (s != CSA2_OK) return s;
-    e = csa2::launch_attend_merge(st, ap, pl, at_ws, &launches);
-  } else {
-    s = join(CSA2_OK);
-    if (s != CSA2_OK) return s;
-    e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
-  }
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "step: attend");
+  // The attention follows the library's own top-k on this stream: its CTAs
+  // start programmatically, the window tiles (the first CTA of each query)
+  // run beside top-k, and the selection is read after waiting for it. Its
+  // other inputs are the step's, complete before the step began or ordered
+  // by events. The merge follows the attention the same way.
+  ap.pdl = 1;
+  e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
+  if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
   if (pool_src) {
     // the candidate source's pool, for the layers after it, on the side
     // stream beside the attention; the caller's stream waits for it last

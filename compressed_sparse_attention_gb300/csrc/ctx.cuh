@@ -8,13 +8,11 @@ struct csa2_ctx {
   csa2_config cfg;
   int device = 0;
   int num_sms = 0;
+  int prio_high = 0;  // the device's greatest stream priority: the side stream's, and the window tile's launches
   csa2::RopeParams rope;
   uint32_t* d_flags = nullptr;
   unsigned long long* d_work = nullptr;  // [2] ticket counters of the index scan (zero between launches)
-  cudaStream_t side = nullptr;    // step side stream: compress and the tail scores, then the window tile
-  cudaEvent_t ev_fork = nullptr;  // recorded on the caller's stream at the start of a step
-  cudaEvent_t ev_idx = nullptr;   // recorded on the caller's stream after the index scan
-  cudaEvent_t ev_tail = nullptr;  // recorded on the side stream after compress and the tail scores
+  cudaStream_t side = nullptr;    // step side stream: a candidate source's pool, beside its attention
   cudaEvent_t ev_join = nullptr;  // recorded on the side stream after its last launch
   cudaEvent_t ev_topk = nullptr;  // recorded on the caller's stream after a candidate source's top-k
   cudaStream_t copy = nullptr;    // host-buffer steps: the copy of q beside the first half of the step

@@ -88,19 +88,22 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const uint32_t mbar = base_s + SM_MISC;
   const uint32_t tslot = base_s + SM_MISC + 8;
 
+  if (p.pdl) pdl_trigger();  // the merge may take the room this grid leaves
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, hh = warp >> 2;  // lane quadrant and head half
   const int row = quad * 32 + lane;           // this thread's tile row / output dim in a 128 block
-  const int qi = blockIdx.x / p.n_split, split = blockIdx.x % p.n_split;
-  // split 0 takes the launch's first tile alone when lead_single is set (the
-  // window tile); the other splits take tiles_per_split tiles each
-  const int lead = p.lead_single ? 1 : 0;
-  const int tile_begin = (lead && split == 0) ? p.tile_base : p.tile_base + lead + (split - lead) * p.tiles_per_split;
-  const int tile_cap0 = (lead && split == 0) ? tile_begin + 1 : tile_begin + p.tiles_per_split;
+  // CTAs are numbered split-major (all queries' first CTAs first, which hold
+  // the window tile and start before the selection exists). Split 0 takes
+  // the launch's first lead_tiles tiles, the others tiles_per_split each.
+  const int qi = blockIdx.x % p.n_query, split = blockIdx.x / p.n_query;
+  const int lead = p.lead_tiles;
+  const int tile_begin = split == 0 ? p.tile_base : p.tile_base + lead + (split - 1) * p.tiles_per_split;
+  const int tile_cap0 = split == 0 ? tile_begin + lead : tile_begin + p.tiles_per_split;
   const int tile_cap = min(tile_cap0, p.tile_base + p.tile_count);
   // every load that depends only on the query index is issued before the
   // setup below, so that their latencies overlap: the query's position and
-  // sequence, this thread's first selection entry, and Q itself
+  // sequence, Q itself, and (after the wait below) this thread's first
+  // selection entry
   const int64_t t = p.q_pos[qi];
   const int b = p.seq_of_q[qi];
   // selection entry of this thread's row in selected tile `tile` (-1 past k)
@@ -110,7 +113,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
                ? p.topk_idx[(int64_t)qi * p.topk + col]
                : -1;
   };
-  int32_t j_next = sel_entry(tile_begin, tile_cap);
+  // A plain launch fetches this thread's first selection entry at once; a
+  // programmatic one (after the step's top-k) only after pdl_wait() below.
+  int32_t j_next = p.pdl ? -1 : sel_entry(tile_begin, tile_cap);
   // Q is copied asynchronously into its swizzled K-major slots (it lands
   // together with the first tile's rows); the rope channels are rotated in
   // place once both have arrived
@@ -136,6 +141,19 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t pool_b0 = p.pool_off != nullptr ? p.pool_off[bs] : 0;
   const int64_t pool_b1 = p.pool_off != nullptr ? p.pool_off[bs + 1] : 0;
   const int64_t lo_raw = (q_ok && p.win_lo) ? p.win_lo[bs] : 0;
+  // Launched programmatically after the step's top-k, this CTA may run before
+  // the selection exists: everything above reads step inputs only, the window
+  // tile needs no selection, and the selection is read after pdl_wait()
+  // before the first selected tile (a plain launch returns at once).
+  // Deferred only when the selection may still be in the making and the
+  // query's first CTA has the window tile to run meanwhile (several CTAs a
+  // query); otherwise the first tile's entries are fetched now, ahead of it.
+  const bool defer_sel = p.pdl != 0 && p.n_split > 1;
+  bool sel_ready = !defer_sel;
+  if (p.pdl && sel_ready) {
+    pdl_wait();
+    j_next = sel_entry(tile_begin, tile_cap);
+  }
 
   if (warp == 0) {
     tmem_alloc(tslot, kTmemCols);
@@ -174,13 +192,31 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
   const int64_t plen = q_ok ? (pool_b1 - pool_b0) : 0;
 
-  for (int tile = tile_begin; tile < tile_end && !aborted; ++tile) {
+  // Two passes over the tiles: with the selection deferred, a CTA that starts
+  // at the window tile runs it alone in the first pass and waits for the
+  // selection between the passes (a wait inside the tile loop measured 4 %
+  // slower in prefill, where it never runs); otherwise the first pass takes
+  // every tile.
+  if (defer_sel && tile_begin >= 1) {
+    pdl_wait();
+    j_next = sel_entry(tile_begin, tile_end);
+    sel_ready = true;
+  }
+  int tile = tile_begin;
+  for (int pass = 0; pass < 2; ++pass) {
+  const int pass_end = (pass == 0 && !sel_ready) ? min(tile_end, 1) : tile_end;
+  if (pass == 1 && !sel_ready) {
+    pdl_wait();
+    j_next = sel_entry(tile, tile_end);
+    sel_ready = true;
+  }
+  for (; tile < pass_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row, the first 128)
     if (tid < kTileRows) {
       const int r = tid;
       int64_t src = -1;
       const int32_t j_cur = j_next;
-      j_next = sel_entry(tile + 1, tile_end);  // one tile ahead
+      j_next = sel_ready ? sel_entry(tile + 1, tile_end) : -1;  // one tile ahead
       if (tile == 0) {
         const int64_t pos = lo_eff + r;
         if (pos <= t && r < p.window) {
@@ -481,6 +517,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     if (!__syncthreads_and(ok)) { aborted = true; break; }
     tc_fence_after();
   }
+  }
 
   // ---- epilogue (no copy of Q may still be landing when the CTA exits,
   // e.g. for a query without tiles)
@@ -614,6 +651,7 @@ constexpr int kMergeHeadsPerCta = 4;
 __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p) {
   __shared__ float wsplit[8][kMergeHeadsPerCta];
   __shared__ float2 rope_tab[kMaxPairs];
+  pdl_wait();  // the partials of the selected tiles (a plain launch returns at once)
   const int qi = blockIdx.x / (kHeads / kMergeHeadsPerCta);
   const int hg = blockIdx.x % (kHeads / kMergeHeadsPerCta);
   const int tid = threadIdx.x, hl = tid >> 6, chunk = tid & 63;
@@ -789,45 +827,33 @@ cudaError_t launch_attend_combine(cudaStream_t st, int n_query, int n_parts, con
 
 int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTileRows - 1) / kTileRows : 0); }
 
-// One launch for the window and the selected tiles (Reuse steps, and
-// csa2_attend): at most one wave of CTAs (one a SM), each query's tiles split
-// evenly over floor(num_sms / n_query) CTAs; with many queries (prefill) one
-// CTA per query runs every tile and writes the output directly.
-AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms) {
-  AttendPlan pl{};
-  pl.n_tiles = attend_num_tiles(topk, has_idx);
-  if (n_query < 1) n_query = 1;
-  pl.split_window = 0;
-  int ns = num_sms / n_query;
-  if (ns > pl.n_tiles) ns = pl.n_tiles;
-  if (ns > 8) ns = 8;
-  if (ns < 1) ns = 1;
-  pl.tps = (pl.n_tiles + ns - 1) / ns;
-  pl.ns = (pl.n_tiles + pl.tps - 1) / pl.tps;
-  pl.n_slots = pl.ns > 1 ? pl.ns : 0;
-  return pl;
-}
-
-// How a step's attention is cut into launches. With few queries (decode) the
-// window tile, which does not depend on the selection, is its own launch (the
-// step runs it on a side stream beside top-k), the selected tiles are cut so
-// that all their CTAs fit in one wave, and a merge combines the partials.
-// Otherwise the single-launch plan above.
+// How one attention call is cut, in one launch. With few queries (decode:
+// 2 Q <= SMs) each query's tiles go to at most one wave of CTAs:
+// floor(SMs / Q) CTAs a query (at most 8), the selected tiles split evenly
+// (tps each) and the first CTA also taking the window tile, which needs no
+// selection: launched after the step's top-k, it runs while the selection is
+// still being made. A merge combines the CTAs' partials. With many queries
+// (prefill) one CTA per query runs every tile and writes the output directly.
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
   AttendPlan pl{};
   pl.n_tiles = attend_num_tiles(topk, has_idx);
   if (n_query < 1) n_query = 1;
-  if (pl.n_tiles >= 2 && 2 * n_query <= num_sms) {
-    pl.split_window = 1;
-    int ns = num_sms / n_query;
-    if (ns > pl.n_tiles - 1) ns = pl.n_tiles - 1;
-    if (ns > 7) ns = 7;
-    pl.tps = (pl.n_tiles - 1 + ns - 1) / ns;
-    pl.ns = (pl.n_tiles - 1 + pl.tps - 1) / pl.tps;
-    pl.n_slots = 1 + pl.ns;
-  } else {
-    pl = attend_plan_single(n_query, topk, has_idx, num_sms);
+  const int n_sel = pl.n_tiles - 1;
+  int ns = 2 * n_query <= num_sms ? num_sms / n_query : 1;
+  if (ns > n_sel) ns = n_sel;
+  if (ns > 8) ns = 8;
+  if (ns < 1) ns = 1;
+  if (ns == 1) {
+    pl.tps = pl.n_tiles;
+    pl.lead = pl.n_tiles;
+    pl.ns = 1;
+    pl.n_slots = 0;
+    return pl;
   }
+  pl.tps = (n_sel + ns - 1) / ns;
+  pl.ns = (n_sel + pl.tps - 1) / pl.tps;
+  pl.lead = 1 + pl.tps;
+  pl.n_slots = pl.ns;
   return pl;
 }
 
@@ -853,7 +879,8 @@ static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams&
 #define CSA2_ATT(F)                                                                                          \
   do {                                                                                                       \
     e = cudaFuncSetAttribute(attend_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttSmemBytes); \
-    if (e == cudaSuccess) attend_kernel<F><<<grid, kAttThreads, kAttSmemBytes, st>>>(p);                     \
+    if (e == cudaSuccess)                                                                                    \
+      e = launch_ex(attend_kernel<F>, grid, dim3(kAttThreads), kAttSmemBytes, st, p.pdl != 0, p.priority, p);  \
   } while (0)
   if (kv_fmt == 1) CSA2_ATT(1);
   else if (kv_fmt == 2) CSA2_ATT(2);
@@ -864,47 +891,27 @@ static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams&
   return cudaGetLastError();
 }
 
-cudaError_t launch_attend_window(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
-                                 int* n_launch) {
-  if (p.n_query == 0 || !pl.split_window) return cudaSuccess;
-  attach_ws(p, pl, ws);
-  p.n_tiles = pl.n_tiles;
-  p.tile_base = 0;
-  p.tile_count = 1;
-  p.n_split = 1;
-  p.tiles_per_split = 1;
-  p.lead_single = 0;
-  p.slot_base = 0;
-  p.direct = 0;
-  return launch_tiles(st, kv_fmt, p, n_launch);
-}
-
 cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                int* n_launch) {
   if (p.n_query == 0) return cudaSuccess;
   attach_ws(p, pl, ws);
   p.n_tiles = pl.n_tiles;
+  p.tile_base = 0;
+  p.tile_count = pl.n_tiles;
   p.n_split = pl.ns;
   p.tiles_per_split = pl.tps;
-  p.lead_single = 0;
-  if (pl.split_window) {
-    p.tile_base = 1;
-    p.tile_count = pl.n_tiles - 1;
-    p.slot_base = 1;
-    p.direct = 0;
-  } else {
-    p.tile_base = 0;
-    p.tile_count = pl.n_tiles;
-    p.slot_base = 0;
-    p.direct = pl.ns == 1 ? 1 : 0;
-  }
+  p.lead_tiles = pl.lead;
+  p.slot_base = 0;
+  p.direct = pl.ns == 1 ? 1 : 0;
   return launch_tiles(st, kv_fmt, p, n_launch);
 }
 
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch) {
   if (p.n_query == 0 || pl.n_slots == 0) return cudaSuccess;
   attach_ws(p, pl, ws);
-  attend_merge_kernel<<<p.n_query * (kHeads / kMergeHeadsPerCta), 256, 0, st>>>(p);
+  const cudaError_t e = launch_ex(attend_merge_kernel, dim3(p.n_query * (kHeads / kMergeHeadsPerCta)), dim3(256), 0,
+                                  st, p.pdl != 0, 0, p);
+  if (e != cudaSuccess) return e;
   *n_launch += 1;
   return cudaGetLastError();
 }
@@ -916,7 +923,7 @@ cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, i
   p.tile_count = p.n_tiles - p.tile_base;
   p.n_split = 1;
   p.tiles_per_split = p.tile_count;
-  p.lead_single = 0;
+  p.lead_tiles = p.tile_count;
   p.slot_base = 0;
   p.n_slots = 0;
   p.direct = 2;
@@ -924,8 +931,7 @@ cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, i
 }
 
 cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch) {
-  // on one stream the window tile and the selected tiles share one launch
-  const AttendPlan pl = attend_plan_single(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
+  const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
   cudaError_t e = launch_attend_main(st, kv_fmt, p, pl, ws, n_launch);
   if (e == cudaSuccess) e = launch_attend_merge(st, p, pl, ws, n_launch);
   return e;

@@ -165,10 +165,12 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     const uint16_t* __restrict__ w_idx, const float* __restrict__ k_norm_w, int idx_dim, float eps,
     RopeParams rp, void* __restrict__ pool_kv, uint8_t* __restrict__ pool_kv_scale,
     void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags, int append,
-    const uint16_t* __restrict__ st_raw, const float* __restrict__ st_gate) {
+    const uint16_t* __restrict__ st_raw, const float* __restrict__ st_gate, const CompressTail tail) {
   __shared__ float c_hat_s[kDim];
   __shared__ float k_lin_s[kIdxDim];
+  __shared__ float k_st_s[kIdxDim];  // the stored key's exact values (tail scoring)
   __shared__ float red_s[8];
+  pdl_trigger();  // the step's index scan starts beside this grid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // ---- index-key weights first: nothing they depend on
   uint4 wa[16], wb[16];
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   uint32_t rw[16];
   float2 gv[16];
   int64_t j, prow;
+  int seq_b = 0;
   if (!append) {
     const int64_t tok0 = (int64_t)blockIdx.x * m;
     // the group's tokens depend only on the group index: load them before the
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
       }
     }
     const int b = find_segment_warp(tok_off, n_seq, tok0);
+    seq_b = b;
     const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
     const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
     j = pos0 / m;
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   } else {
     int b;
     if (!find_append_group(tok_off, first_pos, n_seq, m, blockIdx.x, &b, &j)) return;  // past the last group
+    seq_b = b;
     const int64_t seg0 = tok_off[b], fp = first_pos[b];
     prow = pool_off[b] + j;
     if (prow >= pool_off[b + 1]) {
@@ -304,14 +309,18 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
       const int o = warp * 32 + lane;
       const float kv = k_lin_s[o] * kinv * knw;
       if constexpr (IKF == 0) {
-        reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] = (uint16_t)(pack_bf16(kv, 0.f) & 0xFFFFu);
+        const uint32_t bits = pack_bf16(kv, 0.f) & 0xFFFFu;
+        reinterpret_cast<uint16_t*>(idx_keys)[prow * idx_dim + o] = (uint16_t)bits;
+        k_st_s[o] = bf16lo(bits);
       } else if constexpr (IKF == 1) {
         float amax = fabsf(kv);
 #pragma unroll
         for (int sh = 16; sh > 0; sh >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, sh));
         const uint32_t eb = fp8_scale_byte(amax);
-        reinterpret_cast<uint8_t*>(idx_keys)[prow * idx_dim + o] = f32_to_e4m3(ldexpf(kv, 127 - (int)eb));
+        const uint8_t code = f32_to_e4m3(ldexpf(kv, 127 - (int)eb));
+        reinterpret_cast<uint8_t*>(idx_keys)[prow * idx_dim + o] = code;
         if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + warp] = (uint8_t)eb;
+        k_st_s[o] = e4m3_value(code) * ue8m0_value(eb);
       }
       else {
         // mxfp4: this warp's 32 outputs are one scale block; lanes 2i, 2i+1 share a byte
@@ -323,6 +332,32 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
         const uint32_t partner = __shfl_xor_sync(0xffffffffu, code, 1);
         if ((lane & 1) == 0) reinterpret_cast<uint8_t*>(idx_keys)[prow * (idx_dim / 2) + o / 2] = (uint8_t)(code | (partner << 4));
         if (lane == 0) idx_key_scale[prow * (idx_dim / 32) + warp] = (uint8_t)eb;
+        k_st_s[o] = e2m1x2_to_float2_scaled(code).x * kE2M1Unscale * ue8m0_value(eb);
+      }
+    }
+    if (tail.scores != nullptr) {
+      // this entry's scores for the queries of its sequence that see it
+      // (warp w takes queries w, w + 8, ...; lane l channels 4l .. 4l+3)
+      __syncthreads();
+      const int64_t plen = pool_off[seq_b + 1] - pool_off[seq_b];
+      const float4 kk = *reinterpret_cast<const float4*>(&k_st_s[4 * lane]);
+      for (int q = warp; q < tail.n_query; q += kCmpThreads / 32) {
+        if (tail.seq_of_q[q] != seq_b) continue;
+        const int64_t nv = min((int64_t)max(tail.n_vis[q], 0), min(plen, tail.max_vis));
+        if (j >= nv) continue;
+        float sigma = 0.f;
+        for (int h = 0; h < tail.idx_heads; ++h) {
+          const uint2 v = *reinterpret_cast<const uint2*>(tail.q_idx + ((int64_t)q * tail.idx_heads + h) * kIdxDim +
+                                                          4 * lane);
+          float d = bf16lo(v.x) * kk.x;
+          d = fmaf(bf16hi(v.x), kk.y, d);
+          d = fmaf(bf16lo(v.y), kk.z, d);
+          d = fmaf(bf16hi(v.y), kk.w, d);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          sigma = fmaf(tail.w_heads[(int64_t)q * tail.idx_heads + h], fmaxf(d, 0.f), sigma);
+        }
+        if (lane == 0) tail.scores[(int64_t)q * tail.ld + j] = sigma;
       }
     }
   }
@@ -420,9 +455,11 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
                             const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fmt,
                             int idx_fmt, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
-                            uint8_t* idx_key_scale, uint32_t* flags, const AppendArgs* app, int* n_launch) {
+                            uint8_t* idx_key_scale, uint32_t* flags, const AppendArgs* app, int* n_launch,
+                            const CompressTail* tail) {
   if (n_groups == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_groups);
+  const CompressTail tl = (tail != nullptr && w_idx != nullptr) ? *tail : CompressTail{};
   const int append = app != nullptr ? 1 : 0;
   const uint16_t* st_raw = app != nullptr ? app->state_raw : nullptr;
   const float* st_gate = app != nullptr ? app->state_gate : nullptr;
@@ -430,7 +467,7 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   compress_kernel<KF, IF><<<grid, kCmpThreads, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
                                                 norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
                                                 pool_kv_scale, idx_keys, idx_key_scale, flags, append, \
-                                                st_raw, st_gate)
+                                                st_raw, st_gate, tl)
 #define CSA2_COMPRESS_K(KF)                               \
   do {                                                    \
     if (idx_fmt == 1) CSA2_COMPRESS(KF, 1);               \

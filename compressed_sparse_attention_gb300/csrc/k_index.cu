@@ -125,6 +125,7 @@ template <int NT>
 __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs a) {
   constexpr int HI = NT * 8;
   __shared__ unsigned long long s_tk[2];
+  pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
   const uint16_t* keys = reinterpret_cast<const uint16_t*>(a.keys);
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
     tk.advance();
   }
   tk.finish();
+  pdl_wait();  // launched after compress: this grid ends only once compress has
 }
 
 // fp8 / mxfp4 keys ---------------------------------------------------------
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   constexpr int KB = KF == 3 ? kIdxDim / 2 : kIdxDim;  // code bytes a key
   constexpr int CH = 128 * U;                         // keys a work item
   __shared__ unsigned long long s_tk[2];
+  pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
   const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.keys);
@@ -429,72 +432,10 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
     tk.advance();
   }
   tk.finish();
+  pdl_wait();  // launched after compress: this grid ends only once compress has
 }
 
-// Scores of the entries compressed in this step (a decode step closes at
-// most a group or two per sequence): one warp per query, lane l holding
-// channels 4l .. 4l+3 of every head; keys of any of the three formats decode
-// exactly to fp32, products and sums in fp32. The scan above leaves these
-// entries out when new_first is set, so that it can run while the step's
-// compress is still writing them.
-template <int HI, int KF>
-__global__ void __launch_bounds__(256) index_tail_kernel(const IdxArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = blockIdx.x * 8 + warp;
-  if (q >= a.n_query) return;
-  const int b = a.seq_of_q[q];
-  if (b < 0 || b >= a.n_seq) return;  // flagged by the scan
-  if (a.new_tok[b + 1] <= a.new_tok[b]) return;
-  int n_all;
-  const int j_begin = idx_query_range(a, q, b, false, &n_all);
-  if (j_begin >= n_all) return;
-  float qv[HI][4], w[HI];
-#pragma unroll
-  for (int h = 0; h < HI; ++h) {
-    const uint2 v = *reinterpret_cast<const uint2*>(a.q_idx + ((int64_t)q * HI + h) * kIdxDim + 4 * lane);
-    qv[h][0] = bf16lo(v.x); qv[h][1] = bf16hi(v.x);
-    qv[h][2] = bf16lo(v.y); qv[h][3] = bf16hi(v.y);
-    w[h] = a.w_heads[(int64_t)q * HI + h];
-  }
-  const int64_t row0 = a.pool_off[b];
-  for (int j = j_begin; j < n_all; ++j) {
-    const int64_t row = row0 + j;
-    float k[4];
-    if constexpr (KF == 0) {
-      const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(a.keys) + row * kIdxDim +
-                                                      4 * lane);
-      k[0] = bf16lo(v.x); k[1] = bf16hi(v.x); k[2] = bf16lo(v.y); k[3] = bf16hi(v.y);
-    } else {
-      const float sc = ue8m0_value(a.key_scale[row * (kIdxDim / 32) + lane / 8]);
-      if constexpr (KF == 1) {
-        const uint32_t c = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(a.keys) +
-                                                              row * kIdxDim + 4 * lane);
-        const float2 f0 = e4m3x2_to_float2((uint16_t)(c & 0xFFFFu)), f1 = e4m3x2_to_float2((uint16_t)(c >> 16));
-        k[0] = f0.x * sc; k[1] = f0.y * sc; k[2] = f1.x * sc; k[3] = f1.y * sc;
-      } else {
-        const uint32_t c = *reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(a.keys) +
-                                                              row * (kIdxDim / 2) + 2 * lane);
-        const float2 f0 = e2m1x2_to_float2_scaled(c & 0xFFu), f1 = e2m1x2_to_float2_scaled(c >> 8);
-        const float s2 = sc * kE2M1Unscale;
-        k[0] = f0.x * s2; k[1] = f0.y * s2; k[2] = f1.x * s2; k[3] = f1.y * s2;
-      }
-    }
-    float sigma = 0.f;
-#pragma unroll
-    for (int h = 0; h < HI; ++h) {
-      float d = qv[h][0] * k[0];
-      d = fmaf(qv[h][1], k[1], d);
-      d = fmaf(qv[h][2], k[2], d);
-      d = fmaf(qv[h][3], k[3], d);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      sigma = fmaf(w[h], fmaxf(d, 0.f), sigma);
-    }
-    if (lane == 0) a.scores[(int64_t)q * a.ld + j] = sigma;
-  }
-}
-
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a) {
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a, bool pdl) {
   if (a.n_query == 0 || a.max_vis == 0) return cudaSuccess;
   const int64_t cap = (int64_t)num_sms * 2;
   // chunk of one work item: 256 keys (bf16; fp8 and mxfp4 with 32 heads), 512
@@ -506,11 +447,13 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
   const int64_t items = a.n_chunks * a.n_query;
   if (items >= (int64_t)1 << 32) return cudaErrorInvalidValue;  // item indices are split in 32 bits
   const dim3 grid((unsigned)(items < cap ? items : cap));
-#define CSA2_IDX(NT, UQ, U8)                                                         \
-  do {                                                                               \
-    if (idx_fmt == 1) index_score_fp8_kernel<NT, 1, U8><<<grid, 256, 0, st>>>(a);    \
-    else if (idx_fmt == 3) index_score_fp8_kernel<NT, 3, UQ><<<grid, 256, 0, st>>>(a); \
-    else index_score_bf16_kernel<NT><<<grid, 256, 0, st>>>(a);                       \
+  cudaError_t le = cudaSuccess;
+#define CSA2_IDX(NT, UQ, U8)                                                                          \
+  do {                                                                                                \
+    if (idx_fmt == 1) le = launch_ex(index_score_fp8_kernel<NT, 1, U8>, grid, dim3(256), 0, st, pdl, 0, a); \
+    else if (idx_fmt == 3)                                                                            \
+      le = launch_ex(index_score_fp8_kernel<NT, 3, UQ>, grid, dim3(256), 0, st, pdl, 0, a);           \
+    else le = launch_ex(index_score_bf16_kernel<NT>, grid, dim3(256), 0, st, pdl, 0, a);              \
   } while (0)
   switch (idx_heads) {
     case 8: CSA2_IDX(1, 4, 4); break;
@@ -519,25 +462,7 @@ cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int 
     default: return cudaErrorInvalidValue;
   }
 #undef CSA2_IDX
-  return cudaGetLastError();
-}
-
-cudaError_t launch_index_tail(cudaStream_t st, int idx_heads, int idx_fmt, const IdxArgs& a) {
-  if (a.n_query == 0 || a.max_vis == 0 || a.new_first == nullptr) return cudaSuccess;
-  const dim3 grid((unsigned)((a.n_query + 7) / 8));
-#define CSA2_TAIL(HI)                                                     \
-  do {                                                                    \
-    if (idx_fmt == 1) index_tail_kernel<HI, 1><<<grid, 256, 0, st>>>(a);  \
-    else if (idx_fmt == 3) index_tail_kernel<HI, 3><<<grid, 256, 0, st>>>(a); \
-    else index_tail_kernel<HI, 0><<<grid, 256, 0, st>>>(a);               \
-  } while (0)
-  switch (idx_heads) {
-    case 8: CSA2_TAIL(8); break;
-    case 16: CSA2_TAIL(16); break;
-    case 32: CSA2_TAIL(32); break;
-    default: return cudaErrorInvalidValue;
-  }
-#undef CSA2_TAIL
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

@@ -627,6 +627,8 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_cluster_kernel(const float
   uint32_t* misc = reinterpret_cast<uint32_t*>(tk_smem + L::MISC);
   uint32_t* warp_s = misc;
 
+  pdl_wait();  // the scores of the previous kernel
+  pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
   const uint32_t rank = cluster.block_rank();
   const uint32_t C = cluster.num_blocks();
@@ -913,31 +915,11 @@ struct TkMap {
   }
 };
 
-template <int TPB, int PER>
-__global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
-                                                      const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
-                                                      int32_t* __restrict__ out_idx, const TkMap map) {
-  constexpr int NW = TPB / 32;
-  constexpr int DB = 11;        // digit bits a level
-  constexpr int NB = 1 << DB;
-  constexpr int BPT = NB / TPB;  // bins a thread owns in the scan
-  static_assert(NB % TPB == 0 && TPB % 32 == 0 && PER % 4 == 0, "bins split evenly; float4 loads");
-  __shared__ uint32_t hist[NB];
-  __shared__ uint32_t res[3];
-  __shared__ uint32_t wtot[NW];
-  __shared__ unsigned long long wsum[NW];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = blockIdx.x;
-  const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
-  int32_t* out = out_idx + (int64_t)q * k;
-  if (n <= k) {
-    for (int i = tid; i < k; i += TPB) out[i] = i < n ? map(q, i) : -1;
-    return;
-  }
-  // ---- keys of this thread's entries, and the row's smallest and largest key
-  const float* row = scores + (int64_t)q * ld;
-  const int e0 = PER * tid;
-  uint32_t key[PER];
+// This thread's keys: entries PER t .. PER t + PER - 1 of the row as
+// order-preserving keys (0, below every score's key, past n).
+template <int PER>
+__device__ __forceinline__ void row_load_keys(const float* __restrict__ row, const float* __restrict__ scores, int64_t ld,
+                                              int e0, int n, uint32_t (&key)[PER]) {
   if (((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(scores) & 15) == 0) && e0 + PER <= n) {
 #pragma unroll
     for (int c = 0; c < PER / 4; ++c) {
@@ -951,15 +933,29 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
 #pragma unroll
     for (int i = 0; i < PER; ++i) key[i] = (e0 + i < n) ? score_key(row[e0 + i]) : 0u;
   }
-  // ---- threshold search: keys in play share their bits at and above `hi`
-  // with P (nothing yet at the start). Each level counts the next DB bits of
-  // the keys in play in one CTA-wide histogram (plain shared atomics); a block
-  // scan over the bins, from the top, finds the one that holds the k-th
-  // largest key.
-  int hi = 32;
-  uint32_t P = 0u;
-  uint32_t need = (uint32_t)k;
-  bool exact = false;
+}
+
+// Threshold search over the keys in play, eleven bits a level from the top
+// key bit: one CTA-wide histogram of the keys still in play (plain shared
+// atomics), a block scan over its bins finds the one that holds the k-th
+// largest key, and the search stops once that bin holds exactly the keys
+// still needed, or when no bits are left (ties at one key value). On return
+// the chosen entries are those with (key >> hi) > P, then `need` of those with
+// (key >> hi) == P in index order (all of them when exact).
+template <int TPB, int PER>
+__device__ __forceinline__ void row_radix_search(const uint32_t (&key)[PER], int e0, int n, uint32_t k,
+                                                 uint32_t* hist, uint32_t* res, uint32_t* wtot, uint32_t& P, int& hi,
+                                                 uint32_t& need, bool& exact) {
+  constexpr int NW = TPB / 32;
+  constexpr int DB = 11;        // digit bits a level
+  constexpr int NB = 1 << DB;
+  constexpr int BPT = NB / TPB;  // bins a thread owns in the scan
+  static_assert(NB % TPB == 0 && TPB % 32 == 0, "bins split evenly");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  hi = 32;
+  P = 0u;
+  need = k;
+  exact = false;
   while (hi > 0) {
     const int lo = hi > DB ? hi - DB : 0;
     const int w = hi - lo;
@@ -1030,14 +1026,23 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
       break;
     }
   }
-  // ---- output positions: entries above the threshold, then ties in index order
+}
+
+// Writes the chosen entries of the row in ascending index order: every
+// entry with gt(key), then, in index order, `need` of those with eq(key)
+// (all of them when exact). One 64-bit block scan of (above, at) counts
+// gives each thread the output positions of its consecutive entries.
+template <int TPB, int PER, class Gt, class Eq>
+__device__ __forceinline__ void row_emit(const uint32_t (&key)[PER], int e0, int n, uint32_t need, bool exact, Gt gt,
+                                         Eq eq, unsigned long long* wsum, int32_t* out, const TkMap& map, int q) {
+  constexpr int NW = TPB / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i)
     if (e0 + i < n) {
-      const uint32_t top = key[i] >> hi;
-      n_gt += top > P ? 1u : 0u;
-      n_eq += top == P ? 1u : 0u;
+      n_gt += gt(key[i]) ? 1u : 0u;
+      n_eq += eq(key[i]) ? 1u : 0u;
     }
   unsigned long long v = ((unsigned long long)n_eq << 32) | n_gt;
 #pragma unroll
@@ -1071,9 +1076,8 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
 #pragma unroll
   for (int i = 0; i < PER; ++i)
     if (e0 + i < n) {
-      const uint32_t top = key[i] >> hi;
-      bool take = top > P;
-      if (top == P && eq_left > 0) {
+      bool take = gt(key[i]);
+      if (eq(key[i]) && eq_left > 0) {
         take = true;
         --eq_left;
       }
@@ -1082,11 +1086,210 @@ __global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__
 }
 
 template <int TPB, int PER>
+__global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
+                                                      const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
+                                                      int32_t* __restrict__ out_idx, const TkMap map) {
+  constexpr int NW = TPB / 32;
+  static_assert(PER % 4 == 0, "float4 loads");
+  __shared__ uint32_t hist[1 << 11];
+  __shared__ uint32_t res[3];
+  __shared__ uint32_t wtot[NW];
+  __shared__ unsigned long long wsum[NW];
+  pdl_wait();  // the scores (and pool counts) of the previous kernel
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  const int q = blockIdx.x;
+  const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
+  int32_t* out = out_idx + (int64_t)q * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += TPB) out[i] = i < n ? map(q, i) : -1;
+    return;
+  }
+  const float* row = scores + (int64_t)q * ld;
+  const int e0 = PER * tid;
+  uint32_t key[PER];
+  row_load_keys<PER>(row, scores, ld, e0, n, key);
+  uint32_t P, need;
+  int hi;
+  bool exact;
+  row_radix_search<TPB, PER>(key, e0, n, (uint32_t)k, hist, res, wtot, P, hi, need, exact);
+  row_emit<TPB, PER>(key, e0, n, need, exact, [&](uint32_t x) { return (x >> hi) > P; },
+                     [&](uint32_t x) { return (x >> hi) == P; }, wsum, out, map, q);
+}
+
+// The decode form for rows of up to 16,384 scores held by 1,024 threads
+// (few queries, one CTA each; the whole step waits on the slowest row).
+// Scores near the top sit close to the row's largest key M in key space, so
+// the first level bins the distance d = M - key of every key within 2^24 of
+// M (4,096 bins of 2^12, bin 0 the top; for positive scores that is about
+// two binades below the largest): only keys near the top touch the
+// histogram, which keeps shared-atomic contention low, and one warp scans
+// the bins, so the level costs two barriers. A second level bins the low 12
+// bits of d inside the picked bin, which pins the threshold key exactly;
+// ties at it are taken in index order. Rows whose k largest keys do not all
+// lie within 2^24 of M fall back to the radix search above.
+constexpr int kRelBins = 4096;
+constexpr int kRelShift = 12;
+constexpr int kRelSub = 1 << kRelShift;
+
+// The bin of h (NB bins, bin 0 the top) where the count from the top reaches
+// need, in two stages without a serial walk: every warp sums one group of
+// NB / 32 bins (four per lane, then a warp sum); after a barrier, warp 0
+// scans the 32 group sums, picks the group, scans that group's bins four per
+// lane and picks the bin. Leaves res = (bin, count above it, count in it),
+// or res[0] = ~0 if the bins hold fewer than need. Called by all 1,024
+// threads; ends without a barrier (the caller synchronises before reading).
+template <int NB>
+__device__ __forceinline__ void rel_pick(const uint32_t* h, uint32_t need, uint32_t* res, uint32_t* gsum) {
+  constexpr int G = NB / 32;  // bins a group (one per warp)
+  static_assert(G == 128, "four bins a lane");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    const uint4 v = reinterpret_cast<const uint4*>(h + G * warp)[lane];
+    uint32_t x = v.x + v.y + v.z + v.w;
+    x = __reduce_add_sync(0xffffffffu, x);
+    if (lane == 0) gsum[warp] = x;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const uint32_t s = gsum[lane];
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t reach = __ballot_sync(0xffffffffu, incl >= need);
+  if (reach == 0u) {
+    if (lane == 0) res[0] = 0xFFFFFFFFu;
+    return;
+  }
+  const int g = __ffs(reach) - 1;
+  const uint32_t above_g = __shfl_sync(0xffffffffu, incl - s, g);
+  const uint4 v = reinterpret_cast<const uint4*>(h + G * g)[lane];
+  const uint32_t c4 = v.x + v.y + v.z + v.w;
+  uint32_t inc2 = c4;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc2, o);
+    if (lane >= o) inc2 += u;
+  }
+  const uint32_t need2 = need - above_g;
+  const uint32_t reach2 = __ballot_sync(0xffffffffu, inc2 >= need2);
+  if (lane == __ffs(reach2) - 1) {
+    uint32_t cum = above_g + inc2 - c4;
+    const uint32_t c[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (cum + c[j] >= need) {
+        res[0] = (uint32_t)(G * g + 4 * lane + j);
+        res[1] = cum;
+        res[2] = c[j];
+        break;
+      }
+      cum += c[j];
+    }
+  }
+}
+
+template <int PER>
+__global__ void __launch_bounds__(1024) topk_row_rel_kernel(const float* __restrict__ scores, int64_t ld,
+                                                           const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
+                                                           int32_t* __restrict__ out_idx, const TkMap map) {
+  constexpr int TPB = 1024, NW = 32;
+  static_assert(PER % 4 == 0, "float4 loads");
+  __shared__ __align__(16) uint32_t h1[kRelBins];
+  __shared__ __align__(16) uint32_t h2[kRelSub];  // also the fallback's histogram
+  __shared__ uint32_t res[3];
+  __shared__ uint32_t wtot[NW];
+  __shared__ unsigned long long wsum[NW];
+  __shared__ uint32_t s_max;
+  __shared__ uint32_t gsum[32];
+  pdl_wait();  // the scores of the previous kernel
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int q = blockIdx.x;
+  const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
+  int32_t* out = out_idx + (int64_t)q * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += TPB) out[i] = i < n ? map(q, i) : -1;
+    return;
+  }
+  const float* row = scores + (int64_t)q * ld;
+  const int e0 = PER * tid;
+  uint32_t key[PER];
+  row_load_keys<PER>(row, scores, ld, e0, n, key);
+  // histograms zeroed and the row's largest key found meanwhile
+  {
+    uint4* z1 = reinterpret_cast<uint4*>(h1);
+    uint4* z2 = reinterpret_cast<uint4*>(h2);
+    for (int i = tid; i < kRelBins / 4; i += TPB) z1[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < kRelSub / 4; i += TPB) z2[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid == 0) s_max = 0u;
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (e0 + i < n) mx = max(mx, key[i]);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  __syncthreads();
+  if (lane == 0) atomicMax(&s_max, mx);
+  __syncthreads();
+  const uint32_t M = s_max;
+  // level 1: distance to the top in bins of 2^12 key steps
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const uint32_t d = M - key[i];
+    if (e0 + i < n && d < ((uint32_t)kRelBins << kRelShift)) atomicAdd(&h1[d >> kRelShift], 1u);
+  }
+  __syncthreads();
+  rel_pick<kRelBins>(h1, (uint32_t)k, res, gsum);
+  __syncthreads();
+  const uint32_t b1 = res[0];
+  // every path ends with one threshold D on d = M - key: the entries with
+  // d < D, then `need` of those with d == D in index order (all if exact)
+  uint32_t D, need;
+  bool exact;
+  if (b1 == 0xFFFFFFFFu) {
+    // the k largest keys reach further than 2^24 below the top: the radix
+    // search from the top bit (chosen: key >= P << hi when exact, else
+    // key > P and ties at P)
+    __syncthreads();  // every thread has read res[0]
+    uint32_t P;
+    int hi;
+    row_radix_search<TPB, PER>(key, e0, n, (uint32_t)k, h2, res, wtot, P, hi, need, exact);
+    D = exact ? M - (P << hi) : M - P;
+  } else if (res[2] == (uint32_t)k - res[1]) {
+    // every key of the picked bin is needed: d up to the bin's last step
+    D = ((b1 + 1u) << kRelShift) - 1u;
+    need = 0u;
+    exact = true;
+  } else {
+    // level 2: the low 12 bits of d inside the picked bin pin the threshold
+    const uint32_t need1 = (uint32_t)k - res[1];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const uint32_t d = M - key[i];
+      if (e0 + i < n && (d >> kRelShift) == b1) atomicAdd(&h2[d & (kRelSub - 1)], 1u);
+    }
+    __syncthreads();
+    rel_pick<kRelSub>(h2, need1, res, gsum);
+    __syncthreads();
+    D = (b1 << kRelShift) | res[0];  // the threshold key is M - D
+    need = need1 - res[1];
+    exact = res[2] == need;
+  }
+  row_emit<TPB, PER>(key, e0, n, need, exact, [&](uint32_t x) { return M - x < D; },
+                     [&](uint32_t x) { return M - x == D; }, wsum, out, map, q);
+}
+
+template <int TPB, int PER>
 static cudaError_t launch_topk_row(cudaStream_t st, int n_query, const float* scores, int64_t ld,
                                    const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx,
-                                   const TkMap& map) {
-  topk_row_kernel<TPB, PER><<<n_query, TPB, 0, st>>>(scores, ld, n_vis, max_vis, k, out_idx, map);
-  return cudaGetLastError();
+                                   const TkMap& map, bool pdl) {
+  const cudaError_t e = launch_ex(topk_row_kernel<TPB, PER>, dim3(n_query), dim3(TPB), 0, st, pdl, 0, scores, ld,
+                                  n_vis, max_vis, k, out_idx, map);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The hierarchical indexer's block scores: the largest score among each
@@ -1136,7 +1339,8 @@ cudaError_t launch_candidate_pool(cudaStream_t st, int n_query, const float* sco
 
 template <int PER>
 static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, const float* scores, int64_t ld,
-                                      const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx, bool* launched) {
+                                      const int32_t* n_vis, int64_t max_vis, int k, int32_t* out_idx, bool* launched,
+                                      bool pdl) {
   *launched = false;
   const void* fn = (const void*)topk_cluster_kernel<PER>;
   const uint32_t smem = TkLayout<PER>::SMEM;
@@ -1156,6 +1360,13 @@ static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, 
   cfg.numAttrs = 1;
   int max_clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg);
+  cudaLaunchAttribute attr2[2] = {attr[0], attr[0]};
+  if (pdl) {
+    attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr2[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr2;
+    cfg.numAttrs = 2;
+  }
   if (e != cudaSuccess || max_clusters < 1) {
     cudaGetLastError();  // cluster shape not schedulable here: the caller takes the global-memory path
     return cudaSuccess;
@@ -1172,7 +1383,7 @@ static cudaError_t launch_topk_cluster(cudaStream_t st, int csize, int n_query, 
 
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch, const int32_t* map_blocks,
-                        int map_ld, int map_shift) {
+                        int map_ld, int map_shift, bool pdl) {
   if (n_query == 0) return cudaSuccess;
   TkMap map;
   map.blocks = map_blocks;
@@ -1183,11 +1394,18 @@ cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64
     cudaError_t e;
     // the fewest keys a thread that fit: registers set how many rows an SM
     // holds at once (chunked prefill has thousands of rows of up to 6,144)
-    if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
-    else if (max_vis <= 4096) e = launch_topk_row<256, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
-    else if (max_vis <= 6144) e = launch_topk_row<256, 24>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
-    else if (max_vis <= 8192) e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
-    else e = launch_topk_row<1024, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map);
+    if (max_vis <= 2048) e = launch_topk_row<256, 8>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map, pdl);
+    else if (max_vis <= 4096)
+      e = launch_topk_row<256, 16>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map, pdl);
+    else if (max_vis <= 6144)
+      e = launch_topk_row<256, 24>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map, pdl);
+    else if (max_vis <= 8192)
+      e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map, pdl);
+    else {
+      e = launch_ex(topk_row_rel_kernel<16>, dim3(n_query), dim3(1024), 0, st, pdl, 0, scores, ld, n_vis, max_vis, k,
+                    out_idx, map);
+      if (e == cudaSuccess) e = cudaGetLastError();
+    }
     if (e == cudaSuccess) *n_launch += 1;
     return e;
   }
@@ -1199,8 +1417,9 @@ cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64
   if (c32 <= kTkMaxCluster) {
     bool launched = false;
     cudaError_t e = c16 <= kTkMaxCluster
-                        ? launch_topk_cluster<16>(st, c16, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched)
-                        : launch_topk_cluster<32>(st, c32, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched);
+                        ? launch_topk_cluster<16>(st, c16, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched, pdl)
+                        : launch_topk_cluster<32>(st, c32, n_query, scores, ld, n_vis, max_vis, k, out_idx, &launched,
+                                                  pdl);
     if (e != cudaSuccess) return e;
     if (launched) {
       *n_launch += 1;

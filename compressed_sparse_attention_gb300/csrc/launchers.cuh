@@ -5,6 +5,35 @@
 
 namespace csa2 {
 
+// Launch on `st` with programmatic stream serialization when `pdl` is set:
+// the kernel may start before the previous kernel of the stream ends and
+// waits for it with pdl_wait() before reading what it wrote. `priority`
+// (when nonzero) is the launch's scheduling priority.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      int priority, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (priority != 0) {
+    attr[na].id = cudaLaunchAttributePriority;
+    attr[na].val.priority = priority;
+    ++na;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct AttendParams {
   const uint16_t* q;
   const int64_t* q_pos;
@@ -32,7 +61,7 @@ struct AttendParams {
   int tile_count;       // tiles this launch covers
   int n_split;          // CTAs per query in this launch
   int tiles_per_split;
-  int lead_single;      // 1: split 0 covers the first tile alone, the others tiles_per_split each
+  int lead_tiles;       // tiles of split 0 (the others take tiles_per_split each)
   int n_slots;          // partial slots per query in the workspace
   int slot_base;        // slot of this launch's first split
   int direct;           // 1: write the normalised output, no partials; 2: write the
@@ -47,6 +76,12 @@ struct AttendParams {
   float* part_o;  // [n_query][64][512] fp32, rope channels not rotated back
   float* part_m;  // [n_query][64] reference max, natural-log units (-inf: no rows)
   float* part_l;  // [n_query][64] sum of exp(s_r - m)
+  // launch settings (host only): pdl = programmatic launch after the previous
+  // kernel of the stream (csa2_step's top-k, or its selected tiles for the
+  // merge); the kernel reads the selection only after pdl_wait(). priority:
+  // the launch's scheduling priority (0: the stream's)
+  int pdl;
+  int priority;
 };
 
 cudaError_t launch_store_rows(cudaStream_t st, const float* rows, int64_t n_rows, int dim, const int64_t* pos,
@@ -56,6 +91,22 @@ struct AppendArgs {
   int64_t n_tokens = 0;
   uint16_t* state_raw = nullptr;
   float* state_gate = nullptr;
+};
+// Scores of the entries a decode step compresses, taken by the compress
+// kernel itself from the index keys it stores (the index scan of that step
+// leaves those entries out): for each query q of the group's sequence whose
+// visible count covers entry j, scores[q * ld + j] = sum_h w_heads[q, h] *
+// relu(q_idx[q, h] . key_j) with the stored key's exact values, fp32.
+struct CompressTail {
+  int n_query = 0;
+  int idx_heads = 0;
+  int64_t max_vis = 0;
+  int64_t ld = 0;
+  const int32_t* seq_of_q = nullptr;
+  const int32_t* n_vis = nullptr;
+  const uint16_t* q_idx = nullptr;
+  const float* w_heads = nullptr;
+  float* scores = nullptr;  // NULL: no scoring
 };
 // n_groups: the closing groups (whole-group form) or a bound of them (append
 // form: n_tokens / m + n_seq); n_launch counts the launches made
@@ -68,8 +119,8 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
                             float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
                             uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags,
-                            const AppendArgs* app, int* n_launch);
-// arguments of the index scan (csa2_index_score) and of its tail kernel
+                            const AppendArgs* app, int* n_launch, const CompressTail* tail = nullptr);
+// arguments of the index scan (csa2_index_score)
 struct IdxArgs {
   int n_query = 0, n_seq = 0;
   int64_t n_chunks = 0, max_vis = 0;
@@ -85,7 +136,7 @@ struct IdxArgs {
   uint32_t* flags = nullptr;
   // set: the scan leaves out the entries this step compresses (entries at or
   // above first_pos[b] / m of a sequence with tok_off[b+1] > tok_off[b]) and
-  // the tail kernel scores them
+  // the compress kernel scores them (CompressTail)
   const int64_t* new_first = nullptr;
   const int64_t* new_tok = nullptr;
   int m = 1;
@@ -98,8 +149,10 @@ struct IdxArgs {
   int cand_shift = 0;
   int32_t* n_pool = nullptr;
 };
-cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a);
-cudaError_t launch_index_tail(cudaStream_t st, int idx_heads, int idx_fmt, const IdxArgs& a);
+// pdl: launched programmatically after the step's compress kernel, which
+// it waits for only before its CTAs exit (it reads nothing compress writes)
+cudaError_t launch_index_score(cudaStream_t st, int num_sms, int idx_heads, int idx_fmt, IdxArgs a,
+                               bool pdl = false);
 // tensor-core form of the indexer for many queries per sequence (bf16 keys)
 bool index_tc_suited(int idx_fp8, int n_query, int n_seq, int idx_heads);
 cudaError_t launch_index_score_tc(cudaStream_t st, int num_sms, int idx_heads, int n_query, int n_seq,
@@ -109,26 +162,25 @@ cudaError_t launch_index_score_tc(cudaStream_t st, int num_sms, int idx_heads, i
 size_t topk_workspace_bytes(int n_query, int64_t max_vis);
 // map_blocks set (rows of at most 16,384): row entry e is written as the
 // entry index (map_blocks[q * map_ld + (e >> map_shift)] << map_shift) | low bits
+// pdl: the one-launch forms start programmatically after the previous kernel
+// of the stream (csa2_step's index scan) and wait for it before reading
 cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64_t ld, const int32_t* n_vis,
                         int64_t max_vis, int k, int32_t* out_idx, void* ws, int* n_launch,
-                        const int32_t* map_blocks = nullptr, int map_ld = 0, int map_shift = 0);
+                        const int32_t* map_blocks = nullptr, int map_ld = 0, int map_shift = 0, bool pdl = false);
 size_t candidate_pool_workspace_bytes(int n_query, int64_t max_vis, int shift);
 cudaError_t launch_candidate_pool(cudaStream_t st, int n_query, const float* scores, int64_t ld,
                                   const int32_t* n_vis, int64_t max_vis, int shift, int keep, int32_t* cand,
                                   void* ws, int* n_launch);
 struct AttendPlan {
   int n_tiles;
-  int split_window;  // window tile launched on its own
-  int ns;            // CTAs per query of the main launch
-  int tps;           // tiles per CTA of the main launch
-  int n_slots;       // partial slots per query (0: direct output)
+  int ns;       // CTAs per query
+  int tps;      // selected tiles per CTA
+  int lead;     // tiles of a query's first CTA (the window tile and its tps selected tiles)
+  int n_slots;  // partial slots per query (0: direct output)
 };
 int attend_num_tiles(int topk, bool has_idx);
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
-AttendPlan attend_plan_single(int n_query, int topk, bool has_idx, int num_sms);
 size_t attend_workspace_bytes(int n_query, const AttendPlan& pl);
-cudaError_t launch_attend_window(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
-                                 int* n_launch);
 cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                int* n_launch);
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);

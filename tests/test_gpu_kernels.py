@@ -307,6 +307,63 @@ def test_topk_bit_exact(n, tie_levels, k):
         assert np.array_equal(got[qi], ref), f"query {qi}"
 
 
+def _floats_from_keys(keys):
+    """float32 scores whose order-preserving keys are `keys` (the inverse of
+    the map the selection orders by: positive floats have the top key bit
+    set, negative ones are inverted)."""
+    keys = np.asarray(keys, dtype=np.uint32)
+    bits = np.where(keys & 0x80000000, keys & 0x7FFFFFFF, ~keys).astype(np.uint32)
+    return bits.view(np.float32)
+
+
+@pytest.mark.parametrize("case", ["normal", "huge_max", "bin_exact", "threshold_ties", "negative", "all_equal"])
+def test_topk_decode_row_paths(case):
+    """Rows of 8,193 .. 16,384 scores (the decode form, 1,024 threads a row),
+    shaped to take each path of its search: the two relative levels
+    (normal), the fallback radix search when the k largest reach more than
+    2^24 key steps below the largest (huge_max), a first-level bin that holds
+    exactly the keys still needed (bin_exact), many ties at the threshold
+    value (threshold_ties, all_equal), and negative scores. Bit-exact against
+    the oracle's selection on the same scores."""
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    k, n = 512, 16384
+    lens = [16384, 12000, 8193]
+    rng = np.random.default_rng({"normal": 1, "huge_max": 2, "bin_exact": 3, "threshold_ties": 4,
+                                 "negative": 5, "all_equal": 6}[case])
+    rows = []
+    for r in range(len(lens)):
+        x = rng.standard_normal(n).astype(np.float32)
+        if case == "huge_max":
+            x[rng.integers(0, lens[r])] = 1e30
+        elif case == "bin_exact":
+            top = np.uint32(0x80000000 | np.float32(50.0).view(np.uint32))
+            keys = (top - np.uint32(1 << 25) - rng.integers(0, 1 << 20, n).astype(np.uint32)).astype(np.uint32)
+            pos = rng.permutation(lens[r])[:k]
+            keys[pos] = top - (np.arange(k, dtype=np.uint32) << np.uint32(12))
+            x = _floats_from_keys(keys)
+        elif case == "threshold_ties":
+            x = np.abs(x)
+            pos = rng.permutation(lens[r])
+            x[pos[:400]] = 10.0
+            x[pos[400:700]] = 9.0
+        elif case == "negative":
+            x = -np.abs(x) - 5.0
+        elif case == "all_equal":
+            x[:] = 3.25
+        rows.append(x)
+    sc = torch.from_numpy(np.stack(rows))
+    nv = torch.tensor(lens, dtype=torch.int32)
+    out = torch.empty((len(lens), k), dtype=torch.int32, device=DEV)
+    ws = binding.workspace(ctx.topk_workspace_size(len(lens), n), DEV)
+    ctx.topk(sc.to(DEV), nv.to(DEV), n, k, out, ws)
+    assert ctx.check()[0] == 0
+    got = out.cpu().numpy()
+    for qi, ln in enumerate(lens):
+        ref = O.topk_select(rows[qi][:ln].astype(np.float64), k)
+        assert np.array_equal(got[qi], ref), f"row {qi} (n {ln})"
+
+
 @pytest.mark.parametrize("tie_levels", [0, 2])
 def test_topk_many_queries_mixed_lengths(tie_levels):
     """More queries than the GPU holds top-k clusters for at once, with row
