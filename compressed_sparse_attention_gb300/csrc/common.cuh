@@ -125,18 +125,17 @@ __device__ __forceinline__ float2 e2m1x2_to_float2_scaled(uint32_t two) {
 }
 constexpr float kE2M1Unscale = 16384.0f;  // 2^14
 // eight E2M1 codes (the nibbles n0 .. n7 of w, n0 lowest) -> four f16x2
-// words, each half 2^-14 times its code's value, in the pairs
-// o[0] = (n0, n4), o[1] = (n1, n5), o[2] = (n2, n6), o[3] = (n3, n7) (low
-// half first): a nibble's three magnitude bits go to f16 bits 9..11 (low two
-// exponent bits and the top mantissa bit) and its sign to bit 15, as in the
-// pair decoder above. The pairing puts nibbles i and i + 4 at the same shift,
-// so each word takes two shifts and one three-input logic op.
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
-  constexpr uint32_t kMag = 0x0E000E00u, kSign = 0x80008000u;
-  o[0] = ((w << 9) & kMag) | ((w << 12) & kSign);
-  o[1] = ((w << 5) & kMag) | ((w << 8) & kSign);
-  o[2] = ((w << 1) & kMag) | ((w << 4) & kSign);
-  o[3] = ((w >> 3) & kMag) | (w & kSign);
+// words holding their exact values, o[i] = (n(2i), n(2i+1)), low half first:
+// one hardware conversion per byte (two codes)
+__device__ __forceinline__ void e2m1x8_to_f16x2x4_cvt(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
 }
 // e4m3 byte of the fp4 block scale: e4m3(max(amax, 6 * 2^-9) / 6), the
 // quotient formed in double (exact enough that its rounding to e4m3 equals

@@ -236,18 +236,16 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
 // never mixes two scale blocks; each block's partial dot product is scaled by
 // its power of two in fp32.
 //
-// Both code types decode exactly into f16 with few instructions (one convert
-// per e4m3 pair; two shifts and a logic op per E2M1 pair, which arrives as
-// 2^-14 times its value), so these products run as f16 x f16 -> f32 mma. The
+// Both code types decode exactly into f16 with one hardware conversion per
+// pair of codes (e4m3x2 -> f16x2, e2m1x2 -> f16x2), so these products run as
+// f16 x f16 -> f32 mma. The
 // indexer query is converted to f16 once per query, head h multiplied by a
 // power of two 2^s_h that puts its largest element in [2^14, 2^15): every
 // bf16 element at least 2^-24 of that largest one is then exact in f16, and
 // a smaller one moves by at most 2^-25 of it. The weight w_h takes the
-// inverse power (and the 2^14 of the E2M1 decode), which the ReLU commutes
-// with. k-slot order: for e4m3, mma step (b, 0) holds channel pairs
-// (8t, 8t+1) and (8t+2, 8t+3) of block b, step (b, 1) the pairs (8t+4, 8t+5)
-// and (8t+6, 8t+7); for E2M1 the pairs are (8t, 8t+4), (8t+1, 8t+5) and
-// (8t+2, 8t+6), (8t+3, 8t+7), the order the nibble decoder produces.
+// inverse power, which the ReLU commutes with. k-slot order (both code
+// types): mma step (b, 0) holds channel pairs (8t, 8t+1) and (8t+2, 8t+3) of
+// block b, step (b, 1) the pairs (8t+4, 8t+5) and (8t+6, 8t+7).
 template <int NT, int KF>
 __device__ __forceinline__ void idxq_load_query(const uint16_t* __restrict__ q_idx, const float* __restrict__ w_heads,
                                                 int q, int g, int t, uint32_t (&qb)[NT][8][2], float (&w0)[NT],
@@ -283,20 +281,13 @@ __device__ __forceinline__ void idxq_load_query(const uint16_t* __restrict__ q_i
         y[2 * k] = __uint_as_float(wv[k] << 16) * up;
         y[2 * k + 1] = __uint_as_float(wv[k] & 0xFFFF0000u) * up;
       }
-      if constexpr (KF == 3) {
-        qb[nt][2 * bb][0] = h2_bits(y[0], y[4]);
-        qb[nt][2 * bb][1] = h2_bits(y[1], y[5]);
-        qb[nt][2 * bb + 1][0] = h2_bits(y[2], y[6]);
-        qb[nt][2 * bb + 1][1] = h2_bits(y[3], y[7]);
-      } else {
-        qb[nt][2 * bb][0] = h2_bits(y[0], y[1]);
-        qb[nt][2 * bb][1] = h2_bits(y[2], y[3]);
-        qb[nt][2 * bb + 1][0] = h2_bits(y[4], y[5]);
-        qb[nt][2 * bb + 1][1] = h2_bits(y[6], y[7]);
-      }
+      qb[nt][2 * bb][0] = h2_bits(y[0], y[1]);
+      qb[nt][2 * bb][1] = h2_bits(y[2], y[3]);
+      qb[nt][2 * bb + 1][0] = h2_bits(y[4], y[5]);
+      qb[nt][2 * bb + 1][1] = h2_bits(y[6], y[7]);
     }
     // the C fragment's columns are heads 2t and 2t+1, whose powers lanes 8t and 8t+4 hold
-    const int e = (KF == 3 ? 14 : 0) - sh;
+    const int e = -sh;
     const int e0 = __shfl_sync(0xffffffffu, e, 8 * t), e1 = __shfl_sync(0xffffffffu, e, 8 * t + 4);
     w0[nt] = ldexpf(w_heads[(int64_t)q * HI + nt * 8 + 2 * t], e0);
     w1[nt] = ldexpf(w_heads[(int64_t)q * HI + nt * 8 + 2 * t + 1], e1);
@@ -376,8 +367,8 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
           // this block's 8 codes of rows g (a) and g+8 (b) as f16 pairs in k-slot order
           uint32_t a[4], b[4];
           if constexpr (KF == 3) {
-            e2m1x8_to_f16x2x4(ca[u][bb].x, a);
-            e2m1x8_to_f16x2x4(cb[u][bb].x, b);
+            e2m1x8_to_f16x2x4_cvt(ca[u][bb].x, a);
+            e2m1x8_to_f16x2x4_cvt(cb[u][bb].x, b);
           } else {
             a[0] = e4m3x2_to_f16x2(ca[u][bb].x); a[1] = e4m3x2_to_f16x2(ca[u][bb].x >> 16);
             a[2] = e4m3x2_to_f16x2(ca[u][bb].y); a[3] = e4m3x2_to_f16x2(ca[u][bb].y >> 16);
