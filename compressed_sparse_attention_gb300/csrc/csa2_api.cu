@@ -229,7 +229,8 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                const int64_t* pool_off, const float* norm_w, const uint16_t* w_idx,
                                const float* k_norm_w, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
                                uint8_t* idx_key_scale, bool append = false, uint16_t* state_raw = nullptr,
-                               float* state_gate = nullptr, const csa2::CompressTail* tail = nullptr) {
+                               float* state_gate = nullptr, const csa2::CompressTail* tail = nullptr,
+                               bool pdl = false) {
   const csa2_config& c = ctx->cfg;
   const int m = c.compress_ratio;
   if (n_tokens < 0 || n_seq < 1) return fail(ctx, CSA2_ERR_INVALID_ARG, "compress: n_seq / n_tokens");
@@ -256,7 +257,7 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                         w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
                                         c.kv_format, c.idx_key_format,
                                         pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags,
-                                        append ? &app : nullptr, &nl, tail);
+                                        append ? &app : nullptr, &nl, tail, pdl);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
   ctx->last_launches += nl;
   return CSA2_OK;
@@ -291,7 +292,7 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
                             const int64_t* pool_off, const int32_t* seq_of_q, const int32_t* n_vis, int64_t max_vis,
                             float* scores, int64_t ld, const int64_t* new_first = nullptr,
                             const int64_t* new_tok = nullptr, const int32_t* cand = nullptr,
-                            int32_t* n_pool = nullptr, bool pdl = false) {
+                            int32_t* n_pool = nullptr, bool pdl = false, bool wait_first = false) {
   const csa2_config& c = ctx->cfg;
   // a pool row holds at most cand_keep blocks of entries
   const int64_t row_need = cand != nullptr ? std::min(max_vis, (int64_t)c.cand_keep * c.cand_block) : max_vis;
@@ -327,6 +328,7 @@ static csa2_status do_index(csa2_ctx* ctx, cudaStream_t st, int32_t n_seq, int32
   ia.cand_ld = c.cand_keep;
   ia.cand_shift = cand_shift(c);
   ia.n_pool = n_pool;
+  ia.wait_first = wait_first ? 1 : 0;
   cudaError_t e;
   if (new_first == nullptr && cand == nullptr &&
              csa2::index_tc_suited(kf != CSA2_KV_BF16, n_query, n_seq, c.idx_heads)) {
@@ -808,9 +810,12 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
       ct.w_heads = a->w_heads;
       ct.scores = scores;
     }
+    // the step's first kernel: launched programmatically, it waits for the
+    // previous kernel of the stream before it reads anything (this hides the
+    // launch latency only; its inputs are complete once the wait returns)
     s = do_compress(ctx, st, raw_in, gate_in, a->n_seq, a->n_tokens, a->tok_off, a->first_pos, a->pool_off,
                     a->norm_w, a->w_idx, a->k_norm_w, a->pool_kv, a->pool_scale, a->idx_keys, a->idx_key_scale,
-                    a->append != 0, a->state_raw, a->state_gate, tail ? &ct : nullptr);
+                    a->append != 0, a->state_raw, a->state_gate, tail ? &ct : nullptr, true);
     if (s != CSA2_OK) return join(s);
     launches += ctx->last_launches;
   }
@@ -833,13 +838,21 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
     return CSA2_OK;
   }
   ctx->last_launches = 0;
+  // the scan follows compress programmatically (waiting for it at its end),
+  // or is the step's first kernel (waiting for the stream's previous kernel
+  // at its start); with a compress that is not the overlap form it waits at
+  // its start too
+  const bool scan_first = !full;
+  const bool scan_pdl = scan_first || (overlap && a->n_tokens > 0) || (full && a->n_tokens > 0);
+  const bool scan_wait_first = scan_first || !(overlap && a->n_tokens > 0);
   if (pool_read)  // the hierarchical indexer's second level: score inside the pool only
     s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
-                 a->seq_of_q, a->n_vis, a->max_vis, scores, ldc, nullptr, nullptr, a->cand, n_pool);
+                 a->seq_of_q, a->n_vis, a->max_vis, scores, ldc, nullptr, nullptr, a->cand, n_pool, scan_pdl,
+                 scan_wait_first);
   else
     s = do_index(ctx, st, a->n_seq, a->n_query, a->q_idx, a->w_heads, a->idx_keys, a->idx_key_scale, a->pool_off,
                  a->seq_of_q, a->n_vis, a->max_vis, scores, ld, tail ? a->first_pos : nullptr,
-                 tail ? a->tok_off : nullptr, nullptr, nullptr, overlap && a->n_tokens > 0);
+                 tail ? a->tok_off : nullptr, nullptr, nullptr, scan_pdl, scan_wait_first);
   if (s != CSA2_OK) return join(s);
   launches += ctx->last_launches;
   cudaError_t e = stage_q();

@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     j_next = sel_entry(tile_begin, tile_end);
     sel_ready = true;
   }
+  float lsum[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) lsum[k] = 0.f;
   int tile = tile_begin;
   for (int pass = 0; pass < 2; ++pass) {
   const int pass_end = (pass == 0 && !sel_ready) ? min(tile_end, 1) : tile_end;
@@ -451,15 +454,20 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     }
     __syncthreads();
     {
-      float v[32];
+      // this thread's running row sums (its row, its 32 heads), moved with
+      // the reference max like O; reduced over rows once, after the tiles
+      if (misc[3]) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) lsum[k] *= alpha[32 * hh + k];
+      }
       uint32_t packed[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const float p0 = exp2f(s[2 * k] - m_use[32 * hh + 2 * k]);
         const float p1 = exp2f(s[2 * k + 1] - m_use[32 * hh + 2 * k + 1]);
         packed[k] = pack_bf16(p0, p1);
-        v[2 * k] = bf16lo(packed[k]);
-        v[2 * k + 1] = bf16hi(packed[k]);
+        lsum[2 * k] += bf16lo(packed[k]);  // the weights PV sums, rounded to bf16
+        lsum[2 * k + 1] += bf16hi(packed[k]);
       }
       // P^T row `row`: 64 heads = 8 chunks of 16 B (MN-major B operand); this
       // thread writes chunks 4 hh .. 4 hh + 3
@@ -470,14 +478,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
         *reinterpret_cast<uint4*>(sm + off) =
             make_uint4(packed[4 * c4], packed[4 * c4 + 1], packed[4 * c4 + 2], packed[4 * c4 + 3]);
       }
-      const float a = reduce_scatter32<false>(v, lane);
-      __syncthreads();  // every warp has read red[] (max) before it is reused for sums
-      red[quad * 64 + 32 * hh + lane] = a;
-    }
-    __syncthreads();
-    if (tid < kHeads) {
-      const float ts = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
-      l_run[tid] = alpha[tid] * l_run[tid] + ts;
     }
     // ---- rescale O^T in tensor memory where a head's running max rose
     if (misc[3]) {
@@ -524,6 +524,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   cp_async_wait_all();
   __syncthreads();
   const bool have_o = (tile_begin < tile_end) && !aborted;
+  if (have_o) {
+    // the row sums: over this warp's 32 rows (lanes), then over the 4 quadrants
+    red[quad * 64 + 32 * hh + lane] = reduce_scatter32<false>(lsum, lane);
+    __syncthreads();
+    if (tid < kHeads) l_run[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+    __syncthreads();
+  }
   const int first_rope = kDim - 2 * p.rp.pairs;
   if (p.direct == 2) {
     // unnormalised partial for a log-sum-exp combine elsewhere: O (rope

@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   __shared__ float k_lin_s[kIdxDim];
   __shared__ float k_st_s[kIdxDim];  // the stored key's exact values (tail scoring)
   __shared__ float red_s[8];
+  // As a step's first kernel it may be launched programmatically: it reads
+  // nothing before the previous kernel of the stream has finished (a plain
+  // launch returns at once), which hides only the launch latency.
+  pdl_wait();
   pdl_trigger();  // the step's index scan starts beside this grid
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // ---- index-key weights first: nothing they depend on
@@ -456,18 +460,18 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fmt,
                             int idx_fmt, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
                             uint8_t* idx_key_scale, uint32_t* flags, const AppendArgs* app, int* n_launch,
-                            const CompressTail* tail) {
+                            const CompressTail* tail, bool pdl) {
   if (n_groups == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_groups);
   const CompressTail tl = (tail != nullptr && w_idx != nullptr) ? *tail : CompressTail{};
   const int append = app != nullptr ? 1 : 0;
   const uint16_t* st_raw = app != nullptr ? app->state_raw : nullptr;
   const float* st_gate = app != nullptr ? app->state_gate : nullptr;
-#define CSA2_COMPRESS(KF, IF)                                                                      \
-  compress_kernel<KF, IF><<<grid, kCmpThreads, 0, st>>>(raw, gate, m, n_seq, tok_off, first_pos, pool_off, \
-                                                norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, \
-                                                pool_kv_scale, idx_keys, idx_key_scale, flags, append, \
-                                                st_raw, st_gate, tl)
+  cudaError_t le = cudaSuccess;
+#define CSA2_COMPRESS(KF, IF)                                                                                \
+  le = launch_ex(compress_kernel<KF, IF>, grid, dim3(kCmpThreads), 0, st, pdl, 0, raw, gate, m, n_seq, tok_off, \
+                 first_pos, pool_off, norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, pool_kv_scale, idx_keys, \
+                 idx_key_scale, flags, append, st_raw, st_gate, tl)
 #define CSA2_COMPRESS_K(KF)                               \
   do {                                                    \
     if (idx_fmt == 1) CSA2_COMPRESS(KF, 1);               \
@@ -479,7 +483,7 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
   else CSA2_COMPRESS_K(0);
 #undef CSA2_COMPRESS_K
 #undef CSA2_COMPRESS
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = le != cudaSuccess ? le : cudaGetLastError();
   if (e != cudaSuccess) return e;
   *n_launch += 1;
   if (append && m > 1 && app->n_tokens > 0) {

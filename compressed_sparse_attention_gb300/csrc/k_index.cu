@@ -125,6 +125,7 @@ template <int NT>
 __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs a) {
   constexpr int HI = NT * 8;
   __shared__ unsigned long long s_tk[2];
+  if (a.wait_first) pdl_wait();  // a step's first kernel, launched programmatically
   pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   constexpr int KB = KF == 3 ? kIdxDim / 2 : kIdxDim;  // code bytes a key
   constexpr int CH = 128 * U;                         // keys a work item
   __shared__ unsigned long long s_tk[2];
+  if (a.wait_first) pdl_wait();  // a step's first kernel, launched programmatically
   pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;

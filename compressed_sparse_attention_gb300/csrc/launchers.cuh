@@ -119,7 +119,8 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const float* norm_w, const uint16_t* w_idx, const float* k_norm_w, int idx_dim,
                             float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
                             uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags,
-                            const AppendArgs* app, int* n_launch, const CompressTail* tail = nullptr);
+                            const AppendArgs* app, int* n_launch, const CompressTail* tail = nullptr,
+                            bool pdl = false);
 // arguments of the index scan (csa2_index_score)
 struct IdxArgs {
   int n_query = 0, n_seq = 0;
@@ -140,6 +141,9 @@ struct IdxArgs {
   const int64_t* new_first = nullptr;
   const int64_t* new_tok = nullptr;
   int m = 1;
+  // 1: launched programmatically as a step's first kernel: wait for the
+  // previous kernel of the stream before reading anything
+  int wait_first = 0;
   unsigned long long* work = nullptr;  // [2] ticket counters, zero between launches
   // set: the hierarchical indexer's pool form. Row position p of query q is
   // entry (cand[q * cand_ld + (p >> cand_shift)] << cand_shift) | low bits;
