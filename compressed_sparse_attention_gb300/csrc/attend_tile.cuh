@@ -1,0 +1,367 @@
+// Pieces shared by the two attention kernels (k_attend.cu: rows gathered by
+// the threads themselves, any storage format; k_attend_tma.cu: bf16 rows
+// gathered by the tensor memory accelerator): the shared-memory layout, the
+// per-tile softmax and the output epilogue. Both follow "Reading Notes of
+// DeepSeek-V4.1-Flash", section 3a (softmax with the per-head sink in the
+// denominator) and section 3f, C2 step 3 (the window plus the selected
+// entries); "DeepSeek-V4.1-Flash on WASTE", "What is new" item 1 (the
+// output's rope channels rotated back by -t).
+//
+// Per tile, in transposed form so that the 128 gathered rows are M = 128:
+//   S^T [128 rows x 64 heads] = KV [128 x 512] . Q^T          (K = 512)
+//   O^T [512 dims x 64 heads] += KV^T [512 x 128] . P^T       (K = 128)
+// KV sits in shared memory once, in the 128-byte-swizzled layout that is at
+// the same time the K-major A operand of the first product and the MN-major
+// A operand of the second. S^T (64 columns) and O^T (4 x 64 columns) live in
+// tensor memory. Softmax runs with one thread per (row = TMEM lane, half of
+// the heads): warp w reads lane quadrant w % 4 and heads 32 (w / 4) .. +31.
+#pragma once
+#include "launchers.cuh"
+
+namespace csa2 {
+
+constexpr int kTileRows = 128;
+// 8 math warps: warp w reads tensor-memory lane quadrant w % 4 (tile rows, or
+// output dims, 32 (w % 4) .. +31) and takes heads 32 (w / 4) .. +31 of them
+constexpr int kAttWarps = 8;
+constexpr int kAttThreads = 32 * kAttWarps;
+constexpr int kKvGroups = 4;  // bf16 tiles land in 4 groups of two 64-channel blocks
+constexpr uint32_t SM_Q = 0;                          // [9 dim blocks][64 heads][128 B]; block 8 = rope residual
+constexpr uint32_t SM_KV = 73728;                     // [8 dim blocks][128 rows][128 B]
+constexpr uint32_t SM_P = SM_KV + 131072;             // [128 rows][128 B]  (64 heads, bf16)
+constexpr uint32_t SM_RED = SM_P + 16384;             // float [4][64]
+constexpr uint32_t SM_MRUN = SM_RED + 1024;           // float [64]
+constexpr uint32_t SM_LRUN = SM_MRUN + 256;           // float [64]
+constexpr uint32_t SM_MUSE = SM_LRUN + 256;           // float [64]
+constexpr uint32_t SM_ALPHA = SM_MUSE + 256;          // float [64]
+constexpr uint32_t SM_ROWS = SM_ALPHA + 256;          // int64 [128] row sources, or barriers and row masks
+constexpr uint32_t SM_MISC = SM_ROWS + 1024;          // mbarrier, tmem slot, flags
+constexpr uint32_t SM_ROPE = SM_MISC + 64;            // float2 [32]: cos, sin of t * f_i
+constexpr uint32_t SM_TOTAL = SM_ROPE + 256;
+constexpr uint32_t kAttSmemBytes = SM_TOTAL + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 64, 1, 1);
+
+// Butterfly reduce-scatter of 32 per-lane values over the 32 lanes of a warp:
+// afterwards lane l holds the reduction of value l (step k exchanges the
+// half that lane bit 4-k selects).
+template <bool MAX>
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int half = 16 >> step;
+    const int off = 16 >> step;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < half) {
+        const float lo = v[i], hi = v[half + i];
+        const float send = upper ? lo : hi;
+        const float keep = upper ? hi : lo;
+        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+        v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+      }
+    }
+  }
+  return v[0];
+}
+
+// Barriers of the 256 math threads. SyncCta: the CTA is exactly those
+// threads. SyncMath: named barrier 1, for a CTA that also holds a producer
+// warp which never takes part.
+struct SyncCta {
+  __device__ __forceinline__ void sync() const { __syncthreads(); }
+  __device__ __forceinline__ bool any(bool v) const { return __syncthreads_or(v) != 0; }
+  __device__ __forceinline__ bool all(bool v) const { return __syncthreads_and(v) != 0; }
+};
+struct SyncMath {
+  __device__ __forceinline__ void sync() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+  __device__ __forceinline__ bool any(bool v) const {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 256, p;\nselp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+  }
+  __device__ __forceinline__ bool all(bool v) const {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 256, p;\nselp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+  }
+};
+
+// q's rope channels rotated in place, as hi + lo (both bf16) in dim block 7
+// and the residual block 8: the tensor cores then see the rotation to ~2^-16
+// relative instead of one bf16 rounding. Thread: head tid/4, chunks
+// 56 + 2*(tid&3) .. +1 (the last 64 channels). Called by the 256 math
+// threads once Q has landed.
+__device__ __forceinline__ void q_rope_split(uint8_t* sm, const RopeParams& rp) {
+  const int tid = threadIdx.x;
+  const float2* rope_tab = reinterpret_cast<const float2*>(sm + SM_ROPE);
+  const int h = tid >> 2;
+  const int first_rope = kDim - 2 * rp.pairs;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int c = 56 + 2 * (tid & 3) + u;
+    const uint32_t inblk = (uint32_t)h * 128u + ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+    uint4* hi_p = reinterpret_cast<uint4*>(sm + SM_Q + 7u * 8192u + inblk);
+    const uint4 v = *hi_p;
+    uint32_t w[4] = {v.x, v.y, v.z, v.w}, lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 cs2 = rope_tab[(8 * c + 2 * k - first_rope) >> 1];
+      const float x0 = bf16lo(w[k]), x1 = bf16hi(w[k]);
+      const float y0 = x0 * cs2.x - x1 * cs2.y, y1 = x0 * cs2.y + x1 * cs2.x;
+      w[k] = pack_bf16(y0, y1);
+      lo[k] = pack_bf16(y0 - bf16lo(w[k]), y1 - bf16hi(w[k]));
+    }
+    *hi_p = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(sm + SM_Q + 8u * 8192u + inblk) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Softmax over one tile's rows, after S^T has landed in tensor memory
+// (thread = row = TMEM lane; heads 32 hh .. +31 of warp w, hh = w / 4).
+// A head's reference max moves only when a tile exceeds it by more than 2^8:
+// P = 2^(s - m) then stays below 256 and the softmax is the same for any
+// reference, so most tiles skip both the max reduction (a vote checks the
+// bound) and the O^T rescale. Writes P^T (bf16, the MN-major B operand of the
+// PV product), adds the bf16-rounded weights to this thread's unreduced row
+// sums lsum (scaled with the reference when it moves), rescales O^T in
+// tensor memory where needed, and ends with the async-proxy fence and a
+// barrier of the math threads: P^T and O^T are then ready for the PV product.
+template <class Sync>
+__device__ __forceinline__ void tile_softmax(const AttendParams& p, uint8_t* sm, uint32_t tmem_s, uint32_t tmem_o,
+                                             uint32_t lane_base, bool valid, bool first, uint32_t* rescale,
+                                             float (&lsum)[32], const Sync& sy) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hh = warp >> 2;
+  const int row = quad * 32 + lane;
+  float* red = reinterpret_cast<float*>(sm + SM_RED);
+  float* m_run = reinterpret_cast<float*>(sm + SM_MRUN);
+  float* m_use = reinterpret_cast<float*>(sm + SM_MUSE);
+  float* alpha = reinterpret_cast<float*>(sm + SM_ALPHA);
+  float s[32];
+  {
+    uint32_t r0[32];
+    tmem_ld32(tmem_s + lane_base + 32 * hh, r0);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) s[k] = valid ? __uint_as_float(r0[k]) * p.scale_log2 : -INFINITY;
+  }
+  bool need_max = first;
+  if (!need_max) {
+    bool over = false;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) over |= s[k] > m_run[32 * hh + k] + 8.f;
+    need_max = sy.any(over);
+  }
+  if (need_max) {
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = s[k];
+    red[quad * 64 + 32 * hh + lane] = reduce_scatter32<true>(v, lane);
+  }
+  sy.sync();
+  if (!need_max) {
+    if (tid < kHeads) alpha[tid] = 1.f;  // m_use and m_run stand
+  } else if (tid < kHeads) {
+    const float tmax = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+    const float mo = m_run[tid];
+    const float mn = (mo == -INFINITY || tmax > mo + 8.f) ? fmaxf(mo, tmax) : mo;
+    const float mu = (mn == -INFINITY) ? 0.f : mn;
+    const float al = (mo == -INFINITY) ? 1.f : exp2f(mo - mu);
+    m_use[tid] = mu;
+    alpha[tid] = al;
+    m_run[tid] = mn;
+    if (al != 1.f && !first) *rescale = 1;
+  }
+  sy.sync();
+  const bool do_rescale = *rescale != 0;
+  {
+    if (do_rescale) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) lsum[k] *= alpha[32 * hh + k];
+    }
+    uint32_t packed[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float p0 = exp2f(s[2 * k] - m_use[32 * hh + 2 * k]);
+      const float p1 = exp2f(s[2 * k + 1] - m_use[32 * hh + 2 * k + 1]);
+      packed[k] = pack_bf16(p0, p1);
+      lsum[2 * k] += bf16lo(packed[k]);  // the weights PV sums, rounded to bf16
+      lsum[2 * k + 1] += bf16hi(packed[k]);
+    }
+    // P^T row `row`: 64 heads = 8 chunks of 16 B; this thread writes chunks
+    // 4 hh .. 4 hh + 3
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int c = 4 * hh + c4;
+      const uint32_t off = SM_P + (uint32_t)row * 128u + ((uint32_t)(c ^ (row & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + off) =
+          make_uint4(packed[4 * c4], packed[4 * c4 + 1], packed[4 * c4 + 2], packed[4 * c4 + 3]);
+    }
+  }
+  if (do_rescale) {
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      uint32_t r[32];
+      const uint32_t a = tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base;
+      tmem_ld32(a, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[32 * hh + k]);
+      tmem_st32(a, r);
+    }
+    tmem_wait_st();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  sy.sync();
+  if (tid == 0) *rescale = 0;  // read by every thread before the barrier above
+}
+
+// The epilogue of a CTA's tiles, by the 256 math threads once the last PV
+// product has completed: the row sums reduced, then one of
+//   direct == 2: the unnormalised partial (O^T, m in natural-log units, l) of
+//                csa2_attend_partial, no sink, no rotation back;
+//   direct == 1: the output normalised with the sink, rope channels rotated
+//                back by -t, and lse;
+//   direct == 0: the bf16 partial and (m, l) of this split for the merge.
+template <class Sync>
+__device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm, int qi, int split, bool have_o,
+                                             float (&lsum)[32], uint32_t tmem_o, uint32_t lane_base, float sink_l2,
+                                             const Sync& sy) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hh = warp >> 2;
+  const int row = quad * 32 + lane;
+  float* red = reinterpret_cast<float*>(sm + SM_RED);
+  float* m_run = reinterpret_cast<float*>(sm + SM_MRUN);
+  float* l_run = reinterpret_cast<float*>(sm + SM_LRUN);
+  float* alpha = reinterpret_cast<float*>(sm + SM_ALPHA);
+  const float2* rope_tab = reinterpret_cast<const float2*>(sm + SM_ROPE);
+  if (have_o) {
+    // the row sums: over this warp's 32 rows (lanes), then over the 4 quadrants
+    red[quad * 64 + 32 * hh + lane] = reduce_scatter32<false>(lsum, lane);
+    sy.sync();
+    if (tid < kHeads) l_run[tid] = red[tid] + red[64 + tid] + red[128 + tid] + red[192 + tid];
+    sy.sync();
+  }
+  const int first_rope = kDim - 2 * p.rp.pairs;
+  if (p.direct == 2) {
+    if (tid < kHeads) {
+      const int64_t o = (int64_t)qi * kHeads + tid;
+      p.part_m[o] = have_o ? m_run[tid] * 0.6931471805599453f : -INFINITY;
+      p.part_l[o] = have_o ? l_run[tid] : 0.f;
+    }
+    float* po = p.part_o + (int64_t)qi * kHeads * kDim;
+    for (int mt = 0; mt < 4; ++mt) {
+      const int d = 128 * mt + row;
+      uint32_t r[32];
+      if (have_o) {
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) po[(int64_t)(32 * hh + k) * kDim + d] = __uint_as_float(r[k]);
+    }
+  } else if (p.direct) {
+    // final normalisation with the sink: fo = e^{m - M} / den, den = l e^{m - M} + e^{sink - M}
+    if (tid < kHeads) {
+      const float sk = sink_l2;
+      const float mr = have_o ? m_run[tid] : -INFINITY;
+      const float M = fmaxf(mr, sk);
+      float fo = 0.f, lse = -INFINITY;
+      if (M != -INFINITY) {
+        const float em = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+        const float den = l_run[tid] * em + exp2f(sk - M);
+        fo = em / den;
+        lse = (M + log2f(den)) * 0.6931471805599453f;
+      }
+      alpha[tid] = fo;
+      if (p.lse) p.lse[(int64_t)qi * kHeads + tid] = lse;
+    }
+    sy.sync();
+    uint16_t* out = p.out + (int64_t)qi * kHeads * kDim;
+    float al_all[32];  // this warp's head half, before any store: no reloads
+#pragma unroll
+    for (int k = 0; k < 32; ++k) al_all[k] = alpha[32 * hh + k];
+    for (int mt = 0; mt < 4; ++mt) {
+      const int d = 128 * mt + row;
+      float cs = 1.f, sn = 0.f;
+      const bool rope = p.rp.pairs > 0 && d >= first_rope;
+      if (rope) {
+        const float2 cs2 = rope_tab[(d - first_rope) >> 1];
+        cs = cs2.x;
+        sn = cs2.y;
+      }
+      uint32_t ra[32];
+      if (have_o) {
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, ra);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ra[k] = 0u;
+      }
+      float v[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        v[k] = __uint_as_float(ra[k]) * al_all[k];
+        const float partner = __shfl_xor_sync(0xffffffffu, v[k], 1);
+        if (rope) v[k] = (d & 1) ? (v[k] * cs - partner * sn) : (v[k] * cs + partner * sn);
+      }
+      // lanes d, d+1 swap halves so that each stores two adjacent dims of
+      // one head: the even lane head k, the odd lane head k+1
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        const bool odd = (d & 1) != 0;
+        const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[k] : v[k + 1], 1);
+        const int h = 32 * hh + k + (odd ? 1 : 0);
+        const uint32_t w = odd ? pack_bf16(recv, v[k + 1]) : pack_bf16(v[k], recv);
+        *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + (d & ~1)) = w;
+      }
+    }
+  } else {
+    // unnormalised partial O^T and (m, l) for the merge
+    const int64_t slot = (int64_t)qi * p.n_slots + p.slot_base + split;
+    if (tid < kHeads)
+      p.ws_ml[slot * kHeads + tid] = make_float2(have_o ? m_run[tid] : -INFINITY, have_o ? l_run[tid] : 0.f);
+    if (have_o) {
+      // bf16 partials: the merge's weighted sum then carries 2^-8 of each
+      // partial's magnitude. Lanes d, d+1 swap halves so that each stores two
+      // adjacent dims of one head as one 32-bit word.
+      uint16_t* wo = p.ws_o + slot * kHeads * kDim;
+      for (int mt = 0; mt < 4; ++mt) {
+        const int d = 128 * mt + row;
+        const bool odd = (d & 1) != 0;
+        uint32_t r[32];
+        tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+          const int h = 32 * hh + k + (odd ? 1 : 0);
+          const uint32_t w = odd ? pack_bf16(recv, v1) : pack_bf16(v0, recv);
+          *reinterpret_cast<uint32_t*>(wo + (int64_t)h * kDim + (d & ~1)) = w;
+        }
+      }
+    }
+  }
+}
+
+// the attention launches of one call: thread-gathered rows (k_attend.cu) or,
+// for bf16 rows, TMA-gathered rows (k_attend_tma.cu)
+cudaError_t launch_attend_tiles_tma(cudaStream_t st, const AttendParams& p, int* n_launch);
+
+}  // namespace csa2
