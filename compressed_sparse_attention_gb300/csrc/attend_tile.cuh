@@ -1,6 +1,7 @@
-// Pieces shared by the two attention kernels (k_attend.cu: rows gathered by
-// the threads themselves, any storage format; k_attend_tma.cu: bf16 rows
-// gathered by the tensor memory accelerator): the shared-memory layout, the
+// Pieces shared by the two attention kernels (k_attend.cu: rows gathered and
+// converted by the math threads themselves, fp8 and fp4 storage;
+// k_attend_ws.cu: bf16 rows gathered by producer warps while the math warps
+// compute): the shared-memory layout, the
 // per-tile softmax and the output epilogue. Both follow "Reading Notes of
 // DeepSeek-V4.1-Flash", section 3a (softmax with the per-head sink in the
 // denominator) and section 3f, C2 step 3 (the window plus the selected
@@ -34,7 +35,7 @@ constexpr uint32_t SM_MRUN = SM_RED + 1024;           // float [64]
 constexpr uint32_t SM_LRUN = SM_MRUN + 256;           // float [64]
 constexpr uint32_t SM_MUSE = SM_LRUN + 256;           // float [64]
 constexpr uint32_t SM_ALPHA = SM_MUSE + 256;          // float [64]
-constexpr uint32_t SM_ROWS = SM_ALPHA + 256;          // int64 [128] row sources, or barriers and row masks
+constexpr uint32_t SM_ROWS = SM_ALPHA + 256;          // int64 [128] row sources (thread-gathered kernel)
 constexpr uint32_t SM_MISC = SM_ROWS + 1024;          // mbarrier, tmem slot, flags
 constexpr uint32_t SM_ROPE = SM_MISC + 64;            // float2 [32]: cos, sin of t * f_i
 constexpr uint32_t SM_TOTAL = SM_ROPE + 256;
@@ -68,8 +69,8 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 }
 
 // Barriers of the 256 math threads. SyncCta: the CTA is exactly those
-// threads. SyncMath: named barrier 1, for a CTA that also holds a producer
-// warp which never takes part.
+// threads. SyncMath: named barrier 1, for a CTA that also holds producer
+// warps, which never take part.
 struct SyncCta {
   __device__ __forceinline__ void sync() const { __syncthreads(); }
   __device__ __forceinline__ bool any(bool v) const { return __syncthreads_or(v) != 0; }
@@ -360,8 +361,8 @@ __device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm,
   }
 }
 
-// the attention launches of one call: thread-gathered rows (k_attend.cu) or,
-// for bf16 rows, TMA-gathered rows (k_attend_tma.cu)
-cudaError_t launch_attend_tiles_tma(cudaStream_t st, const AttendParams& p, int* n_launch);
+// the tile launch of one call for bf16 rows (k_attend_ws.cu); fp8 and fp4
+// rows take the thread-gathered kernel of k_attend.cu
+cudaError_t launch_attend_tiles_ws(cudaStream_t st, const AttendParams& p, int* n_launch);
 
 }  // namespace csa2

@@ -219,14 +219,18 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+// Test for the completion of the phase with parity `phase`. The thread is
+// suspended until the phase completes or the hint (1 ms) elapses, instead of
+// polling: waiting threads then take neither issue slots nor shared-memory
+// bandwidth from the warps and the tensor cores still working.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
   uint32_t ok;
   asm volatile(
       "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(phase)
+      : "r"(bar), "r"(phase), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
