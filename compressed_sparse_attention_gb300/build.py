@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libcsa2.so")
-SOURCES = ["csa2_api.cu", "k_compress.cu", "k_index.cu", "k_index_tc.cu", "k_topk.cu", "k_attend.cu", "k_attend_ws.cu",
+SOURCES = ["csa2_api.cu", "k_compress.cu", "k_index.cu", "k_index_tc.cu", "k_topk.cu", "k_attend.cu",
            "csa2_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

@@ -1,12 +1,10 @@
-// Pieces shared by the two attention kernels (k_attend.cu: rows gathered and
-// converted by the math threads themselves, fp8 and fp4 storage;
-// k_attend_ws.cu: bf16 rows gathered by producer warps while the math warps
-// compute): the shared-memory layout, the
-// per-tile softmax and the output epilogue. Both follow "Reading Notes of
-// DeepSeek-V4.1-Flash", section 3a (softmax with the per-head sink in the
-// denominator) and section 3f, C2 step 3 (the window plus the selected
-// entries); "DeepSeek-V4.1-Flash on WASTE", "What is new" item 1 (the
-// output's rope channels rotated back by -t).
+// Pieces of the attention kernel of k_attend.cu (rows gathered, and
+// converted from fp8 or fp4 where stored so, by the CTA's own threads): the
+// shared-memory layout, the per-tile softmax and the output epilogue. They
+// follow "Reading Notes of DeepSeek-V4.1-Flash", section 3a (softmax with
+// the per-head sink in the denominator) and section 3f, C2 step 3 (the
+// window plus the selected entries); "DeepSeek-V4.1-Flash on WASTE", "What
+// is new" item 1 (the output's rope channels rotated back by -t).
 //
 // Per tile, in transposed form so that the 128 gathered rows are M = 128:
 //   S^T [128 rows x 64 heads] = KV [128 x 512] . Q^T          (K = 512)
@@ -68,34 +66,11 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Barriers of the 256 math threads. SyncCta: the CTA is exactly those
-// threads. SyncMath: named barrier 1, for a CTA that also holds producer
-// warps, which never take part.
+// Barriers of the CTA's 256 threads, passed to the shared pieces below.
 struct SyncCta {
   __device__ __forceinline__ void sync() const { __syncthreads(); }
   __device__ __forceinline__ bool any(bool v) const { return __syncthreads_or(v) != 0; }
   __device__ __forceinline__ bool all(bool v) const { return __syncthreads_and(v) != 0; }
-};
-struct SyncMath {
-  __device__ __forceinline__ void sync() const { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-  __device__ __forceinline__ bool any(bool v) const {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 256, p;\nselp.u32 %0, 1, 0, q;\n}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-  }
-  __device__ __forceinline__ bool all(bool v) const {
-    uint32_t r;
-    asm volatile(
-        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, 256, p;\nselp.u32 %0, 1, 0, q;\n}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-  }
 };
 
 // q's rope channels rotated in place, as hi + lo (both bf16) in dim block 7
@@ -360,9 +335,5 @@ __device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm,
     }
   }
 }
-
-// the tile launch of one call for bf16 rows (k_attend_ws.cu); fp8 and fp4
-// rows take the thread-gathered kernel of k_attend.cu
-cudaError_t launch_attend_tiles_ws(cudaStream_t st, const AttendParams& p, int* n_launch);
 
 }  // namespace csa2

@@ -7,8 +7,7 @@
 // the query's window, tiles 1.. are the selected compressed entries, 128 per
 // tile (the products, layout and softmax are those of attend_tile.cuh). In
 // this file the CTA's threads gather the rows themselves, which lets them
-// convert fp8 and fp4 rows to bf16 on the way; bf16 rows take the
-// warp-specialised kernel of k_attend_ws.cu. With several CTAs per
+// convert fp8 and fp4 rows to bf16 on the way. With several CTAs per
 // query (split-K) each writes its unnormalised O^T and (max, sum) and a merge
 // kernel combines them with the sink.
 #include "attend_tile.cuh"
@@ -596,7 +595,6 @@ static void attach_ws(AttendParams& p, const AttendPlan& pl, void* ws) {
 }
 
 static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams& p, int* n_launch) {
-  if (kv_fmt == 0) return launch_attend_tiles_ws(st, p, n_launch);  // bf16 rows: producer warps gather
   const dim3 grid((unsigned)(p.n_query * p.n_split));
   cudaError_t e;
 #define CSA2_ATT(F)                                                                                          \
@@ -605,7 +603,8 @@ static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams&
     if (e == cudaSuccess)                                                                                    \
       e = launch_ex(attend_kernel<F>, grid, dim3(kAttThreads), kAttSmemBytes, st, p.pdl != 0, p.priority, p);  \
   } while (0)
-  if (kv_fmt == 1) CSA2_ATT(1);
+  if (kv_fmt == 0) CSA2_ATT(0);
+  else if (kv_fmt == 1) CSA2_ATT(1);
   else CSA2_ATT(2);
 #undef CSA2_ATT
   if (e != cudaSuccess) return e;
