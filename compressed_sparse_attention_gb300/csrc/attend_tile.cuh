@@ -73,6 +73,123 @@ struct SyncCta {
   __device__ __forceinline__ bool all(bool v) const { return __syncthreads_and(v) != 0; }
 };
 
+// Where one query's rows live: its position t, the first window position it
+// sees (lo_eff), its sequence's window buffer and pool.
+struct QueryRows {
+  int64_t t, lo_eff, win_b0, win_cap, pool_b0, plen;
+};
+
+__device__ __forceinline__ QueryRows query_rows(const AttendParams& p, int64_t t, int bs, bool q_ok) {
+  QueryRows qr;
+  qr.t = t;
+  qr.win_b0 = p.win_off[bs];
+  qr.win_cap = q_ok ? (p.win_off[bs + 1] - qr.win_b0) : 0;
+  // no selection (window-only call): the pool arguments may be NULL
+  qr.pool_b0 = p.pool_off != nullptr ? p.pool_off[bs] : 0;
+  qr.plen = (q_ok && p.pool_off != nullptr) ? (p.pool_off[bs + 1] - qr.pool_b0) : 0;
+  const int64_t lo_raw = (q_ok && p.win_lo) ? p.win_lo[bs] : 0;
+  qr.lo_eff = max(max((int64_t)0, lo_raw), t - (int64_t)p.window + 1);
+  return qr;
+}
+
+// Source row of row r of a query's tile (tile 0: window position lo_eff + r;
+// selected tile: entry j of the selection), -1 for none; bad values are
+// recorded in the error word and skipped.
+__device__ __forceinline__ int64_t tile_row_src(const AttendParams& p, const QueryRows& qr, int tile, int r,
+                                                int32_t j) {
+  int64_t src = -1;
+  if (tile == 0) {
+    const int64_t pos = qr.lo_eff + r;
+    if (pos <= qr.t && r < p.window) {
+      if (qr.t - qr.lo_eff + 1 > qr.win_cap) set_flag(p.flags, CSA2_FLAG_BAD_WINDOW);
+      else src = qr.win_b0 + (pos % qr.win_cap);
+    }
+  } else if (j >= 0 && j >= p.shard_lo && j < p.shard_hi) {
+    // entries outside this launch's shard of the pool are not its rows
+    const int64_t jr = (int64_t)j - p.shard_lo;
+    if (jr < qr.plen) src = qr.pool_b0 + jr;
+    else set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+  } else if (j < -1) {
+    set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
+  }
+  return src;
+}
+
+// Q of query qi copied asynchronously into its swizzled K-major slots (dim
+// blocks 0..7), by the 256 threads; the caller commits the group.
+__device__ __forceinline__ void copy_q_async(const AttendParams& p, uint32_t base_s, int qi) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int h = warp; h < kHeads; h += kAttWarps) {
+    const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
+      const uint32_t dst = base_s + SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
+                           ((uint32_t)((c & 7) ^ (h & 7)) << 4);
+      cp_async16(dst, qh + 8 * c, 16u);
+    }
+  }
+}
+
+// bf16 rows of a tile gathered asynchronously into the swizzled KV operand
+// in kKvGroups commit groups, one per pair of 64-channel blocks (a half warp
+// copies one row's 256 B of a pair); a missing row (-1) reads zeros.
+__device__ __forceinline__ void gather_bf16_tile(uint32_t base_s, const int64_t* rows, const uint16_t* kv) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int g = 0; g < kKvGroups; ++g) {
+#pragma unroll
+    for (int u = 0; u < kTileRows * 16 / kAttThreads; ++u) {
+      const int i = tid + kAttThreads * u;
+      const int r = i >> 4;
+      const int c = 16 * g + (i & 15);
+      const int64_t src = rows[r];
+      const uint32_t dst = base_s + SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
+                           ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+      const uint16_t* gp = src >= 0 ? kv + src * kDim + 8 * c : kv;
+      cp_async16(dst, gp, src >= 0 ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+}
+
+// S^T = KV . Q^T, the K steps of channel-block group g of n_groups (steps
+// 0..31 cover the 8 channel blocks; with the rope residual, the last group
+// adds steps 32..35: q's residual block against the KV's last channel
+// block). Descriptors are constant offsets from the operands' bases: one
+// issuing thread, not the tensor pipe, bounds these N = 64 products.
+// Called by one thread.
+__device__ __forceinline__ void issue_qk(uint32_t base_s, uint32_t tmem_s, int g, int n_groups, bool rope) {
+  const uint64_t ad0 = sdesc_sw128(base_s + SM_KV, 16u, 1024u);
+  const uint64_t bd0 = sdesc_sw128(base_s + SM_Q, 16u, 1024u);
+  const int ks0 = g * 32 / n_groups, ks1 = (g + 1) * 32 / n_groups;
+#pragma unroll
+  for (int ks = ks0; ks < ks1; ++ks)
+    mma_bf16_ss(tmem_s, sdesc_add(ad0, (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u),
+                sdesc_add(bd0, (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u), kIdescQK, ks > 0 ? 1u : 0u);
+  if (g == n_groups - 1 && rope) {
+#pragma unroll
+    for (int ks = 32; ks < 36; ++ks)
+      mma_bf16_ss(tmem_s, sdesc_add(ad0, 7u * 16384u + (uint32_t)(ks & 3) * 32u),
+                  sdesc_add(bd0, 8u * 8192u + (uint32_t)(ks & 3) * 32u), kIdescQK, 1u);
+  }
+}
+
+// O^T (+)= KV^T . P^T in four blocks of 128 output dims (accumulate: add to
+// what O^T holds). Called by one thread.
+__device__ __forceinline__ void issue_pv(uint32_t base_s, uint32_t tmem_o, bool accumulate) {
+  const uint64_t ad0 = sdesc_sw128(base_s + SM_KV, 16384u, 1024u);
+  const uint64_t bd0 = sdesc_sw128(base_s + SM_P, 8192u, 1024u);
+  const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      mma_bf16_ss(tmem_o + 64u * (uint32_t)mt, sdesc_add(ad0, (uint32_t)(2 * mt) * 16384u + (uint32_t)ks * 2048u),
+                  sdesc_add(bd0, (uint32_t)ks * 2048u), kIdescPV, ks > 0 ? 1u : acc0);
+  }
+}
+
 // q's rope channels rotated in place, as hi + lo (both bf16) in dim block 7
 // and the residual block 8: the tensor cores then see the rotation to ~2^-16
 // relative instead of one bf16 rounding. Thread: head tid/4, chunks

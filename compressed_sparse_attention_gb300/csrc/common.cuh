@@ -318,6 +318,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the operand `off` bytes past the one `d` describes (same
+// strides and swizzle). The start-address field holds (address >> 4) in the
+// low 14 bits; shared-memory addresses stay below 2^18, so the add never
+// carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
+
 // 32 lanes x 32 bit, 32 consecutive columns -> 32 registers per thread
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

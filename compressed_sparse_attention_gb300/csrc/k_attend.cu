@@ -59,28 +59,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   // Q is copied asynchronously into its swizzled K-major slots (it lands
   // together with the first tile's rows); the rope channels are rotated in
   // place once both have arrived
-  if (tile_begin < tile_cap) {
-    for (int h = warp; h < kHeads; h += kAttWarps) {
-      const uint16_t* qh = p.q + ((int64_t)qi * kHeads + h) * kDim;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = lane + 32 * cc;  // 16-byte chunk: channels 8c .. 8c+7
-        const uint32_t dst = base_s + SM_Q + (uint32_t)(c >> 3) * 8192u + (uint32_t)h * 128u +
-                             ((uint32_t)((c & 7) ^ (h & 7)) << 4);
-        cp_async16(dst, qh + 8 * c, 16u);
-      }
-    }
-  }
+  if (tile_begin < tile_cap) copy_q_async(p, base_s, qi);
   cp_async_commit();  // Q's group lands before any KV group of the first tile
   const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
   const int tile_end = q_ok ? tile_cap : tile_begin;
   if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
   const int bs = q_ok ? b : 0;  // offsets of a valid sequence (unused when !q_ok)
-  const int64_t win_b0 = p.win_off[bs], win_b1 = p.win_off[bs + 1];
-  // no selection (window-only call): the pool arguments may be NULL
-  const int64_t pool_b0 = p.pool_off != nullptr ? p.pool_off[bs] : 0;
-  const int64_t pool_b1 = p.pool_off != nullptr ? p.pool_off[bs + 1] : 0;
-  const int64_t lo_raw = (q_ok && p.win_lo) ? p.win_lo[bs] : 0;
+  const QueryRows qr = query_rows(p, t, bs, q_ok);
   // Launched programmatically after the step's top-k, this CTA may run before
   // the selection exists: everything above reads step inputs only, the window
   // tile needs no selection, and the selection is read after pdl_wait()
@@ -127,11 +112,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   uint32_t phase = 0;
   bool aborted = false;
 
-  const int64_t win_cap = q_ok ? (win_b1 - win_b0) : 0;
-  const int64_t lo_b = max((int64_t)0, lo_raw);
-  const int64_t lo_eff = max(lo_b, t - (int64_t)p.window + 1);
-  const int64_t plen = q_ok ? (pool_b1 - pool_b0) : 0;
-
   // Two passes over the tiles: with the selection deferred, a CTA that starts
   // at the window tile runs it alone in the first pass and waits for the
   // selection between the passes (a wait inside the tile loop measured 4 %
@@ -156,55 +136,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   for (; tile < pass_end && !aborted; ++tile) {
     // ---- row sources of this tile (one thread per row, the first 128)
     if (tid < kTileRows) {
-      const int r = tid;
-      int64_t src = -1;
       const int32_t j_cur = j_next;
       j_next = sel_ready ? sel_entry(tile + 1, tile_end) : -1;  // one tile ahead
-      if (tile == 0) {
-        const int64_t pos = lo_eff + r;
-        if (pos <= t && r < p.window) {
-          if (t - lo_eff + 1 > win_cap) {
-            set_flag(p.flags, CSA2_FLAG_BAD_WINDOW);
-          } else {
-            src = win_b0 + (pos % win_cap);
-          }
-        }
-      } else {
-        // entries outside this launch's shard of the pool are not its rows
-        const int32_t j = j_cur;
-        if (j >= 0 && j >= p.shard_lo && j < p.shard_hi) {
-          const int64_t jr = (int64_t)j - p.shard_lo;
-          if (jr < plen) src = pool_b0 + jr;
-          else set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
-        } else if (j < -1) {
-          set_flag(p.flags, CSA2_FLAG_BAD_TOPK_INDEX);
-        }
-      }
-      rows[r] = src;
+      rows[tid] = tile_row_src(p, qr, tile, tid, j_cur);
     }
     __syncthreads();
     // ---- gather the tile's rows into the swizzled KV operand
     const void* kvsrc = (tile == 0) ? p.win_kv : p.pool_kv;
     if constexpr (KVF == 0) {
-      // four commit groups, one per pair of 64-channel blocks (16 chunks of
-      // 16 B per row): the QK^T steps of a pair start once its rows land. A
-      // half warp copies one row's 256 B of a pair.
-      const uint16_t* kv = reinterpret_cast<const uint16_t*>(kvsrc);
-#pragma unroll
-      for (int g = 0; g < kKvGroups; ++g) {
-#pragma unroll
-        for (int u = 0; u < kTileRows * 16 / kAttThreads; ++u) {
-          const int i = tid + kAttThreads * u;
-          const int r = i >> 4;
-          const int c = 16 * g + (i & 15);
-          const int64_t src = rows[r];
-          const uint32_t dst = base_s + SM_KV + (uint32_t)(c >> 3) * 16384u + (uint32_t)r * 128u +
-                               ((uint32_t)((c & 7) ^ (r & 7)) << 4);
-          const uint16_t* gp = src >= 0 ? kv + src * kDim + 8 * c : kv;
-          cp_async16(dst, gp, src >= 0 ? 16u : 0u);
-        }
-        cp_async_commit();
-      }
+      gather_bf16_tile(base_s, rows, reinterpret_cast<const uint16_t*>(kvsrc));
     } else if (KVF == 2 && tile != 0) {
       // fp4 pool rows: 256 B of E2M1 codes + 32 e4m3 scales; lane l converts
       // channels 16l .. 16l+15 (8 code bytes, scale l), 8 rows' loads in flight
@@ -309,16 +249,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
       // against the KV's last channel block (the rope channels)
       if (tid == 0) {
         tc_fence_after();
-        const int ks0 = g * 32 / n_groups;
-        const int ks1 = (g == n_groups - 1) ? n_ks : (g + 1) * 32 / n_groups;
-#pragma unroll 4
-        for (int ks = ks0; ks < ks1; ++ks) {
-          const uint32_t koff = (uint32_t)(ks & 3) * 32u;
-          const uint32_t kblk = ks < 32 ? (uint32_t)(ks >> 2) : 7u;
-          const uint64_t ad = sdesc_sw128(base_s + SM_KV + kblk * 16384u + koff, 16u, 1024u);
-          const uint64_t bd = sdesc_sw128(base_s + SM_Q + (uint32_t)(ks >> 2) * 8192u + koff, 16u, 1024u);
-          mma_bf16_ss(tmem_s, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
-        }
+        issue_qk(base_s, tmem_s, g, n_groups, n_ks > 32);
         if (g == n_groups - 1) mma_commit(mbar);
       }
     }
@@ -331,16 +262,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     // ---- O^T += KV^T . P^T
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = sdesc_sw128(base_s + SM_KV + (uint32_t)(2 * mt) * 16384u + (uint32_t)ks * 2048u,
-                                          16384u, 1024u);
-          const uint64_t bd = sdesc_sw128(base_s + SM_P + (uint32_t)ks * 2048u, 8192u, 1024u);
-          mma_bf16_ss(tmem_o + 64u * (uint32_t)mt, ad, bd, kIdescPV, (tile > tile_begin || ks > 0) ? 1u : 0u);
-        }
-      }
+      issue_pv(base_s, tmem_o, tile > tile_begin);
       mma_commit(mbar);
     }
     ok = mbar_wait(mbar, phase, p.flags);
@@ -360,6 +282,186 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     // let any tensor-core work still in flight land before freeing its memory
     mbar_wait(mbar, phase ^ 1u, p.flags, 1000000000ull);
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(taddr, kTmemCols);
+}
+
+// Many queries, bf16 rows (chunked prefill): one persistent CTA per SM takes
+// queries blockIdx.x, blockIdx.x + gridDim.x, ... and runs each query's
+// tiles start to finish as attend_kernel does, with the output written
+// directly. Between queries nothing waits: once the last tile's S^T is
+// ready the next query's Q is copied into the free Q buffer, and once its PV
+// product is done the next query's window rows are gathered into the free
+// KV buffer, both before this query's epilogue, which then runs while they
+// land (the epilogue reads O^T; the next query's first QK^T writes S^T, and
+// its first PV, which overwrites O^T, comes after the epilogue). Tensor
+// memory, the barrier and the sink are set up once per CTA.
+__global__ void __launch_bounds__(kAttThreads, 1) attend_persist_kernel(const AttendParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_s - raw_s);
+  float* m_run = reinterpret_cast<float*>(sm + SM_MRUN);
+  float* l_run = reinterpret_cast<float*>(sm + SM_LRUN);
+  int64_t* rows = reinterpret_cast<int64_t*>(sm + SM_ROWS);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + SM_MISC);  // [0..1] mbar, [2] tmem slot, [3] rescale
+  float2* rope_tab = reinterpret_cast<float2*>(sm + SM_ROPE);
+  const uint32_t mbar = base_s + SM_MISC;
+  const uint32_t tslot = base_s + SM_MISC + 8;
+  const uint16_t* win_kv = reinterpret_cast<const uint16_t*>(p.win_kv);
+  const uint16_t* pool_kv = reinterpret_cast<const uint16_t*>(p.pool_kv);
+
+  if (p.pdl) pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;
+  if (warp == 0) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    fence_mbar_init();
+    misc[3] = 0;
+  }
+  const float sink_l2 = (tid < kHeads) ? p.sink[tid] * 1.4426950408889634f : 0.f;
+  const bool rope = p.rp.pairs > 0;
+  // the selection may be the previous kernel's output (csa2_step's top-k)
+  if (p.pdl) pdl_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = misc[2];
+  const uint32_t tmem_s = taddr;        // columns [0, 64)
+  const uint32_t tmem_o = taddr + 64;   // columns [64, 320)
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  uint32_t phase = 0;
+  bool aborted = false;
+
+  // query qi's position, sequence check, row layout and rope table row
+  QueryRows qr{};
+  bool q_ok = false;
+  auto begin_query = [&](int qi) {
+    const int64_t t = p.q_pos[qi];
+    const int b = p.seq_of_q[qi];
+    q_ok = (b >= 0 && b < p.n_seq && t >= 0);
+    if (!q_ok && tid == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
+    qr = query_rows(p, t, q_ok ? b : 0, q_ok);
+  };
+  // the next query's Q (its own commit group) and window tile (four groups),
+  // into buffers nothing reads any more
+  auto prefetch_window = [&]() {
+    if (tid < kTileRows) rows[tid] = q_ok ? tile_row_src(p, qr, 0, tid, -1) : -1;
+    __syncthreads();
+    gather_bf16_tile(base_s, rows, win_kv);
+  };
+  auto set_rope = [&]() {
+    if (tid < p.rp.pairs) {
+      float c = 1.f, sn = 0.f;
+      if (q_ok) rope_cs(p.rp, tid, qr.t, c, sn);
+      rope_tab[tid] = make_float2(c, sn);
+    }
+    if (tid < kHeads) {
+      m_run[tid] = -INFINITY;
+      l_run[tid] = 0.f;
+    }
+  };
+
+  int qi = blockIdx.x;
+  if (qi < p.n_query) {
+    copy_q_async(p, base_s, qi);
+    cp_async_commit();
+    begin_query(qi);
+    prefetch_window();
+    set_rope();
+  }
+  while (qi < p.n_query) {
+    const int qn = qi + (int)gridDim.x;
+    const bool has_next = qn < p.n_query;
+    const int n_t = q_ok ? p.n_tiles : 0;
+    const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (int64_t)qi * p.topk : nullptr;
+    auto sel_at = [&](int tile) -> int32_t {
+      const int col = (tile - 1) * kTileRows + tid;
+      return (tid < kTileRows && tile >= 1 && tile < n_t && sel != nullptr && col < p.topk) ? sel[col] : -1;
+    };
+    float lsum[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) lsum[k] = 0.f;
+    bool next_issued = false;
+    for (int tile = 0; tile < n_t; ++tile) {
+      const int32_t j_next = sel_at(tile + 1);  // in flight while this tile runs
+#pragma unroll
+      for (int g = 0; g < kKvGroups; ++g) {
+        cp_async_wait_pending(kKvGroups - 1 - g);
+        if (tile == 0 && g == 0 && rope) {
+          __syncthreads();  // Q complete: its rope channels split into hi + lo
+          q_rope_split(sm, p.rp);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          tc_fence_after();
+          issue_qk(base_s, tmem_s, g, kKvGroups, rope);
+          if (g == kKvGroups - 1) mma_commit(mbar);
+        }
+      }
+      bool ok = mbar_wait(mbar, phase, p.flags);
+      phase ^= 1u;
+      if (!__syncthreads_and(ok)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      if (tile == n_t - 1 && has_next) {
+        copy_q_async(p, base_s, qn);  // every QK^T product of this query is done
+        cp_async_commit();
+      }
+      tile_softmax(p, sm, tmem_s, tmem_o, lane_base, rows[row] >= 0, tile == 0, &misc[3], lsum, SyncCta{});
+      if (tid == 0) {
+        tc_fence_after();
+        issue_pv(base_s, tmem_o, tile > 0);
+        mma_commit(mbar);
+      }
+      ok = mbar_wait(mbar, phase, p.flags);
+      phase ^= 1u;
+      if (!__syncthreads_and(ok)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      if (tile + 1 < n_t) {
+        if (tid < kTileRows) rows[tid] = tile_row_src(p, qr, tile + 1, tid, j_next);
+        __syncthreads();
+        gather_bf16_tile(base_s, rows, pool_kv);
+      } else if (has_next) {
+        begin_query(qn);
+        prefetch_window();
+        next_issued = true;
+      }
+    }
+    if (aborted) break;
+    if (has_next && !next_issued) {
+      // a query without tiles: let its own copies land before reusing the buffers
+      cp_async_wait_all();
+      __syncthreads();
+      copy_q_async(p, base_s, qn);
+      cp_async_commit();
+      begin_query(qn);
+      prefetch_window();
+    }
+    __syncthreads();
+    attend_store(p, sm, qi, 0, n_t > 0, lsum, tmem_o, lane_base, sink_l2, SyncCta{});
+    // the epilogue's tensor-memory loads and its reads of the rope table and
+    // the running (max, sum) are complete before the next query takes them
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (has_next) set_rope();
+    qi = qn;
+  }
+  cp_async_wait_all();  // no copy may still be landing when the CTA exits
+  if (aborted) mbar_wait(mbar, phase ^ 1u, p.flags, 1000000000ull);  // tensor-core work in flight lands first
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(taddr, kTmemCols);
@@ -564,6 +666,7 @@ AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
   if (ns > n_sel) ns = n_sel;
   if (ns > 8) ns = 8;
   if (ns < 1) ns = 1;
+  pl.ctas = num_sms;  // persistent CTAs of a one-CTA-a-query plan (one per SM)
   if (ns == 1) {
     pl.tps = pl.n_tiles;
     pl.lead = pl.n_tiles;
@@ -594,7 +697,18 @@ static void attach_ws(AttendParams& p, const AttendPlan& pl, void* ws) {
   }
 }
 
-static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams& p, int* n_launch) {
+static cudaError_t launch_tiles(cudaStream_t st, int kv_fmt, const AttendParams& p, int* n_launch, int persist_ctas = 0) {
+  if (kv_fmt == 0 && persist_ctas > 0 && p.direct == 1 && p.n_split == 1 && p.tile_base == 0 &&
+      p.tile_count == p.n_tiles) {
+    cudaError_t e = cudaFuncSetAttribute(attend_persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kAttSmemBytes);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)min(p.n_query, persist_ctas));
+    e = launch_ex(attend_persist_kernel, grid, dim3(kAttThreads), kAttSmemBytes, st, p.pdl != 0, p.priority, p);
+    if (e != cudaSuccess) return e;
+    *n_launch += 1;
+    return cudaGetLastError();
+  }
   const dim3 grid((unsigned)(p.n_query * p.n_split));
   cudaError_t e;
 #define CSA2_ATT(F)                                                                                          \
@@ -624,7 +738,7 @@ cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, cons
   p.lead_tiles = pl.lead;
   p.slot_base = 0;
   p.direct = pl.ns == 1 ? 1 : 0;
-  return launch_tiles(st, kv_fmt, p, n_launch);
+  return launch_tiles(st, kv_fmt, p, n_launch, pl.ns == 1 ? pl.ctas : 0);
 }
 
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch) {

@@ -181,6 +181,7 @@ struct AttendPlan {
   int tps;      // selected tiles per CTA
   int lead;     // tiles of a query's first CTA (the window tile and its tps selected tiles)
   int n_slots;  // partial slots per query (0: direct output)
+  int ctas;     // CTAs of the persistent launch for many queries (one per SM)
 };
 int attend_num_tiles(int topk, bool has_idx);
 AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
