@@ -321,6 +321,41 @@ __device__ __forceinline__ void tile_softmax(const AttendParams& p, uint8_t* sm,
   if (tid == 0) *rescale = 0;  // read by every thread before the barrier above
 }
 
+// One 128-dim block (dims 128 mt ..) of a [64 heads][512] bf16 output from
+// the threads' fp32 values v (thread: dim 128 mt + row, heads 32 hh .. +31).
+// Lanes d, d+1 swap halves so that each holds two adjacent dims of one head
+// (the even lane head k, the odd lane head k+1), and the pairs are staged in
+// the P buffer (free once the last PV product is done) as [head][128 dims],
+// the 16-byte chunks of odd heads shifted by four so that the two halves of a
+// warp write different banks. The block then leaves in coalesced 16-byte
+// stores, 256 B per head.
+template <class Sync>
+__device__ __forceinline__ void store_out_block(uint8_t* sm, const float (&v)[32], int mt, uint16_t* dst,
+                                                const Sync& sy) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, hh = warp >> 2;
+  const int p2 = (quad * 32 + lane) >> 1;  // dim pair of this thread in the block
+  const bool odd = (lane & 1) != 0;
+  uint8_t* stage = sm + SM_P;
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[k] : v[k + 1], 1);
+    const int h = 32 * hh + k + (odd ? 1 : 0);
+    const uint32_t w = odd ? pack_bf16(recv, v[k + 1]) : pack_bf16(v[k], recv);
+    const int chunk = (p2 >> 2) ^ ((h & 1) << 2);
+    *reinterpret_cast<uint32_t*>(stage + h * 256 + chunk * 16 + (p2 & 3) * 4) = w;
+  }
+  sy.sync();
+#pragma unroll
+  for (int u = 0; u < kHeads * 16 / kAttThreads; ++u) {
+    const int c = tid + kAttThreads * u;
+    const int h = c >> 4, part = c & 15;
+    const uint4 x = *reinterpret_cast<const uint4*>(stage + h * 256 + ((part ^ ((h & 1) << 2)) * 16));
+    *reinterpret_cast<uint4*>(dst + (int64_t)h * kDim + 128 * mt + 8 * part) = x;
+  }
+  sy.sync();  // the stage is free for the next block
+}
+
 // The epilogue of a CTA's tiles, by the 256 math threads once the last PV
 // product has completed: the row sums reduced, then one of
 //   direct == 2: the unnormalised partial (O^T, m in natural-log units, l) of
@@ -391,13 +426,6 @@ __device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm,
     for (int k = 0; k < 32; ++k) al_all[k] = alpha[32 * hh + k];
     for (int mt = 0; mt < 4; ++mt) {
       const int d = 128 * mt + row;
-      float cs = 1.f, sn = 0.f;
-      const bool rope = p.rp.pairs > 0 && d >= first_rope;
-      if (rope) {
-        const float2 cs2 = rope_tab[(d - first_rope) >> 1];
-        cs = cs2.x;
-        sn = cs2.y;
-      }
       uint32_t ra[32];
       if (have_o) {
         tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, ra);
@@ -408,21 +436,24 @@ __device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm,
       }
       float v[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        v[k] = __uint_as_float(ra[k]) * al_all[k];
-        const float partner = __shfl_xor_sync(0xffffffffu, v[k], 1);
-        if (rope) v[k] = (d & 1) ? (v[k] * cs - partner * sn) : (v[k] * cs + partner * sn);
-      }
-      // lanes d, d+1 swap halves so that each stores two adjacent dims of
-      // one head: the even lane head k, the odd lane head k+1
+      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(ra[k]) * al_all[k];
+      // rope channels rotated back by -t: only warps that hold some exchange
+      // values with the pair's other lane (warp-uniform test)
+      if (p.rp.pairs > 0 && 128 * mt + 32 * quad + 31 >= first_rope) {
+        const bool rope = d >= first_rope;
+        float cs = 1.f, sn = 0.f;
+        if (rope) {
+          const float2 cs2 = rope_tab[(d - first_rope) >> 1];
+          cs = cs2.x;
+          sn = cs2.y;
+        }
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const bool odd = (d & 1) != 0;
-        const float recv = __shfl_xor_sync(0xffffffffu, odd ? v[k] : v[k + 1], 1);
-        const int h = 32 * hh + k + (odd ? 1 : 0);
-        const uint32_t w = odd ? pack_bf16(recv, v[k + 1]) : pack_bf16(v[k], recv);
-        *reinterpret_cast<uint32_t*>(out + (int64_t)h * kDim + (d & ~1)) = w;
+        for (int k = 0; k < 32; ++k) {
+          const float partner = __shfl_xor_sync(0xffffffffu, v[k], 1);
+          if (rope) v[k] = (d & 1) ? (v[k] * cs - partner * sn) : (v[k] * cs + partner * sn);
+        }
       }
+      store_out_block(sm, v, mt, out, sy);
     }
   } else {
     // unnormalised partial O^T and (m, l) for the merge
@@ -431,23 +462,16 @@ __device__ __forceinline__ void attend_store(const AttendParams& p, uint8_t* sm,
       p.ws_ml[slot * kHeads + tid] = make_float2(have_o ? m_run[tid] : -INFINITY, have_o ? l_run[tid] : 0.f);
     if (have_o) {
       // bf16 partials: the merge's weighted sum then carries 2^-8 of each
-      // partial's magnitude. Lanes d, d+1 swap halves so that each stores two
-      // adjacent dims of one head as one 32-bit word.
+      // partial's magnitude
       uint16_t* wo = p.ws_o + slot * kHeads * kDim;
       for (int mt = 0; mt < 4; ++mt) {
-        const int d = 128 * mt + row;
-        const bool odd = (d & 1) != 0;
         uint32_t r[32];
         tmem_ld32(tmem_o + (uint32_t)(64 * mt + 32 * hh) + lane_base, r);
         tmem_wait_ld();
+        float v[32];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float v0 = __uint_as_float(r[k]), v1 = __uint_as_float(r[k + 1]);
-          const float recv = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-          const int h = 32 * hh + k + (odd ? 1 : 0);
-          const uint32_t w = odd ? pack_bf16(recv, v1) : pack_bf16(v0, recv);
-          *reinterpret_cast<uint32_t*>(wo + (int64_t)h * kDim + (d & ~1)) = w;
-        }
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+        store_out_block(sm, v, mt, wo, sy);
       }
     }
   }
