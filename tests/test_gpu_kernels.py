@@ -185,6 +185,49 @@ def test_attend_many_queries_single_split_rescale():
         assert_attention_close(case["out"][qi], ref, bnd, f"query {qi}")
 
 
+@pytest.mark.parametrize("window_only", [False, True])
+def test_attend_persistent_many_queries_ragged_and_invalid(window_only):
+    """More queries than SMs over three sequences of different lengths: one
+    CTA per SM takes queries c, c + SMs, c + 2 SMs, ... and prefetches each
+    next query while it stores the current one. The shortest sequence's
+    selections are -1 padded (fewer than 512 visible entries); one query's
+    sequence index is out of range: its flag is raised, its output is the
+    sink-only zero, and the queries after it on the same CTA are unaffected.
+    Window-only: no selection, so every query is a single tile."""
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context(compress_ratio=2)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    wl = Workload("attend_persist", 3, (700, 1500, 2600), 2, seed=31, n_query_per_seq=120, win_linear=True)
+    inp = make_inputs(wl, DEV, with_compress=False)
+    sel = None if window_only else make_selection(wl, inp["n_vis"], 13, DEV)
+    Q = wl.n_query
+    bad = 40
+    seq_of_q = inp["seq_of_q"].clone()
+    seq_of_q[bad] = wl.n_seq + 2
+    out = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((Q, 64), dtype=torch.float32, device=DEV)
+    ws = binding.workspace(ctx.attend_workspace_size(Q), DEV)
+    ctx.attend(wl.n_seq, inp["q"], inp["q_pos"], seq_of_q, inp["win_kv"], None, inp["win_off"], None,
+               None if window_only else inp["pool_kv"], None, None if window_only else inp["pool_off"], sel,
+               inp["sink"], out, lse, ws)
+    flags, _ = ctx.check()
+    assert flags == binding.FLAG_BAD_QUERY
+    assert torch.count_nonzero(out[bad]) == 0
+    sel_np = np.full((Q, 512), -1, dtype=np.int32) if window_only else sel.cpu().numpy()
+    assert window_only or (sel_np[:120] == -1).any()  # padded selections in the short sequence
+    case = dict(inp=inp, sel=sel_np, out=bf16_np(out), lse=f32_np(lse), win_np=bf16_np(inp["win_kv"]),
+                pool_np=bf16_np(inp["pool_kv"]), win_lo=None)
+    # the bad query's CTA mates, both ends of each sequence, and a second-round query
+    for qi in sorted({bad - 1, bad + 1, bad + n_sm, bad + 2 * n_sm, 0, 119, 120, 239, 240, Q - 1, n_sm + 3}):
+        if qi >= Q or qi == bad:
+            continue
+        ref, ref_lse, bnd = _oracle_attend(case, geom, f, qi)
+        assert_attention_close(case["out"][qi], ref, bnd, f"query {qi}")
+        assert np.all(np.abs(case["lse"][qi] - ref_lse) <= case["lse_bound"]), f"lse of query {qi}"
+
+
 def test_attend_reports_bad_index_and_skips_row():
     from compressed_sparse_attention_gb300 import binding
     ctx = context()
