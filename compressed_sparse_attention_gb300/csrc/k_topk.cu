@@ -303,10 +303,15 @@ cudaError_t launch_topk_pairs(cudaStream_t st, int n_query, const float* scores,
 // One 1024-thread CTA per query: the valid pairs of all lists become
 // composites in shared memory (at most kSelCap), a radix select finds the
 // k-th largest, and the chosen entries are written ascending, -1 padded.
+// Lists are list-major ([list][query][k_in]); with scores != nullptr (the
+// slices of one row, query-major [query][list][k_in]) a pair's score is read
+// from the row, scores[q * ld + entry], instead of from ps.
 __global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lists, int k_in,
                                                           const float* __restrict__ ps,
                                                           const int32_t* __restrict__ pi, int k,
-                                                          int32_t* __restrict__ out_idx) {
+                                                          int32_t* __restrict__ out_idx,
+                                                          const float* __restrict__ scores = nullptr,
+                                                          int64_t ld = 0) {
   extern __shared__ __align__(16) unsigned char sm_raw[];
   unsigned long long* cs = reinterpret_cast<unsigned long long*>(sm_raw);  // [kSelCap]
   uint32_t* sel = reinterpret_cast<uint32_t*>(cs + kSelCap);               // [kMaxTopk]
@@ -314,6 +319,8 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lis
   __shared__ unsigned long long bcast[3];
   __shared__ uint32_t n_c, n_sel;
   const int q = blockIdx.x;
+  pdl_wait();  // the lists of the previous kernel (a plain launch returns at once)
+  pdl_trigger();
   if (threadIdx.x == 0) {
     n_c = 0;
     n_sel = 0;
@@ -322,12 +329,13 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lis
   const int total = n_lists * k_in;
   for (int i = threadIdx.x; i < total; i += blockDim.x) {
     const int l = i / k_in, e = i - l * k_in;
-    const int64_t g = ((int64_t)l * n_query + q) * k_in + e;
+    const int64_t g = scores != nullptr ? ((int64_t)q * n_lists + l) * k_in + e : ((int64_t)l * n_query + q) * k_in + e;
     const int32_t j = pi[g];
     if (j >= 0) {
       const uint32_t slot = atomicAdd(&n_c, 1u);
+      const float sc = scores != nullptr ? scores[(int64_t)q * ld + j] : ps[g];
       if (slot < (uint32_t)kSelCap)
-        cs[slot] = ((unsigned long long)score_key(ps[g]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+        cs[slot] = ((unsigned long long)score_key(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
     }
   }
   __syncthreads();
@@ -885,6 +893,14 @@ static int topk_cluster_size(int64_t max_vis, int slice) {
   return (int)(c < 1 ? 1 : c);
 }
 
+// The candidate region of the workspace (after the histograms and counts):
+// the three-launch path's (key, index) candidates, or the sliced path's
+// per-slice lists (n_query x slices x k entry indices, fewer bytes).
+static size_t topk_lists_offset(int n_query) {
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return al((size_t)n_query * kHistBins * 4) + al((size_t)n_query * 4);
+}
+
 size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   return al((size_t)n_query * kHistBins * 4) + al((size_t)n_query * 4) +
@@ -909,8 +925,9 @@ struct TkMap {
   const int32_t* blocks = nullptr;
   int ld = 0;
   int shift = 0;
+  int base = 0;  // without blocks: entry = base + e (a slice of a longer row)
   __device__ __forceinline__ int32_t operator()(int q, int e) const {
-    if (blocks == nullptr) return e;
+    if (blocks == nullptr) return base + e;
     return (blocks[(int64_t)q * ld + (e >> shift)] << shift) | (e & ((1 << shift) - 1));
   }
 };
@@ -1192,10 +1209,15 @@ __device__ __forceinline__ void rel_pick(const uint32_t* h, uint32_t need, uint3
   }
 }
 
+// n_slices > 1: CTA (q, s) = (blockIdx.x / n_slices, blockIdx.x % n_slices)
+// selects among entries [s * 16,384, (s + 1) * 16,384) of row q only and
+// writes that slice's k largest (entry indices of the whole row) to list
+// out_idx[(q * n_slices + s) * k ..]; topk_merge_kernel then merges the lists.
 template <int PER>
 __global__ void __launch_bounds__(1024) topk_row_rel_kernel(const float* __restrict__ scores, int64_t ld,
                                                            const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
-                                                           int32_t* __restrict__ out_idx, const TkMap map) {
+                                                           int32_t* __restrict__ out_idx, TkMap map,
+                                                           int n_slices = 1) {
   constexpr int TPB = 1024, NW = 32;
   static_assert(PER % 4 == 0, "float4 loads");
   __shared__ __align__(16) uint32_t h1[kRelBins];
@@ -1208,14 +1230,17 @@ __global__ void __launch_bounds__(1024) topk_row_rel_kernel(const float* __restr
   pdl_wait();  // the scores of the previous kernel
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31;
-  const int q = blockIdx.x;
-  const int n = (int)min((int64_t)max(n_vis[q], 0), max_vis);
-  int32_t* out = out_idx + (int64_t)q * k;
+  const int q = blockIdx.x / n_slices, sl = blockIdx.x % n_slices;
+  constexpr int kSlice = TPB * PER;
+  const int64_t s0 = (int64_t)sl * kSlice;
+  const int n = (int)max((int64_t)0, min(min((int64_t)max(n_vis[q], 0), max_vis) - s0, (int64_t)kSlice));
+  map.base = (int)s0;
+  int32_t* out = out_idx + (int64_t)blockIdx.x * k;
   if (n <= k) {
     for (int i = tid; i < k; i += TPB) out[i] = i < n ? map(q, i) : -1;
     return;
   }
-  const float* row = scores + (int64_t)q * ld;
+  const float* row = scores + (int64_t)q * ld + s0;
   const int e0 = PER * tid;
   uint32_t key[PER];
   row_load_keys<PER>(row, scores, ld, e0, n, key);
@@ -1403,7 +1428,7 @@ cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64
       e = launch_topk_row<256, 32>(st, n_query, scores, ld, n_vis, max_vis, k, out_idx, map, pdl);
     else {
       e = launch_ex(topk_row_rel_kernel<16>, dim3(n_query), dim3(1024), 0, st, pdl, 0, scores, ld, n_vis, max_vis, k,
-                    out_idx, map);
+                    out_idx, map, 1);
       if (e == cudaSuccess) e = cudaGetLastError();
     }
     if (e == cudaSuccess) *n_launch += 1;
@@ -1424,6 +1449,31 @@ cudaError_t launch_topk(cudaStream_t st, int n_query, const float* scores, int64
     if (launched) {
       *n_launch += 1;
       return cudaSuccess;
+    }
+  }
+  // More queries than clusters fit (ragged serving batches): each
+  // 16,384-score slice selects its own k largest in one CTA (the decode form
+  // above; slices past a row's end exit at once), and one CTA per query
+  // merges the slices' lists with the tie rule, reading the scores by entry. A slice
+  // list holds the k largest of the slice, so the row's k largest are among
+  // the lists' union.
+  {
+    constexpr int kSliceLen = 1024 * 16;
+    const int64_t n_slices = (max_vis + kSliceLen - 1) / kSliceLen;
+    if (n_slices * k <= kSelCap) {
+      int32_t* lists = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + topk_lists_offset(n_query));
+      cudaError_t e = launch_ex(topk_row_rel_kernel<16>, dim3((unsigned)(n_query * n_slices)), dim3(1024), 0, st, pdl, 0,
+                                scores, ld, n_vis, max_vis, k, lists, map, (int)n_slices);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      const size_t smem = (size_t)kSelCap * 8 + (size_t)kMaxTopk * 4;
+      e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess)
+        e = launch_ex(topk_merge_kernel, dim3((unsigned)n_query), dim3(1024), smem, st, pdl, 0, n_query, (int)n_slices,
+                      k, (const float*)nullptr, (const int32_t*)lists, k, out_idx, scores, ld);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e == cudaSuccess) *n_launch += 2;
+      return e;
     }
   }
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
