@@ -633,6 +633,33 @@ def run_e2e(args, ctx, copies, stream, device, wl):
     return dict(ms_per_step=ms / steps, steps=steps, h2d=h2d, d2h=d2h, direct_ms=e2.elapsed_time(e3) / steps)
 
 
+def profile_kernel(args):
+    """A small case for an ncu capture of one kernel: one input copy of the
+    workload (the 1M decodes hold ~1.4 GB, still larger than L2), one full
+    step to make the selection, then five calls of csa2_index_score or
+    csa2_attend on the same inputs."""
+    from compressed_sparse_attention_gb300 import binding, build
+    build.build()
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    wl = PRESETS[args.workload]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=wl.kv_format,
+                          idx_key_format=wl.idx_key_format)
+    c = Copy(ctx, wl, 0, device)
+    c.step(ctx)
+    ws = binding.workspace(ctx.attend_workspace_size(wl.n_query), device)
+    for _ in range(5):
+        if args.profile_kernel == "index":
+            c.index_only(ctx)
+        else:
+            c.attend_only(ctx, ws)
+    torch.cuda.synchronize()
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x}")
+    print(json.dumps({"profile_kernel": args.profile_kernel, "workload": wl.name, "calls": 5}))
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 class OracleSample:
@@ -767,7 +794,13 @@ def main():
     ap.add_argument("--workload", default="decode_64k_b32", choices=sorted(PRESETS))
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the 1M-context line item")
+    ap.add_argument("--profile-kernel", choices=["index", "attend"], default=None,
+                    help="for an ncu capture on a small case: one input copy of --workload, one step, then five "
+                         "calls of that kernel's entry point; prints one line and exits (no timing)")
     args = ap.parse_args()
+    if args.profile_kernel:
+        profile_kernel(args)
+        return
 
     world, rank, local, pg = dist_setup(args)
     wl = PRESETS[args.workload]
