@@ -257,7 +257,7 @@ static csa2_status do_compress(csa2_ctx* ctx, cudaStream_t st, const uint16_t* r
                                         w_idx, k_norm_w, c.idx_dim, c.norm_eps, ctx->rope,
                                         c.kv_format, c.idx_key_format,
                                         pool_kv, pool_kv_scale, idx_keys, idx_key_scale, ctx->d_flags,
-                                        append ? &app : nullptr, &nl, tail, pdl);
+                                        append ? &app : nullptr, &nl, tail, pdl, ctx->num_sms);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "compress");
   ctx->last_launches += nl;
   return CSA2_OK;

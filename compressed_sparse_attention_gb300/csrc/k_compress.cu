@@ -154,47 +154,87 @@ __device__ __forceinline__ bool find_append_group(const int64_t* __restrict__ to
   return false;
 }
 
-// KVF: pool rows 0 bf16, 1 fp8, 2 fp4 (e4m3 / 16); IKF: keys 0 bf16, 1 fp8, 3 mxfp4.
-// st_raw set: the append form (csa2_compress_append), tokens of a group's
-// positions below first_pos[b] come from the state (slot b m + pos mod m).
-template <int KVF, int IKF>
-__global__ void __launch_bounds__(kCmpThreads) compress_kernel(
-    const uint16_t* __restrict__ raw, const float* __restrict__ gate, int m, int n_seq,
-    const int64_t* __restrict__ tok_off, const int64_t* __restrict__ first_pos,
-    const int64_t* __restrict__ pool_off, const float* __restrict__ norm_w,
-    const uint16_t* __restrict__ w_idx, const float* __restrict__ k_norm_w, int idx_dim, float eps,
-    RopeParams rp, void* __restrict__ pool_kv, uint8_t* __restrict__ pool_kv_scale,
-    void* __restrict__ idx_keys, uint8_t* __restrict__ idx_key_scale, uint32_t* flags, int append,
-    const uint16_t* __restrict__ st_raw, const float* __restrict__ st_gate, const CompressTail tail) {
+// The index-key weights W^I [128][512] bf16 as the per-group code reads
+// them: warp w takes rows 16w .. 16w+15, lane l channels 16l .. 16l+15 of
+// each (a: the first 8, b: the last 8). A few groups (decode) hold them in
+// registers, loaded before anything else so that their latency overlaps the
+// group's own loads (247 registers, one CTA per SM). Many groups (chunked
+// prefill) load them where they are used (98 registers, two CTAs per SM, so
+// that two groups' latency chains overlap on each SM): 2,048 groups take
+// 44 µs instead of 69 µs. Both read the same values in the same order.
+struct CmpWRegs {
+  uint4 wa[16], wb[16];
+  __device__ __forceinline__ void get(int u, uint4& a, uint4& b) const {
+    a = wa[u];
+    b = wb[u];
+  }
+};
+struct CmpWGlobal {
+  const uint16_t* w;
+  __device__ __forceinline__ void get(int u, uint4& a, uint4& b) const {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint4* wr = reinterpret_cast<const uint4*>(w + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
+    a = __ldg(wr);
+    b = __ldg(wr + 1);
+  }
+};
+
+struct CmpArgs {
+  const uint16_t* raw;
+  const float* gate;
+  int m, n_seq;
+  const int64_t* tok_off;
+  const int64_t* first_pos;
+  const int64_t* pool_off;
+  int idx_dim;
+  float eps;
+  RopeParams rp;
+  void* pool_kv;
+  uint8_t* pool_kv_scale;
+  void* idx_keys;
+  uint8_t* idx_key_scale;
+  uint32_t* flags;
+  int append;
+  const uint16_t* st_raw;
+  const float* st_gate;
+};
+
+// One closed group grp (the whole-group form's group index, or the append
+// form's running group number), by the CTA's 256 threads: pooling, norm,
+// index key (when has_w), rope, store, and the tail scores. nw, knw: this
+// thread's norm weights. Every thread returns at the same point.
+template <int KVF, int IKF, class W>
+__device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bool has_w, const W& w, float2 nw,
+                                               float knw, const CompressTail& tail) {
   __shared__ float c_hat_s[kDim];
   __shared__ float k_lin_s[kIdxDim];
   __shared__ float k_st_s[kIdxDim];  // the stored key's exact values (tail scoring)
   __shared__ float red_s[8];
-  // As a step's first kernel it may be launched programmatically: it reads
-  // nothing before the previous kernel of the stream has finished (a plain
-  // launch returns at once), which hides only the launch latency.
-  pdl_wait();
-  pdl_trigger();  // the step's index scan starts beside this grid
+  const uint16_t* __restrict__ raw = A.raw;
+  const float* __restrict__ gate = A.gate;
+  const int m = A.m, n_seq = A.n_seq;
+  const int64_t* __restrict__ tok_off = A.tok_off;
+  const int64_t* __restrict__ first_pos = A.first_pos;
+  const int64_t* __restrict__ pool_off = A.pool_off;
+  const int idx_dim = A.idx_dim;
+  const float eps = A.eps;
+  const RopeParams& rp = A.rp;
+  void* __restrict__ pool_kv = A.pool_kv;
+  uint8_t* __restrict__ pool_kv_scale = A.pool_kv_scale;
+  void* __restrict__ idx_keys = A.idx_keys;
+  uint8_t* __restrict__ idx_key_scale = A.idx_key_scale;
+  uint32_t* flags = A.flags;
+  const int append = A.append;
+  const uint16_t* __restrict__ st_raw = A.st_raw;
+  const float* __restrict__ st_gate = A.st_gate;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // ---- index-key weights first: nothing they depend on
-  uint4 wa[16], wb[16];
-  if (w_idx != nullptr) {
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
-      wa[u] = wr[0];
-      wb[u] = wr[1];
-    }
-  }
   const int c0 = 2 * tid;
-  const float2 nw = *reinterpret_cast<const float2*>(norm_w + c0);
-  const float knw = (w_idx != nullptr && warp < idx_dim / 32) ? k_norm_w[warp * 32 + lane] : 0.f;
   uint32_t rw[16];
   float2 gv[16];
   int64_t j, prow;
   int seq_b = 0;
   if (!append) {
-    const int64_t tok0 = (int64_t)blockIdx.x * m;
+    const int64_t tok0 = grp * m;
     // the group's tokens depend only on the group index: load them before the
     // segment lookup (m <= 16)
 #pragma unroll
@@ -217,7 +257,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     }
   } else {
     int b;
-    if (!find_append_group(tok_off, first_pos, n_seq, m, blockIdx.x, &b, &j)) return;  // past the last group
+    if (!find_append_group(tok_off, first_pos, n_seq, m, grp, &b, &j)) return;  // past the last group
     seq_b = b;
     const int64_t seg0 = tok_off[b], fp = first_pos[b];
     prow = pool_off[b] + j;
@@ -281,7 +321,7 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   const float inv = 1.0f / sqrtf(tot / (float)kDim + eps);
   float ch[2] = {pooled[0] * inv * nw.x, pooled[1] * inv * nw.y};
   // ---- index key from the unrotated latent
-  if (w_idx != nullptr) {
+  if (has_w) {
     *reinterpret_cast<float2*>(&c_hat_s[c0]) = make_float2(ch[0], ch[1]);
     __syncthreads();
     float cv[16];
@@ -289,15 +329,17 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
     for (int k = 0; k < 16; ++k) cv[k] = c_hat_s[16 * lane + k];
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
+      uint4 wau, wbu;
+      w.get(u, wau, wbu);
       float acc = 0.f;
-      acc = fmaf(cv[0], bf16lo(wa[u].x), acc); acc = fmaf(cv[1], bf16hi(wa[u].x), acc);
-      acc = fmaf(cv[2], bf16lo(wa[u].y), acc); acc = fmaf(cv[3], bf16hi(wa[u].y), acc);
-      acc = fmaf(cv[4], bf16lo(wa[u].z), acc); acc = fmaf(cv[5], bf16hi(wa[u].z), acc);
-      acc = fmaf(cv[6], bf16lo(wa[u].w), acc); acc = fmaf(cv[7], bf16hi(wa[u].w), acc);
-      acc = fmaf(cv[8], bf16lo(wb[u].x), acc); acc = fmaf(cv[9], bf16hi(wb[u].x), acc);
-      acc = fmaf(cv[10], bf16lo(wb[u].y), acc); acc = fmaf(cv[11], bf16hi(wb[u].y), acc);
-      acc = fmaf(cv[12], bf16lo(wb[u].z), acc); acc = fmaf(cv[13], bf16hi(wb[u].z), acc);
-      acc = fmaf(cv[14], bf16lo(wb[u].w), acc); acc = fmaf(cv[15], bf16hi(wb[u].w), acc);
+      acc = fmaf(cv[0], bf16lo(wau.x), acc); acc = fmaf(cv[1], bf16hi(wau.x), acc);
+      acc = fmaf(cv[2], bf16lo(wau.y), acc); acc = fmaf(cv[3], bf16hi(wau.y), acc);
+      acc = fmaf(cv[4], bf16lo(wau.z), acc); acc = fmaf(cv[5], bf16hi(wau.z), acc);
+      acc = fmaf(cv[6], bf16lo(wau.w), acc); acc = fmaf(cv[7], bf16hi(wau.w), acc);
+      acc = fmaf(cv[8], bf16lo(wbu.x), acc); acc = fmaf(cv[9], bf16hi(wbu.x), acc);
+      acc = fmaf(cv[10], bf16lo(wbu.y), acc); acc = fmaf(cv[11], bf16hi(wbu.y), acc);
+      acc = fmaf(cv[12], bf16lo(wbu.z), acc); acc = fmaf(cv[13], bf16hi(wbu.z), acc);
+      acc = fmaf(cv[14], bf16lo(wbu.w), acc); acc = fmaf(cv[15], bf16hi(wbu.w), acc);
 #pragma unroll
       for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
       if (lane == 0) k_lin_s[warp * 16 + u] = acc;
@@ -397,6 +439,40 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(
   }
 }
 
+// KVF: pool rows 0 bf16, 1 fp8, 2 fp4 (e4m3 / 16); IKF: keys 0 bf16, 1 fp8, 3 mxfp4.
+// st_raw set: the append form (csa2_compress_append), tokens of a group's
+// positions below first_pos[b] come from the state (slot b m + pos mod m).
+// One CTA per group; WREG: the index-key weights held in registers.
+template <int KVF, int IKF, bool WREG>
+__global__ void __launch_bounds__(kCmpThreads) compress_kernel(const CmpArgs A, const uint16_t* __restrict__ w_idx,
+                                                               const float* __restrict__ norm_w,
+                                                               const float* __restrict__ k_norm_w,
+                                                               const CompressTail tail) {
+  // As a step's first kernel it may be launched programmatically: it reads
+  // nothing before the previous kernel of the stream has finished (a plain
+  // launch returns at once), which hides only the launch latency.
+  pdl_wait();
+  pdl_trigger();  // the step's index scan starts beside this grid
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float2 nw = *reinterpret_cast<const float2*>(norm_w + 2 * tid);
+  const float knw = (w_idx != nullptr && warp < A.idx_dim / 32) ? k_norm_w[warp * 32 + lane] : 0.f;
+  if constexpr (WREG) {
+    // ---- index-key weights first: nothing they depend on
+    CmpWRegs w;
+    if (w_idx != nullptr) {
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
+        w.wa[u] = wr[0];
+        w.wb[u] = wr[1];
+      }
+    }
+    compress_group<KVF, IKF>(A, (int64_t)blockIdx.x, w_idx != nullptr, w, nw, knw, tail);
+  } else {
+    compress_group<KVF, IKF>(A, (int64_t)blockIdx.x, w_idx != nullptr, CmpWGlobal{w_idx}, nw, knw, tail);
+  }
+}
+
 // The append form's second launch: the new tokens of each sequence's group
 // still open after the call (positions from floor((p + n) / m) m on) go to
 // their state slots b m + pos mod m. One warp per new token: 1 KiB of raw
@@ -460,18 +536,42 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             const float* k_norm_w, int idx_dim, float eps, const RopeParams& rp, int kv_fmt,
                             int idx_fmt, void* pool_kv, uint8_t* pool_kv_scale, void* idx_keys,
                             uint8_t* idx_key_scale, uint32_t* flags, const AppendArgs* app, int* n_launch,
-                            const CompressTail* tail, bool pdl) {
+                            const CompressTail* tail, bool pdl, int num_sms) {
   if (n_groups == 0) return cudaSuccess;
-  const dim3 grid((unsigned)n_groups);
   const CompressTail tl = (tail != nullptr && w_idx != nullptr) ? *tail : CompressTail{};
   const int append = app != nullptr ? 1 : 0;
-  const uint16_t* st_raw = app != nullptr ? app->state_raw : nullptr;
-  const float* st_gate = app != nullptr ? app->state_gate : nullptr;
+  CmpArgs A{};
+  A.raw = raw;
+  A.gate = gate;
+  A.m = m;
+  A.n_seq = n_seq;
+  A.tok_off = tok_off;
+  A.first_pos = first_pos;
+  A.pool_off = pool_off;
+  A.idx_dim = idx_dim;
+  A.eps = eps;
+  A.rp = rp;
+  A.pool_kv = pool_kv;
+  A.pool_kv_scale = pool_kv_scale;
+  A.idx_keys = idx_keys;
+  A.idx_key_scale = idx_key_scale;
+  A.flags = flags;
+  A.append = append;
+  A.st_raw = app != nullptr ? app->state_raw : nullptr;
+  A.st_gate = app != nullptr ? app->state_gate : nullptr;
+  // More than four groups an SM: the index-key weights are loaded where they
+  // are used, so that two CTAs fit an SM
+  const bool wreg = !(num_sms > 0 && n_groups > 4 * (int64_t)num_sms);
   cudaError_t le = cudaSuccess;
-#define CSA2_COMPRESS(KF, IF)                                                                                \
-  le = launch_ex(compress_kernel<KF, IF>, grid, dim3(kCmpThreads), 0, st, pdl, 0, raw, gate, m, n_seq, tok_off, \
-                 first_pos, pool_off, norm_w, w_idx, k_norm_w, idx_dim, eps, rp, pool_kv, pool_kv_scale, idx_keys, \
-                 idx_key_scale, flags, append, st_raw, st_gate, tl)
+#define CSA2_COMPRESS(KF, IF)                                                                                     \
+  do {                                                                                                            \
+    if (wreg)                                                                                                     \
+      le = launch_ex(compress_kernel<KF, IF, true>, dim3((unsigned)n_groups), dim3(kCmpThreads), 0, st, pdl, 0, A, \
+                     w_idx, norm_w, k_norm_w, tl);                                                                \
+    else                                                                                                          \
+      le = launch_ex(compress_kernel<KF, IF, false>, dim3((unsigned)n_groups), dim3(kCmpThreads), 0, st, pdl, 0,   \
+                     A, w_idx, norm_w, k_norm_w, tl);                                                             \
+  } while (0)
 #define CSA2_COMPRESS_K(KF)                               \
   do {                                                    \
     if (idx_fmt == 1) CSA2_COMPRESS(KF, 1);               \

@@ -120,7 +120,7 @@ cudaError_t launch_compress(cudaStream_t st, int64_t n_groups, const uint16_t* r
                             float eps, const RopeParams& rp, int kv_fmt, int idx_fmt, void* pool_kv,
                             uint8_t* pool_kv_scale, void* idx_keys, uint8_t* idx_key_scale, uint32_t* flags,
                             const AppendArgs* app, int* n_launch, const CompressTail* tail = nullptr,
-                            bool pdl = false);
+                            bool pdl = false, int num_sms = 0);
 // arguments of the index scan (csa2_index_score)
 struct IdxArgs {
   int n_query = 0, n_seq = 0;

@@ -482,6 +482,79 @@ def test_compress(m, fmts):
         assert float(pool[int(pool_off[b]) + first_group[b] + seg_groups[b]].float().abs().sum()) == 0.0
 
 
+@pytest.mark.parametrize("fmts", [(0, 0), (1, 1), (2, 3)], ids=["bf16", "fp8", "fp4_mxfp4"])
+def test_compress_many_groups_equals_per_group(fmts):
+    """A call with more than four groups an SM takes the compressor form that
+    loads the index-key weights where it uses them (two CTAs an SM); the same
+    groups compressed in calls of at most 300 groups take the form that holds
+    them in registers. Both must store bit-identical pool rows and index keys
+    (the same arithmetic in the same order), and the rows must match the
+    oracle."""
+    kv_fmt, key_fmt = fmts
+    m = 2
+    ctx = context(compress_ratio=m, kv_format=kv_fmt, idx_key_format=key_fmt)
+    geom = geometry(ctx.cfg)
+    f = inv_freq(geom)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    g = torch.Generator(device=DEV).manual_seed(77)
+    seg_groups = [4 * n_sm + 37, 211, 5]
+    first_group = [0, 3000, 17]
+    T = sum(seg_groups) * m
+    raw = torch.randn((T, 512), generator=g, device=DEV).to(torch.bfloat16)
+    gate = torch.randn((T, 512), generator=g, device=DEV) * 2
+    norm_w = 0.5 + torch.rand(512, generator=g, device=DEV)
+    w_idx = (torch.randn((128, 512), generator=g, device=DEV) / math.sqrt(512)).to(torch.bfloat16)
+    k_norm_w = 0.5 + torch.rand(128, generator=g, device=DEV)
+    tok_off = np.concatenate([[0], np.cumsum(seg_groups) * m])
+    plen = [first_group[i] + seg_groups[i] for i in range(3)]
+    pool_off = torch.tensor(np.concatenate([[0], np.cumsum(plen)]), dtype=torch.int64, device=DEV)
+    P = int(pool_off[-1])
+
+    def buffers(dim, fmt):
+        if fmt == FMT_BF16:
+            return torch.zeros((P, dim), dtype=torch.bfloat16, device=DEV), None
+        return (torch.zeros((P, code_bytes(dim, fmt)), dtype=torch.uint8, device=DEV),
+                torch.zeros((P, dim // SCALE_BLOCK[fmt]), dtype=torch.uint8, device=DEV))
+
+    def run(chunks):
+        """chunks: per sequence, the group counts of successive calls"""
+        pool, psc = buffers(512, kv_fmt)
+        keys, ksc = buffers(128, key_fmt)
+        done = [0, 0, 0]
+        for step in range(max(len(c) for c in chunks)):
+            # one call over every sequence, each with its groups of this step (maybe none)
+            r_parts, g_parts, offs, firsts = [], [], [0], []
+            for b in range(3):
+                n = chunks[b][step] if step < len(chunks[b]) else 0
+                t0 = int(tok_off[b]) + done[b] * m
+                r_parts.append(raw[t0:t0 + n * m])
+                g_parts.append(gate[t0:t0 + n * m])
+                firsts.append((first_group[b] + done[b]) * m)
+                offs.append(offs[-1] + n * m)
+                done[b] += n
+            ctx.compress(torch.cat(r_parts), torch.cat(g_parts), 3, torch.tensor(offs, dtype=torch.int64, device=DEV),
+                         torch.tensor(firsts, dtype=torch.int64, device=DEV), pool_off, norm_w, w_idx, k_norm_w,
+                         pool, psc, keys, ksc)
+        assert ctx.check()[0] == 0
+        return pool, psc, keys, ksc
+
+    whole = run([[n] for n in seg_groups])
+    small = run([[min(300, n - i) for i in range(0, n, 300)] for n in seg_groups])
+    for a, b in zip(whole, small):
+        if a is not None:
+            assert torch.equal(a, b)
+    pool, psc, keys, ksc = whole
+    raw_np, gate_np = bf16_np(raw), f32_np(gate)
+    for b in range(3):
+        t0, t1 = int(tok_off[b]), int(tok_off[b + 1])
+        kv, c_hat, kidx = O.compress(raw_np[t0:t1], gate_np[t0:t1], m, first_group[b] * m, f32_np(norm_w),
+                                     geom.norm_eps, f, bf16_np(w_idx), f32_np(k_norm_w))
+        r0 = int(pool_off[b]) + first_group[b]
+        rows = slice(r0, r0 + seg_groups[b])
+        assert_rows_close_stored(pool[rows], None if psc is None else psc[rows], kv, kv_fmt, f"kv seq {b}")
+        assert_rows_close_stored(keys[rows], None if ksc is None else ksc[rows], kidx, key_fmt, f"key seq {b}")
+
+
 def test_compress_rejects_misaligned_segment():
     from compressed_sparse_attention_gb300 import binding
     ctx = context(compress_ratio=4)
