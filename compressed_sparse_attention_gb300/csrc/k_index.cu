@@ -49,6 +49,39 @@ __device__ __forceinline__ int64_t idx_row(const IdxArgs& a, int q, int64_t p) {
   return ((int64_t)a.cand[(int64_t)q * a.cand_ld + (p >> sh)] << sh) | (p & ((1 << sh) - 1));
 }
 
+// Per-query metadata a scan CTA reads at every query switch: the key row
+// offset of the query's sequence, the entries it covers (n) and whether the
+// sequence index is valid. Switching query every work item (64K decode: a
+// CTA's items lie about five queries apart) would otherwise wait on two
+// dependent loads (seq_of_q, then pool_off) before any key could be loaded;
+// with the table in shared memory (filled once per CTA, every query's loads
+// in flight together) the key loads of an item issue at once. Batches of up
+// to kIdxMetaCap queries use it. The flags and pool counts that
+// idx_query_range records are written by CTA 0 only.
+constexpr int kIdxMetaCap = 256;
+struct IdxMeta {
+  int64_t off;  // pool_off[b]
+  int32_t n;    // entries covered, 0 when the sequence index is invalid
+  int32_t ok;   // sequence index valid
+};
+__device__ __forceinline__ void idx_fill_meta(const IdxArgs& a, IdxMeta* meta) {
+  for (int q = threadIdx.x; q < a.n_query; q += blockDim.x) {
+    const int b = a.seq_of_q[q];
+    IdxMeta m{0, 0, 0};
+    if (b >= 0 && b < a.n_seq) {
+      int n_all;
+      m.off = a.pool_off[b];
+      m.n = idx_query_range(a, q, b, blockIdx.x == 0, &n_all);
+      m.ok = 1;
+    } else if (blockIdx.x == 0) {
+      set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+      if (a.n_pool != nullptr) a.n_pool[q] = 0;
+    }
+    meta[q] = m;
+  }
+  __syncthreads();
+}
+
 // Work items: each CTA first takes three quarters of its even share by
 // striding (items c, c + G, ...; no synchronisation), then the rest is handed
 // out by a 64-bit ticket counter, so that a CTA that started late (its SM
@@ -125,11 +158,14 @@ template <int NT>
 __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs a) {
   constexpr int HI = NT * 8;
   __shared__ unsigned long long s_tk[2];
+  __shared__ IdxMeta s_meta[kIdxMetaCap];
   if (a.wait_first) pdl_wait();  // a step's first kernel, launched programmatically
   pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
   const uint16_t* keys = reinterpret_cast<const uint16_t*>(a.keys);
+  const bool use_meta = a.n_query <= kIdxMetaCap;
+  if (use_meta) idx_fill_meta(a, s_meta);
   int cur_q = -1;
   uint32_t qb[NT][8][2];
   float w0[NT], w1[NT];
@@ -141,17 +177,26 @@ __global__ void __launch_bounds__(256, 2) index_score_bf16_kernel(const IdxArgs 
     const int64_t j0 = (item - (int64_t)q * a.n_chunks) * kIdxChunk;
     if (q != cur_q) {
       cur_q = q;
-      const int b = a.seq_of_q[q];
-      q_ok = (b >= 0 && b < a.n_seq);
-      if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) {
-          set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
-          if (a.n_pool != nullptr) a.n_pool[q] = 0;
-        }
+      if (use_meta) {
+        const IdxMeta m = s_meta[q];
+        q_ok = m.ok != 0;
+        nv = m.n;
+        kbase = keys + m.off * kIdxDim;
       } else {
-        int n_all;
-        nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
-        kbase = keys + a.pool_off[b] * kIdxDim;
+        const int b = a.seq_of_q[q];
+        q_ok = (b >= 0 && b < a.n_seq);
+        if (!q_ok) {
+          if (threadIdx.x == 0 && j0 == 0) {
+            set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+            if (a.n_pool != nullptr) a.n_pool[q] = 0;
+          }
+        } else {
+          int n_all;
+          nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
+          kbase = keys + a.pool_off[b] * kIdxDim;
+        }
+      }
+      if (q_ok) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint16_t* qh = a.q_idx + ((int64_t)q * HI + nt * 8 + g) * kIdxDim;
@@ -304,11 +349,14 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
   constexpr int KB = KF == 3 ? kIdxDim / 2 : kIdxDim;  // code bytes a key
   constexpr int CH = 128 * U;                         // keys a work item
   __shared__ unsigned long long s_tk[2];
+  __shared__ IdxMeta s_meta[kIdxMetaCap];
   if (a.wait_first) pdl_wait();  // a step's first kernel, launched programmatically
   pdl_trigger();  // the step's top-k may take SMs as this grid's CTAs retire
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int64_t n_items = a.n_chunks * (int64_t)a.n_query;
   const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.keys);
+  const bool use_meta = a.n_query <= kIdxMetaCap;
+  if (use_meta) idx_fill_meta(a, s_meta);
   int cur_q = -1;
   uint32_t qb[NT][8][2];
   float w0[NT], w1[NT];
@@ -321,18 +369,29 @@ __global__ void __launch_bounds__(256, 2) index_score_fp8_kernel(const IdxArgs a
     const int64_t j0 = (item - (int64_t)q * a.n_chunks) * CH;
     if (q != cur_q) {
       cur_q = q;
-      const int b = a.seq_of_q[q];
-      q_ok = (b >= 0 && b < a.n_seq);
-      if (!q_ok) {
-        if (threadIdx.x == 0 && j0 == 0) {
-          set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
-          if (a.n_pool != nullptr) a.n_pool[q] = 0;
-        }
+      int64_t off = 0;
+      if (use_meta) {
+        const IdxMeta m = s_meta[q];
+        q_ok = m.ok != 0;
+        nv = m.n;
+        off = m.off;
       } else {
-        int n_all;
-        nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
-        kbase = keys + a.pool_off[b] * KB;
-        sbase = a.key_scale + a.pool_off[b] * (kIdxDim / 32);
+        const int b = a.seq_of_q[q];
+        q_ok = (b >= 0 && b < a.n_seq);
+        if (!q_ok) {
+          if (threadIdx.x == 0 && j0 == 0) {
+            set_flag(a.flags, CSA2_FLAG_BAD_QUERY);
+            if (a.n_pool != nullptr) a.n_pool[q] = 0;
+          }
+        } else {
+          int n_all;
+          nv = idx_query_range(a, q, b, threadIdx.x == 0 && j0 == 0, &n_all);
+          off = a.pool_off[b];
+        }
+      }
+      if (q_ok) {
+        kbase = keys + off * KB;
+        sbase = a.key_scale + off * (kIdxDim / 32);
         idxq_load_query<NT, KF>(a.q_idx, a.w_heads, q, g, t, qb, w0, w1);
       }
     }
