@@ -36,7 +36,7 @@ METRIC = "CSA2 decode tokens/s and HBM GB/s (% of ~8 TB/s) at 64K and 1M context
 N_COPIES = 4  # rotating input copies: each step's working set is evicted from L2 by the other three
 # dram bytes read + written by one index_score launch on decode_64k_b32, from the
 # ncu capture summarised in profiles/index_score_decode_64k_b32.md (same kernel)
-INDEX_TRAFFIC_BYTES = 134_304_000 + 3_464_192
+INDEX_TRAFFIC_BYTES = 134_319_616 + 3_283_456
 
 
 def load_peaks():
