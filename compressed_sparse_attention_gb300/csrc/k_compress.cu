@@ -157,13 +157,24 @@ __device__ __forceinline__ bool find_append_group(const int64_t* __restrict__ to
 // The index-key weights W^I [128][512] bf16 as the per-group code reads
 // them: warp w takes rows 16w .. 16w+15, lane l channels 16l .. 16l+15 of
 // each (a: the first 8, b: the last 8). A few groups (decode) hold them in
-// registers, loaded before anything else so that their latency overlaps the
-// group's own loads (247 registers, one CTA per SM). Many groups (chunked
-// prefill) load them where they are used (98 registers, two CTAs per SM, so
-// that two groups' latency chains overlap on each SM): 2,048 groups take
-// 44 µs instead of 69 µs. Both read the same values in the same order.
+// registers (247 registers, one CTA per SM); their loads go out right after
+// the group's own tokens, so that the tokens are not queued behind 128 KiB of
+// weights. Many groups (chunked prefill) load them where they are used (98
+// registers, two CTAs per SM, so that two groups' latency chains overlap on
+// each SM): 2,048 groups take 44 µs instead of 69 µs. Both read the same
+// values in the same order.
 struct CmpWRegs {
+  const uint16_t* w;
   uint4 wa[16], wb[16];
+  __device__ __forceinline__ void load() {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint4* wr = reinterpret_cast<const uint4*>(w + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
+      wa[u] = wr[0];
+      wb[u] = wr[1];
+    }
+  }
   __device__ __forceinline__ void get(int u, uint4& a, uint4& b) const {
     a = wa[u];
     b = wb[u];
@@ -171,6 +182,7 @@ struct CmpWRegs {
 };
 struct CmpWGlobal {
   const uint16_t* w;
+  __device__ __forceinline__ void load() {}
   __device__ __forceinline__ void get(int u, uint4& a, uint4& b) const {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint4* wr = reinterpret_cast<const uint4*>(w + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
@@ -202,14 +214,19 @@ struct CmpArgs {
 // One closed group grp (the whole-group form's group index, or the append
 // form's running group number), by the CTA's 256 threads: pooling, norm,
 // index key (when has_w), rope, store, and the tail scores. nw, knw: this
-// thread's norm weights. Every thread returns at the same point.
+// thread's norm weights; w.load() issues the index-key weights' loads (a
+// no-op where they are read in place). Every thread returns at the same point.
 template <int KVF, int IKF, class W>
-__device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bool has_w, const W& w, float2 nw,
-                                               float knw, const CompressTail& tail) {
+__device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bool has_w, W& w, float2 nw, float knw,
+                                               const CompressTail& tail) {
   __shared__ float c_hat_s[kDim];
   __shared__ float k_lin_s[kIdxDim];
   __shared__ float k_st_s[kIdxDim];  // the stored key's exact values (tail scoring)
   __shared__ float red_s[8];
+  __shared__ int64_t seg_s[2];       // whole-group form: warp 0's segment lookup (j, pool row)
+  __shared__ int segb_s[2];          // its sequence and a bad-segment mark
+  __shared__ int tq_s[kCmpThreads];  // tail: the queries that score this entry
+  __shared__ int tq_n;
   const uint16_t* __restrict__ raw = A.raw;
   const float* __restrict__ gate = A.gate;
   const int m = A.m, n_seq = A.n_seq;
@@ -231,12 +248,17 @@ __device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bo
   const int c0 = 2 * tid;
   uint32_t rw[16];
   float2 gv[16];
-  int64_t j, prow;
+  int64_t j = 0, prow = 0;
   int seq_b = 0;
+  // tail scoring: this thread's query (the first 256), its sequence and
+  // visible length, loaded before anything depends on them
+  const bool tail_on = has_w && tail.scores != nullptr;
+  int sq = -1, nvq = 0;
+  if (tid == 0) tq_n = 0;
   if (!append) {
     const int64_t tok0 = grp * m;
-    // the group's tokens depend only on the group index: load them before the
-    // segment lookup (m <= 16)
+    // the group's tokens depend only on the group index: their loads go out
+    // first (m <= 16); the pooling does not wait for the segment lookup
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       if (u < m) {
@@ -244,17 +266,26 @@ __device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bo
         gv[u] = m > 1 ? *reinterpret_cast<const float2*>(gate + (tok0 + u) * kDim + c0) : make_float2(0.f, 0.f);
       }
     }
-    const int b = find_segment_warp(tok_off, n_seq, tok0);
-    seq_b = b;
-    const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
-    const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
-    j = pos0 / m;
-    prow = pool_off[b] + j;
-    if ((seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || tok0 >= seg1 ||
-        prow >= pool_off[b + 1]) {
-      if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
-      return;
+    if (tail_on && tid < tail.n_query) {
+      sq = tail.seq_of_q[tid];
+      nvq = tail.n_vis[tid];
     }
+    if (warp == 0) {  // the others go on to the weights; read back after the first barrier
+      const int b = find_segment_warp(tok_off, n_seq, tok0);
+      const int64_t seg0 = tok_off[b], seg1 = tok_off[b + 1], fp = first_pos[b];
+      const int64_t pos0 = fp + (tok0 - seg0);  // position of the group's first token
+      const int64_t jj = pos0 / m;
+      const int64_t pr = pool_off[b] + jj;
+      const bool bad = (seg0 % m) != 0 || ((seg1 - seg0) % m) != 0 || (fp % m) != 0 || fp < 0 || tok0 >= seg1 ||
+                       pr >= pool_off[b + 1];
+      if (lane == 0) {
+        seg_s[0] = jj;
+        seg_s[1] = pr;
+        segb_s[0] = b;
+        segb_s[1] = bad ? 1 : 0;
+      }
+    }
+    if (has_w) w.load();
   } else {
     int b;
     if (!find_append_group(tok_off, first_pos, n_seq, m, grp, &b, &j)) return;  // past the last group
@@ -280,6 +311,11 @@ __device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bo
         }
       }
     }
+    if (tail_on && tid < tail.n_query) {
+      sq = tail.seq_of_q[tid];
+      nvq = tail.n_vis[tid];
+    }
+    if (has_w) w.load();
   }
   // ---- pooling (fp32): per channel softmax of the gate logits over the group
   float pooled[2];
@@ -315,6 +351,15 @@ __device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bo
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if (lane == 0) red_s[warp] = ss;
   __syncthreads();
+  if (!append) {
+    if (segb_s[1]) {  // the same for every thread: the CTA returns as one
+      if (tid == 0) set_flag(flags, CSA2_FLAG_BAD_SEGMENT);
+      return;
+    }
+    j = seg_s[0];
+    prow = seg_s[1];
+    seq_b = segb_s[0];
+  }
   float tot = 0.f;
 #pragma unroll
   for (int w = 0; w < 8; ++w) tot += red_s[w];
@@ -381,29 +426,57 @@ __device__ __forceinline__ void compress_group(const CmpArgs& A, int64_t grp, bo
         k_st_s[o] = e2m1x2_to_float2_scaled(code).x * kE2M1Unscale * ue8m0_value(eb);
       }
     }
-    if (tail.scores != nullptr) {
-      // this entry's scores for the queries of its sequence that see it
-      // (warp w takes queries w, w + 8, ...; lane l channels 4l .. 4l+3)
-      __syncthreads();
+    if (tail_on) {
+      // this entry's scores for the queries of its sequence that see it: the
+      // CTA lists them (256 queries at a time), then warp w scores list
+      // entries w, w + 8, ...; lane l takes channels 4l .. 4l+3 of every head,
+      // with all heads' loads issued before the first is used
       const int64_t plen = pool_off[seq_b + 1] - pool_off[seq_b];
-      const float4 kk = *reinterpret_cast<const float4*>(&k_st_s[4 * lane]);
-      for (int q = warp; q < tail.n_query; q += kCmpThreads / 32) {
-        if (tail.seq_of_q[q] != seq_b) continue;
-        const int64_t nv = min((int64_t)max(tail.n_vis[q], 0), min(plen, tail.max_vis));
-        if (j >= nv) continue;
-        float sigma = 0.f;
-        for (int h = 0; h < tail.idx_heads; ++h) {
-          const uint2 v = *reinterpret_cast<const uint2*>(tail.q_idx + ((int64_t)q * tail.idx_heads + h) * kIdxDim +
-                                                          4 * lane);
-          float d = bf16lo(v.x) * kk.x;
-          d = fmaf(bf16hi(v.x), kk.y, d);
-          d = fmaf(bf16lo(v.y), kk.z, d);
-          d = fmaf(bf16hi(v.y), kk.w, d);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-          sigma = fmaf(tail.w_heads[(int64_t)q * tail.idx_heads + h], fmaxf(d, 0.f), sigma);
+      const int64_t vis_cap = min(plen, tail.max_vis);
+      for (int q0 = 0; q0 < tail.n_query; q0 += kCmpThreads) {
+        const int q = q0 + tid;
+        if (q0 > 0 && q < tail.n_query) {
+          sq = tail.seq_of_q[q];
+          nvq = tail.n_vis[q];
         }
-        if (lane == 0) tail.scores[(int64_t)q * tail.ld + j] = sigma;
+        if (q < tail.n_query && sq == seq_b && j < min((int64_t)max(nvq, 0), vis_cap)) tq_s[atomicAdd(&tq_n, 1)] = q;
+        __syncthreads();  // the list, and (first pass) the stored key's values
+        const int n_list = tq_n;
+        const float4 kk = *reinterpret_cast<const float4*>(&k_st_s[4 * lane]);
+        for (int i = warp; i < n_list; i += kCmpThreads / 32) {
+          const int qq = tq_s[i];
+          const uint16_t* qrow = tail.q_idx + (int64_t)qq * tail.idx_heads * kIdxDim + 4 * lane;
+          const float* wrow = tail.w_heads + (int64_t)qq * tail.idx_heads;
+          float sigma = 0.f;
+          for (int h0 = 0; h0 < tail.idx_heads; h0 += 8) {
+            uint2 v[8];
+            float wh[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const bool on = h0 + u < tail.idx_heads;
+              v[u] = on ? *reinterpret_cast<const uint2*>(qrow + (int64_t)(h0 + u) * kIdxDim) : make_uint2(0u, 0u);
+              wh[u] = on ? wrow[h0 + u] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (h0 + u < tail.idx_heads) {
+                float d = bf16lo(v[u].x) * kk.x;
+                d = fmaf(bf16hi(v[u].x), kk.y, d);
+                d = fmaf(bf16lo(v[u].y), kk.z, d);
+                d = fmaf(bf16hi(v[u].y), kk.w, d);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                sigma = fmaf(wh[u], fmaxf(d, 0.f), sigma);
+              }
+            }
+          }
+          if (lane == 0) tail.scores[(int64_t)qq * tail.ld + j] = sigma;
+        }
+        if (q0 + kCmpThreads < tail.n_query) {  // another pass: every thread has read the list
+          __syncthreads();
+          if (tid == 0) tq_n = 0;
+          __syncthreads();
+        }
       }
     }
   }
@@ -457,19 +530,12 @@ __global__ void __launch_bounds__(kCmpThreads) compress_kernel(const CmpArgs A, 
   const float2 nw = *reinterpret_cast<const float2*>(norm_w + 2 * tid);
   const float knw = (w_idx != nullptr && warp < A.idx_dim / 32) ? k_norm_w[warp * 32 + lane] : 0.f;
   if constexpr (WREG) {
-    // ---- index-key weights first: nothing they depend on
     CmpWRegs w;
-    if (w_idx != nullptr) {
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint4* wr = reinterpret_cast<const uint4*>(w_idx + (int64_t)(warp * 16 + u) * kDim + 16 * lane);
-        w.wa[u] = wr[0];
-        w.wb[u] = wr[1];
-      }
-    }
+    w.w = w_idx;
     compress_group<KVF, IKF>(A, (int64_t)blockIdx.x, w_idx != nullptr, w, nw, knw, tail);
   } else {
-    compress_group<KVF, IKF>(A, (int64_t)blockIdx.x, w_idx != nullptr, CmpWGlobal{w_idx}, nw, knw, tail);
+    CmpWGlobal w{w_idx};
+    compress_group<KVF, IKF>(A, (int64_t)blockIdx.x, w_idx != nullptr, w, nw, knw, tail);
   }
 }
 
