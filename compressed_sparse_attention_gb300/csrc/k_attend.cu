@@ -544,6 +544,9 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(const AttendParams p)
   o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
   o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
   *reinterpret_cast<uint4*>(p.out + ((int64_t)qi * kHeads + h) * kDim + 8 * chunk) = o;
+  // the next kernel (the next layer's compress in a decode loop) may launch
+  // once every CTA is here; it still reads nothing before this grid is done
+  pdl_trigger();
 }
 
 // Test aid for the bounded waits: one thread initialises an mbarrier that

@@ -407,6 +407,58 @@ def test_topk_decode_row_paths(case):
         assert np.array_equal(got[qi], ref), f"row {qi} (n {ln})"
 
 
+@pytest.mark.parametrize("n", [100000, 262144])
+@pytest.mark.parametrize("case", ["normal", "huge_max", "bin_exact", "rank", "threshold_ties", "negative",
+                                  "all_equal"])
+def test_topk_cluster_row_paths(case, n):
+    """Rows of 100,000 and 262,144 scores (one cluster of 7 or 8 CTAs a row),
+    shaped to take each path of the cluster search: the two relative levels
+    (normal), the digit levels from the top bit when the k largest reach
+    more than 2^24 key steps below the largest (huge_max), a first-level bin
+    that holds exactly the keys still needed (bin_exact), at most 256 keys at
+    the threshold ranked directly (rank), more ties at the threshold value
+    (threshold_ties, all_equal), and negative scores. Bit-exact against the
+    oracle's selection on the same scores."""
+    from compressed_sparse_attention_gb300 import binding
+    ctx = context()
+    k = 512
+    lens = [n, n - 12345, n // 2 + 7]
+    rng = np.random.default_rng({"normal": 11, "huge_max": 12, "bin_exact": 13, "rank": 14, "threshold_ties": 15,
+                                 "negative": 16, "all_equal": 17}[case] + n)
+    rows = []
+    for r in range(len(lens)):
+        x = rng.standard_normal(n).astype(np.float32)
+        if case == "huge_max":
+            x[rng.integers(0, lens[r])] = 1e30
+        elif case == "bin_exact":
+            top = np.uint32(0x80000000 | np.float32(50.0).view(np.uint32))
+            keys = (top - np.uint32(1 << 25) - rng.integers(0, 1 << 20, n).astype(np.uint32)).astype(np.uint32)
+            pos = rng.permutation(lens[r])[:k]
+            keys[pos] = top - (np.arange(k, dtype=np.uint32) << np.uint32(12))
+            x = _floats_from_keys(keys)
+        elif case in ("rank", "threshold_ties"):
+            x = np.abs(x)
+            pos = rng.permutation(lens[r])
+            n_top = 450 if case == "rank" else 400
+            x[pos[:n_top]] = 10.0
+            x[pos[n_top:n_top + (100 if case == "rank" else 300)]] = 9.0
+        elif case == "negative":
+            x = -np.abs(x) - 5.0
+        elif case == "all_equal":
+            x[:] = 3.25
+        rows.append(x)
+    sc = torch.from_numpy(np.stack(rows))
+    nv = torch.tensor(lens, dtype=torch.int32)
+    out = torch.empty((len(lens), k), dtype=torch.int32, device=DEV)
+    ws = binding.workspace(ctx.topk_workspace_size(len(lens), n), DEV)
+    ctx.topk(sc.to(DEV), nv.to(DEV), n, k, out, ws)
+    assert ctx.check()[0] == 0
+    got = out.cpu().numpy()
+    for qi, ln in enumerate(lens):
+        ref = O.topk_select(rows[qi][:ln].astype(np.float64), k)
+        assert np.array_equal(got[qi], ref), f"row {qi} (n {ln})"
+
+
 @pytest.mark.parametrize("tie_levels", [0, 2])
 def test_topk_many_queries_mixed_lengths(tie_levels):
     """More queries than the GPU holds top-k clusters for at once, with row
