@@ -491,6 +491,90 @@ def run_hier_extra(args, device):
             "reindex_speedup": ms_reindex / ms_pool}
 
 
+def run_sharded_extra(args, device):
+    """The pool-sharded step at 1M (fp8) for G = 2 and 4 shards of every
+    sequence's pool, with every shard's kernels run on this one GPU, one
+    shard at a time. Phase 1 is the shard's visible count, scan, local top-k
+    and (score, entry) pairs; phase 2 the merge of the G pair lists and the
+    partial attention; phase 3 the combine. Each phase of each shard is one
+    captured CUDA graph, replayed after an L2 flush and timed alone with CUDA
+    events. On G GPUs the G shards run each phase at once, so the step's
+    compute is the sum over the phases of the slowest shard. The two
+    all-gathers between the phases are not timed (one GPU); their payloads
+    per shard are reported."""
+    from compressed_sparse_attention_gb300 import binding, sharded
+    wl = PRESETS["decode_1m_b8_fp8"]
+    ctx = binding.Context(compress_ratio=wl.m, idx_heads=wl.idx_heads, kv_format=wl.kv_format,
+                          idx_key_format=wl.idx_key_format)
+    base = Copy(ctx, wl, 0, device)
+    ops = sharded.ContextOps(ctx)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > the 129 MB L2
+    stream = torch.cuda.Stream(device=device)
+    reps = max(3, min(args.steps, 20))
+    res = {"workload": wl.name, "timing": "per phase and shard: one graph replay after an L2 flush, CUDA events",
+           "exchanges": "not timed (one GPU)"}
+    with torch.cuda.stream(stream):
+        for G in (2, 4):
+            shards = [sharded.shard_inputs(base.inp, wl.n_seq, G, g) for g in range(G)]
+            gens = [sharded.shard_step(ops, s, wl.topk) for s in shards]
+            graphs, payload = [[], [], []], None
+            for ph in range(3):
+                outs = []
+                for g in range(G):
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=stream):
+                        try:
+                            outs.append(next(gens[g]) if ph == 0 else gens[g].send(payload))
+                        except StopIteration as stop:
+                            outs.append(stop.value)
+                    gr.replay()
+                    graphs[ph].append(gr)
+                torch.cuda.synchronize()
+                if ph < 2:
+                    payload = tuple(torch.stack([o[i] for o in outs]) for i in range(len(outs[0])))
+                if ph == 0:
+                    pairs = payload
+            # the merge of phase 2 alone, on the same gathered pairs
+            sel_m = torch.empty((wl.n_query, wl.topk), dtype=torch.int32, device=device)
+            gm = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gm, stream=stream):
+                ctx.topk_merge(pairs[0], pairs[1], wl.topk, sel_m)
+            ms_merge = 0.0
+            ms = [[0.0] * G for _ in range(3)]
+            for _ in range(reps):
+                for ph in range(3):
+                    for g in range(G):
+                        flush.zero_()
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        graphs[ph][g].replay()
+                        e1.record(stream)
+                        torch.cuda.synchronize()
+                        ms[ph][g] += e0.elapsed_time(e1) / reps
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                gm.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms_merge += e0.elapsed_time(e1) / reps
+            worst = [max(m) for m in ms]
+            step = sum(worst)
+            pairs_b = wl.n_query * wl.topk * 8
+            part_b = wl.n_query * 64 * (512 + 2) * 4
+            res[f"g{G}"] = {"ms_phase1_scan_topk": worst[0], "ms_phase2_merge_attend": worst[1],
+                            "ms_phase3_combine": worst[2], "ms_step_compute": step, "ms_merge_alone": ms_merge,
+                            "tokens_per_s_compute": wl.n_query / (step / 1000.0),
+                            "ms_phase1_per_shard": ms[0], "ms_phase2_per_shard": ms[1],
+                            "exchange_bytes_per_shard": [pairs_b, part_b]}
+            del graphs, gens, shards, payload, pairs, gm
+            torch.cuda.synchronize()
+    flags, _ = ctx.check()
+    if flags:
+        raise RuntimeError(f"device error word 0x{flags:x} on the sharded workload")
+    return res
+
+
 def reuse_bytes(wl):
     """Minimal HBM bytes of one Reuse layer: the borrowed selection, the
     gathered window and selected rows once, q in and the output out."""
@@ -916,6 +1000,10 @@ def main():
             line["extra_mixed_reuse"] = run_mixed_extra(args, device, hbm)
         except Exception as ex:  # reported, never silently dropped
             line["extra_mixed_reuse"] = {"error": repr(ex)[:300]}
+        try:
+            line["extra_sharded"] = run_sharded_extra(args, device)
+        except Exception as ex:  # reported, never silently dropped
+            line["extra_sharded"] = {"error": repr(ex)[:300]}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
         print(json.dumps(line))

@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   float* m_run = reinterpret_cast<float*>(sm + SM_MRUN);
   float* l_run = reinterpret_cast<float*>(sm + SM_LRUN);
   int64_t* rows = reinterpret_cast<int64_t*>(sm + SM_ROWS);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + SM_MISC);  // [0..1] mbar, [2] tmem slot, [3] rescale, [4] abort
+  // misc: [0..1] mbar, [2] tmem slot, [3] rescale, [4] abort, [5..7] the shard's selection columns (first, last, count)
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + SM_MISC);
   const uint32_t mbar = base_s + SM_MISC;
   const uint32_t tslot = base_s + SM_MISC + 8;
 
@@ -46,10 +47,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   // selection entry
   const int64_t t = p.q_pos[qi];
   const int b = p.seq_of_q[qi];
-  // selection entry of this thread's row in selected tile `tile` (-1 past k)
+  // selection entry of this thread's row in selected tile `tile` (-1 past
+  // the columns [sel_off, sel_lim) the selected tiles take)
+  int sel_off = 0, sel_lim = p.topk;
   auto sel_entry = [&](int tile, int tile_lim) -> int32_t {
-    const int col = (tile - 1) * kTileRows + tid;
-    return (tid < kTileRows && tile >= 1 && tile < tile_lim && col < p.topk && p.topk_idx != nullptr)
+    const int col = sel_off + (tile - 1) * kTileRows + tid;
+    return (tid < kTileRows && tile >= 1 && tile < tile_lim && col < sel_lim && p.topk_idx != nullptr)
                ? p.topk_idx[(int64_t)qi * p.topk + col]
                : -1;
   };
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   if (tile_begin < tile_cap) copy_q_async(p, base_s, qi);
   cp_async_commit();  // Q's group lands before any KV group of the first tile
   const bool q_ok = (b >= 0 && b < p.n_seq && t >= 0);
-  const int tile_end = q_ok ? tile_cap : tile_begin;
+  int tile_end = q_ok ? tile_cap : tile_begin;
   if (!q_ok && tid == 0 && split == 0) set_flag(p.flags, CSA2_FLAG_BAD_QUERY);
   const int bs = q_ok ? b : 0;  // offsets of a valid sequence (unused when !q_ok)
   const QueryRows qr = query_rows(p, t, bs, q_ok);
@@ -89,6 +92,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
     fence_mbar_init();
     misc[3] = 0;
     misc[4] = 0;
+    misc[5] = 0xFFFFFFFFu;
+    misc[6] = 0u;
+    misc[7] = 0u;
   }
   if (tid < kHeads) {
     m_run[tid] = -INFINITY;
@@ -111,6 +117,41 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   uint32_t phase = 0;
   bool aborted = false;
+
+  // One shard's part (csa2_attend_partial): when the selection's entries in
+  // the shard fill one run of columns (a selection in ascending order, as
+  // csa2_topk and csa2_topk_merge write it), the selected tiles take that run
+  // only, 128 entries a tile; otherwise every column, the others skipped row
+  // by row. A shard holding a G-th of the pool then runs about k / G rows
+  // instead of k.
+  if (p.direct == 2 && p.topk_idx != nullptr && q_ok) {
+    uint32_t first = 0xFFFFFFFFu, last = 0u, cnt = 0u;
+    for (int c = tid; c < p.topk; c += kAttThreads) {
+      const int32_t j = p.topk_idx[(int64_t)qi * p.topk + c];
+      if (j >= 0 && j >= p.shard_lo && j < p.shard_hi) {
+        first = min(first, (uint32_t)c);
+        last = max(last, (uint32_t)c);
+        ++cnt;
+      }
+    }
+    first = __reduce_min_sync(0xffffffffu, first);
+    last = __reduce_max_sync(0xffffffffu, last);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0 && cnt > 0) {
+      atomicMin(&misc[5], first);
+      atomicMax(&misc[6], last);
+      atomicAdd(&misc[7], cnt);
+    }
+    __syncthreads();
+    const uint32_t n_in = misc[7];
+    if (n_in == 0u || misc[6] - misc[5] + 1u == n_in) {
+      sel_off = n_in == 0u ? 0 : (int)misc[5];
+      sel_lim = sel_off + (int)n_in;
+      tile_end = min(tile_end, 1 + ((int)n_in + kTileRows - 1) / kTileRows);
+      if (tile_end < tile_begin) tile_end = tile_begin;
+      j_next = sel_entry(tile_begin, tile_end);
+    }
+  }
 
   // Two passes over the tiles: with the selection deferred, a CTA that starts
   // at the window tile runs it alone in the first pass and waits for the
@@ -587,23 +628,45 @@ __global__ void __launch_bounds__(256) attend_combine_kernel(int n_query, int n_
   const int tid = threadIdx.x, hl = tid >> 6, chunk = tid & 63;
   const int h = hg * kMergeHeadsPerCta + hl;
   const int64_t t = q_pos[qi];
+  // every load goes out before any is used: the weight threads' (m, l) of
+  // all parts, and every thread's slices of the first four parts' O
+  constexpr int kBatch = 4;
+  float4 oa[kBatch], ob[kBatch];
+  auto load_o = [&](int g0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (g0 + u < n_parts) {
+        const float4* src = reinterpret_cast<const float4*>(
+            part_o + (((int64_t)(g0 + u) * n_query + qi) * kHeads + h) * kDim + 8 * chunk);
+        oa[u] = src[0];
+        ob[u] = src[1];
+      }
+    }
+  };
+  load_o(0);
   if (tid < kMergeHeadsPerCta) {
     const int hh = hg * kMergeHeadsPerCta + tid;
+    float mv[kCombineMaxParts], lv[kCombineMaxParts];
+#pragma unroll
+    for (int g = 0; g < kCombineMaxParts; ++g) {
+      mv[g] = g < n_parts ? part_m[((int64_t)g * n_query + qi) * kHeads + hh] : -INFINITY;
+      lv[g] = g < n_parts ? part_l[((int64_t)g * n_query + qi) * kHeads + hh] : 0.f;
+    }
     const float sk = sink[hh];
     float M = sk;
-    for (int g = 0; g < n_parts; ++g) M = fmaxf(M, part_m[((int64_t)g * n_query + qi) * kHeads + hh]);
+#pragma unroll
+    for (int g = 0; g < kCombineMaxParts; ++g)
+      if (g < n_parts) M = fmaxf(M, mv[g]);
     float den = 0.f;
     if (M != -INFINITY) {
       den = expf(sk - M);
-      for (int g = 0; g < n_parts; ++g) {
-        const float mg = part_m[((int64_t)g * n_query + qi) * kHeads + hh];
-        if (mg != -INFINITY) den += part_l[((int64_t)g * n_query + qi) * kHeads + hh] * expf(mg - M);
-      }
+#pragma unroll
+      for (int g = 0; g < kCombineMaxParts; ++g)
+        if (g < n_parts && mv[g] != -INFINITY) den += lv[g] * expf(mv[g] - M);
     }
-    for (int g = 0; g < n_parts; ++g) {
-      const float mg = part_m[((int64_t)g * n_query + qi) * kHeads + hh];
-      wpart[g][tid] = (M == -INFINITY || mg == -INFINITY) ? 0.f : expf(mg - M) / den;
-    }
+#pragma unroll
+    for (int g = 0; g < kCombineMaxParts; ++g)
+      if (g < n_parts) wpart[g][tid] = (M == -INFINITY || mv[g] == -INFINITY) ? 0.f : expf(mv[g] - M) / den;
     if (lse) lse[(int64_t)qi * kHeads + hh] = (M == -INFINITY) ? -INFINITY : M + logf(den);
   }
   if (tid >= 32 && tid - 32 < rp.pairs) {
@@ -613,16 +676,19 @@ __global__ void __launch_bounds__(256) attend_combine_kernel(int n_query, int n_
   }
   __syncthreads();
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int g = 0; g < n_parts; ++g) {
-    const float w = wpart[g][hl];
-    if (w == 0.f) continue;
-    const float4* src = reinterpret_cast<const float4*>(part_o + (((int64_t)g * n_query + qi) * kHeads + h) * kDim +
-                                                        8 * chunk);
-    const float4 a = src[0], b = src[1];
-    acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
-    acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
-    acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
-    acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+  for (int g0 = 0; g0 < n_parts; g0 += kBatch) {
+    if (g0 > 0) load_o(g0);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (g0 + u >= n_parts) break;
+      const float w = wpart[g0 + u][hl];
+      if (w == 0.f) continue;
+      const float4 a = oa[u], b = ob[u];
+      acc[0] = fmaf(w, a.x, acc[0]); acc[1] = fmaf(w, a.y, acc[1]);
+      acc[2] = fmaf(w, a.z, acc[2]); acc[3] = fmaf(w, a.w, acc[3]);
+      acc[4] = fmaf(w, b.x, acc[4]); acc[5] = fmaf(w, b.y, acc[5]);
+      acc[6] = fmaf(w, b.z, acc[6]); acc[7] = fmaf(w, b.w, acc[7]);
+    }
   }
   const int first_rope = kDim - 2 * rp.pairs;
   if (rp.pairs > 0 && 8 * chunk >= first_rope) {

@@ -74,6 +74,39 @@ class ShardInputs:
     win_lo: Optional[torch.Tensor] = None
 
 
+def shard_inputs(inp: dict, n_seq: int, n_shards: int, shard: int, window_shard: int = 0) -> ShardInputs:
+    """Shard `shard`'s view of a resident batch `inp` (the step's arguments by
+    name, as csa2_step takes them): entries [lo, hi) of every sequence's pool,
+    lo and hi from the longest pool, copied out as one contiguous slice per
+    sequence (rows, scales, index keys and their scales alike), and the window
+    on shard `window_shard` only."""
+    poff = inp["pool_off"].tolist()
+    longest = max(poff[b + 1] - poff[b] for b in range(n_seq))
+    lo, hi = shard_range(longest, n_shards, shard)
+    spans = [(poff[b] + lo, max(poff[b] + lo, min(poff[b + 1], poff[b] + hi))) for b in range(n_seq)]
+    off = [0]
+    for a, e in spans:
+        off.append(off[-1] + e - a)
+
+    def rows(t):
+        if t is None:
+            return None
+        if off[-1] == 0:  # no entries here: one row keeps the arrays addressable
+            return t[:1].clone()
+        return torch.cat([t[a:e] for a, e in spans if e > a]).contiguous()
+
+    win = shard == window_shard
+    dev = inp["q"].device
+    return ShardInputs(
+        lo=lo, hi=hi, with_window=win, n_seq=n_seq, q=inp["q"], q_pos=inp["q_pos"], seq_of_q=inp["seq_of_q"],
+        n_vis=inp["n_vis"], q_idx=inp["q_idx"], w_heads=inp["w_heads"], sink=inp["sink"],
+        pool_off=torch.tensor(off, dtype=torch.int64, device=dev), pool_kv=rows(inp["pool_kv"]),
+        pool_scale=rows(inp.get("pool_scale")), idx_keys=rows(inp["idx_keys"]),
+        idx_key_scale=rows(inp.get("idx_key_scale")), win_kv=inp["win_kv"] if win else None,
+        win_scale=inp.get("win_scale") if win else None, win_off=inp["win_off"] if win else None,
+        win_lo=inp.get("win_lo") if win else None)
+
+
 def shard_step(ctx, s: ShardInputs, k: int):
     """One shard's part of the step (a generator; see the module notes).
     Returns (out [Q, 64, 512] bf16, lse [Q, 64] fp32, selection [Q, k] int32)."""

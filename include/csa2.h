@@ -522,7 +522,11 @@ csa2_status csa2_topk_merge(csa2_ctx* ctx, void* stream, int32_t n_query, int32_
  *   part_l [n_query, 64] fp32 = sum_r exp(s_r - m)
  * Window arguments are read only when with_window != 0. No workspace: one
  * CTA per query. Entries outside the shard are skipped; an entry inside it
- * but past the shard's pool is recorded as CSA2_FLAG_BAD_TOPK_INDEX. */
+ * but past the shard's pool is recorded as CSA2_FLAG_BAD_TOPK_INDEX. When a
+ * query's entries inside the shard fill one run of columns (a selection in
+ * ascending order, as csa2_topk_merge writes it), only that run is read, 128
+ * entries a tile; any other order gives the same rows, tile by tile over
+ * every column. */
 csa2_status csa2_attend_partial(csa2_ctx* ctx, void* stream, int32_t n_seq, int32_t n_query, const uint16_t* q,
                                 const int64_t* q_pos, const int32_t* seq_of_q, int32_t with_window,
                                 const void* win_kv, const uint8_t* win_scale, const int64_t* win_off,

@@ -12,7 +12,9 @@ Checked:
     selected rows (the attention tolerance), and lse within its bound (the
     bf16 weights the denominator sums, and the fp32 scores);
   - a shard that holds none of a short sequence's entries, and shards
-    without the window, contribute empty partials.
+    without the window, contribute empty partials;
+  - the partial attention over the same selection with its columns shuffled
+    (no shard's entries form one run of columns) meets the same bounds.
 """
 import numpy as np
 import pytest
@@ -27,35 +29,6 @@ from workloads import Workload
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 G = 4
-
-
-def _slice_rows(t, rows):
-    return None if t is None else t[rows].contiguous()
-
-
-def _shards(wl, inp):
-    from compressed_sparse_attention_gb300.sharded import ShardInputs, shard_range
-    poff = inp["pool_off"].tolist()
-    longest = max(poff[b + 1] - poff[b] for b in range(wl.n_seq))
-    out = []
-    for g in range(G):
-        lo, hi = shard_range(longest, G, g)
-        rows, off = [], [0]
-        for b in range(wl.n_seq):
-            a, e = poff[b] + lo, min(poff[b + 1], poff[b] + hi)
-            rows.extend(range(a, max(a, e)))
-            off.append(len(rows))
-        r = torch.tensor(rows if rows else [0], dtype=torch.long, device=DEV)
-        first = g == 0
-        out.append(ShardInputs(
-            lo=lo, hi=hi, with_window=first, n_seq=wl.n_seq, q=inp["q"], q_pos=inp["q_pos"],
-            seq_of_q=inp["seq_of_q"], n_vis=inp["n_vis"], q_idx=inp["q_idx"], w_heads=inp["w_heads"],
-            sink=inp["sink"], pool_off=torch.tensor(off, dtype=torch.int64, device=DEV),
-            pool_kv=_slice_rows(inp["pool_kv"], r), pool_scale=_slice_rows(inp.get("pool_scale"), r),
-            idx_keys=_slice_rows(inp["idx_keys"], r), idx_key_scale=_slice_rows(inp.get("idx_key_scale"), r),
-            win_kv=inp["win_kv"] if first else None, win_scale=inp.get("win_scale") if first else None,
-            win_off=inp["win_off"] if first else None))
-    return out
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -77,7 +50,7 @@ def test_sharded_step_equals_unsharded(fp8):
     sel_full = torch.empty((Q, K), dtype=torch.int32, device=DEV)
     ops = sharded.ContextOps(ctx)
     ctx.topk(full, i["n_vis"], max_vis, K, sel_full, ops.topk_workspace(Q, max_vis))
-    shards = _shards(wl, i)
+    shards = [sharded.shard_inputs(i, wl.n_seq, G, g) for g in range(G)]
     # each shard's local scores are the unsharded scores of its entries
     nv = i["n_vis"].tolist()
     for s in shards:
@@ -97,6 +70,23 @@ def test_sharded_step_equals_unsharded(fp8):
         assert torch.equal(s2, sel) and torch.equal(o2.view(torch.int16), out.view(torch.int16))
         assert torch.equal(l2, lse)
     assert torch.equal(sel, sel_full), "the merged selection differs from csa2_topk's on the same scores"
+    # the same selection with its columns shuffled: the partial attention then
+    # cannot take a shard's entries as one run of columns and goes over every
+    # column; the combined output must meet the same bounds
+    perm = torch.stack([torch.randperm(K, generator=torch.Generator().manual_seed(77 + q)) for q in range(Q)])
+    sel_p = torch.gather(sel, 1, perm.to(DEV)).contiguous()
+    parts = []
+    for s_ in shards:
+        po = torch.empty((Q, 64, 512), dtype=torch.float32, device=DEV)
+        pm = torch.empty((Q, 64), dtype=torch.float32, device=DEV)
+        pl = torch.empty((Q, 64), dtype=torch.float32, device=DEV)
+        ctx.attend_partial(s_.n_seq, s_.q, s_.q_pos, s_.seq_of_q, s_.with_window, s_.win_kv, s_.win_scale, s_.win_off,
+                           s_.win_lo, s_.pool_kv, s_.pool_scale, s_.pool_off, sel_p, s_.lo, s_.hi, po, pm, pl)
+        parts.append((po, pm, pl))
+    out_p = torch.empty((Q, 64, 512), dtype=torch.bfloat16, device=DEV)
+    lse_p = torch.empty((Q, 64), dtype=torch.float32, device=DEV)
+    ctx.attend_combine(*(torch.stack([pt[c] for pt in parts]) for c in range(3)), i["q_pos"], i["sink"], out_p, lse_p)
+    assert ctx.check() == (0, 0)
     # the combined output against the oracle
     fmt = wl.kv_format
     sink = f32_np(i["sink"])
@@ -113,10 +103,11 @@ def test_sharded_step_equals_unsharded(fp8):
         rows = O.gather_rows(t, geom, lambda p: win[p % cap], pool, np.arange(chosen.shape[0]))
         qv = bf16_np(i["q"][q])
         ref, ref_lse = O.attend(qv, t, rows, sink, geom.softmax_scale, f)
-        assert_attention_close(bf16_np(out[q]), ref, attention_bound(qv, t, rows, sink, geom.softmax_scale, f),
-                               f"sharded q{q}")
-        d_lse, lb = np.abs(f32_np(lse[q]) - ref_lse), lse_bound(qv, t, rows, geom.softmax_scale, f)
-        assert np.all(d_lse <= lb), (f"q{q}: lse off by {float(d_lse.max()):.3e} at head {int(np.argmax(d_lse - lb))}, "
-                                     f"bound {float(lb[np.argmax(d_lse - lb)]):.3e}; "
-                                     f"gpu {float(f32_np(lse[q])[np.argmax(d_lse - lb)]):.6f} "
-                                     f"oracle {float(ref_lse[np.argmax(d_lse - lb)]):.6f} rows {rows.shape[0]}")
+        for o_, l_, tag in ((out, lse, "sharded"), (out_p, lse_p, "sharded, shuffled selection")):
+            assert_attention_close(bf16_np(o_[q]), ref, attention_bound(qv, t, rows, sink, geom.softmax_scale, f),
+                                   f"{tag} q{q}")
+            d_lse, lb = np.abs(f32_np(l_[q]) - ref_lse), lse_bound(qv, t, rows, geom.softmax_scale, f)
+            assert np.all(d_lse <= lb), (f"{tag} q{q}: lse off by {float(d_lse.max()):.3e} at head "
+                                         f"{int(np.argmax(d_lse - lb))}, bound {float(lb[np.argmax(d_lse - lb)]):.3e}; "
+                                         f"gpu {float(f32_np(l_[q])[np.argmax(d_lse - lb)]):.6f} "
+                                         f"oracle {float(ref_lse[np.argmax(d_lse - lb)]):.6f} rows {rows.shape[0]}")
