@@ -300,12 +300,19 @@ cudaError_t launch_topk_pairs(cudaStream_t st, int n_query, const float* scores,
   return cudaGetLastError();
 }
 
-// One 1024-thread CTA per query: the valid pairs of all lists become
-// composites in shared memory (at most kSelCap), a radix select finds the
-// k-th largest, and the chosen entries are written ascending, -1 padded.
-// Lists are list-major ([list][query][k_in]); with scores != nullptr (the
-// slices of one row, query-major [query][list][k_in]) a pair's score is read
-// from the row, scores[q * ld + entry], instead of from ps.
+__device__ __forceinline__ uint32_t block_scan_incl(uint32_t v, uint32_t* warp_s);  // below
+
+// One 1024-thread CTA per query: pair i of the lists (list-major order)
+// becomes the composite key(score) << 32 | ~entry in shared-memory slot i (0
+// for an empty pair, below every composite), a radix select finds the k-th
+// largest composite, and the chosen entries are written ascending, -1
+// padded. Thread t holds slots [t c, t c + c): when the chosen entries come
+// out ascending in slot order (each list ascending and the lists' entry
+// ranges in list order, as shards' and slices' lists are), a block scan of
+// the threads' chosen counts places them; otherwise each is ranked against
+// the others. Lists are list-major ([list][query][k_in]); with scores !=
+// nullptr (the slices of one row, query-major [query][list][k_in]) a pair's
+// score is read from the row, scores[q * ld + entry], instead of from ps.
 __global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lists, int k_in,
                                                           const float* __restrict__ ps,
                                                           const int32_t* __restrict__ pi, int k,
@@ -317,47 +324,64 @@ __global__ void __launch_bounds__(1024) topk_merge_kernel(int n_query, int n_lis
   uint32_t* sel = reinterpret_cast<uint32_t*>(cs + kSelCap);               // [kMaxTopk]
   __shared__ uint32_t hist_s[256];
   __shared__ unsigned long long bcast[3];
-  __shared__ uint32_t n_c, n_sel;
+  __shared__ uint32_t warp_s[32];
   const int q = blockIdx.x;
   pdl_wait();  // the lists of the previous kernel (a plain launch returns at once)
   pdl_trigger();
-  if (threadIdx.x == 0) {
-    n_c = 0;
-    n_sel = 0;
-  }
-  __syncthreads();
-  const int total = n_lists * k_in;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const int l = i / k_in, e = i - l * k_in;
+  const uint32_t total = min((uint32_t)(n_lists * k_in), (uint32_t)kSelCap);
+  uint32_t n_valid = 0;
+  for (uint32_t i = threadIdx.x; i < total; i += blockDim.x) {
+    const uint32_t l = i / (uint32_t)k_in, e = i - l * (uint32_t)k_in;
     const int64_t g = scores != nullptr ? ((int64_t)q * n_lists + l) * k_in + e : ((int64_t)l * n_query + q) * k_in + e;
     const int32_t j = pi[g];
+    unsigned long long v = 0ull;
     if (j >= 0) {
-      const uint32_t slot = atomicAdd(&n_c, 1u);
       const float sc = scores != nullptr ? scores[(int64_t)q * ld + j] : ps[g];
-      if (slot < (uint32_t)kSelCap)
-        cs[slot] = ((unsigned long long)score_key(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+      v = ((unsigned long long)score_key(sc) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+      ++n_valid;
     }
+    cs[i] = v;
   }
-  __syncthreads();
-  const uint32_t n = min(n_c, (uint32_t)kSelCap);
-  const uint32_t take = min((uint32_t)k, n);
-  unsigned long long thr = 0;
-  if (take > 0 && take < n) thr = radix_select64([&](uint32_t i) { return cs[i]; }, n, take, hist_s, bcast);
-  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+  n_valid = __reduce_add_sync(0xffffffffu, n_valid);
+  if ((threadIdx.x & 31) == 0) warp_s[threadIdx.x >> 5] = n_valid;
+  __syncthreads();  // the slots and the warps' counts are complete
+  uint32_t nv = 0;
+#pragma unroll
+  for (int w = 0; w < 32; ++w) nv += warp_s[w];
+  const uint32_t take = min((uint32_t)k, nv);
+  unsigned long long thr = 1ull;  // every composite is chosen (empty slots are 0)
+  if (take > 0 && take < nv) thr = radix_select64([&](uint32_t i) { return cs[i]; }, total, take, hist_s, bcast);
+  // this thread's slots and their chosen count; the chosen entries in slot order
+  const uint32_t c = (total + blockDim.x - 1) / blockDim.x;
+  const uint32_t s0 = min(total, threadIdx.x * c), s1 = min(total, s0 + c);
+  uint32_t cnt = 0;
+  for (uint32_t i = s0; i < s1; ++i) {
     const unsigned long long v = cs[i];
-    if (take > 0 && v >= thr) {
-      const uint32_t slot = atomicAdd(&n_sel, 1u);
-      if (slot < (uint32_t)kMaxTopk) sel[slot] = 0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull);
+    if (take > 0 && v >= thr && v != 0ull) ++cnt;
+  }
+  const uint32_t pos0 = block_scan_incl(cnt, warp_s) - cnt;  // ends synchronised
+  {
+    uint32_t p = pos0;
+    for (uint32_t i = s0; i < s1; ++i) {
+      const unsigned long long v = cs[i];
+      if (take > 0 && v >= thr && v != 0ull && p < (uint32_t)kMaxTopk) sel[p++] = 0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull);
     }
   }
   __syncthreads();
-  const uint32_t ns = min(n_sel, (uint32_t)kMaxTopk);
+  const uint32_t ns = min(take, (uint32_t)kMaxTopk);
+  bool ok = true;  // strictly ascending in slot order
+  for (uint32_t i = threadIdx.x; i + 1 < ns; i += blockDim.x) ok = ok && sel[i] < sel[i + 1];
+  const bool ordered = __syncthreads_and(ok) != 0;
   int32_t* o = out_idx + (int64_t)q * k;
-  for (uint32_t i = threadIdx.x; i < ns; i += blockDim.x) {
-    const uint32_t v = sel[i];
-    uint32_t r = 0;
-    for (uint32_t jx = 0; jx < ns; ++jx) r += sel[jx] < v ? 1u : 0u;
-    if (r < (uint32_t)k) o[r] = (int32_t)v;
+  if (ordered) {
+    for (uint32_t i = threadIdx.x; i < ns; i += blockDim.x) o[i] = (int32_t)sel[i];
+  } else {
+    for (uint32_t i = threadIdx.x; i < ns; i += blockDim.x) {
+      const uint32_t v = sel[i];
+      uint32_t r = 0;
+      for (uint32_t jx = 0; jx < ns; ++jx) r += sel[jx] < v ? 1u : 0u;
+      if (r < (uint32_t)k) o[r] = (int32_t)v;
+    }
   }
   for (int i = (int)ns + threadIdx.x; i < k; i += blockDim.x) o[i] = -1;
 }

@@ -459,6 +459,46 @@ def test_topk_cluster_row_paths(case, n):
         assert np.array_equal(got[qi], ref), f"row {qi} (n {ln})"
 
 
+@pytest.mark.parametrize("n_lists,order", [(4, "ranges"), (16, "ranges"), (4, "shuffled"), (16, "shuffled")])
+def test_topk_merge_lists(n_lists, order):
+    """csa2_topk_merge over n_lists lists of 512 (score, entry) pairs per
+    query, -1 padded at the ends, scores with ties: lists over ascending
+    disjoint entry ranges (as shards and slices give them), and the same
+    entries shuffled across and within the lists. The selection is the
+    oracle's top-k over the union (entries mapped to a dense row in
+    ascending order, so that ties still go to the lower entry), ascending,
+    -1 padded; bit-exact."""
+    ctx = context()
+    k, k_in, Q = 512, 512, 3
+    rng = np.random.default_rng(900 + n_lists + (order == "shuffled"))
+    score = np.full((n_lists, Q, k_in), -np.inf, dtype=np.float32)
+    idx = np.full((n_lists, Q, k_in), -1, dtype=np.int32)
+    expect = []
+    for q in range(Q):
+        n_valid = [k_in - (rng.integers(0, 200) if (l + q) % 3 == 0 else 0) for l in range(n_lists)]
+        span = 3000
+        ents = np.concatenate([np.sort(rng.choice(span, n_valid[l], replace=False)) + l * span
+                               for l in range(n_lists)]).astype(np.int32)
+        sc = (np.round(rng.standard_normal(ents.shape[0]) * 8) / 8).astype(np.float32)  # many ties
+        if order == "shuffled":
+            perm = rng.permutation(ents.shape[0])
+            ents, sc = ents[perm], sc[perm]
+        pos = 0
+        for l in range(n_lists):
+            idx[l, q, :n_valid[l]] = ents[pos:pos + n_valid[l]]
+            score[l, q, :n_valid[l]] = sc[pos:pos + n_valid[l]]
+            pos += n_valid[l]
+        o = np.argsort(ents, kind="stable")
+        dense = O.topk_select(sc[o].astype(np.float64), k)
+        expect.append(np.where(dense >= 0, ents[o][np.maximum(dense, 0)], -1))
+    out = torch.empty((Q, k), dtype=torch.int32, device=DEV)
+    ctx.topk_merge(torch.from_numpy(score).to(DEV), torch.from_numpy(idx).to(DEV), k, out)
+    assert ctx.check()[0] == 0
+    got = out.cpu().numpy()
+    for q in range(Q):
+        assert np.array_equal(got[q], expect[q]), f"query {q}"
+
+
 @pytest.mark.parametrize("tie_levels", [0, 2])
 def test_topk_many_queries_mixed_lengths(tie_levels):
     """More queries than the GPU holds top-k clusters for at once, with row
