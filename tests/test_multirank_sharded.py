@@ -31,20 +31,38 @@ def _case():
     return wl, make_inputs(wl, "cpu", with_compress=False)
 
 
-def _shard_inputs(wl, inp, rank, world):
-    from compressed_sparse_attention_gb300.sharded import ShardInputs, shard_range
+def _shard_rows_by_index(inp, n_seq, lo, hi):
+    """The shard's rows and offsets from an explicit row list (the slow,
+    obvious form that sharded.shard_inputs is checked against)."""
     poff = inp["pool_off"].tolist()
-    lo, hi = shard_range(max(poff[b + 1] - poff[b] for b in range(wl.n_seq)), world, rank)
     rows, off = [], [0]
-    for b in range(wl.n_seq):
+    for b in range(n_seq):
         a, e = poff[b] + lo, min(poff[b + 1], poff[b] + hi)
         rows.extend(range(a, max(a, e)))
         off.append(len(rows))
-    sel = torch.tensor(rows, dtype=torch.long)
-    return ShardInputs(lo=lo, hi=hi, with_window=(rank == 0), n_seq=wl.n_seq, q=inp["q"], q_pos=inp["q_pos"],
-                       seq_of_q=inp["seq_of_q"], n_vis=inp["n_vis"], q_idx=inp["q_idx"], w_heads=inp["w_heads"],
-                       sink=inp["sink"], pool_off=torch.tensor(off, dtype=torch.int64), pool_kv=inp["pool_kv"][sel],
-                       idx_keys=inp["idx_keys"][sel], win_kv=inp["win_kv"], win_off=inp["win_off"])
+    return torch.tensor(rows, dtype=torch.long), off
+
+
+def test_shard_inputs_slices_every_sequence():
+    """sharded.shard_inputs on CPU tensors: for G = 2, 3, 4 and 7 shards each
+    shard's pool rows, index keys and offsets equal the explicit row list's,
+    only the window shard carries the window, and a shard past every
+    sequence's end keeps one row so that its arrays stay addressable."""
+    from compressed_sparse_attention_gb300 import sharded
+    wl, inp = _case()
+    for world in (2, 3, 4, 7, 36):
+        n_rows = 0
+        for rank in range(world):
+            s = sharded.shard_inputs(inp, wl.n_seq, world, rank)
+            sel, off = _shard_rows_by_index(inp, wl.n_seq, s.lo, s.hi)
+            assert s.pool_off.tolist() == off
+            if sel.numel():
+                assert torch.equal(s.pool_kv, inp["pool_kv"][sel]) and torch.equal(s.idx_keys, inp["idx_keys"][sel])
+            else:
+                assert s.pool_kv.shape[0] == 1 and off[-1] == 0
+            assert s.with_window == (rank == 0) and (s.win_kv is not None) == (rank == 0)
+            n_rows += sel.numel()
+        assert n_rows == int(inp["pool_off"][-1])
 
 
 def _ops():
@@ -64,7 +82,7 @@ def _rank(rank, world, port, queue):
     dist.init_process_group("gloo")
     wl, inp = _case()
     ops, _, _ = _ops()
-    out, lse, sel = sharded.run_distributed(sharded.shard_step(ops, _shard_inputs(wl, inp, rank, world), K))
+    out, lse, sel = sharded.run_distributed(sharded.shard_step(ops, sharded.shard_inputs(inp, wl.n_seq, world, rank), K))
     queue.put((rank, out.view(torch.int16).numpy(), lse.numpy(), sel.numpy()))
     dist.destroy_process_group()
 
