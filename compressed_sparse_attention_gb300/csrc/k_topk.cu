@@ -1078,6 +1078,37 @@ __device__ __forceinline__ void row_emit(const uint32_t (&key)[PER], int e0, int
                                          Eq eq, unsigned long long* wsum, int32_t* out, const TkMap& map, int q) {
   constexpr int NW = TPB / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (exact) {
+    // every tie is taken (the common case): one 32-bit count of the chosen
+    // keys and its block scan place them
+    uint32_t n_ch = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) n_ch += (e0 + i < n && (gt(key[i]) || eq(key[i]))) ? 1u : 0u;
+    uint32_t v = n_ch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t w = lane < NW ? (uint32_t)wsum[lane] : 0u;
+      const uint32_t own = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += u;
+      }
+      if (lane < NW) wsum[lane] = w - own;  // exclusive over warps
+    }
+    __syncthreads();
+    uint32_t pos = (uint32_t)wsum[warp] + v - n_ch;  // exclusive over threads
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (e0 + i < n && (gt(key[i]) || eq(key[i]))) out[pos++] = map(q, e0 + i);
+    return;
+  }
   uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i)
