@@ -939,7 +939,9 @@ size_t topk_workspace_bytes(int n_query, int64_t max_vis) {
 // atomics), a block scan over its bins finds the one that holds the k-th
 // largest, and the search stops once that bin holds exactly the keys still
 // needed, or when no bits are left (ties at one key value, taken in index
-// order). (Finding the row's common prefix first, or 8-bit digits in per-warp
+// order). With 24 keys a thread (rows of up to 6,144) the kernel is held to
+// 64 registers, so that four CTAs share an SM instead of three (chunked
+// prefill step 960 -> 950 us); with 8 keys the bound measured slower. (Finding the row's common prefix first, or 8-bit digits in per-warp
 // histograms, measured slower.) One 64-bit block scan of
 // (above-threshold, at-threshold) counts then gives every thread the output
 // positions of its entries, which come out in ascending index order.
@@ -1158,7 +1160,7 @@ __device__ __forceinline__ void row_emit(const uint32_t (&key)[PER], int e0, int
 }
 
 template <int TPB, int PER>
-__global__ void __launch_bounds__(TPB) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
+__global__ void __launch_bounds__(TPB, (PER == 24 ? 4 : 1)) topk_row_kernel(const float* __restrict__ scores, int64_t ld,
                                                       const int32_t* __restrict__ n_vis, int64_t max_vis, int k,
                                                       int32_t* __restrict__ out_idx, const TkMap map) {
   constexpr int NW = TPB / 32;
