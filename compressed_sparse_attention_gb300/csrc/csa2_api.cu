@@ -710,7 +710,6 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
                     at_bytes, &ap);
   if (s != CSA2_OK) return s;
   const int kvf = ctx->cfg.kv_format;
-  const csa2::AttendPlan pl = csa2::attend_plan(a->n_query, ctx->cfg.topk, true, ctx->num_sms);
   const int m = ctx->cfg.compress_ratio;
   int launches = 0;
   // Every exit after a fork makes the caller's stream wait for the side
@@ -880,7 +879,9 @@ static csa2_status step_impl(csa2_ctx* ctx, cudaStream_t st, const csa2_step_arg
   // other inputs are the step's, complete before the step began or ordered
   // by events. The merge follows the attention the same way.
   ap.pdl = 1;
-  e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches);
+  // rows of up to 16,384 entries take a one-CTA top-k, short enough that a
+  // CTA holding the window tile and a selected tile would run them in series
+  e = csa2::launch_attend(st, ctx->num_sms, kvf, ap, at_ws, &launches, pool_read || a->max_vis <= 16384);
   if (e != cudaSuccess) return join(cuda_fail(ctx, e, "step: attend"));
   if (pool_src) {
     // the candidate source's pool, for the layers after it, on the side

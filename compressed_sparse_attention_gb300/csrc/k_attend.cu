@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) attend_kernel(const AttendPara
   int tile = tile_begin;
   for (int pass = 0; pass < 2; ++pass) {
   const int pass_end = (pass == 0 && !sel_ready) ? min(tile_end, 1) : tile_end;
-  if (pass == 1 && !sel_ready) {
+  if (pass == 1 && !sel_ready && tile < tile_end) {
     pdl_wait();
     j_next = sel_entry(tile, tile_end);
     sel_ready = true;
@@ -724,9 +724,9 @@ int attend_num_tiles(int topk, bool has_idx) { return 1 + (has_idx ? (topk + kTi
 // floor(SMs / Q) CTAs a query (at most 8), the selected tiles split evenly
 // (tps each) and the first CTA also taking the window tile, which needs no
 // selection: launched after the step's top-k, it runs while the selection is
-// still being made. A merge combines the CTAs' partials. With many queries
+// still being made (or, see below, a CTA of its own takes the window tile). A merge combines the CTAs' partials. With many queries
 // (prefill) one CTA per query runs every tile and writes the output directly.
-AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
+AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms, bool own_window) {
   AttendPlan pl{};
   pl.n_tiles = attend_num_tiles(topk, has_idx);
   if (n_query < 1) n_query = 1;
@@ -746,6 +746,16 @@ AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms) {
   pl.tps = (n_sel + ns - 1) / ns;
   pl.ns = (n_sel + pl.tps - 1) / pl.tps;
   pl.lead = 1 + pl.tps;
+  // own_window, with an SM to spare for every query: the window tile gets a
+  // CTA of its own. After a short top-k the first CTA would otherwise still
+  // be on the window tile when the selection is ready, and run its selected
+  // tile after it (tiny decode 24.6 -> 22.0 us a step); after the long rows'
+  // cluster top-k the window tile is long done, and a fifth partial only
+  // lengthens the merge (1M decode +0.4 us).
+  if (own_window && n_query * (pl.ns + 1) <= num_sms && pl.ns + 1 <= 8) {
+    pl.lead = 1;
+    pl.ns += 1;
+  }
   pl.n_slots = pl.ns;
   return pl;
 }
@@ -834,8 +844,9 @@ cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, i
   return launch_tiles(st, kv_fmt, p, n_launch);
 }
 
-cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch) {
-  const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms);
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch,
+                          bool own_window) {
+  const AttendPlan pl = attend_plan(p.n_query, p.topk, p.topk_idx != nullptr, num_sms, own_window);
   cudaError_t e = launch_attend_main(st, kv_fmt, p, pl, ws, n_launch);
   if (e == cudaSuccess) e = launch_attend_merge(st, p, pl, ws, n_launch);
   return e;

@@ -184,12 +184,15 @@ struct AttendPlan {
   int ctas;     // CTAs of the persistent launch for many queries (one per SM)
 };
 int attend_num_tiles(int topk, bool has_idx);
-AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms);
+// own_window: the window tile may take a CTA of its own (the workspace is
+// sized for it, the larger plan)
+AttendPlan attend_plan(int n_query, int topk, bool has_idx, int num_sms, bool own_window = true);
 size_t attend_workspace_bytes(int n_query, const AttendPlan& pl);
 cudaError_t launch_attend_main(cudaStream_t st, int kv_fmt, AttendParams p, const AttendPlan& pl, void* ws,
                                int* n_launch);
 cudaError_t launch_attend_merge(cudaStream_t st, AttendParams p, const AttendPlan& pl, void* ws, int* n_launch);
-cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch);
+cudaError_t launch_attend(cudaStream_t st, int num_sms, int kv_fmt, AttendParams p, void* ws, int* n_launch,
+                          bool own_window = true);
 // one CTA per query over the window tile (when with_window) and the selected
 // tiles, writing the unnormalised partial (direct = 2)
 cudaError_t launch_attend_partial(cudaStream_t st, int kv_fmt, AttendParams p, int with_window, int* n_launch);
